@@ -1,0 +1,349 @@
+"""Pins of the fp64 oracle against what the method and the mathematics fix (CPU only).
+
+Each pin checks the oracle against something other than itself: a hand-worked example,
+a characterisation by brute force (box corners, subset enumeration), a library routine
+(torch's scaled_dot_product_attention in float64), or an invariant the definition implies.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+
+def _f32(a):
+    return np.asarray(a, dtype=np.float32)
+
+
+# ------------------------------------------------------------------ hand-worked example
+@pytest.fixture(scope="module")
+def ex(golden_dir):
+    with open(os.path.join(golden_dir, "worked_example.json")) as f:
+        return json.load(f)
+
+
+def test_golden_summaries(ex):
+    keys = _f32(ex["keys"])[:, None, :]
+    kmin, kmax = O.page_summaries(keys, ex["seq_len"], ex["page_size"], "f32")
+    assert np.array_equal(kmin[:, 0], _f32(ex["kmin"]))
+    assert np.array_equal(kmax[:, 0], _f32(ex["kmax"]))
+
+
+def test_golden_scores_and_selection(ex):
+    keys = _f32(ex["keys"])[:, None, :]
+    q = _f32(ex["q"])
+    kmin, kmax = O.page_summaries(keys, ex["seq_len"], ex["page_size"], "f32")
+    # unscaled per-query-head bounds via a one-head-per-group view
+    per_head = O.quest_scores(q, np.repeat(kmin, 2, axis=1), np.repeat(kmax, 2, axis=1), "f32", 1.0)
+    assert np.array_equal(per_head, np.asarray(ex["bound_per_query_head_unscaled"], dtype=np.float64))
+    s = O.quest_scores(q, kmin, kmax, "f32", 1.0 / math.sqrt(ex["D"]))
+    assert np.allclose(s[0] * math.sqrt(2.0), ex["score_unscaled"], rtol=0, atol=1e-15)
+    for b, sel in ex["selected_by_budget"].items():
+        assert O.select_pages(s[0], int(b)) == sel
+
+
+def test_golden_attention(ex):
+    keys = _f32(ex["keys"])[:, None, :]
+    vals = _f32(ex["values"])[:, None, :]
+    q = _f32(ex["q"])
+    scale = 1.0 / math.sqrt(ex["D"])
+    sel = ex["selected_by_budget"][str(ex["attention_budget"])]
+    out = O.attend_pages(q, keys, vals, ex["seq_len"], ex["page_size"], [sel], "f32", scale)
+    toks = ex["attention_tokens"]
+    v = np.asarray(ex["values"], dtype=np.float64)[toks]
+    for g, logits in enumerate(ex["attention_logits_unscaled"]):
+        w = np.array([math.exp(scale * l) for l in logits])
+        expect = (w[:, None] * v).sum(0) / w.sum()
+        assert np.allclose(out[g], expect, rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------------------ S1 summaries
+def _rand_keys(rng, T, H, D, dtype):
+    x = rng.standard_normal((T, H, D)).astype(np.float32)
+    return x if dtype == "f32" else W.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ps,seq_len", [(16, 16 * 5 + 3), (1, 7), (4, 4), (64, 130)])
+def test_summary_bounds_attained_and_tail_masked(dtype, ps, seq_len):
+    rng = np.random.default_rng(ps * 1000 + seq_len)
+    T = -(-seq_len // ps) * ps + ps
+    keys = _rand_keys(rng, T, 3, 8, dtype)
+    kmin, kmax = O.page_summaries(keys, seq_len, ps, dtype)
+    v = O.to_f64(keys, dtype)
+    lo, hi = O.to_f64(kmin, dtype), O.to_f64(kmax, dtype)
+    for p in range(lo.shape[0]):
+        page = v[p * ps:min((p + 1) * ps, seq_len)]
+        assert np.all(page >= lo[p]) and np.all(page <= hi[p])
+        # attained: every summary element equals the element of some token of the page
+        assert np.all(np.any(page == lo[p], axis=0)) and np.all(np.any(page == hi[p], axis=0))
+    # junk past seq_len changes nothing
+    keys2 = keys.copy()
+    keys2[seq_len:] = _rand_keys(rng, T - seq_len, 3, 8, dtype) if T > seq_len else keys2[seq_len:]
+    kmin2, kmax2 = O.page_summaries(keys2, seq_len, ps, dtype)
+    assert np.array_equal(kmin, kmin2) and np.array_equal(kmax, kmax2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_summary_incremental_equals_rebuild_and_order_free(dtype):
+    rng = np.random.default_rng(7)
+    ps, n = 16, 16 * 3 + 5
+    keys = _rand_keys(rng, n, 2, 16, dtype)
+    full_lo, full_hi = O.page_summaries(keys, n, ps, dtype)
+    P = full_lo.shape[0]
+    lo = np.zeros_like(full_lo)
+    hi = np.zeros_like(full_hi)
+    for t in range(n):
+        p = t // ps
+        lo[p], hi[p] = O.summary_after_append(lo[p], hi[p], keys[t], t, ps, dtype)
+    assert np.array_equal(lo, full_lo) and np.array_equal(hi, full_hi)
+    # order inside a page does not matter
+    perm = np.concatenate([p * ps + rng.permutation(min(ps, n - p * ps)) for p in range(P)])
+    lo2, hi2 = O.page_summaries(keys[perm], n, ps, dtype)
+    assert np.array_equal(lo2, full_lo) and np.array_equal(hi2, full_hi)
+
+
+def test_summary_signed_zero_order():
+    # -0.0 < +0.0 in the min and max
+    keys = _f32([[0.0], [-0.0]])[:, None, :]
+    lo, hi = O.page_summaries(keys, 2, 2, "f32")
+    assert np.signbit(lo[0, 0, 0]) and not np.signbit(hi[0, 0, 0])
+    keys = _f32([[-0.0], [-0.0]])[:, None, :]
+    lo, hi = O.page_summaries(keys, 2, 2, "f32")
+    assert np.signbit(lo[0, 0, 0]) and np.signbit(hi[0, 0, 0])
+
+
+# ------------------------------------------------------------------ S2 Quest bound
+@pytest.mark.parametrize("seed", range(6))
+def test_bound_equals_max_over_box_corners(seed):
+    """The page bound is the maximum of the linear map x -> q.x over the axis-aligned box
+    [kmin, kmax]; a linear function reaches its maximum at a corner, so enumerating all 2^D
+    corners characterises the bound independently of its per-dimension formula."""
+    rng = np.random.default_rng(seed)
+    D, ps, P = 6, 4, 3
+    keys = rng.standard_normal((P * ps, 1, D)).astype(np.float32)
+    q = rng.standard_normal((1, D)).astype(np.float32)
+    kmin, kmax = O.page_summaries(keys, P * ps, ps, "f32")
+    s = O.quest_scores(q, kmin, kmax, "f32", 1.0)
+    qd = q[0].astype(np.float64)
+    for p in range(P):
+        lo, hi = kmin[p, 0].astype(np.float64), kmax[p, 0].astype(np.float64)
+        best = max(float(np.dot(qd, np.where(c, hi, lo))) for c in itertools.product([0, 1], repeat=D))
+        assert abs(s[0, p] - best) <= 1e-12 * (1 + abs(best))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bound_dominates_every_token_logit(seed):
+    rng = np.random.default_rng(100 + seed)
+    H_q, H_kv, D, ps, n = 8, 2, 16, 16, 16 * 4 + 9
+    keys = _rand_keys(rng, n, H_kv, D, "bf16")
+    q = W.f32_to_bf16_bits(rng.standard_normal((H_q, D)).astype(np.float32))
+    kmin, kmax = O.page_summaries(keys, n, ps, "bf16")
+    s = O.quest_scores(q, kmin, kmax, "bf16", 1.0)
+    kv, qv = O.to_f64(keys, "bf16"), O.to_f64(q, "bf16")
+    G = H_q // H_kv
+    for h in range(H_kv):
+        for p in range(s.shape[1]):
+            page = kv[p * ps:min((p + 1) * ps, n), h]
+            for g in range(h * G, (h + 1) * G):
+                logits = page @ qv[g]
+                tol = 1e-12 * float(np.abs(qv[g]).sum() * np.abs(page).max())
+                assert np.all(logits <= s[h, p] + tol)
+
+
+def test_bound_is_exact_logit_at_page_size_one_and_selects_textbook_topk():
+    """With one token per page the box is a point: the bound equals q.k exactly, so the
+    selection equals the textbook top-k of tokens by their max-over-group logit."""
+    rng = np.random.default_rng(5)
+    H_q, H_kv, D, n = 4, 1, 8, 40
+    keys = rng.standard_normal((n, H_kv, D)).astype(np.float32)
+    q = rng.standard_normal((H_q, D)).astype(np.float32)
+    kmin, kmax = O.page_summaries(keys, n, 1, "f32")
+    s = O.quest_scores(q, kmin, kmax, "f32", 1.0)
+    logits = torch.from_numpy(keys[:, 0].astype(np.float64)) @ torch.from_numpy(q.astype(np.float64)).T
+    best = logits.max(dim=1).values
+    assert torch.allclose(torch.from_numpy(s[0]), best, rtol=0, atol=1e-12)
+    b = 9
+    sel = O.select_pages(s[0], b)
+    inner = best[1:n - 1]
+    top = (torch.topk(inner, b - 2).indices + 1).tolist()
+    assert sel == sorted([0, n - 1] + top)
+
+
+def test_bound_group_max_and_scale():
+    rng = np.random.default_rng(11)
+    H_q, H_kv, D, n, ps = 8, 2, 16, 70, 16
+    keys = rng.standard_normal((n, H_kv, D)).astype(np.float32)
+    q = rng.standard_normal((H_q, D)).astype(np.float32)
+    kmin, kmax = O.page_summaries(keys, n, ps, "f32")
+    s = O.quest_scores(q, kmin, kmax, "f32", 0.25)
+    G = H_q // H_kv
+    for h in range(H_kv):
+        singles = [O.quest_scores(q[g:g + 1], kmin[:, h:h + 1], kmax[:, h:h + 1], "f32", 1.0)[0]
+                   for g in range(h * G, (h + 1) * G)]
+        assert np.allclose(s[h], 0.25 * np.max(singles, axis=0), rtol=1e-15, atol=0)
+
+
+def test_split_sign_identity_used_by_the_kernels():
+    """sum_d max(q kmin, q kmax) == sum_d max(q,0) kmax + min(q,0) kmin  (kmin <= kmax).
+    The GPU scorer evaluates the right-hand side; this guards that algebra on the CPU."""
+    rng = np.random.default_rng(3)
+    a, b = rng.standard_normal((2, 1000, 32))
+    lo, hi = np.minimum(a, b), np.maximum(a, b)
+    q = rng.standard_normal(32)
+    lhs = np.maximum(q * lo, q * hi).sum(-1)
+    rhs = (np.maximum(q, 0) * hi + np.minimum(q, 0) * lo).sum(-1)
+    assert np.allclose(lhs, rhs, rtol=1e-14, atol=1e-12)
+
+
+# ------------------------------------------------------------------ S3 selection
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8, 10])
+def test_selection_brute_force_subsets(P):
+    """For every budget the chosen non-forced set is the unique subset S of the right size
+    in which every member beats every non-member under (score desc, index asc)."""
+    rng = np.random.default_rng(P)
+    for trial in range(5):
+        scores = rng.integers(-3, 4, size=P).astype(np.float64)   # many ties on purpose
+        if trial == 4:
+            scores = np.zeros(P)
+        for b in range(2, P + 2):
+            sel = O.select_pages(scores, b)
+            forced = [0] if P == 1 else [0, P - 1]
+            k = min(b, P) - len(forced)
+            others = [p for p in range(P) if p not in forced]
+            winners = []
+            for S in itertools.combinations(others, k):
+                out = [y for y in others if y not in S]
+                if all((scores[x], -x) > (scores[y], -y) for x in S for y in out):
+                    winners.append(sorted(forced + list(S)))
+            assert len(winners) == 1 and winners[0] == sel
+            assert sel == sorted(set(sel)) and len(sel) == min(b, P)
+            assert 0 in sel and (P - 1) in sel
+
+
+def test_selection_tie_lower_index_wins_on_copied_page():
+    rng = np.random.default_rng(21)
+    ps, P, D = 16, 12, 32
+    keys = rng.standard_normal((P * ps, 1, D)).astype(np.float32)
+    q = rng.standard_normal((4, D)).astype(np.float32)
+    kmin, kmax = O.page_summaries(keys, P * ps, ps, "f32")
+    s = O.quest_scores(q, kmin, kmax, "f32", 1.0)
+    X = int(np.argmax(s[0][1:P - 1])) + 1                # best non-forced page
+    Y = P - 2 if X != P - 2 else 1
+    lo, hi = sorted((X, Y))
+    keys[hi * ps:(hi + 1) * ps] = keys[lo * ps:(lo + 1) * ps][::-1]   # identical summary
+    kmin, kmax = O.page_summaries(keys, P * ps, ps, "f32")
+    s = O.quest_scores(q, kmin, kmax, "f32", 1.0)
+    assert s[0, lo] == s[0, hi]
+    sel = O.select_pages(s[0], 3)
+    assert sel == [0, lo, P - 1]
+    # -0.0 and +0.0 scores tie too
+    z = np.array([1.0, -0.0, 0.0, -5.0, 2.0])
+    assert O.select_pages(z, 3) == [0, 1, 4]
+    z = np.array([1.0, 0.0, -0.0, -5.0, 2.0])
+    assert O.select_pages(z, 3) == [0, 1, 4]
+
+
+def test_selection_rejects_budget_below_two():
+    with pytest.raises(ValueError):
+        O.select_pages(np.zeros(3), 1)
+    assert O.select_pages(np.zeros(1), 1) == [0]
+
+
+# ------------------------------------------------------------------ S4 attention
+def _sdpa_reference(q, k, v, scale):
+    """torch's float64 scaled_dot_product_attention with GQA heads expanded; q [H_q, D],
+    k [T, H_kv, D], v [T, H_kv, D_v]."""
+    H_q, H_kv = q.shape[0], k.shape[1]
+    G = H_q // H_kv
+    qt = torch.from_numpy(q)[None, :, None, :]
+    kt = torch.from_numpy(np.repeat(k, G, axis=1)).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(np.repeat(v, G, axis=1)).permute(1, 0, 2)[None]
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)[0, :, 0].numpy()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ps,seq_len", [(16, 16 * 6 + 5), (1, 9), (64, 64)])
+def test_dense_equals_library_attention_and_full_budget_equals_dense(dtype, ps, seq_len):
+    rng = np.random.default_rng(ps + seq_len)
+    H_q, H_kv, D, Dv = 8, 2, 32, 24
+    T = seq_len + ps
+    keys = _rand_keys(rng, T, H_kv, D, dtype)
+    vals = _rand_keys(rng, T, H_kv, Dv, dtype)
+    q = _rand_keys(rng, H_q, 1, D, dtype)[:, 0]
+    scale = 1 / math.sqrt(D)
+    dense = O.dense_attention(q, keys, vals, seq_len, ps, dtype, scale)
+    ref = _sdpa_reference(O.to_f64(q, dtype), O.to_f64(keys[:seq_len], dtype), O.to_f64(vals[:seq_len], dtype), scale)
+    assert np.allclose(dense, ref, rtol=1e-12, atol=1e-12)
+    P = -(-seq_len // ps)
+    (_, _), scores, sel, out = O.decode_step(q, keys, vals, seq_len, ps, P + 3, dtype, scale)
+    assert all(s == list(range(P)) for s in sel)
+    assert np.array_equal(out, dense)
+
+
+def test_sparse_equals_library_attention_on_selected_tokens():
+    rng = np.random.default_rng(77)
+    H_q, H_kv, D, ps, n = 8, 2, 16, 16, 16 * 9 + 4
+    keys = _rand_keys(rng, n + ps, H_kv, D, "bf16")
+    vals = _rand_keys(rng, n + ps, H_kv, D, "bf16")
+    q = _rand_keys(rng, H_q, 1, D, "bf16")[:, 0]
+    scale = 0.3
+    (_, _), scores, sel, out = O.decode_step(q, keys, vals, n, ps, 4, "bf16", scale)
+    G = H_q // H_kv
+    for h in range(H_kv):
+        toks = O.page_tokens(sel[h], n, ps)
+        assert toks.max() < n
+        ref = _sdpa_reference(O.to_f64(q[h * G:(h + 1) * G], "bf16"), O.to_f64(keys[toks, h:h + 1], "bf16"),
+                              O.to_f64(vals[toks, h:h + 1], "bf16"), scale)
+        assert np.allclose(out[h * G:(h + 1) * G], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(9)
+    D = 8
+    q = rng.standard_normal(D)
+    # a single token returns its value
+    v = rng.standard_normal((1, 5))
+    assert np.allclose(O.softmax_attention(q, rng.standard_normal((1, D)), v, 0.7), v[0], rtol=0, atol=1e-15)
+    # identical keys return the mean of the values
+    k = np.tile(rng.standard_normal(D), (6, 1))
+    v = rng.standard_normal((6, 5))
+    assert np.allclose(O.softmax_attention(q, k, v, 0.7), v.mean(0), rtol=1e-14, atol=1e-14)
+    # very large logits stay finite (max subtraction)
+    k = np.tile(np.full(D, 1e3), (2, 1))
+    assert np.all(np.isfinite(O.softmax_attention(np.full(D, 1e3), k, v[:2], 1.0)))
+
+
+def test_block_table_permutation_invariance():
+    rng = np.random.default_rng(4)
+    ps, n, H, D = 16, 16 * 5 + 7, 2, 8
+    P = -(-n // ps)
+    keys = _rand_keys(rng, P * ps, H, D, "bf16")
+    for perm_seed in range(3):
+        perm = np.random.default_rng(perm_seed).permutation(P + 4)[:P]
+        cache = np.zeros((P + 4, ps, H, D), dtype=np.uint16)
+        for p in range(P):
+            cache[perm[p]] = keys[p * ps:(p + 1) * ps]
+        back = O.logical_from_cache(cache, perm, n, ps)
+        assert np.array_equal(back, keys[:n])
+
+
+# ------------------------------------------------------------------ generator sanity
+def test_workload_chunked_draws_are_consistent():
+    w = W.reduced(3)
+    i = 2
+    n = int(w.seq_lens[i])
+    full = w.keys(i)
+    part = w.keys(i, 100, min(n, 5000))
+    assert np.array_equal(full[100:min(n, 5000)], part)
+    k, v, cu = w.packed_prefill()
+    assert np.array_equal(k[cu[i]:cu[i + 1]], full)
+    bt = w.block_table
+    live = np.concatenate([bt[j, :w.pages(w.final_lens)[j]] for j in range(w.B)])
+    assert len(set(live.tolist())) == len(live) and live.max() < w.num_blocks
