@@ -1,0 +1,202 @@
+/*
+ * psk.h -- C ABI of page-selective sparse paged decode attention (one GPU, sm_103a).
+ *
+ * A decode step has four stages, one call each:
+ *
+ *   psk_kv_append_and_summarize   write new tokens into the paged K/V cache and keep each
+ *                                 page's per-KV-head elementwise key min / max summary
+ *                                 in step with it.
+ *   psk_page_score_select         score every page with the Quest-style upper bound
+ *                                 sum_d max(q_d*kmin_d, q_d*kmax_d), max over the GQA
+ *                                 group, times scale; keep the top-b pages per
+ *                                 (sequence, KV head) with the sink and tail forced.
+ *   psk_sparse_paged_decode       exact softmax attention over the selected pages only.
+ *   psk_dense_paged_decode        the same kernel over every page (full-KV baseline).
+ *
+ * Sources of each operation (pages on page-selective sparse KV attention):
+ *   - paged cache [2, num_blocks, page_size, H_kv, D] + block table, per-page key
+ *     min/max statistics, attention exact over the selection:
+ *     EntmaxKV README (deep-spin/entmaxkv), introduction;
+ *   - k_min / k_max refresh on append: EntmaxKV README, kernels/page_metadata.py and the
+ *     decode call that appends k_new / v_new (usage example);
+ *   - Quest-style page upper bound, top-k with the tail page counted in the budget:
+ *     EntmaxKV README, "Two selection strategies", Top-k; kernels/page_criticality.py,
+ *     kernels/page_topk.py;
+ *   - static top-b per (layer, KV head), sink and recent pages always kept and counted
+ *     inside b, GQA group combined by max: LOCKS (locks-kv) PKG-INFO, "How it works",
+ *     "Results" preamble and the configuration table (sink_pages / window_pages = 1 / 1,
+ *     quad_combine = max);
+ *   - prefill untouched, sparse decode reads only the selected pages: LOCKS PKG-INFO,
+ *     "How it works", Sparse decode; AMASS (amass-kv) PyPI page, introduction.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers to contiguous memory in the layouts stated,
+ *     16-byte aligned. Index tensors are int32. q, k_new, v_new, caches, summaries and out
+ *     share the storage type `layout->dtype` (PSK_BF16 or PSK_F32); arithmetic is fp32.
+ *   - The caller owns every buffer. The library allocates nothing, frees nothing and
+ *     keeps no state between calls apart from what it writes into the caller's buffers.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream). Host-side argument checks happen before any launch and are synchronous.
+ *   - Return value: PSK_OK or a psk_status code. PSK_ERR_CUDA reports a launch error.
+ *   - Device-side violations that the host cannot see (a block id outside
+ *     [0, num_blocks), a sequence longer than max_pages pages, a bad selected id, a
+ *     budget below 2 with more than one page) set a sticky bit in the workspace status
+ *     word and skip the affected unit (its selected row is written as -1, its output
+ *     rows as zeros); read it with psk_get_device_status. Nothing traps, asserts or waits.
+ *   - Workspace: every call takes a caller-allocated workspace of at least the size the
+ *     matching psk_*_workspace_size query returns; one buffer sized for the largest may
+ *     be shared by all calls on one stream. It must be zero-filled once before its first
+ *     use (every call leaves its internal counters at zero again); the status word stays
+ *     set until psk_clear_device_status. Calls sharing one workspace must not overlap on
+ *     the GPU (use one stream, or one workspace per stream).
+ *   - Preconditions the library does not check: no two live logical pages map to the same
+ *     physical block; inputs are finite.
+ */
+#ifndef PSK_H
+#define PSK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *psk_stream_t; /* a cudaStream_t */
+
+enum psk_dtype { PSK_F32 = 0, PSK_BF16 = 1 };
+
+enum psk_status {
+  PSK_OK = 0,
+  PSK_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, inconsistent shape       */
+  PSK_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, page_size, group size, ... */
+  PSK_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query returns  */
+  PSK_ERR_CUDA = 4         /* a CUDA launch failed (cudaGetLastError after the launch)  */
+};
+
+/* sticky device status bits (psk_get_device_status) */
+#define PSK_DEV_BAD_BLOCK 0x1u    /* block-table entry outside [0, num_blocks)              */
+#define PSK_DEV_BAD_SEQLEN 0x2u   /* seq_len < 1, or more than max_pages pages              */
+#define PSK_DEV_BAD_SELECTED 0x4u /* selected id outside [0, P) or list not ascending       */
+#define PSK_DEV_BAD_BUDGET 0x8u   /* budget < 2 with P > 1, or budget > b_max               */
+#define PSK_DEV_BAD_APPEND 0x10u  /* append position outside the block-table row, or n < 0  */
+
+/*
+ * Geometry of one layer's paged cache and of the decode batch.
+ *
+ *   k_cache  [num_blocks, page_size, num_kv_heads, head_dim]      (the K half of vLLM's
+ *   v_cache  [num_blocks, page_size, num_kv_heads, v_head_dim]     [2, num_blocks, ...])
+ *   summaries[num_blocks, num_kv_heads, 2, head_dim]  kmin at [...,0,:], kmax at [...,1,:],
+ *             indexed by PHYSICAL block, storage dtype (min / max are exact in any dtype)
+ *   block_table [batch, max_pages] int32: logical page -> physical block
+ *   seq_lens    [batch] int32 (tokens in the cache, >= 1)
+ *   q           [batch, num_q_heads, head_dim]; query head g reads KV head
+ *               g / (num_q_heads / num_kv_heads)
+ *   out         [batch, num_q_heads, v_head_dim]
+ *
+ * latent = 1 selects the MLA form: num_kv_heads = 1, the cache holds one latent vector per
+ * token (k_cache), the value is its first v_head_dim elements and v_cache must be NULL.
+ */
+typedef struct psk_layout {
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t v_head_dim;
+  int32_t page_size;
+  int32_t num_blocks;
+  int32_t max_pages;
+  int32_t dtype; /* enum psk_dtype */
+  int32_t latent;
+} psk_layout;
+
+/* ---------------------------------------------------------------------------------------
+ * Stage 1: append tokens and refresh page summaries.
+ *
+ * For sequence i, the n_i = cu_new[i+1] - cu_new[i] rows k_new[cu_new[i] + j] (j < n_i)
+ * are written at token positions t = start_pos[i] + j: slot t % page_size of physical block
+ * block_table[i][t / page_size]. Every page the call touches gets its summary refreshed so
+ * that it covers all tokens of the page below start_pos[i] + n_i: a page whose first token
+ * is written by this call starts a fresh summary; a page that already held tokens is widened
+ * by the new ones (elementwise min / max, -0.0 ordered below +0.0).
+ *   decode: n_i = 1, start_pos = the sequence length before the append;
+ *   prefill: start_pos = 0, n_i = prompt length.
+ * seq_lens is NOT modified: after the call the caller's length is start_pos[i] + n_i.
+ *
+ *   k_new [total_new, num_kv_heads, head_dim], v_new [total_new, num_kv_heads, v_head_dim]
+ *   (latent: v_new and v_cache NULL). start_pos [batch], cu_new [batch + 1] device int32.
+ *   total_new = cu_new[batch]; max_new >= every n_i (sizes the launch grid).
+ * --------------------------------------------------------------------------------------- */
+int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, const void *v_new,
+                                const int32_t *start_pos, const int32_t *cu_new, int32_t total_new,
+                                int32_t max_new, void *k_cache, void *v_cache, void *summaries,
+                                const int32_t *block_table, void *workspace, size_t workspace_bytes,
+                                psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stages 2 + 3: page scores and top-b selection.
+ *
+ * For sequence i with P_i = ceil(seq_lens[i] / page_size) pages and KV head h:
+ *   score[i,h,p] = scale * max_{g in group(h)} sum_d max(q[i,g,d]*kmin[p,h,d], q[i,g,d]*kmax[p,h,d])
+ * with the summaries of block block_table[i][p]. Selected pages: the sink 0 and the tail
+ * P_i - 1 always, plus the min(b_i, P_i) - |{0, P_i - 1}| highest-scoring other pages, ties
+ * to the lower page index. b_i = budgets[i] (device int32 [batch], 2 <= b_i <= b_max, or any
+ * 1 <= b_i <= b_max when P_i == 1).
+ *
+ *   selected  [batch, num_kv_heads, b_max] int32 out: ascending logical page ids, padded
+ *             with -1 after the min(b_i, P_i) valid entries.
+ *   scores_out [batch, num_kv_heads, max_pages] fp32 out, optional (NULL = not written):
+ *             the scores above for p < P_i; entries p >= P_i are left untouched.
+ * Scores accumulate in fp32. scale is normally 1/sqrt(head_dim).
+ * --------------------------------------------------------------------------------------- */
+int psk_page_score_select(const psk_layout *layout, const void *q, const void *summaries,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          const int32_t *budgets, int32_t b_max, float scale, int32_t *selected,
+                          float *scores_out, void *workspace, size_t workspace_bytes,
+                          psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stage 4: exact softmax attention over the selected pages.
+ *
+ *   out[i,g,:] = sum_t softmax_t(scale * q[i,g] . k_t) v_t
+ * over the tokens t < seq_lens[i] of the pages listed in selected[i, g / G, :] (read up to
+ * the first -1 or b_max entries; ids must be ascending and in [0, P_i)). The pages are split
+ * across CTAs; each split keeps an fp32 online-softmax state (m, l, O) and a combine pass
+ * merges the splits by log-sum-exp. out is written in the storage dtype.
+ * --------------------------------------------------------------------------------------- */
+int psk_sparse_paged_decode(const psk_layout *layout, const void *q, const void *k_cache,
+                            const void *v_cache, const int32_t *block_table,
+                            const int32_t *seq_lens, const int32_t *selected, int32_t b_max,
+                            float scale, void *out, void *workspace, size_t workspace_bytes,
+                            psk_stream_t stream);
+
+/* Full-KV decode with the same kernel skeleton: every page 0 .. P_i - 1 of every KV head. */
+int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *block_table,
+                           const int32_t *seq_lens, float scale, void *out, void *workspace,
+                           size_t workspace_bytes, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Workspace sizes (bytes). Return 0 when the layout is invalid or unsupported.
+ * --------------------------------------------------------------------------------------- */
+size_t psk_append_workspace_size(const psk_layout *layout);
+size_t psk_score_select_workspace_size(const psk_layout *layout, int32_t b_max);
+size_t psk_sparse_decode_workspace_size(const psk_layout *layout, int32_t b_max);
+size_t psk_dense_decode_workspace_size(const psk_layout *layout);
+
+/* Copy the sticky device status word of `workspace` to *flags (synchronises `stream`). */
+int psk_get_device_status(const void *workspace, uint32_t *flags, psk_stream_t stream);
+/* Zero the status word (asynchronous on `stream`). */
+int psk_clear_device_status(void *workspace, psk_stream_t stream);
+
+/* Short English description of a psk_status code (static storage). */
+const char *psk_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int psk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSK_H */

@@ -1,0 +1,200 @@
+"""Python binding of libpsk, the C ABI of page-selective sparse paged decode attention.
+
+Argument marshalling only: every step runs in the library's CUDA kernels. Tensors are
+torch CUDA tensors (torch provides device memory and streams); each call passes their
+device pointers, the layout and the current torch stream to the matching ``psk_*``
+entry point and raises ``PskError`` on a non-zero status. The shared library is loaded
+lazily from this directory on first use and there is no fallback: if ``libpsk.so`` is
+missing the call fails with instructions to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpsk.so")
+
+PSK_F32, PSK_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda"}
+DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND = 0x1, 0x2, 0x4, 0x8, 0x10
+
+EXPORTS = [
+    "psk_kv_append_and_summarize", "psk_page_score_select", "psk_sparse_paged_decode",
+    "psk_dense_paged_decode", "psk_append_workspace_size", "psk_score_select_workspace_size",
+    "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
+    "psk_clear_device_status", "psk_status_string", "psk_version",
+]
+
+
+class PskError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {code})")
+        self.code = code
+
+
+class PskLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim", "v_head_dim", "page_size",
+        "num_blocks", "max_pages", "dtype", "latent")]
+
+
+@dataclass(frozen=True)
+class Layout:
+    """Geometry of one layer's paged cache and decode batch (mirrors ``psk_layout``)."""
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    v_head_dim: int
+    page_size: int
+    num_blocks: int
+    max_pages: int
+    dtype: int = PSK_BF16
+    latent: int = 0
+
+    def c(self) -> PskLayout:
+        return PskLayout(self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim, self.v_head_dim,
+                         self.page_size, self.num_blocks, self.max_pages, self.dtype, self.latent)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpsk.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m page_sparse_kv_gb300.build` "
+                               "(or __graft_entry__.build()); there is no non-CUDA fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        LP = ctypes.POINTER(PskLayout)
+        sig = {
+            "psk_kv_append_and_summarize": (ctypes.c_int, [LP, P, P, P, P, I, I, P, P, P, P, P, Z, P]),
+            "psk_page_score_select": (ctypes.c_int, [LP, P, P, P, P, P, I, F, P, P, P, Z, P]),
+            "psk_sparse_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P, Z, P]),
+            "psk_dense_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, F, P, P, Z, P]),
+            "psk_append_workspace_size": (Z, [LP]),
+            "psk_score_select_workspace_size": (Z, [LP, I]),
+            "psk_sparse_decode_workspace_size": (Z, [LP, I]),
+            "psk_dense_decode_workspace_size": (Z, [LP]),
+            "psk_get_device_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+            "psk_clear_device_status": (ctypes.c_int, [P, P]),
+            "psk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "psk_version": (ctypes.c_int, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------------------ helpers
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        msg = lib().psk_status_string(code).decode()
+        raise PskError(fn, code, msg)
+
+
+def storage_dtype(layout: Layout):
+    import torch
+    return torch.float32 if layout.dtype == PSK_F32 else torch.bfloat16
+
+
+# ------------------------------------------------------------------------------ sizes
+def append_workspace_size(layout: Layout) -> int:
+    return int(lib().psk_append_workspace_size(ctypes.byref(layout.c())))
+
+
+def score_select_workspace_size(layout: Layout, b_max: int) -> int:
+    return int(lib().psk_score_select_workspace_size(ctypes.byref(layout.c()), int(b_max)))
+
+
+def sparse_decode_workspace_size(layout: Layout, b_max: int) -> int:
+    return int(lib().psk_sparse_decode_workspace_size(ctypes.byref(layout.c()), int(b_max)))
+
+
+def dense_decode_workspace_size(layout: Layout) -> int:
+    return int(lib().psk_dense_decode_workspace_size(ctypes.byref(layout.c())))
+
+
+def workspace_size(layout: Layout, b_max: int) -> int:
+    """Bytes of one workspace that serves every call of this layout and budget bound."""
+    sizes = [append_workspace_size(layout), score_select_workspace_size(layout, b_max),
+             sparse_decode_workspace_size(layout, b_max), dense_decode_workspace_size(layout)]
+    if min(sizes) == 0:
+        raise PskError("workspace_size", 2, "layout not supported")
+    return max(sizes)
+
+
+def make_workspace(layout: Layout, b_max: int, device=None):
+    """A zero-filled workspace tensor (uint8) sized for every call of this layout."""
+    import torch
+    return torch.zeros(workspace_size(layout, b_max), dtype=torch.uint8, device=device or "cuda")
+
+
+# ------------------------------------------------------------------------------ calls
+def kv_append_and_summarize(layout: Layout, k_new, v_new, start_pos, cu_new, max_new: int, k_cache, v_cache,
+                            summaries, block_table, workspace, stream=None):
+    total_new = int(k_new.shape[0]) if k_new is not None else 0
+    _check("psk_kv_append_and_summarize", lib().psk_kv_append_and_summarize(
+        ctypes.byref(layout.c()), _ptr(k_new), _ptr(v_new), _ptr(start_pos), _ptr(cu_new), total_new,
+        int(max_new), _ptr(k_cache), _ptr(v_cache), _ptr(summaries), _ptr(block_table), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def page_score_select(layout: Layout, q, summaries, block_table, seq_lens, budgets, b_max: int, scale: float,
+                      selected, workspace, scores_out=None, stream=None):
+    _check("psk_page_score_select", lib().psk_page_score_select(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), _ptr(budgets),
+        int(b_max), float(scale), _ptr(selected), _ptr(scores_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def sparse_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max: int,
+                        scale: float, out, workspace, stream=None):
+    _check("psk_sparse_paged_decode", lib().psk_sparse_paged_decode(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(selected), int(b_max), float(scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dense_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, scale: float, out, workspace,
+                       stream=None):
+    _check("psk_dense_paged_decode", lib().psk_dense_paged_decode(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def get_device_status(workspace, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check("psk_get_device_status", lib().psk_get_device_status(_ptr(workspace), ctypes.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+def clear_device_status(workspace, stream=None):
+    _check("psk_clear_device_status", lib().psk_clear_device_status(_ptr(workspace), _stream(stream)))
+
+
+def version() -> int:
+    return int(lib().psk_version())

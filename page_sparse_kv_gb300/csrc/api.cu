@@ -1,0 +1,236 @@
+// C ABI of libpsk: host-side argument checks, workspace planning and kernel dispatch.
+// Every entry point validates before it launches anything and never allocates.
+#include <cstdint>
+#include <cstring>
+
+#include "psk_common.cuh"
+#include "psk_internal.h"
+
+using namespace psk;
+
+namespace {
+
+int elem_bytes(int dtype) { return dtype == PSK_F32 ? 4 : 2; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every call.
+int check_layout(const psk_layout *L) {
+  if (!L) return PSK_ERR_INVALID_ARG;
+  if (L->batch < 1 || L->num_q_heads < 1 || L->num_kv_heads < 1 || L->head_dim < 1 || L->v_head_dim < 1 ||
+      L->page_size < 1 || L->num_blocks < 1 || L->max_pages < 1)
+    return PSK_ERR_INVALID_ARG;
+  if (L->num_q_heads % L->num_kv_heads != 0) return PSK_ERR_INVALID_ARG;
+  if (L->dtype != PSK_F32 && L->dtype != PSK_BF16) return PSK_ERR_INVALID_ARG;
+  if (L->latent != 0 && L->latent != 1) return PSK_ERR_INVALID_ARG;
+  if (L->latent && (L->num_kv_heads != 1 || L->v_head_dim > L->head_dim)) return PSK_ERR_INVALID_ARG;
+  const int es = elem_bytes(L->dtype);
+  if ((L->head_dim * es) % 16 != 0 || (L->v_head_dim * es) % 16 != 0) return PSK_ERR_UNSUPPORTED;
+  return PSK_OK;
+}
+
+int check_gqa_compute(const psk_layout *L) {
+  if (L->latent) return PSK_ERR_UNSUPPORTED;
+  const int G = L->num_q_heads / L->num_kv_heads;
+  if (!score_supported(L->dtype, L->head_dim, G)) return PSK_ERR_UNSUPPORTED;
+  if (!decode_supported(L->dtype, L->head_dim, L->v_head_dim, G, L->page_size)) return PSK_ERR_UNSUPPORTED;
+  return PSK_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PSK_OK : PSK_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int psk_version(void) { return 100; }
+
+const char *psk_status_string(int status) {
+  switch (status) {
+    case PSK_OK: return "ok";
+    case PSK_ERR_INVALID_ARG: return "invalid argument";
+    case PSK_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PSK_ERR_WORKSPACE: return "workspace missing or too small";
+    case PSK_ERR_CUDA: return "CUDA launch error";
+    default: return "unknown status";
+  }
+}
+
+size_t psk_append_workspace_size(const psk_layout *layout) {
+  return check_layout(layout) == PSK_OK ? kWsHeader : 0;
+}
+
+size_t psk_score_select_workspace_size(const psk_layout *layout, int32_t b_max) {
+  if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
+  ScorePlan plan;
+  return plan_score(*layout, b_max, &plan) ? plan.ws_bytes : 0;
+}
+
+size_t psk_sparse_decode_workspace_size(const psk_layout *layout, int32_t b_max) {
+  if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
+  DecodePlan plan;
+  return plan_decode(*layout, b_max, false, &plan) ? plan.ws_bytes : 0;
+}
+
+size_t psk_dense_decode_workspace_size(const psk_layout *layout) {
+  if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK) return 0;
+  DecodePlan plan;
+  return plan_decode(*layout, layout->max_pages, true, &plan) ? plan.ws_bytes : 0;
+}
+
+int psk_get_device_status(const void *workspace, uint32_t *flags, psk_stream_t stream) {
+  if (!workspace || !flags) return PSK_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return PSK_ERR_CUDA;
+  *flags = v;
+  return PSK_OK;
+}
+
+int psk_clear_device_status(void *workspace, psk_stream_t stream) {
+  if (!workspace) return PSK_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
+}
+
+int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, const void *v_new,
+                                const int32_t *start_pos, const int32_t *cu_new, int32_t total_new,
+                                int32_t max_new, void *k_cache, void *v_cache, void *summaries,
+                                const int32_t *block_table, void *workspace, size_t workspace_bytes,
+                                psk_stream_t stream) {
+  int rc = check_layout(layout);
+  if (rc != PSK_OK) return rc;
+  const psk_layout &L = *layout;
+  if (total_new < 0 || max_new < 0) return PSK_ERR_INVALID_ARG;
+  if (!start_pos || !cu_new || !k_cache || !summaries || !block_table) return PSK_ERR_INVALID_ARG;
+  if (L.latent ? (v_new != nullptr || v_cache != nullptr) : (!v_cache || (total_new > 0 && !v_new)))
+    return PSK_ERR_INVALID_ARG;
+  if (total_new > 0 && !k_new) return PSK_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(summaries))
+    return PSK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWsHeader) return PSK_ERR_WORKSPACE;
+  if (total_new == 0 || max_new == 0) return PSK_OK;
+  AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.start_pos = start_pos;
+  a.cu_new = cu_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.summaries = summaries;
+  a.block_table = block_table;
+  a.ws = workspace;
+  a.B = L.batch;
+  a.H_kv = L.num_kv_heads;
+  a.D = L.head_dim;
+  a.D_v = L.v_head_dim;
+  a.ps = L.page_size;
+  a.nb = L.num_blocks;
+  a.max_pages = L.max_pages;
+  return cuda_status(launch_append(a, L.dtype, max_new, static_cast<cudaStream_t>(stream)));
+}
+
+int psk_page_score_select(const psk_layout *layout, const void *q, const void *summaries,
+                          const int32_t *block_table, const int32_t *seq_lens, const int32_t *budgets,
+                          int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
+                          size_t workspace_bytes, psk_stream_t stream) {
+  int rc = check_layout(layout);
+  if (rc != PSK_OK) return rc;
+  const psk_layout &L = *layout;
+  if (!q || !summaries || !block_table || !seq_lens || !budgets || !selected || b_max < 1)
+    return PSK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summaries)) return PSK_ERR_INVALID_ARG;
+  rc = check_gqa_compute(layout);
+  if (rc != PSK_OK) return rc;
+  ScorePlan plan;
+  if (!plan_score(L, b_max, &plan)) return PSK_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < plan.ws_bytes) return PSK_ERR_WORKSPACE;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  ScoreArgs a;
+  a.q = q;
+  a.summaries = summaries;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.budgets = budgets;
+  a.selected = selected;
+  a.scores_out = scores_out;
+  a.ws = workspace;
+  a.counters = reinterpret_cast<uint32_t *>(ws + plan.off_counters);
+  a.cand_key = reinterpret_cast<uint32_t *>(ws + plan.off_key);
+  a.cand_page = reinterpret_cast<int32_t *>(ws + plan.off_page);
+  a.cand_count = reinterpret_cast<int32_t *>(ws + plan.off_count);
+  a.B = L.batch;
+  a.H_q = L.num_q_heads;
+  a.H_kv = L.num_kv_heads;
+  a.D = L.head_dim;
+  a.ps = L.page_size;
+  a.nb = L.num_blocks;
+  a.max_pages = L.max_pages;
+  a.b_max = b_max;
+  a.chunk = plan.chunk;
+  a.n_chunks_max = plan.n_chunks_max;
+  a.k_cap = plan.k_cap;
+  a.scale = scale;
+  return cuda_status(launch_score_select(a, L.dtype, static_cast<cudaStream_t>(stream)));
+}
+
+static int decode_common(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
+                         int32_t b_max, float scale, void *out, void *workspace, size_t workspace_bytes,
+                         psk_stream_t stream) {
+  int rc = check_layout(layout);
+  if (rc != PSK_OK) return rc;
+  const psk_layout &L = *layout;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PSK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PSK_ERR_INVALID_ARG;
+  rc = check_gqa_compute(layout);
+  if (rc != PSK_OK) return rc;
+  const bool dense = selected == nullptr;
+  DecodePlan plan;
+  if (!plan_decode(L, dense ? L.max_pages : b_max, dense, &plan)) return PSK_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < plan.ws_bytes) return PSK_ERR_WORKSPACE;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  DecodeArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.selected = selected;
+  a.out = out;
+  a.ws = workspace;
+  a.part_o = reinterpret_cast<float *>(ws + plan.off_o);
+  a.part_ml = reinterpret_cast<float *>(ws + plan.off_ml);
+  a.B = L.batch;
+  a.H_q = L.num_q_heads;
+  a.H_kv = L.num_kv_heads;
+  a.D = L.head_dim;
+  a.D_v = L.v_head_dim;
+  a.ps = L.page_size;
+  a.nb = L.num_blocks;
+  a.max_pages = L.max_pages;
+  a.b_max = dense ? L.max_pages : b_max;
+  a.split = plan.split;
+  a.n_splits_max = plan.n_splits_max;
+  a.scale = scale;
+  return cuda_status(launch_decode(a, L.dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int psk_sparse_paged_decode(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
+                            int32_t b_max, float scale, void *out, void *workspace, size_t workspace_bytes,
+                            psk_stream_t stream) {
+  if (!selected || b_max < 1) return PSK_ERR_INVALID_ARG;
+  return decode_common(layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max, scale, out, workspace,
+                       workspace_bytes, stream);
+}
+
+int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens, float scale, void *out,
+                           void *workspace, size_t workspace_bytes, psk_stream_t stream) {
+  return decode_common(layout, q, k_cache, v_cache, block_table, seq_lens, nullptr, 0, scale, out, workspace,
+                       workspace_bytes, stream);
+}
+
+}  // extern "C"

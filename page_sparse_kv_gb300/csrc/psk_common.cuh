@@ -1,0 +1,127 @@
+// Device helpers shared by the psk kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "../../include/psk.h"
+
+namespace psk {
+
+// ------------------------------------------------------------------------------------
+// workspace header: the first 256 bytes of every workspace
+// ------------------------------------------------------------------------------------
+constexpr size_t kWsHeader = 256;
+struct WsHeader {
+  uint32_t status;  // sticky PSK_DEV_* bits
+};
+
+__device__ __forceinline__ void set_status(void *ws, uint32_t bit) {
+  atomicOr(&reinterpret_cast<WsHeader *>(ws)->status, bit);
+}
+
+__host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------------------------
+// storage types: bf16 is carried as its 16-bit pattern
+// ------------------------------------------------------------------------------------
+struct bf16_t {
+  uint16_t bits;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t *>(&b);
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kBytes = 4;
+  static constexpr int kPerChunk = 4;  // elements per 16-byte chunk
+  __device__ __forceinline__ static void to_f2(const uint4 &c, float2 *out) {
+    out[0] = make_float2(__uint_as_float(c.x), __uint_as_float(c.y));
+    out[1] = make_float2(__uint_as_float(c.z), __uint_as_float(c.w));
+  }
+  // 8-byte group (2 elements) -> floats
+  __device__ __forceinline__ static void to_f2_8(const uint2 &c, float2 *out) {
+    out[0] = make_float2(__uint_as_float(c.x), __uint_as_float(c.y));
+  }
+  __device__ __forceinline__ static void store(float *p, float v) { *p = v; }
+};
+template <> struct Elem<bf16_t> {
+  static constexpr int kBytes = 2;
+  static constexpr int kPerChunk = 8;
+  __device__ __forceinline__ static void to_f2(const uint4 &c, float2 *out) {
+    out[0] = bf16x2_to_f2(c.x);
+    out[1] = bf16x2_to_f2(c.y);
+    out[2] = bf16x2_to_f2(c.z);
+    out[3] = bf16x2_to_f2(c.w);
+  }
+  // 8-byte group (4 elements) -> floats
+  __device__ __forceinline__ static void to_f2_8(const uint2 &c, float2 *out) {
+    out[0] = bf16x2_to_f2(c.x);
+    out[1] = bf16x2_to_f2(c.y);
+  }
+  __device__ __forceinline__ static void store(bf16_t *p, float v) { p->bits = f32_to_bf16_bits(v); }
+};
+
+// ------------------------------------------------------------------------------------
+// order-preserving integer images
+// ------------------------------------------------------------------------------------
+// Signed-integer image of a float bit pattern under IEEE totalOrder (non-NaN):
+// -0.0 sorts below +0.0, larger value -> larger integer.
+__device__ __forceinline__ int32_t f32_order_key(uint32_t bits) {
+  int32_t i = static_cast<int32_t>(bits);
+  return i ^ ((i >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ int32_t bf16_order_key(uint32_t bits16) {
+  int32_t i = static_cast<int32_t>(static_cast<int16_t>(static_cast<uint16_t>(bits16)));
+  return i ^ ((i >> 15) & 0x7FFF);
+}
+
+// Unsigned selection key of a score: larger score -> larger key; -0.0 and +0.0 map to the
+// same key (they tie). Key 0 is never produced by a finite score and marks "no candidate".
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------------------------------------
+// packed fp32x2 FMA (sm_100+): d = a * b + c on both lanes
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+// ------------------------------------------------------------------------------------
+// cp.async (16-byte, L2-only) with zero fill
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// copies 16 bytes when `pred`, else writes 16 zero bytes without reading global memory
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
+  int n = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace psk

@@ -1,0 +1,80 @@
+// Launchers shared between the kernel translation units and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/psk.h"
+
+namespace psk {
+
+struct AppendArgs {
+  const void *k_new;
+  const void *v_new;
+  const int32_t *start_pos;
+  const int32_t *cu_new;
+  void *k_cache;
+  void *v_cache;
+  void *summaries;
+  const int32_t *block_table;
+  void *ws;
+  int B, H_kv, D, D_v, ps, nb, max_pages;
+};
+cudaError_t launch_append(const AppendArgs &a, int dtype, int max_new, cudaStream_t s);
+
+struct ScoreArgs {
+  const void *q;
+  const void *summaries;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const int32_t *budgets;
+  int32_t *selected;
+  float *scores_out;
+  void *ws;
+  // workspace regions
+  uint32_t *counters;     // [B * H_kv]
+  uint32_t *cand_key;     // [B * H_kv, n_chunks_max, k_cap]
+  int32_t *cand_page;     // same shape
+  int32_t *cand_count;    // [B * H_kv, n_chunks_max]
+  int B, H_q, H_kv, D, ps, nb, max_pages, b_max;
+  int chunk;              // pages per score CTA
+  int n_chunks_max;
+  int k_cap;              // candidates kept per chunk = min(b_max - 2, chunk) (>= 1)
+  float scale;
+};
+struct ScorePlan {
+  int chunk, n_chunks_max, k_cap;
+  size_t ws_bytes;
+  size_t off_counters, off_key, off_page, off_count;
+};
+bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan);
+cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s);
+bool score_supported(int dtype, int D, int G);
+
+struct DecodeArgs {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const int32_t *selected;  // NULL: dense (every page)
+  void *out;
+  void *ws;
+  float *part_o;   // [B * H_kv, n_splits_max, G, D_v]
+  float *part_ml;  // [B * H_kv, n_splits_max, G, 2]
+  int B, H_q, H_kv, D, D_v, ps, nb, max_pages;
+  int b_max;       // entries per selected row (sparse) or max_pages (dense)
+  int split;       // entries (pages) per CTA
+  int n_splits_max;
+  float scale;
+};
+struct DecodePlan {
+  int split, n_splits_max;
+  size_t ws_bytes, off_o, off_ml;
+};
+bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan);
+cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);
+bool decode_supported(int dtype, int D, int D_v, int G, int ps);
+
+}  // namespace psk

@@ -1,0 +1,449 @@
+// Stages 2 + 3: Quest-style page scores and top-b page selection (GQA caches).
+//
+// Score (EntmaxKV README, "Two selection strategies", Top-k; kernels/page_criticality.py):
+//   score[i,h,p] = scale * max_{g in group(h)} sum_d max(q_gd * kmin_pd, q_gd * kmax_pd)
+// The kernel evaluates each term as max(q,0) * kmax + min(q,0) * kmin, which equals
+// max(q * kmin, q * kmax) exactly whenever kmin <= kmax (one of the two products is +-0),
+// so every kept product is the same fp32 product; accumulation is fp32.
+//
+// Selection (LOCKS PKG-INFO, "How it works", Selection: a static top-b per (layer, KV head);
+// sink and recent page always kept and counted inside b; EntmaxKV "Top-k": the budget
+// includes the always-attended tail page; ties to the lower logical page index).
+//
+// Layout of the work: one CTA (8 warps) per (KV head, chunk of `chunk` pages, sequence).
+// A page's summary for one KV head is 2 * D contiguous elements; LPP = D * sizeof(T) / 16
+// lanes read its kmin and kmax rows with one 16-byte load each, so a warp scores 32 / LPP
+// pages per step with fully used 32-byte sectors. Partial sums are reduced across the LPP
+// lanes by a transposing butterfly (each step halves the values a lane carries), then the
+// group max is taken across the lanes that ended up holding different query heads.
+//
+// Each CTA keeps its chunk's scores as 32-bit order keys in shared memory, selects the
+// chunk-local top-k (k = b - 2 free slots) with an MSB-first 8-bit radix select, and writes
+// the winners (ascending page order) to the workspace. The last CTA of a (sequence, KV head)
+// to finish (an atomic ticket, no waiting) merges all chunk winners with a second radix
+// select and writes the final ascending list: sink, winners, tail, then -1 padding.
+// Top-k of the union of chunk top-k's is the global top-k because every key is unique
+// once ties are ordered by page index.
+#include <algorithm>
+
+#include "psk_common.cuh"
+#include "psk_internal.h"
+
+namespace psk {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMergeCap = 8192;  // candidates the merge CTA can hold
+
+// ------------------------------------------------------------------------------------
+// block-wide helpers (blockDim.x == kThreads)
+// ------------------------------------------------------------------------------------
+// Exclusive prefix sum of one int per thread in thread order; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int x, int *sh, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < kWarps ? sh[lane] : 0;
+    int winc = w;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += y;
+    }
+    if (lane < kWarps) sh[lane] = winc - w;
+    if (lane == kWarps - 1) sh[kWarps] = winc;
+  }
+  __syncthreads();
+  const int res = inc - x + sh[warp];
+  if (total) *total = sh[kWarps];
+  __syncthreads();
+  return res;
+}
+
+// Radix select over keys[0..n) (key 0 = not a candidate): finds the k-th largest key T and
+// how many keys equal to T belong to the top k (the lowest-indexed ones). Requires
+// 1 <= k <= number of nonzero keys.
+__device__ void radix_select(const uint32_t *keys, int n, int k, int *hist, int *sh, uint32_t *T_out,
+                             int *need_eq_out) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist[tid] = 0;  // kThreads == 256 bins
+    __syncthreads();
+    for (int base = 0; base < n; base += kThreads) {
+      const int x = base + tid;
+      const uint32_t key = x < n ? keys[x] : 0u;
+      const bool ok = key != 0u && (key & mask) == prefix;
+      const uint32_t d = ok ? ((key >> shift) & 255u) : 0xFFFFFFFFu;
+      const unsigned grp = __match_any_sync(0xffffffffu, d);
+      if (ok && (__ffs(grp) - 1) == lane) atomicAdd(&hist[d], __popc(grp));
+    }
+    __syncthreads();
+    // suffix sums: thread t looks at bin 255 - t
+    const int bin = 255 - tid;
+    const int hb = hist[bin];
+    const int excl = block_exclusive_scan(hb, sh, nullptr);  // keys with digit > bin
+    const int incl = excl + hb;                              // keys with digit >= bin
+    if (incl >= need && excl < need) {
+      sh[kWarps + 1] = bin;
+      sh[kWarps + 2] = excl;
+    }
+    __syncthreads();
+    const int d = sh[kWarps + 1];
+    need -= sh[kWarps + 2];
+    prefix |= static_cast<uint32_t>(d) << shift;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  *T_out = prefix;
+  *need_eq_out = need;
+}
+
+// Writes, in index order, every item taken by the rule
+//   take_all:  key != 0
+//   otherwise: key > T, or key == T among the first need_eq such items
+// to out_key / out_page (page = pages ? pages[x] : page_base + x). Returns the count.
+__device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int page_base, int n, bool take_all,
+                             uint32_t T, int need_eq, uint32_t *out_key, int32_t *out_page, int *sh) {
+  const int tid = threadIdx.x;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int x0 = min(n, tid * per), x1 = min(n, x0 + per);
+  int eq = 0;
+  if (!take_all)
+    for (int x = x0; x < x1; ++x) eq += keys[x] == T;
+  const int eq_base = take_all ? 0 : block_exclusive_scan(eq, sh, nullptr);
+  int cnt = 0, seen = eq_base;
+  for (int x = x0; x < x1; ++x) {
+    const uint32_t key = keys[x];
+    bool take;
+    if (take_all) {
+      take = key != 0u;
+    } else {
+      take = key > T;
+      if (key == T) take = (seen++ < need_eq);
+    }
+    cnt += take;
+  }
+  int total;
+  const int base = block_exclusive_scan(cnt, sh, &total);
+  int w = base;
+  seen = eq_base;
+  for (int x = x0; x < x1; ++x) {
+    const uint32_t key = keys[x];
+    bool take;
+    if (take_all) {
+      take = key != 0u;
+    } else {
+      take = key > T;
+      if (key == T) take = (seen++ < need_eq);
+    }
+    if (take) {
+      if (out_key) out_key[w] = key;
+      out_page[w] = pages ? pages[x] : page_base + x;
+      ++w;
+    }
+  }
+  return total;
+}
+
+// ------------------------------------------------------------------------------------
+// reductions across the LPP lanes of one page
+// ------------------------------------------------------------------------------------
+// v[g] holds this lane's partial sum for query head g. Returns, on every lane of the page
+// group, max over g of the full sums.
+template <int G, int LPP>
+__device__ __forceinline__ float group_score(float (&v)[G], int lane) {
+  int L = G;
+#pragma unroll
+  for (int mask = LPP / 2; mask >= 1; mask >>= 1) {
+    if (L > 1) {
+      const int half = L / 2;
+      const bool upper = (lane & mask) != 0;
+#pragma unroll
+      for (int k = 0; k < (G > 1 ? G / 2 : 1); ++k) {
+        if (k < half) {
+          const float mine = upper ? v[k + half] : v[k];
+          const float other = upper ? v[k] : v[k + half];
+          v[k] = mine + __shfl_xor_sync(0xffffffffu, other, mask);
+        }
+      }
+      L = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+    }
+  }
+  float mx = v[0];
+#pragma unroll
+  for (int k = 1; k < G; ++k)
+    if (k < L) mx = fmaxf(mx, v[k]);
+  // max over the lanes that carried different heads (the masks used by the transposing steps)
+  constexpr int kLogG = (G >= 8) ? 3 : (G >= 4) ? 2 : (G >= 2) ? 1 : 0;
+  constexpr int kLogL = (LPP >= 32) ? 5 : (LPP >= 16) ? 4 : (LPP >= 8) ? 3 : (LPP >= 4) ? 2 : (LPP >= 2) ? 1 : 0;
+  constexpr int kSteps = kLogG < kLogL ? kLogG : kLogL;
+#pragma unroll
+  for (int s = 0; s < kSteps; ++s) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, LPP >> (s + 1)));
+  return mx;
+}
+
+// ------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 2) score_select_kernel(ScoreArgs a) {
+  constexpr int EPC = Elem<T>::kPerChunk;
+  constexpr int LPP = D / EPC;   // lanes per page
+  constexpr int PPW = 32 / LPP;  // pages per warp step
+  constexpr int U = 4;           // page steps in flight per lane
+  static_assert(LPP >= 1 && LPP <= 32 && (LPP & (LPP - 1)) == 0, "row must be 16..512 bytes, power of 2");
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int hist[256];
+  __shared__ int sh[kWarps + 4];
+  __shared__ int flag_last;
+
+  const int h = blockIdx.x, c = blockIdx.y, i = blockIdx.z;
+  const int unit = i * a.H_kv + h;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
+
+  if (seq_len < 1 || P > a.max_pages) {
+    if (c == 0) {
+      if (tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
+      for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
+    }
+    return;
+  }
+  const int budget = a.budgets[i];
+  if ((budget < 2 && P > 1) || budget < 1 || budget > a.b_max) {
+    if (c == 0) {
+      if (tid == 0) set_status(a.ws, PSK_DEV_BAD_BUDGET);
+      for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
+    }
+    return;
+  }
+  const int nch = (P + a.chunk - 1) / a.chunk;
+  if (c >= nch) return;
+  const int count = min(budget, P);
+  const int n_forced = P == 1 ? 1 : 2;
+  const int k_free = count - n_forced;
+  const bool keep_all = count >= P;
+
+  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);
+  const int p0 = c * a.chunk;
+  const int p1 = min(P, p0 + a.chunk);
+
+  // ---- scores -------------------------------------------------------------------------
+  {
+    const int sub = lane % LPP;  // which 16-byte chunk of the row
+    const int grp = lane / LPP;  // which page of the warp step
+    float2 qp[G][EPC / 2], qn[G][EPC / 2];
+    const T *qrow = reinterpret_cast<const T *>(a.q) + ((size_t)i * a.H_q + (size_t)h * G) * D + sub * EPC;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float2 f[EPC / 2];
+      Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(qrow + (size_t)g * D), f);
+#pragma unroll
+      for (int e = 0; e < EPC / 2; ++e) {
+        qp[g][e] = make_float2(fmaxf(f[e].x, 0.f), fmaxf(f[e].y, 0.f));
+        qn[g][e] = make_float2(fminf(f[e].x, 0.f), fminf(f[e].y, 0.f));
+      }
+    }
+    const T *sumbase = reinterpret_cast<const T *>(a.summaries);
+    const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
+    float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
+
+    for (int base = p0 + warp * PPW; base < p1; base += kWarps * PPW * U) {
+      uint4 lo[U], hi[U];
+      bool okb[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int p = base + u * kWarps * PPW + grp;
+        okb[u] = false;
+        lo[u] = make_uint4(0, 0, 0, 0);
+        hi[u] = lo[u];
+        if (p < p1) {
+          const int blk = bt[p];
+          if (blk >= 0 && blk < a.nb) {
+            const T *s = sumbase + ((size_t)blk * a.H_kv + h) * 2 * D + sub * EPC;
+            lo[u] = __ldg(reinterpret_cast<const uint4 *>(s));
+            hi[u] = __ldg(reinterpret_cast<const uint4 *>(s + D));
+            okb[u] = true;
+          } else if (sub == 0) {
+            set_status(a.ws, PSK_DEV_BAD_BLOCK);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int p = base + u * kWarps * PPW + grp;
+        if (base + u * kWarps * PPW >= p1) break;  // warp-uniform
+        float2 kl[EPC / 2], kh[EPC / 2];
+        Elem<T>::to_f2(lo[u], kl);
+        Elem<T>::to_f2(hi[u], kh);
+        float v[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < EPC / 2; ++e) {
+            acc = ffma2(qp[g][e], kh[e], acc);
+            acc = ffma2(qn[g][e], kl[e], acc);
+          }
+          v[g] = acc.x + acc.y;
+        }
+        const float s = group_score<G, LPP>(v, lane) * a.scale;
+        if (sub == 0 && p < p1) {
+          const bool forced = (p == 0) || (p == P - 1);
+          keys[p - p0] = (okb[u] && !forced) ? score_key(s) : 0u;
+          if (srow) srow[p] = s;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- chunk-local top-k ----------------------------------------------------------------
+  const int slot = unit * a.n_chunks_max + c;
+  if (!keep_all && k_free > 0) {
+    const int n = p1 - p0;
+    int valid = 0;
+    for (int x = tid; x < n; x += kThreads) valid += keys[x] != 0u;
+    int total_valid;
+    block_exclusive_scan(valid, sh, &total_valid);
+    uint32_t thr = 0;
+    int need_eq = 0;
+    const bool take_all = total_valid <= k_free;
+    if (!take_all) radix_select(keys, n, k_free, hist, sh, &thr, &need_eq);
+    uint32_t *ck = a.cand_key + (size_t)slot * a.k_cap;
+    int32_t *cp = a.cand_page + (size_t)slot * a.k_cap;
+    const int wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, ck, cp, sh);
+    if (tid == 0) a.cand_count[slot] = wrote;
+  } else if (tid == 0) {
+    a.cand_count[slot] = 0;
+  }
+
+  // ---- last CTA of the unit merges -------------------------------------------------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&a.counters[unit], 1u);
+    flag_last = (prev == (unsigned)(nch - 1));
+  }
+  __syncthreads();
+  if (!flag_last) return;
+  __threadfence();
+  if (tid == 0) a.counters[unit] = 0u;
+
+  if (keep_all) {
+    for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = x < P ? x : -1;
+    return;
+  }
+  // gather chunk winners (ascending pages, chunk after chunk)
+  uint32_t *mkey = reinterpret_cast<uint32_t *>(smem_raw);
+  int32_t *mpage = reinterpret_cast<int32_t *>(smem_raw + sizeof(uint32_t) * kMergeCap);
+  int n_c = 0;
+  if (k_free > 0) {
+    for (int cc = 0; cc < nch; ++cc) {
+      const int sl = unit * a.n_chunks_max + cc;
+      const int cnt = __ldcg(a.cand_count + sl);
+      const uint32_t *ck = a.cand_key + (size_t)sl * a.k_cap;
+      const int32_t *cp = a.cand_page + (size_t)sl * a.k_cap;
+      for (int x = tid; x < cnt; x += kThreads) {
+        mkey[n_c + x] = __ldcg(ck + x);
+        mpage[n_c + x] = __ldcg(cp + x);
+      }
+      n_c += cnt;
+    }
+  }
+  __syncthreads();
+  // output row: sink, winners, tail, -1 padding
+  if (tid == 0) sel_row[0] = 0;
+  if (k_free > 0) {
+    uint32_t thr = 0;
+    int need_eq = 0;
+    const bool take_all = n_c <= k_free;
+    if (!take_all) radix_select(mkey, n_c, k_free, hist, sh, &thr, &need_eq);
+    const int wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + 1, sh);
+    // fewer winners than free slots only after a flagged bad block: pad the gap
+    for (int x = 1 + wrote + tid; x < count - 1; x += kThreads) sel_row[x] = -1;
+  }
+  if (tid == 0 && P > 1) sel_row[count - 1] = P - 1;
+  for (int x = count + tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
+  const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
+  auto kfn = score_select_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.H_kv, a.n_chunks_max, a.B);
+  kfn<<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
+  const int kfree_max = std::max(1, b_max - 2);
+  int chunk = 512;
+  while (true) {
+    const int nch = (L.max_pages + chunk - 1) / chunk;
+    const int kcap = std::min(kfree_max, chunk);
+    if ((long long)nch * kcap <= kMergeCap) break;
+    chunk *= 2;
+    if (chunk > 16384) return false;
+  }
+  plan->chunk = chunk;
+  plan->n_chunks_max = (L.max_pages + chunk - 1) / chunk;
+  plan->k_cap = std::min(kfree_max, chunk);
+  const size_t units = (size_t)L.batch * L.num_kv_heads;
+  size_t off = kWsHeader;
+  plan->off_counters = off;
+  off = align_up(off + units * 4, 256);
+  plan->off_key = off;
+  off = align_up(off + units * plan->n_chunks_max * plan->k_cap * 4, 256);
+  plan->off_page = off;
+  off = align_up(off + units * plan->n_chunks_max * plan->k_cap * 4, 256);
+  plan->off_count = off;
+  off = align_up(off + units * plan->n_chunks_max * 4, 256);
+  plan->ws_bytes = off;
+  return true;
+}
+
+#define PSK_SCORE_CASES(X)  \
+  X(bf16_t, PSK_BF16, 128, 4) \
+  X(bf16_t, PSK_BF16, 64, 4)  \
+  X(float, PSK_F32, 64, 4)    \
+  X(float, PSK_F32, 128, 4)
+
+bool score_supported(int dtype, int D, int G) {
+#define X(TT, DT, DD, GG) \
+  if (dtype == DT && D == DD && G == GG) return true;
+  PSK_SCORE_CASES(X)
+#undef X
+  return false;
+}
+
+cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s) {
+  const int D = a.D, G = a.H_q / a.H_kv;
+#define X(TT, DT, DD, GG) \
+  if (dtype == DT && D == DD && G == GG) return launch_t<TT, DD, GG>(a, s);
+  PSK_SCORE_CASES(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace psk

@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads and exports every symbol include/psk.h declares; host-side
+argument checks answer without a GPU (no kernel is launched by any call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from page_sparse_kv_gb300.build import build
+    build()
+    import page_sparse_kv_gb300 as psk
+    return psk.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "psk.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(psk_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    import page_sparse_kv_gb300 as psk
+    assert set(psk.EXPORTS) == set(names)
+
+
+def test_status_strings_and_version(lib):
+    import page_sparse_kv_gb300 as psk
+    assert psk.version() == 100
+    for code in range(5):
+        assert lib.psk_status_string(code)
+    assert lib.psk_status_string(99) == b"unknown status"
+
+
+def test_host_checks_reject_before_launch(lib):
+    import page_sparse_kv_gb300 as psk
+    good = psk.Layout(2, 32, 8, 128, 128, 16, 100, 50)
+    assert psk.score_select_workspace_size(good, 10) > 256
+    assert psk.sparse_decode_workspace_size(good, 10) > 256
+    assert psk.dense_decode_workspace_size(good) > 256
+    assert psk.append_workspace_size(good) == 256
+    # unsupported head dim / group size / page size -> size 0
+    assert psk.score_select_workspace_size(psk.Layout(2, 32, 8, 96, 96, 16, 100, 50), 10) == 0
+    assert psk.dense_decode_workspace_size(psk.Layout(2, 24, 8, 128, 128, 16, 100, 50)) == 0
+    assert psk.dense_decode_workspace_size(psk.Layout(2, 32, 8, 128, 128, 8, 100, 50)) == 0
+    # invalid layouts
+    assert psk.append_workspace_size(psk.Layout(0, 32, 8, 128, 128, 16, 100, 50)) == 0
+    assert psk.append_workspace_size(psk.Layout(1, 30, 8, 128, 128, 16, 100, 50)) == 0
+    L = good.c()
+    P = ctypes.c_void_p
+    # null pointers -> PSK_ERR_INVALID_ARG without touching the GPU
+    rc = lib.psk_page_score_select(ctypes.byref(L), None, None, None, None, None, 10, 1.0, None, None, None, 0, None)
+    assert rc == 1
+    rc = lib.psk_dense_paged_decode(ctypes.byref(L), None, None, None, None, None, 1.0, None, None, 0, None)
+    assert rc == 1
+    rc = lib.psk_sparse_paged_decode(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), None, 10, 1.0, P(16),
+                                     P(16), 1 << 30, None)
+    assert rc == 1
+    # misaligned pointer
+    rc = lib.psk_dense_paged_decode(ctypes.byref(L), P(17), P(16), P(16), P(16), P(16), 1.0, P(16), P(16), 1 << 30,
+                                    None)
+    assert rc == 1
+    # too-small workspace -> PSK_ERR_WORKSPACE
+    rc = lib.psk_dense_paged_decode(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), 1.0, P(16), P(16), 64, None)
+    assert rc == 3
+    # empty append is a no-op that returns OK before any launch
+    rc = lib.psk_kv_append_and_summarize(ctypes.byref(L), None, None, P(16), P(16), 0, 0, P(16), P(16), P(16), P(16),
+                                         P(16), 256, None)
+    assert rc == 0
