@@ -188,13 +188,13 @@ def test_nan_junk_past_seq_len_is_never_read():
 
 
 def test_ties_resolve_to_lower_page():
-    """Pages with identical keys (hence identical summaries and scores) tie; the lower page wins."""
-    w = _custom([16 * 12], [3], H_q=4, H_kv=1)
+    """Pages with identical keys (hence identical summaries and scores) tie; with the cutoff
+    inside the tied group the lowest-indexed tied pages win."""
+    w = _custom([16 * 12], [12], H_q=4, H_kv=1)
     cache = upload(w)
     keys = w.keys(0)
-    # copy page 3 into pages 5..10 in the device cache and refresh summaries via append
-    src = keys[3 * 16:4 * 16]
-    for p in range(5, 11):
+    src = keys[3 * 16:4 * 16].copy()
+    for p in range(5, 11):   # pages 5..10 become copies of page 3 (rewritten through the append kernel)
         cache.append(to_torch(src, w.dtype).cuda(), to_torch(w.values(0)[p * 16:(p + 1) * 16], w.dtype).cuda(),
                      torch.tensor([p * 16], dtype=torch.int32, device="cuda"),
                      torch.tensor([0, 16], dtype=torch.int32, device="cuda"), 16)
@@ -202,11 +202,14 @@ def test_ties_resolve_to_lower_page():
     q = w.queries()
     kmin, kmax = O.page_summaries(keys, 16 * 12, 16, w.dtype)
     s = O.quest_scores(q[0], kmin, kmax, w.dtype, 1 / math.sqrt(w.D))[0]
-    # make the tied page the best non-forced page by choosing q = its direction if needed
-    sel = cache.score_select(to_torch(q, w.dtype).cuda(), dev_budgets(w))
-    got = [int(x) for x in sel.cpu().numpy()[0, 0] if x >= 0]
-    assert got == O.select_pages(s, 3)
     assert all(s[p] == s[3] for p in range(5, 11))
+    above = sum(1 for p in (1, 2, 4) if s[p] > s[3])
+    b = 2 + above + 3                                  # takes 3 of the 7 tied pages
+    sel = cache.score_select(to_torch(q, w.dtype).cuda(), torch.tensor([b], dtype=torch.int32, device="cuda"))
+    got = [int(x) for x in sel.cpu().numpy()[0, 0] if x >= 0]
+    ref = O.select_pages(s, b)
+    assert got == ref
+    assert [p for p in ref if p in (3, 5, 6, 7, 8, 9, 10)] == [3, 5, 6]
 
 
 def test_device_status_on_bad_block_table():
