@@ -1,0 +1,380 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of page-selective sparse paged attention on one GB300 (per rank).
+
+One step = the whole hot path over one batch: append one decode token per sequence with its
+page-summary refresh, score + select pages, sparse split-K decode (4 kernel launches).
+The same run times the dense decode step (append + full-KV decode) for the speedup.
+
+Default workload: batched ragged decode, B=64, H_q=32, H_kv=8, D=128, page 16, contexts
+U[8192, 65536], bf16, budget max(4, ceil(5% of pages)), 16 hot pages per KV head.
+Inputs stay larger than L2 every step (summaries ~0.6 GB, selected K/V ~0.5 GB in a 9.7 GB
+pool), so no L2 flush is needed.
+
+    python bench.py [--steps K] [--warmup W] [--impl psk|reference] [--workload 1..4]
+    torchrun --nproc-per-node N bench.py --gpus N      # N independent replicas (weak scaling)
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode µs/step/layer; achieved HBM GB/s vs GB300 peak; speedup vs dense"
+UNIT = "us/step/layer"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# ------------------------------------------------------------------------------------------
+def oracle_sample(w, budget_s: float, start_seq: int = 0):
+    """Times the oracle's sparse decode step (score every page, select, attend) on sequences
+    taken in order from ``start_seq`` until ``budget_s`` seconds of oracle work accumulated.
+    Page summaries are prepared untimed (they are cache state the append step maintains).
+    Returns (seconds per full batch step, sequences timed)."""
+    import oracle as O
+    scale = 1.0 / math.sqrt(w.D)
+    spent, n = 0.0, 0
+    i = start_seq
+    while spent < budget_s and n < w.B:
+        L = int(w.seq_lens[i])
+        keys, vals = w.keys(i), w.values(i)
+        kmin, kmax = O.page_summaries(keys, L, w.page_size, w.dtype)
+        q = w.query(i)
+        t0 = time.perf_counter()
+        s = O.quest_scores(q, kmin, kmax, w.dtype, scale)
+        sel = [O.select_pages(s[h], int(w.budgets[i])) for h in range(w.H_kv)]
+        O.attend_pages(q, keys, vals, L, w.page_size, sel, w.dtype, scale)
+        spent += time.perf_counter() - t0
+        n += 1
+        i = (i + 1) % w.B
+    return spent / n * w.B, n
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    w = W.config(args.workload)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for s in range(args.warmup):
+        oracle_sample(w, per_step, start_seq=s % w.B)
+    times, seqs = [], 0
+    for s in range(args.steps):
+        t, n = oracle_sample(w, per_step, start_seq=(args.warmup + s) % w.B)
+        times.append(t)
+        seqs += n
+    us = statistics.mean(times) * 1e6
+    sample = (f"{seqs} sequence-steps of the fp64 oracle's sparse step (score all pages, select, attend), "
+              f"~{per_step:.0f} s per step, scaled to the {w.B}-sequence batch")
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "D": w.D,
+                       "page_size": w.page_size, "budget": "max(4, ceil(5% of pages))"},
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+def run_psk(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import page_sparse_kv_gb300 as psk
+    import workloads as W
+    from workloads.device import budgets as dev_budgets, to_torch, upload
+
+    w = W.config(args.workload)
+    t_setup = time.time()
+    cache = upload(w)
+    L = cache.layout
+    B, Hq, Hkv, D = w.B, w.H_q, w.H_kv, w.D
+    es = w.elem_bytes
+    dev = cache.device
+    stream = torch.cuda.current_stream()
+
+    # the decode token of every sequence: its last token (re-appended in place each step, so the
+    # cache state is identical before and after a step)
+    lens = w.seq_lens.astype(np.int64)
+    k_last = np.stack([w.keys(i, int(lens[i]) - 1, int(lens[i]))[0] for i in range(B)])
+    v_last = np.stack([w.values(i, int(lens[i]) - 1, int(lens[i]))[0] for i in range(B)])
+    q_host = w.queries()
+    k_new = to_torch(k_last, w.dtype).to(dev)
+    v_new = to_torch(v_last, w.dtype).to(dev)
+    q = to_torch(q_host, w.dtype).to(dev)
+    start = torch.from_numpy((lens - 1).astype(np.int32)).to(dev)
+    cu = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    bud = dev_budgets(w)
+    sel = torch.empty(B, Hkv, w.b_max, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Hq, D, dtype=cache.dtype, device=dev)
+    out_dense = torch.empty_like(out)
+    ws = cache.ws
+    setup_s = time.time() - t_setup
+
+    def append():
+        psk.kv_append_and_summarize(L, k_new, v_new, start, cu, 1, cache.k_cache, cache.v_cache, cache.summaries,
+                                    cache.block_table, ws)
+
+    def score():
+        psk.page_score_select(L, q, cache.summaries, cache.block_table, cache.seq_lens, bud, w.b_max, cache.scale,
+                              sel, ws)
+
+    def decode():
+        psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
+                                w.b_max, cache.scale, out, ws)
+
+    def dense():
+        psk.dense_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, cache.scale,
+                               out_dense, ws)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- warm-up ---------------------------------------------------------------------------
+    for _ in range(args.warmup):
+        append(); score(); decode()
+        append(); dense()
+    torch.cuda.synchronize()
+    assert psk.get_device_status(ws) == 0, "device status set during warm-up"
+
+    # ---- timed sparse steps (per-kernel events on the launching stream) -------------------------
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier()
+    with Clocks(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(K):
+            e = ev[k]
+            e[0].record(stream)
+            append()
+            e[1].record(stream)
+            score()
+            e[2].record(stream)
+            decode()
+            e[3].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        # dense steps in the same clock window
+        Kd = max(3, K // 4)
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(Kd):
+            append(); dense()
+        d1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    sparse_ms = t0.elapsed_time(t1) / K
+    dense_ms = d0.elapsed_time(d1) / Kd
+    t_app = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    t_dec = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
+    if dist is not None:
+        tt = torch.tensor([sparse_ms, dense_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        sparse_ms, dense_ms = tt.tolist()
+
+    # ---- end to end: host buffers through the C ABI (pinned H2D of the step's inputs, D2H of out)
+    qh = to_torch(q_host, w.dtype).pin_memory()
+    kh = to_torch(k_last, w.dtype).pin_memory()
+    vh = to_torch(v_last, w.dtype).pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    Ke = max(3, K // 4)
+    for _ in range(2):
+        q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True); v_new.copy_(vh, non_blocking=True)
+        append(); score(); decode(); oh.copy_(out, non_blocking=True)
+    barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(Ke):
+        q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True); v_new.copy_(vh, non_blocking=True)
+        append(); score(); decode()
+        oh.copy_(out, non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / Ke
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * es
+    d2h = oh.numel() * es
+    assert psk.get_device_status(ws) == 0, "device status set during the timed region"
+
+    # ---- algorithmic bytes --------------------------------------------------------------------
+    P = (lens + w.page_size - 1) // w.page_size
+    summ_bytes = int(P.sum()) * Hkv * 2 * D * es
+    q_bytes = B * Hq * D * es
+    out_bytes = B * Hq * D * es
+    sel_np = sel.cpu().numpy()
+    sel_tokens = 0
+    for i in range(B):
+        for h in range(Hkv):
+            pages = sel_np[i, h][sel_np[i, h] >= 0]
+            sel_tokens += int(np.minimum(w.page_size, lens[i] - pages * w.page_size).sum())
+    kv_bytes = sel_tokens * Hkv // Hkv * (D + w.D_v) * es
+    score_bytes = summ_bytes + q_bytes
+    decode_bytes = kv_bytes + q_bytes + out_bytes
+    step_bytes = summ_bytes + kv_bytes + q_bytes + out_bytes
+    dense_bytes = int(lens.sum()) * Hkv * (D + w.D_v) * es + q_bytes + out_bytes
+    peak, peak_kind = peaks()
+    if t_score >= t_dec:
+        dom, dom_bytes, dom_ms = "score_select_kernel", score_bytes, t_score
+    else:
+        dom, dom_bytes, dom_ms = "decode_split_kernel+combine_kernel", decode_bytes, t_dec
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, nseq = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": secs * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{nseq} of {B} sequences through the fp64 oracle's sparse step (score all pages, select, "
+                         f"attend), scaled to the full batch; single thread"}
+
+    clocks = clk.summary()
+    us = sparse_ms * 1e3
+    line = {
+        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": sparse_ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H_q": Hq, "H_kv": Hkv, "D": D, "page_size": w.page_size,
+                   "contexts": "U[8192, 65536] seeded" if args.workload == 3 else [int(x) for x in lens[:4]],
+                   "budget_pages_total": int(w.budgets.sum()), "l2": "inputs larger than L2, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": dom_bytes, "launch_us": dom_ms * 1e3},
+        "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / (sparse_ms * 1e-3) / 1e9,
+                     "frac_of_measured": step_bytes / (sparse_ms * 1e-3) / 1e9 / peak,
+                     "frac_of_8TBs": step_bytes / (sparse_ms * 1e-3) / 1e9 / 8000.0},
+        "dense": {"us_per_step": dense_ms * 1e3, "bytes": dense_bytes,
+                  "gbs": dense_bytes / (dense_ms * 1e-3) / 1e9},
+        "speedup_vs_dense": dense_ms / sparse_ms,
+        "kernels_us": {"append": t_app * 1e3, "score_select": t_score * 1e3, "sparse_decode": t_dec * 1e3},
+        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * 4,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "setup_s": round(setup_s, 1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="psk", choices=["psk", "reference"])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_psk(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -427,7 +427,7 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
   plan->split = std::min(split, kMaxSplit);
   plan->n_splits_max = (entries + plan->split - 1) / plan->split;
   const int G = L.num_q_heads / L.num_kv_heads;
-  size_t off = kWsHeader;
+  size_t off = ws_scratch_offset((size_t)units);
   plan->off_o = off;
   off = align_up(off + (size_t)units * plan->n_splits_max * G * L.v_head_dim * 4, 256);
   plan->off_ml = off;

@@ -23,6 +23,17 @@ __device__ __forceinline__ void set_status(void *ws, uint32_t bit) {
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace layout shared by every call, so one buffer can serve all of them in stream order:
+//   [0, 256)                      header (status word)
+//   [256, 256 + 4 * units)        score/select merge tickets, one per (sequence, KV head)
+//   [.., + 4 * units)             decode merge tickets
+//   [ws_scratch_offset(units), ..) per-call scratch (candidates, split partials), which any
+//                                 later call may overwrite
+// Tickets are only ever touched by their own op and are back at zero when each call ends.
+inline size_t ws_score_tickets_offset() { return kWsHeader; }
+inline size_t ws_decode_tickets_offset(size_t units) { return kWsHeader + units * 4; }
+inline size_t ws_scratch_offset(size_t units) { return align_up(kWsHeader + 2 * units * 4, 256); }
+
 // ------------------------------------------------------------------------------------
 // storage types: bf16 is carried as its 16-bit pattern
 // ------------------------------------------------------------------------------------

@@ -410,9 +410,8 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   plan->n_chunks_max = (L.max_pages + chunk - 1) / chunk;
   plan->k_cap = std::min(kfree_max, chunk);
   const size_t units = (size_t)L.batch * L.num_kv_heads;
-  size_t off = kWsHeader;
-  plan->off_counters = off;
-  off = align_up(off + units * 4, 256);
+  plan->off_counters = ws_score_tickets_offset();
+  size_t off = ws_scratch_offset(units);
   plan->off_key = off;
   off = align_up(off + units * plan->n_chunks_max * plan->k_cap * 4, 256);
   plan->off_page = off;
