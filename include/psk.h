@@ -177,6 +177,26 @@ int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *
                            size_t workspace_bytes, psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Stage 4 without a workspace (no counterpart in the pages: an addition for callers that
+ * cannot allocate device memory). Some host programs own every byte of device memory
+ * through their own allocator and pass a plugin only its inputs and outputs, or run a loop
+ * that must never call cudaMalloc. This call computes exactly what psk_sparse_paged_decode
+ * computes, but keeps its split partials in a 32 MiB device array inside the library
+ * (allocated once per GPU when the library loads, held until exit); it allocates nothing.
+ *   - Returns PSK_ERR_WORKSPACE when the partials (the size psk_sparse_decode_workspace_size
+ *     reports) exceed 32 MiB.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU race and must be
+ *     serialised by the caller. Each call zeroes the array's header before use.
+ *   - Device-side input violations are not reported (the status word is internal).
+ * --------------------------------------------------------------------------------------- */
+int psk_sparse_paged_decode_noalloc(const psk_layout *layout, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_table,
+                                    const int32_t *seq_lens, const int32_t *selected, int32_t b_max,
+                                    float scale, void *out, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Workspace sizes (bytes). Return 0 when the layout is invalid or unsupported.
  * --------------------------------------------------------------------------------------- */
 size_t psk_append_workspace_size(const psk_layout *layout);

@@ -22,7 +22,7 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND 
 
 EXPORTS = [
     "psk_kv_append_and_summarize", "psk_page_score_select", "psk_sparse_paged_decode",
-    "psk_dense_paged_decode", "psk_append_workspace_size", "psk_score_select_workspace_size",
+    "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version",
 ]
@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
             "psk_page_score_select": (ctypes.c_int, [LP, P, P, P, P, P, I, F, P, P, P, Z, P]),
             "psk_sparse_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P, Z, P]),
             "psk_dense_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, F, P, P, Z, P]),
+            "psk_sparse_paged_decode_noalloc": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P]),
             "psk_append_workspace_size": (Z, [LP]),
             "psk_score_select_workspace_size": (Z, [LP, I]),
             "psk_sparse_decode_workspace_size": (Z, [LP, I]),
@@ -184,6 +185,15 @@ def dense_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_len
     _check("psk_dense_paged_decode", lib().psk_dense_paged_decode(
         ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         float(scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def sparse_paged_decode_noalloc(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max: int,
+                                scale: float, out, stream=None):
+    """sparse_paged_decode without a workspace, for callers that cannot allocate device memory:
+    the library's fixed 32 MiB per-device scratch holds the split partials (see psk.h)."""
+    _check("psk_sparse_paged_decode_noalloc", lib().psk_sparse_paged_decode_noalloc(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(selected), int(b_max), float(scale), _ptr(out), _stream(stream)))
 
 
 def get_device_status(workspace, stream=None) -> int:
