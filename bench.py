@@ -180,6 +180,8 @@ def run_psk(args):
     from workloads.device import budgets as dev_budgets, to_torch, upload
 
     w = W.config(args.workload)
+    if args.batch and args.batch < w.B:
+        w = W.prefix(w, args.batch)
     t_setup = time.time()
     cache = upload(w)
     L = cache.layout
@@ -367,6 +369,7 @@ def main():
     ap.add_argument("--impl", default="psk", choices=["psk", "reference"])
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

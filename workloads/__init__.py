@@ -345,3 +345,11 @@ def reduced(idx: int, seed_offset: int = 0) -> Workload:
                         seq_lens=lens, budgets=_budget_frac(P, 0.05, 4), n_hot=8, hot_rule="random",
                         latent=True, pool_slack=5)
     raise ValueError(idx)
+
+
+def prefix(w: Workload, n: int) -> Workload:
+    """The first n sequences of workload w (same seeds, so the same per-sequence draws), with a
+    physical pool of their own."""
+    return Workload(w.name + f"[:{n}]", w.seed, w.dtype, B=n, H_q=w.H_q, H_kv=w.H_kv, D=w.D, D_v=w.D_v,
+                    page_size=w.page_size, seq_lens=w.seq_lens[:n], budgets=w.budgets[:n], n_hot=w.n_hot,
+                    hot_rule=w.hot_rule, appends=w.appends, latent=w.latent, pool_slack=w.pool_slack)
