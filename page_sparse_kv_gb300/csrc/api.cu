@@ -157,6 +157,7 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.scores_out = scores_out;
   a.ws = workspace;
   a.counters = reinterpret_cast<uint32_t *>(ws + plan.off_counters);
+  a.keys = reinterpret_cast<uint32_t *>(ws + plan.off_keys);
   a.cand_key = reinterpret_cast<uint32_t *>(ws + plan.off_key);
   a.cand_page = reinterpret_cast<int32_t *>(ws + plan.off_page);
   a.cand_count = reinterpret_cast<int32_t *>(ws + plan.off_count);
@@ -168,6 +169,7 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.nb = L.num_blocks;
   a.max_pages = L.max_pages;
   a.b_max = b_max;
+  a.pchunk = plan.pchunk;
   a.chunk = plan.chunk;
   a.n_chunks_max = plan.n_chunks_max;
   a.k_cap = plan.k_cap;
@@ -202,6 +204,7 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.ws = workspace;
   a.part_o = reinterpret_cast<float *>(ws + plan.off_o);
   a.part_ml = reinterpret_cast<float *>(ws + plan.off_ml);
+  a.tickets = reinterpret_cast<uint32_t *>(ws + plan.off_tickets);
   a.B = L.batch;
   a.H_q = L.num_q_heads;
   a.H_kv = L.num_kv_heads;
@@ -211,8 +214,8 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.nb = L.num_blocks;
   a.max_pages = L.max_pages;
   a.b_max = dense ? L.max_pages : b_max;
-  a.split = plan.split;
-  a.n_splits_max = plan.n_splits_max;
+  a.sw = plan.sw;
+  a.n_items_max = plan.n_items_max;
   a.scale = scale;
   return cuda_status(launch_decode(a, L.dtype, static_cast<cudaStream_t>(stream)));
 }

@@ -89,6 +89,7 @@ extern "C" int psk_sparse_paged_decode_noalloc(const psk_layout *layout, const v
   a.ws = scratch;
   a.part_o = reinterpret_cast<float *>(ws + plan.off_o);
   a.part_ml = reinterpret_cast<float *>(ws + plan.off_ml);
+  a.tickets = reinterpret_cast<uint32_t *>(ws + plan.off_tickets);
   a.B = L.batch;
   a.H_q = L.num_q_heads;
   a.H_kv = L.num_kv_heads;
@@ -98,8 +99,8 @@ extern "C" int psk_sparse_paged_decode_noalloc(const psk_layout *layout, const v
   a.nb = L.num_blocks;
   a.max_pages = L.max_pages;
   a.b_max = b_max;
-  a.split = plan.split;
-  a.n_splits_max = plan.n_splits_max;
+  a.sw = plan.sw;
+  a.n_items_max = plan.n_items_max;
   a.scale = scale;
   return launch_decode(a, L.dtype, s) == cudaSuccess ? PSK_OK : PSK_ERR_CUDA;
 }

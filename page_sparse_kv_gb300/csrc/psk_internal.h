@@ -34,19 +34,21 @@ struct ScoreArgs {
   void *ws;
   // workspace regions
   uint32_t *counters;     // [B * H_kv]
+  uint32_t *keys;         // [B * H_kv, max_pages] selection keys written by the score kernel
   uint32_t *cand_key;     // [B * H_kv, n_chunks_max, k_cap]
   int32_t *cand_page;     // same shape
   int32_t *cand_count;    // [B * H_kv, n_chunks_max]
   int B, H_q, H_kv, D, ps, nb, max_pages, b_max;
-  int chunk;              // pages per score CTA
+  int pchunk;             // pages per streaming score CTA
+  int chunk;              // pages per selection CTA
   int n_chunks_max;
   int k_cap;              // candidates kept per chunk = min(b_max - 2, chunk) (>= 1)
   float scale;
 };
 struct ScorePlan {
-  int chunk, n_chunks_max, k_cap;
+  int pchunk, chunk, n_chunks_max, k_cap;
   size_t ws_bytes;
-  size_t off_counters, off_key, off_page, off_count;
+  size_t off_counters, off_keys, off_key, off_page, off_count;
 };
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan);
 cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s);
@@ -61,17 +63,18 @@ struct DecodeArgs {
   const int32_t *selected;  // NULL: dense (every page)
   void *out;
   void *ws;
-  float *part_o;   // [B * H_kv, n_splits_max, G, D_v]
-  float *part_ml;  // [B * H_kv, n_splits_max, G, 2]
+  float *part_o;       // [B * H_kv, n_items_max, G, D_v] per-item partial O (unnormalised)
+  float *part_ml;      // [B * H_kv, n_items_max, G, 2] per-item (m, l)
+  uint32_t *tickets;   // [B * H_kv] merge tickets (zero between calls)
   int B, H_q, H_kv, D, D_v, ps, nb, max_pages;
-  int b_max;       // entries per selected row (sparse) or max_pages (dense)
-  int split;       // entries (pages) per CTA
-  int n_splits_max;
+  int b_max;           // entries per selected row (sparse)
+  int sw;              // list entries per item
+  int n_items_max;     // items per unit
   float scale;
 };
 struct DecodePlan {
-  int split, n_splits_max;
-  size_t ws_bytes, off_o, off_ml;
+  int sw, n_items_max;
+  size_t ws_bytes, off_o, off_ml, off_tickets;
 };
 bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan);
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);

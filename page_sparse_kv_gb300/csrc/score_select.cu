@@ -10,20 +10,24 @@
 // sink and recent page always kept and counted inside b; EntmaxKV "Top-k": the budget
 // includes the always-attended tail page; ties to the lower logical page index).
 //
-// Layout of the work: one CTA (8 warps) per (KV head, chunk of `chunk` pages, sequence).
-// A page's summary for one KV head is 2 * D contiguous elements; LPP = D * sizeof(T) / 16
-// lanes read its kmin and kmax rows with one 16-byte load each, so a warp scores 32 / LPP
-// pages per step with fully used 32-byte sectors. Partial sums are reduced across the LPP
-// lanes by a transposing butterfly (each step halves the values a lane carries), then the
-// group max is taken across the lanes that ended up holding different query heads.
-//
-// Each CTA keeps its chunk's scores as 32-bit order keys in shared memory, selects the
-// chunk-local top-k (k = b - 2 free slots) with an MSB-first 8-bit radix select, and writes
-// the winners (ascending page order) to the workspace. The last CTA of a (sequence, KV head)
-// to finish (an atomic ticket, no waiting) merges all chunk winners with a second radix
-// select and writes the final ascending list: sink, winners, tail, then -1 padding.
-// Top-k of the union of chunk top-k's is the global top-k because every key is unique
-// once ties are ordered by page index.
+// Two kernels per call:
+//   page_score_kernel (K1) streams the summaries: one CTA per (chunk of pages, sequence,
+//   group of up to 8 KV heads); warp w scores KV head w % 8 of the group, so a page's
+//   summaries for all heads (one 4 KB run at D = 128 bf16) are read together. A (page, head)
+//   summary row is read by LPP = D * sizeof(T) / 16 lanes with one 16-byte load each, four
+//   page steps in flight per lane. Partial sums are reduced across the LPP lanes by a
+//   transposing butterfly (each step halves the values a lane carries), then the group max is
+//   taken across the lanes that ended up holding different query heads. K1 writes one 32-bit
+//   order key per page (0 = forced sink / tail, or a flagged bad block) to the workspace.
+//   page_select_kernel (K2) selects: one CTA per (KV head, chunk of up to 16384 pages,
+//   sequence) loads the chunk's keys (L2-resident after K1) into shared memory and finds the
+//   top k = b - 2 with an MSB-first 8-bit radix select (warp-aggregated histogram atomics);
+//   ties go to the lower index through block-wide scans in index order. A unit that fits one
+//   chunk is finished by that CTA; otherwise each chunk writes its winners (ascending) and the
+//   last CTA of the (sequence, KV head) to finish (an atomic ticket, no waiting) merges them
+//   with a second radix select. Top-k of the union of chunk top-k's is the global top-k
+//   because keys are unique once ties are ordered by page index.
+// The output row is: sink, winners (ascending), tail, then -1 padding.
 #include <algorithm>
 
 #include "psk_common.cuh"
@@ -196,16 +200,122 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
 }
 
 // ------------------------------------------------------------------------------------
-// the kernel
+// K1: page scores, streaming
 // ------------------------------------------------------------------------------------
+// One CTA per (chunk of a.pchunk pages, sequence, group of up to 8 KV heads). Warp w scores
+// KV head w % HPC of the group for every (8 / HPC)-th page step, so the warps of a CTA read
+// all heads of a page (one 4 KB run at D = 128 bf16) close together in time. Writes the
+// 32-bit selection key of every page (0 for the forced sink / tail and for pages whose
+// block id is out of range) and, when asked, the fp32 score.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 2) score_select_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
   constexpr int U = 4;           // page steps in flight per lane
   static_assert(LPP >= 1 && LPP <= 32 && (LPP & (LPP - 1)) == 0, "row must be 16..512 bytes, power of 2");
 
+  const int i = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
+  const int p0 = blockIdx.x * a.pchunk;
+  if (p0 >= P) return;
+  const int p1 = min(P, p0 + a.pchunk);
+  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA
+  const int ng = kWarps / hpc;                         // warps per head
+  const int h = blockIdx.z * hpc + warp % hpc;
+  const int wg = warp / hpc;
+  const int unit = i * a.H_kv + h;
+
+  const int sub = lane % LPP;  // which 16-byte chunk of the summary row
+  const int grp = lane / LPP;  // which page of the warp step
+  float2 qp[G][EPC / 2], qn[G][EPC / 2];
+  {
+    const T *qrow = reinterpret_cast<const T *>(a.q) + ((size_t)i * a.H_q + (size_t)h * G) * D + sub * EPC;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float2 f[EPC / 2];
+      Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(qrow + (size_t)g * D), f);
+#pragma unroll
+      for (int e = 0; e < EPC / 2; ++e) {
+        qp[g][e] = make_float2(fmaxf(f[e].x, 0.f), fmaxf(f[e].y, 0.f));
+        qn[g][e] = make_float2(fminf(f[e].x, 0.f), fminf(f[e].y, 0.f));
+      }
+    }
+  }
+  const T *sumbase = reinterpret_cast<const T *>(a.summaries);
+  const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
+  uint32_t *krow = a.keys + (size_t)unit * a.max_pages;
+  float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
+  const int stride = ng * PPW;
+
+  for (int base = p0 + wg * PPW; base < p1; base += stride * U) {
+    uint4 lo[U], hi[U];
+    bool okb[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int p = base + u * stride + grp;
+      okb[u] = false;
+      lo[u] = make_uint4(0, 0, 0, 0);
+      hi[u] = lo[u];
+      if (p < p1) {
+        const int blk = __ldg(bt + p);
+        if (blk >= 0 && blk < a.nb) {
+          const T *sp = sumbase + ((size_t)blk * a.H_kv + h) * 2 * D + sub * EPC;
+          lo[u] = __ldg(reinterpret_cast<const uint4 *>(sp));
+          hi[u] = __ldg(reinterpret_cast<const uint4 *>(sp + D));
+          okb[u] = true;
+        } else if (sub == 0) {
+          set_status(a.ws, PSK_DEV_BAD_BLOCK);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int p = base + u * stride + grp;
+      if (base + u * stride >= p1) break;  // warp-uniform
+      float2 kl[EPC / 2], kh[EPC / 2];
+      Elem<T>::to_f2(lo[u], kl);
+      Elem<T>::to_f2(hi[u], kh);
+      float v[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e) {
+          acc = ffma2(qp[g][e], kh[e], acc);
+          acc = ffma2(qn[g][e], kl[e], acc);
+        }
+        v[g] = acc.x + acc.y;
+      }
+      const float sc = group_score<G, LPP>(v, lane) * a.scale;
+      if (sub == 0 && p < p1) {
+        const bool forced = (p == 0) || (p == P - 1);
+        krow[p] = (okb[u] && !forced) ? score_key(sc) : 0u;
+        if (srow) srow[p] = sc;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// K2: top-b selection
+// ------------------------------------------------------------------------------------
+// One CTA per (KV head, chunk of a.chunk pages, sequence). The chunk's keys come from the
+// workspace (L2-resident right after K1). A unit that fits one chunk is finished by its only
+// CTA; otherwise every chunk writes its local winners and the last CTA to finish merges.
+__device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, int b_max) {
+  const int tid = threadIdx.x;
+  if (tid == 0) sel_row[0] = 0;
+  // fewer winners than free slots happens only after a flagged bad block: pad the gap
+  for (int x = 1 + wrote + tid; x < count - 1; x += kThreads) sel_row[x] = -1;
+  if (tid == 0 && P > 1) sel_row[count - 1] = P - 1;
+  for (int x = count + tid; x < b_max; x += kThreads) sel_row[x] = -1;
+}
+
+__global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int hist[256];
   __shared__ int sh[kWarps + 4];
@@ -213,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_select_kernel(ScoreArgs a) 
 
   const int h = blockIdx.x, c = blockIdx.y, i = blockIdx.z;
   const int unit = i * a.H_kv + h;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
   int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
@@ -233,105 +343,51 @@ __global__ void __launch_bounds__(kThreads, 2) score_select_kernel(ScoreArgs a) 
     }
     return;
   }
+  const int count = min(budget, P);
+  if (count >= P) {  // every page is kept
+    if (c == 0)
+      for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = x < P ? x : -1;
+    return;
+  }
   const int nch = (P + a.chunk - 1) / a.chunk;
   if (c >= nch) return;
-  const int count = min(budget, P);
-  const int n_forced = P == 1 ? 1 : 2;
-  const int k_free = count - n_forced;
-  const bool keep_all = count >= P;
+  const int k_free = count - 2;  // count < P implies P >= 2 and count >= 2
 
   uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);
   const int p0 = c * a.chunk;
   const int p1 = min(P, p0 + a.chunk);
-
-  // ---- scores -------------------------------------------------------------------------
-  {
-    const int sub = lane % LPP;  // which 16-byte chunk of the row
-    const int grp = lane / LPP;  // which page of the warp step
-    float2 qp[G][EPC / 2], qn[G][EPC / 2];
-    const T *qrow = reinterpret_cast<const T *>(a.q) + ((size_t)i * a.H_q + (size_t)h * G) * D + sub * EPC;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float2 f[EPC / 2];
-      Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(qrow + (size_t)g * D), f);
-#pragma unroll
-      for (int e = 0; e < EPC / 2; ++e) {
-        qp[g][e] = make_float2(fmaxf(f[e].x, 0.f), fmaxf(f[e].y, 0.f));
-        qn[g][e] = make_float2(fminf(f[e].x, 0.f), fminf(f[e].y, 0.f));
-      }
-    }
-    const T *sumbase = reinterpret_cast<const T *>(a.summaries);
-    const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
-    float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
-
-    for (int base = p0 + warp * PPW; base < p1; base += kWarps * PPW * U) {
-      uint4 lo[U], hi[U];
-      bool okb[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int p = base + u * kWarps * PPW + grp;
-        okb[u] = false;
-        lo[u] = make_uint4(0, 0, 0, 0);
-        hi[u] = lo[u];
-        if (p < p1) {
-          const int blk = bt[p];
-          if (blk >= 0 && blk < a.nb) {
-            const T *s = sumbase + ((size_t)blk * a.H_kv + h) * 2 * D + sub * EPC;
-            lo[u] = __ldg(reinterpret_cast<const uint4 *>(s));
-            hi[u] = __ldg(reinterpret_cast<const uint4 *>(s + D));
-            okb[u] = true;
-          } else if (sub == 0) {
-            set_status(a.ws, PSK_DEV_BAD_BLOCK);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int p = base + u * kWarps * PPW + grp;
-        if (base + u * kWarps * PPW >= p1) break;  // warp-uniform
-        float2 kl[EPC / 2], kh[EPC / 2];
-        Elem<T>::to_f2(lo[u], kl);
-        Elem<T>::to_f2(hi[u], kh);
-        float v[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < EPC / 2; ++e) {
-            acc = ffma2(qp[g][e], kh[e], acc);
-            acc = ffma2(qn[g][e], kl[e], acc);
-          }
-          v[g] = acc.x + acc.y;
-        }
-        const float s = group_score<G, LPP>(v, lane) * a.scale;
-        if (sub == 0 && p < p1) {
-          const bool forced = (p == 0) || (p == P - 1);
-          keys[p - p0] = (okb[u] && !forced) ? score_key(s) : 0u;
-          if (srow) srow[p] = s;
-        }
-      }
-    }
+  const int n = p1 - p0;
+  const uint32_t *krow = a.keys + (size_t)unit * a.max_pages + p0;
+  int valid = 0;
+  for (int x = tid; x < n; x += kThreads) {
+    const uint32_t k = __ldcg(krow + x);
+    keys[x] = k;
+    valid += k != 0u;
   }
-  __syncthreads();
-
-  // ---- chunk-local top-k ----------------------------------------------------------------
-  const int slot = unit * a.n_chunks_max + c;
-  if (!keep_all && k_free > 0) {
-    const int n = p1 - p0;
-    int valid = 0;
-    for (int x = tid; x < n; x += kThreads) valid += keys[x] != 0u;
-    int total_valid;
-    block_exclusive_scan(valid, sh, &total_valid);
+  int total_valid;
+  block_exclusive_scan(valid, sh, &total_valid);  // also orders the smem writes above
+  int wrote = 0;
+  if (k_free > 0) {
     uint32_t thr = 0;
     int need_eq = 0;
     const bool take_all = total_valid <= k_free;
     if (!take_all) radix_select(keys, n, k_free, hist, sh, &thr, &need_eq);
+    if (nch == 1) {
+      wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + 1, sh);
+      write_row_ends(sel_row, P, count, wrote, a.b_max);
+      return;
+    }
+    const int slot = unit * a.n_chunks_max + c;
     uint32_t *ck = a.cand_key + (size_t)slot * a.k_cap;
     int32_t *cp = a.cand_page + (size_t)slot * a.k_cap;
-    const int wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, ck, cp, sh);
+    wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, ck, cp, sh);
     if (tid == 0) a.cand_count[slot] = wrote;
-  } else if (tid == 0) {
-    a.cand_count[slot] = 0;
+  } else {
+    if (nch == 1) {
+      write_row_ends(sel_row, P, count, 0, a.b_max);
+      return;
+    }
+    if (tid == 0) a.cand_count[unit * a.n_chunks_max + c] = 0;
   }
 
   // ---- last CTA of the unit merges -------------------------------------------------------
@@ -346,72 +402,75 @@ __global__ void __launch_bounds__(kThreads, 2) score_select_kernel(ScoreArgs a) 
   __threadfence();
   if (tid == 0) a.counters[unit] = 0u;
 
-  if (keep_all) {
-    for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = x < P ? x : -1;
-    return;
-  }
-  // gather chunk winners (ascending pages, chunk after chunk)
   uint32_t *mkey = reinterpret_cast<uint32_t *>(smem_raw);
   int32_t *mpage = reinterpret_cast<int32_t *>(smem_raw + sizeof(uint32_t) * kMergeCap);
   int n_c = 0;
-  if (k_free > 0) {
-    for (int cc = 0; cc < nch; ++cc) {
-      const int sl = unit * a.n_chunks_max + cc;
-      const int cnt = __ldcg(a.cand_count + sl);
-      const uint32_t *ck = a.cand_key + (size_t)sl * a.k_cap;
-      const int32_t *cp = a.cand_page + (size_t)sl * a.k_cap;
-      for (int x = tid; x < cnt; x += kThreads) {
-        mkey[n_c + x] = __ldcg(ck + x);
-        mpage[n_c + x] = __ldcg(cp + x);
-      }
-      n_c += cnt;
+  for (int cc = 0; cc < nch; ++cc) {
+    const int sl = unit * a.n_chunks_max + cc;
+    const int cnt = __ldcg(a.cand_count + sl);
+    const uint32_t *ck = a.cand_key + (size_t)sl * a.k_cap;
+    const int32_t *cp = a.cand_page + (size_t)sl * a.k_cap;
+    for (int x = tid; x < cnt; x += kThreads) {
+      mkey[n_c + x] = __ldcg(ck + x);
+      mpage[n_c + x] = __ldcg(cp + x);
     }
+    n_c += cnt;
   }
   __syncthreads();
-  // output row: sink, winners, tail, -1 padding
-  if (tid == 0) sel_row[0] = 0;
+  wrote = 0;
   if (k_free > 0) {
     uint32_t thr = 0;
     int need_eq = 0;
     const bool take_all = n_c <= k_free;
     if (!take_all) radix_select(mkey, n_c, k_free, hist, sh, &thr, &need_eq);
-    const int wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + 1, sh);
-    // fewer winners than free slots only after a flagged bad block: pad the gap
-    for (int x = 1 + wrote + tid; x < count - 1; x += kThreads) sel_row[x] = -1;
+    wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + 1, sh);
   }
-  if (tid == 0 && P > 1) sel_row[count - 1] = P - 1;
-  for (int x = count + tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
+  write_row_ends(sel_row, P, count, wrote, a.b_max);
 }
 
 template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
-  const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
-  auto kfn = score_select_kernel<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
+  dim3 g1((a.max_pages + a.pchunk - 1) / a.pchunk, a.B, a.H_kv / hpc);
+  page_score_kernel<T, D, G><<<g1, kThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.H_kv, a.n_chunks_max, a.B);
-  kfn<<<grid, kThreads, smem, s>>>(a);
+  const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
+  e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 g2(a.H_kv, a.n_chunks_max, a.B);
+  page_select_kernel<<<g2, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
+  if (L.num_kv_heads > kWarps && L.num_kv_heads % kWarps != 0) return false;
+  if (L.num_kv_heads < kWarps && kWarps % L.num_kv_heads != 0) return false;
   const int kfree_max = std::max(1, b_max - 2);
-  int chunk = 512;
+  int chunk = 4096;
   while (true) {
     const int nch = (L.max_pages + chunk - 1) / chunk;
     const int kcap = std::min(kfree_max, chunk);
-    if ((long long)nch * kcap <= kMergeCap) break;
+    if (nch == 1 || (long long)nch * kcap <= kMergeCap) break;
     chunk *= 2;
     if (chunk > 16384) return false;
   }
   plan->chunk = chunk;
   plan->n_chunks_max = (L.max_pages + chunk - 1) / chunk;
   plan->k_cap = std::min(kfree_max, chunk);
+  // pages per streaming CTA: fill the GPU a few times over
+  const long long head_groups = L.num_kv_heads > kWarps ? L.num_kv_heads / kWarps : 1;
+  int pchunk = 64;
+  while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152 * 2)
+    pchunk /= 2;
+  plan->pchunk = pchunk;
   const size_t units = (size_t)L.batch * L.num_kv_heads;
   plan->off_counters = ws_score_tickets_offset();
   size_t off = ws_scratch_offset(units);
+  plan->off_keys = off;
+  off = align_up(off + units * (size_t)L.max_pages * 4, 256);
   plan->off_key = off;
   off = align_up(off + units * plan->n_chunks_max * plan->k_cap * 4, 256);
   plan->off_page = off;
