@@ -80,6 +80,7 @@ enum psk_status {
 #define PSK_DEV_BAD_SELECTED 0x4u /* selected id outside [0, P) or list not ascending       */
 #define PSK_DEV_BAD_BUDGET 0x8u   /* budget < 2 with P > 1, or budget > b_max               */
 #define PSK_DEV_BAD_APPEND 0x10u  /* append position outside the block-table row, or n < 0  */
+#define PSK_DEV_TIMEOUT 0x20u     /* a bounded wait for an asynchronous copy gave up         */
 
 /*
  * Geometry of one layer's paged cache and of the decode batch.

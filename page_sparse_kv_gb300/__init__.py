@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libpsk.so")
 
 PSK_F32, PSK_BF16 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda"}
-DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND = 0x1, 0x2, 0x4, 0x8, 0x10
+DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 
 EXPORTS = [
     "psk_kv_append_and_summarize", "psk_page_score_select", "psk_sparse_paged_decode",

@@ -170,6 +170,7 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.max_pages = L.max_pages;
   a.b_max = b_max;
   a.pchunk = plan.pchunk;
+  a.stage_pages = plan.stage_pages;
   a.chunk = plan.chunk;
   a.n_chunks_max = plan.n_chunks_max;
   a.k_cap = plan.k_cap;

@@ -40,13 +40,14 @@ struct ScoreArgs {
   int32_t *cand_count;    // [B * H_kv, n_chunks_max]
   int B, H_q, H_kv, D, ps, nb, max_pages, b_max;
   int pchunk;             // pages per streaming score CTA
+  int stage_pages;        // pages per shared-memory stage of the score kernel
   int chunk;              // pages per selection CTA
   int n_chunks_max;
   int k_cap;              // candidates kept per chunk = min(b_max - 2, chunk) (>= 1)
   float scale;
 };
 struct ScorePlan {
-  int pchunk, chunk, n_chunks_max, k_cap;
+  int pchunk, stage_pages, chunk, n_chunks_max, k_cap;
   size_t ws_bytes;
   size_t off_counters, off_keys, off_key, off_page, off_count;
 };

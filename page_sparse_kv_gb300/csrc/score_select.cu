@@ -202,18 +202,28 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
 // ------------------------------------------------------------------------------------
 // K1: page scores, streaming
 // ------------------------------------------------------------------------------------
-// One CTA per (chunk of a.pchunk pages, sequence, group of up to 8 KV heads). Warp w scores
-// KV head w % HPC of the group for every (8 / HPC)-th page step, so the warps of a CTA read
-// all heads of a page (one 4 KB run at D = 128 bf16) close together in time. Writes the
-// 32-bit selection key of every page (0 for the forced sink / tail and for pages whose
-// block id is out of range) and, when asked, the fp32 score.
+// One CTA per (chunk of a.pchunk pages, sequence, group of up to 8 KV heads). The summaries of
+// a page for the CTA's heads are one contiguous run (H * 2 * D elements; 4 KB at H = 8,
+// D = 128 bf16), so warp 0 fetches each page with one bulk copy (TMA engine) into a ring of
+// kStages shared-memory stages of a.stage_pages pages, completion tracked by one mbarrier per
+// stage (bounded waits). All warps then score from shared memory: warp w takes KV head w % HPC
+// of the group and every (8 / HPC)-th page step. Writes one 32-bit order key per page (0 for
+// the forced sink / tail and for pages whose block id is out of range) and, when asked, the
+// fp32 score.
+constexpr int kStages = 3;
+constexpr int kStageBytes = 32768;
+constexpr int kMaxStagePages = 32;
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
-  constexpr int U = 4;           // page steps in flight per lane
+  constexpr int ES = Elem<T>::kBytes;
   static_assert(LPP >= 1 && LPP <= 32 && (LPP & (LPP - 1)) == 0, "row must be 16..512 bytes, power of 2");
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ int okflag[kStages][kMaxStagePages];
 
   const int i = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -225,9 +235,50 @@ __global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
   const int p1 = min(P, p0 + a.pchunk);
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA
   const int ng = kWarps / hpc;                         // warps per head
-  const int h = blockIdx.z * hpc + warp % hpc;
+  const int h0 = blockIdx.z * hpc;
+  const int hh = warp % hpc;
+  const int h = h0 + hh;
   const int wg = warp / hpc;
   const int unit = i * a.H_kv + h;
+  const int group_bytes = hpc * 2 * D * ES;            // one page's summaries for the CTA's heads
+  const int sp = a.stage_pages;
+  const int n_stages = (p1 - p0 + sp - 1) / sp;
+  const T *sumbase = reinterpret_cast<const T *>(a.summaries);
+  const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) mbar_init(smem_u32(&bars[k]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // warp 0: fetch the pages of stage `st` (chunk-local stage index) into ring slot st % kStages
+  auto produce = [&](int st) {
+    const int slot = st % kStages;
+    const int pb = p0 + st * sp;
+    bool ok = false;
+    int blk = -1;
+    if (lane < sp) {
+      const int p = pb + lane;
+      if (p < p1) {
+        blk = __ldg(bt + p);
+        ok = blk >= 0 && blk < a.nb;
+        if (!ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+      }
+      okflag[slot][lane] = ok;
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, ok);
+    const uint32_t bar = smem_u32(&bars[slot]);
+    __syncwarp();  // the flags above are ordered before lane 0's release-arrive
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(mask) * group_bytes);
+    __syncwarp();
+    if (ok)
+      bulk_g2s(smem_u32(smem_raw + (size_t)slot * kStageBytes + (size_t)lane * group_bytes),
+               sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar);
+  };
+
+  if (warp == 0)
+    for (int st = 0; st < kStages && st < n_stages; ++st) produce(st);
 
   const int sub = lane % LPP;  // which 16-byte chunk of the summary row
   const int grp = lane / LPP;  // which page of the warp step
@@ -245,40 +296,27 @@ __global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
       }
     }
   }
-  const T *sumbase = reinterpret_cast<const T *>(a.summaries);
-  const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
   uint32_t *krow = a.keys + (size_t)unit * a.max_pages;
   float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
-  const int stride = ng * PPW;
 
-  for (int base = p0 + wg * PPW; base < p1; base += stride * U) {
-    uint4 lo[U], hi[U];
-    bool okb[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int p = base + u * stride + grp;
-      okb[u] = false;
-      lo[u] = make_uint4(0, 0, 0, 0);
-      hi[u] = lo[u];
-      if (p < p1) {
-        const int blk = __ldg(bt + p);
-        if (blk >= 0 && blk < a.nb) {
-          const T *sp = sumbase + ((size_t)blk * a.H_kv + h) * 2 * D + sub * EPC;
-          lo[u] = __ldg(reinterpret_cast<const uint4 *>(sp));
-          hi[u] = __ldg(reinterpret_cast<const uint4 *>(sp + D));
-          okb[u] = true;
-        } else if (sub == 0) {
-          set_status(a.ws, PSK_DEV_BAD_BLOCK);
-        }
+  for (int st = 0; st < n_stages; ++st) {
+    const int slot = st % kStages;
+    mbar_wait(smem_u32(&bars[slot]), (st / kStages) & 1, a.ws);
+    const unsigned char *stage = smem_raw + (size_t)slot * kStageBytes;
+    const int pb = p0 + st * sp;
+    const int np = min(sp, p1 - pb);
+    for (int j0 = wg * PPW; j0 < np; j0 += ng * PPW) {  // warp-uniform bound
+      const int j = j0 + grp;
+      const bool live = j < np && okflag[slot][j < sp ? j : 0];
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (live) {
+        const unsigned char *row = stage + (size_t)j * group_bytes + (size_t)hh * 2 * D * ES + sub * 16;
+        lo = *reinterpret_cast<const uint4 *>(row);
+        hi = *reinterpret_cast<const uint4 *>(row + D * ES);
       }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int p = base + u * stride + grp;
-      if (base + u * stride >= p1) break;  // warp-uniform
       float2 kl[EPC / 2], kh[EPC / 2];
-      Elem<T>::to_f2(lo[u], kl);
-      Elem<T>::to_f2(hi[u], kh);
+      Elem<T>::to_f2(lo, kl);
+      Elem<T>::to_f2(hi, kh);
       float v[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -291,11 +329,17 @@ __global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
         v[g] = acc.x + acc.y;
       }
       const float sc = group_score<G, LPP>(v, lane) * a.scale;
-      if (sub == 0 && p < p1) {
+      if (sub == 0 && j < np) {
+        const int p = pb + j;
         const bool forced = (p == 0) || (p == P - 1);
-        krow[p] = (okb[u] && !forced) ? score_key(sc) : 0u;
+        krow[p] = (live && !forced) ? score_key(sc) : 0u;
         if (srow) srow[p] = sc;
       }
+    }
+    __syncthreads();  // every warp is done with this slot
+    if (warp == 0 && st + kStages < n_stages) {
+      fence_proxy_async_smem();
+      produce(st + kStages);
     }
   }
 }
@@ -316,7 +360,7 @@ __device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, in
 }
 
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ int hist[256];
   __shared__ int sh[kWarps + 4];
   __shared__ int flag_last;
@@ -432,8 +476,11 @@ template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
   dim3 g1((a.max_pages + a.pchunk - 1) / a.pchunk, a.B, a.H_kv / hpc);
-  page_score_kernel<T, D, G><<<g1, kThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const int k1_smem = kStages * kStageBytes;
+  cudaError_t e = cudaFuncSetAttribute(page_score_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, k1_smem);
+  if (e != cudaSuccess) return e;
+  page_score_kernel<T, D, G><<<g1, kThreads, k1_smem, s>>>(a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
   e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -462,10 +509,17 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   plan->k_cap = std::min(kfree_max, chunk);
   // pages per streaming CTA: fill the GPU a few times over
   const long long head_groups = L.num_kv_heads > kWarps ? L.num_kv_heads / kWarps : 1;
-  int pchunk = 64;
+  int pchunk = 128;
   while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152 * 2)
     pchunk /= 2;
   plan->pchunk = pchunk;
+  {
+    const int hpc = L.num_kv_heads < kWarps ? L.num_kv_heads : kWarps;
+    const int es = L.dtype == PSK_F32 ? 4 : 2;
+    const int group_bytes = hpc * 2 * L.head_dim * es;
+    if (group_bytes > kStageBytes) return false;
+    plan->stage_pages = std::min(kMaxStagePages, kStageBytes / group_bytes);
+  }
   const size_t units = (size_t)L.batch * L.num_kv_heads;
   plan->off_counters = ws_score_tickets_offset();
   size_t off = ws_scratch_offset(units);
