@@ -46,15 +46,15 @@ struct DT {
   static constexpr int ROW = D * ES;               // bytes per row
   static constexpr int TILE = 16 * ROW;
   static constexpr int STAGE = 2 * TILE;           // K tile + V tile
-  static constexpr int LOADS = 16 * NC / 32;       // 16-byte chunks per lane per tile (each of K, V)
   static constexpr int NV = 4 * G;                 // partial logits per lane before reduce
   static constexpr int KEEP = NV >= 8 ? NV / 8 : 1;
   static constexpr size_t STAGES = (size_t)NW * NST * STAGE;
-  static constexpr size_t SMEM = STAGES                       // stages (reused by the merges)
+  static constexpr size_t SMEM = 128                           // alignment slack
+                                 + STAGES                      // stages (reused by the merges)
                                  + (size_t)NW * 16 * G * 8     // (p, p) pairs
-                                 + (size_t)NW * G * D * 4      // warp O for the CTA merge
                                  + (size_t)NW * G * 2 * 4      // warp m, l
-                                 + (size_t)kSwMax * 3 * 4;     // entry table
+                                 + (size_t)kSwMax * 2 * 4;     // entry table
+  static_assert(STAGES >= (size_t)NW * G * D * 4, "stage memory must hold the warps' O for the CTA merge");
   static_assert(NC % 8 == 0, "a row must be a multiple of 128 bytes");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
 };
@@ -162,15 +162,17 @@ __device__ void merge_unit(const DecodeArgs &a, int unit, float *wsm, float *red
 }
 
 template <typename T, int D, int G, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV) {
   using TR = DT<T, D, G, NW, NST>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char *stages = smem;
-  float2 *pp_all = reinterpret_cast<float2 *>(smem + TR::STAGES);
-  float *wO = reinterpret_cast<float *>(pp_all + NW * 16 * G);
-  float *wML = wO + NW * G * D;
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  unsigned char *stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
+  float2 *pp_all = reinterpret_cast<float2 *>(stages + TR::STAGES);
+  float *wML = reinterpret_cast<float *>(pp_all + NW * 16 * G);
   int *ent_blk = reinterpret_cast<int *>(wML + NW * G * 2);
   int *ent_valid = ent_blk + kSwMax;
+  float *wO = reinterpret_cast<float *>(stages);  // after the pipeline has drained
+  __shared__ __align__(8) uint64_t bars[NW][NST];
   __shared__ int flag_last;
 
   const int s = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
@@ -191,6 +193,10 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a) {
     if (e0 < a.b_max && row[e0] >= 0) n_ent = min(a.sw, a.b_max - e0);
   } else if (e0 < P) {
     n_ent = min(a.sw, P - e0);
+  }
+  if (lane == 0) {
+    for (int k = 0; k < NST; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
+    fence_mbar_init();
   }
   for (int x = tid; x < n_ent; x += NW * 32) {
     int p = e0 + x, blk = -1;
@@ -248,52 +254,42 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a) {
     const int ntiles = n_ent * stp;
     unsigned char *my_stages = stages + (size_t)warp * NST * TR::STAGE;
     float2 *pp = pp_all + warp * 16 * G;
-    const T *kc = reinterpret_cast<const T *>(a.k_cache);
-    const T *vc = reinterpret_cast<const T *>(a.v_cache);
-    const size_t head_off = (size_t)h * D;
-    const size_t tok_stride = (size_t)a.H_kv * D;
-
     auto tile_rows = [&](int it) -> int {
-      const int e = it / stp, sub = it - e * stp;
+      const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
       return min(16, ent_valid[e] - sub * 16);
     };
-    auto load_tile = [&](int it, int stage) {
-      if (it < ntiles) {
-        const int e = it / stp, sub = it - e * stp;
+    // lane 0 of the warp issues the K and V tile copies of its c-th tile into stage c % NST; a
+    // tile without rows still arrives (0 bytes) so every stage's phases stay in step.
+    auto issue = [&](int c) {
+      const int it = warp + c * NW;
+      if (it >= ntiles) return;
+      if (lane == 0) {
+        const int stg = c % NST;
+        const uint32_t bar = smem_u32(&bars[warp][stg]);
+        const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
         const int nv = min(16, ent_valid[e] - sub * 16);
         if (nv > 0) {
-          const size_t tok0 = (size_t)ent_blk[e] * a.ps + sub * 16;
-          const uint32_t sK = smem_u32(my_stages + (size_t)stage * TR::STAGE);
-          const uint32_t sV = sK + TR::TILE;
-#pragma unroll
-          for (int u = 0; u < TR::LOADS; ++u) {
-            const int q = lane + 32 * u;
-            const int r = q / TR::NC, col = q - r * TR::NC;
-            const bool ok = r < nv;
-            const size_t goff = (tok0 + (ok ? r : 0)) * tok_stride + head_off + (size_t)col * TR::EPC;
-            cp_async16(sK + r * TR::ROW + col * 16, kc + goff, ok);
-            cp_async16(sV + r * TR::ROW + col * 16, vc + goff, ok);
-          }
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(bar, 2u * TR::TILE);
+          const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
+          const int row = ent_blk[e] * a.ps + sub * 16;
+          tma_load_3d(sK, &tmK, 0, h, row, bar);
+          tma_load_3d(sK + TR::TILE, &tmV, 0, h, row, bar);
+        } else {
+          mbar_arrive_expect_tx(bar, 0u);
         }
       }
-      cp_async_commit();
     };
 
-    int next = warp;
 #pragma unroll
-    for (int st = 0; st < NST - 1; ++st) {
-      load_tile(next, st);
-      next += NW;
-    }
-    int stage = 0;
-    for (int cur = warp; cur < ntiles; cur += NW) {
-      load_tile(next, (stage + NST - 1) % NST);
-      next += NW;
-      cp_async_wait<NST - 1>();
-      __syncwarp();
+    for (int c = 0; c < NST - 1; ++c) issue(c);
+    for (int c = 0, cur = warp; cur < ntiles; ++c, cur += NW) {
+      issue(c + NST - 1);
+      const int stage = c % NST;
+      mbar_wait(smem_u32(&bars[warp][stage]), (c / NST) & 1, a.ws);
       const int nv = tile_rows(cur);
       if (nv > 0) {
-        const unsigned char *sK = my_stages + (size_t)stage * TR::STAGE;
+        const unsigned char *sK = my_stages + (size_t)stage * TR::STAGE;  // landed: waited above
         const unsigned char *sV = sK + TR::TILE;
         // ---- QK ----
         float v[TR::NV];
@@ -377,7 +373,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a) {
         }
         __syncwarp();
         // ---- PV ----
-        for (int tk = 0; tk < nv; ++tk) {
+        auto pv_row = [&](int tk) {
           float2 vf[TR::VPL / 2];
           const unsigned char *vr = sV + tk * TR::ROW + lane * TR::VPL * TR::ES;
           if constexpr (TR::VPL * TR::ES == 16) {
@@ -392,12 +388,17 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a) {
 #pragma unroll
             for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = ffma2(pg, vf[e], O[g][e]);
           }
+        };
+        if (nv == 16) {
+#pragma unroll
+          for (int tk = 0; tk < 16; ++tk) pv_row(tk);
+        } else {
+          for (int tk = 0; tk < nv; ++tk) pv_row(tk);
         }
       }
       __syncwarp();
-      stage = (stage + 1) % NST;
     }
-    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the stages; wO below reuses them
 
     // ---- merge the warps of the CTA into one partial ----------------------------------------
 #pragma unroll
@@ -456,14 +457,20 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a) {
 
 template <typename T, int D, int G>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
-  constexpr int NW = 4, NST = 3;
+  constexpr int NW = 4, NST = 2;
   using TR = DT<T, D, G, NW, NST>;
   static_assert(TR::STAGES >= (size_t)kMaxItems * G * 4, "stage memory must hold the merge weights");
   auto kfn = decode_split_kernel<T, D, G, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
   if (e != cudaSuccess) return e;
+  CUtensorMap tmK, tmV;
+  const long long rows = (long long)a.nb * a.ps;
+  const int dt = sizeof(T) == 4 ? PSK_F32 : PSK_BF16;
+  if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv, rows, 16) ||
+      !encode_cache_map(&tmV, a.v_cache, dt, D, a.H_kv, rows, 16))
+    return cudaErrorInvalidValue;
   dim3 grid(a.n_items_max, a.H_kv, a.B);
-  kfn<<<grid, NW * 32, TR::SMEM, s>>>(a);
+  kfn<<<grid, NW * 32, TR::SMEM, s>>>(a, tmK, tmV);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
 // Device helpers shared by the psk kernels (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -160,6 +161,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+
+// 3-D tiled tensor copy global -> shared (TMA), completing on `bar`. The innermost coordinate
+// is always 0 here, so it meets the 16-byte start rule for every element type.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Host: encode a 3-D tiled tensor map over a paged cache [rows, H, D] (elements of `dtype`) with
+// a box of `box_rows` rows x 1 head x D elements. Returns false on failure.
+bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int D, int H, long long rows, int box_rows);
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
