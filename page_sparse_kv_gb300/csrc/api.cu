@@ -30,7 +30,7 @@ int check_layout(const psk_layout *L) {
 }
 
 int check_gqa_compute(const psk_layout *L) {
-  if (L->latent) return PSK_ERR_UNSUPPORTED;
+  if (L->latent) return mla_supported(*L) ? PSK_OK : PSK_ERR_UNSUPPORTED;
   const int G = L->num_q_heads / L->num_kv_heads;
   if (!score_supported(L->dtype, L->head_dim, G)) return PSK_ERR_UNSUPPORTED;
   if (!decode_supported(L->dtype, L->head_dim, L->v_head_dim, G, L->page_size)) return PSK_ERR_UNSUPPORTED;
@@ -66,16 +66,20 @@ size_t psk_score_select_workspace_size(const psk_layout *layout, int32_t b_max) 
   return plan_score(*layout, b_max, &plan) ? plan.ws_bytes : 0;
 }
 
+static bool plan_any_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan) {
+  return L.latent ? plan_mla_decode(L, entries, plan) : plan_decode(L, entries, dense, plan);
+}
+
 size_t psk_sparse_decode_workspace_size(const psk_layout *layout, int32_t b_max) {
   if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
   DecodePlan plan;
-  return plan_decode(*layout, b_max, false, &plan) ? plan.ws_bytes : 0;
+  return plan_any_decode(*layout, b_max, false, &plan) ? plan.ws_bytes : 0;
 }
 
 size_t psk_dense_decode_workspace_size(const psk_layout *layout) {
   if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK) return 0;
   DecodePlan plan;
-  return plan_decode(*layout, layout->max_pages, true, &plan) ? plan.ws_bytes : 0;
+  return plan_any_decode(*layout, layout->max_pages, true, &plan) ? plan.ws_bytes : 0;
 }
 
 int psk_get_device_status(const void *workspace, uint32_t *flags, psk_stream_t stream) {
@@ -175,6 +179,9 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.n_chunks_max = plan.n_chunks_max;
   a.k_cap = plan.k_cap;
   a.scale = scale;
+  if (L.latent)
+    return cuda_status(launch_mla_score_select(a, reinterpret_cast<uint16_t *>(ws + plan.off_qsplit),
+                                               static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_score_select(a, L.dtype, static_cast<cudaStream_t>(stream)));
 }
 
@@ -185,13 +192,14 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
-  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PSK_ERR_INVALID_ARG;
+  if (!q || !k_cache || !block_table || !seq_lens || !out) return PSK_ERR_INVALID_ARG;
+  if (L.latent ? v_cache != nullptr : v_cache == nullptr) return PSK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PSK_ERR_INVALID_ARG;
   rc = check_gqa_compute(layout);
   if (rc != PSK_OK) return rc;
   const bool dense = selected == nullptr;
   DecodePlan plan;
-  if (!plan_decode(L, dense ? L.max_pages : b_max, dense, &plan)) return PSK_ERR_UNSUPPORTED;
+  if (!plan_any_decode(L, dense ? L.max_pages : b_max, dense, &plan)) return PSK_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.ws_bytes) return PSK_ERR_WORKSPACE;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   DecodeArgs a;
@@ -218,6 +226,7 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.sw = plan.sw;
   a.n_items_max = plan.n_items_max;
   a.scale = scale;
+  if (L.latent) return cuda_status(launch_mla_decode(a, static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_decode(a, L.dtype, static_cast<cudaStream_t>(stream)));
 }
 

@@ -1,0 +1,530 @@
+// The latent (MLA) form of the page score and the decode, on the 5th-generation tensor cores.
+//
+// 128 query heads share one latent KV head of 576 dims (the value is its first 512 dims), so
+// both the Quest-style page bound and the attention are dense tile products here (LOCKS
+// PKG-INFO, "How it works", MLA: the same page selection on the latent cache, max-unioned
+// over the query heads; EntmaxKV README, Top-k: the Quest-style bound).
+//
+// Score: with qn = min(q, 0) and qp = max(q, 0) (exact in bf16), a page's bound for query head
+// g is sum_d qn[g,d] * kmin[d] + qp[g,d] * kmax[d], i.e. the product of the page's summary row
+// [kmin | kmax] (1152 elements, its stored layout) with [qn | qp]. One CTA computes
+//   S^T[page, head] = Summ[128 pages x 1152] * Qs[128 heads x 1152]^T
+// with tcgen05.mma (bf16 inputs, fp32 accumulation in tensor memory): M = 128 pages are the
+// tensor-memory lanes and N = 128 heads the columns, so the max over the group is a loop over
+// one thread's columns. Operands are staged per 64-element K block by cp.async with the
+// 128-byte swizzle into a 3-stage ring; tcgen05.commit on a per-stage mbarrier frees a stage.
+//
+// Decode: one CTA per (split of the page list, half of the value dims, sequence). Q (128 x 576)
+// stays in shared memory (TMA, 128-byte swizzle); K tiles of 32 tokens x 576 stream through a
+// double buffer (TMA). Per tile: S = Q K^T (M = 128 heads, N = 32 tokens) into tensor memory;
+// each thread owns one head's row: online softmax in fp32 (log2 domain), P written as bf16 to
+// shared memory (64-byte swizzle); O += P V (N = 256 value dims, V read MN-major straight out
+// of the same K tile) accumulates in tensor memory. O needs 256 of the 512 tensor-memory
+// columns per half of the value dims, hence the split of D_v across two CTAs (each recomputes
+// S). Splits are merged by log-sum-exp by the last CTA of each (sequence, half).
+#include <algorithm>
+
+#include "psk_common.cuh"
+#include "psk_internal.h"
+
+namespace psk {
+namespace {
+
+constexpr int kD = 576, kDv = 512, kHeads = 128;
+constexpr int kKB = kD / 64;  // 64-element K blocks of a latent row
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------------------------
+// tcgen05 helpers
+// ------------------------------------------------------------------------------------
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets, layout
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle), descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(layout & 7) << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K-major or
+// MN-major, N and M.
+__device__ __forceinline__ uint32_t umma_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(slot), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%"
+      "22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%"
+      "21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+  return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// ------------------------------------------------------------------------------------
+// score
+// ------------------------------------------------------------------------------------
+// q [B, 128, 576] -> [B, 128, 1152] = [min(q, 0) | max(q, 0)] (bit operations on bf16: a
+// negative value (sign set, -0.0 included) goes to the first half, the rest to the second).
+__global__ void mla_qsplit_kernel(const uint16_t *q, uint16_t *qs, int rows) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * (kD / 8)) return;
+  const int row = idx / (kD / 8), c = idx - row * (kD / 8);
+  const uint4 w = *reinterpret_cast<const uint4 *>(q + (size_t)row * kD + c * 8);
+  auto neg_mask = [](uint32_t x) { return ((x & 0x80008000u) >> 15) * 0xFFFFu; };
+  const uint4 m = make_uint4(neg_mask(w.x), neg_mask(w.y), neg_mask(w.z), neg_mask(w.w));
+  *reinterpret_cast<uint4 *>(qs + (size_t)row * 2 * kD + c * 8) = make_uint4(w.x & m.x, w.y & m.y, w.z & m.z, w.w & m.w);
+  *reinterpret_cast<uint4 *>(qs + (size_t)row * 2 * kD + kD + c * 8) =
+      make_uint4(w.x & ~m.x, w.y & ~m.y, w.z & ~m.z, w.w & ~m.w);
+}
+
+constexpr int kScStages = 3;
+constexpr int kScStage = 32768;  // 16 KB of page rows + 16 KB of head rows (one 64-element K block each)
+constexpr int kScSmem = 1024 + kScStages * kScStage;
+constexpr int kScKBlocks = 2 * kD / 64;  // 18
+
+__global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint16_t *qs) {
+  extern __shared__ unsigned char dyn[];
+  unsigned char *base = align1024(dyn);
+  __shared__ __align__(8) uint64_t bars[kScStages];
+  __shared__ uint32_t tslot;
+  const int i = blockIdx.y, tile = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
+  const int p0 = tile * 128;
+  if (p0 >= P) return;
+  const int r = tid;  // this thread's page row and head row
+  const int p = p0 + r;
+  bool ok = false;
+  int blk = 0;
+  if (p < P) {
+    blk = a.block_table[(size_t)i * a.max_pages + p];
+    ok = blk >= 0 && blk < a.nb;
+    if (!ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+  }
+  const uint16_t *srow = reinterpret_cast<const uint16_t *>(a.summaries) + (size_t)(ok ? blk : 0) * 2 * kD;
+  const uint16_t *qrow = qs + ((size_t)i * kHeads + r) * 2 * kD;
+
+  if (tid == 0) {
+    for (int k = 0; k < kScStages; ++k) mbar_init(smem_u32(&bars[k]), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tslot), 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+
+  auto fill = [&](int kb, int st) {
+    const uint32_t sa = smem_u32(base + st * kScStage), sb = sa + 16384;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t off = r * 128 + ((c ^ (r & 7)) * 16);
+      cp_async16(sa + off, srow + kb * 64 + c * 8, ok);
+      cp_async16(sb + off, qrow + kb * 64 + c * 8, true);
+    }
+  };
+  fill(0, 0);
+  cp_async_commit();
+  fill(1, 1);
+  cp_async_commit();
+  const uint32_t idesc = umma_idesc(128, 128, false);
+  for (int kb = 0; kb < kScKBlocks; ++kb) {
+    const int st = kb % kScStages;
+    cp_async_wait<1>();
+    fence_proxy_async_smem();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      const uint32_t sa = smem_u32(base + st * kScStage), sb = sa + 16384;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tmem, umma_desc(sa + ks * 32, 16, 1024, 2), umma_desc(sb + ks * 32, 16, 1024, 2), idesc,
+                  (kb | ks) != 0);
+      umma_commit(smem_u32(&bars[st]));
+    }
+    if (kb + 2 < kScKBlocks) {
+      const int nst = (kb + 2) % kScStages;
+      if (kb >= 1) mbar_wait(smem_u32(&bars[nst]), ((kb - 1) / kScStages) & 1, a.ws);  // MMAs of kb-1 done
+      fill(kb + 2, nst);
+    }
+    cp_async_commit();
+  }
+  mbar_wait(smem_u32(&bars[(kScKBlocks - 1) % kScStages]), ((kScKBlocks - 1) / kScStages) & 1, a.ws);
+  tc_fence_after();
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+  }
+  if (p < P) {
+    const float sc = mx * a.scale;
+    const bool forced = (p == 0) || (p == P - 1);
+    a.keys[(size_t)i * a.max_pages + p] = (ok && !forced) ? score_key(sc) : 0u;
+    if (a.scores_out) a.scores_out[(size_t)i * a.max_pages + p] = sc;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// ------------------------------------------------------------------------------------
+// decode
+// ------------------------------------------------------------------------------------
+constexpr int kTok = 32;                        // tokens per tile
+constexpr int kQBytes = kKB * kHeads * 128;     // 147456: Q as 9 swizzled [128 x 64] blocks
+constexpr int kKTile = kKB * kTok * 128;        // 36864: a K tile as 9 swizzled [32 x 64] blocks
+constexpr int kPBytes = kHeads * kTok * 2;      // 8192: P [128 x 32] bf16, 64-byte swizzle
+constexpr int kDecSmem = 1024 + kQBytes + 2 * kKTile + kPBytes;
+constexpr int kMlaMaxSw = 128;                  // pages per split
+constexpr int kMlaMaxItems = 128;               // splits per (sequence, half); their merge weights fit the K stages
+static_assert(kMlaMaxItems * kHeads * 4 <= 2 * kKTile, "merge weights must fit the K stages");
+constexpr uint32_t kOCol = 0, kSCol = 256;      // tensor-memory columns of O and S
+
+__global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
+                                                           const __grid_constant__ CUtensorMap tmK) {
+  extern __shared__ unsigned char dyn[];
+  unsigned char *base = align1024(dyn);
+  unsigned char *sQ = base;
+  unsigned char *sK = base + kQBytes;
+  unsigned char *sP = sK + 2 * kKTile;
+  __shared__ __align__(8) uint64_t qbar, kbar[2], sbar, obar;
+  __shared__ uint32_t tslot;
+  __shared__ int ent_blk[kMlaMaxSw], ent_valid[kMlaMaxSw];
+  __shared__ short tiles[2 * kMlaMaxSw];
+  __shared__ int n_tiles_sh;
+  __shared__ int flag_last;
+
+  const int s = blockIdx.x, vh = blockIdx.y, i = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int unit = i * 2 + vh;
+  const size_t pbase = (size_t)unit * a.n_items_max + s;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  const int e0 = s * a.sw;
+
+  int n_ent = 0;
+  if (seq_len < 1 || P > a.max_pages) {
+    if (s == 0 && vh == 0 && tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
+  } else if (a.selected) {
+    const int32_t *row = a.selected + (size_t)i * a.b_max;
+    if (e0 < a.b_max && row[e0] >= 0) n_ent = min(a.sw, a.b_max - e0);
+  } else if (e0 < P) {
+    n_ent = min(a.sw, P - e0);
+  }
+  for (int x = tid; x < n_ent; x += 128) {
+    int pg = e0 + x, blk = -1;
+    bool ok = true;
+    if (a.selected) {
+      const int32_t *row = a.selected + (size_t)i * a.b_max;
+      pg = row[e0 + x];
+      const int prev = (e0 + x > 0) ? row[e0 + x - 1] : -1;
+      if (pg >= 0 && (pg >= P || pg <= prev || (e0 + x > 0 && prev < 0))) {
+        if (vh == 0) set_status(a.ws, PSK_DEV_BAD_SELECTED);
+        ok = false;
+      }
+      if (pg < 0) ok = false;
+    }
+    if (ok) {
+      blk = a.block_table[(size_t)i * a.max_pages + pg];
+      if (blk < 0 || blk >= a.nb) {
+        if (vh == 0) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+        ok = false;
+      }
+    }
+    ent_blk[x] = blk;
+    ent_valid[x] = ok ? min(a.ps, seq_len - pg * a.ps) : 0;
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&qbar), 1);
+    mbar_init(smem_u32(&kbar[0]), 1);
+    mbar_init(smem_u32(&kbar[1]), 1);
+    mbar_init(smem_u32(&sbar), 1);
+    mbar_init(smem_u32(&obar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tslot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {  // the tile list: (entry, 32-token half) pairs with at least one live row
+    int n = 0;
+    for (int e = 0; e < n_ent; ++e)
+      for (int hh = 0; hh * kTok < ent_valid[e]; ++hh) tiles[n++] = (short)(e * 2 + hh);
+    n_tiles_sh = n;
+  }
+  __syncthreads();
+  const uint32_t tmem = tslot;
+  const int n_tiles = n_tiles_sh;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  float m_run = -INFINITY, l_run = 0.f;
+  const float qs = a.scale * kLog2e;
+
+  auto issue_tile = [&](int t) {  // thread 0 only
+    const int st = t & 1;
+    const int e = tiles[t] >> 1, hh = tiles[t] & 1;
+    const int row0 = ent_blk[e] * a.ps + hh * kTok;
+    const uint32_t bar = smem_u32(&kbar[st]);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, kKTile);
+    const uint32_t dst = smem_u32(sK + st * kKTile);
+#pragma unroll 1
+    for (int kb = 0; kb < kKB; ++kb) tma_load_2d(dst + kb * kTok * 128, &tmK, kb * 64, row0, bar);
+  };
+
+  if (n_tiles > 0) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(smem_u32(&qbar), kQBytes);
+#pragma unroll 1
+      for (int kb = 0; kb < kKB; ++kb) tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, kb * 64, i * kHeads, smem_u32(&qbar));
+      issue_tile(0);
+      if (n_tiles > 1) issue_tile(1);
+    }
+    mbar_wait(smem_u32(&qbar), 0, a.ws);
+    const uint32_t idesc_qk = umma_idesc(128, kTok, false);
+    const uint32_t idesc_pv = umma_idesc(128, 256, true);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int st = t & 1;
+      mbar_wait(smem_u32(&kbar[st]), (t >> 1) & 1, a.ws);
+      tc_fence_after();
+      if (tid == 0) {
+        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * kKTile);
+#pragma unroll 1
+        for (int kb = 0; kb < kKB; ++kb)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + kSCol, umma_desc(q0 + kb * kHeads * 128 + ks * 32, 16, 1024, 2),
+                      umma_desc(k0 + kb * kTok * 128 + ks * 32, 16, 1024, 2), idesc_qk, (kb | ks) != 0);
+        umma_commit(smem_u32(&sbar));
+      }
+      mbar_wait(smem_u32(&sbar), t & 1, a.ws);
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld32(tmem + lane_base + kSCol, sv);
+      const int e = tiles[t] >> 1, hh = tiles[t] & 1;
+      const int nv = min(kTok, ent_valid[e] - hh * kTok);
+      float x[32];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = j < nv ? __uint_as_float(sv[j]) * qs : -INFINITY;
+        mt = fmaxf(mt, x[j]);
+      }
+      if (t > 0) mbar_wait(smem_u32(&obar), (t - 1) & 1, a.ws);  // P.V of tile t-1 done: P and O free
+      tc_fence_after();
+      const float m_new = fmaxf(m_run, mt);
+      // rescale O when this head's running max moved; the tensor-memory loads and stores are
+      // warp-collective, so a warp rescales together (alpha = 1 on lanes whose max held)
+      const bool moved = t > 0 && m_new > m_run;
+      if (__any_sync(0xffffffffu, moved)) {
+        const float al = moved ? exp2f(m_run - m_new) : 1.f;
+        l_run *= al;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kOCol + c0, ov);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
+          tmem_st32(tmem + lane_base + kOCol + c0, ov);
+        }
+      }
+      m_run = m_new;
+      uint32_t pw[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float p0 = exp2f(x[2 * j] - m_run), p1 = exp2f(x[2 * j + 1] - m_run);
+        l_run += p0 + p1;
+        pw[j] = (uint32_t)f32_to_bf16_bits(p0) | ((uint32_t)f32_to_bf16_bits(p1) << 16);
+      }
+      // P row r = tid: 4 chunks of 16 bytes, 64-byte swizzle
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4 *>(sP + tid * 64 + ((c ^ ((tid >> 1) & 3)) * 16)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {
+        const uint32_t p0a = smem_u32(sP), v0 = smem_u32(sK + st * kKTile + vh * 4 * kTok * 128);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 512, 4), umma_desc(v0 + ks * 16 * 128, kTok * 128, 1024, 2),
+                    idesc_pv, (t | ks) != 0);
+        umma_commit(smem_u32(&obar));
+        if (t + 2 < n_tiles) {
+          mbar_wait(smem_u32(&obar), t & 1, a.ws);  // P.V has read this K tile
+          issue_tile(t + 2);
+        }
+      }
+    }
+    mbar_wait(smem_u32(&obar), (n_tiles - 1) & 1, a.ws);
+    tc_fence_after();
+    // partial O row (unnormalised) and (m, l) of head `tid`
+    float *po = a.part_o + (pbase * kHeads + tid) * 256;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      uint32_t ov[32];
+      tmem_ld32(tmem + lane_base + kOCol + c0, ov);
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4 *>(po + c0 + j) = make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
+                                                               __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+    }
+    a.part_ml[(pbase * kHeads + tid) * 2] = m_run;
+    a.part_ml[(pbase * kHeads + tid) * 2 + 1] = l_run;
+  } else {
+    a.part_ml[(pbase * kHeads + tid) * 2] = -INFINITY;
+    a.part_ml[(pbase * kHeads + tid) * 2 + 1] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+
+  // ---- the last CTA of (sequence, half) merges the splits ----------------------------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) flag_last = atomicAdd(a.tickets + unit, 1u) == (unsigned)(a.n_items_max - 1);
+  __syncthreads();
+  if (!flag_last) return;
+  __threadfence();
+  if (tid == 0) a.tickets[unit] = 0u;
+  const size_t it0 = (size_t)unit * a.n_items_max;
+  float *wsm = reinterpret_cast<float *>(sK);  // [n_items][128] merge weights (stages are free now)
+  float M = -INFINITY;
+  for (int k = 0; k < a.n_items_max; ++k) M = fmaxf(M, __ldcg(a.part_ml + ((it0 + k) * kHeads + tid) * 2));
+  float L = 0.f;
+  for (int k = 0; k < a.n_items_max; ++k) {
+    const float mk = __ldcg(a.part_ml + ((it0 + k) * kHeads + tid) * 2);
+    const float w = mk == -INFINITY ? 0.f : exp2f(mk - M);
+    if (w > 0.f) L = fmaf(w, __ldcg(a.part_ml + ((it0 + k) * kHeads + tid) * 2 + 1), L);
+    wsm[k * kHeads + tid] = w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint16_t *out = reinterpret_cast<uint16_t *>(a.out) + ((size_t)i * kHeads + tid) * kDv + vh * 256;
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    for (int k = 0; k < a.n_items_max; ++k) {
+      const float w = wsm[k * kHeads + tid];
+      if (w == 0.f) continue;
+      const float *pk = a.part_o + ((it0 + k) * kHeads + tid) * 256 + c * 32;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 o = __ldcg(reinterpret_cast<const float4 *>(pk + j));
+        acc[j] = fmaf(w, o.x, acc[j]);
+        acc[j + 1] = fmaf(w, o.y, acc[j + 1]);
+        acc[j + 2] = fmaf(w, o.z, acc[j + 2]);
+        acc[j + 3] = fmaf(w, o.w, acc[j + 3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+      uint4 w;
+      w.x = (uint32_t)f32_to_bf16_bits(acc[j] * inv) | ((uint32_t)f32_to_bf16_bits(acc[j + 1] * inv) << 16);
+      w.y = (uint32_t)f32_to_bf16_bits(acc[j + 2] * inv) | ((uint32_t)f32_to_bf16_bits(acc[j + 3] * inv) << 16);
+      w.z = (uint32_t)f32_to_bf16_bits(acc[j + 4] * inv) | ((uint32_t)f32_to_bf16_bits(acc[j + 5] * inv) << 16);
+      w.w = (uint32_t)f32_to_bf16_bits(acc[j + 6] * inv) | ((uint32_t)f32_to_bf16_bits(acc[j + 7] * inv) << 16);
+      *reinterpret_cast<uint4 *>(out + c * 32 + j) = w;
+    }
+  }
+}
+
+}  // namespace
+
+bool mla_supported(const psk_layout &L) {
+  return L.latent == 1 && L.dtype == PSK_BF16 && L.num_kv_heads == 1 && L.num_q_heads == kHeads && L.head_dim == kD &&
+         L.v_head_dim == kDv && (L.page_size == 32 || L.page_size == 64);
+}
+
+size_t mla_qsplit_bytes(const psk_layout &L) { return (size_t)L.batch * kHeads * 2 * kD * 2; }
+
+cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s) {
+  const int rows = a.B * kHeads;
+  const int n = rows * (kD / 8);
+  mla_qsplit_kernel<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<const uint16_t *>(a.q), qsplit, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(mla_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.max_pages + 127) / 128, a.B);
+  mla_score_kernel<<<grid, 128, kScSmem, s>>>(a, qsplit);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_page_select(a, s);
+}
+
+bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
+  const long long units = (long long)L.batch * 2;
+  int items = (int)std::max(1LL, (152 + units - 1) / units);
+  items = std::min(items, std::min(entries, kMlaMaxItems));
+  int sw = (entries + items - 1) / items;
+  sw = std::min(sw, kMlaMaxSw);
+  plan->sw = sw;
+  plan->n_items_max = (entries + sw - 1) / sw;
+  size_t off = ws_scratch_offset((size_t)units);
+  plan->off_o = off;
+  off = align_up(off + (size_t)units * plan->n_items_max * kHeads * 256 * 4, 256);
+  plan->off_ml = off;
+  off = align_up(off + (size_t)units * plan->n_items_max * kHeads * 2 * 4, 256);
+  plan->ws_bytes = off;
+  plan->off_tickets = ws_decode_tickets_offset((size_t)units);
+  return plan->n_items_max <= kMlaMaxItems;
+}
+
+cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
+  CUtensorMap tmQ, tmK;
+  if (!encode_matrix_map_sw128(&tmQ, a.q, kD, (long long)a.B * kHeads, 64, kHeads) ||
+      !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kTok))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_items_max, 2, a.B);
+  mla_decode_kernel<<<grid, 128, kDecSmem, s>>>(a, tmQ, tmK);
+  return cudaGetLastError();
+}
+
+}  // namespace psk

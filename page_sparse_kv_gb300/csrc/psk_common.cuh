@@ -174,6 +174,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 // Host: encode a 3-D tiled tensor map over a paged cache [rows, H, D] (elements of `dtype`) with
 // a box of `box_rows` rows x 1 head x D elements. Returns false on failure.
 bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int D, int H, long long rows, int box_rows);
+// Host: 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {box_cols, box_rows}
+// box and the 128-byte swizzle (box_cols * 2 must be 128).
+bool encode_matrix_map_sw128(CUtensorMap *map, const void *base, long long cols, long long rows, int box_cols,
+                             int box_rows);
+
+// 2-D tiled tensor copy global -> shared (TMA); x * 2 bytes must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 

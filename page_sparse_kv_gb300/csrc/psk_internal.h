@@ -49,9 +49,10 @@ struct ScoreArgs {
 struct ScorePlan {
   int pchunk, stage_pages, chunk, n_chunks_max, k_cap;
   size_t ws_bytes;
-  size_t off_counters, off_keys, off_key, off_page, off_count;
+  size_t off_counters, off_keys, off_key, off_page, off_count, off_qsplit;
 };
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan);
+cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s);
 cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s);
 bool score_supported(int dtype, int D, int G);
 
@@ -80,5 +81,12 @@ struct DecodePlan {
 bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan);
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);
 bool decode_supported(int dtype, int D, int D_v, int G, int ps);
+
+// latent (MLA) form on the tensor cores
+bool mla_supported(const psk_layout &L);
+size_t mla_qsplit_bytes(const psk_layout &L);
+cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s);
+bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan);
+cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
 
 }  // namespace psk

@@ -482,15 +482,19 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   page_score_kernel<T, D, G><<<g1, kThreads, k1_smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_page_select(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
   const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
-  e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 g2(a.H_kv, a.n_chunks_max, a.B);
   page_select_kernel<<<g2, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
-
-}  // namespace
 
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   if (L.num_kv_heads > kWarps && L.num_kv_heads % kWarps != 0) return false;
@@ -517,8 +521,8 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
     const int hpc = L.num_kv_heads < kWarps ? L.num_kv_heads : kWarps;
     const int es = L.dtype == PSK_F32 ? 4 : 2;
     const int group_bytes = hpc * 2 * L.head_dim * es;
-    if (group_bytes > kStageBytes) return false;
-    plan->stage_pages = std::min(kMaxStagePages, kStageBytes / group_bytes);
+    plan->stage_pages = group_bytes > kStageBytes ? 1 : std::min(kMaxStagePages, kStageBytes / group_bytes);
+    if (group_bytes > kStageBytes && !L.latent) return false;
   }
   const size_t units = (size_t)L.batch * L.num_kv_heads;
   plan->off_counters = ws_score_tickets_offset();
@@ -531,6 +535,8 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   off = align_up(off + units * plan->n_chunks_max * plan->k_cap * 4, 256);
   plan->off_count = off;
   off = align_up(off + units * plan->n_chunks_max * 4, 256);
+  plan->off_qsplit = off;
+  if (L.latent) off = align_up(off + mla_qsplit_bytes(L), 256);
   plan->ws_bytes = off;
   return true;
 }

@@ -108,7 +108,7 @@ def w_vals(w, i, n):
     return base if extra is None else np.concatenate([base, np.stack(extra)])[:n]
 
 
-@pytest.mark.parametrize("idx", [1, 3, 4])
+@pytest.mark.parametrize("idx", [1, 3, 4, 5])
 def test_reduced_workload_parity(idx):
     w = W.reduced(idx)
     cache = upload(w)
