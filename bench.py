@@ -194,16 +194,16 @@ def run_psk(args):
     # cache state is identical before and after a step)
     lens = w.seq_lens.astype(np.int64)
     k_last = np.stack([w.keys(i, int(lens[i]) - 1, int(lens[i]))[0] for i in range(B)])
-    v_last = np.stack([w.values(i, int(lens[i]) - 1, int(lens[i]))[0] for i in range(B)])
+    v_last = None if w.latent else np.stack([w.values(i, int(lens[i]) - 1, int(lens[i]))[0] for i in range(B)])
     q_host = w.queries()
     k_new = to_torch(k_last, w.dtype).to(dev)
-    v_new = to_torch(v_last, w.dtype).to(dev)
+    v_new = None if w.latent else to_torch(v_last, w.dtype).to(dev)
     q = to_torch(q_host, w.dtype).to(dev)
     start = torch.from_numpy((lens - 1).astype(np.int32)).to(dev)
     cu = torch.arange(B + 1, dtype=torch.int32, device=dev)
     bud = dev_budgets(w)
     sel = torch.empty(B, Hkv, w.b_max, dtype=torch.int32, device=dev)
-    out = torch.empty(B, Hq, D, dtype=cache.dtype, device=dev)
+    out = torch.empty(B, Hq, w.D_v, dtype=cache.dtype, device=dev)
     out_dense = torch.empty_like(out)
     ws = cache.ws
     setup_s = time.time() - t_setup
@@ -278,24 +278,28 @@ def run_psk(args):
     # ---- end to end: host buffers through the C ABI (pinned H2D of the step's inputs, D2H of out)
     qh = to_torch(q_host, w.dtype).pin_memory()
     kh = to_torch(k_last, w.dtype).pin_memory()
-    vh = to_torch(v_last, w.dtype).pin_memory()
+    vh = None if w.latent else to_torch(v_last, w.dtype).pin_memory()
     oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     Ke = max(3, K // 4)
     for _ in range(2):
-        q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True); v_new.copy_(vh, non_blocking=True)
+        q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True)
+        if vh is not None:
+            v_new.copy_(vh, non_blocking=True)
         append(); score(); decode(); oh.copy_(out, non_blocking=True)
     barrier()
     x0 = torch.cuda.Event(enable_timing=True)
     x1 = torch.cuda.Event(enable_timing=True)
     x0.record(stream)
     for _ in range(Ke):
-        q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True); v_new.copy_(vh, non_blocking=True)
+        q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True)
+        if vh is not None:
+            v_new.copy_(vh, non_blocking=True)
         append(); score(); decode()
         oh.copy_(out, non_blocking=True)
     x1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = x0.elapsed_time(x1) / Ke
-    h2d = (qh.numel() + kh.numel() + vh.numel()) * es
+    h2d = (qh.numel() + kh.numel() + (0 if vh is None else vh.numel())) * es
     d2h = oh.numel() * es
     assert psk.get_device_status(ws) == 0, "device status set during the timed region"
 
@@ -303,18 +307,19 @@ def run_psk(args):
     P = (lens + w.page_size - 1) // w.page_size
     summ_bytes = int(P.sum()) * Hkv * 2 * D * es
     q_bytes = B * Hq * D * es
-    out_bytes = B * Hq * D * es
+    out_bytes = B * Hq * w.D_v * es
+    kv_row = D if w.latent else D + w.D_v  # a latent row carries the value in its first D_v dims
     sel_np = sel.cpu().numpy()
     sel_tokens = 0
     for i in range(B):
         for h in range(Hkv):
             pages = sel_np[i, h][sel_np[i, h] >= 0]
             sel_tokens += int(np.minimum(w.page_size, lens[i] - pages * w.page_size).sum())
-    kv_bytes = sel_tokens * Hkv // Hkv * (D + w.D_v) * es
+    kv_bytes = sel_tokens * kv_row * es
     score_bytes = summ_bytes + q_bytes
     decode_bytes = kv_bytes + q_bytes + out_bytes
     step_bytes = summ_bytes + kv_bytes + q_bytes + out_bytes
-    dense_bytes = int(lens.sum()) * Hkv * (D + w.D_v) * es + q_bytes + out_bytes
+    dense_bytes = int(lens.sum()) * Hkv * kv_row * es + q_bytes + out_bytes
     peak, peak_kind = peaks()
     if t_score >= t_dec:
         dom, dom_bytes, dom_ms = "score_select_kernel", score_bytes, t_score
@@ -367,7 +372,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="psk", choices=["psk", "reference"])
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

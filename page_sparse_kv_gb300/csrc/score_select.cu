@@ -74,28 +74,61 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *sh, int *total) 
 
 // Radix select over keys[0..n) (key 0 = not a candidate): finds the k-th largest key T and
 // how many keys equal to T belong to the top k (the lowest-indexed ones). Requires
-// 1 <= k <= number of nonzero keys.
+// 1 <= k <= number of nonzero keys. hist: 8 warps x 256 private bins (8 KB).
+// The digits start at the highest bit in which the candidates' min and max keys differ (the
+// bits above are common to all of them), 8 bits per pass; each warp counts into its own
+// histogram with plain shared-memory atomics and a pass sums the 8 histograms per bin.
 __device__ void radix_select(const uint32_t *keys, int n, int k, int *hist, int *sh, uint32_t *T_out,
                              int *need_eq_out) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  uint32_t prefix = 0, mask = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // common high bits of the candidates
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int x = tid; x < n; x += kThreads) {
+    const uint32_t key = keys[x];
+    if (key != 0u) {
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  __shared__ uint32_t red_min[kWarps], red_max[kWarps];
+  if (lane == 0) {
+    red_min[warp] = kmin;
+    red_max[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = red_min[0];
+  kmax = red_max[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    kmin = min(kmin, red_min[w]);
+    kmax = max(kmax, red_max[w]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  const int top = diff ? 31 - __clz(diff) : 0;  // highest differing bit
+  int shift = top >= 7 ? top - 7 : 0;
+  uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
+  uint32_t mask = shift + 8 >= 32 ? 0u : (0xFFFFFFFFu << (shift + 8));
   int need = k;
+  int *myhist = hist + warp * 256;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;  // kThreads == 256 bins
+  for (;;) {
+    for (int b = tid; b < kWarps * 256; b += kThreads) hist[b] = 0;
     __syncthreads();
-    for (int base = 0; base < n; base += kThreads) {
-      const int x = base + tid;
-      const uint32_t key = x < n ? keys[x] : 0u;
-      const bool ok = key != 0u && (key & mask) == prefix;
-      const uint32_t d = ok ? ((key >> shift) & 255u) : 0xFFFFFFFFu;
-      const unsigned grp = __match_any_sync(0xffffffffu, d);
-      if (ok && (__ffs(grp) - 1) == lane) atomicAdd(&hist[d], __popc(grp));
+    for (int x = tid; x < n; x += kThreads) {
+      const uint32_t key = keys[x];
+      if (key != 0u && (key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
-    // suffix sums: thread t looks at bin 255 - t
+    // bin 255 - tid, summed over the warps' histograms; suffix sums by a block scan
     const int bin = 255 - tid;
-    const int hb = hist[bin];
+    int hb = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) hb += hist[w * 256 + bin];
     const int excl = block_exclusive_scan(hb, sh, nullptr);  // keys with digit > bin
     const int incl = excl + hb;                              // keys with digit >= bin
     if (incl >= need && excl < need) {
@@ -108,6 +141,9 @@ __device__ void radix_select(const uint32_t *keys, int n, int k, int *hist, int 
     prefix |= static_cast<uint32_t>(d) << shift;
     mask |= 255u << shift;
     __syncthreads();
+    if (shift == 0) break;
+    shift = shift >= 8 ? shift - 8 : 0;
+    // a digit that overlaps bits already fixed is harmless: they match the prefix
   }
   *T_out = prefix;
   *need_eq_out = need;
@@ -361,8 +397,8 @@ __device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, in
 
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ int hist[256];
-  __shared__ int sh[kWarps + 4];
+  __shared__ int hist[kWarps * 256];
+  __shared__ int sh[2 * kWarps + 4];
   __shared__ int flag_last;
 
   const int h = blockIdx.x, c = blockIdx.y, i = blockIdx.z;

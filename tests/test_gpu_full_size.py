@@ -176,3 +176,30 @@ def test_llama_layer_with_64_appends_full_size():
             check_output(from_torch(dense.float(), "f32")[0],
                          O.dense_attention(q_np[0], K, V, n, w.page_size, w.dtype, scale), w.dtype)
     assert psk.get_device_status(cache.ws) == 0
+
+
+def test_mla_full_size_sampled():
+    """16 sequences of 131072 tokens over one 576-dim latent head, 128 query heads, page 64,
+    5 % budget: tcgen05 score and decode; two sequences checked (one also dense)."""
+    w = W.config(5)
+    cache = upload(w)
+    q_np = w.queries()
+    sel, sc, out, dense = _run_batch(w, cache, q_np)
+    scale = 1.0 / math.sqrt(w.D)
+    summ = from_torch(cache.summaries, w.dtype)
+    for i in (3, 11):
+        n = int(w.seq_lens[i])
+        P = -(-n // w.page_size)
+        kmin, kmax = _oracle_summaries_chunked(w, i, n)
+        blocks = w.block_table[i, :P]
+        assert np.array_equal(summ[blocks, :, 0], kmin) and np.array_equal(summ[blocks, :, 1], kmax)
+        s_ref = O.quest_scores(q_np[i], kmin, kmax, w.dtype, scale)
+        tol = score_tolerance(q_np[i], kmin, kmax, w.dtype, scale)
+        assert np.all(np.abs(sc[i, :, :P] - s_ref) <= tol)
+        ok, near, got, ref = compare_selection(sel[i, 0], s_ref[0], int(w.budgets[i]))
+        assert ok, f"seq {i}: selection differs beyond near ties"
+        keys = w.keys(i)
+        vals = keys[..., :w.D_v]
+        check_output(out[i], O.attend_pages(q_np[i], keys, vals, n, w.page_size, [got], w.dtype, scale), w.dtype)
+        if i == 3:
+            check_output(dense[i], O.dense_attention(q_np[i], keys, vals, n, w.page_size, w.dtype, scale), w.dtype)
