@@ -25,6 +25,7 @@
 // write an empty partial first); the CTA holding the last ticket (no waiting) merges the
 // unit's partials by log-sum-exp with all its threads and writes the G output rows.
 #include <algorithm>
+#include <cstdlib>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
@@ -481,6 +482,10 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
   // 32 list entries per CTA; fewer while the grid would not fill the GPU (152 SMs x 2 CTAs) a
   // few times over, more when a unit would need over kMaxItems partials
   int sw = 32;
+  if (const char *env = std::getenv("PSK_DECODE_SPLIT")) {  // tuning override: entries per CTA
+    const int v = std::atoi(env);
+    if (v >= 1 && v <= kSwMax) sw = v;
+  }
   while (sw > 4 && units * ((entries + sw - 1) / sw) < 4LL * 152 * 2) sw /= 2;
   while (sw < kSwMax && (entries + sw - 1) / sw > kMaxItems) sw *= 2;
   (void)dense;

@@ -145,6 +145,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
 // Bounded wait for the phase with parity `parity`: gives up after kMbarSpinLimit polls (each
 // poll may suspend the thread for a short hardware-defined time), sets PSK_DEV_TIMEOUT and
 // returns false, so a lost copy can never hang the GPU.
