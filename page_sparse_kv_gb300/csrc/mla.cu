@@ -221,6 +221,7 @@ constexpr int kMlaMaxSw = 128;                  // pages per split
 constexpr int kMlaMaxItems = 128;               // splits per (sequence, half); their merge weights fit the K stages
 static_assert(kMlaMaxItems * kHeads * 4 <= 2 * kKTile, "merge weights must fit the K stages");
 constexpr uint32_t kOCol = 0, kSCol = 256;      // tensor-memory columns of O and S
+constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is rescaled
 
 __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
                                                            const __grid_constant__ CUtensorMap tmK) {
@@ -324,20 +325,23 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
     mbar_wait(smem_u32(&qbar), 0, a.ws);
     const uint32_t idesc_qk = umma_idesc(128, kTok, false);
     const uint32_t idesc_pv = umma_idesc(128, 256, true);
-    for (int t = 0; t < n_tiles; ++t) {
+    // thread 0: S = Q K^T of tile t once its K tile has landed
+    auto issue_qk = [&](int t) {
       const int st = t & 1;
       mbar_wait(smem_u32(&kbar[st]), (t >> 1) & 1, a.ws);
       tc_fence_after();
-      if (tid == 0) {
-        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * kKTile);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * kKTile);
 #pragma unroll 1
-        for (int kb = 0; kb < kKB; ++kb)
+      for (int kb = 0; kb < kKB; ++kb)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + kSCol, umma_desc(q0 + kb * kHeads * 128 + ks * 32, 16, 1024, 2),
-                      umma_desc(k0 + kb * kTok * 128 + ks * 32, 16, 1024, 2), idesc_qk, (kb | ks) != 0);
-        umma_commit(smem_u32(&sbar));
-      }
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + kSCol, umma_desc(q0 + kb * kHeads * 128 + ks * 32, 16, 1024, 2),
+                    umma_desc(k0 + kb * kTok * 128 + ks * 32, 16, 1024, 2), idesc_qk, (kb | ks) != 0);
+      umma_commit(smem_u32(&sbar));
+    };
+    for (int t = 0; t < n_tiles; ++t) {
+      const int st = t & 1;
+      if (t == 0 && tid == 0) issue_qk(0);  // later tiles' QK is issued right after the previous P.V
       mbar_wait(smem_u32(&sbar), t & 1, a.ws);
       tc_fence_after();
       uint32_t sv[32];
@@ -353,12 +357,16 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
       }
       if (t > 0) mbar_wait(smem_u32(&obar), (t - 1) & 1, a.ws);  // P.V of tile t-1 done: P and O free
       tc_fence_after();
-      const float m_new = fmaxf(m_run, mt);
-      // rescale O when this head's running max moved; the tensor-memory loads and stores are
-      // warp-collective, so a warp rescales together (alpha = 1 on lanes whose max held)
-      const bool moved = t > 0 && m_new > m_run;
-      if (__any_sync(0xffffffffu, moved)) {
-        const float al = moved ? exp2f(m_run - m_new) : 1.f;
+      // The exponent reference m_run moves only when this head's max exceeds it by more than
+      // kRescaleSlack (log2 units): p stays <= 2^kRescaleSlack, exact to fp32 rounding, and the
+      // normaliser l uses the same reference, so the result is unchanged while the costly
+      // rescale of O in tensor memory becomes rare. The tensor-memory loads and stores are
+      // warp-collective, so a warp rescales together (alpha = 1 on lanes that keep theirs).
+      const bool moved = t == 0 || mt > m_run + kRescaleSlack;
+      const float m_new = moved ? fmaxf(m_run, mt) : m_run;
+      const bool rescale = t > 0 && moved;
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float al = rescale ? exp2f(m_run - m_new) : 1.f;
         l_run *= al;
 #pragma unroll 1
         for (int c0 = 0; c0 < 256; c0 += 32) {
@@ -393,6 +401,7 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
           umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 512, 4), umma_desc(v0 + ks * 16 * 128, kTok * 128, 1024, 2),
                     idesc_pv, (t | ks) != 0);
         umma_commit(smem_u32(&obar));
+        if (t + 1 < n_tiles) issue_qk(t + 1);  // queued behind P.V(t); S was read before the barrier above
         if (t + 2 < n_tiles) {
           mbar_wait(smem_u32(&obar), t & 1, a.ws);  // P.V has read this K tile
           issue_tile(t + 2);

@@ -240,27 +240,25 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
 // ------------------------------------------------------------------------------------
 // One CTA per (chunk of a.pchunk pages, sequence, group of up to 8 KV heads). The summaries of
 // a page for the CTA's heads are one contiguous run (H * 2 * D elements; 4 KB at H = 8,
-// D = 128 bf16). A producer warp fetches each page with one bulk copy (TMA engine) into a ring
-// of kStages shared-memory stages of a.stage_pages pages; each stage has a "full" mbarrier
-// (copy bytes) and an "empty" mbarrier (one arrival per consumer warp), so the eight consumer
-// warps run decoupled, with bounded waits. Consumer warp w scores KV head w % HPC of the group
-// for every (8 / HPC)-th page step, from shared memory. Writes one 32-bit order key per page (0
-// for the forced sink / tail and for pages whose block id is out of range) and, when asked,
-// the fp32 score.
+// D = 128 bf16), so warp 0 fetches each page with one bulk copy (TMA engine) into a ring of
+// kStages shared-memory stages of a.stage_pages pages, completion tracked by one mbarrier per
+// stage (bounded waits). All warps then score from shared memory: warp w takes KV head w % HPC
+// of the group and every (8 / HPC)-th page step. Writes one 32-bit order key per page (0 for
+// the forced sink / tail and for pages whose block id is out of range) and, when asked, the
+// fp32 score.
 constexpr int kStages = 3;
 constexpr int kStageBytes = 32768;
 constexpr int kMaxStagePages = 32;
-constexpr int kScoreThreads = kThreads + 32;  // 8 consumer warps + 1 producer warp
 
 template <typename T, int D, int G>
-__global__ void __maxnreg__(112) page_score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
   constexpr int ES = Elem<T>::kBytes;
   static_assert(LPP >= 1 && LPP <= 32 && (LPP & (LPP - 1)) == 0, "row must be 16..512 bytes, power of 2");
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ __align__(8) uint64_t bars[kStages];
   __shared__ int okflag[kStages][kMaxStagePages];
 
   const int i = blockIdx.y;
@@ -272,59 +270,52 @@ __global__ void __maxnreg__(112) page_score_kernel(ScoreArgs a) {
   if (p0 >= P) return;
   const int p1 = min(P, p0 + a.pchunk);
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA
-  const int ng = kWarps / hpc;                         // consumer warps per head
+  const int ng = kWarps / hpc;                         // warps per head
   const int h0 = blockIdx.z * hpc;
-  const int group_bytes = hpc * 2 * D * ES;            // one page's summaries for the CTA's heads
-  const int sp = a.stage_pages;
-  const int n_stages = (p1 - p0 + sp - 1) / sp;
-
-  if (tid == 0) {
-    for (int k = 0; k < kStages; ++k) {
-      mbar_init(smem_u32(&full_bar[k]), 1);
-      mbar_init(smem_u32(&empty_bar[k]), kWarps);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == kWarps) {  // ---- producer warp ----
-    const T *sumbase = reinterpret_cast<const T *>(a.summaries);
-    const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
-    for (int st = 0; st < n_stages; ++st) {
-      const int slot = st % kStages;
-      if (st >= kStages) mbar_wait(smem_u32(&empty_bar[slot]), ((st / kStages) - 1) & 1, a.ws);
-      const int pb = p0 + st * sp;
-      bool ok = false;
-      int blk = -1;
-      if (lane < sp) {
-        const int p = pb + lane;
-        if (p < p1) {
-          blk = __ldg(bt + p);
-          ok = blk >= 0 && blk < a.nb;
-          if (!ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
-        }
-        okflag[slot][lane] = ok;
-      }
-      const unsigned mask = __ballot_sync(0xffffffffu, ok);
-      const uint32_t bar = smem_u32(&full_bar[slot]);
-      __syncwarp();  // the flags above are ordered before lane 0's release-arrive
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, (uint32_t)__popc(mask) * group_bytes);
-      }
-      __syncwarp();
-      if (ok)
-        bulk_g2s(smem_u32(smem_raw + (size_t)slot * kStageBytes + (size_t)lane * group_bytes),
-                 sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar);
-    }
-    return;
-  }
-
-  // ---- consumer warps ----
   const int hh = warp % hpc;
   const int h = h0 + hh;
   const int wg = warp / hpc;
   const int unit = i * a.H_kv + h;
+  const int group_bytes = hpc * 2 * D * ES;            // one page's summaries for the CTA's heads
+  const int sp = a.stage_pages;
+  const int n_stages = (p1 - p0 + sp - 1) / sp;
+  const T *sumbase = reinterpret_cast<const T *>(a.summaries);
+  const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) mbar_init(smem_u32(&bars[k]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // warp 0: fetch the pages of stage `st` (chunk-local stage index) into ring slot st % kStages
+  auto produce = [&](int st) {
+    const int slot = st % kStages;
+    const int pb = p0 + st * sp;
+    bool ok = false;
+    int blk = -1;
+    if (lane < sp) {
+      const int p = pb + lane;
+      if (p < p1) {
+        blk = __ldg(bt + p);
+        ok = blk >= 0 && blk < a.nb;
+        if (!ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+      }
+      okflag[slot][lane] = ok;
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, ok);
+    const uint32_t bar = smem_u32(&bars[slot]);
+    __syncwarp();  // the flags above are ordered before lane 0's release-arrive
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(mask) * group_bytes);
+    __syncwarp();
+    if (ok)
+      bulk_g2s(smem_u32(smem_raw + (size_t)slot * kStageBytes + (size_t)lane * group_bytes),
+               sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar);
+  };
+
+  if (warp == 0)
+    for (int st = 0; st < kStages && st < n_stages; ++st) produce(st);
+
   const int sub = lane % LPP;  // which 16-byte chunk of the summary row
   const int grp = lane / LPP;  // which page of the warp step
   float2 qp[G][EPC / 2], qn[G][EPC / 2];
@@ -346,7 +337,7 @@ __global__ void __maxnreg__(112) page_score_kernel(ScoreArgs a) {
 
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % kStages;
-    mbar_wait(smem_u32(&full_bar[slot]), (st / kStages) & 1, a.ws);
+    mbar_wait(smem_u32(&bars[slot]), (st / kStages) & 1, a.ws);
     const unsigned char *stage = smem_raw + (size_t)slot * kStageBytes;
     const int pb = p0 + st * sp;
     const int np = min(sp, p1 - pb);
@@ -381,8 +372,11 @@ __global__ void __maxnreg__(112) page_score_kernel(ScoreArgs a) {
         if (srow) srow[p] = sc;
       }
     }
-    __syncwarp();  // every lane of this warp is done reading the slot
-    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+    __syncthreads();  // every warp is done with this slot
+    if (warp == 0 && st + kStages < n_stages) {
+      fence_proxy_async_smem();
+      produce(st + kStages);
+    }
   }
 }
 
@@ -521,7 +515,7 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   const int k1_smem = kStages * kStageBytes;
   cudaError_t e = cudaFuncSetAttribute(page_score_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, k1_smem);
   if (e != cudaSuccess) return e;
-  page_score_kernel<T, D, G><<<g1, kScoreThreads, k1_smem, s>>>(a);
+  page_score_kernel<T, D, G><<<g1, kThreads, k1_smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_page_select(a, s);
