@@ -508,7 +508,8 @@ cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaSt
 
 bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   const long long units = (long long)L.batch * 2;
-  int items = (int)std::max(1LL, (152 + units - 1) / units);
+  // one CTA per SM (shared memory) and one wave: at most 152 / units splits per (sequence, half)
+  int items = (int)std::max(1LL, 152 / units);
   items = std::min(items, std::min(entries, kMlaMaxItems));
   int sw = (entries + items - 1) / items;
   sw = std::min(sw, kMlaMaxSw);

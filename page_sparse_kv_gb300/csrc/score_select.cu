@@ -251,7 +251,7 @@ constexpr int kStageBytes = 32768;
 constexpr int kMaxStagePages = 32;
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
@@ -341,35 +341,52 @@ __global__ void __launch_bounds__(kThreads) page_score_kernel(ScoreArgs a) {
     const unsigned char *stage = smem_raw + (size_t)slot * kStageBytes;
     const int pb = p0 + st * sp;
     const int np = min(sp, p1 - pb);
-    for (int j0 = wg * PPW; j0 < np; j0 += ng * PPW) {  // warp-uniform bound
-      const int j = j0 + grp;
-      const bool live = j < np && okflag[slot][j < sp ? j : 0];
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (live) {
-        const unsigned char *row = stage + (size_t)j * group_bytes + (size_t)hh * 2 * D * ES + sub * 16;
-        lo = *reinterpret_cast<const uint4 *>(row);
-        hi = *reinterpret_cast<const uint4 *>(row + D * ES);
-      }
-      float2 kl[EPC / 2], kh[EPC / 2];
-      Elem<T>::to_f2(lo, kl);
-      Elem<T>::to_f2(hi, kh);
-      float v[G];
+    // two page steps per iteration (both steps' loads first, then two independent chains)
+    for (int j0 = wg * PPW; j0 < np; j0 += 2 * ng * PPW) {  // warp-uniform bound
+      uint4 lo[2], hi[2];
+      bool live[2];
+      int jj[2];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < EPC / 2; ++e) {
-          acc = ffma2(qp[g][e], kh[e], acc);
-          acc = ffma2(qn[g][e], kl[e], acc);
+      for (int u = 0; u < 2; ++u) {
+        const int j = j0 + u * ng * PPW + grp;
+        jj[u] = j;
+        live[u] = j < np && okflag[slot][j < sp ? j : 0];
+        lo[u] = make_uint4(0, 0, 0, 0);
+        hi[u] = lo[u];
+        if (live[u]) {
+          const unsigned char *row = stage + (size_t)j * group_bytes + (size_t)hh * 2 * D * ES + sub * 16;
+          lo[u] = *reinterpret_cast<const uint4 *>(row);
+          hi[u] = *reinterpret_cast<const uint4 *>(row + D * ES);
         }
-        v[g] = acc.x + acc.y;
       }
-      const float sc = group_score<G, LPP>(v, lane) * a.scale;
-      if (sub == 0 && j < np) {
-        const int p = pb + j;
-        const bool forced = (p == 0) || (p == P - 1);
-        krow[p] = (live && !forced) ? score_key(sc) : 0u;
-        if (srow) srow[p] = sc;
+      float v[2][G];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float2 kl[EPC / 2], kh[EPC / 2];
+        Elem<T>::to_f2(lo[u], kl);
+        Elem<T>::to_f2(hi[u], kh);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < EPC / 2; ++e) {
+            acc = ffma2(qp[g][e], kh[e], acc);
+            acc = ffma2(qn[g][e], kl[e], acc);
+          }
+          v[u][g] = acc.x + acc.y;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (u == 1 && j0 + ng * PPW >= np) break;  // warp-uniform
+        const float sc = group_score<G, LPP>(v[u], lane) * a.scale;
+        const int j = jj[u];
+        if (sub == 0 && j < np) {
+          const int p = pb + j;
+          const bool forced = (p == 0) || (p == P - 1);
+          krow[p] = (live[u] && !forced) ? score_key(sc) : 0u;
+          if (srow) srow[p] = sc;
+        }
       }
     }
     __syncthreads();  // every warp is done with this slot
