@@ -229,7 +229,7 @@ def run_psk(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- warm-up ---------------------------------------------------------------------------
+    launches_per_step = 5 if w.latent else 4  # append, (q split,) score, select, decode
     for _ in range(args.warmup):
         append(); score(); decode()
         append(); dense()
@@ -267,13 +267,51 @@ def run_psk(args):
     barrier()
     sparse_ms = t0.elapsed_time(t1) / K
     dense_ms = d0.elapsed_time(d1) / Kd
+
+    # ---- the same steps captured once into CUDA graphs and replayed --------------------------
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()  # warm the capture stream
+        stream.wait_stream(side)
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    try:
+        g_sparse = graph_of(lambda: (append(), score(), decode()))
+        g_dense = graph_of(lambda: (append(), dense()))
+        for _ in range(3):
+            g_sparse.replay()
+            g_dense.replay()
+        barrier()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(K):
+            g_sparse.replay()
+        r1.record(stream)
+        r2 = torch.cuda.Event(enable_timing=True)
+        r2.record(stream)
+        for _ in range(Kd):
+            g_dense.replay()
+        r3 = torch.cuda.Event(enable_timing=True)
+        r3.record(stream)
+        torch.cuda.synchronize()
+        graph_sparse_ms = r0.elapsed_time(r1) / K
+        graph_dense_ms = r2.elapsed_time(r3) / Kd
+    except Exception as exc:  # capture not possible here: report eager numbers only
+        print(f"graph capture failed: {exc}", file=sys.stderr)
+        graph_sparse_ms = graph_dense_ms = float('nan')
     t_app = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
     t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
     t_dec = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
     if dist is not None:
-        tt = torch.tensor([sparse_ms, dense_ms], device=dev)
+        tt = torch.tensor([sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        sparse_ms, dense_ms = tt.tolist()
+        sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = tt.tolist()
 
     # ---- end to end: host buffers through the C ABI (pinned H2D of the step's inputs, D2H of out)
     qh = to_torch(q_host, w.dtype).pin_memory()
@@ -353,9 +391,12 @@ def run_psk(args):
         "dense": {"us_per_step": dense_ms * 1e3, "bytes": dense_bytes,
                   "gbs": dense_bytes / (dense_ms * 1e-3) / 1e9},
         "speedup_vs_dense": dense_ms / sparse_ms,
+        "graph": None if graph_sparse_ms != graph_sparse_ms else {
+            "us_per_step": graph_sparse_ms * 1e3, "dense_us_per_step": graph_dense_ms * 1e3,
+            "speedup_vs_dense": graph_dense_ms / graph_sparse_ms},
         "kernels_us": {"append": t_app * 1e3, "score_select": t_score * 1e3, "sparse_decode": t_dec * 1e3},
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": K * 4,
+        "gpu_launches": K * launches_per_step,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "setup_s": round(setup_s, 1),
