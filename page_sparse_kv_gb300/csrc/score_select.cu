@@ -29,6 +29,7 @@
 //   because keys are unique once ties are ordered by page index.
 // The output row is: sink, winners (ascending), tail, then -1 padding.
 #include <algorithm>
+#include <cstdlib>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
@@ -525,144 +526,6 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   write_row_ends(sel_row, P, count, wrote, a.b_max);
 }
 
-// One warp per (sequence, KV head) unit of at most kWarpSelMax pages: the same selection as
-// page_select_kernel with warp-synchronous steps only (no block barriers), which keeps the
-// latency low for batch-1 decode. The unit's keys are staged once in shared memory; each radix
-// pass counts into the warp's own 256-bin histogram and finds the threshold digit with a warp
-// scan; the winners are written in index order by ballot compaction, the first need_eq keys
-// equal to the threshold (lowest indices) included.
-constexpr int kWarpSelMax = 4096;
-constexpr int kWarpSelWarps = 4;
-
-__global__ void __launch_bounds__(kWarpSelWarps * 32) page_select_warp_kernel(ScoreArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ int hist_all[kWarpSelWarps][256];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x * kWarpSelWarps + warp;
-  if (unit >= a.B * a.H_kv) return;  // whole warp leaves; this kernel has no block barriers
-  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw) + (size_t)warp * kWarpSelMax;
-  int *hist = hist_all[warp];
-  const int i = unit / a.H_kv;
-  const int seq_len = a.seq_lens[i];
-  const int P = (seq_len + a.ps - 1) / a.ps;
-  int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
-  if (seq_len < 1 || P > a.max_pages || P > kWarpSelMax) {
-    if (lane == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
-    for (int x = lane; x < a.b_max; x += 32) sel_row[x] = -1;
-    return;
-  }
-  const int budget = a.budgets[i];
-  if ((budget < 2 && P > 1) || budget < 1 || budget > a.b_max) {
-    if (lane == 0) set_status(a.ws, PSK_DEV_BAD_BUDGET);
-    for (int x = lane; x < a.b_max; x += 32) sel_row[x] = -1;
-    return;
-  }
-  const int count = min(budget, P);
-  if (count >= P) {
-    for (int x = lane; x < a.b_max; x += 32) sel_row[x] = x < P ? x : -1;
-    return;
-  }
-  const int k_free = count - 2;
-  const uint32_t *krow = a.keys + (size_t)unit * a.max_pages;
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  int valid = 0;
-  for (int x = lane; x < P; x += 32) {
-    const uint32_t k = __ldcg(krow + x);
-    keys[x] = k;
-    if (k != 0u) {
-      kmin = min(kmin, k);
-      kmax = max(kmax, k);
-      ++valid;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    valid += __shfl_xor_sync(0xffffffffu, valid, o);
-  }
-  __syncwarp();
-  const bool take_all = valid <= k_free;
-  uint32_t thr = 0;
-  int need = k_free;
-  if (k_free > 0 && !take_all) {
-    const uint32_t diff = kmin ^ kmax;
-    const int top = diff ? 31 - __clz(diff) : 0;
-    int shift = top >= 7 ? top - 7 : 0;
-    uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
-    uint32_t mask = shift + 8 >= 32 ? 0u : (0xFFFFFFFFu << (shift + 8));
-#pragma unroll 1
-    for (;;) {
-#pragma unroll
-      for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0;
-      __syncwarp();
-      for (int x = lane; x < P; x += 32) {
-        const uint32_t key = keys[x];
-        if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
-      }
-      __syncwarp();
-      // lane l owns bins 255 - 8l - j (j = 0..7), i.e. the digits in descending order
-      int c[8], tot = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - 8 * lane - j];
-        tot += c[j];
-      }
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int run = incl - tot;  // keys with a larger digit than this lane's first bin
-      int found_digit = -1, found_above = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (found_digit < 0 && run + c[j] >= need && run < need) {
-          found_digit = 255 - 8 * lane - j;
-          found_above = run;
-        }
-        run += c[j];
-      }
-      const unsigned who = __ballot_sync(0xffffffffu, found_digit >= 0);
-      const int src = __ffs(who) - 1;
-      const int d = __shfl_sync(0xffffffffu, found_digit, src);
-      need -= __shfl_sync(0xffffffffu, found_above, src);
-      prefix |= static_cast<uint32_t>(d) << shift;
-      mask |= 255u << shift;
-      __syncwarp();
-      if (shift == 0) break;
-      shift = shift >= 8 ? shift - 8 : 0;
-    }
-    thr = prefix;
-  }
-  // winners in index order: sink, winners, tail, padding
-  int written = 0, eq_seen = 0;
-  if (k_free > 0) {
-    const unsigned lt = (1u << lane) - 1u;
-    for (int base = 0; base < P; base += 32) {
-      const int x = base + lane;
-      const uint32_t key = x < P ? keys[x] : 0u;
-      bool take;
-      if (take_all) {
-        take = key != 0u;
-      } else {
-        const unsigned eqm = __ballot_sync(0xffffffffu, key != 0u && key == thr);
-        const bool eq = (eqm >> lane) & 1u;
-        take = key > thr || (eq && eq_seen + __popc(eqm & lt) < need);
-        eq_seen += __popc(eqm);
-      }
-      const unsigned tm = __ballot_sync(0xffffffffu, take);
-      if (take) sel_row[1 + written + __popc(tm & lt)] = x;
-      written += __popc(tm);
-    }
-  }
-  if (lane == 0) sel_row[0] = 0;
-  for (int x = 1 + written + lane; x < count - 1; x += 32) sel_row[x] = -1;
-  if (lane == 0) sel_row[count - 1] = P - 1;
-  for (int x = count + lane; x < a.b_max; x += 32) sel_row[x] = -1;
-}
-
 template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
@@ -679,14 +542,6 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
-  if (a.max_pages <= kWarpSelMax) {
-    const int smem = kWarpSelWarps * kWarpSelMax * 4;
-    cudaError_t e = cudaFuncSetAttribute(page_select_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int units = a.B * a.H_kv;
-    page_select_warp_kernel<<<(units + kWarpSelWarps - 1) / kWarpSelWarps, kWarpSelWarps * 32, smem, s>>>(a);
-    return cudaGetLastError();
-  }
   const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -715,6 +570,10 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   int pchunk = 128;
   while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152 * 2)
     pchunk /= 2;
+  if (const char *env = std::getenv("PSK_SCORE_PCHUNK")) {  // tuning override: pages per score CTA
+    const int v = std::atoi(env);
+    if (v >= 8 && v <= 4096) pchunk = v;
+  }
   plan->pchunk = pchunk;
   {
     const int hpc = L.num_kv_heads < kWarps ? L.num_kv_heads : kWarps;
