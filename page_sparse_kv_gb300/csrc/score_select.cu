@@ -44,108 +44,109 @@ constexpr int kMergeCap = 8192;  // candidates the merge CTA can hold
 // ------------------------------------------------------------------------------------
 // block-wide helpers (blockDim.x == kThreads)
 // ------------------------------------------------------------------------------------
-// Exclusive prefix sum of one int per thread in thread order; *total gets the sum.
-__device__ __forceinline__ int block_exclusive_scan(int x, int *sh, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  if (lane == 31) sh[warp] = inc;
+// Exclusive prefix of one int per thread in thread order with two barriers: the counts go to
+// shared memory, warp 0 scans them (8 per lane), everyone reads its base. cnt: kThreads + 1 ints.
+__device__ __forceinline__ int block_scan_w0(int x, int *cnt, int *total) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  cnt[tid] = x;
   __syncthreads();
-  if (warp == 0) {
-    const int w = lane < kWarps ? sh[lane] : 0;
-    int winc = w;
+  if (tid < 32) {
+    int v[kThreads / 32], sum = 0;
 #pragma unroll
-    for (int o = 1; o < kWarps; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, winc, o);
-      if (lane >= o) winc += y;
+    for (int j = 0; j < kThreads / 32; ++j) {
+      v[j] = cnt[lane * (kThreads / 32) + j];
+      sum += v[j];
     }
-    if (lane < kWarps) sh[lane] = winc - w;
-    if (lane == kWarps - 1) sh[kWarps] = winc;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < kThreads / 32; ++j) {
+      cnt[lane * (kThreads / 32) + j] = run;
+      run += v[j];
+    }
+    if (lane == 31) cnt[kThreads] = incl;
   }
   __syncthreads();
-  const int res = inc - x + sh[warp];
-  if (total) *total = sh[kWarps];
-  __syncthreads();
-  return res;
+  const int r = cnt[tid];
+  if (total) *total = cnt[kThreads];
+  return r;
 }
 
 // Radix select over keys[0..n) (key 0 = not a candidate): finds the k-th largest key T and
 // how many keys equal to T belong to the top k (the lowest-indexed ones). Requires
-// 1 <= k <= number of nonzero keys. hist: 8 warps x 256 private bins (8 KB).
-// The digits start at the highest bit in which the candidates' min and max keys differ (the
-// bits above are common to all of them), 8 bits per pass; each warp counts into its own
-// histogram with plain shared-memory atomics and a pass sums the 8 histograms per bin.
-__device__ void radix_select(const uint32_t *keys, int n, int k, int *hist, int *sh, uint32_t *T_out,
-                             int *need_eq_out) {
+// 1 <= k <= number of nonzero keys, and kmin / kmax = the smallest / largest nonzero key.
+// The digits start at the highest bit in which kmin and kmax differ (the bits above are common
+// to every candidate), 8 bits per pass. Each warp counts into its own 256-bin histogram with
+// plain shared-memory atomics; warp 0 alone sums the warps' histograms, scans the 256 bins
+// from the top, picks the digit and clears the other histogram buffer, so a pass costs two
+// block barriers. hist: 2 buffers x 8 warps x 256 bins.
+__device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, uint32_t kmax, int *hist, int *sh,
+                             uint32_t *T_out, int *need_eq_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // common high bits of the candidates
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int x = tid; x < n; x += kThreads) {
-    const uint32_t key = keys[x];
-    if (key != 0u) {
-      kmin = min(kmin, key);
-      kmax = max(kmax, key);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  __shared__ uint32_t red_min[kWarps], red_max[kWarps];
-  if (lane == 0) {
-    red_min[warp] = kmin;
-    red_max[warp] = kmax;
-  }
-  __syncthreads();
-  kmin = red_min[0];
-  kmax = red_max[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) {
-    kmin = min(kmin, red_min[w]);
-    kmax = max(kmax, red_max[w]);
-  }
   const uint32_t diff = kmin ^ kmax;
   const int top = diff ? 31 - __clz(diff) : 0;  // highest differing bit
   int shift = top >= 7 ? top - 7 : 0;
   uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
   uint32_t mask = shift + 8 >= 32 ? 0u : (0xFFFFFFFFu << (shift + 8));
   int need = k;
-  int *myhist = hist + warp * 256;
+  int buf = 0;
+  for (int b = tid; b < 2 * kWarps * 256; b += kThreads) hist[b] = 0;
+  __syncthreads();
 #pragma unroll 1
   for (;;) {
-    for (int b = tid; b < kWarps * 256; b += kThreads) hist[b] = 0;
-    __syncthreads();
+    int *hb = hist + buf * kWarps * 256;
+    int *myhist = hb + warp * 256;
     for (int x = tid; x < n; x += kThreads) {
       const uint32_t key = keys[x];
       if (key != 0u && (key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
-    // bin 255 - tid, summed over the warps' histograms; suffix sums by a block scan
-    const int bin = 255 - tid;
-    int hb = 0;
+    if (warp == 0) {
+      // lane l owns bins 255 - 8l - j (descending digits)
+      int c[8], tot = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) hb += hist[w * 256 + bin];
-    const int excl = block_exclusive_scan(hb, sh, nullptr);  // keys with digit > bin
-    const int incl = excl + hb;                              // keys with digit >= bin
-    if (incl >= need && excl < need) {
-      sh[kWarps + 1] = bin;
-      sh[kWarps + 2] = excl;
+      for (int j = 0; j < 8; ++j) {
+        const int bin = 255 - 8 * lane - j;
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += hb[w * 256 + bin];
+        c[j] = v;
+        tot += v;
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - tot;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + c[j] >= need && run < need) {
+          sh[0] = 255 - 8 * lane - j;
+          sh[1] = run;
+        }
+        run += c[j];
+      }
+      int *other = hist + (buf ^ 1) * kWarps * 256;
+      for (int b = lane; b < kWarps * 256; b += 32) other[b] = 0;
     }
     __syncthreads();
-    const int d = sh[kWarps + 1];
-    need -= sh[kWarps + 2];
+    const int d = sh[0];
+    need -= sh[1];
     prefix |= static_cast<uint32_t>(d) << shift;
     mask |= 255u << shift;
-    __syncthreads();
+    buf ^= 1;
     if (shift == 0) break;
     shift = shift >= 8 ? shift - 8 : 0;
     // a digit that overlaps bits already fixed is harmless: they match the prefix
   }
+  __syncthreads();  // every thread has read sh before the caller reuses it
   *T_out = prefix;
   *need_eq_out = need;
 }
@@ -154,16 +155,18 @@ __device__ void radix_select(const uint32_t *keys, int n, int k, int *hist, int 
 //   take_all:  key != 0
 //   otherwise: key > T, or key == T among the first need_eq such items
 // to out_key / out_page (page = pages ? pages[x] : page_base + x). Returns the count.
+// cnt: kThreads + 1 ints of scratch.
 __device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int page_base, int n, bool take_all,
-                             uint32_t T, int need_eq, uint32_t *out_key, int32_t *out_page, int *sh) {
+                             uint32_t T, int need_eq, uint32_t *out_key, int32_t *out_page, int *cnt) {
   const int tid = threadIdx.x;
   const int per = (n + kThreads - 1) / kThreads;
   const int x0 = min(n, tid * per), x1 = min(n, x0 + per);
   int eq = 0;
   if (!take_all)
     for (int x = x0; x < x1; ++x) eq += keys[x] == T;
-  const int eq_base = take_all ? 0 : block_exclusive_scan(eq, sh, nullptr);
-  int cnt = 0, seen = eq_base;
+  const int eq_base = take_all ? 0 : block_scan_w0(eq, cnt, nullptr);
+  if (!take_all) __syncthreads();  // cnt is reused below
+  int c = 0, seen = eq_base;
   for (int x = x0; x < x1; ++x) {
     const uint32_t key = keys[x];
     bool take;
@@ -173,10 +176,10 @@ __device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int pag
       take = key > T;
       if (key == T) take = (seen++ < need_eq);
     }
-    cnt += take;
+    c += take;
   }
   int total;
-  const int base = block_exclusive_scan(cnt, sh, &total);
+  const int base = block_scan_w0(c, cnt, &total);
   int w = base;
   seen = eq_base;
   for (int x = x0; x < x1; ++x) {
@@ -413,10 +416,51 @@ __device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, in
   for (int x = count + tid; x < b_max; x += kThreads) sel_row[x] = -1;
 }
 
+// Count, min and max of the nonzero keys of keys[0..n) over the block (two barriers).
+__device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t *kmin, uint32_t *kmax,
+                              uint32_t *red /* 3 * kWarps */) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
+  for (int x = tid; x < n; x += kThreads) {
+    const uint32_t k = keys[x];
+    if (k != 0u) {
+      ++c;
+      lo = min(lo, k);
+      hi = max(hi, k);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    red[warp] = c;
+    red[kWarps + warp] = lo;
+    red[2 * kWarps + warp] = hi;
+  }
+  __syncthreads();
+  c = 0;
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    c += red[w];
+    lo = min(lo, red[kWarps + w]);
+    hi = max(hi, red[2 * kWarps + w]);
+  }
+  *count = (int)c;
+  *kmin = lo;
+  *kmax = hi;
+  __syncthreads();  // red is reused by the caller's next call
+}
+
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ int hist[kWarps * 256];
-  __shared__ int sh[2 * kWarps + 4];
+  __shared__ int hist[2 * kWarps * 256];
+  __shared__ int cnt[kThreads + 1];
+  __shared__ uint32_t red[3 * kWarps];
   __shared__ int flag_last;
 
   const int h = blockIdx.x, c = blockIdx.y, i = blockIdx.z;
@@ -456,29 +500,26 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   const int p1 = min(P, p0 + a.chunk);
   const int n = p1 - p0;
   const uint32_t *krow = a.keys + (size_t)unit * a.max_pages + p0;
-  int valid = 0;
-  for (int x = tid; x < n; x += kThreads) {
-    const uint32_t k = __ldcg(krow + x);
-    keys[x] = k;
-    valid += k != 0u;
-  }
+  for (int x = tid; x < n; x += kThreads) keys[x] = __ldcg(krow + x);
+  __syncthreads();
   int total_valid;
-  block_exclusive_scan(valid, sh, &total_valid);  // also orders the smem writes above
+  uint32_t kmin, kmax;
+  nonzero_stats(keys, n, &total_valid, &kmin, &kmax, red);
   int wrote = 0;
   if (k_free > 0) {
     uint32_t thr = 0;
     int need_eq = 0;
     const bool take_all = total_valid <= k_free;
-    if (!take_all) radix_select(keys, n, k_free, hist, sh, &thr, &need_eq);
+    if (!take_all) radix_select(keys, n, k_free, kmin, kmax, hist, cnt, &thr, &need_eq);
     if (nch == 1) {
-      wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + 1, sh);
+      wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + 1, cnt);
       write_row_ends(sel_row, P, count, wrote, a.b_max);
       return;
     }
     const int slot = unit * a.n_chunks_max + c;
     uint32_t *ck = a.cand_key + (size_t)slot * a.k_cap;
     int32_t *cp = a.cand_page + (size_t)slot * a.k_cap;
-    wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, ck, cp, sh);
+    wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, ck, cp, cnt);
     if (tid == 0) a.cand_count[slot] = wrote;
   } else {
     if (nch == 1) {
@@ -520,8 +561,13 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
     uint32_t thr = 0;
     int need_eq = 0;
     const bool take_all = n_c <= k_free;
-    if (!take_all) radix_select(mkey, n_c, k_free, hist, sh, &thr, &need_eq);
-    wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + 1, sh);
+    if (!take_all) {
+      int nz;
+      uint32_t mlo, mhi;
+      nonzero_stats(mkey, n_c, &nz, &mlo, &mhi, red);
+      radix_select(mkey, n_c, k_free, mlo, mhi, hist, cnt, &thr, &need_eq);
+    }
+    wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + 1, cnt);
   }
   write_row_ends(sel_row, P, count, wrote, a.b_max);
 }
