@@ -338,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
   }
   uint32_t *krow = a.keys + (size_t)unit * a.max_pages;
   float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
+  // this lane's byte offset inside a page's run: its head and its chunk
+  const uint32_t lane_off = (uint32_t)hh * 2 * D * ES + sub * 16;
 
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % kStages;
@@ -345,23 +347,18 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
     const unsigned char *stage = smem_raw + (size_t)slot * kStageBytes;
     const int pb = p0 + st * sp;
     const int np = min(sp, p1 - pb);
-    // two page steps per iteration (both steps' loads first, then two independent chains)
+    // two page steps per iteration (both steps' loads first, then two independent chains).
+    // Loads are unconditional (always inside the stage); pages that are not live (past the
+    // chunk, or a flagged block) are dropped when the key is written.
+    const uint32_t stage_addr = smem_u32(stage) + lane_off;
     for (int j0 = wg * PPW; j0 < np; j0 += 2 * ng * PPW) {  // warp-uniform bound
       uint4 lo[2], hi[2];
-      bool live[2];
-      int jj[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int j = j0 + u * ng * PPW + grp;
-        jj[u] = j;
-        live[u] = j < np && okflag[slot][j < sp ? j : 0];
-        lo[u] = make_uint4(0, 0, 0, 0);
-        hi[u] = lo[u];
-        if (live[u]) {
-          const unsigned char *row = stage + (size_t)j * group_bytes + (size_t)hh * 2 * D * ES + sub * 16;
-          lo[u] = *reinterpret_cast<const uint4 *>(row);
-          hi[u] = *reinterpret_cast<const uint4 *>(row + D * ES);
-        }
+        const int jl = min(j0 + u * ng * PPW + grp, sp - 1);  // stays inside the stage
+        const uint32_t addr = stage_addr + (uint32_t)jl * (uint32_t)group_bytes;
+        lo[u] = lds128(addr);
+        hi[u] = lds128(addr + D * ES);
       }
       float v[2][G];
 #pragma unroll
@@ -382,13 +379,14 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        if (u == 1 && j0 + ng * PPW >= np) break;  // warp-uniform
+        const int jb = j0 + u * ng * PPW;
+        if (u == 1 && jb >= np) break;  // warp-uniform
         const float sc = group_score<G, LPP>(v[u], lane) * a.scale;
-        const int j = jj[u];
+        const int j = jb + grp;
         if (sub == 0 && j < np) {
           const int p = pb + j;
           const bool forced = (p == 0) || (p == P - 1);
-          krow[p] = (live[u] && !forced) ? score_key(sc) : 0u;
+          krow[p] = (okflag[slot][j] && !forced) ? score_key(sc) : 0u;
           if (srow) srow[p] = sc;
         }
       }
