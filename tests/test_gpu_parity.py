@@ -171,6 +171,8 @@ def _custom(seq_lens, budgets, ps=16, dtype="bf16", H_q=8, H_kv=2, D=128, n_hot=
     dict(seq_lens=[32 * 50 + 31, 32], budgets=[5, 3], ps=32),          # page_size 32
     dict(seq_lens=[16 * 20 + 9, 77], budgets=[6, 3], dtype="f32", D=64, H_q=4, H_kv=1),
     dict(seq_lens=[16 * 30 + 2, 300], budgets=[5, 4], D=64),
+    dict(seq_lens=[16 * 70 + 3, 500], budgets=[9, 4], D=64, H_q=4, H_kv=1),   # 256-byte page runs
+    dict(seq_lens=[16 * 45 + 8, 16 * 9], budgets=[7, 3], H_q=16, H_kv=4),      # 4 KV heads
 ])
 def test_edge_cases(case):
     w = _custom(**case)
