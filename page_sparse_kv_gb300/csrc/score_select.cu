@@ -292,21 +292,20 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
   }
   __syncthreads();
 
+  // warp 0: block id of this lane's page of stage `st` (-1 past the chunk); loaded one stage
+  // ahead of its use so the latency hides behind the current stage's work
+  auto block_of = [&](int st) -> int {
+    const int p = p0 + st * sp + lane;
+    return (lane < sp && st < n_stages && p < p1) ? __ldg(bt + p) : -1;
+  };
   // warp 0: fetch the pages of stage `st` (chunk-local stage index) into ring slot st % kStages
-  auto produce = [&](int st) {
+  auto produce = [&](int st, int blk) {
     const int slot = st % kStages;
-    const int pb = p0 + st * sp;
-    bool ok = false;
-    int blk = -1;
-    if (lane < sp) {
-      const int p = pb + lane;
-      if (p < p1) {
-        blk = __ldg(bt + p);
-        ok = blk >= 0 && blk < a.nb;
-        if (!ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
-      }
-      okflag[slot][lane] = ok;
-    }
+    const int p = p0 + st * sp + lane;
+    const bool in_chunk = lane < sp && p < p1;
+    const bool ok = in_chunk && blk >= 0 && blk < a.nb;
+    if (in_chunk && !ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+    if (lane < sp) okflag[slot][lane] = ok;
     const unsigned mask = __ballot_sync(0xffffffffu, ok);
     const uint32_t bar = smem_u32(&bars[slot]);
     __syncwarp();  // the flags above are ordered before lane 0's release-arrive
@@ -318,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
   };
 
   if (warp == 0)
-    for (int st = 0; st < kStages && st < n_stages; ++st) produce(st);
+    for (int st = 0; st < kStages && st < n_stages; ++st) produce(st, block_of(st));
 
   const int sub = lane % LPP;  // which 16-byte chunk of the summary row
   const int grp = lane / LPP;  // which page of the warp step
@@ -343,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
 
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % kStages;
+    const int next_blk = warp == 0 ? block_of(st + kStages) : -1;  // in flight during this stage
     mbar_wait(smem_u32(&bars[slot]), (st / kStages) & 1, a.ws);
     const unsigned char *stage = smem_raw + (size_t)slot * kStageBytes;
     const int pb = p0 + st * sp;
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
     __syncthreads();  // every warp is done with this slot
     if (warp == 0 && st + kStages < n_stages) {
       fence_proxy_async_smem();
-      produce(st + kStages);
+      produce(st + kStages, next_blk);
     }
   }
 }
