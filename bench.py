@@ -2,15 +2,18 @@
 """Decode-step benchmark of page-selective sparse paged attention on one GB300 (per rank).
 
 One step = the whole hot path over one batch: append one decode token per sequence with its
-page-summary refresh, score + select pages, sparse split-K decode (4 kernel launches).
-The same run times the dense decode step (append + full-KV decode) for the speedup.
+page-summary refresh, score + select pages, sparse split-K decode (4 kernel launches; 5 on the
+latent config). The step's launches are captured once into a CUDA graph and the reported value
+is the mean over K graph replays (CUDA events on the launching stream); the same window also
+times the eager launches (with a per-call split) and the dense step (append + full-KV decode)
+both ways, so the speedup compares like with like.
 
 Default workload: batched ragged decode, B=64, H_q=32, H_kv=8, D=128, page 16, contexts
 U[8192, 65536], bf16, budget max(4, ceil(5% of pages)), 16 hot pages per KV head.
 Inputs stay larger than L2 every step (summaries ~0.6 GB, selected K/V ~0.5 GB in a 9.7 GB
 pool), so no L2 flush is needed.
 
-    python bench.py [--steps K] [--warmup W] [--impl psk|reference] [--workload 1..4]
+    python bench.py [--steps K] [--warmup W] [--impl psk|reference] [--workload 1..5]
     torchrun --nproc-per-node N bench.py --gpus N      # N independent replicas (weak scaling)
 """
 from __future__ import annotations
@@ -39,12 +42,44 @@ UNIT = "us/step/layer"
 
 
 def peaks():
+    """HBM GB/s and bf16 TFLOP/s (burst, sustained) measured on this GPU model, else the fallback."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "kind": "measured"}
     except Exception:
-        return 6800.0, "fallback"
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "kind": "fallback"}
+
+
+# DRAM bytes (read + write) per launch of the dominant call, from one ncu capture of that call
+# (dram__bytes_read.sum + dram__bytes_write.sum, summed over its kernels), keyed by workload and
+# call, with a digest of the sources the kernels are built from: a digest that no longer matches
+# means the kernels changed since the capture, and the traffic is reported as null.
+TRAFFIC = {}
+KERNEL_SOURCES = {
+    "page_score_kernel+page_select_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
+    "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),
+    "mla_qsplit_kernel+mla_score_kernel+page_select_kernel": ("mla.cu", "score_select.cu", "psk_common.cuh",
+                                                              "psk_internal.h"),
+    "mla_decode_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
+}
+
+
+def kernel_digest(call: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[call]:
+        with open(os.path.join(ROOT, "page_sparse_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(workload: str, call: str):
+    rec = TRAFFIC.get((workload, call))
+    if rec is None or rec["digest"] != kernel_digest(call):
+        return None
+    return rec["bytes"]
 
 
 def dist_env():
@@ -110,6 +145,20 @@ class Clocks:
 # ------------------------------------------------------------------------------------------
 # oracle timing (CPU baseline / reference arm)
 # ------------------------------------------------------------------------------------------
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings over the process group (the slowest replica sets
+    the step time). NaN (a mode a rank could not run) stays NaN."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    nan = torch.isnan(t).to(torch.float64)
+    dist.all_reduce(nan, op=dist.ReduceOp.MAX)
+    t = torch.nan_to_num(t, nan=0.0)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t[nan > 0] = float("nan")
+    return t.tolist()
+
+
 def oracle_sample(w, budget_s: float, start_seq: int = 0):
     """Times the oracle's sparse decode step (score every page, select, attend) on sequences
     taken in order from ``start_seq`` until ``budget_s`` seconds of oracle work accumulated.
@@ -117,7 +166,7 @@ def oracle_sample(w, budget_s: float, start_seq: int = 0):
     Returns (seconds per full batch step, sequences timed)."""
     import oracle as O
     scale = 1.0 / math.sqrt(w.D)
-    spent, n = 0.0, 0
+    spent, n, pages = 0.0, 0, 0
     i = start_seq
     while spent < budget_s and n < w.B:
         L = int(w.seq_lens[i])
@@ -130,8 +179,10 @@ def oracle_sample(w, budget_s: float, start_seq: int = 0):
         O.attend_pages(q, keys, vals, L, w.page_size, sel, w.dtype, scale)
         spent += time.perf_counter() - t0
         n += 1
+        pages += -(-L // w.page_size)
         i = (i + 1) % w.B
-    return spent / n * w.B, n
+    total_pages = int(((w.seq_lens + w.page_size - 1) // w.page_size).sum())
+    return spent / pages * total_pages, n
 
 
 def run_reference(args):
@@ -236,39 +287,7 @@ def run_psk(args):
     torch.cuda.synchronize()
     assert psk.get_device_status(ws) == 0, "device status set during warm-up"
 
-    # ---- timed sparse steps (per-kernel events on the launching stream) -------------------------
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    barrier()
-    with Clocks(local) as clk:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for k in range(K):
-            e = ev[k]
-            e[0].record(stream)
-            append()
-            e[1].record(stream)
-            score()
-            e[2].record(stream)
-            decode()
-            e[3].record(stream)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        # dense steps in the same clock window
-        Kd = max(3, K // 4)
-        d0 = torch.cuda.Event(enable_timing=True)
-        d1 = torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        for _ in range(Kd):
-            append(); dense()
-        d1.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    sparse_ms = t0.elapsed_time(t1) / K
-    dense_ms = d0.elapsed_time(d1) / Kd
-
-    # ---- the same steps captured once into CUDA graphs and replayed --------------------------
+    # ---- the same steps captured once into CUDA graphs (replayed inside the timed window) ------
     def graph_of(fn):
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
@@ -286,32 +305,55 @@ def run_psk(args):
         for _ in range(3):
             g_sparse.replay()
             g_dense.replay()
-        barrier()
-        r0 = torch.cuda.Event(enable_timing=True)
-        r1 = torch.cuda.Event(enable_timing=True)
-        r0.record(stream)
-        for _ in range(K):
-            g_sparse.replay()
-        r1.record(stream)
-        r2 = torch.cuda.Event(enable_timing=True)
-        r2.record(stream)
-        for _ in range(Kd):
-            g_dense.replay()
-        r3 = torch.cuda.Event(enable_timing=True)
-        r3.record(stream)
         torch.cuda.synchronize()
-        graph_sparse_ms = r0.elapsed_time(r1) / K
-        graph_dense_ms = r2.elapsed_time(r3) / Kd
     except Exception as exc:  # capture not possible here: report eager numbers only
         print(f"graph capture failed: {exc}", file=sys.stderr)
-        graph_sparse_ms = graph_dense_ms = float('nan')
+        g_sparse = g_dense = None
+
+    # ---- timed region: eager steps with per-kernel events, dense steps, graph replays ----------
+    K = args.steps
+    Kd = max(3, K // 4)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    barrier()
+    with Clocks(local) as clk:
+        marks[0].record(stream)
+        for k in range(K):
+            e = ev[k]
+            e[0].record(stream)
+            append()
+            e[1].record(stream)
+            score()
+            e[2].record(stream)
+            decode()
+            e[3].record(stream)
+        marks[1].record(stream)
+        for _ in range(Kd):
+            append(); dense()
+        marks[2].record(stream)
+        if g_sparse is not None:
+            marks[3].record(stream)
+            for _ in range(K):
+                g_sparse.replay()
+            marks[4].record(stream)
+            for _ in range(Kd):
+                g_dense.replay()
+            marks[5].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    sparse_ms = marks[0].elapsed_time(marks[1]) / K
+    dense_ms = marks[1].elapsed_time(marks[2]) / Kd
+    if g_sparse is not None:
+        graph_sparse_ms = marks[3].elapsed_time(marks[4]) / K
+        graph_dense_ms = marks[4].elapsed_time(marks[5]) / Kd
+    else:
+        graph_sparse_ms = graph_dense_ms = float("nan")
     t_app = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
     t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
     t_dec = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
     if dist is not None:
-        tt = torch.tensor([sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = tt.tolist()
+        sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = max_over_ranks(
+            [sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], dev)
 
     # ---- end to end: host buffers through the C ABI (pinned H2D of the step's inputs, D2H of out)
     qh = to_torch(q_host, w.dtype).pin_memory()
@@ -358,42 +400,63 @@ def run_psk(args):
     decode_bytes = kv_bytes + q_bytes + out_bytes
     step_bytes = summ_bytes + kv_bytes + q_bytes + out_bytes
     dense_bytes = int(lens.sum()) * Hkv * kv_row * es + q_bytes + out_bytes
-    peak, peak_kind = peaks()
+    pk = peaks()
+    peak_hbm = pk["hbm"]
+    flops_decode = 2 * Hq * (D + w.D_v) * sel_tokens  # QK^T and P.V over the selected tokens
     if t_score >= t_dec:
-        dom, dom_bytes, dom_ms = "score_select_kernel", score_bytes, t_score
+        dom = ("mla_qsplit_kernel+mla_score_kernel+page_select_kernel" if w.latent
+               else "page_score_kernel+page_select_kernel")
+        roof = {"bound": "hbm", "kernel": dom, "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
+                "unit": "GB/s", "algorithmic_per_launch": score_bytes, "algorithmic_unit": "B",
+                "launch_us": t_score * 1e3}
+    elif w.latent:
+        # arithmetic intensity ~300 flop/B, above the measured ridge (~250-290): tensor-bound
+        dom = "mla_decode_kernel"
+        roof = {"bound": "tensor", "kernel": dom, "achieved": flops_decode / (t_dec * 1e-3) / 1e12,
+                "peak": pk["bf16_sustained"], "unit": "TFLOP/s", "algorithmic_per_launch": flops_decode,
+                "algorithmic_unit": "flop", "launch_us": t_dec * 1e3,
+                "hbm": {"bytes": decode_bytes, "gbs": decode_bytes / (t_dec * 1e-3) / 1e9, "peak": peak_hbm}}
     else:
-        dom, dom_bytes, dom_ms = "decode_split_kernel+combine_kernel", decode_bytes, t_dec
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        dom = "decode_split_kernel"
+        roof = {"bound": "hbm", "kernel": dom, "achieved": decode_bytes / (t_dec * 1e-3) / 1e9, "peak": peak_hbm,
+                "unit": "GB/s", "algorithmic_per_launch": decode_bytes, "algorithmic_unit": "B",
+                "launch_us": t_dec * 1e3}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_kind"] = pk["kind"] + (" sustained bf16" if roof["bound"] == "tensor" else " copy")
+    roof["traffic"] = traffic_of(w.name, dom)
+    roof["traffic_digest"] = kernel_digest(dom)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, nseq = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": secs * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{nseq} of {B} sequences through the fp64 oracle's sparse step (score all pages, select, "
-                         f"attend), scaled to the full batch; single thread"}
+                         f"attend), scaled to the full batch by pages; single thread"}
 
     clocks = clk.summary()
-    us = sparse_ms * 1e3
+    graphed = graph_sparse_ms == graph_sparse_ms
+    step_ms = graph_sparse_ms if graphed else sparse_ms
+    step_dense_ms = graph_dense_ms if graphed else dense_ms
+    us = step_ms * 1e3
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": sparse_ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H_q": Hq, "H_kv": Hkv, "D": D, "page_size": w.page_size,
                    "contexts": "U[8192, 65536] seeded" if args.workload == 3 else [int(x) for x in lens[:4]],
                    "budget_pages_total": int(w.budgets.sum()), "l2": "inputs larger than L2, no flush",
+                   "timing": ("CUDA-graph replay of the step's launches" if graphed else "eager launches")
+                             + "; CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
-                     "algorithmic_bytes_per_launch": dom_bytes, "launch_us": dom_ms * 1e3},
-        "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / (sparse_ms * 1e-3) / 1e9,
-                     "frac_of_measured": step_bytes / (sparse_ms * 1e-3) / 1e9 / peak,
-                     "frac_of_8TBs": step_bytes / (sparse_ms * 1e-3) / 1e9 / 8000.0},
-        "dense": {"us_per_step": dense_ms * 1e3, "bytes": dense_bytes,
-                  "gbs": dense_bytes / (dense_ms * 1e-3) / 1e9},
-        "speedup_vs_dense": dense_ms / sparse_ms,
-        "graph": None if graph_sparse_ms != graph_sparse_ms else {
-            "us_per_step": graph_sparse_ms * 1e3, "dense_us_per_step": graph_dense_ms * 1e3,
-            "speedup_vs_dense": graph_dense_ms / graph_sparse_ms},
+        "roofline": roof,
+        "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+                     "frac_of_measured": step_bytes / (step_ms * 1e-3) / 1e9 / peak_hbm,
+                     "frac_of_8TBs": step_bytes / (step_ms * 1e-3) / 1e9 / 8000.0},
+        "dense": {"us_per_step": step_dense_ms * 1e3, "bytes": dense_bytes,
+                  "gbs": dense_bytes / (step_dense_ms * 1e-3) / 1e9},
+        "speedup_vs_dense": step_dense_ms / step_ms,
+        "eager": {"us_per_step": sparse_ms * 1e3, "dense_us_per_step": dense_ms * 1e3,
+                  "speedup_vs_dense": dense_ms / sparse_ms},
         "kernels_us": {"append": t_app * 1e3, "score_select": t_score * 1e3, "sparse_decode": t_dec * 1e3},
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
