@@ -253,6 +253,7 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
 constexpr int kStages = 3;
 constexpr int kStageBytes = 32768;
 constexpr int kMaxStagePages = 32;
+constexpr int kPageSteps = 2;  // page steps per loop iteration
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
@@ -347,22 +348,22 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
     const unsigned char *stage = smem_raw + (size_t)slot * kStageBytes;
     const int pb = p0 + st * sp;
     const int np = min(sp, p1 - pb);
-    // two page steps per iteration (both steps' loads first, then two independent chains).
+    // kPageSteps page steps per iteration (all steps' loads first, then independent chains).
     // Loads are unconditional (always inside the stage); pages that are not live (past the
     // chunk, or a flagged block) are dropped when the key is written.
     const uint32_t stage_addr = smem_u32(stage) + lane_off;
-    for (int j0 = wg * PPW; j0 < np; j0 += 2 * ng * PPW) {  // warp-uniform bound
-      uint4 lo[2], hi[2];
+    for (int j0 = wg * PPW; j0 < np; j0 += kPageSteps * ng * PPW) {  // warp-uniform bound
+      uint4 lo[kPageSteps], hi[kPageSteps];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kPageSteps; ++u) {
         const int jl = min(j0 + u * ng * PPW + grp, sp - 1);  // stays inside the stage
         const uint32_t addr = stage_addr + (uint32_t)jl * (uint32_t)group_bytes;
         lo[u] = lds128(addr);
         hi[u] = lds128(addr + D * ES);
       }
-      float v[2][G];
+      float v[kPageSteps][G];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kPageSteps; ++u) {
         float2 kl[EPC / 2], kh[EPC / 2];
         Elem<T>::to_f2(lo[u], kl);
         Elem<T>::to_f2(hi[u], kh);
@@ -378,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kPageSteps; ++u) {
         const int jb = j0 + u * ng * PPW;
-        if (u == 1 && jb >= np) break;  // warp-uniform
+        if (u > 0 && jb >= np) break;  // warp-uniform
         const float sc = group_score<G, LPP>(v[u], lane) * a.scale;
         const int j = jb + grp;
         if (sub == 0 && j < np) {
