@@ -56,7 +56,14 @@ def peaks():
 # (dram__bytes_read.sum + dram__bytes_write.sum, summed over its kernels), keyed by workload and
 # call, with a digest of the sources the kernels are built from: a digest that no longer matches
 # means the kernels changed since the capture, and the traffic is reported as null.
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
+    #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
+    ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel+page_select_kernel"):
+        {"bytes": 578_190_000 + 6_740_000 + 4_630_000, "digest": "e966b3830c744db3"},
+    ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
+        {"bytes": 467_000_000 + 1_960_000, "digest": "a32daa4d8a55dc09"},
+}
 KERNEL_SOURCES = {
     "page_score_kernel+page_select_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
     "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),

@@ -14,14 +14,17 @@
 // one thread's columns. Operands are staged per 64-element K block by cp.async with the
 // 128-byte swizzle into a 3-stage ring; tcgen05.commit on a per-stage mbarrier frees a stage.
 //
-// Decode: one CTA per (split of the page list, half of the value dims, sequence). Q (128 x 576)
-// stays in shared memory (TMA, 128-byte swizzle); K tiles of 32 tokens x 576 stream through a
-// double buffer (TMA). Per tile: S = Q K^T (M = 128 heads, N = 32 tokens) into tensor memory;
-// each thread owns one head's row: online softmax in fp32 (log2 domain), P written as bf16 to
-// shared memory (64-byte swizzle); O += P V (N = 256 value dims, V read MN-major straight out
-// of the same K tile) accumulates in tensor memory. O needs 256 of the 512 tensor-memory
-// columns per half of the value dims, hence the split of D_v across two CTAs (each recomputes
-// S). Splits are merged by log-sum-exp by the last CTA of each (sequence, half).
+// Decode: one CTA per (split of the page list, half of the value dims, sequence). O for 128
+// heads x 256 value dims fills 256 of the 512 tensor-memory columns, hence the split of D_v
+// across two CTAs (each computes S itself). Q dims 0..383 live in tensor memory as the A
+// operand of S = Q K^T (192 columns), dims 384..575 in shared memory (TMA, 128-byte swizzle);
+// K tiles of 32 tokens x 576 stream through a 4-stage TMA ring. Per tile: S (M = 128 heads,
+// N = 32 tokens) into one of two tensor-memory buffers; each softmax thread owns one head's
+// row: online softmax in fp32 (log2 domain), P written as bf16 to shared memory (64-byte
+// swizzle, two buffers); O += P V (N = 256 value dims, V read MN-major straight out of the K
+// tile) accumulates in tensor memory. A fifth warp issues the TMA copies and the MMAs, S of the
+// next tile ahead of P.V of this one. Splits are merged by log-sum-exp by the last CTA of each
+// (sequence, half).
 #include <algorithm>
 
 #include "psk_common.cuh"
@@ -57,6 +60,14 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The same with A read from tensor memory (a_tmem: lane 0, first column of the K step; M = 128
+// rows on the 128 lanes, two bf16 per 32-bit column).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -213,24 +224,42 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
 // decode
 // ------------------------------------------------------------------------------------
 constexpr int kTok = 32;                        // tokens per tile
-constexpr int kQBytes = kKB * kHeads * 128;     // 147456: Q as 9 swizzled [128 x 64] blocks
+constexpr int kQTmemKB = 6;                     // K blocks of Q held in tensor memory (dims 0..383)
+constexpr int kQSmemKB = kKB - kQTmemKB;        // K blocks of Q in shared memory (dims 384..575)
+constexpr int kQSBytes = kQSmemKB * kHeads * 128;  // 49152: 3 swizzled [128 x 64] blocks
 constexpr int kKTile = kKB * kTok * 128;        // 36864: a K tile as 9 swizzled [32 x 64] blocks
+constexpr int kKStages = 4;                     // K tiles in flight
 constexpr int kPBytes = kHeads * kTok * 2;      // 8192: P [128 x 32] bf16, 64-byte swizzle
-constexpr int kDecSmem = 1024 + kQBytes + 2 * kKTile + kPBytes;
+constexpr int kDecSmem = 1024 + kQSBytes + kKStages * kKTile + 2 * kPBytes;
+constexpr int kDecThreads = 160;                // 4 softmax warps (one thread per head) + 1 issuing warp
 constexpr int kMlaMaxSw = 128;                  // pages per split
 constexpr int kMlaMaxItems = 128;               // splits per (sequence, half); their merge weights fit the K stages
-static_assert(kMlaMaxItems * kHeads * 4 <= 2 * kKTile, "merge weights must fit the K stages");
-constexpr uint32_t kOCol = 0, kSCol = 256;      // tensor-memory columns of O and S
+static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKTile, "merge weights must fit the K stages");
+// tensor-memory columns: O (128 x 256 fp32), two S buffers (128 x 32 fp32), Q dims 0..383 as
+// bf16 pairs (192 columns)
+constexpr uint32_t kOCol = 0, kSCol = 256, kQCol = 320;
+static_assert(kQCol + kQTmemKB * 32 == 512, "tensor-memory budget");
 constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is rescaled
 
-__global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
-                                                           const __grid_constant__ CUtensorMap tmK) {
+// One CTA per (split, half of D_v, sequence); warps 0-3 own one query head per thread (the
+// tensor-memory lanes), warp 4's lane 0 issues every TMA copy and every MMA. The tile pipeline:
+//   K(t)  : TMA into stage t % 4                 (kfull[t % 4]; freed by the commit after P.V(t))
+//   S(t)  = Q K(t)^T into S buffer t % 2         (A = Q from tensor memory for dims 0..383 and
+//                                                 from shared memory for 384..575; sfull[t % 2])
+//   P(t)  : softmax warps read S(t) (sfree), write P(t) to buffer t % 2 (pready[t % 2])
+//   O    += P(t) V(t)                            (V = the first 512 dims of K(t), MN-major;
+//                                                 pvdone[t % 2])
+// S(t+1) is issued before P.V(t), so the tensor cores compute the next tile's logits while the
+// softmax warps work on this one; up to four K tiles are in flight.
+__global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
+                                                                   const __grid_constant__ CUtensorMap tmK) {
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
-  unsigned char *sQ = base;
-  unsigned char *sK = base + kQBytes;
-  unsigned char *sP = sK + 2 * kKTile;
-  __shared__ __align__(8) uint64_t qbar, kbar[2], sbar, obar;
+  unsigned char *sQ = base;                    // Q dims 384..575
+  unsigned char *sK = base + kQSBytes;         // kKStages K tiles
+  unsigned char *sP = sK + kKStages * kKTile;  // two P buffers
+  __shared__ __align__(8) uint64_t qbar, kfull[kKStages], kempty[kKStages], sfull[2], sfree[2], pready[2], pvdone[2], drained;
+  __shared__ int abort_sh;  // set by the first wait that gives up: every later wait returns at once
   __shared__ uint32_t tslot;
   __shared__ int ent_blk[kMlaMaxSw], ent_valid[kMlaMaxSw];
   __shared__ short tiles[2 * kMlaMaxSw];
@@ -238,7 +267,7 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
   __shared__ int flag_last;
 
   const int s = blockIdx.x, vh = blockIdx.y, i = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = i * 2 + vh;
   const size_t pbase = (size_t)unit * a.n_items_max + s;
   const int seq_len = a.seq_lens[i];
@@ -254,7 +283,7 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
   } else if (e0 < P) {
     n_ent = min(a.sw, P - e0);
   }
-  for (int x = tid; x < n_ent; x += 128) {
+  for (int x = tid; x < n_ent; x += kDecThreads) {
     int pg = e0 + x, blk = -1;
     bool ok = true;
     if (a.selected) {
@@ -279,10 +308,18 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
   }
   if (tid == 0) {
     mbar_init(smem_u32(&qbar), 1);
-    mbar_init(smem_u32(&kbar[0]), 1);
-    mbar_init(smem_u32(&kbar[1]), 1);
-    mbar_init(smem_u32(&sbar), 1);
-    mbar_init(smem_u32(&obar), 1);
+    mbar_init(smem_u32(&drained), 1);
+    abort_sh = 0;
+    for (int k = 0; k < kKStages; ++k) {
+      mbar_init(smem_u32(&kfull[k]), 1);
+      mbar_init(smem_u32(&kempty[k]), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&sfull[k]), 1);
+      mbar_init(smem_u32(&sfree[k]), 4);
+      mbar_init(smem_u32(&pready[k]), 4);
+      mbar_init(smem_u32(&pvdone[k]), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(smem_u32(&tslot), 512);
@@ -295,57 +332,121 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
       for (int hh = 0; hh * kTok < ent_valid[e]; ++hh) tiles[n++] = (short)(e * 2 + hh);
     n_tiles_sh = n;
   }
-  __syncthreads();
   const uint32_t tmem = tslot;
-  const int n_tiles = n_tiles_sh;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  float m_run = -INFINITY, l_run = 0.f;
-  const float qs = a.scale * kLog2e;
-
-  auto issue_tile = [&](int t) {  // thread 0 only
-    const int st = t & 1;
-    const int e = tiles[t] >> 1, hh = tiles[t] & 1;
-    const int row0 = ent_blk[e] * a.ps + hh * kTok;
-    const uint32_t bar = smem_u32(&kbar[st]);
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, kKTile);
-    const uint32_t dst = smem_u32(sK + st * kKTile);
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  if (warp < 4 && n_ent > 0) {  // Q dims 0..383 of head `tid` into tensor memory (bf16 pairs)
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) +
+                                                        ((size_t)i * kHeads + tid) * kD);
 #pragma unroll 1
-    for (int kb = 0; kb < kKB; ++kb) tma_load_2d(dst + kb * kTok * 128, &tmK, kb * 64, row0, bar);
+    for (int c = 0; c < kQTmemKB; ++c) {
+      uint32_t w[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 v = __ldg(qrow + c * 8 + j);
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_base + kQCol + c * 32, w);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int n_tiles = n_tiles_sh;
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) -> bool {
+    if (*reinterpret_cast<volatile int *>(&abort_sh)) return false;
+    if (mbar_wait(smem_u32(bar), parity, a.ws)) return true;
+    *reinterpret_cast<volatile int *>(&abort_sh) = 1;
+    return false;
   };
 
-  if (n_tiles > 0) {
-    if (tid == 0) {
-      mbar_arrive_expect_tx(smem_u32(&qbar), kQBytes);
+  if (warp == 4) {
+    // ---------------- issuing thread: TMA copies and MMAs ----------------
+    if (lane == 0 && n_tiles > 0) {
+      int n_loaded = 0, n_waited = 0;  // K tiles issued / K tiles whose arrival was observed
+      auto load_tile = [&](int t) {
+        const int st = t % kKStages;
+        const int e = tiles[t] >> 1, hh = tiles[t] & 1;
+        const int row0 = ent_blk[e] * a.ps + hh * kTok;
+        const uint32_t bar = smem_u32(&kfull[st]);
+        mbar_arrive_expect_tx(bar, kKTile);
+        const uint32_t dst = smem_u32(sK + st * kKTile);
 #pragma unroll 1
-      for (int kb = 0; kb < kKB; ++kb) tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, kb * 64, i * kHeads, smem_u32(&qbar));
-      issue_tile(0);
-      if (n_tiles > 1) issue_tile(1);
-    }
-    mbar_wait(smem_u32(&qbar), 0, a.ws);
-    const uint32_t idesc_qk = umma_idesc(128, kTok, false);
-    const uint32_t idesc_pv = umma_idesc(128, 256, true);
-    // thread 0: S = Q K^T of tile t once its K tile has landed
-    auto issue_qk = [&](int t) {
-      const int st = t & 1;
-      mbar_wait(smem_u32(&kbar[st]), (t >> 1) & 1, a.ws);
-      tc_fence_after();
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * kKTile);
+        for (int kb = 0; kb < kKB; ++kb) tma_load_2d(dst + kb * kTok * 128, &tmK, kb * 64, row0, bar);
+        n_loaded = t + 1;
+      };
+      mbar_arrive_expect_tx(smem_u32(&qbar), kQSBytes);
 #pragma unroll 1
-      for (int kb = 0; kb < kKB; ++kb)
+      for (int kb = 0; kb < kQSmemKB; ++kb)
+        tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, (kQTmemKB + kb) * 64, i * kHeads, smem_u32(&qbar));
+      for (int t = 0; t < kKStages && t < n_tiles; ++t) load_tile(t);
+      bool ok = wait_ok(&qbar, 0);
+      const uint32_t idesc_qk = umma_idesc(128, kTok, false);
+      const uint32_t idesc_pv = umma_idesc(128, 256, true);
+      auto issue_qk = [&](int u) -> bool {
+        const int st = u % kKStages, sb = u & 1;
+        if (!wait_ok(&kfull[st], (u / kKStages) & 1)) return false;
+        n_waited = u + 1;
+        if (u >= 2 && !wait_ok(&sfree[sb], ((u >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + kSCol + sb * kTok;
+        const uint32_t k0 = smem_u32(sK + st * kKTile), q0 = smem_u32(sQ);
+#pragma unroll 1
+        for (int kb = 0; kb < kKB; ++kb)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + kSCol, umma_desc(q0 + kb * kHeads * 128 + ks * 32, 16, 1024, 2),
-                    umma_desc(k0 + kb * kTok * 128 + ks * 32, 16, 1024, 2), idesc_qk, (kb | ks) != 0);
-      umma_commit(smem_u32(&sbar));
-    };
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bdesc = umma_desc(k0 + kb * kTok * 128 + ks * 32, 16, 1024, 2);
+            if (kb < kQTmemKB)
+              umma_bf16_ts(d, tmem + kQCol + kb * 32 + ks * 8, bdesc, idesc_qk, (kb | ks) != 0);
+            else
+              umma_bf16(d, umma_desc(q0 + (kb - kQTmemKB) * kHeads * 128 + ks * 32, 16, 1024, 2), bdesc, idesc_qk, 1);
+          }
+        umma_commit(smem_u32(&sfull[sb]));
+        return true;
+      };
+      ok = ok && issue_qk(0);
+#pragma unroll 1
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        if (t >= 1 && t + kKStages - 1 < n_tiles) {  // refill the stage P.V(t-1) has released
+          if (!wait_ok(&kempty[(t - 1) % kKStages], ((t - 1) / kKStages) & 1)) break;
+          load_tile(t + kKStages - 1);
+        }
+        if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
+        const int sb = t & 1;
+        if (!wait_ok(&pready[sb], (t >> 1) & 1)) break;
+        tc_fence_after();
+        const uint32_t p0a = smem_u32(sP + sb * kPBytes);
+        const uint32_t v0 = smem_u32(sK + (t % kKStages) * kKTile + vh * 4 * kTok * 128);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 512, 4), umma_desc(v0 + ks * 16 * 128, kTok * 128, 1024, 2),
+                    idesc_pv, (t | ks) != 0);
+        umma_commit(smem_u32(&pvdone[sb]));
+        umma_commit(smem_u32(&kempty[t % kKStages]));
+      }
+      // Drain before tensor memory and shared memory are released, also after a wait gave up:
+      // every MMA this thread issued (one commit tracks them all) and every K copy in flight.
+      umma_commit(smem_u32(&drained));
+      mbar_wait(smem_u32(&drained), 0, a.ws);
+      for (int t = n_waited; t < n_loaded; ++t) mbar_wait(smem_u32(&kfull[t % kKStages]), (t / kKStages) & 1, a.ws);
+      if (!ok) mbar_wait(smem_u32(&qbar), 0, a.ws);
+    }
+  } else if (n_tiles > 0) {
+    // ---------------- softmax warps: one query head per thread ----------------
+    float m_run = -INFINITY, l_run = 0.f;
+    const float qs = a.scale * kLog2e;
+#pragma unroll 1
     for (int t = 0; t < n_tiles; ++t) {
-      const int st = t & 1;
-      if (t == 0 && tid == 0) issue_qk(0);  // later tiles' QK is issued right after the previous P.V
-      mbar_wait(smem_u32(&sbar), t & 1, a.ws);
+      const int sb = t & 1;
+      if (!__all_sync(0xffffffffu, wait_ok(&sfull[sb], (t >> 1) & 1))) break;  // warp-uniform exit
       tc_fence_after();
       uint32_t sv[32];
-      tmem_ld32(tmem + lane_base + kSCol, sv);
+      tmem_ld32(tmem + lane_base + kSCol + sb * kTok, sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sfree[sb]));
       const int e = tiles[t] >> 1, hh = tiles[t] & 1;
       const int nv = min(kTok, ent_valid[e] - hh * kTok);
       float x[32];
@@ -355,17 +456,17 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
         x[j] = j < nv ? __uint_as_float(sv[j]) * qs : -INFINITY;
         mt = fmaxf(mt, x[j]);
       }
-      if (t > 0) mbar_wait(smem_u32(&obar), (t - 1) & 1, a.ws);  // P.V of tile t-1 done: P and O free
-      tc_fence_after();
       // The exponent reference m_run moves only when this head's max exceeds it by more than
       // kRescaleSlack (log2 units): p stays <= 2^kRescaleSlack, exact to fp32 rounding, and the
-      // normaliser l uses the same reference, so the result is unchanged while the costly
-      // rescale of O in tensor memory becomes rare. The tensor-memory loads and stores are
-      // warp-collective, so a warp rescales together (alpha = 1 on lanes that keep theirs).
+      // normaliser l uses the same reference, so the result is unchanged while the rescale of
+      // O in tensor memory becomes rare. Tensor-memory loads and stores are warp-collective, so
+      // a warp rescales together (alpha = 1 on lanes that keep their reference).
       const bool moved = t == 0 || mt > m_run + kRescaleSlack;
       const float m_new = moved ? fmaxf(m_run, mt) : m_run;
       const bool rescale = t > 0 && moved;
       if (__any_sync(0xffffffffu, rescale)) {
+        if (!__all_sync(0xffffffffu, wait_ok(&pvdone[(t - 1) & 1], ((t - 1) >> 1) & 1))) break;  // O holds P.V(t-1)
+        tc_fence_after();
         const float al = rescale ? exp2f(m_run - m_new) : 1.f;
         l_run *= al;
 #pragma unroll 1
@@ -385,30 +486,19 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
         l_run += p0 + p1;
         pw[j] = (uint32_t)f32_to_bf16_bits(p0) | ((uint32_t)f32_to_bf16_bits(p1) << 16);
       }
+      if (t >= 2 && !__all_sync(0xffffffffu, wait_ok(&pvdone[sb], ((t >> 1) - 1) & 1))) break;  // P.V(t-2) read buffer sb
       // P row r = tid: 4 chunks of 16 bytes, 64-byte swizzle
+      unsigned char *prow = sP + sb * kPBytes + tid * 64;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4 *>(sP + tid * 64 + ((c ^ ((tid >> 1) & 3)) * 16)) =
+        *reinterpret_cast<uint4 *>(prow + ((c ^ ((tid >> 1) & 3)) * 16)) =
             make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0) {
-        const uint32_t p0a = smem_u32(sP), v0 = smem_u32(sK + st * kKTile + vh * 4 * kTok * 128);
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 512, 4), umma_desc(v0 + ks * 16 * 128, kTok * 128, 1024, 2),
-                    idesc_pv, (t | ks) != 0);
-        umma_commit(smem_u32(&obar));
-        if (t + 1 < n_tiles) issue_qk(t + 1);  // queued behind P.V(t); S was read before the barrier above
-        if (t + 2 < n_tiles) {
-          mbar_wait(smem_u32(&obar), t & 1, a.ws);  // P.V has read this K tile
-          issue_tile(t + 2);
-        }
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pready[sb]));
     }
-    mbar_wait(smem_u32(&obar), (n_tiles - 1) & 1, a.ws);
+    __all_sync(0xffffffffu, wait_ok(&pvdone[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
     tc_fence_after();
     // partial O row (unnormalised) and (m, l) of head `tid`
     float *po = a.part_o + (pbase * kHeads + tid) * 256;
@@ -436,7 +526,7 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a, const 
   __syncthreads();
   if (tid == 0) flag_last = atomicAdd(a.tickets + unit, 1u) == (unsigned)(a.n_items_max - 1);
   __syncthreads();
-  if (!flag_last) return;
+  if (!flag_last || tid >= kHeads) return;
   __threadfence();
   if (tid == 0) a.tickets[unit] = 0u;
   const size_t it0 = (size_t)unit * a.n_items_max;
@@ -508,11 +598,21 @@ cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaSt
 
 bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   const long long units = (long long)L.batch * 2;
-  // one CTA per SM (shared memory) and one wave: at most 152 / units splits per (sequence, half)
-  int items = (int)std::max(1LL, 152 / units);
-  items = std::min(items, std::min(entries, kMlaMaxItems));
-  int sw = (entries + items - 1) / items;
-  sw = std::min(sw, kMlaMaxSw);
+  // One CTA per SM (shared memory). Pick the split width that minimises
+  //   waves * (pages per split + ~2 pages of fixed per-CTA cost) + ~0.5 page per split merged.
+  int sw = std::max(1, std::min(entries, kMlaMaxSw));
+  double best = 1e300;
+  for (int items = 1; items <= std::min(std::max(entries, 1), kMlaMaxItems); ++items) {
+    const int w = (std::max(entries, 1) + items - 1) / items;
+    if (w > kMlaMaxSw) continue;
+    const int n = (std::max(entries, 1) + w - 1) / w;
+    const long long waves = (units * n + 151) / 152;
+    const double cost = (double)waves * (w + 2.0) + 0.5 * n;
+    if (cost < best - 1e-9) {
+      best = cost;
+      sw = w;
+    }
+  }
   plan->sw = sw;
   plan->n_items_max = (entries + sw - 1) / sw;
   size_t off = ws_scratch_offset((size_t)units);
@@ -533,7 +633,7 @@ cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_items_max, 2, a.B);
-  mla_decode_kernel<<<grid, 128, kDecSmem, s>>>(a, tmQ, tmK);
+  mla_decode_kernel<<<grid, kDecThreads, kDecSmem, s>>>(a, tmQ, tmK);
   return cudaGetLastError();
 }
 
