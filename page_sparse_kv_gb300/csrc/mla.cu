@@ -223,47 +223,46 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
 // ------------------------------------------------------------------------------------
 // decode
 // ------------------------------------------------------------------------------------
-constexpr int kTok = 32;                        // tokens per tile
+constexpr int kHalf = 32;                       // tokens per TMA box (half a tile)
+constexpr int kTile = 64;                       // tokens per tile
 constexpr int kQTmemKB = 6;                     // K blocks of Q held in tensor memory (dims 0..383)
 constexpr int kQSmemKB = kKB - kQTmemKB;        // K blocks of Q in shared memory (dims 384..575)
 constexpr int kQSBytes = kQSmemKB * kHeads * 128;  // 49152: 3 swizzled [128 x 64] blocks
-constexpr int kKTile = kKB * kTok * 128;        // 36864: a K tile as 9 swizzled [32 x 64] blocks
-constexpr int kKStages = 4;                     // K tiles in flight
-constexpr int kPBytes = kHeads * kTok * 2;      // 8192: P [128 x 32] bf16, 64-byte swizzle
-constexpr int kDecSmem = 1024 + kQSBytes + kKStages * kKTile + 2 * kPBytes;
+constexpr int kKBlock = kTile * 128;            // 8192: one 64-dim block of a tile, 128-byte swizzle
+constexpr int kKTile = kKB * kKBlock;           // 73728: a K tile (64 tokens x 576)
+constexpr int kKStages = 2;
+constexpr int kPBytes = kHeads * kTile * 2;     // 16384: P [128 x 64] bf16, 128-byte swizzle
+constexpr int kDecSmem = 1024 + kQSBytes + kKStages * kKTile + kPBytes;
 constexpr int kDecThreads = 160;                // 4 softmax warps (one thread per head) + 1 issuing warp
 constexpr int kMlaMaxSw = 128;                  // pages per split
 constexpr int kMlaMaxItems = 128;               // splits per (sequence, half); their merge weights fit the K stages
 static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKTile, "merge weights must fit the K stages");
-// tensor-memory columns: O (128 x 256 fp32), two S buffers (128 x 32 fp32), Q dims 0..383 as
-// bf16 pairs (192 columns)
+// tensor-memory columns: O (128 x 256 fp32), S (128 x 64 fp32), Q dims 0..383 as bf16 pairs
 constexpr uint32_t kOCol = 0, kSCol = 256, kQCol = 320;
 static_assert(kQCol + kQTmemKB * 32 == 512, "tensor-memory budget");
 constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is rescaled
 
 // One CTA per (split, half of D_v, sequence); warps 0-3 own one query head per thread (the
-// tensor-memory lanes), warp 4's lane 0 issues every TMA copy and every MMA. The tile pipeline:
-//   K(t)  : TMA into stage t % 4                 (kfull[t % 4]; freed by the commit after P.V(t))
-//   S(t)  = Q K(t)^T into S buffer t % 2         (A = Q from tensor memory for dims 0..383 and
-//                                                 from shared memory for 384..575; sfull[t % 2])
-//   P(t)  : softmax warps read S(t) (sfree), write P(t) to buffer t % 2 (pready[t % 2])
-//   O    += P(t) V(t)                            (V = the first 512 dims of K(t), MN-major;
-//                                                 pvdone[t % 2])
-// S(t+1) is issued before P.V(t), so the tensor cores compute the next tile's logits while the
-// softmax warps work on this one; up to four K tiles are in flight.
+// tensor-memory lanes), warp 4's lane 0 issues every TMA copy and every MMA. A tcgen05.mma
+// costs about the same to issue whatever its N up to 256, so S uses 64-token tiles (N = 64):
+//   K(t)  : TMA (two 32-row boxes per 64-dim block) into stage t % 2   (kfull; freed after P.V(t))
+//   S(t)  = Q K(t)^T (A = Q from tensor memory for dims 0..383, from shared memory for the rest)
+//   P(t)  : softmax warps read S(t), rescale O when needed, write P(t)   (pready)
+//   O    += P(t) V(t)   (V = the first 512 dims of K(t), MN-major)        (pvdone)
+// in the order P.V(t), S(t+1), then the copy of K(t+2) into the stage P.V(t) released.
 __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK) {
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
   unsigned char *sQ = base;                    // Q dims 384..575
   unsigned char *sK = base + kQSBytes;         // kKStages K tiles
-  unsigned char *sP = sK + kKStages * kKTile;  // two P buffers
-  __shared__ __align__(8) uint64_t qbar, kfull[kKStages], kempty[kKStages], sfull[2], sfree[2], pready[2], pvdone[2], drained;
+  unsigned char *sP = sK + kKStages * kKTile;  // P
+  __shared__ __align__(8) uint64_t qbar, kfull[kKStages], kempty[kKStages], sfull, pready, pvdone, drained;
   __shared__ int abort_sh;  // set by the first wait that gives up: every later wait returns at once
   __shared__ uint32_t tslot;
   __shared__ int ent_blk[kMlaMaxSw], ent_valid[kMlaMaxSw];
-  __shared__ short tiles[2 * kMlaMaxSw];
-  __shared__ int n_tiles_sh;
+  __shared__ short halves[2 * kMlaMaxSw];  // (entry, 32-token half) pairs with at least one live row
+  __shared__ int n_halves_sh;
   __shared__ int flag_last;
 
   const int s = blockIdx.x, vh = blockIdx.y, i = blockIdx.z;
@@ -309,28 +308,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   if (tid == 0) {
     mbar_init(smem_u32(&qbar), 1);
     mbar_init(smem_u32(&drained), 1);
-    abort_sh = 0;
+    mbar_init(smem_u32(&sfull), 1);
+    mbar_init(smem_u32(&pready), 4);
+    mbar_init(smem_u32(&pvdone), 1);
     for (int k = 0; k < kKStages; ++k) {
       mbar_init(smem_u32(&kfull[k]), 1);
       mbar_init(smem_u32(&kempty[k]), 1);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&sfull[k]), 1);
-      mbar_init(smem_u32(&sfree[k]), 4);
-      mbar_init(smem_u32(&pready[k]), 4);
-      mbar_init(smem_u32(&pvdone[k]), 1);
-    }
+    abort_sh = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(smem_u32(&tslot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) {  // the tile list: (entry, 32-token half) pairs with at least one live row
+  if (tid == 0) {
     int n = 0;
     for (int e = 0; e < n_ent; ++e)
-      for (int hh = 0; hh * kTok < ent_valid[e]; ++hh) tiles[n++] = (short)(e * 2 + hh);
-    n_tiles_sh = n;
+      for (int hh = 0; hh * kHalf < ent_valid[e]; ++hh) halves[n++] = (short)(e * 2 + hh);
+    n_halves_sh = n;
   }
   const uint32_t tmem = tslot;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -354,7 +350,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int n_tiles = n_tiles_sh;
+  const int n_halves = n_halves_sh;
+  const int n_tiles = (n_halves + 1) / 2;
+  // live rows of the two halves of tile t (0 for a missing second half)
+  auto half_rows = [&](int hx) -> int {
+    if (hx >= n_halves) return 0;
+    const int e = halves[hx] >> 1, hh = halves[hx] & 1;
+    return min(kHalf, ent_valid[e] - hh * kHalf);
+  };
   auto wait_ok = [&](uint64_t *bar, uint32_t parity) -> bool {
     if (*reinterpret_cast<volatile int *>(&abort_sh)) return false;
     if (mbar_wait(smem_u32(bar), parity, a.ws)) return true;
@@ -368,13 +371,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       int n_loaded = 0, n_waited = 0;  // K tiles issued / K tiles whose arrival was observed
       auto load_tile = [&](int t) {
         const int st = t % kKStages;
-        const int e = tiles[t] >> 1, hh = tiles[t] & 1;
-        const int row0 = ent_blk[e] * a.ps + hh * kTok;
+        const int nh = (2 * t + 1 < n_halves) ? 2 : 1;
         const uint32_t bar = smem_u32(&kfull[st]);
-        mbar_arrive_expect_tx(bar, kKTile);
+        mbar_arrive_expect_tx(bar, (uint32_t)(nh * kKB * kHalf * 128));
         const uint32_t dst = smem_u32(sK + st * kKTile);
+        for (int h2 = 0; h2 < nh; ++h2) {
+          const int hx = 2 * t + h2;
+          const int e = halves[hx] >> 1, hh = halves[hx] & 1;
+          const int row0 = ent_blk[e] * a.ps + hh * kHalf;
 #pragma unroll 1
-        for (int kb = 0; kb < kKB; ++kb) tma_load_2d(dst + kb * kTok * 128, &tmK, kb * 64, row0, bar);
+          for (int kb = 0; kb < kKB; ++kb)
+            tma_load_2d(dst + kb * kKBlock + h2 * kHalf * 128, &tmK, kb * 64, row0, bar);
+        }
         n_loaded = t + 1;
       };
       mbar_arrive_expect_tx(smem_u32(&qbar), kQSBytes);
@@ -383,48 +391,46 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
         tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, (kQTmemKB + kb) * 64, i * kHeads, smem_u32(&qbar));
       for (int t = 0; t < kKStages && t < n_tiles; ++t) load_tile(t);
       bool ok = wait_ok(&qbar, 0);
-      const uint32_t idesc_qk = umma_idesc(128, kTok, false);
+      const uint32_t idesc_qk = umma_idesc(128, kTile, false);
       const uint32_t idesc_pv = umma_idesc(128, 256, true);
       auto issue_qk = [&](int u) -> bool {
-        const int st = u % kKStages, sb = u & 1;
+        const int st = u % kKStages;
         if (!wait_ok(&kfull[st], (u / kKStages) & 1)) return false;
         n_waited = u + 1;
-        if (u >= 2 && !wait_ok(&sfree[sb], ((u >> 1) - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + kSCol + sb * kTok;
+        const uint32_t d = tmem + kSCol;
         const uint32_t k0 = smem_u32(sK + st * kKTile), q0 = smem_u32(sQ);
 #pragma unroll 1
         for (int kb = 0; kb < kKB; ++kb)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bdesc = umma_desc(k0 + kb * kTok * 128 + ks * 32, 16, 1024, 2);
+            const uint64_t bdesc = umma_desc(k0 + kb * kKBlock + ks * 32, 16, 1024, 2);
             if (kb < kQTmemKB)
               umma_bf16_ts(d, tmem + kQCol + kb * 32 + ks * 8, bdesc, idesc_qk, (kb | ks) != 0);
             else
               umma_bf16(d, umma_desc(q0 + (kb - kQTmemKB) * kHeads * 128 + ks * 32, 16, 1024, 2), bdesc, idesc_qk, 1);
           }
-        umma_commit(smem_u32(&sfull[sb]));
+        umma_commit(smem_u32(&sfull));
         return true;
       };
       ok = ok && issue_qk(0);
 #pragma unroll 1
       for (int t = 0; ok && t < n_tiles; ++t) {
-        if (t >= 1 && t + kKStages - 1 < n_tiles) {  // refill the stage P.V(t-1) has released
-          if (!wait_ok(&kempty[(t - 1) % kKStages], ((t - 1) / kKStages) & 1)) break;
-          load_tile(t + kKStages - 1);
-        }
-        if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
-        const int sb = t & 1;
-        if (!wait_ok(&pready[sb], (t >> 1) & 1)) break;
+        if (!wait_ok(&pready, t & 1)) break;  // P(t) written, O rescaled, S(t) read
         tc_fence_after();
-        const uint32_t p0a = smem_u32(sP + sb * kPBytes);
-        const uint32_t v0 = smem_u32(sK + (t % kKStages) * kKTile + vh * 4 * kTok * 128);
+        const uint32_t p0a = smem_u32(sP);
+        const uint32_t v0 = smem_u32(sK + (t % kKStages) * kKTile + vh * 4 * kKBlock);
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 512, 4), umma_desc(v0 + ks * 16 * 128, kTok * 128, 1024, 2),
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 1024, 2), umma_desc(v0 + ks * 16 * 128, kKBlock, 1024, 2),
                     idesc_pv, (t | ks) != 0);
-        umma_commit(smem_u32(&pvdone[sb]));
+        umma_commit(smem_u32(&pvdone));
         umma_commit(smem_u32(&kempty[t % kKStages]));
+        if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
+        if (t + kKStages < n_tiles) {  // refill the stage P.V(t) releases
+          if (!wait_ok(&kempty[t % kKStages], (t / kKStages) & 1)) break;
+          load_tile(t + kKStages);
+        }
       }
       // Drain before tensor memory and shared memory are released, also after a wait gave up:
       // every MMA this thread issued (one commit tracks them all) and every K copy in flight.
@@ -439,23 +445,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
     const float qs = a.scale * kLog2e;
 #pragma unroll 1
     for (int t = 0; t < n_tiles; ++t) {
-      const int sb = t & 1;
-      if (!__all_sync(0xffffffffu, wait_ok(&sfull[sb], (t >> 1) & 1))) break;  // warp-uniform exit
+      if (!__all_sync(0xffffffffu, wait_ok(&sfull, t & 1))) break;  // warp-uniform exit
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + lane_base + kSCol + sb * kTok, sv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sfree[sb]));
-      const int e = tiles[t] >> 1, hh = tiles[t] & 1;
-      const int nv = min(kTok, ent_valid[e] - hh * kTok);
-      float x[32];
+      const int nva = half_rows(2 * t), nvb = half_rows(2 * t + 1);
+      float x[kTile];
       float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x[j] = j < nv ? __uint_as_float(sv[j]) * qs : -INFINITY;
-        mt = fmaxf(mt, x[j]);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + kSCol + c * 32, sv);
+        const int nv = c == 0 ? nva : nvb;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[c * 32 + j] = j < nv ? __uint_as_float(sv[j]) * qs : -INFINITY;
+          mt = fmaxf(mt, x[c * 32 + j]);
+        }
       }
+      // O holds P.V(t-1) and P is free once pvdone completes for t-1
+      if (t > 0 && !__all_sync(0xffffffffu, wait_ok(&pvdone, (t - 1) & 1))) break;
+      tc_fence_after();
       // The exponent reference m_run moves only when this head's max exceeds it by more than
       // kRescaleSlack (log2 units): p stays <= 2^kRescaleSlack, exact to fp32 rounding, and the
       // normaliser l uses the same reference, so the result is unchanged while the rescale of
@@ -465,8 +473,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       const float m_new = moved ? fmaxf(m_run, mt) : m_run;
       const bool rescale = t > 0 && moved;
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!__all_sync(0xffffffffu, wait_ok(&pvdone[(t - 1) & 1], ((t - 1) >> 1) & 1))) break;  // O holds P.V(t-1)
-        tc_fence_after();
         const float al = rescale ? exp2f(m_run - m_new) : 1.f;
         l_run *= al;
 #pragma unroll 1
@@ -479,26 +485,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
         }
       }
       m_run = m_new;
-      uint32_t pw[16];
+      // P row r = tid: 8 chunks of 16 bytes, 128-byte swizzle
+      unsigned char *prow = sP + tid * 128;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float p0 = exp2f(x[2 * j] - m_run), p1 = exp2f(x[2 * j + 1] - m_run);
-        l_run += p0 + p1;
-        pw[j] = (uint32_t)f32_to_bf16_bits(p0) | ((uint32_t)f32_to_bf16_bits(p1) << 16);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t pw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p0 = exp2f(x[c * 8 + 2 * j] - m_run), p1 = exp2f(x[c * 8 + 2 * j + 1] - m_run);
+          l_run += p0 + p1;
+          pw[j] = (uint32_t)f32_to_bf16_bits(p0) | ((uint32_t)f32_to_bf16_bits(p1) << 16);
+        }
+        *reinterpret_cast<uint4 *>(prow + ((c ^ (tid & 7)) * 16)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       }
-      if (t >= 2 && !__all_sync(0xffffffffu, wait_ok(&pvdone[sb], ((t >> 1) - 1) & 1))) break;  // P.V(t-2) read buffer sb
-      // P row r = tid: 4 chunks of 16 bytes, 64-byte swizzle
-      unsigned char *prow = sP + sb * kPBytes + tid * 64;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4 *>(prow + ((c ^ ((tid >> 1) & 3)) * 16)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      // Rows past the live tokens (the tail page past seq_len, or a missing second half) hold
+      // whatever the stage last received; their P is 0, but 0 * NaN is NaN, so the value rows
+      // this CTA multiplies are zeroed (128 bytes per row and 64-dim block).
+      if (nva < kHalf || nvb < kHalf) {
+        unsigned char *vblk = sK + (t % kKStages) * kKTile + vh * 4 * kKBlock;
+        for (int x2 = tid; x2 < 4 * kTile * 8; x2 += kHeads) {
+          const int kb = x2 / (kTile * 8), r = (x2 / 8) % kTile, c = x2 % 8;
+          const bool live = r < kHalf ? r < nva : (r - kHalf) < nvb;
+          if (!live) *reinterpret_cast<uint4 *>(vblk + kb * kKBlock + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&pready[sb]));
+      if (lane == 0) mbar_arrive(smem_u32(&pready));
     }
-    __all_sync(0xffffffffu, wait_ok(&pvdone[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
+    __all_sync(0xffffffffu, wait_ok(&pvdone, (n_tiles - 1) & 1));
     tc_fence_after();
     // partial O row (unnormalised) and (m, l) of head `tid`
     float *po = a.part_o + (pbase * kHeads + tid) * 256;
@@ -628,7 +644,7 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
   CUtensorMap tmQ, tmK;
   if (!encode_matrix_map_sw128(&tmQ, a.q, kD, (long long)a.B * kHeads, 64, kHeads) ||
-      !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kTok))
+      !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kHalf))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;

@@ -189,6 +189,33 @@ def test_nan_junk_past_seq_len_is_never_read():
     _run_and_check(w, cache, [0, 1], summ, w.queries(), step_tag="nan junk")
 
 
+def _custom_mla(seq_lens, budgets, ps=64, seed=11):
+    return W.Workload("custom-mla", seed, "bf16", B=len(seq_lens), H_q=128, H_kv=1, D=576, D_v=512, page_size=ps,
+                      seq_lens=seq_lens, budgets=budgets, n_hot=2, hot_rule="random", latent=True, pool_slack=3)
+
+
+@pytest.mark.parametrize("case", [
+    dict(seq_lens=[64 * 3 + 5, 17, 64 * 20], budgets=[2, 2, 5], ps=64),      # one-page and odd-half tails
+    dict(seq_lens=[32 * 41 + 3, 32 * 7, 9], budgets=[5, 4, 2], ps=32),       # 32-token pages, odd page counts
+    dict(seq_lens=[64 * 40 + 33, 64 * 9], budgets=[40, 9], ps=64),           # b >= P and b = P
+])
+def test_mla_edge_cases(case):
+    w = _custom_mla(**case)
+    cache = upload(w)
+    seqs = list(range(w.B))
+    summ = _check_cache_and_summaries(w, cache, seqs)
+    _run_and_check(w, cache, seqs, summ, w.queries(), step_tag="mla " + str(case))
+
+
+@pytest.mark.parametrize("ps", [32, 64])
+def test_mla_nan_junk_past_seq_len_is_never_read(ps):
+    """The latent decode multiplies whole 32-row boxes: the rows past seq_len must not reach O."""
+    w = _custom_mla([ps * 5 + 3, ps * 9 + ps - 1, ps * 2 + 1], [3, 4, 2], ps=ps)
+    cache = upload(w, junk=float("nan"))
+    summ = _check_cache_and_summaries(w, cache, [0, 1, 2])
+    _run_and_check(w, cache, [0, 1, 2], summ, w.queries(), step_tag=f"mla nan junk ps {ps}")
+
+
 def test_ties_resolve_to_lower_page():
     """Pages with identical keys (hence identical summaries and scores) tie; with the cutoff
     inside the tied group the lowest-indexed tied pages win."""
