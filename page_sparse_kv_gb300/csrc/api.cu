@@ -225,6 +225,8 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.b_max = dense ? L.max_pages : b_max;
   a.sw = plan.sw;
   a.n_items_max = plan.n_items_max;
+  a.flat = plan.flat;
+  a.counts = reinterpret_cast<int32_t *>(ws + plan.off_counts);
   a.scale = scale;
   if (L.latent) return cuda_status(launch_mla_decode(a, static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_decode(a, L.dtype, static_cast<cudaStream_t>(stream)));

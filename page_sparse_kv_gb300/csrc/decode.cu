@@ -26,6 +26,7 @@
 // unit's partials by log-sum-exp with all its threads and writes the G output rows.
 #include <algorithm>
 #include <cstdlib>
+#include <string>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
@@ -36,6 +37,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSwMax = 256;    // list entries per split, upper bound
 constexpr int kMaxItems = 256; // splits per (sequence, KV head), upper bound (bounds the merge)
+constexpr int kFlatMaxCtas = 2048;   // grid of the flat layout, upper bound (sizes the partials)
+constexpr int kFlatMaxUnits = 4096;  // units the flat layout takes (its prefix sums live in shared memory)
+constexpr long long kFlatMinShare = 8;  // list entries per CTA of the flat layout, lower bound
 
 template <typename T, int D, int G, int NW, int NST>
 struct DT {
@@ -84,14 +88,13 @@ __device__ __forceinline__ void reduce_dg(float (&v)[NV], int lane) {
   }
 }
 
-// The last CTA of a unit: merge its n partials (m, l, O) by log-sum-exp into the G output rows.
+// The last CTA of a unit: merge its n partials (m, l, O) at slots it0 .. it0 + n - 1 by
+// log-sum-exp into the G output rows.
 // wsm: >= n * G floats of shared memory; red: >= 2 * G * NW floats.
 template <typename T, int D, int G, int NW>
-__device__ void merge_unit(const DecodeArgs &a, int unit, float *wsm, float *red) {
+__device__ void merge_unit(const DecodeArgs &a, int unit, size_t it0, int n, float *wsm, float *red) {
   constexpr int NT = NW * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = a.n_items_max;
-  const size_t it0 = (size_t)unit * n;
   // 1. per-head max of m over the partials
   float mx[G];
 #pragma unroll
@@ -162,44 +165,13 @@ __device__ void merge_unit(const DecodeArgs &a, int unit, float *wsm, float *red
   }
 }
 
-template <typename T, int D, int G, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
-                                                               const __grid_constant__ CUtensorMap tmV) {
-  using TR = DT<T, D, G, NW, NST>;
-  extern __shared__ __align__(128) unsigned char smem_dyn[];
-  unsigned char *stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
-  float2 *pp_all = reinterpret_cast<float2 *>(stages + TR::STAGES);
-  float *wML = reinterpret_cast<float *>(pp_all + NW * 16 * G);
-  int *ent_blk = reinterpret_cast<int *>(wML + NW * G * 2);
-  int *ent_valid = ent_blk + kSwMax;
-  float *wO = reinterpret_cast<float *>(stages);  // after the pipeline has drained
-  __shared__ __align__(8) uint64_t bars[NW][NST];
-  __shared__ int flag_last;
-
-  const int s = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
-  const int unit = i * a.H_kv + h;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tq = lane >> 3, dg = lane & 7;
-  const int seq_len = a.seq_lens[i];
-  const int P = (seq_len + a.ps - 1) / a.ps;
-  const int e0 = s * a.sw;
-  const size_t pbase = (size_t)unit * a.n_items_max + s;
-
-  // ---- entries of this split -------------------------------------------------------------
-  int n_ent = 0;
-  if (seq_len < 1 || P > a.max_pages) {
-    if (s == 0 && tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
-  } else if (a.selected) {
-    const int32_t *row = a.selected + (size_t)unit * a.b_max;
-    if (e0 < a.b_max && row[e0] >= 0) n_ent = min(a.sw, a.b_max - e0);
-  } else if (e0 < P) {
-    n_ent = min(a.sw, P - e0);
-  }
-  if (lane == 0) {
-    for (int k = 0; k < NST; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
-    fence_mbar_init();
-  }
-  for (int x = tid; x < n_ent; x += NW * 32) {
+// List entries [e0, e0 + n) of unit (i, h) (selected row, or pages e0.. when dense) into the
+// entry table: physical block and live rows (0 for padding and for flagged entries). All
+// threads of the CTA take part; the caller synchronises.
+template <int NT>
+__device__ void load_entries(const DecodeArgs &a, int i, int unit, int P, int seq_len, int e0, int n, int *ent_blk,
+                             int *ent_valid) {
+  for (int x = threadIdx.x; x < n; x += NT) {
     int p = e0 + x, blk = -1;
     bool ok = true;
     if (a.selected) {
@@ -222,25 +194,290 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
     ent_blk[x] = blk;
     ent_valid[x] = ok ? min(a.ps, seq_len - p * a.ps) : 0;
   }
+}
+
+// Query slices of this lane (chunks dg, dg + 8, ... of each of the G rows), scaled into the log2
+// domain.
+template <typename T, int D, int G, int NW, int NST>
+__device__ __forceinline__ void load_q(const DecodeArgs &a, int i, int h, int dg,
+                                       float2 (&q2)[G][DT<T, D, G, NW, NST>::CPL * DT<T, D, G, NW, NST>::EPC / 2]) {
+  using TR = DT<T, D, G, NW, NST>;
+  const T *qb = reinterpret_cast<const T *>(a.q) + ((size_t)i * a.H_q + (size_t)h * G) * D;
+  const float qs = a.scale * kLog2e;
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int c = 0; c < TR::CPL; ++c) {
+      float2 f[TR::EPC / 2];
+      Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(qb + (size_t)g * D + (dg + 8 * c) * TR::EPC), f);
+#pragma unroll
+      for (int e = 0; e < TR::EPC / 2; ++e) q2[g][c * TR::EPC / 2 + e] = make_float2(f[e].x * qs, f[e].y * qs);
+    }
+}
+
+// Streams the 16-token tiles of the n_ent entries in the entry table through this warp's TMA
+// ring (warp w takes tiles w, w + NW, ...) and folds them into the warp's (m, l, O). cw is the
+// warp's running tile count: ring stage and mbarrier phase carry on across calls.
+template <typename T, int D, int G, int NW, int NST>
+__device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMap *tmK, const CUtensorMap *tmV, int h,
+                                           const float2 (&q2)[G][DT<T, D, G, NW, NST>::CPL * DT<T, D, G, NW, NST>::EPC / 2],
+                                           const int *ent_blk, const int *ent_valid, int n_ent, unsigned char *stages,
+                                           float2 *pp_all, uint64_t (*bars)[NST], int &cw, float (&m)[G], float (&l)[G],
+                                           float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2]) {
+  using TR = DT<T, D, G, NW, NST>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tq = lane >> 3, dg = lane & 7;
+  const int stp = a.ps / 16;  // tiles per page
+  const int ntiles = n_ent * stp;
+  unsigned char *my_stages = stages + (size_t)warp * NST * TR::STAGE;
+  float2 *pp = pp_all + warp * 16 * G;
+  const int cw0 = cw;
+  auto tile_rows = [&](int it) -> int {
+    const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
+    return min(16, ent_valid[e] - sub * 16);
+  };
+  // lane 0 issues the K and V tile copies of the warp's k-th tile; a tile without rows still
+  // arrives (0 bytes) so every stage's phases stay in step.
+  auto issue = [&](int k) {
+    const int it = warp + k * NW;
+    if (it >= ntiles) return;
+    if (lane == 0) {
+      const int stg = (cw0 + k) % NST;
+      const uint32_t bar = smem_u32(&bars[warp][stg]);
+      const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
+      const int nv = min(16, ent_valid[e] - sub * 16);
+      if (nv > 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, 2u * TR::TILE);
+        const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
+        const int row = ent_blk[e] * a.ps + sub * 16;
+        tma_load_3d(sK, tmK, 0, h, row, bar);
+        tma_load_3d(sK + TR::TILE, tmV, 0, h, row, bar);
+      } else {
+        mbar_arrive_expect_tx(bar, 0u);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int k = 0; k < NST - 1; ++k) issue(k);
+  int k = 0;
+  for (int cur = warp; cur < ntiles; ++k, cur += NW) {
+    issue(k + NST - 1);
+    const int stage = (cw0 + k) % NST;
+    mbar_wait(smem_u32(&bars[warp][stage]), ((cw0 + k) / NST) & 1, a.ws);
+    const int nv = tile_rows(cur);
+    if (nv > 0) {
+      const unsigned char *sK = my_stages + (size_t)stage * TR::STAGE;  // landed: waited above
+      const unsigned char *sV = sK + TR::TILE;
+      // ---- QK ----
+      float v[TR::NV];
+      {
+        float2 acc[4][G];
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+          for (int g = 0; g < G; ++g) acc[tt][g] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const unsigned char *rowp = sK + (tt * 4 + tq) * TR::ROW;
+#pragma unroll
+          for (int c = 0; c < TR::CPL; ++c) {
+            const uint4 kw = *reinterpret_cast<const uint4 *>(rowp + (dg + 8 * c) * 16);
+            float2 kf[TR::EPC / 2];
+            Elem<T>::to_f2(kw, kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+              for (int e = 0; e < TR::EPC / 2; ++e)
+                acc[tt][g] = ffma2(q2[g][c * TR::EPC / 2 + e], kf[e], acc[tt][g]);
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+          for (int g = 0; g < G; ++g) v[tt * G + g] = acc[tt][g].x + acc[tt][g].y;
+      }
+      reduce_dg<TR::NV>(v, lane);
+      // lane holds token t for heads hb * KEEP + j (G >= 2), or head 0 (G == 1)
+      const int t = (dg >> 1) * 4 + tq;
+      const int hb = (G >= 2) ? (dg & 1) : 0;
+#pragma unroll
+      for (int j = 0; j < TR::KEEP; ++j)
+        if (t >= nv) v[j] = -INFINITY;
+      float mx[TR::KEEP], oth[TR::KEEP];
+#pragma unroll
+      for (int j = 0; j < TR::KEEP; ++j) {
+        float x = v[j];
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+        mx[j] = x;
+        oth[j] = (G >= 2) ? __shfl_xor_sync(0xffffffffu, x, 1) : x;
+      }
+      float mnew[G];
+      bool moved = false;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int j = g % TR::KEEP, half = g / TR::KEEP;
+        const float tmax = (G == 1 || half == hb) ? mx[j] : oth[j];
+        mnew[g] = fmaxf(m[g], tmax);
+        moved |= mnew[g] != m[g];
+      }
+      if (moved) {  // warp-uniform
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float al = exp2f(m[g] - mnew[g]);
+          m[g] = mnew[g];
+          l[g] *= al;
+          const float2 aa = make_float2(al, al);
+#pragma unroll
+          for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = ffma2(O[g][e], aa, make_float2(0.f, 0.f));
+        }
+      }
+      const bool writer = (G >= 2) || ((dg & 1) == 0);
+#pragma unroll
+      for (int j = 0; j < TR::KEEP; ++j) {
+        const int gj = hb * TR::KEEP + j;
+        float mg = m[0];
+#pragma unroll
+        for (int g = 1; g < G; ++g)
+          if (g == gj) mg = m[g];
+        const float p = exp2f(v[j] - mg);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g == gj && writer) l[g] += p;
+        if (writer) pp[t * G + gj] = make_float2(p, p);
+      }
+      __syncwarp();
+      // ---- PV ----
+      auto pv_row = [&](int tk) {
+        float2 vf[TR::VPL / 2];
+        const unsigned char *vr = sV + tk * TR::ROW + lane * TR::VPL * TR::ES;
+        if constexpr (TR::VPL * TR::ES == 16) {
+          Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(vr), vf);
+        } else {
+          Elem<T>::to_f2_8(*reinterpret_cast<const uint2 *>(vr), vf);
+        }
+        const float2 *pr = pp + tk * G;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 pg = pr[g];
+#pragma unroll
+          for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = ffma2(pg, vf[e], O[g][e]);
+        }
+      };
+      if (nv == 16) {
+#pragma unroll
+        for (int tk = 0; tk < 16; ++tk) pv_row(tk);
+      } else {
+        for (int tk = 0; tk < nv; ++tk) pv_row(tk);
+      }
+    }
+    __syncwarp();
+  }
+  cw = cw0 + k;
+}
+
+// Merges the NW warp states of the CTA into one partial (m, l and O relative to m) at `slot`.
+// wO aliases the stages: the caller has synchronised after the last tile.
+template <typename T, int D, int G, int NW, int NST>
+__device__ __forceinline__ void write_partial(const DecodeArgs &a, size_t slot, float (&m)[G], float (&l)[G],
+                                              float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2], float *wO, float *wML) {
+  using TR = DT<T, D, G, NW, NST>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float x = l[g];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+#pragma unroll
+    for (int e = 0; e < TR::VPL / 2; ++e)
+      reinterpret_cast<float2 *>(wO + (warp * G + g) * D + lane * TR::VPL)[e] = O[g][e];
+    if (lane == 0) {
+      wML[(warp * G + g) * 2] = m[g];
+      wML[(warp * G + g) * 2 + 1] = x;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wML[(w * G + g) * 2]);
+    float acc = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float sc = exp2f(wML[(w * G + g) * 2] - M);
+        acc = fmaf(sc, wO[(w * G + g) * D + d], acc);
+        L = fmaf(sc, wML[(w * G + g) * 2 + 1], L);
+      }
+    }
+    a.part_o[(slot * G + g) * D + d] = acc;
+    if (d == 0) {
+      a.part_ml[(slot * G + g) * 2] = M;
+      a.part_ml[(slot * G + g) * 2 + 1] = L;
+    }
+  }
+}
+
+template <typename T, int D, int G, int NW, int NST>
+struct DecodeSmem {
+  using TR = DT<T, D, G, NW, NST>;
+  unsigned char *stages;
+  float2 *pp_all;
+  float *wML;
+  int *ent_blk, *ent_valid;
+  int *extra;  // flat layout: the unit prefix sums
+  __device__ explicit DecodeSmem(unsigned char *raw) {
+    stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127));
+    pp_all = reinterpret_cast<float2 *>(stages + TR::STAGES);
+    wML = reinterpret_cast<float *>(pp_all + NW * 16 * G);
+    ent_blk = reinterpret_cast<int *>(wML + NW * G * 2);
+    ent_valid = ent_blk + kSwMax;
+    extra = ent_valid + kSwMax;
+  }
+};
+
+// ---- split layout: one CTA per (split of `sw` list entries, KV head, sequence) ----------------
+template <typename T, int D, int G, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV) {
+  using TR = DT<T, D, G, NW, NST>;
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  DecodeSmem<T, D, G, NW, NST> sm(smem_dyn);
+  __shared__ __align__(8) uint64_t bars[NW][NST];
+  __shared__ int flag_last;
+
+  const int s = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+  const int unit = i * a.H_kv + h;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  const int e0 = s * a.sw;
+  const size_t pbase = (size_t)unit * a.n_items_max + s;
+
+  int n_ent = 0;
+  if (seq_len < 1 || P > a.max_pages) {
+    if (s == 0 && tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
+  } else if (a.selected) {
+    const int32_t *row = a.selected + (size_t)unit * a.b_max;
+    if (e0 < a.b_max && row[e0] >= 0) n_ent = min(a.sw, a.b_max - e0);
+  } else if (e0 < P) {
+    n_ent = min(a.sw, P - e0);
+  }
+  if (lane == 0) {
+    for (int k = 0; k < NST; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
+    fence_mbar_init();
+  }
+  load_entries<NW * 32>(a, i, unit, P, seq_len, e0, n_ent, sm.ent_blk, sm.ent_valid);
   __syncthreads();
 
   if (n_ent > 0) {
-    // ---- per-lane query slices (scaled into the log2 domain) ------------------------------
     float2 q2[G][TR::CPL * TR::EPC / 2];
-    {
-      const T *qb = reinterpret_cast<const T *>(a.q) + ((size_t)i * a.H_q + (size_t)h * G) * D;
-      const float qs = a.scale * kLog2e;
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int c = 0; c < TR::CPL; ++c) {
-          float2 f[TR::EPC / 2];
-          Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(qb + (size_t)g * D + (dg + 8 * c) * TR::EPC), f);
-#pragma unroll
-          for (int e = 0; e < TR::EPC / 2; ++e) q2[g][c * TR::EPC / 2 + e] = make_float2(f[e].x * qs, f[e].y * qs);
-        }
-    }
-
+    load_q<T, D, G, NW, NST>(a, i, h, lane & 7, q2);
     float m[G], l[G];
     float2 O[G][TR::VPL / 2];
 #pragma unroll
@@ -250,193 +487,11 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
 #pragma unroll
       for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = make_float2(0.f, 0.f);
     }
-
-    const int stp = a.ps / 16;  // tiles per page
-    const int ntiles = n_ent * stp;
-    unsigned char *my_stages = stages + (size_t)warp * NST * TR::STAGE;
-    float2 *pp = pp_all + warp * 16 * G;
-    auto tile_rows = [&](int it) -> int {
-      const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
-      return min(16, ent_valid[e] - sub * 16);
-    };
-    // lane 0 of the warp issues the K and V tile copies of its c-th tile into stage c % NST; a
-    // tile without rows still arrives (0 bytes) so every stage's phases stay in step.
-    auto issue = [&](int c) {
-      const int it = warp + c * NW;
-      if (it >= ntiles) return;
-      if (lane == 0) {
-        const int stg = c % NST;
-        const uint32_t bar = smem_u32(&bars[warp][stg]);
-        const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
-        const int nv = min(16, ent_valid[e] - sub * 16);
-        if (nv > 0) {
-          fence_proxy_async_smem();
-          mbar_arrive_expect_tx(bar, 2u * TR::TILE);
-          const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
-          const int row = ent_blk[e] * a.ps + sub * 16;
-          tma_load_3d(sK, &tmK, 0, h, row, bar);
-          tma_load_3d(sK + TR::TILE, &tmV, 0, h, row, bar);
-        } else {
-          mbar_arrive_expect_tx(bar, 0u);
-        }
-      }
-    };
-
-#pragma unroll
-    for (int c = 0; c < NST - 1; ++c) issue(c);
-    for (int c = 0, cur = warp; cur < ntiles; ++c, cur += NW) {
-      issue(c + NST - 1);
-      const int stage = c % NST;
-      mbar_wait(smem_u32(&bars[warp][stage]), (c / NST) & 1, a.ws);
-      const int nv = tile_rows(cur);
-      if (nv > 0) {
-        const unsigned char *sK = my_stages + (size_t)stage * TR::STAGE;  // landed: waited above
-        const unsigned char *sV = sK + TR::TILE;
-        // ---- QK ----
-        float v[TR::NV];
-        {
-          float2 acc[4][G];
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt)
-#pragma unroll
-            for (int g = 0; g < G; ++g) acc[tt][g] = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const unsigned char *rowp = sK + (tt * 4 + tq) * TR::ROW;
-#pragma unroll
-            for (int c = 0; c < TR::CPL; ++c) {
-              const uint4 kw = *reinterpret_cast<const uint4 *>(rowp + (dg + 8 * c) * 16);
-              float2 kf[TR::EPC / 2];
-              Elem<T>::to_f2(kw, kf);
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < TR::EPC / 2; ++e)
-                  acc[tt][g] = ffma2(q2[g][c * TR::EPC / 2 + e], kf[e], acc[tt][g]);
-            }
-          }
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt)
-#pragma unroll
-            for (int g = 0; g < G; ++g) v[tt * G + g] = acc[tt][g].x + acc[tt][g].y;
-        }
-        reduce_dg<TR::NV>(v, lane);
-        // lane holds token t for heads hb * KEEP + j (G >= 2), or head 0 (G == 1)
-        const int t = (dg >> 1) * 4 + tq;
-        const int hb = (G >= 2) ? (dg & 1) : 0;
-#pragma unroll
-        for (int j = 0; j < TR::KEEP; ++j)
-          if (t >= nv) v[j] = -INFINITY;
-        float mx[TR::KEEP], oth[TR::KEEP];
-#pragma unroll
-        for (int j = 0; j < TR::KEEP; ++j) {
-          float x = v[j];
-          x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-          x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-          x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
-          x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
-          mx[j] = x;
-          oth[j] = (G >= 2) ? __shfl_xor_sync(0xffffffffu, x, 1) : x;
-        }
-        float mnew[G];
-        bool moved = false;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int j = g % TR::KEEP, half = g / TR::KEEP;
-          const float tmax = (G == 1 || half == hb) ? mx[j] : oth[j];
-          mnew[g] = fmaxf(m[g], tmax);
-          moved |= mnew[g] != m[g];
-        }
-        if (moved) {  // warp-uniform
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float al = exp2f(m[g] - mnew[g]);
-            m[g] = mnew[g];
-            l[g] *= al;
-            const float2 aa = make_float2(al, al);
-#pragma unroll
-            for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = ffma2(O[g][e], aa, make_float2(0.f, 0.f));
-          }
-        }
-        const bool writer = (G >= 2) || ((dg & 1) == 0);
-#pragma unroll
-        for (int j = 0; j < TR::KEEP; ++j) {
-          const int gj = hb * TR::KEEP + j;
-          float mg = m[0];
-#pragma unroll
-          for (int g = 1; g < G; ++g)
-            if (g == gj) mg = m[g];
-          const float p = exp2f(v[j] - mg);
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            if (g == gj && writer) l[g] += p;
-          if (writer) pp[t * G + gj] = make_float2(p, p);
-        }
-        __syncwarp();
-        // ---- PV ----
-        auto pv_row = [&](int tk) {
-          float2 vf[TR::VPL / 2];
-          const unsigned char *vr = sV + tk * TR::ROW + lane * TR::VPL * TR::ES;
-          if constexpr (TR::VPL * TR::ES == 16) {
-            Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(vr), vf);
-          } else {
-            Elem<T>::to_f2_8(*reinterpret_cast<const uint2 *>(vr), vf);
-          }
-          const float2 *pr = pp + tk * G;
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float2 pg = pr[g];
-#pragma unroll
-            for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = ffma2(pg, vf[e], O[g][e]);
-          }
-        };
-        if (nv == 16) {
-#pragma unroll
-          for (int tk = 0; tk < 16; ++tk) pv_row(tk);
-        } else {
-          for (int tk = 0; tk < nv; ++tk) pv_row(tk);
-        }
-      }
-      __syncwarp();
-    }
-    __syncthreads();  // every warp is done with the stages; wO below reuses them
-
-    // ---- merge the warps of the CTA into one partial ----------------------------------------
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float x = l[g];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      l[g] = x;
-#pragma unroll
-      for (int e = 0; e < TR::VPL / 2; ++e)
-        reinterpret_cast<float2 *>(wO + (warp * G + g) * D + lane * TR::VPL)[e] = O[g][e];
-      if (lane == 0) {
-        wML[(warp * G + g) * 2] = m[g];
-        wML[(warp * G + g) * 2 + 1] = l[g];
-      }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < G * D; idx += NW * 32) {
-      const int g = idx / D, d = idx - g * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, wML[(w * G + g) * 2]);
-      float acc = 0.f, L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sc = exp2f(wML[(w * G + g) * 2] - M);
-          acc = fmaf(sc, wO[(w * G + g) * D + d], acc);
-          L = fmaf(sc, wML[(w * G + g) * 2 + 1], L);
-        }
-      }
-      a.part_o[(pbase * G + g) * D + d] = acc;
-      if (d == 0) {
-        a.part_ml[(pbase * G + g) * 2] = M;
-        a.part_ml[(pbase * G + g) * 2 + 1] = L;
-      }
-    }
+    int cw = 0;
+    warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages, sm.pp_all, bars, cw,
+                                 m, l, O);
+    __syncthreads();  // every warp is done with the stages; the merge below reuses them
+    write_partial<T, D, G, NW, NST>(a, pbase, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
   } else if (tid < G) {  // nothing to read: an empty partial
     a.part_ml[(pbase * G + tid) * 2] = -INFINITY;
     a.part_ml[(pbase * G + tid) * 2 + 1] = 0.f;
@@ -453,7 +508,161 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   if (!flag_last) return;
   __threadfence();
   if (tid == 0) a.tickets[unit] = 0u;
-  merge_unit<T, D, G, NW>(a, unit, reinterpret_cast<float *>(stages), wML);
+  merge_unit<T, D, G, NW>(a, unit, (size_t)unit * a.n_items_max, a.n_items_max, reinterpret_cast<float *>(sm.stages),
+                          sm.wML);
+}
+
+// ---- flat layout ---------------------------------------------------------------------------------
+// List entries per unit of a sparse call: one past the last non-negative id of the unit's row
+// (0 for a sequence whose length is out of range). One warp per unit.
+__global__ void decode_counts_kernel(DecodeArgs a) {
+  const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (unit >= a.B * a.H_kv) return;
+  const int i = unit / a.H_kv;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  int last = -1;
+  if (seq_len >= 1 && P <= a.max_pages) {
+    const int32_t *row = a.selected + (size_t)unit * a.b_max;
+    for (int x = lane; x < a.b_max; x += 32)
+      if (row[x] >= 0) last = x;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  if (lane == 0) a.counts[unit] = last + 1;
+}
+
+// A persistent grid of C CTAs cuts the concatenation of all units' lists (E entries) into C
+// equal shares: CTA c streams entries [c E / C, (c + 1) E / C), which may cover the end of one
+// unit, whole units and the start of another. Each (CTA, unit) segment leaves one partial at
+// slot c + u (unique: shares are ordered like the units), and the last CTA of a unit to finish
+// (ticket, no waiting) merges the unit's partials. Units without entries get zero rows from CTA
+// u % C. Balancing by entries removes the tail that budget-sized splits leave when budgets differ.
+template <typename T, int D, int G, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                                                              const __grid_constant__ CUtensorMap tmV) {
+  using TR = DT<T, D, G, NW, NST>;
+  constexpr int NT = NW * 32;
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  DecodeSmem<T, D, G, NW, NST> sm(smem_dyn);
+  int *start = sm.extra;  // [U + 1] exclusive prefix of the units' entry counts
+  __shared__ __align__(8) uint64_t bars[NW][NST];
+  __shared__ int flag_last;
+  __shared__ int scan_tot[NW];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int U = a.B * a.H_kv;
+  const int c = blockIdx.x;
+
+  // ---- entry counts and their prefix sums ----------------------------------------------------
+  for (int u = tid; u < U; u += NT) {  // coalesced, independent loads
+    int cnt;
+    if (a.selected) {
+      cnt = a.counts[u];
+    } else {
+      const int sl = a.seq_lens[u / a.H_kv];
+      const int P = (sl + a.ps - 1) / a.ps;
+      cnt = (sl >= 1 && P <= a.max_pages) ? P : 0;
+    }
+    start[u + 1] = cnt;
+  }
+  __syncthreads();
+  const int per = (U + NT - 1) / NT;  // contiguous units per thread for the scan
+  const int u0 = min(U, tid * per), u1 = min(U, u0 + per);
+  int run = 0;
+  for (int u = u0; u < u1; ++u) run += start[u + 1];
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scan_tot[warp] = incl;
+  if (lane == 0) {
+    for (int k = 0; k < NST; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  int base = incl - run;
+  for (int w = 0; w < warp; ++w) base += scan_tot[w];
+  for (int u = u0; u < u1; ++u) {
+    const int cnt = start[u + 1];
+    start[u + 1] = base + cnt;
+    base += cnt;
+  }
+  if (tid == 0) start[0] = 0;
+  __syncthreads();
+  const long long E = start[U];
+  // CTAs with a share: every share holds at least kFlatMinShare entries (and is never empty)
+  const int C = (int)min((long long)gridDim.x, max(1LL, E / kFlatMinShare));
+
+  // ---- units without entries: zero rows (and the status for a bad length) ----------------------
+  for (int u = c; u < U; u += gridDim.x) {
+    if (start[u + 1] != start[u]) continue;
+    const int i = u / a.H_kv;
+    const int sl = a.seq_lens[i];
+    if ((sl < 1 || (sl + a.ps - 1) / a.ps > a.max_pages) && (u % a.H_kv) == 0 && tid == 0)
+      set_status(a.ws, PSK_DEV_BAD_SEQLEN);
+    T *out = reinterpret_cast<T *>(a.out) + ((size_t)i * a.H_q + (size_t)(u % a.H_kv) * G) * D;
+    for (int idx = tid; idx < G * D; idx += NT) Elem<T>::store(out + idx, 0.f);
+  }
+  if (c >= C) return;
+
+  auto cta_of = [&](long long e) -> int {  // the CTA whose share holds entry e
+    return (int)min((long long)C - 1, ((e + 1) * C - 1) / E);
+  };
+  const long long e_lo = (long long)c * E / C, e_hi = (long long)(c + 1) * E / C;
+  int u;
+  {  // the unit holding entry e_lo: the last u with start[u] <= e_lo
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (start[mid] <= e_lo) lo = mid; else hi = mid - 1;
+    }
+    u = lo;
+  }
+  int cw = 0;
+  for (long long e = e_lo; e < e_hi;) {
+    while (start[u + 1] <= e) ++u;  // skip units without entries
+    const long long seg_end = min(e_hi, (long long)start[u + 1]);
+    const int i = u / a.H_kv, h = u % a.H_kv;
+    const int seq_len = a.seq_lens[i];
+    const int P = (seq_len + a.ps - 1) / a.ps;
+    float2 q2[G][TR::CPL * TR::EPC / 2];
+    load_q<T, D, G, NW, NST>(a, i, h, lane & 7, q2);
+    float m[G], l[G];
+    float2 O[G][TR::VPL / 2];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int x = 0; x < TR::VPL / 2; ++x) O[g][x] = make_float2(0.f, 0.f);
+    }
+    for (long long x0 = e; x0 < seg_end; x0 += kSwMax) {
+      const int n = (int)min((long long)kSwMax, seg_end - x0);
+      __syncthreads();  // the previous entry table and stages are no longer in use
+      load_entries<NT>(a, i, u, P, seq_len, (int)(x0 - start[u]), n, sm.ent_blk, sm.ent_valid);
+      __syncthreads();
+      warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, q2, sm.ent_blk, sm.ent_valid, n, sm.stages, sm.pp_all, bars, cw, m,
+                                   l, O);
+    }
+    __syncthreads();  // every warp is done with the stages; the merges below reuse them
+    write_partial<T, D, G, NW, NST>(a, (size_t)c + u, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
+    const int c_first = cta_of(start[u]), c_last = cta_of((long long)start[u + 1] - 1);
+    const int nseg = c_last - c_first + 1;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) flag_last = atomicAdd(a.tickets + u, 1u) == (unsigned)(nseg - 1);
+    __syncthreads();
+    if (flag_last) {
+      __threadfence();
+      if (tid == 0) a.tickets[u] = 0u;
+      merge_unit<T, D, G, NW>(a, u, (size_t)c_first + u, nseg, reinterpret_cast<float *>(sm.stages), sm.wML);
+    }
+    e = seg_end;
+  }
 }
 
 template <typename T, int D, int G>
@@ -461,43 +670,80 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   constexpr int NW = 4, NST = 2;
   using TR = DT<T, D, G, NW, NST>;
   static_assert(TR::STAGES >= (size_t)kMaxItems * G * 4, "stage memory must hold the merge weights");
-  auto kfn = decode_split_kernel<T, D, G, NW, NST>;
-  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
-  if (e != cudaSuccess) return e;
+  static_assert(TR::STAGES >= (size_t)kFlatMaxCtas * G * 4, "stage memory must hold the merge weights");
   CUtensorMap tmK, tmV;
   const long long rows = (long long)a.nb * a.ps;
   const int dt = sizeof(T) == 4 ? PSK_F32 : PSK_BF16;
   if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv, rows, 16) ||
       !encode_cache_map(&tmV, a.v_cache, dt, D, a.H_kv, rows, 16))
     return cudaErrorInvalidValue;
-  dim3 grid(a.n_items_max, a.H_kv, a.B);
-  kfn<<<grid, NW * 32, TR::SMEM, s>>>(a, tmK, tmV);
+  cudaError_t e;
+  if (!a.flat) {
+    auto kfn = decode_split_kernel<T, D, G, NW, NST>;
+    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.n_items_max, a.H_kv, a.B);
+    kfn<<<grid, NW * 32, TR::SMEM, s>>>(a, tmK, tmV);
+    return cudaGetLastError();
+  }
+  const int U = a.B * a.H_kv;
+  if (a.selected) {
+    decode_counts_kernel<<<(U + 7) / 8, 256, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kfn = decode_flat_kernel<T, D, G, NW, NST>;
+  const size_t smem = TR::SMEM + (size_t)(U + 1) * 4;
+  e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, NW * 32, smem)) != cudaSuccess) return e;
+  const int ctas = std::max(1, std::min(kFlatMaxCtas, sms * std::max(1, per_sm)));
+  kfn<<<ctas, NW * 32, smem, s>>>(a, tmK, tmV);
   return cudaGetLastError();
 }
-
 }  // namespace
 
 bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan) {
   const long long units = (long long)L.batch * L.num_kv_heads;
-  // 64 list entries per CTA (measured best on the batched workload); fewer while the grid would
-  // not fill the GPU (152 SMs x 2 CTAs) a few times over, more when a unit would need over
-  // kMaxItems partials
-  int sw = 64;
-  if (const char *env = std::getenv("PSK_DECODE_SPLIT")) {  // tuning override: entries per CTA
-    const int v = std::atoi(env);
-    if (v >= 1 && v <= kSwMax) sw = v;
-  }
-  while (sw > 4 && units * ((entries + sw - 1) / sw) < 4LL * 152 * 2) sw /= 2;
-  while (sw < kSwMax && (entries + sw - 1) / sw > kMaxItems) sw *= 2;
-  (void)dense;
-  plan->sw = sw;
-  plan->n_items_max = (entries + sw - 1) / sw;
   const int G = L.num_q_heads / L.num_kv_heads;
+  // Dense: the flat layout (equal shares of all units' page lists over a persistent grid)
+  // whenever its prefix sums fit in shared memory. Sparse: the split layout, measured faster on
+  // the batched workload (the flat one adds a count pass over the selected rows and more
+  // partials, and short budget lists leave its shares little to balance).
+  bool flat = dense && units <= kFlatMaxUnits;
+  if (const char *env = std::getenv("PSK_DECODE_LAYOUT"))  // tuning override: "split" or "flat"
+    flat = std::string(env) == "split" ? false : (std::string(env) == "flat" ? units <= kFlatMaxUnits : flat);
+  size_t slots;
+  if (flat) {
+    plan->sw = kSwMax;
+    plan->n_items_max = 1;
+    slots = (size_t)kFlatMaxCtas + (size_t)units;
+  } else {
+    // 64 list entries per CTA (measured best on the batched workload); fewer while the grid
+    // would not fill the GPU (152 SMs x 2 CTAs) a few times over, more when a unit would need
+    // over kMaxItems partials
+    int sw = 64;
+    if (const char *env = std::getenv("PSK_DECODE_SPLIT")) {  // tuning override: entries per CTA
+      const int v = std::atoi(env);
+      if (v >= 1 && v <= kSwMax) sw = v;
+    }
+    while (sw > 4 && units * ((entries + sw - 1) / sw) < 4LL * 152 * 2) sw /= 2;
+    while (sw < kSwMax && (entries + sw - 1) / sw > kMaxItems) sw *= 2;
+    plan->sw = sw;
+    plan->n_items_max = (entries + sw - 1) / sw;
+    slots = (size_t)units * plan->n_items_max;
+  }
+  plan->flat = flat ? 1 : 0;
   size_t off = ws_scratch_offset((size_t)units);
   plan->off_o = off;
-  off = align_up(off + (size_t)units * plan->n_items_max * G * L.v_head_dim * 4, 256);
+  off = align_up(off + slots * G * L.v_head_dim * 4, 256);
   plan->off_ml = off;
-  off = align_up(off + (size_t)units * plan->n_items_max * G * 2 * 4, 256);
+  off = align_up(off + slots * G * 2 * 4, 256);
+  plan->off_counts = off;
+  off = align_up(off + (size_t)units * 4, 256);
   plan->ws_bytes = off;
   plan->off_tickets = ws_decode_tickets_offset((size_t)units);
   return plan->n_items_max <= kMaxItems;

@@ -638,6 +638,8 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   off = align_up(off + (size_t)units * plan->n_items_max * kHeads * 2 * 4, 256);
   plan->ws_bytes = off;
   plan->off_tickets = ws_decode_tickets_offset((size_t)units);
+  plan->flat = 0;
+  plan->off_counts = 0;
   return plan->n_items_max <= kMlaMaxItems;
 }
 

@@ -70,13 +70,15 @@ struct DecodeArgs {
   uint32_t *tickets;   // [B * H_kv] merge tickets (zero between calls)
   int B, H_q, H_kv, D, D_v, ps, nb, max_pages;
   int b_max;           // entries per selected row (sparse)
-  int sw;              // list entries per item
-  int n_items_max;     // items per unit
+  int sw;              // list entries per item (split layout)
+  int n_items_max;     // items per unit (split layout)
+  int32_t *counts;     // [B * H_kv] list entries per unit (flat layout, sparse)
+  int flat;            // 1: flat layout (the units' lists cut into equal shares of a persistent grid)
   float scale;
 };
 struct DecodePlan {
-  int sw, n_items_max;
-  size_t ws_bytes, off_o, off_ml, off_tickets;
+  int sw, n_items_max, flat;
+  size_t ws_bytes, off_o, off_ml, off_tickets, off_counts;
 };
 bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan);
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);

@@ -4,7 +4,8 @@
 //   score[i,h,p] = scale * max_{g in group(h)} sum_d max(q_gd * kmin_pd, q_gd * kmax_pd)
 // The kernel evaluates each term as max(q,0) * kmax + min(q,0) * kmin, which equals
 // max(q * kmin, q * kmax) exactly whenever kmin <= kmax (one of the two products is +-0),
-// so every kept product is the same fp32 product; accumulation is fp32.
+// so every kept product is the same fp32 product; accumulation is fp32 (bf16 caches: mixed
+// fma.f32.bf16 on the raw bf16 pairs; fp32 caches: packed fp32x2 FMAs).
 //
 // Selection (LOCKS PKG-INFO, "How it works", Selection: a static top-b per (layer, KV head);
 // sink and recent page always kept and counted inside b; EntmaxKV "Top-k": the budget
@@ -21,7 +22,7 @@
 //   order key per page (0 = forced sink / tail, or a flagged bad block) to the workspace.
 //   page_select_kernel (K2) selects: one CTA per (KV head, chunk of up to 16384 pages,
 //   sequence) loads the chunk's keys (L2-resident after K1) into shared memory and finds the
-//   top k = b - 2 with an MSB-first 8-bit radix select (warp-aggregated histogram atomics);
+//   top k = b - 2 with an MSB-first 8-bit radix select (per-warp histograms);
 //   ties go to the lower index through block-wide scans in index order. A unit that fits one
 //   chunk is finished by that CTA; otherwise each chunk writes its winners (ascending) and the
 //   last CTA of the (sequence, KV head) to finish (an atomic ticket, no waiting) merges them
@@ -39,6 +40,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+static_assert(kThreads == 256, "the radix pass maps one thread to each 8-bit digit");
 constexpr int kMergeCap = 8192;  // candidates the merge CTA can hold
 
 // ------------------------------------------------------------------------------------
@@ -82,9 +84,10 @@ __device__ __forceinline__ int block_scan_w0(int x, int *cnt, int *total) {
 // 1 <= k <= number of nonzero keys, and kmin / kmax = the smallest / largest nonzero key.
 // The digits start at the highest bit in which kmin and kmax differ (the bits above are common
 // to every candidate), 8 bits per pass. Each warp counts into its own 256-bin histogram with
-// plain shared-memory atomics; warp 0 alone sums the warps' histograms, scans the 256 bins
-// from the top, picks the digit and clears the other histogram buffer, so a pass costs two
-// block barriers. hist: 2 buffers x 8 warps x 256 bins.
+// shared-memory atomics; then thread t owns digit 255 - t: it sums (and clears) that bin over
+// the warps, and a block-wide scan in descending digit order finds the digit holding the k-th
+// key. Three barriers per pass. hist: kWarps x 256 bins, zero on entry and on return;
+// sh: >= 2 + kWarps ints.
 __device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, uint32_t kmax, int *hist, int *sh,
                              uint32_t *T_out, int *need_eq_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -94,57 +97,45 @@ __device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, 
   uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
   uint32_t mask = shift + 8 >= 32 ? 0u : (0xFFFFFFFFu << (shift + 8));
   int need = k;
-  int buf = 0;
-  for (int b = tid; b < 2 * kWarps * 256; b += kThreads) hist[b] = 0;
-  __syncthreads();
+  int *wsum = sh + 2;
+  int *myhist = hist + warp * 256;
 #pragma unroll 1
   for (;;) {
-    int *hb = hist + buf * kWarps * 256;
-    int *myhist = hb + warp * 256;
     for (int x = tid; x < n; x += kThreads) {
       const uint32_t key = keys[x];
       if (key != 0u && (key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255 - 8l - j (descending digits)
-      int c[8], tot = 0;
+    const int bin = 255 - tid;  // descending digits in thread order
+    int v = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int bin = 255 - 8 * lane - j;
-        int v = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      v += hist[w * 256 + bin];
+      hist[w * 256 + bin] = 0;
+    }
+    int incl = v;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += hb[w * 256 + bin];
-        c[j] = v;
-        tot += v;
-      }
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int run = incl - tot;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (run + c[j] >= need && run < need) {
-          sh[0] = 255 - 8 * lane - j;
-          sh[1] = run;
-        }
-        run += c[j];
-      }
-      int *other = hist + (buf ^ 1) * kWarps * 256;
-      for (int b = lane; b < kWarps * 256; b += 32) other[b] = 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) incl += wsum[w];
+    const int excl = incl - v;
+    if (excl < need && incl >= need) {
+      sh[0] = bin;
+      sh[1] = excl;
     }
     __syncthreads();
     const int d = sh[0];
     need -= sh[1];
     prefix |= static_cast<uint32_t>(d) << shift;
     mask |= 255u << shift;
-    buf ^= 1;
     if (shift == 0) break;
     shift = shift >= 8 ? shift - 8 : 0;
     // a digit that overlaps bits already fixed is harmless: they match the prefix
+    __syncthreads();  // sh and wsum are rewritten by the next pass
   }
   __syncthreads();  // every thread has read sh before the caller reuses it
   *T_out = prefix;
@@ -239,6 +230,18 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
   return mx;
 }
 
+// acc + q0*k0 + q1*k1 for bf16 pairs q = (q0, q1), k = (k0, k1) (low half first): each step is
+// one fp32 fma of a bf16 x bf16 product, which is exact in fp32, so the sum is the same as with
+// both operands widened to fp32 first. Keeping q as bf16 pairs (32 registers for G = 4) instead
+// of fp32 lets three CTAs share an SM.
+__device__ __forceinline__ float dot2_bf16(uint32_t q, uint32_t k, float acc) {
+  float r;
+  asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+      " fma.rn.f32.bf16 %0, a0, b0, %3;\n fma.rn.f32.bf16 %0, a1, b1, %0;\n}\n"
+      : "=f"(r) : "r"(q), "r"(k), "f"(acc));
+  return r;
+}
+
 // ------------------------------------------------------------------------------------
 // K1: page scores, streaming
 // ------------------------------------------------------------------------------------
@@ -250,13 +253,13 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
 // of the group and every (8 / HPC)-th page step. Writes one 32-bit order key per page (0 for
 // the forced sink / tail and for pages whose block id is out of range) and, when asked, the
 // fp32 score.
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kStageBytes = 32768;
 constexpr int kMaxStagePages = 32;
 constexpr int kPageSteps = 2;  // page steps per loop iteration
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) page_score_kernel(ScoreArgs a) {
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
@@ -323,16 +326,28 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
   const int sub = lane % LPP;  // which 16-byte chunk of the summary row
   const int grp = lane / LPP;  // which page of the warp step
   float2 qp[G][EPC / 2], qn[G][EPC / 2];
+  uint32_t qpw[G][4], qnw[G][4];  // bf16 path: max(q,0) / min(q,0) as bf16 pairs (exact)
   {
     const T *qrow = reinterpret_cast<const T *>(a.q) + ((size_t)i * a.H_q + (size_t)h * G) * D + sub * EPC;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float2 f[EPC / 2];
-      Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(qrow + (size_t)g * D), f);
+      const uint4 w = *reinterpret_cast<const uint4 *>(qrow + (size_t)g * D);
+      if constexpr (sizeof(T) == 2) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int e = 0; e < EPC / 2; ++e) {
-        qp[g][e] = make_float2(fmaxf(f[e].x, 0.f), fmaxf(f[e].y, 0.f));
-        qn[g][e] = make_float2(fminf(f[e].x, 0.f), fminf(f[e].y, 0.f));
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t m = ((ws[e] & 0x80008000u) >> 15) * 0xFFFFu;  // negative halves
+          qnw[g][e] = ws[e] & m;
+          qpw[g][e] = ws[e] & ~m;
+        }
+      } else {
+        float2 f[EPC / 2];
+        Elem<T>::to_f2(w, f);
+#pragma unroll
+        for (int e = 0; e < EPC / 2; ++e) {
+          qp[g][e] = make_float2(fmaxf(f[e].x, 0.f), fmaxf(f[e].y, 0.f));
+          qn[g][e] = make_float2(fminf(f[e].x, 0.f), fminf(f[e].y, 0.f));
+        }
       }
     }
   }
@@ -364,18 +379,33 @@ __global__ void __launch_bounds__(kThreads, 2) page_score_kernel(ScoreArgs a) {
       float v[kPageSteps][G];
 #pragma unroll
       for (int u = 0; u < kPageSteps; ++u) {
-        float2 kl[EPC / 2], kh[EPC / 2];
-        Elem<T>::to_f2(lo[u], kl);
-        Elem<T>::to_f2(hi[u], kh);
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t kl[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
+          const uint32_t kh[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float2 acc = make_float2(0.f, 0.f);
+          for (int g = 0; g < G; ++g) {
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-          for (int e = 0; e < EPC / 2; ++e) {
-            acc = ffma2(qp[g][e], kh[e], acc);
-            acc = ffma2(qn[g][e], kl[e], acc);
+            for (int e = 0; e < 4; ++e) {
+              a0 = dot2_bf16(qpw[g][e], kh[e], a0);
+              a1 = dot2_bf16(qnw[g][e], kl[e], a1);
+            }
+            v[u][g] = a0 + a1;
           }
-          v[u][g] = acc.x + acc.y;
+        } else {
+          float2 kl[EPC / 2], kh[EPC / 2];
+          Elem<T>::to_f2(lo[u], kl);
+          Elem<T>::to_f2(hi[u], kh);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < EPC / 2; ++e) {
+              acc = ffma2(qp[g][e], kh[e], acc);
+              acc = ffma2(qn[g][e], kl[e], acc);
+            }
+            v[u][g] = acc.x + acc.y;
+          }
         }
       }
 #pragma unroll
@@ -457,7 +487,7 @@ __device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t 
 
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ int hist[2 * kWarps * 256];
+  __shared__ int hist[kWarps * 256];  // zero between radix selects
   __shared__ int cnt[kThreads + 1];
   __shared__ uint32_t red[3 * kWarps];
   __shared__ int flag_last;
@@ -500,6 +530,7 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   const int n = p1 - p0;
   const uint32_t *krow = a.keys + (size_t)unit * a.max_pages + p0;
   for (int x = tid; x < n; x += kThreads) keys[x] = __ldcg(krow + x);
+  for (int x = tid; x < kWarps * 256; x += kThreads) hist[x] = 0;
   __syncthreads();
   int total_valid;
   uint32_t kmin, kmax;

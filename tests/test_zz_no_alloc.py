@@ -52,7 +52,13 @@ def test_noalloc_matches_workspace_decode_twice(cache_and_workload):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(cache_and_workload):
-    big = psk.Layout(64, 32, 8, 128, 128, 16, 1 << 20, 8192)
+    """The refusal happens on the host, before any launch. The layout is first checked, by the
+    host-only size query, to need more than the fixed array; only then is the entry point called
+    (its pointer arguments are placeholders that no kernel may ever see)."""
+    big = psk.Layout(4096, 32, 8, 128, 128, 16, 1 << 20, 8192)
+    need = psk.sparse_decode_workspace_size(big, 8192)
+    if not need > (32 << 20):
+        pytest.fail(f"layout needs only {need} bytes of scratch: it would be accepted, so it is not called")
     P = ctypes.c_void_p
     rc = psk.lib().psk_sparse_paged_decode_noalloc(ctypes.byref(big.c()), P(256), P(256), P(256), P(256), P(256),
                                                    P(256), 8192, 0.1, P(256), None)
