@@ -60,9 +60,9 @@ TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
     ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel+page_select_kernel"):
-        {"bytes": 578_190_000 + 6_740_000 + 4_630_000, "digest": "e966b3830c744db3"},
+        {"bytes": 579_010_000 + 5_100_000 + 4_630_000, "digest": "8a66e149f6fec54d"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 467_000_000 + 1_960_000, "digest": "a32daa4d8a55dc09"},
+        {"bytes": 466_990_000 + 1_750_000, "digest": "316441adf4e514da"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel+page_select_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),

@@ -233,7 +233,7 @@ __device__ __forceinline__ float group_score(float (&v)[G], int lane) {
 // acc + q0*k0 + q1*k1 for bf16 pairs q = (q0, q1), k = (k0, k1) (low half first): each step is
 // one fp32 fma of a bf16 x bf16 product, which is exact in fp32, so the sum is the same as with
 // both operands widened to fp32 first. Keeping q as bf16 pairs (32 registers for G = 4) instead
-// of fp32 lets three CTAs share an SM.
+// of fp32 lets four CTAs share an SM.
 __device__ __forceinline__ float dot2_bf16(uint32_t q, uint32_t k, float acc) {
   float r;
   asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
@@ -254,12 +254,12 @@ __device__ __forceinline__ float dot2_bf16(uint32_t q, uint32_t k, float acc) {
 // the forced sink / tail and for pages whose block id is out of range) and, when asked, the
 // fp32 score.
 constexpr int kStages = 2;
-constexpr int kStageBytes = 32768;
+constexpr int kStageBytes = 24576;
 constexpr int kMaxStagePages = 32;
-constexpr int kPageSteps = 2;  // page steps per loop iteration
+constexpr int kPageSteps = 1;  // page steps per loop iteration
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 3) page_score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
@@ -618,7 +618,10 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
-  const size_t smem = std::max<size_t>((size_t)a.chunk * 4, (size_t)kMergeCap * 8);
+  // keys of one chunk; the merge buffer only when a unit spans several chunks (the smaller
+  // footprint keeps every CTA of a one-chunk call resident at once)
+  const size_t keys_bytes = (size_t)std::min(a.chunk, a.max_pages) * 4;
+  const size_t smem = a.n_chunks_max == 1 ? keys_bytes : std::max<size_t>(keys_bytes, (size_t)kMergeCap * 8);
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 g2(a.H_kv, a.n_chunks_max, a.B);
