@@ -233,7 +233,7 @@ constexpr int kKTile = kKB * kKBlock;           // 73728: a K tile (64 tokens x 
 constexpr int kKStages = 2;
 constexpr int kPBytes = kHeads * kTile * 2;     // 16384: P [128 x 64] bf16, 128-byte swizzle
 constexpr int kDecSmem = 1024 + kQSBytes + kKStages * kKTile + kPBytes;
-constexpr int kDecThreads = 160;                // 4 softmax warps (one thread per head) + 1 issuing warp
+constexpr int kDecThreads = 192;                // 4 softmax warps (one thread per head), MMA warp, TMA warp
 constexpr int kMlaMaxSw = 128;                  // pages per split
 constexpr int kMlaMaxItems = 128;               // splits per (sequence, half); their merge weights fit the K stages
 static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKTile, "merge weights must fit the K stages");
@@ -257,7 +257,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   unsigned char *sQ = base;                    // Q dims 384..575
   unsigned char *sK = base + kQSBytes;         // kKStages K tiles
   unsigned char *sP = sK + kKStages * kKTile;  // P
-  __shared__ __align__(8) uint64_t qbar, kfull[kKStages], kempty[kKStages], sfull, pready, pvdone, drained;
+  // K tile parts: A = the 64-dim blocks only S reads (free once S(t) is done), B = the four
+  // value blocks of this half of D_v (free once P.V(t) is done)
+  __shared__ __align__(8) uint64_t qbar, kfa[kKStages], kfb[kKStages], kea[kKStages], keb[kKStages], sfull, sfree,
+      pready, pvdone, drained;
   __shared__ int abort_sh;  // set by the first wait that gives up: every later wait returns at once
   __shared__ uint32_t tslot;
   __shared__ int ent_blk[kMlaMaxSw], ent_valid[kMlaMaxSw];
@@ -309,11 +312,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
     mbar_init(smem_u32(&qbar), 1);
     mbar_init(smem_u32(&drained), 1);
     mbar_init(smem_u32(&sfull), 1);
+    mbar_init(smem_u32(&sfree), 4);
     mbar_init(smem_u32(&pready), 4);
     mbar_init(smem_u32(&pvdone), 1);
     for (int k = 0; k < kKStages; ++k) {
-      mbar_init(smem_u32(&kfull[k]), 1);
-      mbar_init(smem_u32(&kempty[k]), 1);
+      mbar_init(smem_u32(&kfa[k]), 1);
+      mbar_init(smem_u32(&kfb[k]), 1);
+      mbar_init(smem_u32(&kea[k]), 1);
+      mbar_init(smem_u32(&keb[k]), 1);
     }
     abort_sh = 0;
     fence_mbar_init();
@@ -365,79 +371,112 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
     return false;
   };
 
-  if (warp == 4) {
-    // ---------------- issuing thread: TMA copies and MMAs ----------------
+  // the k-th 64-dim block S reads: part A (blocks outside this CTA's value half) first, then
+  // part B (the value blocks vh * 4 .. vh * 4 + 3)
+  auto s_block = [&](int k) -> int {
+    const int kb = k < kKB - 4 ? k : (k - (kKB - 4)) + vh * 4;  // k >= 5: part B
+    return k < kKB - 4 ? (kb < vh * 4 ? kb : kb + 4) : kb;
+  };
+  if (warp == 5) {
+    // ---------------- loading thread: TMA copies ----------------
     if (lane == 0 && n_tiles > 0) {
-      int n_loaded = 0, n_waited = 0;  // K tiles issued / K tiles whose arrival was observed
-      auto load_tile = [&](int t) {
+      int na = 0, nb = 0;  // part A / part B copies issued
+      auto load_part = [&](int t, bool part_b) {
         const int st = t % kKStages;
         const int nh = (2 * t + 1 < n_halves) ? 2 : 1;
-        const uint32_t bar = smem_u32(&kfull[st]);
-        mbar_arrive_expect_tx(bar, (uint32_t)(nh * kKB * kHalf * 128));
+        const uint32_t bar = smem_u32(part_b ? &kfb[st] : &kfa[st]);
+        const int nblk = part_b ? 4 : kKB - 4;
+        mbar_arrive_expect_tx(bar, (uint32_t)(nh * nblk * kHalf * 128));
         const uint32_t dst = smem_u32(sK + st * kKTile);
         for (int h2 = 0; h2 < nh; ++h2) {
           const int hx = 2 * t + h2;
           const int e = halves[hx] >> 1, hh = halves[hx] & 1;
           const int row0 = ent_blk[e] * a.ps + hh * kHalf;
 #pragma unroll 1
-          for (int kb = 0; kb < kKB; ++kb)
+          for (int k = part_b ? kKB - 4 : 0; k < (part_b ? kKB : kKB - 4); ++k) {
+            const int kb = s_block(k);
             tma_load_2d(dst + kb * kKBlock + h2 * kHalf * 128, &tmK, kb * 64, row0, bar);
+          }
         }
-        n_loaded = t + 1;
       };
       mbar_arrive_expect_tx(smem_u32(&qbar), kQSBytes);
 #pragma unroll 1
       for (int kb = 0; kb < kQSmemKB; ++kb)
         tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, (kQTmemKB + kb) * 64, i * kHeads, smem_u32(&qbar));
-      for (int t = 0; t < kKStages && t < n_tiles; ++t) load_tile(t);
+#pragma unroll 1
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % kKStages;
+        if (t >= kKStages && !wait_ok(&kea[st], ((t - kKStages) / kKStages) & 1)) break;  // S(t-2) done
+        load_part(t, false);
+        na = t + 1;
+        if (t >= kKStages && !wait_ok(&keb[st], ((t - kKStages) / kKStages) & 1)) break;  // P.V(t-2) done
+        load_part(t, true);
+        nb = t + 1;
+      }
+      // every copy in flight lands before shared memory is released (also after a wait gave up)
+      for (int t = max(0, na - kKStages); t < na; ++t) mbar_wait(smem_u32(&kfa[t % kKStages]), (t / kKStages) & 1, a.ws);
+      for (int t = max(0, nb - kKStages); t < nb; ++t) mbar_wait(smem_u32(&kfb[t % kKStages]), (t / kKStages) & 1, a.ws);
+      mbar_wait(smem_u32(&qbar), 0, a.ws);
+    }
+  } else if (warp == 4) {
+    // ---------------- issuing thread: MMAs ----------------
+    if (lane == 0 && n_tiles > 0) {
       bool ok = wait_ok(&qbar, 0);
       const uint32_t idesc_qk = umma_idesc(128, kTile, false);
       const uint32_t idesc_pv = umma_idesc(128, 256, true);
-      auto issue_qk = [&](int u) -> bool {
+      // S(u) = Q K(u)^T in two parts: the blocks outside this CTA's value half (part A), then the
+      // value blocks (part B); P.V of the previous tile is issued between them so that the value
+      // blocks it frees can be refilled early. Descriptors advance by (bytes >> 4).
+      const uint32_t q0 = smem_u32(sQ);
+      auto issue_s_part = [&](int u, bool part_b) -> bool {
         const int st = u % kKStages;
-        if (!wait_ok(&kfull[st], (u / kKStages) & 1)) return false;
-        n_waited = u + 1;
+        if (!wait_ok(part_b ? &kfb[st] : &kfa[st], (u / kKStages) & 1)) return false;
         tc_fence_after();
         const uint32_t d = tmem + kSCol;
-        const uint32_t k0 = smem_u32(sK + st * kKTile), q0 = smem_u32(sQ);
+        const uint32_t k0 = smem_u32(sK + st * kKTile);
 #pragma unroll 1
-        for (int kb = 0; kb < kKB; ++kb)
+        for (int k = part_b ? kKB - 4 : 0; k < (part_b ? kKB : kKB - 4); ++k) {
+          const int kb = s_block(k);
+          const uint64_t b0 = umma_desc(k0 + kb * kKBlock, 16, 1024, 2);
+          if (kb < kQTmemKB) {
+            const uint32_t a0 = tmem + kQCol + kb * 32;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bdesc = umma_desc(k0 + kb * kKBlock + ks * 32, 16, 1024, 2);
-            if (kb < kQTmemKB)
-              umma_bf16_ts(d, tmem + kQCol + kb * 32 + ks * 8, bdesc, idesc_qk, (kb | ks) != 0);
-            else
-              umma_bf16(d, umma_desc(q0 + (kb - kQTmemKB) * kHeads * 128 + ks * 32, 16, 1024, 2), bdesc, idesc_qk, 1);
+            for (int ks = 0; ks < 4; ++ks) umma_bf16_ts(d, a0 + ks * 8, b0 + 2 * ks, idesc_qk, (k | ks) != 0);
+          } else {
+            const uint64_t a0 = umma_desc(q0 + (kb - kQTmemKB) * kHeads * 128, 16, 1024, 2);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma_bf16(d, a0 + 2 * ks, b0 + 2 * ks, idesc_qk, (k | ks) != 0);
           }
-        umma_commit(smem_u32(&sfull));
+        }
+        umma_commit(smem_u32(part_b ? &sfull : &kea[st]));
         return true;
       };
-      ok = ok && issue_qk(0);
+      auto issue_pv = [&](int t) -> bool {
+        if (!wait_ok(&pready, t & 1)) return false;  // P(t) written, O rescaled
+        tc_fence_after();
+        const uint64_t pa = umma_desc(smem_u32(sP), 16, 1024, 2);
+        const uint64_t vb = umma_desc(smem_u32(sK + (t % kKStages) * kKTile + vh * 4 * kKBlock), kKBlock, 1024, 2);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // P: +32 bytes per 16 tokens; V: +16 rows of 128 bytes
+          umma_bf16(tmem + kOCol, pa + 2 * ks, vb + 128 * ks, idesc_pv, (t | ks) != 0);
+        umma_commit(smem_u32(&pvdone));
+        umma_commit(smem_u32(&keb[t % kKStages]));
+        return true;
+      };
+      ok = ok && issue_s_part(0, false) && issue_s_part(0, true);
 #pragma unroll 1
       for (int t = 0; ok && t < n_tiles; ++t) {
-        if (!wait_ok(&pready, t & 1)) break;  // P(t) written, O rescaled, S(t) read
-        tc_fence_after();
-        const uint32_t p0a = smem_u32(sP);
-        const uint32_t v0 = smem_u32(sK + (t % kKStages) * kKTile + vh * 4 * kKBlock);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + kOCol, umma_desc(p0a + ks * 32, 16, 1024, 2), umma_desc(v0 + ks * 16 * 128, kKBlock, 1024, 2),
-                    idesc_pv, (t | ks) != 0);
-        umma_commit(smem_u32(&pvdone));
-        umma_commit(smem_u32(&kempty[t % kKStages]));
-        if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
-        if (t + kKStages < n_tiles) {  // refill the stage P.V(t) releases
-          if (!wait_ok(&kempty[t % kKStages], (t / kKStages) & 1)) break;
-          load_tile(t + kKStages);
+        if (t + 1 < n_tiles) {
+          // S(t+1) part A as soon as the softmax warps hold S(t) in registers
+          if (!wait_ok(&sfree, t & 1) || !issue_s_part(t + 1, false)) break;
+          if (!issue_pv(t) || !issue_s_part(t + 1, true)) break;
+        } else if (!issue_pv(t)) {
+          break;
         }
       }
-      // Drain before tensor memory and shared memory are released, also after a wait gave up:
-      // every MMA this thread issued (one commit tracks them all) and every K copy in flight.
+      // every MMA issued completes before tensor memory and shared memory are released
       umma_commit(smem_u32(&drained));
       mbar_wait(smem_u32(&drained), 0, a.ws);
-      for (int t = n_waited; t < n_loaded; ++t) mbar_wait(smem_u32(&kfull[t % kKStages]), (t / kKStages) & 1, a.ws);
-      if (!ok) mbar_wait(smem_u32(&qbar), 0, a.ws);
     }
   } else if (n_tiles > 0) {
     // ---------------- softmax warps: one query head per thread ----------------
@@ -461,6 +500,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
           mt = fmaxf(mt, x[c * 32 + j]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sfree));  // the issuing thread may overwrite S now
       // O holds P.V(t-1) and P is free once pvdone completes for t-1
       if (t > 0 && !__all_sync(0xffffffffu, wait_ok(&pvdone, (t - 1) & 1))) break;
       tc_fence_after();
