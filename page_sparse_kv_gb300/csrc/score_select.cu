@@ -146,33 +146,28 @@ __device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, 
 //   take_all:  key != 0
 //   otherwise: key > T, or key == T among the first need_eq such items
 // to out_key / out_page (page = pages ? pages[x] : page_base + x). Returns the count.
+// One block scan of the packed per-thread counts (equal << 16 | greater; both <= 16384) gives
+// every thread its output position: greater-before + min(equal-before, need_eq).
 // cnt: kThreads + 1 ints of scratch.
 __device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int page_base, int n, bool take_all,
                              uint32_t T, int need_eq, uint32_t *out_key, int32_t *out_page, int *cnt) {
   const int tid = threadIdx.x;
   const int per = (n + kThreads - 1) / kThreads;
   const int x0 = min(n, tid * per), x1 = min(n, x0 + per);
-  int eq = 0;
-  if (!take_all)
-    for (int x = x0; x < x1; ++x) eq += keys[x] == T;
-  const int eq_base = take_all ? 0 : block_scan_w0(eq, cnt, nullptr);
-  if (!take_all) __syncthreads();  // cnt is reused below
-  int c = 0, seen = eq_base;
+  int gt = 0, eq = 0;
   for (int x = x0; x < x1; ++x) {
     const uint32_t key = keys[x];
-    bool take;
     if (take_all) {
-      take = key != 0u;
+      gt += key != 0u;
     } else {
-      take = key > T;
-      if (key == T) take = (seen++ < need_eq);
+      gt += key > T;
+      eq += key == T;
     }
-    c += take;
   }
   int total;
-  const int base = block_scan_w0(c, cnt, &total);
-  int w = base;
-  seen = eq_base;
+  const int pre = block_scan_w0((eq << 16) | gt, cnt, &total);
+  int seen = pre >> 16;
+  int w = (pre & 0xFFFF) + (take_all ? 0 : min(seen, need_eq));
   for (int x = x0; x < x1; ++x) {
     const uint32_t key = keys[x];
     bool take;
@@ -188,7 +183,7 @@ __device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int pag
       ++w;
     }
   }
-  return total;
+  return (total & 0xFFFF) + (take_all ? 0 : min(total >> 16, need_eq));
 }
 
 // ------------------------------------------------------------------------------------
@@ -445,19 +440,10 @@ __device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, in
   for (int x = count + tid; x < b_max; x += kThreads) sel_row[x] = -1;
 }
 
-// Count, min and max of the nonzero keys of keys[0..n) over the block (two barriers).
-__device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t *kmin, uint32_t *kmax,
-                              uint32_t *red /* 3 * kWarps */) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
-  for (int x = tid; x < n; x += kThreads) {
-    const uint32_t k = keys[x];
-    if (k != 0u) {
-      ++c;
-      lo = min(lo, k);
-      hi = max(hi, k);
-    }
-  }
+// Block-wide sum of c and min / max of lo / hi (two barriers; red: 3 * kWarps words).
+__device__ void block_stats(uint32_t c, uint32_t lo, uint32_t hi, uint32_t *red, int *count, uint32_t *kmin,
+                            uint32_t *kmax) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     c += __shfl_xor_sync(0xffffffffu, c, o);
@@ -483,6 +469,21 @@ __device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t 
   *kmin = lo;
   *kmax = hi;
   __syncthreads();  // red is reused by the caller's next call
+}
+
+// Count, min and max of the nonzero keys of keys[0..n) over the block (two barriers).
+__device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t *kmin, uint32_t *kmax,
+                              uint32_t *red /* 3 * kWarps */) {
+  uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
+  for (int x = threadIdx.x; x < n; x += kThreads) {
+    const uint32_t k = keys[x];
+    if (k != 0u) {
+      ++c;
+      lo = min(lo, k);
+      hi = max(hi, k);
+    }
+  }
+  block_stats(c, lo, hi, red, count, kmin, kmax);
 }
 
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
@@ -529,12 +530,22 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   const int p1 = min(P, p0 + a.chunk);
   const int n = p1 - p0;
   const uint32_t *krow = a.keys + (size_t)unit * a.max_pages + p0;
-  for (int x = tid; x < n; x += kThreads) keys[x] = __ldcg(krow + x);
-  for (int x = tid; x < kWarps * 256; x += kThreads) hist[x] = 0;
-  __syncthreads();
   int total_valid;
   uint32_t kmin, kmax;
-  nonzero_stats(keys, n, &total_valid, &kmin, &kmax, red);
+  {  // keys to shared memory, with the count, min and max of the nonzero ones on the way
+    uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
+    for (int x = tid; x < n; x += kThreads) {
+      const uint32_t k = __ldcg(krow + x);
+      keys[x] = k;
+      if (k != 0u) {
+        ++c;
+        lo = min(lo, k);
+        hi = max(hi, k);
+      }
+    }
+    for (int x = tid; x < kWarps * 256; x += kThreads) hist[x] = 0;
+    block_stats(c, lo, hi, red, &total_valid, &kmin, &kmax);  // its barrier also publishes keys[]
+  }
   int wrote = 0;
   if (k_free > 0) {
     uint32_t thr = 0;
