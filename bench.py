@@ -60,7 +60,10 @@ TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
     ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel+page_select_kernel"):
-        {"bytes": 579_010_000 + 5_100_000 + 4_630_000, "digest": "RECAPTURE"},
+        {"bytes": 579_110_000 + 4_910_000 + 4_630_000, "digest": "cc196af5753a9e1c"},
+    # ncu ... -k regex:"mla_decode" -s 0 -c 1 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
+    ("mla-b16-128k-5pct", "mla_decode_kernel"):
+        {"bytes": 124_100_000 + 2_630_000, "digest": "7b7ccb4781475091"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
         {"bytes": 466_990_000 + 1_750_000, "digest": "316441adf4e514da"},
 }
