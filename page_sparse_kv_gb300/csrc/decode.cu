@@ -423,6 +423,46 @@ __device__ __forceinline__ void write_partial(const DecodeArgs &a, size_t slot, 
   }
 }
 
+// The same merge of the warps written straight to the G output rows (normalised by l): for a
+// unit that one CTA covers entirely.
+template <typename T, int D, int G, int NW, int NST>
+__device__ __forceinline__ void write_output(const DecodeArgs &a, int unit, float (&m)[G], float (&l)[G],
+                                             float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2], float *wO, float *wML) {
+  using TR = DT<T, D, G, NW, NST>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float x = l[g];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+#pragma unroll
+    for (int e = 0; e < TR::VPL / 2; ++e)
+      reinterpret_cast<float2 *>(wO + (warp * G + g) * D + lane * TR::VPL)[e] = O[g][e];
+    if (lane == 0) {
+      wML[(warp * G + g) * 2] = m[g];
+      wML[(warp * G + g) * 2 + 1] = x;
+    }
+  }
+  __syncthreads();
+  T *out = reinterpret_cast<T *>(a.out) + ((size_t)(unit / a.H_kv) * a.H_q + (size_t)(unit % a.H_kv) * G) * D;
+  for (int idx = tid; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wML[(w * G + g) * 2]);
+    float acc = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float sc = exp2f(wML[(w * G + g) * 2] - M);
+        acc = fmaf(sc, wO[(w * G + g) * D + d], acc);
+        L = fmaf(sc, wML[(w * G + g) * 2 + 1], L);
+      }
+    }
+    Elem<T>::store(out + idx, L > 0.f ? acc / L : 0.f);
+  }
+}
+
 template <typename T, int D, int G, int NW, int NST>
 struct DecodeSmem {
   using TR = DT<T, D, G, NW, NST>;
@@ -451,8 +491,10 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   __shared__ __align__(8) uint64_t bars[NW][NST];
   __shared__ int flag_last;
 
-  const int s = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
-  const int unit = i * a.H_kv + h;
+  // blockIdx.x = unit, blockIdx.y = split: CTAs are launched split-major, so every unit's first
+  // (full) splits run before the shorter last splits and the tail of the grid is short work
+  const int unit = blockIdx.x, s = blockIdx.y;
+  const int i = unit / a.H_kv, h = unit - i * a.H_kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
@@ -475,6 +517,17 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   load_entries<NW * 32>(a, i, unit, P, seq_len, e0, n_ent, sm.ent_blk, sm.ent_valid);
   __syncthreads();
 
+  // a unit whose whole list fits this split (sparse: no entry at index sw) needs no partials and
+  // no merge: split 0 writes the normalised output and the other splits leave at once
+  bool alone = false;
+  if (a.selected) {
+    const int32_t *row = a.selected + (size_t)unit * a.b_max;
+    alone = a.n_items_max == 1 || a.b_max <= a.sw || row[a.sw] < 0;
+  } else {
+    alone = a.n_items_max == 1 || P <= a.sw;
+  }
+  if (alone && s > 0) return;
+
   if (n_ent > 0) {
     float2 q2[G][TR::CPL * TR::EPC / 2];
     load_q<T, D, G, NW, NST>(a, i, h, lane & 7, q2);
@@ -491,7 +544,15 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
     warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages, sm.pp_all, bars, cw,
                                  m, l, O);
     __syncthreads();  // every warp is done with the stages; the merge below reuses them
+    if (alone) {
+      write_output<T, D, G, NW, NST>(a, unit, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
+      return;
+    }
     write_partial<T, D, G, NW, NST>(a, pbase, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
+  } else if (alone) {  // nothing to read and nothing to merge: zero rows
+    T *out = reinterpret_cast<T *>(a.out) + ((size_t)i * a.H_q + (size_t)h * G) * D;
+    for (int idx = tid; idx < G * D; idx += NW * 32) Elem<T>::store(out + idx, 0.f);
+    return;
   } else if (tid < G) {  // nothing to read: an empty partial
     a.part_ml[(pbase * G + tid) * 2] = -INFINITY;
     a.part_ml[(pbase * G + tid) * 2 + 1] = 0.f;
@@ -682,7 +743,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     auto kfn = decode_split_kernel<T, D, G, NW, NST>;
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_items_max, a.H_kv, a.B);
+    dim3 grid(a.B * a.H_kv, a.n_items_max);
     kfn<<<grid, NW * 32, TR::SMEM, s>>>(a, tmK, tmV);
     return cudaGetLastError();
   }
