@@ -40,6 +40,7 @@ constexpr int kMaxItems = 256; // splits per (sequence, KV head), upper bound (b
 constexpr int kFlatMaxCtas = 2048;   // grid of the flat layout, upper bound (sizes the partials)
 constexpr int kFlatMaxUnits = 4096;  // units the flat layout takes (its prefix sums live in shared memory)
 constexpr long long kFlatMinShare = 8;  // list entries per CTA of the flat layout, lower bound
+constexpr int kFastMerge = 8;          // partials a unit merge reads in one round trip
 
 template <typename T, int D, int G, int NW, int NST>
 struct DT {
@@ -91,10 +92,41 @@ __device__ __forceinline__ void reduce_dg(float (&v)[NV], int lane) {
 // The last CTA of a unit: merge its n partials (m, l, O) at slots it0 .. it0 + n - 1 by
 // log-sum-exp into the G output rows.
 // wsm: >= n * G floats of shared memory; red: >= 2 * G * NW floats.
-template <typename T, int D, int G, int NW>
+template <typename T, int D, int G, int NW, bool kFast>
 __device__ void merge_unit(const DecodeArgs &a, int unit, size_t it0, int n, float *wsm, float *red) {
   constexpr int NT = NW * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (kFast && n <= kFastMerge) {
+    // Few partials: every thread reads the (m, l) of its head from all of them together with its
+    // O elements (independent loads, one round trip) and merges on its own, without barriers.
+    T *out = reinterpret_cast<T *>(a.out) + ((size_t)(unit / a.H_kv) * a.H_q + (size_t)(unit % a.H_kv) * G) * D;
+#pragma unroll 1
+    for (int idx = tid; idx < G * D; idx += NT) {
+      const int g = idx / D;
+      float mk[kFastMerge], lk[kFastMerge], ok[kFastMerge];
+#pragma unroll
+      for (int k = 0; k < kFastMerge; ++k)
+        if (k < n) {
+          mk[k] = __ldcg(a.part_ml + ((it0 + k) * G + g) * 2);
+          lk[k] = __ldcg(a.part_ml + ((it0 + k) * G + g) * 2 + 1);
+          ok[k] = __ldcg(a.part_o + (it0 + k) * G * D + idx);
+        }
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kFastMerge; ++k)
+        if (k < n) M = fmaxf(M, mk[k]);
+      float acc = 0.f, L = 0.f;
+#pragma unroll
+      for (int k = 0; k < kFastMerge; ++k)
+        if (k < n && mk[k] != -INFINITY) {
+          const float w = exp2f(mk[k] - M);
+          acc = fmaf(w, ok[k], acc);
+          L = fmaf(w, lk[k], L);
+        }
+      Elem<T>::store(out + idx, L > 0.f ? acc / L : 0.f);
+    }
+    return;
+  }
   // 1. per-head max of m over the partials
   float mx[G];
 #pragma unroll
@@ -569,7 +601,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   if (!flag_last) return;
   __threadfence();
   if (tid == 0) a.tickets[unit] = 0u;
-  merge_unit<T, D, G, NW>(a, unit, (size_t)unit * a.n_items_max, a.n_items_max, reinterpret_cast<float *>(sm.stages),
+  merge_unit<T, D, G, NW, true>(a, unit, (size_t)unit * a.n_items_max, a.n_items_max, reinterpret_cast<float *>(sm.stages),
                           sm.wML);
 }
 
@@ -720,7 +752,7 @@ __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, cons
     if (flag_last) {
       __threadfence();
       if (tid == 0) a.tickets[u] = 0u;
-      merge_unit<T, D, G, NW>(a, u, (size_t)c_first + u, nseg, reinterpret_cast<float *>(sm.stages), sm.wML);
+      merge_unit<T, D, G, NW, false>(a, u, (size_t)c_first + u, nseg, reinterpret_cast<float *>(sm.stages), sm.wML);
     }
     e = seg_end;
   }

@@ -655,9 +655,11 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   plan->chunk = chunk;
   plan->n_chunks_max = (L.max_pages + chunk - 1) / chunk;
   plan->k_cap = std::min(kfree_max, chunk);
-  // pages per streaming CTA: fill the GPU a few times over
+  // pages per streaming CTA: 64 (measured best on the batched workload: many waves, so the
+  // last one is a small part of the launch); fewer while the grid would not fill the GPU a few
+  // times over
   const long long head_groups = L.num_kv_heads > kWarps ? L.num_kv_heads / kWarps : 1;
-  int pchunk = 128;
+  int pchunk = 64;
   while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152 * 2)
     pchunk /= 2;
   if (const char *env = std::getenv("PSK_SCORE_PCHUNK")) {  // tuning override: pages per score CTA
