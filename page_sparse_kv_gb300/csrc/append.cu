@@ -86,6 +86,37 @@ __global__ void append_summarize_kernel(AppendArgs a) {
   T *kc = reinterpret_cast<T *>(a.k_cache);
   T *sm = reinterpret_cast<T *>(a.summaries);
 
+  const int ncv = a.v_cache ? a.H_kv * (a.D_v / EPC) : 0;  // latent cache: the value is part of the key row
+  const size_t row_v = (size_t)a.H_kv * a.D_v;
+  const T *vn = reinterpret_cast<const T *>(a.v_new);
+  T *vc = reinterpret_cast<T *>(a.v_cache);
+  if (t_hi - t_lo == 1 && nck <= (int)blockDim.x && ncv <= (int)blockDim.x) {
+    // one new token on this page (the decode step): every load of the thread is issued before
+    // any store, so the page costs one round trip after its block id
+    const int c = threadIdx.x;
+    const int t = t_lo;
+    uint4 x{}, olo{}, ohi{}, xv{};
+    T *sum_lo = nullptr;
+    if (c < nck) {
+      const int h = c / cpr_k;
+      const int e0 = (c - h * cpr_k) * EPC;
+      sum_lo = sm + ((size_t)blk * a.H_kv + h) * 2 * a.D + e0;
+      x = __ldg(reinterpret_cast<const uint4 *>(kn + (size_t)(c0 + t - s0) * row_k + (size_t)c * EPC));
+      if (!fresh) {
+        olo = *reinterpret_cast<const uint4 *>(sum_lo);
+        ohi = *reinterpret_cast<const uint4 *>(sum_lo + a.D);
+      }
+    }
+    if (c < ncv) xv = __ldg(reinterpret_cast<const uint4 *>(vn + (size_t)(c0 + t - s0) * row_v + (size_t)c * EPC));
+    if (c < nck) {
+      *reinterpret_cast<uint4 *>(kc + ((size_t)blk * ps + (t - p * ps)) * row_k + (size_t)c * EPC) = x;
+      *reinterpret_cast<uint4 *>(sum_lo) = fresh ? x : chunk_min<T>(olo, x);
+      *reinterpret_cast<uint4 *>(sum_lo + a.D) = fresh ? x : chunk_max<T>(ohi, x);
+    }
+    if (c < ncv) *reinterpret_cast<uint4 *>(vc + ((size_t)blk * ps + (t - p * ps)) * row_v + (size_t)c * EPC) = xv;
+    return;
+  }
+
   for (int c = threadIdx.x; c < nck; c += blockDim.x) {
     const int h = c / cpr_k;
     const int e0 = (c - h * cpr_k) * EPC;
@@ -112,11 +143,6 @@ __global__ void append_summarize_kernel(AppendArgs a) {
     *reinterpret_cast<uint4 *>(sum_hi) = hi;
   }
 
-  if (a.v_cache == nullptr) return;  // latent cache: the value is part of the key row
-  const int ncv = a.H_kv * (a.D_v / EPC);
-  const size_t row_v = (size_t)a.H_kv * a.D_v;
-  const T *vn = reinterpret_cast<const T *>(a.v_new);
-  T *vc = reinterpret_cast<T *>(a.v_cache);
   for (int c = threadIdx.x; c < ncv; c += blockDim.x) {
     for (int t = t_lo; t < t_hi; ++t) {
       const uint4 x = *reinterpret_cast<const uint4 *>(vn + (size_t)(c0 + t - s0) * row_v + (size_t)c * EPC);

@@ -815,15 +815,15 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
     plan->n_items_max = 1;
     slots = (size_t)kFlatMaxCtas + (size_t)units;
   } else {
-    // 64 list entries per CTA (measured best on the batched workload); fewer while the grid
-    // would not fill the GPU (152 SMs x 2 CTAs) a few times over, more when a unit would need
-    // over kMaxItems partials
+    // 64 list entries per CTA (measured best on the batched workload); fewer (down to 8) while
+    // the grid would not fill the GPU (152 SMs x 2 CTAs) a few times over, more when a unit
+    // would need over kMaxItems partials
     int sw = 64;
+    while (sw > 8 && units * ((entries + sw - 1) / sw) < 4LL * 152 * 2) sw /= 2;  // 8: measured best at B = 1
     if (const char *env = std::getenv("PSK_DECODE_SPLIT")) {  // tuning override: entries per CTA
       const int v = std::atoi(env);
       if (v >= 1 && v <= kSwMax) sw = v;
     }
-    while (sw > 4 && units * ((entries + sw - 1) / sw) < 4LL * 152 * 2) sw /= 2;
     while (sw < kSwMax && (entries + sw - 1) / sw > kMaxItems) sw *= 2;
     plan->sw = sw;
     plan->n_items_max = (entries + sw - 1) / sw;
