@@ -226,6 +226,7 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.sw = plan.sw;
   a.n_items_max = plan.n_items_max;
   a.flat = plan.flat;
+  a.taper = plan.taper;
   a.counts = reinterpret_cast<int32_t *>(ws + plan.off_counts);
   a.scale = scale;
   if (L.latent) return cuda_status(launch_mla_decode(a, static_cast<cudaStream_t>(stream)));

@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
-  const int e0 = s * a.sw;
+  const int e0 = split_off(s, a.sw, a.taper), len = split_len(s, a.sw, a.taper);
   const size_t pbase = (size_t)unit * a.n_items_max + s;
 
   int n_ent = 0;
@@ -538,9 +538,9 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
     if (s == 0 && tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
   } else if (a.selected) {
     const int32_t *row = a.selected + (size_t)unit * a.b_max;
-    if (e0 < a.b_max && row[e0] >= 0) n_ent = min(a.sw, a.b_max - e0);
+    if (e0 < a.b_max && row[e0] >= 0) n_ent = min(len, a.b_max - e0);
   } else if (e0 < P) {
-    n_ent = min(a.sw, P - e0);
+    n_ent = min(len, P - e0);
   }
   if (lane == 0) {
     for (int k = 0; k < NST; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
@@ -813,6 +813,7 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
   if (flat) {
     plan->sw = kSwMax;
     plan->n_items_max = 1;
+    plan->taper = 0;
     slots = (size_t)kFlatMaxCtas + (size_t)units;
   } else {
     // 64 list entries per CTA (measured best on the batched workload); fewer (down to 8) while
@@ -827,6 +828,16 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
     while (sw < kSwMax && (entries + sw - 1) / sw > kMaxItems) sw *= 2;
     plan->sw = sw;
     plan->n_items_max = (entries + sw - 1) / sw;
+    plan->taper = 0;
+    // sparse lists longer than one split: tapered splits when they stay few enough to merge
+    if (!dense && entries > sw && !std::getenv("PSK_DECODE_NO_TAPER")) {
+      int n = 0;
+      while (split_off(n, sw, 1) < entries) ++n;
+      if (n <= kMaxItems) {
+        plan->taper = 1;
+        plan->n_items_max = n;
+      }
+    }
     slots = (size_t)units * plan->n_items_max;
   }
   plan->flat = flat ? 1 : 0;

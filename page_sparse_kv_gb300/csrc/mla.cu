@@ -142,17 +142,20 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
   if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
   const int p0 = tile * 128;
   if (p0 >= P) return;
-  const int r = tid;  // this thread's page row and head row
-  const int p = p0 + r;
-  bool ok = false;
-  int blk = 0;
-  if (p < P) {
-    blk = a.block_table[(size_t)i * a.max_pages + p];
-    ok = blk >= 0 && blk < a.nb;
-    if (!ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+  // block id of every page row of the tile (0 and not loaded for rows past P or a bad block)
+  __shared__ int row_blk[128];
+  {
+    const int p = p0 + tid;
+    int blk = -1;
+    if (p < P) {
+      blk = a.block_table[(size_t)i * a.max_pages + p];
+      if (blk < 0 || blk >= a.nb) {
+        set_status(a.ws, PSK_DEV_BAD_BLOCK);
+        blk = -1;
+      }
+    }
+    row_blk[tid] = blk;
   }
-  const uint16_t *srow = reinterpret_cast<const uint16_t *>(a.summaries) + (size_t)(ok ? blk : 0) * 2 * kD;
-  const uint16_t *qrow = qs + ((size_t)i * kHeads + r) * 2 * kD;
 
   if (tid == 0) {
     for (int k = 0; k < kScStages; ++k) mbar_init(smem_u32(&bars[k]), 1);
@@ -163,14 +166,22 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tslot;
+  const uint16_t *qbase = qs + (size_t)i * kHeads * 2 * kD;
+  const uint16_t *sbase = reinterpret_cast<const uint16_t *>(a.summaries);
 
+  // One 64-element K block of 128 page rows and 128 head rows, 128-byte swizzle. Eight
+  // consecutive threads copy the eight 16-byte chunks of one row, so every request of a warp
+  // covers whole 128-byte lines.
   auto fill = [&](int kb, int st) {
     const uint32_t sa = smem_u32(base + st * kScStage), sb = sa + 16384;
+    const int c = tid & 7;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int k = 0; k < 8; ++k) {
+      const int r = (tid >> 3) + 16 * k;
       const uint32_t off = r * 128 + ((c ^ (r & 7)) * 16);
-      cp_async16(sa + off, srow + kb * 64 + c * 8, ok);
-      cp_async16(sb + off, qrow + kb * 64 + c * 8, true);
+      const int blk = row_blk[r];
+      cp_async16(sa + off, sbase + (size_t)(blk < 0 ? 0 : blk) * 2 * kD + kb * 64 + c * 8, blk >= 0);
+      cp_async16(sb + off, qbase + (size_t)r * 2 * kD + kb * 64 + c * 8, true);
     }
   };
   fill(0, 0);
@@ -209,10 +220,11 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
 #pragma unroll
     for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
   }
+  const int p = p0 + tid;  // this thread's tensor-memory lane = page row
   if (p < P) {
     const float sc = mx * a.scale;
     const bool forced = (p == 0) || (p == P - 1);
-    a.keys[(size_t)i * a.max_pages + p] = (ok && !forced) ? score_key(sc) : 0u;
+    a.keys[(size_t)i * a.max_pages + p] = (row_blk[tid] >= 0 && !forced) ? score_key(sc) : 0u;
     if (a.scores_out) a.scores_out[(size_t)i * a.max_pages + p] = sc;
   }
   tc_fence_before();
@@ -681,6 +693,7 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   plan->ws_bytes = off;
   plan->off_tickets = ws_decode_tickets_offset((size_t)units);
   plan->flat = 0;
+  plan->taper = 0;
   plan->off_counts = 0;
   return plan->n_items_max <= kMlaMaxItems;
 }

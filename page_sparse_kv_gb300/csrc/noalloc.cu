@@ -102,6 +102,7 @@ extern "C" int psk_sparse_paged_decode_noalloc(const psk_layout *layout, const v
   a.sw = plan.sw;
   a.n_items_max = plan.n_items_max;
   a.flat = plan.flat;
+  a.taper = plan.taper;
   a.counts = reinterpret_cast<int32_t *>(ws + plan.off_counts);
   a.scale = scale;
   return launch_decode(a, L.dtype, s) == cudaSuccess ? PSK_OK : PSK_ERR_CUDA;

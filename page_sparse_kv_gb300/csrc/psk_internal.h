@@ -74,13 +74,29 @@ struct DecodeArgs {
   int n_items_max;     // items per unit (split layout)
   int32_t *counts;     // [B * H_kv] list entries per unit (flat layout, sparse)
   int flat;            // 1: flat layout (the units' lists cut into equal shares of a persistent grid)
+  int taper;           // split layout: 1 = split lengths halve every two splits (see split_len)
   float scale;
 };
 struct DecodePlan {
-  int sw, n_items_max, flat;
+  int sw, n_items_max, flat, taper;
   size_t ws_bytes, off_o, off_ml, off_tickets, off_counts;
 };
 bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan);
+// Split layout: list entries of split s, and where it starts. With taper, the lengths are
+// sw, sw, sw/2, sw/2, sw/4, ... (never below min(8, sw)): CTAs launch split-major, so the last
+// CTAs of the grid carry the shortest pieces.
+__host__ __device__ inline int split_len(int s, int sw, int taper) {
+  if (!taper) return sw;
+  const int floor_len = sw < 8 ? sw : 8;
+  const int v = (s >> 1) >= 31 ? 0 : (sw >> (s >> 1));
+  return v > floor_len ? v : floor_len;
+}
+__host__ __device__ inline int split_off(int s, int sw, int taper) {
+  if (!taper) return s * sw;
+  int o = 0;
+  for (int j = 0; j < s; ++j) o += split_len(j, sw, 1);
+  return o;
+}
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);
 bool decode_supported(int dtype, int D, int D_v, int G, int ps);
 
