@@ -1,0 +1,118 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each test swaps one oracle function for a copy with a typical slip (a dropped term, a wrong
+reduction, a tie broken the other way, the tail not forced, tokens past seq_len counted, signed
+zeros confused, the scale left out) and checks that a pin of test_oracle_pins.py then fails. The
+mistakes are planted in the oracle only, on the CPU; nothing here touches a GPU.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.psk_oracle as OP
+import test_oracle_pins as PINS
+
+ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention")}
+
+
+@pytest.fixture
+def plant(monkeypatch):
+    def _plant(name, fn):
+        monkeypatch.setattr(OP, name, fn)  # calls inside the oracle module
+        monkeypatch.setattr(O, name, fn)   # calls through the package, as the pins make them
+    return _plant
+
+
+def _fails(pin, *args):
+    with pytest.raises(AssertionError):
+        pin(*args)
+
+
+# ---- planted mistakes ---------------------------------------------------------------------
+def _quest_kmax_only(q, kmin, kmax, dtype, scale):  # drops the q * kmin term
+    return ORIG["quest_scores"](q, kmax, kmax, dtype, scale)
+
+
+def _quest_group_mean(q, kmin, kmax, dtype, scale):  # mean over the GQA group instead of max
+    qv, lo, hi = O.to_f64(q, dtype), O.to_f64(kmin, dtype), O.to_f64(kmax, dtype)
+    G = qv.shape[0] // lo.shape[1]
+    per = [[np.maximum(qv[h * G + j] * lo[:, h, :], qv[h * G + j] * hi[:, h, :]).sum(axis=1) for j in range(G)]
+           for h in range(lo.shape[1])]
+    return np.stack([np.mean(p, axis=0) for p in per]) * scale
+
+
+def _quest_no_scale(q, kmin, kmax, dtype, scale):  # forgets 1/sqrt(D)
+    return ORIG["quest_scores"](q, kmin, kmax, dtype, 1.0)
+
+
+def _select_ties_high(scores, budget):  # ties go to the higher page index
+    P = len(scores)
+    forced = O.forced_pages(P)
+    count = min(budget, P)
+    ranked = sorted((p for p in range(P) if p not in forced), key=lambda p: (-float(scores[p]), -p))
+    return sorted(forced + ranked[:count - len(forced)])
+
+
+def _select_tail_not_forced(scores, budget):  # only the sink is forced
+    P = len(scores)
+    count = min(budget, P)
+    ranked = sorted(range(1, P), key=lambda p: (-float(scores[p]), p))
+    return sorted([0] + ranked[:count - 1])
+
+
+def _summaries_whole_pages(keys, seq_len, page_size, dtype):  # counts the tail page's junk rows
+    P = -(-seq_len // page_size)
+    return ORIG["page_summaries"](keys, min(len(keys), P * page_size), page_size, dtype)
+
+
+def _summaries_plain_minmax(keys, seq_len, page_size, dtype):  # -0.0 and +0.0 compare equal
+    v = O.to_f64(keys, dtype)[:seq_len]
+    P = -(-seq_len // page_size)
+    lo = np.stack([v[p * page_size:(p + 1) * page_size].min(axis=0) for p in range(P)])
+    hi = np.stack([v[p * page_size:(p + 1) * page_size].max(axis=0) for p in range(P)])
+    return O.exact_to_storage(lo, dtype), O.exact_to_storage(hi, dtype)
+
+
+def _attention_unscaled(q, k, v, scale):  # logits without the scale
+    return ORIG["softmax_attention"](q, k, v, 1.0)
+
+
+# ---- each one is caught -------------------------------------------------------------------
+def test_dropped_kmin_term_is_caught(plant):
+    plant("quest_scores", _quest_kmax_only)
+    _fails(PINS.test_bound_dominates_every_token_logit, 0)
+
+
+def test_group_mean_instead_of_max_is_caught(plant):
+    plant("quest_scores", _quest_group_mean)
+    _fails(PINS.test_bound_group_max_and_scale)
+
+
+def test_missing_scale_is_caught(plant):
+    plant("quest_scores", _quest_no_scale)
+    _fails(PINS.test_bound_group_max_and_scale)
+
+
+def test_ties_to_higher_index_are_caught(plant):
+    plant("select_pages", _select_ties_high)
+    _fails(PINS.test_selection_tie_lower_index_wins_on_copied_page)
+
+
+def test_tail_not_forced_is_caught(plant):
+    plant("select_pages", _select_tail_not_forced)
+    _fails(PINS.test_selection_brute_force_subsets, 5)
+
+
+def test_tokens_past_seq_len_in_summaries_are_caught(plant):
+    plant("page_summaries", _summaries_whole_pages)
+    _fails(PINS.test_summary_bounds_attained_and_tail_masked, "f32", 16, 16 * 5 + 3)
+
+
+def test_signed_zero_order_is_caught(plant):
+    plant("page_summaries", _summaries_plain_minmax)
+    _fails(PINS.test_summary_signed_zero_order)
+
+
+def test_unscaled_attention_is_caught(plant):
+    plant("softmax_attention", _attention_unscaled)
+    _fails(PINS.test_dense_equals_library_attention_and_full_budget_equals_dense, "f32", 16, 16 * 6 + 5)
