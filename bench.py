@@ -60,12 +60,12 @@ TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
     ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel+page_select_kernel"):
-        {"bytes": 579_110_000 + 4_910_000 + 4_630_000, "digest": "cc196af5753a9e1c"},
+        {"bytes": 578_770_000 + 5_670_000 + 4_630_000, "digest": "9bf36a667019a5b6"},
     # ncu ... -k regex:"mla_decode" -s 0 -c 1 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
     ("mla-b16-128k-5pct", "mla_decode_kernel"):
-        {"bytes": 124_100_000 + 2_630_000, "digest": "7b7ccb4781475091"},
+        {"bytes": 124_100_000 + 2_960_000, "digest": "38d10a9193009fbd"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 466_990_000 + 1_750_000, "digest": "316441adf4e514da"},
+        {"bytes": 468_580_000 + 1_660_000, "digest": "93d5ad7fdf55b742"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel+page_select_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
