@@ -162,6 +162,7 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.ws = workspace;
   a.counters = reinterpret_cast<uint32_t *>(ws + plan.off_counters);
   a.keys = reinterpret_cast<uint32_t *>(ws + plan.off_keys);
+  a.key_stride = (L.max_pages + 3) & ~3;
   a.cand_key = reinterpret_cast<uint32_t *>(ws + plan.off_key);
   a.cand_page = reinterpret_cast<int32_t *>(ws + plan.off_page);
   a.cand_count = reinterpret_cast<int32_t *>(ws + plan.off_count);

@@ -283,8 +283,9 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
         mbar_arrive_expect_tx(bar, 2u * TR::TILE);
         const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
         const int row = ent_blk[e] * a.ps + sub * 16;
-        tma_load_3d(sK, tmK, 0, h, row, bar);
-        tma_load_3d(sK + TR::TILE, tmV, 0, h, row, bar);
+        const uint64_t pol = l2_evict_first_policy();  // K/V rows are read once per step
+        tma_load_3d_stream(sK, tmK, 0, h, row, bar, pol);
+        tma_load_3d_stream(sK + TR::TILE, tmV, 0, h, row, bar, pol);
       } else {
         mbar_arrive_expect_tx(bar, 0u);
       }

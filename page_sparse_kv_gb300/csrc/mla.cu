@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
   if (p < P) {
     const float sc = mx * a.scale;
     const bool forced = (p == 0) || (p == P - 1);
-    a.keys[(size_t)i * a.max_pages + p] = (row_blk[tid] >= 0 && !forced) ? score_key(sc) : 0u;
+    a.keys[(size_t)i * a.key_stride + p] = (row_blk[tid] >= 0 && !forced) ? score_key(sc) : 0u;
     if (a.scores_out) a.scores_out[(size_t)i * a.max_pages + p] = sc;
   }
   tc_fence_before();

@@ -39,6 +39,7 @@ struct ScoreArgs {
   int32_t *cand_page;     // same shape
   int32_t *cand_count;    // [B * H_kv, n_chunks_max]
   int B, H_q, H_kv, D, ps, nb, max_pages, b_max;
+  int key_stride;         // keys per (sequence, KV head) row of `keys`: max_pages rounded up to 4
   int pchunk;             // pages per streaming score CTA
   int stage_pages;        // pages per shared-memory stage of the score kernel
   int chunk;              // pages per selection CTA

@@ -297,6 +297,9 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
     const int p = p0 + st * sp + lane;
     return (lane < sp && st < n_stages && p < p1) ? __ldg(bt + p) : -1;
   };
+  // the summaries are read once per step and exceed L2: keep them from evicting what the select
+  // and decode kernels read next (keys, selected rows, partials)
+  const uint64_t stream_policy = l2_evict_first_policy();
   // warp 0: fetch the pages of stage `st` (chunk-local stage index) into ring slot st % kStages
   auto produce = [&](int st, int blk) {
     const int slot = st % kStages;
@@ -311,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
     if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(mask) * group_bytes);
     __syncwarp();
     if (ok)
-      bulk_g2s(smem_u32(smem_raw + (size_t)slot * kStageBytes + (size_t)lane * group_bytes),
-               sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar);
+      bulk_g2s_stream(smem_u32(smem_raw + (size_t)slot * kStageBytes + (size_t)lane * group_bytes),
+                      sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar, stream_policy);
   };
 
   if (warp == 0)
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
       }
     }
   }
-  uint32_t *krow = a.keys + (size_t)unit * a.max_pages;
+  uint32_t *krow = a.keys + (size_t)unit * a.key_stride;
   float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
   // this lane's byte offset inside a page's run: its head and its chunk
   const uint32_t lane_off = (uint32_t)hh * 2 * D * ES + sub * 16;
@@ -529,19 +532,31 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   const int p0 = c * a.chunk;
   const int p1 = min(P, p0 + a.chunk);
   const int n = p1 - p0;
-  const uint32_t *krow = a.keys + (size_t)unit * a.max_pages + p0;
+  const uint32_t *krow = a.keys + (size_t)unit * a.key_stride + p0;  // 16-byte aligned (stride, p0: x4)
   int total_valid;
   uint32_t kmin, kmax;
-  {  // keys to shared memory, with the count, min and max of the nonzero ones on the way
+  {  // keys to shared memory, four per load, with the count, min and max of the nonzero ones
     uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
-    for (int x = tid; x < n; x += kThreads) {
-      const uint32_t k = __ldcg(krow + x);
-      keys[x] = k;
+    auto take = [&](uint32_t k) {
       if (k != 0u) {
         ++c;
         lo = min(lo, k);
         hi = max(hi, k);
       }
+    };
+    const int n4 = n >> 2;
+    for (int x = tid; x < n4; x += kThreads) {
+      const uint4 k4 = __ldcg(reinterpret_cast<const uint4 *>(krow) + x);
+      reinterpret_cast<uint4 *>(keys)[x] = k4;
+      take(k4.x);
+      take(k4.y);
+      take(k4.z);
+      take(k4.w);
+    }
+    for (int x = 4 * n4 + tid; x < n; x += kThreads) {
+      const uint32_t k = __ldcg(krow + x);
+      keys[x] = k;
+      take(k);
     }
     for (int x = tid; x < kWarps * 256; x += kThreads) hist[x] = 0;
     block_stats(c, lo, hi, red, &total_valid, &kmin, &kmax);  // its barrier also publishes keys[]
@@ -678,7 +693,7 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   plan->off_counters = ws_score_tickets_offset();
   size_t off = ws_scratch_offset(units);
   plan->off_keys = off;
-  off = align_up(off + units * (size_t)L.max_pages * 4, 256);
+  off = align_up(off + units * (size_t)((L.max_pages + 3) & ~3) * 4, 256);
   plan->off_key = off;
   off = align_up(off + units * plan->n_chunks_max * plan->k_cap * 4, 256);
   plan->off_page = off;
