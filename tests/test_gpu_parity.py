@@ -276,6 +276,42 @@ def test_host_argument_errors():
     assert e.value.code == 1
 
 
+def test_split_count_does_not_change_the_output(monkeypatch):
+    """Split-K over the page list with an LSE merge must not change the result beyond fp32
+    rounding: the same sparse decode (fp32 cache) with splits of 1, 2, 7 and 64 list entries and
+    the default (tapered) splits, each against the default and against the oracle."""
+    w = _custom([16 * 300 + 5, 16 * 77, 16 * 40 + 9], [40, 23, 41], dtype="f32", D=64, H_q=4, H_kv=1)
+    cache = upload(w)
+    q_np = w.queries()
+    q = to_torch(q_np, w.dtype).cuda()
+    sel = cache.score_select(q, dev_budgets(w))
+    outs = {}
+    for sw in (None, 1, 2, 7, 64):
+        if sw is None:
+            monkeypatch.delenv("PSK_DECODE_SPLIT", raising=False)
+        else:
+            monkeypatch.setenv("PSK_DECODE_SPLIT", str(sw))
+        ws = psk.make_workspace(cache.layout, cache.b_max, device="cuda")  # sized for this split
+        out = torch.empty(w.B, w.H_q, w.D_v, dtype=cache.dtype, device="cuda")
+        psk.sparse_paged_decode(cache.layout, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
+                                cache.b_max, cache.scale, out, ws)
+        torch.cuda.synchronize()
+        assert psk.get_device_status(ws) == 0
+        outs[sw] = from_torch(out.float(), "f32").astype(np.float64)
+    monkeypatch.delenv("PSK_DECODE_SPLIT", raising=False)
+    ref = outs[None]
+    for sw, o in outs.items():
+        for i in range(w.B):
+            assert np.abs(o[i] - ref[i]).max() <= 1e-5 * np.abs(ref[i]).max(), f"split {sw} seq {i}"
+    sel_np = sel.cpu().numpy()
+    scale = 1.0 / math.sqrt(w.D)
+    for i in range(w.B):
+        n = int(w.seq_lens[i])
+        use = [[int(x) for x in sel_np[i, h] if x >= 0] for h in range(w.H_kv)]
+        check_output(outs[1][i], O.attend_pages(q_np[i], w.keys(i), w.values(i), n, w.page_size, use, w.dtype, scale),
+                     w.dtype)
+
+
 def test_full_budget_sparse_equals_dense_bitwise():
     """With b >= P every page is selected; the sparse and dense calls then run the same tiles
     in the same split layout and must agree exactly."""
