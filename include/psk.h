@@ -149,6 +149,9 @@ int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, con
  *   scores_out [batch, num_kv_heads, max_pages] fp32 out, optional (NULL = not written):
  *             the scores above for p < P_i; entries p >= P_i are left untouched.
  * Scores accumulate in fp32. scale is normally 1/sqrt(head_dim).
+ * Without scores_out the summaries of the sink and the tail page are not read (those pages
+ * are kept whatever their score), so a one-token decode append, which touches only the tail
+ * page, may run concurrently with this call on another stream.
  * --------------------------------------------------------------------------------------- */
 int psk_page_score_select(const psk_layout *layout, const void *q, const void *summaries,
                           const int32_t *block_table, const int32_t *seq_lens,

@@ -153,6 +153,8 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
         set_status(a.ws, PSK_DEV_BAD_BLOCK);
         blk = -1;
       }
+      // sink and tail are kept whatever their score: not read unless scores are requested
+      if (!a.scores_out && (p == 0 || p == P - 1)) blk = -1;
     }
     row_blk[tid] = blk;
   }

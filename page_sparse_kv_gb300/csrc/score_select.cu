@@ -305,8 +305,12 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
     const int slot = st % kStages;
     const int p = p0 + st * sp + lane;
     const bool in_chunk = lane < sp && p < p1;
-    const bool ok = in_chunk && blk >= 0 && blk < a.nb;
-    if (in_chunk && !ok) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+    const bool valid = blk >= 0 && blk < a.nb;
+    if (in_chunk && !valid) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+    // the sink and the tail are kept whatever their score: without scores_out their summaries
+    // are not read (so an append to the tail page may run concurrently)
+    const bool needed = a.scores_out != nullptr || (p != 0 && p != P - 1);
+    const bool ok = in_chunk && valid && needed;
     if (lane < sp) okflag[slot][lane] = ok;
     const unsigned mask = __ballot_sync(0xffffffffu, ok);
     const uint32_t bar = smem_u32(&bars[slot]);
