@@ -40,7 +40,11 @@ struct ScoreArgs {
   int32_t *cand_count;    // [B * H_kv, n_chunks_max]
   int B, H_q, H_kv, D, ps, nb, max_pages, b_max;
   int key_stride;         // keys per (sequence, KV head) row of `keys`: max_pages rounded up to 4
-  int pchunk;             // pages per streaming score CTA
+  int pchunk;             // pages per streaming score CTA (body region)
+  int body_chunks;        // score CTAs per (sequence, head group) in the body region (set at launch)
+  int tail_pages;         // last pages of each sequence scored by the tail region (set at launch)
+  int tail_chunk;         // pages per tail-region CTA (set at launch)
+  int tail_chunks;        // tail-region CTAs per (sequence, head group) (set at launch)
   int stage_pages;        // pages per shared-memory stage of the score kernel
   int chunk;              // pages per selection CTA
   int n_chunks_max;

@@ -240,7 +240,8 @@ __device__ __forceinline__ float dot2_bf16(uint32_t q, uint32_t k, float acc) {
 // ------------------------------------------------------------------------------------
 // K1: page scores, streaming
 // ------------------------------------------------------------------------------------
-// One CTA per (chunk of a.pchunk pages, sequence, group of up to 8 KV heads). The summaries of
+// One CTA per (chunk, sequence, group of up to 8 KV heads): chunks of a.pchunk pages first, then
+// each sequence's last a.tail_pages pages in chunks of a.tail_chunk (see launch_t). The summaries of
 // a page for the CTA's heads are one contiguous run (H * 2 * D elements; 4 KB at H = 8,
 // D = 128 bf16), so warp 0 fetches each page with one bulk copy (TMA engine) into a ring of
 // kStages shared-memory stages of a.stage_pages pages, completion tracked by one mbarrier per
@@ -252,6 +253,8 @@ constexpr int kStages = 2;
 constexpr int kStageBytes = 24576;
 constexpr int kMaxStagePages = 32;
 constexpr int kPageSteps = 1;  // page steps per loop iteration
+constexpr int kTailChunk = 16;  // pages per CTA of the tail region
+constexpr int kTailWaves = 1;   // resident waves of CTAs that the tail region fills
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
@@ -264,17 +267,28 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   __shared__ __align__(8) uint64_t bars[kStages];
   __shared__ int okflag[kStages][kMaxStagePages];
 
-  const int i = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA
+  const int ng = kWarps / hpc;                         // warps per head
+  // work item of this CTA: (chunk, sequence, head group) with the chunk index fastest, first in
+  // the body region (chunks of a.pchunk pages) and then in the tail region (each sequence's last
+  // a.tail_pages pages in chunks of a.tail_chunk), so the CTAs dispatched last are short
+  int x = blockIdx.x;
+  const int n_body = a.body_chunks * a.B * (a.H_kv / hpc);
+  const bool in_tail = x >= n_body;
+  if (in_tail) x -= n_body;
+  const int per_seq = in_tail ? a.tail_chunks : a.body_chunks;
+  const int c = x % per_seq;
+  x /= per_seq;
+  const int i = x % a.B;
+  const int h0 = (x / a.B) * hpc;
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
   if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
-  const int p0 = blockIdx.x * a.pchunk;
-  if (p0 >= P) return;
-  const int p1 = min(P, p0 + a.pchunk);
-  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA
-  const int ng = kWarps / hpc;                         // warps per head
-  const int h0 = blockIdx.z * hpc;
+  const int body_end = P - min(P, a.tail_pages);
+  const int p0 = in_tail ? body_end + c * a.tail_chunk : c * a.pchunk;
+  const int p1 = in_tail ? min(P, p0 + a.tail_chunk) : min(body_end, p0 + a.pchunk);
+  if (p0 >= p1) return;
   const int hh = warp % hpc;
   const int h = h0 + hh;
   const int wg = warp / hpc;
@@ -635,14 +649,38 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
 template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
-  dim3 g1((a.max_pages + a.pchunk - 1) / a.pchunk, a.B, a.H_kv / hpc);
   const int k1_smem = kStages * kStageBytes;
-  cudaError_t e = cudaFuncSetAttribute(page_score_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, k1_smem);
+  auto kfn = page_score_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, k1_smem);
   if (e != cudaSuccess) return e;
-  page_score_kernel<T, D, G><<<g1, kThreads, k1_smem, s>>>(a);
+  // Tail region: about kTailWaves waves of short CTAs over the sequences' last pages. A grid of
+  // equal chunks ends with its last wave draining for one whole CTA lifetime at falling
+  // occupancy; short CTAs last make that drain short.
+  ScoreArgs b = a;
+  {
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, k1_smem)) != cudaSuccess) return e;
+    b.tail_chunk = kTailChunk;
+    const long long rows = (long long)a.B * (a.H_kv / hpc);
+    long long tail = ((long long)sms * std::max(1, per_sm) * kTailChunk * kTailWaves + rows - 1) / rows;
+    if (const char *env = std::getenv("PSK_SCORE_TAIL")) tail = std::atoi(env);  // tuning override: pages
+    if (const char *env = std::getenv("PSK_SCORE_TAIL_CHUNK")) {  // tuning override: pages per tail CTA
+      const int v = std::atoi(env);
+      if (v >= 1 && v <= 4096) b.tail_chunk = v;
+    }
+    tail = (tail + b.tail_chunk - 1) / b.tail_chunk * b.tail_chunk;
+    b.tail_pages = (int)std::max(0LL, std::min(tail, (long long)a.max_pages));
+    b.tail_chunks = (b.tail_pages + b.tail_chunk - 1) / b.tail_chunk;
+    b.body_chunks = (a.max_pages + a.pchunk - 1) / a.pchunk;
+  }
+  const long long n_ctas = (long long)(b.body_chunks + b.tail_chunks) * b.B * (b.H_kv / hpc);
+  if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
+  kfn<<<(unsigned)n_ctas, kThreads, k1_smem, s>>>(b);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_page_select(a, s);
+  return launch_page_select(b, s);
 }
 
 }  // namespace
