@@ -1,12 +1,23 @@
 // C ABI of libpsk: host-side argument checks, workspace planning and kernel dispatch.
 // Every entry point validates before it launches anything and never allocates.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
 
 using namespace psk;
+
+namespace psk {
+bool pdl_enabled(bool first_of_call) {
+  static const int mode = [] {
+    const char *env = std::getenv("PSK_PDL");
+    return env ? std::atoi(env) : 1;
+  }();
+  return mode == 1 || (mode == 2 && !first_of_call);
+}
+}  // namespace psk
 
 namespace {
 

@@ -52,6 +52,7 @@ __device__ __forceinline__ uint4 chunk_max(uint4 a, uint4 b) {
 
 template <typename T>
 __global__ void append_summarize_kernel(AppendArgs a) {
+  pdl_begin();
   const int i = blockIdx.y;
   const int j = blockIdx.x;
   const int c0 = a.cu_new[i];
@@ -160,10 +161,9 @@ cudaError_t launch_append(const AppendArgs &a, int dtype, int max_new, cudaStrea
   const int pages = (max_new + a.ps - 2) / a.ps + 1;
   dim3 grid(pages, a.B);
   if (dtype == PSK_F32)
-    append_summarize_kernel<float><<<grid, threads, 0, s>>>(a);
+    return launch_kernel(true, append_summarize_kernel<float>, grid, threads, 0, s, a);
   else
-    append_summarize_kernel<bf16_t><<<grid, threads, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_kernel(true, append_summarize_kernel<bf16_t>, grid, threads, 0, s, a);
 }
 
 }  // namespace psk

@@ -518,6 +518,7 @@ struct DecodeSmem {
 template <typename T, int D, int G, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV) {
+  pdl_begin();
   using TR = DT<T, D, G, NW, NST>;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
   DecodeSmem<T, D, G, NW, NST> sm(smem_dyn);
@@ -610,6 +611,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
 // List entries per unit of a sparse call: one past the last non-negative id of the unit's row
 // (0 for a sequence whose length is out of range). One warp per unit.
 __global__ void decode_counts_kernel(DecodeArgs a) {
+  pdl_begin();
   const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (unit >= a.B * a.H_kv) return;
@@ -636,6 +638,7 @@ __global__ void decode_counts_kernel(DecodeArgs a) {
 template <typename T, int D, int G, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                               const __grid_constant__ CUtensorMap tmV) {
+  pdl_begin();
   using TR = DT<T, D, G, NW, NST>;
   constexpr int NT = NW * 32;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
@@ -777,13 +780,11 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.B * a.H_kv, a.n_items_max);
-    kfn<<<grid, NW * 32, TR::SMEM, s>>>(a, tmK, tmV);
-    return cudaGetLastError();
+    return launch_kernel(true, kfn, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
   }
   const int U = a.B * a.H_kv;
   if (a.selected) {
-    decode_counts_kernel<<<(U + 7) / 8, 256, 0, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_kernel(true, decode_counts_kernel, (U + 7) / 8, 256, 0, s, a);
     if (e != cudaSuccess) return e;
   }
   auto kfn = decode_flat_kernel<T, D, G, NW, NST>;
@@ -795,8 +796,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, NW * 32, smem)) != cudaSuccess) return e;
   const int ctas = std::max(1, std::min(kFlatMaxCtas, sms * std::max(1, per_sm)));
-  kfn<<<ctas, NW * 32, smem, s>>>(a, tmK, tmV);
-  return cudaGetLastError();
+  return launch_kernel(!a.selected, kfn, ctas, NW * 32, smem, s, a, tmK, tmV);
 }
 }  // namespace
 

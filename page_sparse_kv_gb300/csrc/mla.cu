@@ -114,6 +114,7 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
 // q [B, 128, 576] -> [B, 128, 1152] = [min(q, 0) | max(q, 0)] (bit operations on bf16: a
 // negative value (sign set, -0.0 included) goes to the first half, the rest to the second).
 __global__ void mla_qsplit_kernel(const uint16_t *q, uint16_t *qs, int rows) {
+  pdl_begin();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * (kD / 8)) return;
   const int row = idx / (kD / 8), c = idx - row * (kD / 8);
@@ -131,6 +132,7 @@ constexpr int kScSmem = 1024 + kScStages * kScStage;
 constexpr int kScKBlocks = 2 * kD / 64;  // 18
 
 __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint16_t *qs) {
+  pdl_begin();
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
   __shared__ __align__(8) uint64_t bars[kScStages];
@@ -266,6 +268,7 @@ constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is res
 // in the order P.V(t), S(t+1), then the copy of K(t+2) into the stage P.V(t) released.
 __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK) {
+  pdl_begin();
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
   unsigned char *sQ = base;                    // Q dims 384..575
@@ -656,14 +659,13 @@ size_t mla_qsplit_bytes(const psk_layout &L) { return (size_t)L.batch * kHeads *
 cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s) {
   const int rows = a.B * kHeads;
   const int n = rows * (kD / 8);
-  mla_qsplit_kernel<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<const uint16_t *>(a.q), qsplit, rows);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(true, mla_qsplit_kernel, (n + 255) / 256, 256, 0, s,
+                                reinterpret_cast<const uint16_t *>(a.q), qsplit, rows);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.max_pages + 127) / 128, a.B);
-  mla_score_kernel<<<grid, 128, kScSmem, s>>>(a, qsplit);
-  e = cudaGetLastError();
+  e = launch_kernel(false, mla_score_kernel, grid, 128, kScSmem, s, a, (const uint16_t *)qsplit);
   if (e != cudaSuccess) return e;
   return launch_page_select(a, s);
 }
@@ -708,8 +710,7 @@ cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_items_max, 2, a.B);
-  mla_decode_kernel<<<grid, kDecThreads, kDecSmem, s>>>(a, tmQ, tmK);
-  return cudaGetLastError();
+  return launch_kernel(true, mla_decode_kernel, grid, kDecThreads, kDecSmem, s, a, tmQ, tmK);
 }
 
 }  // namespace psk

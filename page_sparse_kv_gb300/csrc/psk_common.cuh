@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/psk.h"
 
@@ -20,6 +21,44 @@ struct WsHeader {
 
 __device__ __forceinline__ void set_status(void *ws, uint32_t bit) {
   atomicOr(&reinterpret_cast<WsHeader *>(ws)->status, bit);
+}
+
+// ------------------------------------------------------------------------------------
+// Programmatic dependent launch: every kernel is launched with programmatic stream
+// serialisation, so it may be scheduled while the kernel before it in the stream drains. Its
+// first act is pdl_begin(): griddepcontrol.wait blocks until the previous grid has completed and
+// its writes are visible (no global memory is touched before it, so any producer / consumer
+// order, and any reuse of a buffer, is as safe as with plain stream order), then
+// griddepcontrol.launch_dependents lets the next kernel in the stream be scheduled once every
+// CTA of this grid has started. In a kernel launched without the attribute both are no-ops.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+  pdl_wait();
+  pdl_trigger();
+}
+
+// Which launches carry the attribute: kernels that follow another kernel of the same call always
+// (score after q split, select after score, flat decode after counts), the first kernel of a call
+// too unless PSK_PDL=2; PSK_PDL=0 launches every kernel in plain stream order.
+bool pdl_enabled(bool first_of_call);
+
+// Launch with the programmatic-serialisation attribute (when enabled for this kind of launch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool first_of_call, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled(first_of_call) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

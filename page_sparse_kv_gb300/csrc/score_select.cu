@@ -258,6 +258,7 @@ constexpr int kTailWaves = 1;   // resident waves of CTAs that the tail region f
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
+  pdl_wait();  // the select launch is released at the end of the loop (see below)
   constexpr int EPC = Elem<T>::kPerChunk;
   constexpr int LPP = D / EPC;   // lanes per page
   constexpr int PPW = 32 / LPP;  // pages per warp step
@@ -444,6 +445,9 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
       produce(st + kStages, next_blk);
     }
   }
+  // released here rather than at the start: select CTAs made resident early would sit waiting
+  // through this grid's drain
+  pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------
@@ -508,6 +512,7 @@ __device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t 
 }
 
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
+  pdl_begin();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ int hist[kWarps * 256];  // zero between radix selects
   __shared__ int cnt[kThreads + 1];
@@ -677,8 +682,7 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   }
   const long long n_ctas = (long long)(b.body_chunks + b.tail_chunks) * b.B * (b.H_kv / hpc);
   if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
-  kfn<<<(unsigned)n_ctas, kThreads, k1_smem, s>>>(b);
-  e = cudaGetLastError();
+  e = launch_kernel(true, kfn, (unsigned)n_ctas, kThreads, k1_smem, s, b);
   if (e != cudaSuccess) return e;
   return launch_page_select(b, s);
 }
@@ -693,8 +697,7 @@ cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 g2(a.H_kv, a.n_chunks_max, a.B);
-  page_select_kernel<<<g2, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(false, page_select_kernel, g2, kThreads, smem, s, a);
 }
 
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
