@@ -518,7 +518,7 @@ struct DecodeSmem {
 template <typename T, int D, int G, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV) {
-  pdl_begin();
+  pdl_wait();  // dependents are released when this grid completes
   using TR = DT<T, D, G, NW, NST>;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
   DecodeSmem<T, D, G, NW, NST> sm(smem_dyn);
@@ -638,7 +638,7 @@ __global__ void decode_counts_kernel(DecodeArgs a) {
 template <typename T, int D, int G, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                               const __grid_constant__ CUtensorMap tmV) {
-  pdl_begin();
+  pdl_wait();  // dependents are released when this grid completes
   using TR = DT<T, D, G, NW, NST>;
   constexpr int NT = NW * 32;
   extern __shared__ __align__(128) unsigned char smem_dyn[];

@@ -132,7 +132,7 @@ constexpr int kScSmem = 1024 + kScStages * kScStage;
 constexpr int kScKBlocks = 2 * kD / 64;  // 18
 
 __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint16_t *qs) {
-  pdl_begin();
+  pdl_wait();  // dependents are released when this grid completes
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
   __shared__ __align__(8) uint64_t bars[kScStages];
@@ -268,7 +268,7 @@ constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is res
 // in the order P.V(t), S(t+1), then the copy of K(t+2) into the stage P.V(t) released.
 __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK) {
-  pdl_begin();
+  pdl_wait();  // dependents are released when this grid completes
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
   unsigned char *sQ = base;                    // Q dims 384..575

@@ -512,7 +512,7 @@ __device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t 
 }
 
 __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
-  pdl_begin();
+  pdl_wait();  // dependents are released when this grid completes
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ int hist[kWarps * 256];  // zero between radix selects
   __shared__ int cnt[kThreads + 1];
