@@ -37,6 +37,11 @@
  *     keeps no state between calls apart from what it writes into the caller's buffers.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream). Host-side argument checks happen before any launch and are synchronous.
+ *   - Kernels are launched with programmatic stream serialisation (programmatic dependent
+ *     launch): a kernel may be scheduled while the kernel before it on `stream` drains, but
+ *     it waits for that kernel's completion (griddepcontrol.wait) before it reads or writes
+ *     any global memory, so stream order is kept exactly. Setting PSK_PDL=0 in the
+ *     environment before the first call launches in plain stream order.
  *   - Return value: PSK_OK or a psk_status code. PSK_ERR_CUDA reports a launch error.
  *   - Device-side violations that the host cannot see (a block id outside
  *     [0, num_blocks), a sequence longer than max_pages pages, a bad selected id, a
