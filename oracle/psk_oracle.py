@@ -25,7 +25,12 @@ online softmax or algebraic rewriting:
                          the current tail page are always kept and counted inside b
                          (LOCKS "Results" preamble: "sink + recent counted inside b";
                          EntmaxKV "Top-k": the budget includes the always-attended
-                         tail page); ties go to the lower logical page index.
+                         tail page); ties go to the lower logical page index. The
+                         always-kept set generalises to the first sink_pages and the
+                         last window_pages pages (LOCKS configuration table), and b
+                         may come from a fraction of the pages or a fixed page count
+                         (same table; the fraction rounds by the retained-count rule
+                         of the vllm-rlt pull request #157 discussion).
   S4 attention        -- exact softmax attention over the selected pages' tokens
                          only (EntmaxKV introduction: "the attention is exact over
                          that selection"; LOCKS "How it works", Sparse decode), the
@@ -36,6 +41,8 @@ points the pages leave open:
   * a page's "tail" is page ceil(seq_len / page_size) - 1, the page that holds
     token seq_len - 1;
   * the selected count is min(b, P); with P == 1 the sink is the tail;
+  * overlapping sink and window sets count once; a budget below the forced set's size is
+    an error, and a budget mode's result is raised to that size;
   * min / max order signed zeros as -0.0 < +0.0 (IEEE 754 totalOrder on non-NaN);
   * ties in the page score (including -0.0 vs +0.0) go to the lower page index;
   * the scale 1/sqrt(D) is applied after the group max and is the same scale
@@ -153,37 +160,78 @@ def quest_scores(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarray, dtype: str, 
 # ----------------------------------------------------------------------------------
 # S3: top-b selection with forced sink and tail
 # ----------------------------------------------------------------------------------
-def forced_pages(P: int) -> list[int]:
-    """The always-kept pages: the sink (page 0) and the tail (page P-1)."""
-    return [0] if P == 1 else [0, P - 1]
+def forced_pages(P: int, sink_pages: int = 1, window_pages: int = 1) -> list[int]:
+    """The always-kept pages, ascending: the first ``sink_pages`` pages and the last
+    ``window_pages`` pages (the tail page among them), clipped to the P pages that exist
+    (LOCKS PKG-INFO, "Configuration (LocksConfig)": sink_pages / window_pages, the always-kept
+    first / recent pages, default 1 / 1). With the defaults: the sink (page 0) and the tail
+    (page P-1)."""
+    if sink_pages < 1 or window_pages < 1:
+        raise ValueError("sink_pages and window_pages are at least 1")
+    return sorted(set(range(min(sink_pages, P))) | set(range(max(0, P - window_pages), P)))
 
 
-def select_pages(scores: np.ndarray, budget: int) -> list[int]:
+def select_pages(scores: np.ndarray, budget: int, sink_pages: int = 1, window_pages: int = 1) -> list[int]:
     """Selected logical pages of one (sequence, KV head), ascending.
 
-    scores: [P] page scores. The sink and tail pages are always kept and count inside the
-    budget; the remaining min(budget, P) - |forced| pages are the highest-scoring others,
-    ties going to the lower page index.
+    scores: [P] page scores. The forced pages (``forced_pages``) are always kept and count
+    inside the budget; the remaining min(budget, P) - |forced| pages are the highest-scoring
+    others, ties going to the lower page index.
     """
     P = len(scores)
-    forced = forced_pages(P)
-    if P > 1 and budget < 2:
-        raise ValueError("budget must hold the sink and the tail page")
+    forced = forced_pages(P, sink_pages, window_pages)
+    if budget < len(forced):
+        raise ValueError("budget must hold every always-kept page")
     count = min(budget, P)
     others = [p for p in range(P) if p not in forced]
     ranked = sorted(others, key=lambda p: (-float(scores[p]), p))
     return sorted(forced + ranked[:count - len(forced)])
 
 
-def cutoff_score(scores: np.ndarray, budget: int) -> float | None:
-    """Score of the last non-forced page that made the cut (None if every page is kept)."""
+def cutoff_score(scores: np.ndarray, budget: int, sink_pages: int = 1, window_pages: int = 1) -> float | None:
+    """Score of the last non-forced page that made the cut (None if no free page is chosen by
+    score: every page is kept, or the budget holds only the forced pages)."""
     P = len(scores)
-    if min(budget, P) >= P:
+    forced = forced_pages(P, sink_pages, window_pages)
+    k_free = min(budget, P) - len(forced)
+    if min(budget, P) >= P or k_free <= 0:
         return None
-    forced = forced_pages(P)
     others = [p for p in range(P) if p not in forced]
     ranked = sorted(others, key=lambda p: (-float(scores[p]), p))
-    return float(scores[ranked[min(budget, P) - len(forced) - 1]])
+    return float(scores[ranked[k_free - 1]])
+
+
+# ----------------------------------------------------------------------------------
+# S3 budget modes
+# ----------------------------------------------------------------------------------
+def retained_count(N: int, r: float) -> int:
+    """Pages kept out of N for a fractional budget r: min(N, max(1, ceil(N * r))) (the
+    retained-count rule of the vllm-rlt pull request #157 discussion, the commit that aligns
+    the rounding with the FlashLoop reference: a ceiling, not rounding to nearest). N * r is
+    evaluated in IEEE double precision, as the rule's own Python code does."""
+    if N < 1:
+        raise ValueError("N >= 1")
+    return min(N, max(1, math.ceil(float(N) * float(r))))
+
+
+def budget_for(P: int, *, fraction: float | None = None, pages: int | None = None,
+               sink_pages: int = 1, window_pages: int = 1) -> int:
+    """Per-(sequence, KV head) budget of a budget mode (LOCKS PKG-INFO, "Configuration
+    (LocksConfig)": ``budget`` = a fixed fraction of the pages, ``budget_pages`` = a fixed
+    absolute number of pages per unit). A fraction uses ``retained_count``; either mode is then
+    raised to the number of always-kept pages, which the budget includes, and capped at P."""
+    forced = len(forced_pages(P, sink_pages, window_pages))
+    if (fraction is None) == (pages is None):
+        raise ValueError("exactly one of fraction, pages")
+    if fraction is not None:
+        if not (0.0 < fraction <= 1.0):
+            raise ValueError("fraction in (0, 1]")
+        b = retained_count(P, fraction)
+    else:
+        if pages < 1:
+            raise ValueError("pages >= 1")
+        b = min(P, pages)
+    return max(b, forced)
 
 
 # ----------------------------------------------------------------------------------
@@ -242,13 +290,13 @@ def logical_from_cache(cache: np.ndarray, block_row: np.ndarray, seq_len: int, p
 # ----------------------------------------------------------------------------------
 # one decode step of one sequence, end to end
 # ----------------------------------------------------------------------------------
-def decode_step(q, keys, values, seq_len, page_size, budget, dtype, scale):
+def decode_step(q, keys, values, seq_len, page_size, budget, dtype, scale, sink_pages=1, window_pages=1):
     """Score, select and attend for one sequence whose keys/values (logical order) already
     include the current token. Returns (summaries (kmin, kmax), scores [H_kv, P],
     selected per KV head, out [H_q, D_v])."""
     kmin, kmax = page_summaries(keys, seq_len, page_size, dtype)
     scores = quest_scores(q, kmin, kmax, dtype, scale)
-    selected = [select_pages(scores[h], budget) for h in range(scores.shape[0])]
+    selected = [select_pages(scores[h], budget, sink_pages, window_pages) for h in range(scores.shape[0])]
     out = attend_pages(q, keys, values, seq_len, page_size, selected, dtype, scale)
     return (kmin, kmax), scores, selected, out
 

@@ -12,7 +12,8 @@ import oracle as O
 import oracle.psk_oracle as OP
 import test_oracle_pins as PINS
 
-ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention")}
+ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention",
+                                             "forced_pages", "retained_count")}
 
 
 @pytest.fixture
@@ -45,19 +46,27 @@ def _quest_no_scale(q, kmin, kmax, dtype, scale):  # forgets 1/sqrt(D)
     return ORIG["quest_scores"](q, kmin, kmax, dtype, 1.0)
 
 
-def _select_ties_high(scores, budget):  # ties go to the higher page index
+def _select_ties_high(scores, budget, sink_pages=1, window_pages=1):  # ties go to the higher page index
     P = len(scores)
-    forced = O.forced_pages(P)
+    forced = O.forced_pages(P, sink_pages, window_pages)
     count = min(budget, P)
     ranked = sorted((p for p in range(P) if p not in forced), key=lambda p: (-float(scores[p]), -p))
     return sorted(forced + ranked[:count - len(forced)])
 
 
-def _select_tail_not_forced(scores, budget):  # only the sink is forced
+def _select_tail_not_forced(scores, budget, sink_pages=1, window_pages=1):  # only the sink is forced
     P = len(scores)
     count = min(budget, P)
     ranked = sorted(range(1, P), key=lambda p: (-float(scores[p]), p))
     return sorted([0] + ranked[:count - 1])
+
+
+def _forced_window_of_one(P, sink_pages=1, window_pages=1):  # window_pages read as 1
+    return ORIG["forced_pages"](P, sink_pages, 1)
+
+
+def _retained_round_nearest(N, r):  # rounds N * r to nearest instead of the ceiling
+    return min(N, max(1, int(round(N * r))))
 
 
 def _summaries_whole_pages(keys, seq_len, page_size, dtype):  # counts the tail page's junk rows
@@ -116,3 +125,13 @@ def test_signed_zero_order_is_caught(plant):
 def test_unscaled_attention_is_caught(plant):
     plant("softmax_attention", _attention_unscaled)
     _fails(PINS.test_dense_equals_library_attention_and_full_budget_equals_dense, "f32", 16, 16 * 6 + 5)
+
+
+def test_window_of_one_is_caught(plant):
+    plant("forced_pages", _forced_window_of_one)
+    _fails(PINS.test_selection_brute_force_with_sink_and_window, 6, 1, 3)
+
+
+def test_fraction_rounded_to_nearest_is_caught(plant, golden_dir):
+    plant("retained_count", _retained_round_nearest)
+    _fails(PINS.test_retained_count_golden_and_closed_forms, golden_dir)

@@ -256,6 +256,82 @@ def test_selection_rejects_budget_below_two():
     assert O.select_pages(np.zeros(1), 1) == [0]
 
 
+# ------------------------------------------------------------------ S3 always-kept sets and budget modes
+SW_CASES = [(1, 1), (2, 1), (1, 3), (3, 2), (4, 4)]
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 7, 9])
+def test_forced_set_closed_forms(P):
+    """The always-kept set of sink_pages S and window_pages W is a prefix plus a suffix of the
+    pages: it holds min(P, S + W) pages, all of them once S + W >= P, page 0 and page P - 1
+    always, and its complement is the contiguous run [S, P - W)."""
+    assert O.forced_pages(P) == O.forced_pages(P, 1, 1) == ([0] if P == 1 else [0, P - 1])
+    for S in range(1, 6):
+        for W in range(1, 6):
+            f = O.forced_pages(P, S, W)
+            assert len(f) == min(P, S + W) and f == sorted(set(f))
+            assert f[0] == 0 and f[-1] == P - 1
+            rest = [p for p in range(P) if p not in f]
+            assert rest == list(range(S, P - W)) if S + W < P else rest == []
+    with pytest.raises(ValueError):
+        O.forced_pages(4, 0, 1)
+
+
+@pytest.mark.parametrize("S,W", SW_CASES)
+@pytest.mark.parametrize("P", [1, 3, 6, 9])
+def test_selection_brute_force_with_sink_and_window(P, S, W):
+    """With S first and W recent pages kept, the free pages chosen are the unique subset of the
+    others in which every member beats every non-member under (score desc, index asc), and the
+    output is every forced page plus that subset."""
+    rng = np.random.default_rng(100 * P + 10 * S + W)
+    n_forced = min(P, S + W)
+    for trial in range(3):
+        scores = rng.integers(-2, 3, size=P).astype(np.float64)
+        for b in range(n_forced, P + 2):
+            sel = O.select_pages(scores, b, S, W)
+            first, last = list(range(min(S, P))), list(range(max(0, P - W), P))
+            forced = sorted(set(first + last))
+            others = [p for p in range(P) if p not in forced]
+            k = min(b, P) - len(forced)
+            winners = [sorted(forced + list(T)) for T in itertools.combinations(others, k)
+                       if all((scores[x], -x) > (scores[y], -y) for x in T for y in others if y not in T)]
+            assert len(winners) == 1 and winners[0] == sel and len(sel) == min(b, P)
+        if P > n_forced:
+            with pytest.raises(ValueError):
+                O.select_pages(scores, n_forced - 1, S, W)
+
+
+def test_retained_count_golden_and_closed_forms(golden_dir):
+    """The printed boundary case of the retained-count rule (a ceiling, not rounding to
+    nearest), then the rule's ends: r = 1 keeps all, a tiny r keeps one, the count never
+    falls as r grows, and exact fractions give exact counts."""
+    with open(os.path.join(golden_dir, "retained_count.json")) as f:
+        gold = json.load(f)
+    for c in gold["cases"]:
+        assert O.retained_count(c["N"], c["r"]) == c["k"]
+    for N in (1, 2, 13, 100, 4096):
+        assert O.retained_count(N, 1.0) == N
+        assert O.retained_count(N, 1e-9) == 1
+        ks = [O.retained_count(N, r) for r in np.linspace(0.01, 1.0, 50)]
+        assert ks == sorted(ks)
+    assert O.retained_count(100, 0.05) == 5 and O.retained_count(101, 0.05) == 6
+    assert O.retained_count(2048, 0.25) == 512
+
+
+def test_budget_modes():
+    """A fraction goes through the retained-count rule, a page count is capped at P, and both
+    are raised to the always-kept set they include."""
+    assert O.budget_for(13, fraction=0.1) == 2
+    assert O.budget_for(13, fraction=0.1, sink_pages=2, window_pages=3) == 5
+    assert O.budget_for(2200, fraction=0.05) == 110
+    assert O.budget_for(50, pages=128) == 50 and O.budget_for(500, pages=128) == 128
+    assert O.budget_for(500, pages=4, sink_pages=1, window_pages=10) == 11
+    assert O.budget_for(3, pages=1) == 2 and O.budget_for(1, pages=1) == 1
+    for bad in (dict(), dict(fraction=0.1, pages=3), dict(fraction=0.0), dict(fraction=1.5), dict(pages=0)):
+        with pytest.raises(ValueError):
+            O.budget_for(10, **bad)
+
+
 # ------------------------------------------------------------------ S4 attention
 def _sdpa_reference(q, k, v, scale):
     """torch's float64 scaled_dot_product_attention with GQA heads expanded; q [H_q, D],
