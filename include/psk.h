@@ -83,7 +83,7 @@ enum psk_status {
 #define PSK_DEV_BAD_BLOCK 0x1u    /* block-table entry outside [0, num_blocks)              */
 #define PSK_DEV_BAD_SEQLEN 0x2u   /* seq_len < 1, or more than max_pages pages              */
 #define PSK_DEV_BAD_SELECTED 0x4u /* selected id outside [0, P) or list not ascending       */
-#define PSK_DEV_BAD_BUDGET 0x8u   /* budget < 2 with P > 1, or budget > b_max               */
+#define PSK_DEV_BAD_BUDGET 0x8u   /* budget below the always-kept count, or above b_max      */
 #define PSK_DEV_BAD_APPEND 0x10u  /* append position outside the block-table row, or n < 0  */
 #define PSK_DEV_TIMEOUT 0x20u     /* a bounded wait for an asynchronous copy gave up         */
 
@@ -163,6 +163,43 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
                           const int32_t *budgets, int32_t b_max, float scale, int32_t *selected,
                           float *scores_out, void *workspace, size_t workspace_bytes,
                           psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stages 2 + 3 with general always-kept sets and budget modes (LOCKS PKG-INFO,
+ * "Configuration (LocksConfig)": sink_pages / window_pages, budget, budget_pages).
+ *
+ * Always-kept pages of sequence i: F_i = [0, sink_pages) U [P_i - window_pages, P_i), clipped
+ * to [0, P_i); |F_i| = min(P_i, sink_pages + window_pages). The budget b_i counts them:
+ *   PSK_BUDGET_PER_SEQUENCE  b_i = budgets[i] (device int32 [batch]); a b_i below |F_i| or
+ *                            above b_max flags PSK_DEV_BAD_BUDGET and writes the row as -1;
+ *   PSK_BUDGET_PAGES         b_i = max(|F_i|, min(P_i, budget_pages)), budget_pages >= 1;
+ *   PSK_BUDGET_FRACTION      b_i = max(|F_i|, min(P_i, max(1, ceil(P_i * budget_fraction)))),
+ *                            0 < budget_fraction <= 1, P_i * budget_fraction evaluated in IEEE
+ *                            double (the retained-count rule of the vllm-rlt pull request #157
+ *                            discussion: a ceiling, not rounding to nearest).
+ * Selected: F_i plus the min(b_i, P_i) - |F_i| highest-scoring other pages, ties to the lower
+ * page index, ascending, padded with -1 to b_max. For the two scalar modes the call returns
+ * PSK_ERR_INVALID_ARG unless b_max holds the largest b_i any sequence of at most max_pages
+ * pages can get. Everything else is as psk_page_score_select, which is this call with
+ * PSK_BUDGET_PER_SEQUENCE and sink_pages = window_pages = 1. Without scores_out the
+ * summaries of the always-kept pages are not read.
+ * --------------------------------------------------------------------------------------- */
+enum psk_budget_mode { PSK_BUDGET_PER_SEQUENCE = 0, PSK_BUDGET_PAGES = 1, PSK_BUDGET_FRACTION = 2 };
+
+typedef struct psk_select_params {
+  const int32_t *budgets;  /* PSK_BUDGET_PER_SEQUENCE: device int32 [batch]; else ignored */
+  double budget_fraction;  /* PSK_BUDGET_FRACTION                                         */
+  int32_t budget_pages;    /* PSK_BUDGET_PAGES                                            */
+  int32_t mode;            /* enum psk_budget_mode                                        */
+  int32_t sink_pages;      /* >= 1                                                        */
+  int32_t window_pages;    /* >= 1                                                        */
+} psk_select_params;
+
+int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void *summaries,
+                             const int32_t *block_table, const int32_t *seq_lens,
+                             const psk_select_params *params, int32_t b_max, float scale,
+                             int32_t *selected, float *scores_out, void *workspace,
+                             size_t workspace_bytes, psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Stage 4: exact softmax attention over the selected pages.

@@ -21,7 +21,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "
 DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 
 EXPORTS = [
-    "psk_kv_append_and_summarize", "psk_page_score_select", "psk_sparse_paged_decode",
+    "psk_kv_append_and_summarize", "psk_page_score_select", "psk_page_score_select_ex", "psk_sparse_paged_decode",
     "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version",
@@ -38,6 +38,15 @@ class PskLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "v_head_dim", "page_size",
         "num_blocks", "max_pages", "dtype", "latent")]
+
+
+BUDGET_PER_SEQUENCE, BUDGET_PAGES, BUDGET_FRACTION = 0, 1, 2
+
+
+class PskSelectParams(ctypes.Structure):
+    """Mirrors ``psk_select_params``."""
+    _fields_ = [("budgets", ctypes.c_void_p), ("budget_fraction", ctypes.c_double), ("budget_pages", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("sink_pages", ctypes.c_int32), ("window_pages", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -75,6 +84,8 @@ def lib() -> ctypes.CDLL:
         sig = {
             "psk_kv_append_and_summarize": (ctypes.c_int, [LP, P, P, P, P, I, I, P, P, P, P, P, Z, P]),
             "psk_page_score_select": (ctypes.c_int, [LP, P, P, P, P, P, I, F, P, P, P, Z, P]),
+            "psk_page_score_select_ex": (ctypes.c_int, [LP, P, P, P, P, ctypes.POINTER(PskSelectParams), I, F, P, P,
+                                                        P, Z, P]),
             "psk_sparse_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P, Z, P]),
             "psk_dense_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, F, P, P, Z, P]),
             "psk_sparse_paged_decode_noalloc": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P]),
@@ -168,6 +179,28 @@ def page_score_select(layout: Layout, q, summaries, block_table, seq_lens, budge
                       selected, workspace, scores_out=None, stream=None):
     _check("psk_page_score_select", lib().psk_page_score_select(
         ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), _ptr(budgets),
+        int(b_max), float(scale), _ptr(selected), _ptr(scores_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_max: int, scale: float, selected,
+                         workspace, *, budgets=None, budget_pages: int | None = None,
+                         budget_fraction: float | None = None, sink_pages: int = 1, window_pages: int = 1,
+                         scores_out=None, stream=None):
+    """Score + select with the first ``sink_pages`` and last ``window_pages`` pages always kept
+    and exactly one budget mode: ``budgets`` (device int32 per sequence), ``budget_pages`` (a
+    fixed page count) or ``budget_fraction`` (a fraction of each sequence's pages)."""
+    modes = [budgets is not None, budget_pages is not None, budget_fraction is not None]
+    if sum(modes) != 1:
+        raise ValueError("give exactly one of budgets, budget_pages, budget_fraction")
+    prm = PskSelectParams()
+    prm.budgets = _ptr(budgets) if budgets is not None else None
+    prm.budget_fraction = float(budget_fraction or 0.0)
+    prm.budget_pages = int(budget_pages or 0)
+    prm.mode = BUDGET_PER_SEQUENCE if modes[0] else (BUDGET_PAGES if modes[1] else BUDGET_FRACTION)
+    prm.sink_pages, prm.window_pages = int(sink_pages), int(window_pages)
+    _check("psk_page_score_select_ex", lib().psk_page_score_select_ex(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), ctypes.byref(prm),
         int(b_max), float(scale), _ptr(selected), _ptr(scores_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 

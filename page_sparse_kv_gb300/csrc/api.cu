@@ -1,5 +1,7 @@
 // C ABI of libpsk: host-side argument checks, workspace planning and kernel dispatch.
 // Every entry point validates before it launches anything and never allocates.
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -150,11 +152,48 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
                           const int32_t *block_table, const int32_t *seq_lens, const int32_t *budgets,
                           int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
                           size_t workspace_bytes, psk_stream_t stream) {
+  psk_select_params params = {};
+  params.budgets = budgets;
+  params.mode = PSK_BUDGET_PER_SEQUENCE;
+  params.sink_pages = 1;
+  params.window_pages = 1;
+  return psk_page_score_select_ex(layout, q, summaries, block_table, seq_lens, &params, b_max, scale, selected,
+                                  scores_out, workspace, workspace_bytes, stream);
+}
+
+// Largest budget a sequence of P pages gets in a scalar budget mode (the same arithmetic as
+// the select kernel's).
+static long long scalar_mode_budget(const psk_select_params &sp, long long P) {
+  const long long forced = std::min(P, (long long)sp.sink_pages + sp.window_pages);
+  long long b;
+  if (sp.mode == PSK_BUDGET_FRACTION)
+    b = std::min(P, std::max(1LL, (long long)std::ceil((double)P * sp.budget_fraction)));
+  else
+    b = std::min(P, (long long)sp.budget_pages);
+  return std::max(forced, b);
+}
+
+int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void *summaries,
+                             const int32_t *block_table, const int32_t *seq_lens, const psk_select_params *params,
+                             int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
+                             size_t workspace_bytes, psk_stream_t stream) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
-  if (!q || !summaries || !block_table || !seq_lens || !budgets || !selected || b_max < 1)
+  if (!q || !summaries || !block_table || !seq_lens || !params || !selected || b_max < 1)
     return PSK_ERR_INVALID_ARG;
+  const psk_select_params &sp = *params;
+  if (sp.sink_pages < 1 || sp.window_pages < 1) return PSK_ERR_INVALID_ARG;
+  if (sp.mode == PSK_BUDGET_PER_SEQUENCE) {
+    if (!sp.budgets) return PSK_ERR_INVALID_ARG;
+  } else if (sp.mode == PSK_BUDGET_PAGES || sp.mode == PSK_BUDGET_FRACTION) {
+    if (sp.mode == PSK_BUDGET_PAGES && sp.budget_pages < 1) return PSK_ERR_INVALID_ARG;
+    if (sp.mode == PSK_BUDGET_FRACTION && !(sp.budget_fraction > 0.0 && sp.budget_fraction <= 1.0))
+      return PSK_ERR_INVALID_ARG;
+    if (scalar_mode_budget(sp, L.max_pages) > b_max) return PSK_ERR_INVALID_ARG;  // monotone in P
+  } else {
+    return PSK_ERR_INVALID_ARG;
+  }
   if (!aligned16(q) || !aligned16(summaries)) return PSK_ERR_INVALID_ARG;
   rc = check_gqa_compute(layout);
   if (rc != PSK_OK) return rc;
@@ -167,7 +206,7 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.summaries = summaries;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
-  a.budgets = budgets;
+  a.budgets = sp.mode == PSK_BUDGET_PER_SEQUENCE ? sp.budgets : nullptr;
   a.selected = selected;
   a.scores_out = scores_out;
   a.ws = workspace;
@@ -191,6 +230,11 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
   a.n_chunks_max = plan.n_chunks_max;
   a.k_cap = plan.k_cap;
   a.scale = scale;
+  a.sink = sp.sink_pages;
+  a.window = sp.window_pages;
+  a.budget_mode = sp.mode;
+  a.budget_pages = sp.budget_pages;
+  a.budget_frac = sp.budget_fraction;
   if (L.latent)
     return cuda_status(launch_mla_score_select(a, reinterpret_cast<uint16_t *>(ws + plan.off_qsplit),
                                                static_cast<cudaStream_t>(stream)));

@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
         set_status(a.ws, PSK_DEV_BAD_BLOCK);
         blk = -1;
       }
-      // sink and tail are kept whatever their score: not read unless scores are requested
-      if (!a.scores_out && (p == 0 || p == P - 1)) blk = -1;
+      // always-kept pages are kept whatever their score: not read unless scores are requested
+      if (!a.scores_out && always_kept(p, P, a.sink, a.window)) blk = -1;
     }
     row_blk[tid] = blk;
   }
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
   const int p = p0 + tid;  // this thread's tensor-memory lane = page row
   if (p < P) {
     const float sc = mx * a.scale;
-    const bool forced = (p == 0) || (p == P - 1);
+    const bool forced = always_kept(p, P, a.sink, a.window);
     a.keys[(size_t)i * a.key_stride + p] = (row_blk[tid] >= 0 && !forced) ? score_key(sc) : 0u;
     if (a.scores_out) a.scores_out[(size_t)i * a.max_pages + p] = sc;
   }

@@ -50,7 +50,16 @@ struct ScoreArgs {
   int n_chunks_max;
   int k_cap;              // candidates kept per chunk = min(b_max - 2, chunk) (>= 1)
   float scale;
+  int sink, window;       // always-kept first / last pages (>= 1 each)
+  int budget_mode;        // enum psk_budget_mode
+  int budget_pages;       // PSK_BUDGET_PAGES
+  double budget_frac;     // PSK_BUDGET_FRACTION
 };
+
+// Page p of a sequence of P pages is always kept: one of the first `sink` or the last `window`.
+__host__ __device__ inline bool always_kept(int p, int P, int sink, int window) {
+  return p < sink || p >= P - window;
+}
 struct ScorePlan {
   int pchunk, stage_pages, chunk, n_chunks_max, k_cap;
   size_t ws_bytes;

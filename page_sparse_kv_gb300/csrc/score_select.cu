@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
     const bool in_chunk = lane < sp && p < p1;
     const bool valid = blk >= 0 && blk < a.nb;
     if (in_chunk && !valid) set_status(a.ws, PSK_DEV_BAD_BLOCK);
-    // the sink and the tail are kept whatever their score: without scores_out their summaries
+    // always-kept pages are kept whatever their score: without scores_out their summaries
     // are not read (so an append to the tail page may run concurrently)
-    const bool needed = a.scores_out != nullptr || (p != 0 && p != P - 1);
+    const bool needed = a.scores_out != nullptr || !always_kept(p, P, a.sink, a.window);
     const bool ok = in_chunk && valid && needed;
     if (lane < sp) okflag[slot][lane] = ok;
     const unsigned mask = __ballot_sync(0xffffffffu, ok);
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
         const int j = jb + grp;
         if (sub == 0 && j < np) {
           const int p = pb + j;
-          const bool forced = (p == 0) || (p == P - 1);
+          const bool forced = always_kept(p, P, a.sink, a.window);
           krow[p] = (okflag[slot][j] && !forced) ? score_key(sc) : 0u;
           if (srow) srow[p] = sc;
         }
@@ -456,13 +456,26 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
 // One CTA per (KV head, chunk of a.chunk pages, sequence). The chunk's keys come from the
 // workspace (L2-resident right after K1). A unit that fits one chunk is finished by its only
 // CTA; otherwise every chunk writes its local winners and the last CTA to finish merges.
-__device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, int b_max) {
+// Row of a unit with count < P selected pages: the first S pages, the `wrote` winners (written
+// by the caller at sel_row + S, all inside [S, P - W)), the last W pages, then -1 to b_max.
+// count < P implies S + W < P, so the two always-kept runs do not overlap.
+__device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, int b_max, int S, int W) {
   const int tid = threadIdx.x;
-  if (tid == 0) sel_row[0] = 0;
+  for (int x = tid; x < S; x += kThreads) sel_row[x] = x;
   // fewer winners than free slots happens only after a flagged bad block: pad the gap
-  for (int x = 1 + wrote + tid; x < count - 1; x += kThreads) sel_row[x] = -1;
-  if (tid == 0 && P > 1) sel_row[count - 1] = P - 1;
+  for (int x = S + wrote + tid; x < count - W; x += kThreads) sel_row[x] = -1;
+  for (int x = tid; x < W; x += kThreads) sel_row[count - W + x] = P - W + x;
   for (int x = count + tid; x < b_max; x += kThreads) sel_row[x] = -1;
+}
+
+// Budget of a sequence of P pages (always >= the always-kept count in the scalar modes).
+__device__ int unit_budget(const ScoreArgs &a, int i, int P, int n_forced) {
+  if (a.budget_mode == PSK_BUDGET_FRACTION) {
+    const int r = (int)ceil((double)P * a.budget_frac);  // IEEE double product, then the ceiling
+    return max(n_forced, min(P, max(1, r)));
+  }
+  if (a.budget_mode == PSK_BUDGET_PAGES) return max(n_forced, min(P, a.budget_pages));
+  return a.budgets[i];
 }
 
 // Block-wide sum of c and min / max of lo / hi (two barriers; red: 3 * kWarps words).
@@ -533,8 +546,9 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
     }
     return;
   }
-  const int budget = a.budgets[i];
-  if ((budget < 2 && P > 1) || budget < 1 || budget > a.b_max) {
+  const int n_forced = min(P, a.sink + a.window);
+  const int budget = unit_budget(a, i, P, n_forced);
+  if (budget < n_forced || budget > a.b_max) {
     if (c == 0) {
       if (tid == 0) set_status(a.ws, PSK_DEV_BAD_BUDGET);
       for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
@@ -549,7 +563,7 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
   }
   const int nch = (P + a.chunk - 1) / a.chunk;
   if (c >= nch) return;
-  const int k_free = count - 2;  // count < P implies P >= 2 and count >= 2
+  const int k_free = count - n_forced;  // count < P implies n_forced = sink + window < P
 
   uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);
   const int p0 = c * a.chunk;
@@ -591,8 +605,8 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
     const bool take_all = total_valid <= k_free;
     if (!take_all) radix_select(keys, n, k_free, kmin, kmax, hist, cnt, &thr, &need_eq);
     if (nch == 1) {
-      wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + 1, cnt);
-      write_row_ends(sel_row, P, count, wrote, a.b_max);
+      wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + a.sink, cnt);
+      write_row_ends(sel_row, P, count, wrote, a.b_max, a.sink, a.window);
       return;
     }
     const int slot = unit * a.n_chunks_max + c;
@@ -602,7 +616,7 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
     if (tid == 0) a.cand_count[slot] = wrote;
   } else {
     if (nch == 1) {
-      write_row_ends(sel_row, P, count, 0, a.b_max);
+      write_row_ends(sel_row, P, count, 0, a.b_max, a.sink, a.window);
       return;
     }
     if (tid == 0) a.cand_count[unit * a.n_chunks_max + c] = 0;
@@ -646,9 +660,9 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
       nonzero_stats(mkey, n_c, &nz, &mlo, &mhi, red);
       radix_select(mkey, n_c, k_free, mlo, mhi, hist, cnt, &thr, &need_eq);
     }
-    wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + 1, cnt);
+    wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + a.sink, cnt);
   }
-  write_row_ends(sel_row, P, count, wrote, a.b_max);
+  write_row_ends(sel_row, P, count, wrote, a.b_max, a.sink, a.window);
 }
 
 template <typename T, int D, int G>

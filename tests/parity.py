@@ -22,22 +22,23 @@ BF16_MAX_ABS, BF16_MEAN_ABS = 2e-2, 2e-3
 F32_ROW_REL = 1e-5
 
 
-def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int):
+def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int, sink_pages: int = 1,
+                      window_pages: int = 1):
     """gpu_row: int32 [b_max] (ascending ids, -1 padded); scores: oracle fp64 [P].
     Returns (ok, near_tie, gpu_ids, oracle_ids)."""
-    ref = O.select_pages(scores, budget)
+    ref = O.select_pages(scores, budget, sink_pages, window_pages)
     got = [int(x) for x in gpu_row if x >= 0]
     pad_ok = all(x < 0 for x in gpu_row[len(got):])
     if got == ref and pad_ok:
         return True, False, got, ref
     if len(got) != len(ref) or not pad_ok or got != sorted(set(got)):
         return False, False, got, ref
-    cut = O.cutoff_score(scores, budget)
+    cut = O.cutoff_score(scores, budget, sink_pages, window_pages)
     diff = set(got) ^ set(ref)
     if cut is None:
         return False, False, got, ref
     near = all(abs(scores[p] - cut) <= NEAR_TIE_REL * abs(cut) for p in diff)
-    forced_ok = 0 in got and (len(scores) - 1) in got
+    forced_ok = set(O.forced_pages(len(scores), sink_pages, window_pages)) <= set(got)
     return (near and forced_ok), near, got, ref
 
 

@@ -76,3 +76,38 @@ def test_host_checks_reject_before_launch(lib):
     rc = lib.psk_kv_append_and_summarize(ctypes.byref(L), None, None, P(16), P(16), 0, 0, P(16), P(16), P(16), P(16),
                                          P(16), 256, None)
     assert rc == 0
+
+
+def test_select_params_host_checks(lib):
+    """The general score/select entry rejects bad always-kept sizes, budget modes and a b_max
+    too small for a scalar budget mode before any launch (the workspace is too small here, so a
+    call that got past the checks would answer PSK_ERR_WORKSPACE, still without a launch)."""
+    import page_sparse_kv_gb300 as psk
+    L = psk.Layout(2, 32, 8, 128, 128, 16, 100, 50).c()
+    P = ctypes.c_void_p
+
+    def call(b_max, **kw):
+        prm = psk.PskSelectParams()
+        prm.budgets = kw.get("budgets")
+        prm.budget_fraction = kw.get("fraction", 0.0)
+        prm.budget_pages = kw.get("pages", 0)
+        prm.mode = kw.get("mode", psk.BUDGET_PER_SEQUENCE)
+        prm.sink_pages = kw.get("sink", 1)
+        prm.window_pages = kw.get("window", 1)
+        return lib.psk_page_score_select_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), ctypes.byref(prm), b_max,
+                                            1.0, P(16), None, P(16), 64, None)
+
+    assert call(10, budgets=16) == 3                                          # checks pass, workspace short
+    assert call(10) == 1                                                      # per-sequence without budgets
+    assert call(10, budgets=16, sink=0) == 1 and call(10, budgets=16, window=0) == 1
+    assert call(10, mode=7, budgets=16) == 1
+    assert call(10, mode=psk.BUDGET_PAGES, pages=0) == 1
+    assert call(10, mode=psk.BUDGET_PAGES, pages=10) == 3
+    assert call(10, mode=psk.BUDGET_PAGES, pages=11) == 1                     # 11 pages exceed b_max
+    assert call(12, mode=psk.BUDGET_PAGES, pages=4, sink=4, window=8) == 3   # raised to the 12 kept
+    assert call(11, mode=psk.BUDGET_PAGES, pages=4, sink=4, window=8) == 1
+    assert call(10, mode=psk.BUDGET_FRACTION, fraction=0.0) == 1
+    assert call(10, mode=psk.BUDGET_FRACTION, fraction=1.5) == 1
+    assert call(3, mode=psk.BUDGET_FRACTION, fraction=0.05) == 3             # ceil(50 * 0.05) = 3
+    assert call(2, mode=psk.BUDGET_FRACTION, fraction=0.05) == 1
+    assert call(49, mode=psk.BUDGET_FRACTION, fraction=1.0) == 1             # every one of 50 pages

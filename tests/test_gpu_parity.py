@@ -216,6 +216,81 @@ def test_mla_nan_junk_past_seq_len_is_never_read(ps):
     _run_and_check(w, cache, [0, 1, 2], summ, w.queries(), step_tag=f"mla nan junk ps {ps}")
 
 
+def _run_select_params(w, cache, S, W, mode, value, step_tag):
+    """Score + select through the general entry (first S and last W pages kept, one budget mode)
+    and the sparse decode over its rows, each against the oracle."""
+    seqs = list(range(w.B))
+    summ = _check_cache_and_summaries(w, cache, seqs)
+    L = cache.layout
+    q_np = w.queries()
+    q = to_torch(q_np, w.dtype).cuda()
+    lens = [int(x) for x in w.seq_lens]
+    Ps = [-(-n // w.page_size) for n in lens]
+    if mode == "per_seq":
+        b_seq = [int(x) for x in w.budgets]
+        b_max = max(b_seq)
+        kw = dict(budgets=dev_budgets(w))
+    else:
+        arg = dict(fraction=value) if mode == "fraction" else dict(pages=value)
+        b_seq = [O.budget_for(P, sink_pages=S, window_pages=W, **arg) for P in Ps]
+        b_max = O.budget_for(L.max_pages, sink_pages=S, window_pages=W, **arg)
+        kw = dict(budget_fraction=value) if mode == "fraction" else dict(budget_pages=value)
+    ws = psk.make_workspace(L, b_max, device="cuda")
+    sel = torch.full((w.B, w.H_kv, b_max), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((w.B, w.H_kv, w.max_pages), float("nan"), device="cuda")
+    psk.page_score_select_ex(L, q, cache.summaries, cache.block_table, cache.seq_lens, b_max, cache.scale, sel, ws,
+                             sink_pages=S, window_pages=W, scores_out=scores, **kw)
+    out = torch.empty(w.B, w.H_q, w.D_v, dtype=cache.dtype, device="cuda")
+    psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel, b_max,
+                            cache.scale, out, ws)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(ws) == 0
+    sel_np, sc_np = sel.cpu().numpy(), scores.cpu().numpy()
+    out_np = from_torch(out.float(), "f32")
+    scale = 1.0 / math.sqrt(w.D)
+    for i in seqs:
+        n, P = lens[i], Ps[i]
+        kmin, kmax = summ[i]
+        s_ref = O.quest_scores(q_np[i], kmin, kmax, w.dtype, scale)
+        tol = score_tolerance(q_np[i], kmin, kmax, w.dtype, scale)
+        assert np.all(np.abs(sc_np[i, :, :P] - s_ref) <= tol), f"{step_tag} seq {i}: scores"
+        use = []
+        for h in range(w.H_kv):
+            ok, near, got, ref = compare_selection(sel_np[i, h], s_ref[h], b_seq[i], S, W)
+            assert ok, f"{step_tag} seq {i} head {h}: selected {got} vs oracle {ref}"
+            assert len(got) == min(b_seq[i], P)
+            use.append(got)
+        ref_out = O.attend_pages(q_np[i], w_keys(w, i, n), w_vals(w, i, n), n, w.page_size, use, w.dtype, scale)
+        check_output(out_np[i], ref_out, w.dtype)
+
+
+@pytest.mark.parametrize("case", [
+    dict(S=4, W=8, mode="per_seq", value=None, budgets=[40, 20, 12, 3, 12]),
+    dict(S=1, W=10, mode="pages", value=20, budgets=[2] * 5),
+    dict(S=2, W=3, mode="fraction", value=0.05, budgets=[2] * 5),
+    dict(S=3, W=2, mode="fraction", value=0.1, budgets=[2] * 5, dtype="f32", D=64, H_q=4, H_kv=1),
+    dict(S=1, W=1, mode="pages", value=7, budgets=[2] * 5, H_q=64, H_kv=16),
+])
+def test_sink_window_and_budget_modes(case):
+    """First S and last W pages always kept (inside the budget), budgets per sequence, as a fixed
+    page count or as a fraction of each sequence's pages rounded by the retained-count ceiling;
+    P = 301, 77, 41, 3 and 12 pages (the short ones keep every page)."""
+    extra = {k: case[k] for k in ("dtype", "D", "H_q", "H_kv") if k in case}
+    w = _custom([16 * 300 + 5, 16 * 77, 16 * 40 + 9, 33, 16 * 12], case["budgets"], **extra)
+    cache = upload(w)
+    _run_select_params(w, cache, case["S"], case["W"], case["mode"], case["value"], str(case))
+
+
+@pytest.mark.parametrize("case", [
+    dict(S=1, W=10, mode="pages", value=40, ps=64),    # the latent example of the configuration table, scaled
+    dict(S=2, W=4, mode="fraction", value=0.05, ps=32),
+])
+def test_mla_sink_window_and_budget_modes(case):
+    w = _custom_mla([case["ps"] * 300 + 5, case["ps"] * 90, case["ps"] * 13 + 1], [2, 2, 2], ps=case["ps"])
+    cache = upload(w)
+    _run_select_params(w, cache, case["S"], case["W"], case["mode"], case["value"], "mla " + str(case))
+
+
 def test_ties_resolve_to_lower_page():
     """Pages with identical keys (hence identical summaries and scores) tie; with the cutoff
     inside the tied group the lowest-indexed tied pages win."""
