@@ -57,15 +57,17 @@ def peaks():
 # call, with a digest of the sources the kernels are built from: a digest that no longer matches
 # means the kernels changed since the capture, and the traffic is reported as null.
 TRAFFIC = {
+    # python bench.py --steps 5 --warmup 3 --no-cpu-baseline, then
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
     ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel+page_select_kernel"):
-        {"bytes": 578_770_000 + 5_670_000 + 4_630_000, "digest": "9bf36a667019a5b6"},
-    # ncu ... -k regex:"mla_decode" -s 0 -c 1 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
-    ("mla-b16-128k-5pct", "mla_decode_kernel"):
-        {"bytes": 124_100_000 + 2_960_000, "digest": "38d10a9193009fbd"},
+        {"bytes": 577_377_280 + 4_712_192 + 4_620_032 + 0, "digest": "216194fe6d198738"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 468_580_000 + 1_660_000, "digest": "93d5ad7fdf55b742"},
+        {"bytes": 466_771_968 + 1_059_328, "digest": "98da506b5604161d"},
+    # python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline, then
+    # ncu ... -k regex:"mla_|page_select" -s 4 -c 4 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
+    ("mla-b16-128k-5pct", "mla_qsplit_kernel+mla_score_kernel+page_select_kernel"):
+        {"bytes": 2_363_136 + 0 + 80_296_192 + 27_648 + 197_632 + 0, "digest": "4949e54626c4b333"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel+page_select_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
