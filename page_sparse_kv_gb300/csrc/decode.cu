@@ -858,7 +858,13 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
   X(bf16_t, PSK_BF16, 128, 4) \
   X(bf16_t, PSK_BF16, 64, 4)  \
   X(float, PSK_F32, 64, 4)    \
-  X(float, PSK_F32, 128, 4)
+  X(float, PSK_F32, 128, 4)   \
+  X(bf16_t, PSK_BF16, 128, 1) \
+  X(bf16_t, PSK_BF16, 128, 2) \
+  X(bf16_t, PSK_BF16, 64, 1)  \
+  X(bf16_t, PSK_BF16, 64, 2)  \
+  X(float, PSK_F32, 64, 1)    \
+  X(float, PSK_F32, 128, 1)
 
 bool decode_supported(int dtype, int D, int D_v, int G, int ps) {
   if (D_v != D || ps % 16 != 0 || ps > 64) return false;

@@ -765,11 +765,17 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   return true;
 }
 
-#define PSK_SCORE_CASES(X)  \
+#define PSK_SCORE_CASES(X)   \
   X(bf16_t, PSK_BF16, 128, 4) \
   X(bf16_t, PSK_BF16, 64, 4)  \
   X(float, PSK_F32, 64, 4)    \
-  X(float, PSK_F32, 128, 4)
+  X(float, PSK_F32, 128, 4)   \
+  X(bf16_t, PSK_BF16, 128, 1) \
+  X(bf16_t, PSK_BF16, 128, 2) \
+  X(bf16_t, PSK_BF16, 64, 1)  \
+  X(bf16_t, PSK_BF16, 64, 2)  \
+  X(float, PSK_F32, 64, 1)    \
+  X(float, PSK_F32, 128, 1)
 
 bool score_supported(int dtype, int D, int G) {
 #define X(TT, DT, DD, GG) \

@@ -173,6 +173,12 @@ def _custom(seq_lens, budgets, ps=16, dtype="bf16", H_q=8, H_kv=2, D=128, n_hot=
     dict(seq_lens=[16 * 30 + 2, 300], budgets=[5, 4], D=64),
     dict(seq_lens=[16 * 70 + 3, 500], budgets=[9, 4], D=64, H_q=4, H_kv=1),   # 256-byte page runs
     dict(seq_lens=[16 * 45 + 8, 16 * 9], budgets=[7, 3], H_q=16, H_kv=4),      # 4 KV heads
+    dict(seq_lens=[16 * 50 + 3, 16 * 9], budgets=[7, 3], H_q=8, H_kv=8),       # G = 1 (MHA)
+    dict(seq_lens=[16 * 45 + 8, 300], budgets=[6, 4], H_q=16, H_kv=8),         # G = 2
+    dict(seq_lens=[16 * 33 + 1, 77], budgets=[5, 3], D=64, H_q=4, H_kv=4),     # G = 1, D = 64
+    dict(seq_lens=[16 * 61 + 2, 250], budgets=[8, 4], D=64, H_q=8, H_kv=4),    # G = 2, D = 64
+    dict(seq_lens=[16 * 20 + 9, 77], budgets=[6, 3], dtype="f32", D=64, H_q=2, H_kv=2),   # fp32, G = 1
+    dict(seq_lens=[16 * 27 + 4, 40], budgets=[5, 3], dtype="f32", H_q=1, H_kv=1),        # fp32, D = 128, G = 1
 ])
 def test_edge_cases(case):
     w = _custom(**case)
