@@ -126,6 +126,7 @@ __device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, 
     if (excl < need && incl >= need) {
       sh[0] = bin;
       sh[1] = excl;
+      sh[2 + kWarps] = v;  // keys in the chosen bin
     }
     __syncthreads();
     const int d = sh[0];
@@ -133,6 +134,13 @@ __device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, 
     prefix |= static_cast<uint32_t>(d) << shift;
     mask |= 255u << shift;
     if (shift == 0) break;
+    if (sh[2 + kWarps] == need) {
+      // every key of the chosen bin is taken, and so is every key above it: the selection is
+      // "key >= prefix" (prefix has zeros below this digit), with no tie left to break
+      prefix = prefix == 0u ? 0u : prefix - 1u;
+      need = 0;
+      break;
+    }
     shift = shift >= 8 ? shift - 8 : 0;
     // a digit that overlaps bits already fixed is harmless: they match the prefix
     __syncthreads();  // sh and wsum are rewritten by the next pass
