@@ -157,6 +157,25 @@ def quest_scores(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarray, dtype: str, 
     return out
 
 
+def quest_scores_per_query_head(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarray, dtype: str,
+                                scale: float) -> np.ndarray:
+    """The same bound for each query head on its own, with no group combine (EntmaxKV README,
+    "Two selection strategies", Top-k: the pages are ranked and kept per query head).
+
+    q: [H_q, D] stored; kmin, kmax: [P, H_kv, D] stored. Returns float64 [H_q, P]:
+      score[g, p] = scale * sum_d max(q[g,d]*kmin[p,h,d], q[g,d]*kmax[p,h,d]),  h = g // (H_q // H_kv).
+    """
+    qv, lo, hi = to_f64(q, dtype), to_f64(kmin, dtype), to_f64(kmax, dtype)
+    H_q = qv.shape[0]
+    P, H_kv, D = lo.shape
+    G = H_q // H_kv
+    out = np.empty((H_q, P))
+    for g in range(H_q):
+        h = g // G
+        out[g] = np.maximum(qv[g] * lo[:, h, :], qv[g] * hi[:, h, :]).sum(axis=1) * scale
+    return out
+
+
 # ----------------------------------------------------------------------------------
 # S3: top-b selection with forced sink and tail
 # ----------------------------------------------------------------------------------
@@ -165,9 +184,10 @@ def forced_pages(P: int, sink_pages: int = 1, window_pages: int = 1) -> list[int
     ``window_pages`` pages (the tail page among them), clipped to the P pages that exist
     (LOCKS PKG-INFO, "Configuration (LocksConfig)": sink_pages / window_pages, the always-kept
     first / recent pages, default 1 / 1). With the defaults: the sink (page 0) and the tail
-    (page P-1)."""
-    if sink_pages < 1 or window_pages < 1:
-        raise ValueError("sink_pages and window_pages are at least 1")
+    (page P-1). sink_pages = 0 keeps only recent pages, as EntmaxKV's top-k does (README, "Two
+    selection strategies": the budget includes the always-attended tail page)."""
+    if sink_pages < 0 or window_pages < 1:
+        raise ValueError("sink_pages >= 0 and window_pages >= 1 (the tail page is always kept)")
     return sorted(set(range(min(sink_pages, P))) | set(range(max(0, P - window_pages), P)))
 
 
@@ -267,6 +287,23 @@ def attend_pages(q: np.ndarray, keys: np.ndarray, values: np.ndarray, seq_len: i
         for j in range(G):
             g = h * G + j
             out[g] = softmax_attention(qv[g], kh, vh, scale)
+    return out
+
+
+def attend_pages_per_query_head(q: np.ndarray, keys: np.ndarray, values: np.ndarray, seq_len: int,
+                                page_size: int, selected, dtype: str, scale: float) -> np.ndarray:
+    """Decode output when pages are selected per query head: query head g attends the tokens of
+    its own selected pages of its KV head. selected: per query head a list of logical pages.
+    Returns float64 [H_q, D_v]."""
+    qv = to_f64(q, dtype)
+    H_q = qv.shape[0]
+    H_kv = keys.shape[1]
+    G = H_q // H_kv
+    out = np.empty((H_q, values.shape[2]))
+    for g in range(H_q):
+        h = g // G
+        t = page_tokens(selected[g], seq_len, page_size)
+        out[g] = softmax_attention(qv[g], to_f64(keys[t, h], dtype), to_f64(values[t, h], dtype), scale)
     return out
 
 

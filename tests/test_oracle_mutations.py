@@ -13,7 +13,7 @@ import oracle.psk_oracle as OP
 import test_oracle_pins as PINS
 
 ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention",
-                                             "forced_pages", "retained_count")}
+                                             "forced_pages", "retained_count", "quest_scores_per_query_head")}
 
 
 @pytest.fixture
@@ -67,6 +67,12 @@ def _forced_window_of_one(P, sink_pages=1, window_pages=1):  # window_pages read
 
 def _retained_round_nearest(N, r):  # rounds N * r to nearest instead of the ceiling
     return min(N, max(1, int(round(N * r))))
+
+
+def _per_query_head_wrong_kv_head(q, kmin, kmax, dtype, scale):  # query head g read KV head g % H_kv
+    H_q, H_kv = q.shape[0], kmin.shape[1]
+    order = [(g % H_kv) * (H_q // H_kv) + g // H_kv for g in range(H_q)]
+    return ORIG["quest_scores_per_query_head"](q[order], kmin, kmax, dtype, scale)[np.argsort(order)]
 
 
 def _summaries_whole_pages(keys, seq_len, page_size, dtype):  # counts the tail page's junk rows
@@ -135,3 +141,8 @@ def test_window_of_one_is_caught(plant):
 def test_fraction_rounded_to_nearest_is_caught(plant, golden_dir):
     plant("retained_count", _retained_round_nearest)
     _fails(PINS.test_retained_count_golden_and_closed_forms, golden_dir)
+
+
+def test_per_query_head_wrong_kv_head_is_caught(plant):
+    plant("quest_scores_per_query_head", _per_query_head_wrong_kv_head)
+    _fails(PINS.test_per_query_head_bound_tight_on_single_token_pages_and_dominating, 0)

@@ -257,14 +257,14 @@ def test_selection_rejects_budget_below_two():
 
 
 # ------------------------------------------------------------------ S3 always-kept sets and budget modes
-SW_CASES = [(1, 1), (2, 1), (1, 3), (3, 2), (4, 4)]
+SW_CASES = [(1, 1), (2, 1), (1, 3), (3, 2), (4, 4), (0, 1), (0, 3)]
 
 
 @pytest.mark.parametrize("P", [1, 2, 3, 5, 7, 9])
 def test_forced_set_closed_forms(P):
     """The always-kept set of sink_pages S and window_pages W is a prefix plus a suffix of the
-    pages: it holds min(P, S + W) pages, all of them once S + W >= P, page 0 and page P - 1
-    always, and its complement is the contiguous run [S, P - W)."""
+    pages: it holds min(P, S + W) pages, all of them once S + W >= P, page 0 (when S >= 1) and
+    page P - 1 always, and its complement is the contiguous run [S, P - W)."""
     assert O.forced_pages(P) == O.forced_pages(P, 1, 1) == ([0] if P == 1 else [0, P - 1])
     for S in range(1, 6):
         for W in range(1, 6):
@@ -273,8 +273,12 @@ def test_forced_set_closed_forms(P):
             assert f[0] == 0 and f[-1] == P - 1
             rest = [p for p in range(P) if p not in f]
             assert rest == list(range(S, P - W)) if S + W < P else rest == []
-    with pytest.raises(ValueError):
-        O.forced_pages(4, 0, 1)
+    for W in range(1, 6):  # no sink: only the last W pages (the tail among them)
+        f = O.forced_pages(P, 0, W)
+        assert f == list(range(max(0, P - W), P)) and len(f) == min(P, W) and f[-1] == P - 1
+    for bad in ((1, 0), (-1, 1)):
+        with pytest.raises(ValueError):
+            O.forced_pages(4, *bad)
 
 
 @pytest.mark.parametrize("S,W", SW_CASES)
@@ -330,6 +334,59 @@ def test_budget_modes():
     for bad in (dict(), dict(fraction=0.1, pages=3), dict(fraction=0.0), dict(fraction=1.5), dict(pages=0)):
         with pytest.raises(ValueError):
             O.budget_for(10, **bad)
+
+
+# ------------------------------------------------------------------ per-query-head selection
+@pytest.mark.parametrize("seed", [0, 1])
+def test_per_query_head_bound_tight_on_single_token_pages_and_dominating(seed):
+    """Per query head, the bound is at or above every logit of its KV head's tokens in the page,
+    equals the logit exactly on a page that holds one valid token, and its group max is the
+    grouped bound."""
+    rng = np.random.default_rng(300 + seed)
+    H_q, H_kv, D, ps = 8, 2, 16, 16
+    n = 16 * 4 + 1                                    # the tail page holds one token
+    keys = _rand_keys(rng, n, H_kv, D, "bf16")
+    q = W.f32_to_bf16_bits(rng.standard_normal((H_q, D)).astype(np.float32))
+    kmin, kmax = O.page_summaries(keys, n, ps, "bf16")
+    s = O.quest_scores_per_query_head(q, kmin, kmax, "bf16", 1.0)
+    kv, qv = O.to_f64(keys, "bf16"), O.to_f64(q, "bf16")
+    G = H_q // H_kv
+    P = s.shape[1]
+    for g in range(H_q):
+        h = g // G
+        for p in range(P):
+            page = kv[p * ps:min((p + 1) * ps, n), h]
+            logits = page @ qv[g]
+            tol = 1e-12 * float(np.abs(qv[g]).sum() * np.abs(page).max())
+            assert np.all(logits <= s[g, p] + tol)
+        assert abs(s[g, P - 1] - float(kv[n - 1, h] @ qv[g])) <= 1e-12 * float(np.abs(qv[g]).sum() + 1)
+    grouped = O.quest_scores(q, kmin, kmax, "bf16", 1.0)
+    assert np.array_equal(s.reshape(H_kv, G, P).max(axis=1), grouped)
+
+
+def test_per_query_head_attention_reduces_to_grouped_and_dense():
+    """Each query head given its KV head's list is the grouped decode; every page for every head
+    is dense attention; one head's own list is torch's attention on those tokens."""
+    rng = np.random.default_rng(91)
+    H_q, H_kv, D, ps, n = 8, 2, 16, 16, 16 * 7 + 5
+    keys = _rand_keys(rng, n + ps, H_kv, D, "f32")
+    vals = _rand_keys(rng, n + ps, H_kv, D, "f32")
+    q = _rand_keys(rng, H_q, 1, D, "f32")[:, 0]
+    scale = 0.25
+    G = H_q // H_kv
+    per_kv = [[0, 3, 7], [0, 2, 5, 7]]
+    a = O.attend_pages_per_query_head(q, keys, vals, n, ps, [per_kv[g // G] for g in range(H_q)], "f32", scale)
+    assert np.array_equal(a, O.attend_pages(q, keys, vals, n, ps, per_kv, "f32", scale))
+    P = -(-n // ps)
+    d = O.attend_pages_per_query_head(q, keys, vals, n, ps, [list(range(P))] * H_q, "f32", scale)
+    assert np.array_equal(d, O.dense_attention(q, keys, vals, n, ps, "f32", scale))
+    own = [[0, 1 + (g % 5), P - 1] for g in range(H_q)]
+    out = O.attend_pages_per_query_head(q, keys, vals, n, ps, own, "f32", scale)
+    for g in (0, 5):
+        t = O.page_tokens(own[g], n, ps)
+        ref = _sdpa_reference(O.to_f64(q[g:g + 1], "f32"), O.to_f64(keys[t, g // G][:, None], "f32"),
+                              O.to_f64(vals[t, g // G][:, None], "f32"), scale)
+        assert np.allclose(out[g], ref[0], rtol=1e-12, atol=1e-12)
 
 
 # ------------------------------------------------------------------ S4 attention
