@@ -176,7 +176,8 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
  * "Configuration (LocksConfig)": sink_pages / window_pages, budget, budget_pages).
  *
  * Always-kept pages of sequence i: F_i = [0, sink_pages) U [P_i - window_pages, P_i), clipped
- * to [0, P_i); |F_i| = min(P_i, sink_pages + window_pages). The budget b_i counts them:
+ * to [0, P_i); |F_i| = min(P_i, sink_pages + window_pages); sink_pages >= 0, window_pages >= 1
+ * (the tail page is always kept). The budget b_i counts them:
  *   PSK_BUDGET_PER_SEQUENCE  b_i = budgets[i] (device int32 [batch]); a b_i below |F_i| or
  *                            above b_max flags PSK_DEV_BAD_BUDGET and writes the row as -1;
  *   PSK_BUDGET_PAGES         b_i = max(|F_i|, min(P_i, budget_pages)), budget_pages >= 1;
@@ -190,6 +191,14 @@ int psk_page_score_select(const psk_layout *layout, const void *q, const void *s
  * pages can get. Everything else is as psk_page_score_select, which is this call with
  * PSK_BUDGET_PER_SEQUENCE and sink_pages = window_pages = 1. Without scores_out the
  * summaries of the always-kept pages are not read.
+ *
+ * per_query_head = 1 (GQA only; EntmaxKV README, "Two selection strategies", Top-k: pages are
+ * kept per query head) ranks and selects pages for every query head g on its own, with
+ *   score[i,g,p] = scale * sum_d max(q[i,g,d]*kmin[p,h,d], q[i,g,d]*kmax[p,h,d]),  h = g / G,
+ * so selected is [batch, num_q_heads, b_max] and scores_out [batch, num_q_heads, max_pages];
+ * decode such rows with psk_sparse_paged_decode_ex and PSK_DECODE_PER_QUERY_HEAD. Each query
+ * head then reads its own pages, so the decode moves up to G times the K/V bytes of per-KV-head
+ * selection at the same budget.
  * --------------------------------------------------------------------------------------- */
 enum psk_budget_mode { PSK_BUDGET_PER_SEQUENCE = 0, PSK_BUDGET_PAGES = 1, PSK_BUDGET_FRACTION = 2 };
 
@@ -198,8 +207,9 @@ typedef struct psk_select_params {
   double budget_fraction;  /* PSK_BUDGET_FRACTION                                         */
   int32_t budget_pages;    /* PSK_BUDGET_PAGES                                            */
   int32_t mode;            /* enum psk_budget_mode                                        */
-  int32_t sink_pages;      /* >= 1                                                        */
+  int32_t sink_pages;      /* >= 0                                                        */
   int32_t window_pages;    /* >= 1                                                        */
+  int32_t per_query_head;  /* 0: one row per (sequence, KV head); 1: per (sequence, q head) */
 } psk_select_params;
 
 int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void *summaries,
@@ -228,6 +238,20 @@ int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *
                            const void *v_cache, const int32_t *block_table,
                            const int32_t *seq_lens, float scale, void *out, void *workspace,
                            size_t workspace_bytes, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * psk_sparse_paged_decode with flags. PSK_DECODE_PER_QUERY_HEAD: selected is
+ * [batch, num_q_heads, b_max] (rows of psk_page_score_select_ex with per_query_head = 1) and
+ * query head g attends its own row's pages of KV head g / G. flags = 0 is
+ * psk_sparse_paged_decode. GQA only; the workspace is the one psk_sparse_decode_workspace_size
+ * sizes (it covers both forms).
+ * --------------------------------------------------------------------------------------- */
+#define PSK_DECODE_PER_QUERY_HEAD 0x1u
+int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_table,
+                               const int32_t *seq_lens, const int32_t *selected, int32_t b_max,
+                               float scale, uint32_t flags, void *out, void *workspace,
+                               size_t workspace_bytes, psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Stage 4 without a workspace (no counterpart in the pages: an addition for callers that

@@ -22,7 +22,7 @@ DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND,
 
 EXPORTS = [
     "psk_kv_append_and_summarize", "psk_page_score_select", "psk_page_score_select_ex", "psk_sparse_paged_decode",
-    "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
+    "psk_sparse_paged_decode_ex", "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version",
 ]
@@ -41,12 +41,14 @@ class PskLayout(ctypes.Structure):
 
 
 BUDGET_PER_SEQUENCE, BUDGET_PAGES, BUDGET_FRACTION = 0, 1, 2
+DECODE_PER_QUERY_HEAD = 0x1
 
 
 class PskSelectParams(ctypes.Structure):
     """Mirrors ``psk_select_params``."""
     _fields_ = [("budgets", ctypes.c_void_p), ("budget_fraction", ctypes.c_double), ("budget_pages", ctypes.c_int32),
-                ("mode", ctypes.c_int32), ("sink_pages", ctypes.c_int32), ("window_pages", ctypes.c_int32)]
+                ("mode", ctypes.c_int32), ("sink_pages", ctypes.c_int32), ("window_pages", ctypes.c_int32),
+                ("per_query_head", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -87,6 +89,7 @@ def lib() -> ctypes.CDLL:
             "psk_page_score_select_ex": (ctypes.c_int, [LP, P, P, P, P, ctypes.POINTER(PskSelectParams), I, F, P, P,
                                                         P, Z, P]),
             "psk_sparse_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P, Z, P]),
+            "psk_sparse_paged_decode_ex": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, ctypes.c_uint32, P, P, Z, P]),
             "psk_dense_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, F, P, P, Z, P]),
             "psk_sparse_paged_decode_noalloc": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P]),
             "psk_append_workspace_size": (Z, [LP]),
@@ -186,10 +189,12 @@ def page_score_select(layout: Layout, q, summaries, block_table, seq_lens, budge
 def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_max: int, scale: float, selected,
                          workspace, *, budgets=None, budget_pages: int | None = None,
                          budget_fraction: float | None = None, sink_pages: int = 1, window_pages: int = 1,
-                         scores_out=None, stream=None):
+                         per_query_head: bool = False, scores_out=None, stream=None):
     """Score + select with the first ``sink_pages`` and last ``window_pages`` pages always kept
     and exactly one budget mode: ``budgets`` (device int32 per sequence), ``budget_pages`` (a
-    fixed page count) or ``budget_fraction`` (a fraction of each sequence's pages)."""
+    fixed page count) or ``budget_fraction`` (a fraction of each sequence's pages). With
+    ``per_query_head`` the rows are per (sequence, query head): ``selected`` is
+    [batch, num_q_heads, b_max]."""
     modes = [budgets is not None, budget_pages is not None, budget_fraction is not None]
     if sum(modes) != 1:
         raise ValueError("give exactly one of budgets, budget_pages, budget_fraction")
@@ -199,6 +204,7 @@ def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_
     prm.budget_pages = int(budget_pages or 0)
     prm.mode = BUDGET_PER_SEQUENCE if modes[0] else (BUDGET_PAGES if modes[1] else BUDGET_FRACTION)
     prm.sink_pages, prm.window_pages = int(sink_pages), int(window_pages)
+    prm.per_query_head = 1 if per_query_head else 0
     _check("psk_page_score_select_ex", lib().psk_page_score_select_ex(
         ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), ctypes.byref(prm),
         int(b_max), float(scale), _ptr(selected), _ptr(scores_out), _ptr(workspace),
@@ -211,6 +217,15 @@ def sparse_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_le
         ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(selected), int(b_max), float(scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def sparse_paged_decode_ex(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max: int,
+                           scale: float, out, workspace, per_query_head: bool = False, stream=None):
+    """sparse_paged_decode over rows per (sequence, query head) when ``per_query_head``."""
+    _check("psk_sparse_paged_decode_ex", lib().psk_sparse_paged_decode_ex(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(selected), int(b_max), float(scale), DECODE_PER_QUERY_HEAD if per_query_head else 0, _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def dense_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, scale: float, out, workspace,

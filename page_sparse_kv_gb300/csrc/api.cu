@@ -52,6 +52,20 @@ int check_gqa_compute(const psk_layout *L) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PSK_OK : PSK_ERR_CUDA; }
 
+// The per-query-head view of a GQA layout: one unit head per query head (num_kv_heads =
+// num_q_heads, group size 1); unit head h reads cache head h >> kv_shift, G = 2^kv_shift. False
+// when that form is not built for this layout (G not a power of two included).
+bool per_query_head_view(const psk_layout &L, psk_layout *V, int *kv_shift) {
+  if (L.latent) return false;
+  const int G = L.num_q_heads / L.num_kv_heads;
+  if (G & (G - 1)) return false;
+  *V = L;
+  V->num_kv_heads = L.num_q_heads;
+  *kv_shift = __builtin_ctz((unsigned)G);
+  return score_supported(L.dtype, L.head_dim, 1) &&
+         decode_supported(L.dtype, L.head_dim, L.v_head_dim, 1, L.page_size);
+}
+
 }  // namespace
 
 extern "C" {
@@ -73,10 +87,18 @@ size_t psk_append_workspace_size(const psk_layout *layout) {
   return check_layout(layout) == PSK_OK ? kWsHeader : 0;
 }
 
+// Score / select and sparse decode sizes cover both the per-KV-head and the per-query-head
+// forms, so one workspace serves every call of a layout.
 size_t psk_score_select_workspace_size(const psk_layout *layout, int32_t b_max) {
   if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
   ScorePlan plan;
-  return plan_score(*layout, b_max, &plan) ? plan.ws_bytes : 0;
+  if (!plan_score(*layout, b_max, &plan)) return 0;
+  size_t bytes = plan.ws_bytes;
+  psk_layout V;
+  int kv_shift;
+  if (per_query_head_view(*layout, &V, &kv_shift) && plan_score(V, b_max, &plan, kv_shift))
+    bytes = std::max(bytes, plan.ws_bytes);
+  return bytes;
 }
 
 static bool plan_any_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan) {
@@ -86,7 +108,13 @@ static bool plan_any_decode(const psk_layout &L, int entries, bool dense, Decode
 size_t psk_sparse_decode_workspace_size(const psk_layout *layout, int32_t b_max) {
   if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
   DecodePlan plan;
-  return plan_any_decode(*layout, b_max, false, &plan) ? plan.ws_bytes : 0;
+  if (!plan_any_decode(*layout, b_max, false, &plan)) return 0;
+  size_t bytes = plan.ws_bytes;
+  psk_layout V;
+  int kv_shift;
+  if (per_query_head_view(*layout, &V, &kv_shift) && plan_decode(V, b_max, false, &plan))
+    bytes = std::max(bytes, plan.ws_bytes);
+  return bytes;
 }
 
 size_t psk_dense_decode_workspace_size(const psk_layout *layout) {
@@ -183,7 +211,8 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
   if (!q || !summaries || !block_table || !seq_lens || !params || !selected || b_max < 1)
     return PSK_ERR_INVALID_ARG;
   const psk_select_params &sp = *params;
-  if (sp.sink_pages < 1 || sp.window_pages < 1) return PSK_ERR_INVALID_ARG;
+  if (sp.sink_pages < 0 || sp.window_pages < 1) return PSK_ERR_INVALID_ARG;
+  if (sp.per_query_head != 0 && sp.per_query_head != 1) return PSK_ERR_INVALID_ARG;
   if (sp.mode == PSK_BUDGET_PER_SEQUENCE) {
     if (!sp.budgets) return PSK_ERR_INVALID_ARG;
   } else if (sp.mode == PSK_BUDGET_PAGES || sp.mode == PSK_BUDGET_FRACTION) {
@@ -197,8 +226,12 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
   if (!aligned16(q) || !aligned16(summaries)) return PSK_ERR_INVALID_ARG;
   rc = check_gqa_compute(layout);
   if (rc != PSK_OK) return rc;
+  // the units' layout: the cache's own, or its per-query-head view
+  psk_layout U = L;
+  int kv_shift = 0;
+  if (sp.per_query_head && !per_query_head_view(L, &U, &kv_shift)) return PSK_ERR_UNSUPPORTED;
   ScorePlan plan;
-  if (!plan_score(L, b_max, &plan)) return PSK_ERR_UNSUPPORTED;
+  if (!plan_score(U, b_max, &plan, kv_shift)) return PSK_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.ws_bytes) return PSK_ERR_WORKSPACE;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   ScoreArgs a;
@@ -218,7 +251,9 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
   a.cand_count = reinterpret_cast<int32_t *>(ws + plan.off_count);
   a.B = L.batch;
   a.H_q = L.num_q_heads;
-  a.H_kv = L.num_kv_heads;
+  a.H_kv = U.num_kv_heads;
+  a.H_kv_cache = L.num_kv_heads;
+  a.kv_shift = kv_shift;
   a.D = L.head_dim;
   a.ps = L.page_size;
   a.nb = L.num_blocks;
@@ -244,7 +279,7 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
 static int decode_common(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
                          int32_t b_max, float scale, void *out, void *workspace, size_t workspace_bytes,
-                         psk_stream_t stream) {
+                         psk_stream_t stream, bool per_query_head = false) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
@@ -254,8 +289,11 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   rc = check_gqa_compute(layout);
   if (rc != PSK_OK) return rc;
   const bool dense = selected == nullptr;
+  psk_layout U = L;  // the units' layout (per-query-head view for per-query-head rows)
+  int kv_shift = 0;
+  if (per_query_head && (dense || !per_query_head_view(L, &U, &kv_shift))) return PSK_ERR_UNSUPPORTED;
   DecodePlan plan;
-  if (!plan_any_decode(L, dense ? L.max_pages : b_max, dense, &plan)) return PSK_ERR_UNSUPPORTED;
+  if (!plan_any_decode(U, dense ? L.max_pages : b_max, dense, &plan)) return PSK_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.ws_bytes) return PSK_ERR_WORKSPACE;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   DecodeArgs a;
@@ -272,7 +310,9 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.tickets = reinterpret_cast<uint32_t *>(ws + plan.off_tickets);
   a.B = L.batch;
   a.H_q = L.num_q_heads;
-  a.H_kv = L.num_kv_heads;
+  a.H_kv = U.num_kv_heads;
+  a.H_kv_cache = L.num_kv_heads;
+  a.kv_shift = kv_shift;
   a.D = L.head_dim;
   a.D_v = L.v_head_dim;
   a.ps = L.page_size;
@@ -296,6 +336,15 @@ int psk_sparse_paged_decode(const psk_layout *layout, const void *q, const void 
   if (!selected || b_max < 1) return PSK_ERR_INVALID_ARG;
   return decode_common(layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max, scale, out, workspace,
                        workspace_bytes, stream);
+}
+
+int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
+                               int32_t b_max, float scale, uint32_t flags, void *out, void *workspace,
+                               size_t workspace_bytes, psk_stream_t stream) {
+  if (!selected || b_max < 1 || (flags & ~PSK_DECODE_PER_QUERY_HEAD) != 0) return PSK_ERR_INVALID_ARG;
+  return decode_common(layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max, scale, out, workspace,
+                       workspace_bytes, stream, (flags & PSK_DECODE_PER_QUERY_HEAD) != 0);
 }
 
 int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,

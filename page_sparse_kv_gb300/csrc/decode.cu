@@ -284,8 +284,8 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
         const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
         const int row = ent_blk[e] * a.ps + sub * 16;
         const uint64_t pol = l2_evict_first_policy();  // K/V rows are read once per step
-        tma_load_3d_stream(sK, tmK, 0, h, row, bar, pol);
-        tma_load_3d_stream(sK + TR::TILE, tmV, 0, h, row, bar, pol);
+        tma_load_3d_stream(sK, tmK, 0, h >> a.kv_shift, row, bar, pol);  // the unit head's cache head
+        tma_load_3d_stream(sK + TR::TILE, tmV, 0, h >> a.kv_shift, row, bar, pol);
       } else {
         mbar_arrive_expect_tx(bar, 0u);
       }
@@ -771,8 +771,8 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   CUtensorMap tmK, tmV;
   const long long rows = (long long)a.nb * a.ps;
   const int dt = sizeof(T) == 4 ? PSK_F32 : PSK_BF16;
-  if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv, rows, 16) ||
-      !encode_cache_map(&tmV, a.v_cache, dt, D, a.H_kv, rows, 16))
+  if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv_cache, rows, 16) ||
+      !encode_cache_map(&tmV, a.v_cache, dt, D, a.H_kv_cache, rows, 16))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (!a.flat) {

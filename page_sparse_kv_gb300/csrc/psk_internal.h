@@ -50,7 +50,9 @@ struct ScoreArgs {
   int n_chunks_max;
   int k_cap;              // candidates kept per chunk = min(b_max - 2, chunk) (>= 1)
   float scale;
-  int sink, window;       // always-kept first / last pages (>= 1 each)
+  int sink, window;       // always-kept first (>= 0) / last (>= 1) pages
+  int H_kv_cache;         // KV heads of the cache (H_kv above counts the units' heads)
+  int kv_shift;           // unit head h reads cache head h >> kv_shift (log2 G when selecting per query head)
   int budget_mode;        // enum psk_budget_mode
   int budget_pages;       // PSK_BUDGET_PAGES
   double budget_frac;     // PSK_BUDGET_FRACTION
@@ -65,7 +67,9 @@ struct ScorePlan {
   size_t ws_bytes;
   size_t off_counters, off_keys, off_key, off_page, off_count, off_qsplit;
 };
-bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan);
+// kv_shift > 0: L is the per-query-head view (num_kv_heads = num_q_heads), whose unit heads share
+// cache heads 2^kv_shift at a time.
+bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift = 0);
 cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s);
 cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s);
 bool score_supported(int dtype, int D, int G);
@@ -84,6 +88,8 @@ struct DecodeArgs {
   uint32_t *tickets;   // [B * H_kv] merge tickets (zero between calls)
   int B, H_q, H_kv, D, D_v, ps, nb, max_pages;
   int b_max;           // entries per selected row (sparse)
+  int H_kv_cache;      // KV heads of the cache (H_kv above counts the units' heads)
+  int kv_shift;        // unit head h reads cache head h >> kv_shift
   int sw;              // list entries per item (split layout)
   int n_items_max;     // items per unit (split layout)
   int32_t *counts;     // [B * H_kv] list entries per unit (flat layout, sparse)

@@ -264,7 +264,10 @@ constexpr int kPageSteps = 1;  // page steps per loop iteration
 constexpr int kTailChunk = 16;  // pages per CTA of the tail region
 constexpr int kTailWaves = 1;   // resident waves of CTAs that the tail region fills
 
-template <typename T, int D, int G>
+// kPerQueryHead: the units are the per-query-head view (G = 1 per unit), whose heads share cache
+// heads 2^kv_shift at a time; otherwise unit heads are cache heads (a shift of 0 known at compile
+// time, which the per-KV-head form is measurably faster with).
+template <typename T, int D, int G, bool kPerQueryHead>
 __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   pdl_wait();  // the select launch is released at the end of the loop (see below)
   constexpr int EPC = Elem<T>::kPerChunk;
@@ -277,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   __shared__ int okflag[kStages][kMaxStagePages];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kv_shift = kPerQueryHead ? a.kv_shift : 0;
+  const int H_cache = kPerQueryHead ? a.H_kv_cache : a.H_kv;
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA
   const int ng = kWarps / hpc;                         // warps per head
   // work item of this CTA: (chunk, sequence, head group) with the chunk index fastest, first in
@@ -302,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   const int h = h0 + hh;
   const int wg = warp / hpc;
   const int unit = i * a.H_kv + h;
-  const int group_bytes = hpc * 2 * D * ES;            // one page's summaries for the CTA's heads
+  // one page's summaries for the CTA's heads: cache heads h0 >> kv_shift .. (h0 + hpc - 1) >> kv_shift
+  const int group_bytes = (hpc >> kv_shift) * 2 * D * ES;
   const int sp = a.stage_pages;
   const int n_stages = (p1 - p0 + sp - 1) / sp;
   const T *sumbase = reinterpret_cast<const T *>(a.summaries);
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
     __syncwarp();
     if (ok)
       bulk_g2s_stream(smem_u32(smem_raw + (size_t)slot * kStageBytes + (size_t)lane * group_bytes),
-                      sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar, stream_policy);
+                      sumbase + ((size_t)blk * H_cache + (h0 >> kv_shift)) * 2 * D, group_bytes, bar, stream_policy);
   };
 
   if (warp == 0)
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   uint32_t *krow = a.keys + (size_t)unit * a.key_stride;
   float *srow = a.scores_out ? a.scores_out + (size_t)unit * a.max_pages : nullptr;
   // this lane's byte offset inside a page's run: its head and its chunk
-  const uint32_t lane_off = (uint32_t)hh * 2 * D * ES + sub * 16;
+  const uint32_t lane_off = (uint32_t)(hh >> kv_shift) * 2 * D * ES + sub * 16;
 
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % kStages;
@@ -677,7 +683,12 @@ template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
   const int k1_smem = kStages * kStageBytes;
-  auto kfn = page_score_kernel<T, D, G>;
+  auto kfn = page_score_kernel<T, D, G, false>;
+  if constexpr (G == 1) {
+    if (a.kv_shift != 0) kfn = page_score_kernel<T, D, G, true>;
+  } else {
+    if (a.kv_shift != 0) return cudaErrorInvalidValue;  // the per-query-head view has G = 1
+  }
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, k1_smem);
   if (e != cudaSuccess) return e;
   // Tail region: about kTailWaves waves of short CTAs over the sequences' last pages. A grid of
@@ -722,10 +733,10 @@ cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
   return launch_kernel(false, page_select_kernel, g2, kThreads, smem, s, a);
 }
 
-bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
+bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
   if (L.num_kv_heads > kWarps && L.num_kv_heads % kWarps != 0) return false;
   if (L.num_kv_heads < kWarps && kWarps % L.num_kv_heads != 0) return false;
-  const int kfree_max = std::max(1, b_max - 2);
+  const int kfree_max = std::max(1, b_max - 1);  // at least the tail page is always kept
   int chunk = 4096;
   while (true) {
     const int nch = (L.max_pages + chunk - 1) / chunk;
@@ -752,7 +763,7 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan) {
   {
     const int hpc = L.num_kv_heads < kWarps ? L.num_kv_heads : kWarps;
     const int es = L.dtype == PSK_F32 ? 4 : 2;
-    const int group_bytes = hpc * 2 * L.head_dim * es;
+    const int group_bytes = (hpc >> kv_shift) * 2 * L.head_dim * es;
     plan->stage_pages = group_bytes > kStageBytes ? 1 : std::min(kMaxStagePages, kStageBytes / group_bytes);
     if (group_bytes > kStageBytes && !L.latent) return false;
   }

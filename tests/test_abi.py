@@ -94,12 +94,15 @@ def test_select_params_host_checks(lib):
         prm.mode = kw.get("mode", psk.BUDGET_PER_SEQUENCE)
         prm.sink_pages = kw.get("sink", 1)
         prm.window_pages = kw.get("window", 1)
+        prm.per_query_head = kw.get("pqh", 0)
         return lib.psk_page_score_select_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), ctypes.byref(prm), b_max,
                                             1.0, P(16), None, P(16), 64, None)
 
     assert call(10, budgets=16) == 3                                          # checks pass, workspace short
     assert call(10) == 1                                                      # per-sequence without budgets
-    assert call(10, budgets=16, sink=0) == 1 and call(10, budgets=16, window=0) == 1
+    assert call(10, budgets=16, sink=-1) == 1 and call(10, budgets=16, window=0) == 1
+    assert call(10, budgets=16, sink=0) == 3                                  # recent pages only
+    assert call(10, budgets=16, pqh=1) == 3 and call(10, budgets=16, pqh=2) == 1
     assert call(10, mode=7, budgets=16) == 1
     assert call(10, mode=psk.BUDGET_PAGES, pages=0) == 1
     assert call(10, mode=psk.BUDGET_PAGES, pages=10) == 3
@@ -111,3 +114,16 @@ def test_select_params_host_checks(lib):
     assert call(3, mode=psk.BUDGET_FRACTION, fraction=0.05) == 3             # ceil(50 * 0.05) = 3
     assert call(2, mode=psk.BUDGET_FRACTION, fraction=0.05) == 1
     assert call(49, mode=psk.BUDGET_FRACTION, fraction=1.0) == 1             # every one of 50 pages
+    # the decode with flags: unknown flag bits, or no selected rows, answer before any launch
+    rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), P(16), 10, 1.0, 0x2,
+                                        P(16), P(16), 1 << 30, None)
+    assert rc == 1
+    rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), None, 10, 1.0, 0x1,
+                                        P(16), P(16), 1 << 30, None)
+    assert rc == 1
+    rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), P(16), 10, 1.0, 0x1,
+                                        P(16), P(16), 64, None)
+    assert rc == 3
+    # one workspace covers the per-query-head form too
+    big = psk.Layout(2, 32, 8, 128, 128, 16, 100, 50)
+    assert psk.score_select_workspace_size(big, 10) > 0 and psk.sparse_decode_workspace_size(big, 10) > 0

@@ -222,9 +222,19 @@ def test_mla_nan_junk_past_seq_len_is_never_read(ps):
     _run_and_check(w, cache, [0, 1, 2], summ, w.queries(), step_tag=f"mla nan junk ps {ps}")
 
 
-def _run_select_params(w, cache, S, W, mode, value, step_tag):
-    """Score + select through the general entry (first S and last W pages kept, one budget mode)
-    and the sparse decode over its rows, each against the oracle."""
+def _qhead_tolerance(q, kmin, kmax, dtype, scale):
+    """Per (query head, page) bound on fp32 accumulation error of the per-query-head score (the
+    same rule as parity.score_tolerance, without the group max)."""
+    qv, lo, hi = O.to_f64(q, dtype), O.to_f64(kmin, dtype), O.to_f64(kmax, dtype)
+    G = qv.shape[0] // lo.shape[1]
+    mag = np.maximum(np.abs(lo), np.abs(hi))
+    return np.stack([np.abs(qv[g]) @ mag[:, g // G, :].T for g in range(qv.shape[0])]) * 2e-6 * scale + 1e-30
+
+
+def _run_select_params(w, cache, S, W, mode, value, step_tag, per_query_head=False):
+    """Score + select through the general entry (first S and last W pages kept, one budget mode,
+    rows per KV head or per query head) and the sparse decode over its rows, each against the
+    oracle."""
     seqs = list(range(w.B))
     summ = _check_cache_and_summaries(w, cache, seqs)
     L = cache.layout
@@ -242,13 +252,14 @@ def _run_select_params(w, cache, S, W, mode, value, step_tag):
         b_max = O.budget_for(L.max_pages, sink_pages=S, window_pages=W, **arg)
         kw = dict(budget_fraction=value) if mode == "fraction" else dict(budget_pages=value)
     ws = psk.make_workspace(L, b_max, device="cuda")
-    sel = torch.full((w.B, w.H_kv, b_max), -7, dtype=torch.int32, device="cuda")
-    scores = torch.full((w.B, w.H_kv, w.max_pages), float("nan"), device="cuda")
+    R = w.H_q if per_query_head else w.H_kv  # rows per sequence
+    sel = torch.full((w.B, R, b_max), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((w.B, R, w.max_pages), float("nan"), device="cuda")
     psk.page_score_select_ex(L, q, cache.summaries, cache.block_table, cache.seq_lens, b_max, cache.scale, sel, ws,
-                             sink_pages=S, window_pages=W, scores_out=scores, **kw)
+                             sink_pages=S, window_pages=W, per_query_head=per_query_head, scores_out=scores, **kw)
     out = torch.empty(w.B, w.H_q, w.D_v, dtype=cache.dtype, device="cuda")
-    psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel, b_max,
-                            cache.scale, out, ws)
+    psk.sparse_paged_decode_ex(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel, b_max,
+                               cache.scale, out, ws, per_query_head=per_query_head)
     torch.cuda.synchronize()
     assert psk.get_device_status(ws) == 0
     sel_np, sc_np = sel.cpu().numpy(), scores.cpu().numpy()
@@ -257,17 +268,38 @@ def _run_select_params(w, cache, S, W, mode, value, step_tag):
     for i in seqs:
         n, P = lens[i], Ps[i]
         kmin, kmax = summ[i]
-        s_ref = O.quest_scores(q_np[i], kmin, kmax, w.dtype, scale)
-        tol = score_tolerance(q_np[i], kmin, kmax, w.dtype, scale)
+        if per_query_head:
+            s_ref = O.quest_scores_per_query_head(q_np[i], kmin, kmax, w.dtype, scale)
+            tol = _qhead_tolerance(q_np[i], kmin, kmax, w.dtype, scale)
+        else:
+            s_ref = O.quest_scores(q_np[i], kmin, kmax, w.dtype, scale)
+            tol = score_tolerance(q_np[i], kmin, kmax, w.dtype, scale)
         assert np.all(np.abs(sc_np[i, :, :P] - s_ref) <= tol), f"{step_tag} seq {i}: scores"
         use = []
-        for h in range(w.H_kv):
+        for h in range(R):
             ok, near, got, ref = compare_selection(sel_np[i, h], s_ref[h], b_seq[i], S, W)
             assert ok, f"{step_tag} seq {i} head {h}: selected {got} vs oracle {ref}"
             assert len(got) == min(b_seq[i], P)
             use.append(got)
-        ref_out = O.attend_pages(q_np[i], w_keys(w, i, n), w_vals(w, i, n), n, w.page_size, use, w.dtype, scale)
+        attend = O.attend_pages_per_query_head if per_query_head else O.attend_pages
+        ref_out = attend(q_np[i], w_keys(w, i, n), w_vals(w, i, n), n, w.page_size, use, w.dtype, scale)
         check_output(out_np[i], ref_out, w.dtype)
+
+
+@pytest.mark.parametrize("case", [
+    dict(S=1, W=1, mode="per_seq", value=None, budgets=[40, 20, 12, 3, 12]),
+    dict(S=0, W=1, mode="pages", value=16, budgets=[2] * 5, dtype="f32", D=64, H_q=4, H_kv=1),
+    dict(S=2, W=2, mode="fraction", value=0.05, budgets=[2] * 5, H_q=16, H_kv=8),
+    dict(S=1, W=3, mode="pages", value=9, budgets=[2] * 5, D=64, H_q=32, H_kv=8),
+])
+def test_per_query_head_selection(case):
+    """Pages ranked and kept per query head (the EntmaxKV top-k form; S = 0 with W = 1 is its
+    tail-only always-kept set); each query head attends its own pages of its KV head."""
+    extra = {k: case[k] for k in ("dtype", "D", "H_q", "H_kv") if k in case}
+    w = _custom([16 * 300 + 5, 16 * 77, 16 * 40 + 9, 33, 16 * 12], case["budgets"], **extra)
+    cache = upload(w)
+    _run_select_params(w, cache, case["S"], case["W"], case["mode"], case["value"], "per q head " + str(case),
+                       per_query_head=True)
 
 
 @pytest.mark.parametrize("case", [
