@@ -60,20 +60,21 @@ TRAFFIC = {
     # python bench.py --steps 5 --warmup 3 --no-cpu-baseline, then
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
-    ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel+page_select_kernel"):
-        {"bytes": 577_377_280 + 4_712_192 + 4_620_032 + 0, "digest": "216194fe6d198738"},
+    ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel"):
+        {"bytes": 577_380_096 + 4_456_448, "digest": "753019946b9d2b6d"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 466_771_968 + 1_059_328, "digest": "98da506b5604161d"},
+        {"bytes": 466_839_808 + 1_123_072, "digest": "05a88d2b4ae2d1df"},
     # python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline, then
-    # ncu ... -k regex:"mla_|page_select" -s 4 -c 4 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
-    ("mla-b16-128k-5pct", "mla_qsplit_kernel+mla_score_kernel+page_select_kernel"):
-        {"bytes": 2_363_136 + 0 + 80_296_192 + 27_648 + 197_632 + 0, "digest": "4949e54626c4b333"},
+    # ncu ... -k regex:"mla_" -s 0 -c 3 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
+    ("mla-b16-128k-5pct", "mla_qsplit_kernel+mla_score_kernel"):
+        {"bytes": 2_363_136 + 0 + 80_308_480 + 49_920, "digest": "95508ed7a135ebfd"},
+    ("mla-b16-128k-5pct", "mla_decode_kernel"):
+        {"bytes": 124_111_616 + 125_440, "digest": "95508ed7a135ebfd"},
 }
 KERNEL_SOURCES = {
-    "page_score_kernel+page_select_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
+    "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
     "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),
-    "mla_qsplit_kernel+mla_score_kernel+page_select_kernel": ("mla.cu", "score_select.cu", "psk_common.cuh",
-                                                              "psk_internal.h"),
+    "mla_qsplit_kernel+mla_score_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
     "mla_decode_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
 }
 
@@ -279,6 +280,15 @@ def run_psk(args):
         psk.page_score_select(L, q, cache.summaries, cache.block_table, cache.seq_lens, bud, w.b_max, cache.scale,
                               sel, ws)
 
+    # the same two stages as separate calls, so each kernel gets its own events in the eager loop
+    sel_prm = psk.select_params(budgets=bud)
+
+    def score_only():
+        psk.page_score(L, q, cache.summaries, cache.block_table, cache.seq_lens, sel_prm, w.b_max, cache.scale, ws)
+
+    def select_only():
+        psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
+
     def decode():
         psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
                                 w.b_max, cache.scale, out, ws)
@@ -368,7 +378,7 @@ def run_psk(args):
 
     K = args.steps
     Kd = max(3, K // 4)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     evd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
     evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     evgd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
@@ -383,10 +393,12 @@ def run_psk(args):
         e[0].record(stream)
         append()
         e[1].record(stream)
-        score()
+        score_only()
         e[2].record(stream)
-        decode()
+        select_only()
         e[3].record(stream)
+        decode()
+        e[4].record(stream)
     marks[1].record(stream)
     for k in range(Kd):
         flush_l2()
@@ -428,7 +440,8 @@ def run_psk(args):
             graph_sparse_ms = graph_dense_ms = float("nan")
     t_app = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
     t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
-    t_dec = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
+    t_select = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
+    t_dec = statistics.mean(ev[k][3].elapsed_time(ev[k][4]) for k in range(K))
     if dist is not None:
         sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = max_over_ranks(
             [sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], dev)
@@ -510,9 +523,9 @@ def run_psk(args):
     pk = peaks()
     peak_hbm = pk["hbm"]
     flops_decode = 2 * Hq * (D + w.D_v) * sel_tokens  # QK^T and P.V over the selected tokens
-    if t_score >= t_dec:
-        dom = ("mla_qsplit_kernel+mla_score_kernel+page_select_kernel" if w.latent
-               else "page_score_kernel+page_select_kernel")
+    # the dominant kernel by time (score, select or decode), each timed by its own events
+    if t_score >= t_dec and t_score >= t_select:
+        dom = "mla_qsplit_kernel+mla_score_kernel" if w.latent else "page_score_kernel"
         roof = {"bound": "hbm", "kernel": dom, "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
                 "unit": "GB/s", "algorithmic_per_launch": score_bytes, "algorithmic_unit": "B",
                 "launch_us": t_score * 1e3}
@@ -569,7 +582,8 @@ def run_psk(args):
         "speedup_vs_dense": step_dense_ms / step_ms,
         "eager": {"us_per_step": sparse_ms * 1e3, "dense_us_per_step": dense_ms * 1e3,
                   "speedup_vs_dense": dense_ms / sparse_ms},
-        "kernels_us": {"append": t_app * 1e3, "score_select": t_score * 1e3, "sparse_decode": t_dec * 1e3},
+        "kernels_us": {"append": t_app * 1e3, "score": t_score * 1e3, "select": t_select * 1e3,
+                       "score_select": (t_score + t_select) * 1e3, "sparse_decode": t_dec * 1e3},
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "timing": ("CUDA-graph replay" if e2e_ms != e2e_eager_ms else "eager launches")
                           + " of pinned-host H2D copies + the step + D2H of the output",

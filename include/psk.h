@@ -219,6 +219,23 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
                              size_t workspace_bytes, psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * The two stages of psk_page_score_select_ex as separate calls, for callers that run other
+ * work between them or time them apart. psk_page_score writes one selection key per
+ * (unit, page) into the workspace (and scores_out when given); psk_page_select turns those
+ * keys into the selected rows. The pair must be made in that order on one stream with the
+ * same workspace, layout, params and b_max, and no other call on that workspace in between
+ * (the keys live in its per-call scratch). Their results equal psk_page_score_select_ex's.
+ * psk_page_select reads seq_lens, the budget and the always-kept sizes from params, and the keys.
+ * --------------------------------------------------------------------------------------- */
+int psk_page_score(const psk_layout *layout, const void *q, const void *summaries,
+                   const int32_t *block_table, const int32_t *seq_lens,
+                   const psk_select_params *params, int32_t b_max, float scale, float *scores_out,
+                   void *workspace, size_t workspace_bytes, psk_stream_t stream);
+int psk_page_select(const psk_layout *layout, const int32_t *seq_lens,
+                    const psk_select_params *params, int32_t b_max, int32_t *selected,
+                    void *workspace, size_t workspace_bytes, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Stage 4: exact softmax attention over the selected pages.
  *
  *   out[i,g,:] = sum_t softmax_t(scale * q[i,g] . k_t) v_t

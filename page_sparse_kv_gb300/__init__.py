@@ -21,7 +21,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "
 DEV_BAD_BLOCK, DEV_BAD_SEQLEN, DEV_BAD_SELECTED, DEV_BAD_BUDGET, DEV_BAD_APPEND, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 
 EXPORTS = [
-    "psk_kv_append_and_summarize", "psk_page_score_select", "psk_page_score_select_ex", "psk_sparse_paged_decode",
+    "psk_kv_append_and_summarize", "psk_page_score_select", "psk_page_score_select_ex", "psk_page_score",
+    "psk_page_select", "psk_sparse_paged_decode",
     "psk_sparse_paged_decode_ex", "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version",
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
             "psk_page_score_select_ex": (ctypes.c_int, [LP, P, P, P, P, ctypes.POINTER(PskSelectParams), I, F, P, P,
                                                         P, Z, P]),
             "psk_sparse_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P, Z, P]),
+            "psk_page_score": (ctypes.c_int, [LP, P, P, P, P, ctypes.POINTER(PskSelectParams), I, F, P, P, Z, P]),
+            "psk_page_select": (ctypes.c_int, [LP, P, ctypes.POINTER(PskSelectParams), I, P, P, Z, P]),
             "psk_sparse_paged_decode_ex": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, ctypes.c_uint32, P, P, Z, P]),
             "psk_dense_paged_decode": (ctypes.c_int, [LP, P, P, P, P, P, F, P, P, Z, P]),
             "psk_sparse_paged_decode_noalloc": (ctypes.c_int, [LP, P, P, P, P, P, P, I, F, P, P]),
@@ -186,15 +189,9 @@ def page_score_select(layout: Layout, q, summaries, block_table, seq_lens, budge
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_max: int, scale: float, selected,
-                         workspace, *, budgets=None, budget_pages: int | None = None,
-                         budget_fraction: float | None = None, sink_pages: int = 1, window_pages: int = 1,
-                         per_query_head: bool = False, scores_out=None, stream=None):
-    """Score + select with the first ``sink_pages`` and last ``window_pages`` pages always kept
-    and exactly one budget mode: ``budgets`` (device int32 per sequence), ``budget_pages`` (a
-    fixed page count) or ``budget_fraction`` (a fraction of each sequence's pages). With
-    ``per_query_head`` the rows are per (sequence, query head): ``selected`` is
-    [batch, num_q_heads, b_max]."""
+def select_params(*, budgets=None, budget_pages: int | None = None, budget_fraction: float | None = None,
+                  sink_pages: int = 1, window_pages: int = 1, per_query_head: bool = False) -> PskSelectParams:
+    """A ``psk_select_params`` with exactly one budget mode (see ``page_score_select_ex``)."""
     modes = [budgets is not None, budget_pages is not None, budget_fraction is not None]
     if sum(modes) != 1:
         raise ValueError("give exactly one of budgets, budget_pages, budget_fraction")
@@ -205,6 +202,36 @@ def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_
     prm.mode = BUDGET_PER_SEQUENCE if modes[0] else (BUDGET_PAGES if modes[1] else BUDGET_FRACTION)
     prm.sink_pages, prm.window_pages = int(sink_pages), int(window_pages)
     prm.per_query_head = 1 if per_query_head else 0
+    return prm
+
+
+def page_score(layout: Layout, q, summaries, block_table, seq_lens, params: PskSelectParams, b_max: int,
+               scale: float, workspace, scores_out=None, stream=None):
+    """Stage 2 alone: selection keys into ``workspace`` (and scores into ``scores_out``)."""
+    _check("psk_page_score", lib().psk_page_score(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), ctypes.byref(params),
+        int(b_max), float(scale), _ptr(scores_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def page_select(layout: Layout, seq_lens, params: PskSelectParams, b_max: int, selected, workspace, stream=None):
+    """Stage 3 alone: the selected rows from the keys ``page_score`` left in ``workspace``."""
+    _check("psk_page_select", lib().psk_page_select(
+        ctypes.byref(layout.c()), _ptr(seq_lens), ctypes.byref(params), int(b_max), _ptr(selected), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_max: int, scale: float, selected,
+                         workspace, *, budgets=None, budget_pages: int | None = None,
+                         budget_fraction: float | None = None, sink_pages: int = 1, window_pages: int = 1,
+                         per_query_head: bool = False, scores_out=None, stream=None):
+    """Score + select with the first ``sink_pages`` and last ``window_pages`` pages always kept
+    and exactly one budget mode: ``budgets`` (device int32 per sequence), ``budget_pages`` (a
+    fixed page count) or ``budget_fraction`` (a fraction of each sequence's pages). With
+    ``per_query_head`` the rows are per (sequence, query head): ``selected`` is
+    [batch, num_q_heads, b_max]."""
+    prm = select_params(budgets=budgets, budget_pages=budget_pages, budget_fraction=budget_fraction,
+                        sink_pages=sink_pages, window_pages=window_pages, per_query_head=per_query_head)
     _check("psk_page_score_select_ex", lib().psk_page_score_select_ex(
         ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), ctypes.byref(prm),
         int(b_max), float(scale), _ptr(selected), _ptr(scores_out), _ptr(workspace),

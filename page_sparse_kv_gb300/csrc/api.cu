@@ -201,15 +201,19 @@ static long long scalar_mode_budget(const psk_select_params &sp, long long P) {
   return std::max(forced, b);
 }
 
-int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void *summaries,
-                             const int32_t *block_table, const int32_t *seq_lens, const psk_select_params *params,
-                             int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
-                             size_t workspace_bytes, psk_stream_t stream) {
+// Score and / or select (stages: kStageScore, kStageSelect). A select-only call reads the keys
+// a score-only call left in the same workspace.
+static int score_select_common(const psk_layout *layout, const void *q, const void *summaries,
+                               const int32_t *block_table, const int32_t *seq_lens, const psk_select_params *params,
+                               int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
+                               size_t workspace_bytes, psk_stream_t stream, int stages) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
-  if (!q || !summaries || !block_table || !seq_lens || !params || !selected || b_max < 1)
-    return PSK_ERR_INVALID_ARG;
+  const bool do_score = (stages & kStageScore) != 0, do_select = (stages & kStageSelect) != 0;
+  if (!seq_lens || !params || b_max < 1) return PSK_ERR_INVALID_ARG;
+  if (do_score && (!q || !summaries || !block_table)) return PSK_ERR_INVALID_ARG;
+  if (do_select && !selected) return PSK_ERR_INVALID_ARG;
   const psk_select_params &sp = *params;
   if (sp.sink_pages < 0 || sp.window_pages < 1) return PSK_ERR_INVALID_ARG;
   if (sp.per_query_head != 0 && sp.per_query_head != 1) return PSK_ERR_INVALID_ARG;
@@ -223,7 +227,7 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
   } else {
     return PSK_ERR_INVALID_ARG;
   }
-  if (!aligned16(q) || !aligned16(summaries)) return PSK_ERR_INVALID_ARG;
+  if (do_score && (!aligned16(q) || !aligned16(summaries))) return PSK_ERR_INVALID_ARG;
   rc = check_gqa_compute(layout);
   if (rc != PSK_OK) return rc;
   // the units' layout: the cache's own, or its per-query-head view
@@ -272,8 +276,29 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
   a.budget_frac = sp.budget_fraction;
   if (L.latent)
     return cuda_status(launch_mla_score_select(a, reinterpret_cast<uint16_t *>(ws + plan.off_qsplit),
-                                               static_cast<cudaStream_t>(stream)));
-  return cuda_status(launch_score_select(a, L.dtype, static_cast<cudaStream_t>(stream)));
+                                               static_cast<cudaStream_t>(stream), stages));
+  return cuda_status(launch_score_select(a, L.dtype, static_cast<cudaStream_t>(stream), stages));
+}
+
+int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void *summaries,
+                             const int32_t *block_table, const int32_t *seq_lens, const psk_select_params *params,
+                             int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
+                             size_t workspace_bytes, psk_stream_t stream) {
+  return score_select_common(layout, q, summaries, block_table, seq_lens, params, b_max, scale, selected, scores_out,
+                             workspace, workspace_bytes, stream, kStageScore | kStageSelect);
+}
+
+int psk_page_score(const psk_layout *layout, const void *q, const void *summaries, const int32_t *block_table,
+                   const int32_t *seq_lens, const psk_select_params *params, int32_t b_max, float scale,
+                   float *scores_out, void *workspace, size_t workspace_bytes, psk_stream_t stream) {
+  return score_select_common(layout, q, summaries, block_table, seq_lens, params, b_max, scale, nullptr, scores_out,
+                             workspace, workspace_bytes, stream, kStageScore);
+}
+
+int psk_page_select(const psk_layout *layout, const int32_t *seq_lens, const psk_select_params *params,
+                    int32_t b_max, int32_t *selected, void *workspace, size_t workspace_bytes, psk_stream_t stream) {
+  return score_select_common(layout, nullptr, nullptr, nullptr, seq_lens, params, b_max, 0.f, selected, nullptr,
+                             workspace, workspace_bytes, stream, kStageSelect);
 }
 
 static int decode_common(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,

@@ -656,7 +656,8 @@ bool mla_supported(const psk_layout &L) {
 
 size_t mla_qsplit_bytes(const psk_layout &L) { return (size_t)L.batch * kHeads * 2 * kD * 2; }
 
-cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s) {
+cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s, int stages) {
+  if (!(stages & kStageScore)) return launch_page_select(a, s, true);
   const int rows = a.B * kHeads;
   const int n = rows * (kD / 8);
   cudaError_t e = launch_kernel(true, mla_qsplit_kernel, (n + 255) / 256, 256, 0, s,
@@ -666,7 +667,7 @@ cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaSt
   if (e != cudaSuccess) return e;
   dim3 grid((a.max_pages + 127) / 128, a.B);
   e = launch_kernel(false, mla_score_kernel, grid, 128, kScSmem, s, a, (const uint16_t *)qsplit);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !(stages & kStageSelect)) return e;
   return launch_page_select(a, s);
 }
 

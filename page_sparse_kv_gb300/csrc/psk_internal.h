@@ -70,8 +70,11 @@ struct ScorePlan {
 // kv_shift > 0: L is the per-query-head view (num_kv_heads = num_q_heads), whose unit heads share
 // cache heads 2^kv_shift at a time.
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift = 0);
-cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s);
-cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s);
+// Stages of a score / select launch: the page-score kernels (keys into the workspace, scores_out)
+// and the selection kernel (keys -> selected rows).
+constexpr int kStageScore = 1, kStageSelect = 2;
+cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s, bool first_of_call = false);
+cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s, int stages = kStageScore | kStageSelect);
 bool score_supported(int dtype, int D, int G);
 
 struct DecodeArgs {
@@ -123,7 +126,8 @@ bool decode_supported(int dtype, int D, int D_v, int G, int ps);
 // latent (MLA) form on the tensor cores
 bool mla_supported(const psk_layout &L);
 size_t mla_qsplit_bytes(const psk_layout &L);
-cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s);
+cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaStream_t s,
+                                    int stages = kStageScore | kStageSelect);
 bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan);
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
 

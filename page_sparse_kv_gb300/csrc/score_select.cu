@@ -680,7 +680,8 @@ __global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
+cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
+  if (!(stages & kStageScore)) return launch_page_select(a, s, true);
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
   const int k1_smem = kStages * kStageBytes;
   auto kfn = page_score_kernel<T, D, G, false>;
@@ -716,13 +717,13 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s) {
   const long long n_ctas = (long long)(b.body_chunks + b.tail_chunks) * b.B * (b.H_kv / hpc);
   if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
   e = launch_kernel(true, kfn, (unsigned)n_ctas, kThreads, k1_smem, s, b);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !(stages & kStageSelect)) return e;
   return launch_page_select(b, s);
 }
 
 }  // namespace
 
-cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
+cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s, bool first_of_call) {
   // keys of one chunk; the merge buffer only when a unit spans several chunks (the smaller
   // footprint keeps every CTA of a one-chunk call resident at once)
   const size_t keys_bytes = (size_t)std::min(a.chunk, a.max_pages) * 4;
@@ -730,7 +731,7 @@ cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 g2(a.H_kv, a.n_chunks_max, a.B);
-  return launch_kernel(false, page_select_kernel, g2, kThreads, smem, s, a);
+  return launch_kernel(first_of_call, page_select_kernel, g2, kThreads, smem, s, a);
 }
 
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
@@ -804,10 +805,10 @@ bool score_supported(int dtype, int D, int G) {
   return false;
 }
 
-cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s) {
+cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s, int stages) {
   const int D = a.D, G = a.H_q / a.H_kv;
 #define X(TT, DT, DD, GG) \
-  if (dtype == DT && D == DD && G == GG) return launch_t<TT, DD, GG>(a, s);
+  if (dtype == DT && D == DD && G == GG) return launch_t<TT, DD, GG>(a, s, stages);
   PSK_SCORE_CASES(X)
 #undef X
   return cudaErrorInvalidValue;

@@ -329,6 +329,32 @@ def test_mla_sink_window_and_budget_modes(case):
     _run_select_params(w, cache, case["S"], case["W"], case["mode"], case["value"], "mla " + str(case))
 
 
+@pytest.mark.parametrize("latent", [False, True])
+def test_split_score_then_select_equals_combined(latent):
+    """psk_page_score followed by psk_page_select on the same workspace gives the combined call's
+    scores and selected rows bit for bit."""
+    if latent:
+        w = _custom_mla([64 * 200 + 5, 64 * 31, 64 * 3 + 1], [20, 7, 3])
+    else:
+        w = _custom([16 * 700 + 3, 16 * 77, 5000, 17], [90, 9, 30, 2])
+    cache = upload(w)
+    L = cache.layout
+    q = dev_queries(w)
+    bud = dev_budgets(w)
+    sc1 = torch.full((w.B, w.H_kv, w.max_pages), float("nan"), device="cuda")
+    sel1 = cache.score_select(q, bud, scores_out=sc1)
+    prm = psk.select_params(budgets=bud)
+    sc2 = torch.full_like(sc1, float("nan"))
+    sel2 = torch.full_like(sel1, -7)
+    psk.page_score(L, q, cache.summaries, cache.block_table, cache.seq_lens, prm, cache.b_max, cache.scale, cache.ws,
+                   scores_out=sc2)
+    psk.page_select(L, cache.seq_lens, prm, cache.b_max, sel2, cache.ws)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    assert torch.equal(sel1, sel2)
+    assert torch.equal(torch.nan_to_num(sc1, nan=-1e30), torch.nan_to_num(sc2, nan=-1e30))
+
+
 def test_ties_resolve_to_lower_page():
     """Pages with identical keys (hence identical summaries and scores) tie; with the cutoff
     inside the tied group the lowest-indexed tied pages win."""
