@@ -73,6 +73,7 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift = 
 // Stages of a score / select launch: the page-score kernels (keys into the workspace, scores_out)
 // and the selection kernel (keys -> selected rows).
 constexpr int kStageScore = 1, kStageSelect = 2;
+constexpr int kMergeCap = 8192;  // candidates the selection's merge CTA holds (shared memory)
 cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s, bool first_of_call = false);
 cudaError_t launch_score_select(const ScoreArgs &a, int dtype, cudaStream_t s, int stages = kStageScore | kStageSelect);
 bool score_supported(int dtype, int D, int G);

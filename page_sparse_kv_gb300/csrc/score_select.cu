@@ -1,4 +1,4 @@
-// Stages 2 + 3: Quest-style page scores and top-b page selection (GQA caches).
+// Stage 2: Quest-style page scores (GQA caches); stage 3, the selection, is in select.cu.
 //
 // Score (EntmaxKV README, "Two selection strategies", Top-k; kernels/page_criticality.py):
 //   score[i,h,p] = scale * max_{g in group(h)} sum_d max(q_gd * kmin_pd, q_gd * kmax_pd)
@@ -7,28 +7,14 @@
 // so every kept product is the same fp32 product; accumulation is fp32 (bf16 caches: mixed
 // fma.f32.bf16 on the raw bf16 pairs; fp32 caches: packed fp32x2 FMAs).
 //
-// Selection (LOCKS PKG-INFO, "How it works", Selection: a static top-b per (layer, KV head);
-// sink and recent page always kept and counted inside b; EntmaxKV "Top-k": the budget
-// includes the always-attended tail page; ties to the lower logical page index).
-//
-// Two kernels per call:
-//   page_score_kernel (K1) streams the summaries: one CTA per (chunk of pages, sequence,
-//   group of up to 8 KV heads); warp w scores KV head w % 8 of the group, so a page's
-//   summaries for all heads (one 4 KB run at D = 128 bf16) are read together. A (page, head)
-//   summary row is read by LPP = D * sizeof(T) / 16 lanes with one 16-byte load each, four
-//   page steps in flight per lane. Partial sums are reduced across the LPP lanes by a
-//   transposing butterfly (each step halves the values a lane carries), then the group max is
-//   taken across the lanes that ended up holding different query heads. K1 writes one 32-bit
-//   order key per page (0 = forced sink / tail, or a flagged bad block) to the workspace.
-//   page_select_kernel (K2) selects: one CTA per (KV head, chunk of up to 16384 pages,
-//   sequence) loads the chunk's keys (L2-resident after K1) into shared memory and finds the
-//   top k = b - 2 with an MSB-first 8-bit radix select (per-warp histograms);
-//   ties go to the lower index through block-wide scans in index order. A unit that fits one
-//   chunk is finished by that CTA; otherwise each chunk writes its winners (ascending) and the
-//   last CTA of the (sequence, KV head) to finish (an atomic ticket, no waiting) merges them
-//   with a second radix select. Top-k of the union of chunk top-k's is the global top-k
-//   because keys are unique once ties are ordered by page index.
-// The output row is: sink, winners (ascending), tail, then -1 padding.
+// page_score_kernel streams the summaries: one CTA per (chunk of pages, sequence, group of up
+// to 8 KV heads); warp w scores KV head w % 8 of the group, so a page's summaries for all heads
+// (one 4 KB run at D = 128 bf16) are read together. A (page, head) summary row is read by
+// LPP = D * sizeof(T) / 16 lanes with one 16-byte load each. Partial sums are reduced across
+// the LPP lanes by a transposing butterfly (each step halves the values a lane carries), then
+// the group max is taken across the lanes that ended up holding different query heads. The
+// kernel writes one 32-bit order key per page to the workspace (0 = an always-kept page, or a
+// flagged bad block), which the selection kernel reads.
 #include <algorithm>
 #include <cstdlib>
 
@@ -38,161 +24,8 @@
 namespace psk {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // score kernel: eight warps, one KV head of the group each
 constexpr int kWarps = kThreads / 32;
-static_assert(kThreads == 256, "the radix pass maps one thread to each 8-bit digit");
-constexpr int kMergeCap = 8192;  // candidates the merge CTA can hold
-
-// ------------------------------------------------------------------------------------
-// block-wide helpers (blockDim.x == kThreads)
-// ------------------------------------------------------------------------------------
-// Exclusive prefix of one int per thread in thread order with two barriers: the counts go to
-// shared memory, warp 0 scans them (8 per lane), everyone reads its base. cnt: kThreads + 1 ints.
-__device__ __forceinline__ int block_scan_w0(int x, int *cnt, int *total) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  cnt[tid] = x;
-  __syncthreads();
-  if (tid < 32) {
-    int v[kThreads / 32], sum = 0;
-#pragma unroll
-    for (int j = 0; j < kThreads / 32; ++j) {
-      v[j] = cnt[lane * (kThreads / 32) + j];
-      sum += v[j];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int run = incl - sum;
-#pragma unroll
-    for (int j = 0; j < kThreads / 32; ++j) {
-      cnt[lane * (kThreads / 32) + j] = run;
-      run += v[j];
-    }
-    if (lane == 31) cnt[kThreads] = incl;
-  }
-  __syncthreads();
-  const int r = cnt[tid];
-  if (total) *total = cnt[kThreads];
-  return r;
-}
-
-// Radix select over keys[0..n) (key 0 = not a candidate): finds the k-th largest key T and
-// how many keys equal to T belong to the top k (the lowest-indexed ones). Requires
-// 1 <= k <= number of nonzero keys, and kmin / kmax = the smallest / largest nonzero key.
-// The digits start at the highest bit in which kmin and kmax differ (the bits above are common
-// to every candidate), 8 bits per pass. Each warp counts into its own 256-bin histogram with
-// shared-memory atomics; then thread t owns digit 255 - t: it sums (and clears) that bin over
-// the warps, and a block-wide scan in descending digit order finds the digit holding the k-th
-// key. Three barriers per pass. hist: kWarps x 256 bins, zero on entry and on return;
-// sh: >= 2 + kWarps ints.
-__device__ void radix_select(const uint32_t *keys, int n, int k, uint32_t kmin, uint32_t kmax, int *hist, int *sh,
-                             uint32_t *T_out, int *need_eq_out) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t diff = kmin ^ kmax;
-  const int top = diff ? 31 - __clz(diff) : 0;  // highest differing bit
-  int shift = top >= 7 ? top - 7 : 0;
-  uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
-  uint32_t mask = shift + 8 >= 32 ? 0u : (0xFFFFFFFFu << (shift + 8));
-  int need = k;
-  int *wsum = sh + 2;
-  int *myhist = hist + warp * 256;
-#pragma unroll 1
-  for (;;) {
-    for (int x = tid; x < n; x += kThreads) {
-      const uint32_t key = keys[x];
-      if (key != 0u && (key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1);
-    }
-    __syncthreads();
-    const int bin = 255 - tid;  // descending digits in thread order
-    int v = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      v += hist[w * 256 + bin];
-      hist[w * 256 + bin] = 0;
-    }
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    for (int w = 0; w < warp; ++w) incl += wsum[w];
-    const int excl = incl - v;
-    if (excl < need && incl >= need) {
-      sh[0] = bin;
-      sh[1] = excl;
-      sh[2 + kWarps] = v;  // keys in the chosen bin
-    }
-    __syncthreads();
-    const int d = sh[0];
-    need -= sh[1];
-    prefix |= static_cast<uint32_t>(d) << shift;
-    mask |= 255u << shift;
-    if (shift == 0) break;
-    if (sh[2 + kWarps] == need) {
-      // every key of the chosen bin is taken, and so is every key above it: the selection is
-      // "key >= prefix" (prefix has zeros below this digit), with no tie left to break
-      prefix = prefix == 0u ? 0u : prefix - 1u;
-      need = 0;
-      break;
-    }
-    shift = shift >= 8 ? shift - 8 : 0;
-    // a digit that overlaps bits already fixed is harmless: they match the prefix
-    __syncthreads();  // sh and wsum are rewritten by the next pass
-  }
-  __syncthreads();  // every thread has read sh before the caller reuses it
-  *T_out = prefix;
-  *need_eq_out = need;
-}
-
-// Writes, in index order, every item taken by the rule
-//   take_all:  key != 0
-//   otherwise: key > T, or key == T among the first need_eq such items
-// to out_key / out_page (page = pages ? pages[x] : page_base + x). Returns the count.
-// One block scan of the packed per-thread counts (equal << 16 | greater; both <= 16384) gives
-// every thread its output position: greater-before + min(equal-before, need_eq).
-// cnt: kThreads + 1 ints of scratch.
-__device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int page_base, int n, bool take_all,
-                             uint32_t T, int need_eq, uint32_t *out_key, int32_t *out_page, int *cnt) {
-  const int tid = threadIdx.x;
-  const int per = (n + kThreads - 1) / kThreads;
-  const int x0 = min(n, tid * per), x1 = min(n, x0 + per);
-  int gt = 0, eq = 0;
-  for (int x = x0; x < x1; ++x) {
-    const uint32_t key = keys[x];
-    if (take_all) {
-      gt += key != 0u;
-    } else {
-      gt += key > T;
-      eq += key == T;
-    }
-  }
-  int total;
-  const int pre = block_scan_w0((eq << 16) | gt, cnt, &total);
-  int seen = pre >> 16;
-  int w = (pre & 0xFFFF) + (take_all ? 0 : min(seen, need_eq));
-  for (int x = x0; x < x1; ++x) {
-    const uint32_t key = keys[x];
-    bool take;
-    if (take_all) {
-      take = key != 0u;
-    } else {
-      take = key > T;
-      if (key == T) take = (seen++ < need_eq);
-    }
-    if (take) {
-      if (out_key) out_key[w] = key;
-      out_page[w] = pages ? pages[x] : page_base + x;
-      ++w;
-    }
-  }
-  return (total & 0xFFFF) + (take_all ? 0 : min(total >> 16, need_eq));
-}
 
 // ------------------------------------------------------------------------------------
 // reductions across the LPP lanes of one page
@@ -464,221 +297,6 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   pdl_trigger();
 }
 
-// ------------------------------------------------------------------------------------
-// K2: top-b selection
-// ------------------------------------------------------------------------------------
-// One CTA per (KV head, chunk of a.chunk pages, sequence). The chunk's keys come from the
-// workspace (L2-resident right after K1). A unit that fits one chunk is finished by its only
-// CTA; otherwise every chunk writes its local winners and the last CTA to finish merges.
-// Row of a unit with count < P selected pages: the first S pages, the `wrote` winners (written
-// by the caller at sel_row + S, all inside [S, P - W)), the last W pages, then -1 to b_max.
-// count < P implies S + W < P, so the two always-kept runs do not overlap.
-__device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, int b_max, int S, int W) {
-  const int tid = threadIdx.x;
-  for (int x = tid; x < S; x += kThreads) sel_row[x] = x;
-  // fewer winners than free slots happens only after a flagged bad block: pad the gap
-  for (int x = S + wrote + tid; x < count - W; x += kThreads) sel_row[x] = -1;
-  for (int x = tid; x < W; x += kThreads) sel_row[count - W + x] = P - W + x;
-  for (int x = count + tid; x < b_max; x += kThreads) sel_row[x] = -1;
-}
-
-// Budget of a sequence of P pages (always >= the always-kept count in the scalar modes).
-__device__ int unit_budget(const ScoreArgs &a, int i, int P, int n_forced) {
-  if (a.budget_mode == PSK_BUDGET_FRACTION) {
-    const int r = (int)ceil((double)P * a.budget_frac);  // IEEE double product, then the ceiling
-    return max(n_forced, min(P, max(1, r)));
-  }
-  if (a.budget_mode == PSK_BUDGET_PAGES) return max(n_forced, min(P, a.budget_pages));
-  return a.budgets[i];
-}
-
-// Block-wide sum of c and min / max of lo / hi (two barriers; red: 3 * kWarps words).
-__device__ void block_stats(uint32_t c, uint32_t lo, uint32_t hi, uint32_t *red, int *count, uint32_t *kmin,
-                            uint32_t *kmax) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  if (lane == 0) {
-    red[warp] = c;
-    red[kWarps + warp] = lo;
-    red[2 * kWarps + warp] = hi;
-  }
-  __syncthreads();
-  c = 0;
-  lo = 0xFFFFFFFFu;
-  hi = 0u;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    c += red[w];
-    lo = min(lo, red[kWarps + w]);
-    hi = max(hi, red[2 * kWarps + w]);
-  }
-  *count = (int)c;
-  *kmin = lo;
-  *kmax = hi;
-  __syncthreads();  // red is reused by the caller's next call
-}
-
-// Count, min and max of the nonzero keys of keys[0..n) over the block (two barriers).
-__device__ void nonzero_stats(const uint32_t *keys, int n, int *count, uint32_t *kmin, uint32_t *kmax,
-                              uint32_t *red /* 3 * kWarps */) {
-  uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
-  for (int x = threadIdx.x; x < n; x += kThreads) {
-    const uint32_t k = keys[x];
-    if (k != 0u) {
-      ++c;
-      lo = min(lo, k);
-      hi = max(hi, k);
-    }
-  }
-  block_stats(c, lo, hi, red, count, kmin, kmax);
-}
-
-__global__ void __launch_bounds__(kThreads) page_select_kernel(ScoreArgs a) {
-  pdl_wait();  // dependents are released when this grid completes
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ int hist[kWarps * 256];  // zero between radix selects
-  __shared__ int cnt[kThreads + 1];
-  __shared__ uint32_t red[3 * kWarps];
-  __shared__ int flag_last;
-
-  const int h = blockIdx.x, c = blockIdx.y, i = blockIdx.z;
-  const int unit = i * a.H_kv + h;
-  const int tid = threadIdx.x;
-  const int seq_len = a.seq_lens[i];
-  const int P = (seq_len + a.ps - 1) / a.ps;
-  int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
-
-  if (seq_len < 1 || P > a.max_pages) {
-    if (c == 0) {
-      if (tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
-      for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
-    }
-    return;
-  }
-  const int n_forced = min(P, a.sink + a.window);
-  const int budget = unit_budget(a, i, P, n_forced);
-  if (budget < n_forced || budget > a.b_max) {
-    if (c == 0) {
-      if (tid == 0) set_status(a.ws, PSK_DEV_BAD_BUDGET);
-      for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = -1;
-    }
-    return;
-  }
-  const int count = min(budget, P);
-  if (count >= P) {  // every page is kept
-    if (c == 0)
-      for (int x = tid; x < a.b_max; x += kThreads) sel_row[x] = x < P ? x : -1;
-    return;
-  }
-  const int nch = (P + a.chunk - 1) / a.chunk;
-  if (c >= nch) return;
-  const int k_free = count - n_forced;  // count < P implies n_forced = sink + window < P
-
-  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);
-  const int p0 = c * a.chunk;
-  const int p1 = min(P, p0 + a.chunk);
-  const int n = p1 - p0;
-  const uint32_t *krow = a.keys + (size_t)unit * a.key_stride + p0;  // 16-byte aligned (stride, p0: x4)
-  int total_valid;
-  uint32_t kmin, kmax;
-  {  // keys to shared memory, four per load, with the count, min and max of the nonzero ones
-    uint32_t c = 0, lo = 0xFFFFFFFFu, hi = 0u;
-    auto take = [&](uint32_t k) {
-      if (k != 0u) {
-        ++c;
-        lo = min(lo, k);
-        hi = max(hi, k);
-      }
-    };
-    const int n4 = n >> 2;
-    for (int x = tid; x < n4; x += kThreads) {
-      const uint4 k4 = __ldcg(reinterpret_cast<const uint4 *>(krow) + x);
-      reinterpret_cast<uint4 *>(keys)[x] = k4;
-      take(k4.x);
-      take(k4.y);
-      take(k4.z);
-      take(k4.w);
-    }
-    for (int x = 4 * n4 + tid; x < n; x += kThreads) {
-      const uint32_t k = __ldcg(krow + x);
-      keys[x] = k;
-      take(k);
-    }
-    for (int x = tid; x < kWarps * 256; x += kThreads) hist[x] = 0;
-    block_stats(c, lo, hi, red, &total_valid, &kmin, &kmax);  // its barrier also publishes keys[]
-  }
-  int wrote = 0;
-  if (k_free > 0) {
-    uint32_t thr = 0;
-    int need_eq = 0;
-    const bool take_all = total_valid <= k_free;
-    if (!take_all) radix_select(keys, n, k_free, kmin, kmax, hist, cnt, &thr, &need_eq);
-    if (nch == 1) {
-      wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + a.sink, cnt);
-      write_row_ends(sel_row, P, count, wrote, a.b_max, a.sink, a.window);
-      return;
-    }
-    const int slot = unit * a.n_chunks_max + c;
-    uint32_t *ck = a.cand_key + (size_t)slot * a.k_cap;
-    int32_t *cp = a.cand_page + (size_t)slot * a.k_cap;
-    wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, ck, cp, cnt);
-    if (tid == 0) a.cand_count[slot] = wrote;
-  } else {
-    if (nch == 1) {
-      write_row_ends(sel_row, P, count, 0, a.b_max, a.sink, a.window);
-      return;
-    }
-    if (tid == 0) a.cand_count[unit * a.n_chunks_max + c] = 0;
-  }
-
-  // ---- last CTA of the unit merges -------------------------------------------------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(&a.counters[unit], 1u);
-    flag_last = (prev == (unsigned)(nch - 1));
-  }
-  __syncthreads();
-  if (!flag_last) return;
-  __threadfence();
-  if (tid == 0) a.counters[unit] = 0u;
-
-  uint32_t *mkey = reinterpret_cast<uint32_t *>(smem_raw);
-  int32_t *mpage = reinterpret_cast<int32_t *>(smem_raw + sizeof(uint32_t) * kMergeCap);
-  int n_c = 0;
-  for (int cc = 0; cc < nch; ++cc) {
-    const int sl = unit * a.n_chunks_max + cc;
-    const int cnt = __ldcg(a.cand_count + sl);
-    const uint32_t *ck = a.cand_key + (size_t)sl * a.k_cap;
-    const int32_t *cp = a.cand_page + (size_t)sl * a.k_cap;
-    for (int x = tid; x < cnt; x += kThreads) {
-      mkey[n_c + x] = __ldcg(ck + x);
-      mpage[n_c + x] = __ldcg(cp + x);
-    }
-    n_c += cnt;
-  }
-  __syncthreads();
-  wrote = 0;
-  if (k_free > 0) {
-    uint32_t thr = 0;
-    int need_eq = 0;
-    const bool take_all = n_c <= k_free;
-    if (!take_all) {
-      int nz;
-      uint32_t mlo, mhi;
-      nonzero_stats(mkey, n_c, &nz, &mlo, &mhi, red);
-      radix_select(mkey, n_c, k_free, mlo, mhi, hist, cnt, &thr, &need_eq);
-    }
-    wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + a.sink, cnt);
-  }
-  write_row_ends(sel_row, P, count, wrote, a.b_max, a.sink, a.window);
-}
-
 template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   if (!(stages & kStageScore)) return launch_page_select(a, s, true);
@@ -722,17 +340,6 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
 }
 
 }  // namespace
-
-cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s, bool first_of_call) {
-  // keys of one chunk; the merge buffer only when a unit spans several chunks (the smaller
-  // footprint keeps every CTA of a one-chunk call resident at once)
-  const size_t keys_bytes = (size_t)std::min(a.chunk, a.max_pages) * 4;
-  const size_t smem = a.n_chunks_max == 1 ? keys_bytes : std::max<size_t>(keys_bytes, (size_t)kMergeCap * 8);
-  cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 g2(a.H_kv, a.n_chunks_max, a.B);
-  return launch_kernel(first_of_call, page_select_kernel, g2, kThreads, smem, s, a);
-}
 
 bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
   if (L.num_kv_heads > kWarps && L.num_kv_heads % kWarps != 0) return false;
