@@ -61,18 +61,21 @@ TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
     ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel"):
-        {"bytes": 577_380_096 + 4_456_448, "digest": "753019946b9d2b6d"},
+        {"bytes": 577_377_024 + 4_418_816, "digest": "71afaa7efc0fe70e"},
+    ("batched-ragged-b64-8k..64k-5pct", "page_select_kernel"):
+        {"bytes": 4_623_104 + 0, "digest": "d62c370dc82f0afb"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 466_839_808 + 1_123_072, "digest": "05a88d2b4ae2d1df"},
+        {"bytes": 466_841_088 + 1_147_648, "digest": "e3dda5f1d761e9ec"},
     # python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline, then
     # ncu ... -k regex:"mla_" -s 0 -c 3 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
     ("mla-b16-128k-5pct", "mla_qsplit_kernel+mla_score_kernel"):
-        {"bytes": 2_363_136 + 0 + 80_308_480 + 49_920, "digest": "95508ed7a135ebfd"},
+        {"bytes": 2_363_392 + 0 + 80_301_312 + 57_600, "digest": "8389efad62f45629"},
     ("mla-b16-128k-5pct", "mla_decode_kernel"):
-        {"bytes": 124_111_616 + 125_440, "digest": "95508ed7a135ebfd"},
+        {"bytes": 124_114_944 + 124_672, "digest": "8389efad62f45629"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
+    "page_select_kernel": ("select.cu", "psk_common.cuh", "psk_internal.h"),
     "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),
     "mla_qsplit_kernel+mla_score_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
     "mla_decode_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
