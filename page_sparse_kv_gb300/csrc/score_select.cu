@@ -356,12 +356,13 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
   plan->chunk = chunk;
   plan->n_chunks_max = (L.max_pages + chunk - 1) / chunk;
   plan->k_cap = std::min(kfree_max, chunk);
-  // pages per streaming CTA: 64 (measured best on the batched workload: many waves, so the
-  // last one is a small part of the launch); fewer while the grid would not fill the GPU a few
-  // times over
+  // pages per streaming CTA of the body region: 64 (measured best on the batched workload, 48,
+  // 96 and 128 slower); fewer only while the body would not fill one resident wave (four CTAs on
+  // each of 152 SMs), since the tail region supplies the short CTAs at the end (one 1M-token
+  // sequence: 64 pages 62.9 us against 66.2 us at 32)
   const long long head_groups = L.num_kv_heads > kWarps ? L.num_kv_heads / kWarps : 1;
   int pchunk = 64;
-  while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152 * 2)
+  while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152)
     pchunk /= 2;
   if (const char *env = std::getenv("PSK_SCORE_PCHUNK")) {  // tuning override: pages per score CTA
     const int v = std::atoi(env);

@@ -354,17 +354,26 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
 
   uint32_t *mkey = reinterpret_cast<uint32_t *>(smem_raw);
   int32_t *mpage = reinterpret_cast<int32_t *>(smem_raw + sizeof(uint32_t) * kMergeCap);
-  int n_c = 0;
-  for (int cc = 0; cc < nch; ++cc) {
-    const int sl = unit * a.n_chunks_max + cc;
-    const int cnt = __ldcg(a.cand_count + sl);
-    const uint32_t *ck = a.cand_key + (size_t)sl * a.k_cap;
-    const int32_t *cp = a.cand_page + (size_t)sl * a.k_cap;
-    for (int x = tid; x < cnt; x += kSelThreads) {
-      mkey[n_c + x] = __ldcg(ck + x);
-      mpage[n_c + x] = __ldcg(cp + x);
+  int *moff = reinterpret_cast<int *>(smem_raw + 2 * sizeof(uint32_t) * kMergeCap);  // [nch + 1]
+  // every chunk's winner count at once, then their offsets (a walk over the chunks that waited
+  // for each count before the next copy took 16 dependent round trips at 16 chunks)
+  const int *cnt_row = a.cand_count + (size_t)unit * a.n_chunks_max;
+  for (int cc = tid; cc < nch; cc += kSelThreads) moff[cc + 1] = __ldcg(cnt_row + cc);
+  __syncthreads();
+  if (tid == 0) {
+    moff[0] = 0;
+    for (int cc = 0; cc < nch; ++cc) moff[cc + 1] += moff[cc];
+  }
+  __syncthreads();
+  const int n_c = moff[nch];
+  const uint32_t *ck_row = a.cand_key + (size_t)unit * a.n_chunks_max * a.k_cap;
+  const int32_t *cp_row = a.cand_page + (size_t)unit * a.n_chunks_max * a.k_cap;
+  for (int idx = tid; idx < nch * a.k_cap; idx += kSelThreads) {
+    const int cc = idx / a.k_cap, x = idx - cc * a.k_cap;
+    if (x < moff[cc + 1] - moff[cc]) {
+      mkey[moff[cc] + x] = __ldcg(ck_row + idx);
+      mpage[moff[cc] + x] = __ldcg(cp_row + idx);
     }
-    n_c += cnt;
   }
   __syncthreads();
   wrote = 0;
@@ -398,7 +407,8 @@ cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s, bool first_of
   // keys of one chunk; the merge buffer only when a unit spans several chunks (the smaller
   // footprint keeps every CTA of a one-chunk call resident at once)
   const size_t keys_bytes = (size_t)std::min(a.chunk, a.max_pages) * 4;
-  const size_t smem = a.n_chunks_max == 1 ? keys_bytes : std::max<size_t>(keys_bytes, (size_t)kMergeCap * 8);
+  const size_t merge_bytes = (size_t)kMergeCap * 8 + (size_t)(a.n_chunks_max + 1) * 4;  // keys, pages, offsets
+  const size_t smem = a.n_chunks_max == 1 ? keys_bytes : std::max<size_t>(keys_bytes, merge_bytes);
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.H_kv, a.n_chunks_max, a.B);
