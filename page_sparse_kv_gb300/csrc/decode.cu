@@ -249,10 +249,13 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int i, int h, int dg
 
 // Streams the 16-token tiles of the n_ent entries in the entry table through this warp's TMA
 // ring (warp w takes tiles w, w + NW, ...) and folds them into the warp's (m, l, O). cw is the
-// warp's running tile count: ring stage and mbarrier phase carry on across calls.
+// warp's running tile count: ring stage and mbarrier phase carry on across calls. q_seq >= 0:
+// q2 is loaded here (sequence q_seq), after the first tiles' copies are issued, so that its
+// global load overlaps their latency; q_seq < 0: the caller has loaded q2.
 template <typename T, int D, int G, int NW, int NST>
 __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMap *tmK, const CUtensorMap *tmV, int h,
-                                           const float2 (&q2)[G][DT<T, D, G, NW, NST>::CPL * DT<T, D, G, NW, NST>::EPC / 2],
+                                           int q_seq,
+                                           float2 (&q2)[G][DT<T, D, G, NW, NST>::CPL * DT<T, D, G, NW, NST>::EPC / 2],
                                            const int *ent_blk, const int *ent_valid, int n_ent, unsigned char *stages,
                                            float2 *pp_all, uint64_t (*bars)[NST], int &cw, float (&m)[G], float (&l)[G],
                                            float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2]) {
@@ -294,6 +297,7 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
 
 #pragma unroll
   for (int k = 0; k < NST - 1; ++k) issue(k);
+  if (q_seq >= 0) load_q<T, D, G, NW, NST>(a, q_seq, h, dg, q2);
   int k = 0;
   for (int cur = warp; cur < ntiles; ++k, cur += NW) {
     issue(k + NST - 1);
@@ -535,6 +539,9 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   const int e0 = split_off(s, a.sw, a.taper), len = split_len(s, a.sw, a.taper);
   const size_t pbase = (size_t)unit * a.n_items_max + s;
 
+  // the list entry the alone test below reads, issued with the others (independent of them)
+  const int32_t sw_entry =
+      (a.selected && a.n_items_max > 1 && a.b_max > a.sw) ? a.selected[(size_t)unit * a.b_max + a.sw] : -1;
   int n_ent = 0;
   if (seq_len < 1 || P > a.max_pages) {
     if (s == 0 && tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
@@ -555,16 +562,14 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   // no merge: split 0 writes the normalised output and the other splits leave at once
   bool alone = false;
   if (a.selected) {
-    const int32_t *row = a.selected + (size_t)unit * a.b_max;
-    alone = a.n_items_max == 1 || a.b_max <= a.sw || row[a.sw] < 0;
+    alone = a.n_items_max == 1 || a.b_max <= a.sw || sw_entry < 0;
   } else {
     alone = a.n_items_max == 1 || P <= a.sw;
   }
   if (alone && s > 0) return;
 
   if (n_ent > 0) {
-    float2 q2[G][TR::CPL * TR::EPC / 2];
-    load_q<T, D, G, NW, NST>(a, i, h, lane & 7, q2);
+    float2 q2[G][TR::CPL * TR::EPC / 2];  // loaded by warp_tiles, behind the first tile copies
     float m[G], l[G];
     float2 O[G][TR::VPL / 2];
 #pragma unroll
@@ -575,8 +580,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
       for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = make_float2(0.f, 0.f);
     }
     int cw = 0;
-    warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages, sm.pp_all, bars, cw,
-                                 m, l, O);
+    warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, i, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages, sm.pp_all, bars,
+                                 cw, m, l, O);
     __syncthreads();  // every warp is done with the stages; the merge below reuses them
     if (alone) {
       write_output<T, D, G, NW, NST>(a, unit, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
@@ -742,7 +747,7 @@ __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, cons
       __syncthreads();  // the previous entry table and stages are no longer in use
       load_entries<NT>(a, i, u, P, seq_len, (int)(x0 - start[u]), n, sm.ent_blk, sm.ent_valid);
       __syncthreads();
-      warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, q2, sm.ent_blk, sm.ent_valid, n, sm.stages, sm.pp_all, bars, cw, m,
+      warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, -1, q2, sm.ent_blk, sm.ent_valid, n, sm.stages, sm.pp_all, bars, cw, m,
                                    l, O);
     }
     __syncthreads();  // every warp is done with the stages; the merges below reuse them

@@ -236,14 +236,15 @@ __device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, in
   for (int x = count + tid; x < b_max; x += kSelThreads) sel_row[x] = -1;
 }
 
-// Budget of a sequence of P pages (at least the always-kept count in the scalar modes).
-__device__ int unit_budget(const ScoreArgs &a, int i, int P, int n_forced) {
+// Budget of a sequence of P pages (at least the always-kept count in the scalar modes);
+// budget_in: the sequence's entry of a.budgets in the per-sequence mode.
+__device__ int unit_budget(const ScoreArgs &a, int budget_in, int P, int n_forced) {
   if (a.budget_mode == PSK_BUDGET_FRACTION) {
     const int r = (int)ceil((double)P * a.budget_frac);  // IEEE double product, then the ceiling
     return max(n_forced, min(P, max(1, r)));
   }
   if (a.budget_mode == PSK_BUDGET_PAGES) return max(n_forced, min(P, a.budget_pages));
-  return a.budgets[i];
+  return budget_in;
 }
 
 __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a) {
@@ -256,6 +257,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
   const int unit = i * a.H_kv + h;
   const int tid = threadIdx.x;
   const int seq_len = a.seq_lens[i];
+  // the budget load is issued together with the length's (both are one L2 round trip)
+  const int budget_in = a.budget_mode == PSK_BUDGET_PER_SEQUENCE ? a.budgets[i] : 0;
   const int P = (seq_len + a.ps - 1) / a.ps;
   int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
 
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     return;
   }
   const int n_forced = min(P, a.sink + a.window);
-  const int budget = unit_budget(a, i, P, n_forced);
+  const int budget = unit_budget(a, budget_in, P, n_forced);
   if (budget < n_forced || budget > a.b_max) {
     if (c == 0) {
       if (tid == 0) set_status(a.ws, PSK_DEV_BAD_BUDGET);
