@@ -275,8 +275,13 @@ def run_psk(args):
     ws = cache.ws
     setup_s = time.time() - t_setup
 
+    # --v-host: the value tier in pinned host memory, read (and appended to) over NVLink-C2C
+    v_store = cache.v_cache.cpu().pin_memory() if args.v_host else cache.v_cache
+    if args.v_host and (w.latent or w.dtype != "bf16" or D != 128):
+        raise SystemExit("--v-host is built for GQA bf16 caches with head_dim 128")
+
     def append():
-        psk.kv_append_and_summarize(L, k_new, v_new, start, cu, 1, cache.k_cache, cache.v_cache, cache.summaries,
+        psk.kv_append_and_summarize(L, k_new, v_new, start, cu, 1, cache.k_cache, v_store, cache.summaries,
                                     cache.block_table, ws)
 
     def score():
@@ -293,8 +298,12 @@ def run_psk(args):
         psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
 
     def decode():
-        psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
-                                w.b_max, cache.scale, out, ws)
+        if args.v_host:
+            psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_store, cache.block_table, cache.seq_lens, sel, w.b_max,
+                                       cache.scale, out, ws, v_host=True)
+        else:
+            psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
+                                    w.b_max, cache.scale, out, ws)
 
     def dense():
         psk.dense_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, cache.scale,
@@ -545,6 +554,9 @@ def run_psk(args):
                 "unit": "GB/s", "algorithmic_per_launch": decode_bytes, "algorithmic_unit": "B",
                 "launch_us": t_dec * 1e3}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if args.v_host and dom == "decode_split_kernel":
+        roof["note"] = "V of the selected pages crosses NVLink-C2C, not HBM; achieved counts K and V bytes"
+
     roof["peak_kind"] = pk["kind"] + (" sustained bf16" if roof["bound"] == "tensor" else " copy")
     roof["traffic"] = traffic_of(w.name, dom)
     roof["traffic_digest"] = kernel_digest(dom)
@@ -575,7 +587,9 @@ def run_psk(args):
                    "timing": ("CUDA-graph replay of the step's launches (the append on a second stream beside "
                               "score + select)" if graphed else "eager launches")
                              + "; CUDA events on the launching stream",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "v_cache": ("pinned host memory, read over NVLink-C2C (the selected pages' V bytes do not "
+                               "cross HBM; the dense step keeps V in HBM)") if args.v_host else "HBM"},
         "roofline": roof,
         "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / (step_ms * 1e-3) / 1e9,
                      "frac_of_measured": step_bytes / (step_ms * 1e-3) / 1e9 / peak_hbm,
@@ -612,6 +626,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--v-host", action="store_true",
+                    help="keep the value cache in pinned host memory (the value tier; GQA bf16, head_dim 128)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -257,13 +257,21 @@ int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *
                            size_t workspace_bytes, psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * psk_sparse_paged_decode with flags. PSK_DECODE_PER_QUERY_HEAD: selected is
+ * psk_sparse_paged_decode with flags (below). PSK_DECODE_PER_QUERY_HEAD: selected is
  * [batch, num_q_heads, b_max] (rows of psk_page_score_select_ex with per_query_head = 1) and
  * query head g attends its own row's pages of KV head g / G. flags = 0 is
  * psk_sparse_paged_decode. GQA only; the workspace is the one psk_sparse_decode_workspace_size
  * sizes (it covers both forms).
  * --------------------------------------------------------------------------------------- */
 #define PSK_DECODE_PER_QUERY_HEAD 0x1u
+/* PSK_DECODE_V_HOST: the value tier in host memory (LOCKS PKG-INFO, "Configuration", variant
+ * mem-v: V in DRAM, K resident). v_cache is host memory the GPU can address directly (pinned
+ * with cudaHostAlloc / cudaMallocHost, addressed by its host pointer under unified addressing)
+ * and is read over NVLink-C2C with plain loads, only for the selected pages' valid rows; K, the
+ * summaries and the rest stay in device memory. psk_kv_append_and_summarize writes new values
+ * to such a v_cache directly. Built for sparse GQA decode, PSK_BF16, head_dim 128 (else
+ * PSK_ERR_UNSUPPORTED). */
+#define PSK_DECODE_V_HOST 0x2u
 int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const void *k_cache,
                                const void *v_cache, const int32_t *block_table,
                                const int32_t *seq_lens, const int32_t *selected, int32_t b_max,

@@ -42,7 +42,7 @@ class PskLayout(ctypes.Structure):
 
 
 BUDGET_PER_SEQUENCE, BUDGET_PAGES, BUDGET_FRACTION = 0, 1, 2
-DECODE_PER_QUERY_HEAD = 0x1
+DECODE_PER_QUERY_HEAD, DECODE_V_HOST = 0x1, 0x2
 
 
 class PskSelectParams(ctypes.Structure):
@@ -113,10 +113,13 @@ def lib() -> ctypes.CDLL:
 
 # ------------------------------------------------------------------------------ helpers
 def _ptr(t):
+    """Device-addressable pointer of a contiguous tensor: a CUDA tensor, or a pinned host tensor
+    (under unified addressing the GPU reads and writes it by its host pointer, e.g. the value
+    cache of the host-memory value tier)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("expected a CUDA tensor or a pinned host tensor")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return ctypes.c_void_p(t.data_ptr())
@@ -247,11 +250,14 @@ def sparse_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_le
 
 
 def sparse_paged_decode_ex(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max: int,
-                           scale: float, out, workspace, per_query_head: bool = False, stream=None):
-    """sparse_paged_decode over rows per (sequence, query head) when ``per_query_head``."""
+                           scale: float, out, workspace, per_query_head: bool = False, v_host: bool = False,
+                           stream=None):
+    """sparse_paged_decode over rows per (sequence, query head) when ``per_query_head``; with
+    ``v_host`` the value cache is a pinned host tensor read over NVLink-C2C."""
+    flags = (DECODE_PER_QUERY_HEAD if per_query_head else 0) | (DECODE_V_HOST if v_host else 0)
     _check("psk_sparse_paged_decode_ex", lib().psk_sparse_paged_decode_ex(
         ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
-        _ptr(selected), int(b_max), float(scale), DECODE_PER_QUERY_HEAD if per_query_head else 0, _ptr(out),
+        _ptr(selected), int(b_max), float(scale), flags, _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

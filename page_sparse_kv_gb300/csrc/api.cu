@@ -304,7 +304,7 @@ int psk_page_select(const psk_layout *layout, const int32_t *seq_lens, const psk
 static int decode_common(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
                          int32_t b_max, float scale, void *out, void *workspace, size_t workspace_bytes,
-                         psk_stream_t stream, bool per_query_head = false) {
+                         psk_stream_t stream, bool per_query_head = false, bool v_host = false) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
@@ -317,6 +317,8 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   psk_layout U = L;  // the units' layout (per-query-head view for per-query-head rows)
   int kv_shift = 0;
   if (per_query_head && (dense || !per_query_head_view(L, &U, &kv_shift))) return PSK_ERR_UNSUPPORTED;
+  // the value tier in host memory: sparse GQA decode, bf16, head_dim 128
+  if (v_host && (dense || L.latent || L.dtype != PSK_BF16 || L.head_dim != 128)) return PSK_ERR_UNSUPPORTED;
   DecodePlan plan;
   if (!plan_any_decode(U, dense ? L.max_pages : b_max, dense, &plan)) return PSK_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.ws_bytes) return PSK_ERR_WORKSPACE;
@@ -338,6 +340,7 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.H_kv = U.num_kv_heads;
   a.H_kv_cache = L.num_kv_heads;
   a.kv_shift = kv_shift;
+  a.v_host = v_host ? 1 : 0;
   a.D = L.head_dim;
   a.D_v = L.v_head_dim;
   a.ps = L.page_size;
@@ -367,9 +370,11 @@ int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const vo
                                const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
                                int32_t b_max, float scale, uint32_t flags, void *out, void *workspace,
                                size_t workspace_bytes, psk_stream_t stream) {
-  if (!selected || b_max < 1 || (flags & ~PSK_DECODE_PER_QUERY_HEAD) != 0) return PSK_ERR_INVALID_ARG;
+  if (!selected || b_max < 1 || (flags & ~(PSK_DECODE_PER_QUERY_HEAD | PSK_DECODE_V_HOST)) != 0)
+    return PSK_ERR_INVALID_ARG;
   return decode_common(layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max, scale, out, workspace,
-                       workspace_bytes, stream, (flags & PSK_DECODE_PER_QUERY_HEAD) != 0);
+                       workspace_bytes, stream, (flags & PSK_DECODE_PER_QUERY_HEAD) != 0,
+                       (flags & PSK_DECODE_V_HOST) != 0);
 }
 
 int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,

@@ -252,7 +252,11 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int i, int h, int dg
 // warp's running tile count: ring stage and mbarrier phase carry on across calls. q_seq >= 0:
 // q2 is loaded here (sequence q_seq), after the first tiles' copies are issued, so that its
 // global load overlaps their latency; q_seq < 0: the caller has loaded q2.
-template <typename T, int D, int G, int NW, int NST>
+// kHostV: V rows live in host memory the GPU reads over NVLink-C2C through unified addressing
+// (the value tier); only K goes through the TMA ring, and each lane loads its own V slice of
+// the tile's valid rows with plain loads when the tile starts, so the C2C latency overlaps the
+// QK product and the softmax. Built for 8 bytes of V per lane and row (bf16, D = 128).
+template <typename T, int D, int G, int NW, int NST, bool kHostV = false>
 __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMap *tmK, const CUtensorMap *tmV, int h,
                                            int q_seq,
                                            float2 (&q2)[G][DT<T, D, G, NW, NST>::CPL * DT<T, D, G, NW, NST>::EPC / 2],
@@ -283,12 +287,12 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
       const int nv = min(16, ent_valid[e] - sub * 16);
       if (nv > 0) {
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, 2u * TR::TILE);
+        mbar_arrive_expect_tx(bar, (kHostV ? 1u : 2u) * TR::TILE);
         const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
         const int row = ent_blk[e] * a.ps + sub * 16;
         const uint64_t pol = l2_evict_first_policy();  // K/V rows are read once per step
         tma_load_3d_stream(sK, tmK, 0, h >> a.kv_shift, row, bar, pol);  // the unit head's cache head
-        tma_load_3d_stream(sK + TR::TILE, tmV, 0, h >> a.kv_shift, row, bar, pol);
+        if (!kHostV) tma_load_3d_stream(sK + TR::TILE, tmV, 0, h >> a.kv_shift, row, bar, pol);
       } else {
         mbar_arrive_expect_tx(bar, 0u);
       }
@@ -299,8 +303,20 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
   for (int k = 0; k < NST - 1; ++k) issue(k);
   if (q_seq >= 0) load_q<T, D, G, NW, NST>(a, q_seq, h, dg, q2);
   int k = 0;
+  static_assert(!kHostV || TR::VPL * TR::ES == 8, "the host value path loads 8 bytes per lane and row");
   for (int cur = warp; cur < ntiles; ++k, cur += NW) {
     issue(k + NST - 1);
+    uint2 vh[kHostV ? 16 : 1];  // kHostV: this lane's V slice of the tile's rows
+    if constexpr (kHostV) {
+      const int e = stp == 1 ? cur : cur / stp, sub = cur - e * stp;
+      const int nvh = min(16, ent_valid[e] - sub * 16);
+      const size_t row0 = (size_t)ent_blk[e] * a.ps + sub * 16;
+      const T *vb = reinterpret_cast<const T *>(a.v_cache) + (row0 * a.H_kv_cache + (h >> a.kv_shift)) * D +
+                    lane * TR::VPL;
+#pragma unroll
+      for (int tk = 0; tk < 16; ++tk)  // only rows below seq_len: the rest may hold anything
+        vh[tk] = tk < nvh ? *reinterpret_cast<const uint2 *>(vb + (size_t)tk * a.H_kv_cache * D) : make_uint2(0u, 0u);
+    }
     const int stage = (cw0 + k) % NST;
     mbar_wait(smem_u32(&bars[warp][stage]), ((cw0 + k) / NST) & 1, a.ws);
     const int nv = tile_rows(cur);
@@ -392,7 +408,9 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
       auto pv_row = [&](int tk) {
         float2 vf[TR::VPL / 2];
         const unsigned char *vr = sV + tk * TR::ROW + lane * TR::VPL * TR::ES;
-        if constexpr (TR::VPL * TR::ES == 16) {
+        if constexpr (kHostV) {
+          Elem<T>::to_f2_8(vh[tk], vf);
+        } else if constexpr (TR::VPL * TR::ES == 16) {
           Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(vr), vf);
         } else {
           Elem<T>::to_f2_8(*reinterpret_cast<const uint2 *>(vr), vf);
@@ -408,6 +426,10 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
       if (nv == 16) {
 #pragma unroll
         for (int tk = 0; tk < 16; ++tk) pv_row(tk);
+      } else if constexpr (kHostV) {  // unrolled, so that vh stays in registers
+#pragma unroll
+        for (int tk = 0; tk < 16; ++tk)
+          if (tk < nv) pv_row(tk);
       } else {
         for (int tk = 0; tk < nv; ++tk) pv_row(tk);
       }
@@ -519,7 +541,7 @@ struct DecodeSmem {
 };
 
 // ---- split layout: one CTA per (split of `sw` list entries, KV head, sequence) ----------------
-template <typename T, int D, int G, int NW, int NST>
+template <typename T, int D, int G, int NW, int NST, bool kHostV>
 __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV) {
   pdl_wait();  // dependents are released when this grid completes
@@ -580,8 +602,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
       for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = make_float2(0.f, 0.f);
     }
     int cw = 0;
-    warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, i, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages, sm.pp_all, bars,
-                                 cw, m, l, O);
+    warp_tiles<T, D, G, NW, NST, kHostV>(a, &tmK, &tmV, h, i, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages,
+                                         sm.pp_all, bars, cw, m, l, O);
     __syncthreads();  // every warp is done with the stages; the merge below reuses them
     if (alone) {
       write_output<T, D, G, NW, NST>(a, unit, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
@@ -776,12 +798,25 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   CUtensorMap tmK, tmV;
   const long long rows = (long long)a.nb * a.ps;
   const int dt = sizeof(T) == 4 ? PSK_F32 : PSK_BF16;
+  // host values: no tensor map over host memory (V is read with plain loads); tmV repeats tmK
   if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv_cache, rows, 16) ||
-      !encode_cache_map(&tmV, a.v_cache, dt, D, a.H_kv_cache, rows, 16))
+      !encode_cache_map(&tmV, a.v_host ? a.k_cache : a.v_cache, dt, D, a.H_kv_cache, rows, 16))
     return cudaErrorInvalidValue;
   cudaError_t e;
+  if (a.v_host) {  // the value tier: sparse split layout only
+    if constexpr (sizeof(T) == 2 && D == 128) {
+      if (a.flat || !a.selected) return cudaErrorInvalidValue;
+      auto kfn = decode_split_kernel<T, D, G, NW, NST, true>;
+      e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
+      if (e != cudaSuccess) return e;
+      dim3 grid(a.B * a.H_kv, a.n_items_max);
+      return launch_kernel(true, kfn, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
+    } else {
+      return cudaErrorInvalidValue;
+    }
+  }
   if (!a.flat) {
-    auto kfn = decode_split_kernel<T, D, G, NW, NST>;
+    auto kfn = decode_split_kernel<T, D, G, NW, NST, false>;
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.B * a.H_kv, a.n_items_max);

@@ -94,6 +94,7 @@ struct DecodeArgs {
   int b_max;           // entries per selected row (sparse)
   int H_kv_cache;      // KV heads of the cache (H_kv above counts the units' heads)
   int kv_shift;        // unit head h reads cache head h >> kv_shift
+  int v_host;          // 1: v_cache is host memory read over NVLink-C2C (sparse split, bf16, D = 128)
   int sw;              // list entries per item (split layout)
   int n_items_max;     // items per unit (split layout)
   int32_t *counts;     // [B * H_kv] list entries per unit (flat layout, sparse)

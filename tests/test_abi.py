@@ -115,9 +115,16 @@ def test_select_params_host_checks(lib):
     assert call(2, mode=psk.BUDGET_FRACTION, fraction=0.05) == 1
     assert call(49, mode=psk.BUDGET_FRACTION, fraction=1.0) == 1             # every one of 50 pages
     # the decode with flags: unknown flag bits, or no selected rows, answer before any launch
-    rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), P(16), 10, 1.0, 0x2,
+    # (0x4 is no flag; every call here must be refused before a launch, since its pointers are
+    # placeholders)
+    rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), P(16), 10, 1.0, 0x4,
                                         P(16), P(16), 1 << 30, None)
     assert rc == 1
+    # the host value tier is refused for shapes it is not built for (fp32 here)
+    L32 = psk.Layout(2, 32, 8, 128, 128, 16, 100, 50, dtype=psk.PSK_F32).c()
+    rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L32), P(16), P(16), P(16), P(16), P(16), P(16), 10, 1.0, 0x2,
+                                        P(16), P(16), 1 << 30, None)
+    assert rc == 2
     rc = lib.psk_sparse_paged_decode_ex(ctypes.byref(L), P(16), P(16), P(16), P(16), P(16), None, 10, 1.0, 0x1,
                                         P(16), P(16), 1 << 30, None)
     assert rc == 1

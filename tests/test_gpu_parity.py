@@ -355,6 +355,51 @@ def test_split_score_then_select_equals_combined(latent):
     assert torch.equal(torch.nan_to_num(sc1, nan=-1e30), torch.nan_to_num(sc2, nan=-1e30))
 
 
+def test_value_tier_in_host_memory():
+    """V in pinned host memory, read over NVLink-C2C (PSK_DECODE_V_HOST): the decode equals the
+    device-memory decode bit for bit and the oracle; a decode append writes the new token's value
+    straight into the host cache."""
+    w = _custom([16 * 300 + 5, 16 * 77 + 9, 5000, 17], [40, 9, 30, 2], H_q=32, H_kv=8)
+    cache = upload(w)
+    L = cache.layout
+    q_np = w.queries()
+    q = to_torch(q_np, w.dtype).cuda()
+    v_host = cache.v_cache.cpu().pin_memory()
+    sel = cache.score_select(q, dev_budgets(w))
+    out_dev = cache.sparse_decode(q, sel)
+    out_host = torch.empty_like(out_dev)
+    psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_host, cache.block_table, cache.seq_lens, sel, cache.b_max,
+                               cache.scale, out_host, cache.ws, v_host=True)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    assert torch.equal(out_dev, out_host)
+    # one decode token per sequence appended with the value written to host memory
+    rng = np.random.default_rng(5)
+    lens = w.seq_lens.astype(np.int64)
+    k_new = W.f32_to_bf16_bits(rng.standard_normal((w.B, w.H_kv, w.D)).astype(np.float32))
+    v_new = W.f32_to_bf16_bits(rng.standard_normal((w.B, w.H_kv, w.D)).astype(np.float32))
+    start = torch.from_numpy(lens.astype(np.int32)).cuda()
+    cu = torch.arange(w.B + 1, dtype=torch.int32, device="cuda")
+    psk.kv_append_and_summarize(L, to_torch(k_new, w.dtype).cuda(), to_torch(v_new, w.dtype).cuda(), start, cu, 1,
+                                cache.k_cache, v_host, cache.summaries, cache.block_table, cache.ws)
+    cache.seq_lens.copy_(torch.from_numpy((lens + 1).astype(np.int32)).cuda())
+    sel2 = cache.score_select(q, dev_budgets(w))
+    out2 = torch.empty_like(out_dev)
+    psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_host, cache.block_table, cache.seq_lens, sel2, cache.b_max,
+                               cache.scale, out2, cache.ws, v_host=True)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    sel_np = sel2.cpu().numpy()
+    out_np = from_torch(out2.float(), "f32")
+    scale = 1.0 / math.sqrt(w.D)
+    for i in range(w.B):
+        n = int(lens[i]) + 1
+        keys = np.concatenate([w.keys(i), k_new[i][None]])
+        vals = np.concatenate([w.values(i), v_new[i][None]])
+        use = [[int(x) for x in sel_np[i, h] if x >= 0] for h in range(w.H_kv)]
+        check_output(out_np[i], O.attend_pages(q_np[i], keys, vals, n, w.page_size, use, w.dtype, scale), w.dtype)
+
+
 def test_ties_resolve_to_lower_page():
     """Pages with identical keys (hence identical summaries and scores) tie; with the cutoff
     inside the tied group the lowest-indexed tied pages win."""
