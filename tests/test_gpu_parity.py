@@ -5,6 +5,7 @@ score chunks, several decode splits, ragged tail pages, shuffled physical blocks
 oracle still finishes in seconds.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -508,3 +509,44 @@ def test_full_budget_sparse_equals_dense_bitwise():
     torch.cuda.synchronize()
     # splits differ between the two calls (budget-sized vs page-sized), so compare to tolerance
     check_output(from_torch(sp.float(), "f32"), from_torch(de.float(), "f32").astype(np.float64), "bf16")
+
+
+_PDL_CHILD = r"""
+import math, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import oracle as O
+import page_sparse_kv_gb300 as psk
+import workloads as W
+from workloads.device import budgets as dev_budgets, from_torch, to_torch, upload
+from parity import check_output
+w = W.Workload("custom", 7, "bf16", B=3, H_q=8, H_kv=2, D=128, D_v=128, page_size=16,
+               seq_lens=[16 * 90 + 3, 16 * 20, 500], budgets=[9, 4, 6], n_hot=0, hot_rule="random", pool_slack=3)
+cache = upload(w)
+q_np = w.queries()
+q = to_torch(q_np, w.dtype).cuda()
+sel = cache.score_select(q, dev_budgets(w))
+out = cache.sparse_decode(q, sel)
+torch.cuda.synchronize()
+assert psk.get_device_status(cache.ws) == 0
+sel_np, out_np = sel.cpu().numpy(), from_torch(out.float(), "f32")
+for i in range(w.B):
+    n = int(w.seq_lens[i])
+    use = [[int(x) for x in sel_np[i, h] if x >= 0] for h in range(w.H_kv)]
+    ref = O.attend_pages(q_np[i], w.keys(i), w.values(i), n, w.page_size, use, w.dtype, 1 / math.sqrt(w.D))
+    check_output(out_np[i], ref, w.dtype)
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("mode", ["0", "2"])
+def test_launch_modes_without_and_with_in_call_pdl(mode):
+    """PSK_PDL=0 (plain stream order) and PSK_PDL=2 (programmatic launch only between the kernels
+    of one call) give oracle-matching results; the setting is read once per process, so each runs
+    in a child process."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PSK_PDL=mode, PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+    r = subprocess.run([sys.executable, "-c", _PDL_CHILD, root], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
