@@ -10,7 +10,12 @@
  *                                 sum_d max(q_d*kmin_d, q_d*kmax_d), max over the GQA
  *                                 group, times scale; keep the top-b pages per
  *                                 (sequence, KV head) with the sink and tail forced.
+ *                                 (_ex: general always-kept sets, budget modes and
+ *                                 per-query-head rows; psk_page_score + psk_page_select:
+ *                                 the same two stages as separate calls.)
  *   psk_sparse_paged_decode       exact softmax attention over the selected pages only.
+ *                                 (_ex: per-query-head rows, value cache in host memory;
+ *                                 _noalloc: the same without a caller workspace.)
  *   psk_dense_paged_decode        the same kernel over every page (full-KV baseline).
  *
  * Sources of each operation (pages on page-selective sparse KV attention):

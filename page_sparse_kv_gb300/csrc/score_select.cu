@@ -79,7 +79,7 @@ __device__ __forceinline__ float dot2_bf16(uint32_t q, uint32_t k, float acc) {
 }
 
 // ------------------------------------------------------------------------------------
-// K1: page scores, streaming
+// page scores, streaming
 // ------------------------------------------------------------------------------------
 // One CTA per (chunk, sequence, group of up to 8 KV heads): chunks of a.pchunk pages first, then
 // each sequence's last a.tail_pages pages in chunks of a.tail_chunk (see launch_t). The summaries of
@@ -88,8 +88,8 @@ __device__ __forceinline__ float dot2_bf16(uint32_t q, uint32_t k, float acc) {
 // kStages shared-memory stages of a.stage_pages pages, completion tracked by one mbarrier per
 // stage (bounded waits). All warps then score from shared memory: warp w takes KV head w % HPC
 // of the group and every (8 / HPC)-th page step. Writes one 32-bit order key per page (0 for
-// the forced sink / tail and for pages whose block id is out of range) and, when asked, the
-// fp32 score.
+// an always-kept page and for pages whose block id is out of range) and, when asked, the fp32
+// score.
 constexpr int kStages = 2;
 constexpr int kStageBytes = 24576;
 constexpr int kMaxStagePages = 32;
