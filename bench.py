@@ -61,17 +61,21 @@ TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
     ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel"):
-        {"bytes": 577_377_024 + 4_418_816, "digest": "71afaa7efc0fe70e"},
+        {"bytes": 577_373_952 + 4_458_240, "digest": "6b457f0a50eb5b54"},
     ("batched-ragged-b64-8k..64k-5pct", "page_select_kernel"):
-        {"bytes": 4_623_104 + 0, "digest": "d62c370dc82f0afb"},
+        {"bytes": 4_622_848 + 0, "digest": "9b065b1469e13666"},
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 466_841_088 + 1_147_648, "digest": "e3dda5f1d761e9ec"},
+        {"bytes": 466_761_728 + 1_079_040, "digest": "17d6bc14093fb0fd"},
+    # python bench.py --workload 4 --steps 5 --warmup 3 --no-cpu-baseline, then
+    # ncu ... -k regex:"page_score" -s 2 -c 1 python bench.py --workload 4 --steps 5 --warmup 3 --no-cpu-baseline
+    ("long-1m-b1", "page_score_kernel"):
+        {"bytes": 268_734_720 + 3_986_432, "digest": "6b457f0a50eb5b54"},
     # python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline, then
     # ncu ... -k regex:"mla_" -s 0 -c 3 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
     ("mla-b16-128k-5pct", "mla_qsplit_kernel+mla_score_kernel"):
-        {"bytes": 2_363_392 + 0 + 80_301_312 + 57_600, "digest": "8389efad62f45629"},
+        {"bytes": 2_363_648 + 0 + 80_295_680 + 34_560, "digest": "494eab7f3bf82b5b"},
     ("mla-b16-128k-5pct", "mla_decode_kernel"):
-        {"bytes": 124_114_944 + 124_672, "digest": "8389efad62f45629"},
+        {"bytes": 124_142_336 + 216_832, "digest": "494eab7f3bf82b5b"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
