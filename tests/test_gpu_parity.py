@@ -356,11 +356,12 @@ def test_split_score_then_select_equals_combined(latent):
     assert torch.equal(torch.nan_to_num(sc1, nan=-1e30), torch.nan_to_num(sc2, nan=-1e30))
 
 
-def test_value_tier_in_host_memory():
+@pytest.mark.parametrize("ps", [16, 64])
+def test_value_tier_in_host_memory(ps):
     """V in pinned host memory, read over NVLink-C2C (PSK_DECODE_V_HOST): the decode equals the
     device-memory decode bit for bit and the oracle; a decode append writes the new token's value
-    straight into the host cache."""
-    w = _custom([16 * 300 + 5, 16 * 77 + 9, 5000, 17], [40, 9, 30, 2], H_q=32, H_kv=8)
+    straight into the host cache. Pages of 64 tokens are four tiles each."""
+    w = _custom([ps * 75 + 5, ps * 19 + 9, ps * 40 + ps // 2 + 3, 17], [40, 9, 30, 2], ps=ps, H_q=32, H_kv=8)
     cache = upload(w)
     L = cache.layout
     q_np = w.queries()
