@@ -301,13 +301,14 @@ def run_psk(args):
     def select_only():
         psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
 
-    def decode():
+    def decode(dst=None):  # dst: the output buffer (default: `out` in device memory)
+        o = out if dst is None else dst
         if args.v_host:
             psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_store, cache.block_table, cache.seq_lens, sel, w.b_max,
-                                       cache.scale, out, ws, v_host=True)
+                                       cache.scale, o, ws, v_host=True)
         else:
             psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
-                                    w.b_max, cache.scale, out, ws)
+                                    w.b_max, cache.scale, o, ws)
 
     def dense():
         psk.dense_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, cache.scale,
@@ -342,7 +343,7 @@ def run_psk(args):
     # stream beside score + select, and the decode waits for both.
     side_s = torch.cuda.Stream()
 
-    def step_overlapped(pre_main=None, pre_side=None, post=None):
+    def step_overlapped(pre_main=None, pre_side=None, post=None, dec_out=None):
         cur = torch.cuda.current_stream()
         fork = torch.cuda.Event()
         fork.record(cur)
@@ -357,7 +358,7 @@ def run_psk(args):
             pre_main()
         score()
         cur.wait_event(join)
-        decode()
+        decode(dec_out)
         if post is not None:
             post()
 
@@ -462,7 +463,9 @@ def run_psk(args):
         sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = max_over_ranks(
             [sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], dev)
 
-    # ---- end to end: host buffers through the C ABI (pinned H2D of the step's inputs, D2H of out)
+    # ---- end to end: host buffers through the C ABI. The step's inputs are copied from pinned
+    # host memory (H2D); the decode writes its output straight into the pinned host buffer (the
+    # GPU addresses it under unified addressing, the bytes cross NVLink-C2C inside the step)
     qh = to_torch(q_host, w.dtype).pin_memory()
     kh = to_torch(k_last, w.dtype).pin_memory()
     vh = None if w.latent else to_torch(v_last, w.dtype).pin_memory()
@@ -472,7 +475,7 @@ def run_psk(args):
         q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True)
         if vh is not None:
             v_new.copy_(vh, non_blocking=True)
-        append(); score(); decode(); oh.copy_(out, non_blocking=True)
+        append(); score(); decode(oh)
     barrier()
     exs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
     for k in range(Ke):
@@ -481,8 +484,7 @@ def run_psk(args):
         q.copy_(qh, non_blocking=True); k_new.copy_(kh, non_blocking=True)
         if vh is not None:
             v_new.copy_(vh, non_blocking=True)
-        append(); score(); decode()
-        oh.copy_(out, non_blocking=True)
+        append(); score(); decode(oh)
         exs[k][1].record(stream)
     torch.cuda.synchronize()
     e2e_eager_ms = per_step(exs)
@@ -492,8 +494,7 @@ def run_psk(args):
             k_new.copy_(kh, non_blocking=True)
             if vh is not None:
                 v_new.copy_(vh, non_blocking=True)
-        step_overlapped(pre_main=lambda: q.copy_(qh, non_blocking=True), pre_side=copy_kv,
-                        post=lambda: oh.copy_(out, non_blocking=True))
+        step_overlapped(pre_main=lambda: q.copy_(qh, non_blocking=True), pre_side=copy_kv, dec_out=oh)
 
     e2e_ms = e2e_eager_ms
     if g_sparse is not None:  # the same step with its copies, replayed as one CUDA graph
@@ -607,7 +608,9 @@ def run_psk(args):
                        "score_select": (t_score + t_select) * 1e3, "sparse_decode": t_dec * 1e3},
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "timing": ("CUDA-graph replay" if e2e_ms != e2e_eager_ms else "eager launches")
-                          + " of pinned-host H2D copies + the step + D2H of the output",
+                          + " of pinned-host H2D copies of q and the new K/V + the step, whose decode writes "
+                            "the output straight into a pinned host buffer (the D2H bytes cross NVLink-C2C "
+                            "inside the step)",
                 "eager_value": e2e_eager_ms * 1e3},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,

@@ -551,3 +551,22 @@ def test_launch_modes_without_and_with_in_call_pdl(mode):
     env = dict(os.environ, PSK_PDL=mode, PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
     r = subprocess.run([sys.executable, "-c", _PDL_CHILD, root], env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("latent", [False, True])
+def test_decode_writes_into_pinned_host_output(latent):
+    """The decode's output buffer may be pinned host memory (written over NVLink-C2C by the
+    kernels, as the end-to-end benchmark does): the bytes equal those of a device output."""
+    if latent:
+        w = _custom_mla([64 * 60 + 5, 64 * 31, 64 * 3 + 1], [9, 7, 3])
+    else:
+        w = _custom([16 * 300 + 5, 16 * 77, 5000, 17], [40, 9, 30, 2])
+    cache = upload(w)
+    q = dev_queries(w)
+    sel = cache.score_select(q, dev_budgets(w))
+    out_dev = cache.sparse_decode(q, sel)
+    out_host = torch.full(out_dev.shape, float("nan"), dtype=out_dev.dtype).pin_memory()
+    cache.sparse_decode(q, sel, out=out_host)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    assert torch.equal(out_dev.cpu(), out_host)
