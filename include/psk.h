@@ -108,6 +108,12 @@ enum psk_status {
  * latent = 1 selects the MLA form: num_kv_heads = 1, the cache holds one latent vector per
  * token (k_cache), the value is its first v_head_dim elements and v_cache must be NULL.
  *
+ * Selection limit: a sequence longer than one selection chunk (4096, 8192 or 16384 pages) is
+ * selected chunk by chunk and the chunks' winners are merged by one CTA holding at most 8192
+ * candidates, so score / select calls need some chunk c in {4096, 8192, 16384} with
+ * ceil(max_pages / c) = 1 or ceil(max_pages / c) * min(b_max - 1, c) <= 8192 (e.g. max_pages =
+ * 65536 allows b_max up to 2049); otherwise they return PSK_ERR_UNSUPPORTED (size query: 0).
+ *
  * Built shapes (anything else returns PSK_ERR_UNSUPPORTED and a workspace size of 0):
  *   GQA: v_head_dim = head_dim; page_size 16, 32, 48 or 64; num_kv_heads a divisor or a
  *        multiple of 8; PSK_BF16 with head_dim 64 or 128 and group size

@@ -134,3 +134,35 @@ def test_select_params_host_checks(lib):
     # one workspace covers the per-query-head form too
     big = psk.Layout(2, 32, 8, 128, 128, 16, 100, 50)
     assert psk.score_select_workspace_size(big, 10) > 0 and psk.sparse_decode_workspace_size(big, 10) > 0
+
+
+def test_workspace_sizes_cover_every_form(lib):
+    """Host planning only: for a spread of layouts each call's workspace size is positive, the
+    combined size covers all of them, and a GQA layout's score / decode sizes also cover its
+    per-query-head form (one workspace serves both)."""
+    import page_sparse_kv_gb300 as psk
+    cases = [  # batch, H_q, H_kv, D, page, num_blocks, max_pages, dtype
+        (64, 32, 8, 128, 16, 150000, 4096, psk.PSK_BF16),
+        (1, 32, 8, 128, 16, 70000, 65536, psk.PSK_BF16),
+        (3, 16, 8, 64, 32, 500, 200, psk.PSK_BF16),
+        (5, 8, 8, 128, 64, 900, 300, psk.PSK_BF16),
+        (2, 4, 1, 64, 16, 300, 100, psk.PSK_F32),
+        (7, 64, 16, 128, 48, 2000, 333, psk.PSK_BF16),
+    ]
+    for B, Hq, Hkv, D, ps, nb, mp, dt in cases:
+        L = psk.Layout(B, Hq, Hkv, D, D, ps, nb, mp, dtype=dt)
+        V = psk.Layout(B, Hq, Hq, D, D, ps, nb, mp, dtype=dt)  # the per-query-head view's shape
+        for b in (2, 5, 128, min(mp, 2048)):
+            sizes = [psk.append_workspace_size(L), psk.score_select_workspace_size(L, b),
+                     psk.sparse_decode_workspace_size(L, b), psk.dense_decode_workspace_size(L)]
+            assert min(sizes) > 0, (L, b, sizes)
+            assert psk.workspace_size(L, b) == max(sizes)
+            assert psk.score_select_workspace_size(L, b) >= psk.score_select_workspace_size(V, b)
+            assert psk.sparse_decode_workspace_size(L, b) >= psk.sparse_decode_workspace_size(V, b)
+    # the selection limit: 65536 pages allow b_max 2049 (4 chunks of 16384 x 2048 winners = 8192),
+    # not 2050
+    L = psk.Layout(1, 32, 8, 128, 128, 16, 70000, 65536)
+    assert psk.score_select_workspace_size(L, 2049) > 0 and psk.score_select_workspace_size(L, 2050) == 0
+    # the latent form has its own sizes and no per-query-head form
+    M = psk.Layout(16, 128, 1, 576, 512, 64, 40000, 2048, latent=1)
+    assert psk.score_select_workspace_size(M, 103) > 0 and psk.sparse_decode_workspace_size(M, 103) > 0
