@@ -35,9 +35,14 @@
  *     "How it works", Sparse decode; AMASS (amass-kv) PyPI page, introduction.
  *
  * Conventions for every call
- *   - All tensor pointers are DEVICE pointers to contiguous memory in the layouts stated,
- *     16-byte aligned. Index tensors are int32. q, k_new, v_new, caches, summaries and out
- *     share the storage type `layout->dtype` (PSK_BF16 or PSK_F32); arithmetic is fp32.
+ *   - All tensor pointers address contiguous memory in the layouts stated, 16-byte aligned.
+ *     k_cache, summaries, the workspace, v_cache (unless PSK_DECODE_V_HOST) and the latent
+ *     form's q are read by TMA / bulk copies or atomics and must be device memory; the other
+ *     buffers (q, k_new, v_new, block_table, seq_lens, budgets, selected, scores_out, out)
+ *     may also be host memory the GPU addresses directly (pinned, under unified addressing),
+ *     e.g. an output written straight to the host. Index tensors are int32. q, k_new, v_new,
+ *     caches, summaries and out share the storage type `layout->dtype` (PSK_BF16 or
+ *     PSK_F32); arithmetic is fp32.
  *   - The caller owns every buffer. The library allocates nothing, frees nothing and
  *     keeps no state between calls apart from what it writes into the caller's buffers.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
@@ -50,7 +55,7 @@
  *   - Return value: PSK_OK or a psk_status code. PSK_ERR_CUDA reports a launch error.
  *   - Device-side violations that the host cannot see (a block id outside
  *     [0, num_blocks), a sequence longer than max_pages pages, a bad selected id, a
- *     budget below 2 with more than one page) set a sticky bit in the workspace status
+ *     budget below the always-kept page count) set a sticky bit in the workspace status
  *     word and skip the affected unit (its selected row is written as -1, its output
  *     rows as zeros); read it with psk_get_device_status. Nothing traps, asserts or waits.
  *   - Workspace: every call takes a caller-allocated workspace of at least the size the
@@ -164,7 +169,7 @@ int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, con
  *   score[i,h,p] = scale * max_{g in group(h)} sum_d max(q[i,g,d]*kmin[p,h,d], q[i,g,d]*kmax[p,h,d])
  * with the summaries of block block_table[i][p]. Selected pages: the sink 0 and the tail
  * P_i - 1 always, plus the min(b_i, P_i) - |{0, P_i - 1}| highest-scoring other pages, ties
- * to the lower page index. b_i = budgets[i] (device int32 [batch], 2 <= b_i <= b_max, or any
+ * to the lower page index. b_i = budgets[i] (int32 [batch], 2 <= b_i <= b_max, or any
  * 1 <= b_i <= b_max when P_i == 1).
  *
  *   selected  [batch, num_kv_heads, b_max] int32 out: ascending logical page ids, padded
