@@ -13,7 +13,7 @@ import math
 
 import torch
 
-from . import (PSK_BF16, PSK_F32, Layout, dense_paged_decode, kv_append_and_summarize, make_workspace,
+from . import (PSK_F32, Layout, dense_paged_decode, kv_append_and_summarize, make_workspace,
                page_score_select, sparse_paged_decode)
 
 
