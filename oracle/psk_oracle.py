@@ -257,6 +257,15 @@ def budget_for(P: int, *, fraction: float | None = None, pages: int | None = Non
 # ----------------------------------------------------------------------------------
 # S4: exact softmax attention over selected tokens
 # ----------------------------------------------------------------------------------
+def latent_values(keys: np.ndarray, v_head_dim: int) -> np.ndarray:
+    """Values of a latent (MLA) cache: the first v_head_dim dims of each token's latent key
+    (DeepSeek-shaped latent attention: one 576-dim latent per token, of which the first 512 are
+    the value). keys [T, 1, D] stored -> [T, 1, v_head_dim], the same stored elements."""
+    if not (0 < v_head_dim <= keys.shape[2]):
+        raise ValueError("0 < v_head_dim <= head_dim")
+    return keys[:, :, :v_head_dim]
+
+
 def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
     """out = softmax(scale * k q) v for one query vector; q [D], k [n, D], v [n, D_v], float64."""
     logits = scale * (k @ q)

@@ -104,7 +104,7 @@ def w_keys(w, i, n):
 
 
 def w_vals(w, i, n):
-    base = w.values(i)
+    base = O.latent_values(w.keys(i), w.D_v) if w.latent else w.values(i)
     extra = _APPENDED.get((id(w), i, "v"))
     return base if extra is None else np.concatenate([base, np.stack(extra)])[:n]
 

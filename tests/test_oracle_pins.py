@@ -336,6 +336,27 @@ def test_budget_modes():
             O.budget_for(10, **bad)
 
 
+# ------------------------------------------------------------------ latent values
+def test_latent_values_are_the_key_prefix_and_match_the_inputs():
+    """The latent cache's value is the first D_v dims of the key: the oracle's reading, the
+    synthetic latent workload's values, and one attention check where a value column taken from
+    beyond D_v would change the output."""
+    w = W.reduced(5)
+    keys = w.keys(0)
+    v = O.latent_values(keys, w.D_v)
+    assert v.shape == (keys.shape[0], 1, w.D_v) and np.array_equal(v, keys[:, :, :w.D_v])
+    assert np.array_equal(v, w.values(0))
+    q = w.queries()[0]
+    n = int(w.seq_lens[0])
+    P = -(-n // w.page_size)
+    a = O.attend_pages(q, keys, v, n, w.page_size, [list(range(P))], w.dtype, 0.05)
+    shifted = keys[:, :, keys.shape[2] - w.D_v:]
+    b = O.attend_pages(q, keys, shifted, n, w.page_size, [list(range(P))], w.dtype, 0.05)
+    assert not np.allclose(a, b)
+    with pytest.raises(ValueError):
+        O.latent_values(keys, keys.shape[2] + 1)
+
+
 # ------------------------------------------------------------------ per-query-head selection
 @pytest.mark.parametrize("seed", [0, 1])
 def test_per_query_head_bound_tight_on_single_token_pages_and_dominating(seed):
