@@ -13,11 +13,26 @@
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import oracle as O
 
 NEAR_TIE_REL = 1e-6
+
+# Every selection comparison of the session: units compared, and the near ties accepted at the
+# cutoff with where they occurred (the test id and the differing pages with their oracle scores
+# relative to the cutoff). tests/conftest.py prints the tally in the terminal summary.
+SELECTION_LOG = {"units": 0, "near_ties": []}
+
+
+def _log(near: bool, diff=(), scores=None, cut=None):
+    SELECTION_LOG["units"] += 1
+    if near:
+        where = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        rel = [float(abs(scores[p] - cut) / abs(cut)) if cut else 0.0 for p in sorted(diff)]
+        SELECTION_LOG["near_ties"].append({"test": where, "pages": sorted(int(p) for p in diff), "rel_to_cutoff": rel})
 BF16_MAX_ABS, BF16_MEAN_ABS = 2e-2, 2e-3
 F32_ROW_REL = 1e-5
 
@@ -30,6 +45,7 @@ def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int, sink
     got = [int(x) for x in gpu_row if x >= 0]
     pad_ok = all(x < 0 for x in gpu_row[len(got):])
     if got == ref and pad_ok:
+        _log(False)
         return True, False, got, ref
     if len(got) != len(ref) or not pad_ok or got != sorted(set(got)):
         return False, False, got, ref
@@ -39,6 +55,8 @@ def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int, sink
         return False, False, got, ref
     near = all(abs(scores[p] - cut) <= NEAR_TIE_REL * abs(cut) for p in diff)
     forced_ok = set(O.forced_pages(len(scores), sink_pages, window_pages)) <= set(got)
+    if near and forced_ok:
+        _log(True, diff, scores, cut)
     return (near and forced_ok), near, got, ref
 
 

@@ -13,7 +13,8 @@ import oracle.psk_oracle as OP
 import test_oracle_pins as PINS
 
 ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention",
-                                             "forced_pages", "retained_count", "quest_scores_per_query_head")}
+                                             "forced_pages", "retained_count", "quest_scores_per_query_head",
+                                             "cutoff_score")}
 
 
 @pytest.fixture
@@ -92,6 +93,16 @@ def _attention_unscaled(q, k, v, scale):  # logits without the scale
     return ORIG["softmax_attention"](q, k, v, 1.0)
 
 
+def _cutoff_one_too_far(scores, budget, sink_pages=1, window_pages=1):  # the k_free-th ranked page, one past the cut
+    P = len(scores)
+    forced = O.forced_pages(P, sink_pages, window_pages)
+    k_free = min(budget, P) - len(forced)
+    if min(budget, P) >= P or k_free <= 0:
+        return None
+    ranked = sorted((p for p in range(P) if p not in forced), key=lambda p: (-float(scores[p]), p))
+    return float(scores[ranked[min(k_free, len(ranked) - 1)]])
+
+
 # ---- each one is caught -------------------------------------------------------------------
 def test_dropped_kmin_term_is_caught(plant):
     plant("quest_scores", _quest_kmax_only)
@@ -146,3 +157,13 @@ def test_fraction_rounded_to_nearest_is_caught(plant, golden_dir):
 def test_per_query_head_wrong_kv_head_is_caught(plant):
     plant("quest_scores_per_query_head", _per_query_head_wrong_kv_head)
     _fails(PINS.test_per_query_head_bound_tight_on_single_token_pages_and_dominating, 0)
+
+
+def test_cutoff_one_place_too_far_is_caught(plant, golden_dir):
+    plant("cutoff_score", _cutoff_one_too_far)
+    import json
+    import os
+    with open(os.path.join(golden_dir, "worked_example.json")) as f:
+        ex = json.load(f)
+    _fails(PINS.test_golden_cutoff_score, ex)
+    _fails(PINS.test_cutoff_score_is_the_weakest_winner_by_enumeration, 8)

@@ -48,6 +48,40 @@ def test_golden_scores_and_selection(ex):
         assert O.select_pages(s[0], int(b)) == sel
 
 
+def test_golden_cutoff_score(ex):
+    """The cutoff (the score of the last page chosen by score), hand-derived on the worked
+    example (ties included) and on a case with distinct scores."""
+    s = np.asarray(ex["score_unscaled"], dtype=np.float64)
+    for b, cut in ex["cutoff_by_budget_unscaled"].items():
+        assert O.cutoff_score(s, int(b)) == cut, f"budget {b}"
+    s = np.asarray(ex["distinct_scores_unscaled"], dtype=np.float64)
+    for b, cut in ex["distinct_cutoff_by_budget"].items():
+        assert O.cutoff_score(s, int(b)) == cut, f"budget {b}"
+
+
+@pytest.mark.parametrize("P", [3, 5, 8, 10])
+def test_cutoff_score_is_the_weakest_winner_by_enumeration(P):
+    """Against subset enumeration: the cutoff is the lowest score among the pages of the unique
+    winning subset (every member beats every non-member under (score desc, index asc)), and
+    None exactly when no page is chosen by score. Sink / window sets of several sizes."""
+    rng = np.random.default_rng(100 + P)
+    for trial in range(4):
+        scores = rng.integers(-3, 4, size=P).astype(np.float64) if trial < 3 else rng.standard_normal(P)
+        for S, Wn in ((1, 1), (0, 1), (2, 2)):
+            forced = sorted(set(range(min(S, P))) | set(range(max(0, P - Wn), P)))
+            for b in range(len(forced), P + 2):
+                k = min(b, P) - len(forced)
+                others = [p for p in range(P) if p not in forced]
+                winners = [Sub for Sub in itertools.combinations(others, k)
+                           if all((scores[x], -x) > (scores[y], -y) for x in Sub for y in others if y not in Sub)]
+                assert len(winners) == 1
+                got = O.cutoff_score(scores, b, S, Wn)
+                if k <= 0 or min(b, P) >= P:
+                    assert got is None
+                else:
+                    assert got == min(scores[x] for x in winners[0])
+
+
 def test_golden_attention(ex):
     keys = _f32(ex["keys"])[:, None, :]
     vals = _f32(ex["values"])[:, None, :]
