@@ -298,13 +298,16 @@ int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const vo
  * Stage 4 without a workspace (no counterpart in the pages: an addition for callers that
  * cannot allocate device memory). Some host programs own every byte of device memory
  * through their own allocator and pass a plugin only its inputs and outputs, or run a loop
- * that must never call cudaMalloc. This call computes exactly what psk_sparse_paged_decode
- * computes, but keeps its split partials in a 32 MiB device array inside the library
- * (allocated once per GPU when the library loads, held until exit); it allocates nothing.
+ * that must never call cudaMalloc. This call computes what psk_sparse_paged_decode computes
+ * for the GQA form (rows per (sequence, KV head), values in device memory; no _ex flags;
+ * latent layouts return PSK_ERR_UNSUPPORTED), but keeps its split partials in a 32 MiB
+ * device array inside the library (one per GPU, held until exit); it allocates nothing.
  *   - Returns PSK_ERR_WORKSPACE when the partials (the size psk_sparse_decode_workspace_size
  *     reports) exceed 32 MiB.
- *   - The first call on each device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *   - Each call looks up the array's address in the current context (cudaGetSymbolAddress).
+ *     With lazy module loading (the CUDA default) the first call on each device loads the
+ *     array, which may synchronise: make one warm-up call before any stream capture or
+ *     latency-critical loop, or set CUDA_MODULE_LOADING=EAGER.
  *   - All calls share the one array: calls that overlap on the GPU race and must be
  *     serialised by the caller. Each call zeroes the array's header before use.
  *   - Device-side input violations are not reported (the status word is internal).
@@ -313,6 +316,18 @@ int psk_sparse_paged_decode_noalloc(const psk_layout *layout, const void *q, con
                                     const void *v_cache, const int32_t *block_table,
                                     const int32_t *seq_lens, const int32_t *selected, int32_t b_max,
                                     float scale, void *out, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Self-test of the bounded waits (failure detection; no counterpart in the pages). Every
+ * streaming kernel waits for its asynchronous copies on mbarriers with a bounded number of
+ * polls and, if a copy never lands, sets PSK_DEV_TIMEOUT and returns instead of hanging. This
+ * call runs that same wait, with spin_limit polls (1 .. 4194304, the kernels' own limit), on a
+ * phase that cannot complete (an expected transaction count with no copy issued), so the
+ * timeout path can be observed: afterwards psk_get_device_status reports PSK_DEV_TIMEOUT and
+ * the context stays usable (nothing was in flight). Asynchronous on `stream`.
+ * --------------------------------------------------------------------------------------- */
+int psk_selftest_bounded_wait(void *workspace, size_t workspace_bytes, uint32_t spin_limit,
+                              psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Workspace sizes (bytes). Return 0 when the layout is invalid or unsupported.

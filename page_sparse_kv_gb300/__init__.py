@@ -25,7 +25,7 @@ EXPORTS = [
     "psk_page_select", "psk_sparse_paged_decode",
     "psk_sparse_paged_decode_ex", "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
-    "psk_clear_device_status", "psk_status_string", "psk_version",
+    "psk_clear_device_status", "psk_status_string", "psk_version", "psk_selftest_bounded_wait",
 ]
 
 
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
             "psk_clear_device_status": (ctypes.c_int, [P, P]),
             "psk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "psk_version": (ctypes.c_int, []),
+            "psk_selftest_bounded_wait": (ctypes.c_int, [P, Z, ctypes.c_uint32, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -285,6 +286,13 @@ def get_device_status(workspace, stream=None) -> int:
 
 def clear_device_status(workspace, stream=None):
     _check("psk_clear_device_status", lib().psk_clear_device_status(_ptr(workspace), _stream(stream)))
+
+
+def selftest_bounded_wait(workspace, spin_limit: int, stream=None):
+    """Runs the kernels' bounded wait on a phase that never completes (see psk.h): afterwards
+    the workspace status word holds DEV_TIMEOUT."""
+    _check("psk_selftest_bounded_wait", lib().psk_selftest_bounded_wait(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(spin_limit), _stream(stream)))
 
 
 def version() -> int:

@@ -11,16 +11,6 @@
 
 using namespace psk;
 
-namespace psk {
-bool pdl_enabled(bool first_of_call) {
-  static const int mode = [] {
-    const char *env = std::getenv("PSK_PDL");
-    return env ? std::atoi(env) : 1;
-  }();
-  return mode == 1 || (mode == 2 && !first_of_call);
-}
-}  // namespace psk
-
 namespace {
 
 int elem_bytes(int dtype) { return dtype == PSK_F32 ? 4 : 2; }

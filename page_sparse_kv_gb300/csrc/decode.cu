@@ -7,9 +7,10 @@
 // Work: one CTA of NW warps per (split of `sw` list entries, KV head, sequence). The group's G
 // query heads share every K/V element loaded, so each element is converted once and used G
 // times. A page is cut into 16-token tiles; warp w takes tiles w, w + NW, ... of the split and
-// keeps its own (m, l, O) state. Tiles are staged into a per-warp ring of NST shared-memory
-// stages with 16-byte cp.async (rows past seq_len are zero-filled and never read), NST - 1
-// tiles in flight per warp.
+// keeps its own (m, l, O) state. Lane 0 of each warp stages the tiles into the warp's ring of
+// NST shared-memory stages with 3-D TMA copies (K and V, box D x 1 head x 16 rows, L2
+// evict-first), completing on the stage's mbarrier, NST - 1 tiles in flight per warp. Rows past
+// seq_len may hold anything: their logits are masked to -inf and P.V stops at the last valid row.
 //
 // Per tile and warp: lane = (tq = lane / 8, dg = lane % 8). QK: the lane owns the 16-byte
 // chunks dg, dg + 8, ... of each K row and the matching q slices (scaled by scale * log2(e) so
@@ -25,8 +26,6 @@
 // write an empty partial first); the CTA holding the last ticket (no waiting) merges the
 // unit's partials by log-sum-exp with all its threads and writes the G output rows.
 #include <algorithm>
-#include <cstdlib>
-#include <string>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
@@ -802,40 +801,30 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv_cache, rows, 16) ||
       !encode_cache_map(&tmV, a.v_host ? a.k_cache : a.v_cache, dt, D, a.H_kv_cache, rows, 16))
     return cudaErrorInvalidValue;
-  cudaError_t e;
   if (a.v_host) {  // the value tier: sparse split layout only
     if constexpr (sizeof(T) == 2 && D == 128) {
       if (a.flat || !a.selected) return cudaErrorInvalidValue;
-      auto kfn = decode_split_kernel<T, D, G, NW, NST, true>;
-      e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
-      if (e != cudaSuccess) return e;
       dim3 grid(a.B * a.H_kv, a.n_items_max);
-      return launch_kernel(true, kfn, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
+      return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, true>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
     } else {
       return cudaErrorInvalidValue;
     }
   }
   if (!a.flat) {
-    auto kfn = decode_split_kernel<T, D, G, NW, NST, false>;
-    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TR::SMEM);
-    if (e != cudaSuccess) return e;
     dim3 grid(a.B * a.H_kv, a.n_items_max);
-    return launch_kernel(true, kfn, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
+    return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, false>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
   }
   const int U = a.B * a.H_kv;
+  cudaError_t e;
   if (a.selected) {
     e = launch_kernel(true, decode_counts_kernel, (U + 7) / 8, 256, 0, s, a);
     if (e != cudaSuccess) return e;
   }
   auto kfn = decode_flat_kernel<T, D, G, NW, NST>;
   const size_t smem = TR::SMEM + (size_t)(U + 1) * 4;
-  e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, NW * 32, smem)) != cudaSuccess) return e;
-  const int ctas = std::max(1, std::min(kFlatMaxCtas, sms * std::max(1, per_sm)));
+  int per_sm = 0;
+  if ((e = kernel_setup(reinterpret_cast<const void *>(kfn), NW * 32, smem, &per_sm)) != cudaSuccess) return e;
+  const int ctas = std::max(1, std::min(kFlatMaxCtas, sm_count() * std::max(1, per_sm)));
   return launch_kernel(!a.selected, kfn, ctas, NW * 32, smem, s, a, tmK, tmV);
 }
 }  // namespace
@@ -848,8 +837,9 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
   // the batched workload (the flat one adds a count pass over the selected rows and more
   // partials, and short budget lists leave its shares little to balance).
   bool flat = dense && units <= kFlatMaxUnits;
-  if (const char *env = std::getenv("PSK_DECODE_LAYOUT"))  // tuning override: "split" or "flat"
-    flat = std::string(env) == "split" ? false : (std::string(env) == "flat" ? units <= kFlatMaxUnits : flat);
+  const Tuning &tu = tuning();
+  if (tu.decode_layout == 1) flat = false;                          // tuning override: "split"
+  if (tu.decode_layout == 2) flat = units <= kFlatMaxUnits;         // tuning override: "flat"
   size_t slots;
   if (flat) {
     plan->sw = kSwMax;
@@ -858,20 +848,18 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
     slots = (size_t)kFlatMaxCtas + (size_t)units;
   } else {
     // 64 list entries per CTA (measured best on the batched workload); fewer (down to 8) while
-    // the grid would not fill the GPU (152 SMs x 2 CTAs) a few times over, more when a unit
+    // the grid would not fill the GPU (all SMs x 2 CTAs) a few times over, more when a unit
     // would need over kMaxItems partials
     int sw = 64;
-    while (sw > 8 && units * ((entries + sw - 1) / sw) < 4LL * 152 * 2) sw /= 2;  // 8: measured best at B = 1
-    if (const char *env = std::getenv("PSK_DECODE_SPLIT")) {  // tuning override: entries per CTA
-      const int v = std::atoi(env);
-      if (v >= 1 && v <= kSwMax) sw = v;
-    }
+    const long long fill = 4LL * sm_count() * 2;
+    while (sw > 8 && units * ((entries + sw - 1) / sw) < fill) sw /= 2;  // 8: measured best at B = 1
+    if (tu.decode_split >= 1 && tu.decode_split <= kSwMax) sw = tu.decode_split;  // tuning override: entries per CTA
     while (sw < kSwMax && (entries + sw - 1) / sw > kMaxItems) sw *= 2;
     plan->sw = sw;
     plan->n_items_max = (entries + sw - 1) / sw;
     plan->taper = 0;
     // sparse lists longer than one split: tapered splits when they stay few enough to merge
-    if (!dense && entries > sw && !std::getenv("PSK_DECODE_NO_TAPER")) {
+    if (!dense && entries > sw && !tu.decode_no_taper) {
       int n = 0;
       while (split_off(n, sw, 1) < entries) ++n;
       if (n <= kMaxItems) {

@@ -18,13 +18,14 @@
 // heads x 256 value dims fills 256 of the 512 tensor-memory columns, hence the split of D_v
 // across two CTAs (each computes S itself). Q dims 0..383 live in tensor memory as the A
 // operand of S = Q K^T (192 columns), dims 384..575 in shared memory (TMA, 128-byte swizzle);
-// K tiles of 32 tokens x 576 stream through a 4-stage TMA ring. Per tile: S (M = 128 heads,
-// N = 32 tokens) into one of two tensor-memory buffers; each softmax thread owns one head's
-// row: online softmax in fp32 (log2 domain), P written as bf16 to shared memory (64-byte
-// swizzle, two buffers); O += P V (N = 256 value dims, V read MN-major straight out of the K
-// tile) accumulates in tensor memory. A fifth warp issues the TMA copies and the MMAs, S of the
-// next tile ahead of P.V of this one. Splits are merged by log-sum-exp by the last CTA of each
-// (sequence, half).
+// K tiles of 64 tokens x 576 (two 32-row TMA boxes per 64-dim block) stream through a 2-stage
+// ring in two parts with their own full / empty mbarriers. Per tile: S (M = 128 heads, N = 64
+// tokens) into tensor memory; each softmax thread owns one head's row: online softmax in fp32
+// (log2 domain, lazy rescale), P written as bf16 to shared memory (128-byte swizzle); O += P V
+// (N = 256 value dims, V read MN-major straight out of the K tile) accumulates in tensor
+// memory. Six warps: four softmax warps (one thread per head), one warp whose lane 0 issues the
+// MMAs (S of the next tile ahead of P.V of this one) and one whose lane 0 issues the TMA copies.
+// Splits are merged by log-sum-exp by the last CTA of each (sequence, half).
 #include <algorithm>
 
 #include "psk_common.cuh"
@@ -663,8 +664,6 @@ cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaSt
   cudaError_t e = launch_kernel(true, mla_qsplit_kernel, (n + 255) / 256, 256, 0, s,
                                 reinterpret_cast<const uint16_t *>(a.q), qsplit, rows);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(mla_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem);
-  if (e != cudaSuccess) return e;
   dim3 grid((a.max_pages + 127) / 128, a.B);
   e = launch_kernel(false, mla_score_kernel, grid, 128, kScSmem, s, a, (const uint16_t *)qsplit);
   if (e != cudaSuccess || !(stages & kStageSelect)) return e;
@@ -673,6 +672,7 @@ cudaError_t launch_mla_score_select(const ScoreArgs &a, uint16_t *qsplit, cudaSt
 
 bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   const long long units = (long long)L.batch * 2;
+  const long long sms = sm_count();
   // One CTA per SM (shared memory). Pick the split width that minimises
   //   waves * (pages per split + ~2 pages of fixed per-CTA cost) + ~0.5 page per split merged.
   int sw = std::max(1, std::min(entries, kMlaMaxSw));
@@ -681,7 +681,7 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
     const int w = (std::max(entries, 1) + items - 1) / items;
     if (w > kMlaMaxSw) continue;
     const int n = (std::max(entries, 1) + w - 1) / w;
-    const long long waves = (units * n + 151) / 152;
+    const long long waves = (units * n + sms - 1) / sms;
     const double cost = (double)waves * (w + 2.0) + 0.5 * n;
     if (cost < best - 1e-9) {
       best = cost;
@@ -708,8 +708,6 @@ cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
   if (!encode_matrix_map_sw128(&tmQ, a.q, kD, (long long)a.B * kHeads, 64, kHeads) ||
       !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kHalf))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
-  if (e != cudaSuccess) return e;
   dim3 grid(a.n_items_max, 2, a.B);
   return launch_kernel(true, mla_decode_kernel, grid, kDecThreads, kDecSmem, s, a, tmQ, tmK);
 }

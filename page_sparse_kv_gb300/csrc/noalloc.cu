@@ -4,45 +4,42 @@
 // real-time loop that must never enter cudaMalloc and its possible device synchronisation). For
 // them the split-K partials live in a fixed, file-scope device array instead of a caller buffer.
 //
-// The array is kNoAllocScratchBytes (32 MiB) per GPU that loads the library, held until the
-// process exits. Problems whose partials do not fit are rejected with PSK_ERR_WORKSPACE.
+// The array is kNoAllocScratchBytes (32 MiB) per GPU that loads it, held until the process
+// exits. Problems whose partials do not fit are rejected with PSK_ERR_WORKSPACE. Only the GQA
+// split decode is served (per-KV-head rows, values in device memory); latent caches return
+// PSK_ERR_UNSUPPORTED.
 //
 // Host code cannot use the array's name as a device address (on the host it is only a stand-in
-// symbol), so the first call on each device, with that device current, looks the address up with
-// cudaGetSymbolAddress and caches it; that first call must therefore happen before any stream
-// capture. Every call shares the one array and keeps the previous call's contents: the header
-// (status word and merge tickets) is zeroed at the start of each call, and calls that overlap on
-// the GPU (different streams, or different host threads) race on it and must be serialised by the
-// caller. Device-side input violations are flagged in this internal header, which is not
-// reported back; validate inputs with the workspace entry point if that matters.
+// symbol). Each call, with the caller's device current, looks the address up with
+// cudaGetSymbolAddress in the current context, so a device reset or a context the caller made
+// current through the driver API never leaves a stale address behind. With lazy module loading
+// (the CUDA default) the first call on each device loads the module that holds the array, which
+// may synchronise: make one warm-up call before any stream capture or latency-critical loop (or
+// set CUDA_MODULE_LOADING=EAGER). Every call shares the one array and keeps the previous call's
+// contents: the header (status word and merge tickets) is zeroed at the start of each call, and
+// calls that overlap on the GPU (different streams, or different host threads) race on it and
+// must be serialised by the caller. Device-side input violations are flagged in this internal
+// header, which is not reported back; validate inputs with the workspace entry point if that
+// matters.
 //
 // No counterpart exists in the pages this library follows.
-#include <mutex>
-
 #include "psk_common.cuh"
 #include "psk_internal.h"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_psk_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array in the current context.
 int scratch_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PSK_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_psk_noalloc_scratch) != cudaSuccess || !p) return PSK_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_psk_noalloc_scratch) != cudaSuccess || !p) {
+    (void)cudaGetLastError();
+    return PSK_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return PSK_OK;
 }
 

@@ -44,10 +44,38 @@ __device__ __forceinline__ void pdl_begin() {
 // too unless PSK_PDL=2; PSK_PDL=0 launches every kernel in plain stream order.
 bool pdl_enabled(bool first_of_call);
 
+// Host-side facts the launchers need, each computed once per device and cached (they never
+// change for a device): its SM count, and per (kernel, threads, dynamic shared memory) the
+// opt-in shared-memory limit set on the kernel and its resident CTAs per SM.
+int sm_count();
+// Sets the kernel's dynamic shared-memory limit to at least `smem` (once per device) and, when
+// per_sm is given, returns its occupancy in CTAs per SM for `threads` threads.
+cudaError_t kernel_setup(const void *fn, int threads, size_t smem, int *per_sm = nullptr);
+// Drops the cached set-up of a kernel on the current device (after a launch failed, e.g. because
+// a device reset discarded the attribute), so the next kernel_setup sets it again.
+void kernel_forget(const void *fn);
+
+// Tuning overrides from the environment, read once per process: PSK_SCORE_TAIL (pages),
+// PSK_SCORE_TAIL_CHUNK, PSK_SCORE_PCHUNK, PSK_DECODE_LAYOUT ("split" / "flat"), PSK_DECODE_SPLIT
+// (list entries per CTA), PSK_DECODE_NO_TAPER. -1 / 0 = not set.
+struct Tuning {
+  long long score_tail = -1;
+  int score_tail_chunk = -1, score_pchunk = -1;
+  int decode_layout = 0;  // 0 default, 1 split, 2 flat
+  int decode_split = -1;
+  bool decode_no_taper = false;
+};
+const Tuning &tuning();
+
 // Launch with the programmatic-serialisation attribute (when enabled for this kind of launch).
+// The kernel's shared-memory limit is set (once per device, cached) before the launch; a launch
+// that fails drops that cache entry and is tried once more after setting it again.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(bool first_of_call, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t s, Args &&...args) {
+                          cudaStream_t s, const Args &...args) {
+  const void *fn = reinterpret_cast<const void *>(kernel);
+  cudaError_t e = kernel_setup(fn, (int)(block.x * block.y * block.z), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -58,7 +86,14 @@ cudaError_t launch_kernel(bool first_of_call, void (*kernel)(KArgs...), dim3 gri
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled(first_of_call) ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    kernel_forget(fn);
+    if (kernel_setup(fn, (int)(block.x * block.y * block.z), smem) == cudaSuccess)
+      e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  }
+  return e;
 }
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -187,15 +222,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
-// Bounded wait for the phase with parity `parity`: gives up after kMbarSpinLimit polls (each
-// poll may suspend the thread for a short hardware-defined time), sets PSK_DEV_TIMEOUT and
-// returns false, so a lost copy can never hang the GPU.
+// Bounded wait for the phase with parity `parity`: gives up after `limit` polls (each poll may
+// suspend the thread for a short hardware-defined time), sets PSK_DEV_TIMEOUT and returns false,
+// so a lost copy can never hang the GPU. Every kernel waits with kMbarSpinLimit polls; the
+// self-test entry point runs the same wait with a short limit on a phase that cannot complete.
 constexpr uint32_t kMbarSpinLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, void *ws) {
-  for (uint32_t it = 0; it < kMbarSpinLimit; ++it)
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, void *ws, uint32_t limit) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   set_status(ws, PSK_DEV_TIMEOUT);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, void *ws) {
+  return mbar_wait_limit(bar, parity, ws, kMbarSpinLimit);
 }
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16), completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

@@ -48,7 +48,8 @@ struct ScoreArgs {
   int stage_pages;        // pages per shared-memory stage of the score kernel
   int chunk;              // pages per selection CTA
   int n_chunks_max;
-  int k_cap;              // candidates kept per chunk = min(b_max - 2, chunk) (>= 1)
+  int k_cap;              // candidates kept per chunk = min(max(1, b_max - 1), chunk): with sink_pages = 0
+                          // only the tail page is always kept
   float scale;
   int sink, window;       // always-kept first (>= 0) / last (>= 1) pages
   int H_kv_cache;         // KV heads of the cache (H_kv above counts the units' heads)

@@ -16,7 +16,6 @@
 // kernel writes one 32-bit order key per page to the workspace (0 = an always-kept page, or a
 // flagged bad block), which the selection kernel reads.
 #include <algorithm>
-#include <cstdlib>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
@@ -308,25 +307,19 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   } else {
     if (a.kv_shift != 0) return cudaErrorInvalidValue;  // the per-query-head view has G = 1
   }
-  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, k1_smem);
-  if (e != cudaSuccess) return e;
   // Tail region: about kTailWaves waves of short CTAs over the sequences' last pages. A grid of
   // equal chunks ends with its last wave draining for one whole CTA lifetime at falling
   // occupancy; short CTAs last make that drain short.
   ScoreArgs b = a;
   {
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, k1_smem)) != cudaSuccess) return e;
-    b.tail_chunk = kTailChunk;
+    int per_sm = 0;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kfn), kThreads, k1_smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    const Tuning &tu = tuning();
+    b.tail_chunk = tu.score_tail_chunk > 0 ? tu.score_tail_chunk : kTailChunk;
     const long long rows = (long long)a.B * (a.H_kv / hpc);
-    long long tail = ((long long)sms * std::max(1, per_sm) * kTailChunk * kTailWaves + rows - 1) / rows;
-    if (const char *env = std::getenv("PSK_SCORE_TAIL")) tail = std::atoi(env);  // tuning override: pages
-    if (const char *env = std::getenv("PSK_SCORE_TAIL_CHUNK")) {  // tuning override: pages per tail CTA
-      const int v = std::atoi(env);
-      if (v >= 1 && v <= 4096) b.tail_chunk = v;
-    }
+    long long tail = ((long long)sm_count() * std::max(1, per_sm) * kTailChunk * kTailWaves + rows - 1) / rows;
+    if (tu.score_tail >= 0) tail = tu.score_tail;  // tuning override: pages
     tail = (tail + b.tail_chunk - 1) / b.tail_chunk * b.tail_chunk;
     b.tail_pages = (int)std::max(0LL, std::min(tail, (long long)a.max_pages));
     b.tail_chunks = (b.tail_pages + b.tail_chunk - 1) / b.tail_chunk;
@@ -334,7 +327,7 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   }
   const long long n_ctas = (long long)(b.body_chunks + b.tail_chunks) * b.B * (b.H_kv / hpc);
   if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
-  e = launch_kernel(true, kfn, (unsigned)n_ctas, kThreads, k1_smem, s, b);
+  const cudaError_t e = launch_kernel(true, kfn, (unsigned)n_ctas, kThreads, k1_smem, s, b);
   if (e != cudaSuccess || !(stages & kStageSelect)) return e;
   return launch_page_select(b, s);
 }
@@ -358,16 +351,14 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
   plan->k_cap = std::min(kfree_max, chunk);
   // pages per streaming CTA of the body region: 64 (measured best on the batched workload, 48,
   // 96 and 128 slower); fewer only while the body would not fill one resident wave (four CTAs on
-  // each of 152 SMs), since the tail region supplies the short CTAs at the end (one 1M-token
-  // sequence: 64 pages 62.9 us against 66.2 us at 32)
+  // each SM), since the tail region supplies the short CTAs at the end (one 1M-token sequence:
+  // 64 pages 62.9 us against 66.2 us at 32)
   const long long head_groups = L.num_kv_heads > kWarps ? L.num_kv_heads / kWarps : 1;
   int pchunk = 64;
-  while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < 4 * 152)
+  const long long wave = 4LL * sm_count();
+  while (pchunk > 16 && (long long)L.batch * head_groups * ((L.max_pages + pchunk - 1) / pchunk) < wave)
     pchunk /= 2;
-  if (const char *env = std::getenv("PSK_SCORE_PCHUNK")) {  // tuning override: pages per score CTA
-    const int v = std::atoi(env);
-    if (v >= 8 && v <= 4096) pchunk = v;
-  }
+  if (tuning().score_pchunk > 0) pchunk = tuning().score_pchunk;  // tuning override: pages per score CTA
   plan->pchunk = pchunk;
   {
     const int hpc = L.num_kv_heads < kWarps ? L.num_kv_heads : kWarps;

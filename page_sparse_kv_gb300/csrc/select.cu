@@ -225,15 +225,16 @@ __device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int pag
 }
 
 // Row of a unit with count < P selected pages: the first S pages, the `wrote` winners (written
-// by the caller at sel_row + S, all inside [S, P - W)), the last W pages, then -1 to b_max.
-// count < P implies S + W < P, so the two always-kept runs do not overlap.
-__device__ void write_row_ends(int32_t *sel_row, int P, int count, int wrote, int b_max, int S, int W) {
+// by the caller at sel_row + S, all inside [S, P - W)), the last W pages straight after them,
+// then -1 to b_max. count < P implies S + W < P, so the two always-kept runs do not overlap.
+// wrote < count - S - W happens only after a flagged bad block: the row is then shorter, and the
+// -1 padding still comes only at its end (the decode reads a row up to its first -1).
+__device__ void write_row_ends(int32_t *sel_row, int P, int wrote, int b_max, int S, int W) {
   const int tid = threadIdx.x;
   for (int x = tid; x < S; x += kSelThreads) sel_row[x] = x;
-  // fewer winners than free slots happens only after a flagged bad block: pad the gap
-  for (int x = S + wrote + tid; x < count - W; x += kSelThreads) sel_row[x] = -1;
-  for (int x = tid; x < W; x += kSelThreads) sel_row[count - W + x] = P - W + x;
-  for (int x = count + tid; x < b_max; x += kSelThreads) sel_row[x] = -1;
+  const int w0 = S + wrote;
+  for (int x = tid; x < W; x += kSelThreads) sel_row[w0 + x] = P - W + x;
+  for (int x = w0 + W + tid; x < b_max; x += kSelThreads) sel_row[x] = -1;
 }
 
 // Budget of a sequence of P pages (at least the always-kept count in the scalar modes);
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     if (!take_all) radix_select(keys, n, k_free, kmin, kmax, hist, sc, &thr, &need_eq);
     if (nch == 1) {
       wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + a.sink, sc);
-      write_row_ends(sel_row, P, count, wrote, a.b_max, a.sink, a.window);
+      write_row_ends(sel_row, P, wrote, a.b_max, a.sink, a.window);
       return;
     }
     const int slot = unit * a.n_chunks_max + c;
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     if (tid == 0) a.cand_count[slot] = wrote;
   } else {
     if (nch == 1) {
-      write_row_ends(sel_row, P, count, 0, a.b_max, a.sink, a.window);
+      write_row_ends(sel_row, P, 0, a.b_max, a.sink, a.window);
       return;
     }
     if (tid == 0) a.cand_count[unit * a.n_chunks_max + c] = 0;
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     }
     wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + a.sink, sc);
   }
-  write_row_ends(sel_row, P, count, wrote, a.b_max, a.sink, a.window);
+  write_row_ends(sel_row, P, wrote, a.b_max, a.sink, a.window);
 }
 
 }  // namespace
@@ -412,8 +413,6 @@ cudaError_t launch_page_select(const ScoreArgs &a, cudaStream_t s, bool first_of
   const size_t keys_bytes = (size_t)std::min(a.chunk, a.max_pages) * 4;
   const size_t merge_bytes = (size_t)kMergeCap * 8 + (size_t)(a.n_chunks_max + 1) * 4;  // keys, pages, offsets
   const size_t smem = a.n_chunks_max == 1 ? keys_bytes : std::max<size_t>(keys_bytes, merge_bytes);
-  cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   dim3 grid(a.H_kv, a.n_chunks_max, a.B);
   return launch_kernel(first_of_call, page_select_kernel, grid, kSelThreads, smem, s, a);
 }

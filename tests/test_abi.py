@@ -76,6 +76,11 @@ def test_host_checks_reject_before_launch(lib):
     rc = lib.psk_kv_append_and_summarize(ctypes.byref(L), None, None, P(16), P(16), 0, 0, P(16), P(16), P(16), P(16),
                                          P(16), 256, None)
     assert rc == 0
+    # the bounded-wait self-test: no workspace, a small one, or a poll limit outside 1 .. 2^22
+    assert lib.psk_selftest_bounded_wait(None, 256, 10, None) == 1
+    assert lib.psk_selftest_bounded_wait(P(256), 64, 10, None) == 3
+    assert lib.psk_selftest_bounded_wait(P(256), 256, 0, None) == 1
+    assert lib.psk_selftest_bounded_wait(P(256), 256, (1 << 22) + 1, None) == 1
 
 
 def test_select_params_host_checks(lib):

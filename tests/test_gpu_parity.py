@@ -446,6 +446,111 @@ def test_device_status_on_bad_block_table():
     assert psk.get_device_status(cache.ws) & psk.DEV_BAD_SELECTED
 
 
+def test_device_status_bad_budget():
+    """A per-sequence budget below the always-kept count (sink + tail) or above b_max: the select
+    kernel flags PSK_DEV_BAD_BUDGET and writes that sequence's rows as -1; the other sequences
+    are selected normally."""
+    w = _custom([16 * 20, 16 * 30 + 3, 16 * 12], [4, 4, 4], H_q=8, H_kv=2)
+    cache = upload(w)
+    q_np = w.queries()
+    q = to_torch(q_np, w.dtype).cuda()
+    for bad in (1, cache.b_max + 1):
+        psk.clear_device_status(cache.ws)
+        bud = torch.tensor([4, bad, 4], dtype=torch.int32, device="cuda")
+        sel = cache.score_select(q, bud)
+        torch.cuda.synchronize()
+        assert psk.get_device_status(cache.ws) == psk.DEV_BAD_BUDGET
+        sel_np = sel.cpu().numpy()
+        assert np.all(sel_np[1] == -1)
+        scale = 1.0 / math.sqrt(w.D)
+        for i in (0, 2):
+            kmin, kmax = _oracle_summaries(w, i)
+            s_ref = O.quest_scores(q_np[i], kmin, kmax, w.dtype, scale)
+            for h in range(w.H_kv):
+                assert compare_selection(sel_np[i, h], s_ref[h], 4)[0]
+    psk.clear_device_status(cache.ws)
+
+
+def test_device_status_bad_seq_len():
+    """seq_len 0, or more pages than a block-table row holds: score / select and decode flag
+    PSK_DEV_BAD_SEQLEN, the sequence's rows are -1 and its outputs zero; the other sequences'
+    outputs still match the oracle."""
+    w = _custom([16 * 20, 16 * 30 + 3], [5, 5], H_q=8, H_kv=2)
+    cache = upload(w)
+    q_np = w.queries()
+    q = to_torch(q_np, w.dtype).cuda()
+    scale = 1.0 / math.sqrt(w.D)
+    good_len = int(w.seq_lens[1])
+    for bad_len in (0, w.max_pages * w.page_size + 1):
+        psk.clear_device_status(cache.ws)
+        cache.seq_lens.copy_(torch.tensor([bad_len, good_len], dtype=torch.int32, device="cuda"))
+        sel = cache.score_select(q, dev_budgets(w))
+        out = cache.sparse_decode(q, sel)
+        dense = cache.dense_decode(q)
+        torch.cuda.synchronize()
+        assert psk.get_device_status(cache.ws) == psk.DEV_BAD_SEQLEN
+        sel_np = sel.cpu().numpy()
+        assert np.all(sel_np[0] == -1)
+        assert torch.all(out[0] == 0) and torch.all(dense[0] == 0)
+        kmin, kmax = _oracle_summaries(w, 1)
+        s_ref = O.quest_scores(q_np[1], kmin, kmax, w.dtype, scale)
+        use = []
+        for h in range(w.H_kv):
+            ok, _, got, _ = compare_selection(sel_np[1, h], s_ref[h], int(w.budgets[1]))
+            assert ok
+            use.append(got)
+        ref = O.attend_pages(q_np[1], w.keys(1), w.values(1), good_len, w.page_size, use, w.dtype, scale)
+        check_output(from_torch(out.float(), "f32")[1], ref, w.dtype)
+        # the sparse decode checks lengths on its own too: a valid row with a bad length
+        psk.clear_device_status(cache.ws)
+        cache.seq_lens.copy_(torch.tensor([int(w.seq_lens[0]), good_len], dtype=torch.int32, device="cuda"))
+        sel_ok = cache.score_select(q, dev_budgets(w))
+        cache.seq_lens.copy_(torch.tensor([bad_len, good_len], dtype=torch.int32, device="cuda"))
+        out2 = cache.sparse_decode(q, sel_ok)
+        torch.cuda.synchronize()
+        assert psk.get_device_status(cache.ws) == psk.DEV_BAD_SEQLEN
+        assert torch.all(out2[0] == 0)
+    cache.seq_lens.copy_(torch.from_numpy(w.seq_lens.astype(np.int32)).cuda())
+    psk.clear_device_status(cache.ws)
+
+
+def test_device_status_bad_append():
+    """An append whose positions run past the block-table row, or a negative start: the append
+    kernel flags PSK_DEV_BAD_APPEND and writes nothing for that page; the cache and summaries of
+    every page inside the row are unchanged and still equal the oracle's."""
+    w = _custom([16 * 6, 16 * 5 + 7], [3, 3], H_q=4, H_kv=1)
+    cache = upload(w)
+    k_before = cache.k_cache.clone()
+    s_before = cache.summaries.clone()
+    k_new = torch.ones(2, w.H_kv, w.D, dtype=torch.bfloat16, device="cuda")
+    v_new = torch.ones(2, w.H_kv, w.D, dtype=torch.bfloat16, device="cuda")
+    for start in ([w.max_pages * w.page_size, int(w.seq_lens[1])], [-3, int(w.seq_lens[1])]):
+        psk.clear_device_status(cache.ws)
+        # sequence 0 appends one token at the given start; sequence 1 appends nothing
+        cache.append(k_new[:1], v_new[:1], torch.tensor(start, dtype=torch.int32, device="cuda"),
+                     torch.tensor([0, 1, 1], dtype=torch.int32, device="cuda"), 1)
+        torch.cuda.synchronize()
+        assert psk.get_device_status(cache.ws) == psk.DEV_BAD_APPEND
+        assert torch.equal(cache.k_cache, k_before) and torch.equal(cache.summaries, s_before)
+    _check_cache_and_summaries(w, cache, [0, 1])
+    psk.clear_device_status(cache.ws)
+
+
+@pytest.mark.parametrize("limit", [1, 4096])
+def test_device_status_bounded_wait_times_out(limit):
+    """The bounded mbarrier wait every streaming kernel uses gives up on a phase that cannot
+    complete (an expected transaction count with no copy issued): PSK_DEV_TIMEOUT is set, the
+    kernel returns, and the context stays usable for a full step checked against the oracle."""
+    w = _custom([16 * 40 + 3, 16 * 9], [6, 3], H_q=8, H_kv=2)
+    cache = upload(w)
+    psk.selftest_bounded_wait(cache.ws, limit)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == psk.DEV_TIMEOUT
+    psk.clear_device_status(cache.ws)
+    summ = _check_cache_and_summaries(w, cache, [0, 1])
+    _run_and_check(w, cache, [0, 1], summ, w.queries(), step_tag="after a timed-out wait")
+
+
 def test_host_argument_errors():
     w = _custom([64], [2], H_q=4, H_kv=1)
     cache = upload(w)
@@ -462,45 +567,67 @@ def test_host_argument_errors():
     assert e.value.code == 1
 
 
-def test_split_count_does_not_change_the_output(monkeypatch):
+_SPLIT_CHILD = r"""
+import sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import page_sparse_kv_gb300 as psk
+import workloads as W
+from workloads.device import budgets as dev_budgets, from_torch, to_torch, upload
+w = W.Workload("custom", 7, "f32", B=3, H_q=4, H_kv=1, D=64, D_v=64, page_size=16,
+               seq_lens=[16 * 300 + 5, 16 * 77, 16 * 40 + 9], budgets=[40, 23, 41], n_hot=0, hot_rule="random",
+               pool_slack=3)
+cache = upload(w)
+q = to_torch(w.queries(), w.dtype).cuda()
+sel = cache.score_select(q, dev_budgets(w))
+out = cache.sparse_decode(q, sel)
+torch.cuda.synchronize()
+assert psk.get_device_status(cache.ws) == 0
+np.save(sys.argv[2] + ".out.npy", from_torch(out.float(), "f32"))
+np.save(sys.argv[2] + ".sel.npy", sel.cpu().numpy())
+print("ok")
+"""
+
+
+def test_split_count_does_not_change_the_output(tmp_path):
     """Split-K over the page list with an LSE merge must not change the result beyond fp32
     rounding: the same sparse decode (fp32 cache) with splits of 1, 2, 7 and 64 list entries and
-    the default (tapered) splits, each against the default and against the oracle."""
-    w = _custom([16 * 300 + 5, 16 * 77, 16 * 40 + 9], [40, 23, 41], dtype="f32", D=64, H_q=4, H_kv=1)
-    cache = upload(w)
-    q_np = w.queries()
-    q = to_torch(q_np, w.dtype).cuda()
-    sel = cache.score_select(q, dev_budgets(w))
-    outs = {}
+    the default (tapered) splits, each against the default and against the oracle. The split
+    width is a tuning override read once per process, so each width runs in a child process."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs, sels = {}, {}
     for sw in (None, 1, 2, 7, 64):
-        if sw is None:
-            monkeypatch.delenv("PSK_DECODE_SPLIT", raising=False)
-        else:
-            monkeypatch.setenv("PSK_DECODE_SPLIT", str(sw))
-        ws = psk.make_workspace(cache.layout, cache.b_max, device="cuda")  # sized for this split
-        out = torch.empty(w.B, w.H_q, w.D_v, dtype=cache.dtype, device="cuda")
-        psk.sparse_paged_decode(cache.layout, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
-                                cache.b_max, cache.scale, out, ws)
-        torch.cuda.synchronize()
-        assert psk.get_device_status(ws) == 0
-        outs[sw] = from_torch(out.float(), "f32").astype(np.float64)
-    monkeypatch.delenv("PSK_DECODE_SPLIT", raising=False)
+        env = dict(os.environ, PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+        env.pop("PSK_DECODE_SPLIT", None)
+        if sw is not None:
+            env["PSK_DECODE_SPLIT"] = str(sw)
+        tag = str(tmp_path / f"split{sw}")
+        r = subprocess.run([sys.executable, "-c", _SPLIT_CHILD, root, tag], env=env, capture_output=True, text=True,
+                           timeout=600)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+        outs[sw] = np.load(tag + ".out.npy").astype(np.float64)
+        sels[sw] = np.load(tag + ".sel.npy")
     ref = outs[None]
     for sw, o in outs.items():
-        for i in range(w.B):
+        assert np.array_equal(sels[sw], sels[None])
+        for i in range(o.shape[0]):
             assert np.abs(o[i] - ref[i]).max() <= 1e-5 * np.abs(ref[i]).max(), f"split {sw} seq {i}"
-    sel_np = sel.cpu().numpy()
+    w = _custom([16 * 300 + 5, 16 * 77, 16 * 40 + 9], [40, 23, 41], dtype="f32", D=64, H_q=4, H_kv=1)
+    q_np = w.queries()
     scale = 1.0 / math.sqrt(w.D)
     for i in range(w.B):
         n = int(w.seq_lens[i])
-        use = [[int(x) for x in sel_np[i, h] if x >= 0] for h in range(w.H_kv)]
+        use = [[int(x) for x in sels[1][i, h] if x >= 0] for h in range(w.H_kv)]
         check_output(outs[1][i], O.attend_pages(q_np[i], w.keys(i), w.values(i), n, w.page_size, use, w.dtype, scale),
                      w.dtype)
 
 
-def test_full_budget_sparse_equals_dense_bitwise():
-    """With b >= P every page is selected; the sparse and dense calls then run the same tiles
-    in the same split layout and must agree exactly."""
+def test_full_budget_sparse_matches_dense():
+    """With b >= P every page is selected; the sparse and dense calls then attend the same tokens
+    (in differently sized splits, so the fp32 merge order differs) and agree to the bf16
+    tolerance."""
     w = _custom([16 * 37 + 5, 16 * 64], [64, 64])
     cache = upload(w)
     q = dev_queries(w)
@@ -508,7 +635,6 @@ def test_full_budget_sparse_equals_dense_bitwise():
     sp = cache.sparse_decode(q, sel)
     de = cache.dense_decode(q)
     torch.cuda.synchronize()
-    # splits differ between the two calls (budget-sized vs page-sized), so compare to tolerance
     check_output(from_torch(sp.float(), "f32"), from_torch(de.float(), "f32").astype(np.float64), "bf16")
 
 
