@@ -179,30 +179,86 @@ def max_over_ranks(values, device):
     return t.tolist()
 
 
-def oracle_sample(w, budget_s: float, start_seq: int = 0):
-    """Times the oracle's sparse decode step (score every page, select, attend) on sequences
-    taken in order from ``start_seq`` until ``budget_s`` seconds of oracle work accumulated.
-    Page summaries are prepared untimed (they are cache state the append step maintains).
-    Returns (seconds per full batch step, sequences timed)."""
+def _oracle_worker(workload: int, batch: int, units, n_steps: int, seconds: float, barrier, results):
+    """One host core's share of the oracle baseline: the oracle's sparse decode step (score every
+    page, select, attend) over this worker's (sequence, KV head) units, repeated for ``seconds``
+    per timed step. A unit is the oracle's functions applied to that KV head's slice of the
+    sequence (its query heads, keys, values and summaries). Page summaries and inputs are
+    prepared before the timed steps (they are cache state the append step maintains). Puts
+    [(seconds, unit pages), ...] per step on ``results``."""
     import oracle as O
+    import workloads as W
+    w = W.config(workload)
+    if batch and batch < w.B:
+        w = W.prefix(w, batch)
     scale = 1.0 / math.sqrt(w.D)
-    spent, n, pages = 0.0, 0, 0
-    i = start_seq
-    while spent < budget_s and n < w.B:
+    G = w.H_q // w.H_kv
+    prep = []
+    for i in sorted({u[0] for u in units}):
         L = int(w.seq_lens[i])
-        keys, vals = w.keys(i), w.values(i)
-        kmin, kmax = O.page_summaries(keys, L, w.page_size, w.dtype)
-        q = w.query(i)
+        keys, vals, q = w.keys(i), w.values(i), w.query(i)
+        for h in sorted(u[1] for u in units if u[0] == i):
+            k_h = np.ascontiguousarray(keys[:, h:h + 1])
+            v_h = np.ascontiguousarray(vals[:, h:h + 1])
+            kmin, kmax = O.page_summaries(k_h, L, w.page_size, w.dtype)
+            prep.append((i, L, k_h, v_h, kmin, kmax, np.ascontiguousarray(q[h * G:(h + 1) * G])))
+        del keys, vals
+    out = []
+    for _ in range(n_steps):
+        barrier.wait(timeout=1800)
         t0 = time.perf_counter()
-        s = O.quest_scores(q, kmin, kmax, w.dtype, scale)
-        sel = [O.select_pages(s[h], int(w.budgets[i])) for h in range(w.H_kv)]
-        O.attend_pages(q, keys, vals, L, w.page_size, sel, w.dtype, scale)
-        spent += time.perf_counter() - t0
-        n += 1
-        pages += -(-L // w.page_size)
-        i = (i + 1) % w.B
-    total_pages = int(((w.seq_lens + w.page_size - 1) // w.page_size).sum())
-    return spent / pages * total_pages, n
+        pages, k = 0, 0
+        while True:
+            i, L, k_h, v_h, kmin, kmax, q_h = prep[k % len(prep)]
+            s = O.quest_scores(q_h, kmin, kmax, w.dtype, scale)
+            sel = [O.select_pages(s[0], int(w.budgets[i]))]
+            O.attend_pages(q_h, k_h, v_h, L, w.page_size, sel, w.dtype, scale)
+            pages += -(-L // w.page_size)
+            k += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        out.append((time.perf_counter() - t0, pages))
+    results.put(out)
+
+
+def oracle_parallel(workload: int, batch: int, n_steps: int, seconds: float):
+    """Times the fp64 oracle's sparse step on every host core this process may use: one spawned
+    process per core, each holding a contiguous share of the batch's (sequence, KV head) units;
+    every step is a window of about ``seconds`` in which all workers run at once (a barrier
+    starts it). A step's time is the batch's unit pages divided by the rate of the window (all
+    workers' unit pages over the slowest worker's time). Returns (per-step seconds for the
+    whole batch, cores, sequence-steps)."""
+    import multiprocessing as mp
+    import workloads as W
+    w = W.config(workload)
+    if batch and batch < w.B:
+        w = W.prefix(w, batch)
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    units = [(i, h) for i in range(w.B) for h in range(w.H_kv)]
+    n = max(1, min(cores, len(units)))
+    shares = [units[j * len(units) // n:(j + 1) * len(units) // n] for j in range(n)]
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(n)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(workload, batch, shares[j], n_steps, seconds, barrier, results))
+             for j in range(n)]
+    for pr in procs:
+        pr.start()
+    outs = [results.get(timeout=3600) for _ in procs]
+    for pr in procs:
+        pr.join(timeout=60)
+    total_pages = int(((w.seq_lens + w.page_size - 1) // w.page_size).sum()) * w.H_kv
+    per_step = []
+    seq_steps = 0
+    for s in range(n_steps):
+        t = max(o[s][0] for o in outs)
+        pg = sum(o[s][1] for o in outs)
+        per_step.append(total_pages / (pg / t))
+        seq_steps += round(pg / (total_pages / w.B))
+    return per_step, n, seq_steps
 
 
 def run_reference(args):
@@ -211,23 +267,19 @@ def run_reference(args):
         return
     import workloads as W
     w = W.config(args.workload)
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
-    for s in range(args.warmup):
-        oracle_sample(w, per_step, start_seq=s % w.B)
-    times, seqs = [], 0
-    for s in range(args.steps):
-        t, n = oracle_sample(w, per_step, start_seq=(args.warmup + s) % w.B)
-        times.append(t)
-        seqs += n
+    per_step_s = max(0.3, args.ref_seconds / max(1, args.steps + args.warmup))  # the whole run: ref_seconds of windows
+    times, cores, seqs = oracle_parallel(args.workload, 0, args.warmup + args.steps, per_step_s)
+    times = times[args.warmup:]
     us = statistics.mean(times) * 1e6
-    sample = (f"{seqs} sequence-steps of the fp64 oracle's sparse step (score all pages, select, attend), "
-              f"~{per_step:.0f} s per step, scaled to the {w.B}-sequence batch")
+    sample = (f"about {seqs} sequence-steps (in pages) of the fp64 oracle's sparse step (score all pages, select, "
+              f"attend), {cores} processes on {cores} host cores, {per_step_s:.2f} s windows, scaled to the "
+              f"{w.B}-sequence batch by pages")
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "D": w.D,
                        "page_size": w.page_size, "budget": "max(4, ceil(5% of pages))"},
-            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -327,40 +379,18 @@ def run_psk(args):
     assert psk.get_device_status(ws) == 0, "device status set during warm-up"
 
     # ---- the same steps captured once into CUDA graphs (replayed inside the timed window) ------
-    def graph_of(fn):
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            fn()  # warm the capture stream
-        stream.wait_stream(side)
-        with torch.cuda.graph(g):
-            fn()
-        return g
-
     # The one-token append touches only the tail page, whose summary the score call does not
     # read (the tail is kept whatever its score): the graphed step runs the append on a side
-    # stream beside score + select, and the decode waits for both.
-    side_s = torch.cuda.Stream()
+    # stream beside score + select, and the decode waits for both (page_sparse_kv_gb300.step,
+    # the same step tests/test_gpu_step_graph.py checks against the oracle).
+    from page_sparse_kv_gb300.step import DecodeStep, capture as graph_of
+    sparse_step = DecodeStep(append, score, decode)
 
     def step_overlapped(pre_main=None, pre_side=None, post=None, dec_out=None):
-        cur = torch.cuda.current_stream()
-        fork = torch.cuda.Event()
-        fork.record(cur)
-        side_s.wait_event(fork)
-        with torch.cuda.stream(side_s):
-            if pre_side is not None:
-                pre_side()
-            append()
-            join = torch.cuda.Event()
-            join.record(side_s)
-        if pre_main is not None:
-            pre_main()
-        score()
-        cur.wait_event(join)
-        decode(dec_out)
-        if post is not None:
-            post()
+        if dec_out is None:
+            sparse_step.launch(pre_main, pre_side, post)
+        else:
+            DecodeStep(append, score, lambda: decode(dec_out)).launch(pre_main, pre_side, post)
 
     try:
         g_sparse = graph_of(step_overlapped)
@@ -568,10 +598,11 @@ def run_psk(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, nseq = oracle_sample(w, args.cpu_seconds)
-        cpu = {"value": secs * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{nseq} of {B} sequences through the fp64 oracle's sparse step (score all pages, select, "
-                         f"attend), scaled to the full batch by pages; single thread"}
+        secs, cores, nseq = oracle_parallel(args.workload, args.batch, 1, args.cpu_seconds)
+        cpu = {"value": secs[0] * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"about {nseq} sequence-steps (in pages) of the {B}-sequence batch through the fp64 oracle's "
+                         f"sparse step (score all pages, select, attend), one process per host core for "
+                         f"{args.cpu_seconds:.0f} s, scaled to the full batch by pages"}
 
     clocks = clk.summary()
     graphed = graph_sparse_ms == graph_sparse_ms
@@ -630,7 +661,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="psk", choices=["psk", "reference"])
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle window of the cpu_baseline leg")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="--impl reference: total seconds of timed oracle windows over warm-up + steps")
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--v-host", action="store_true",

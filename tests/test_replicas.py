@@ -58,7 +58,12 @@ def test_reference_arm_line_rank_0():
     import json
     env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
-                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=600)
+                        "--steps", "1", "--warmup", "3", "--ref-seconds", "2"], env=env, capture_output=True, text=True,
+                       timeout=600)
     assert r.returncode == 0
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the oracle runs on every host core this process may use (one process each), at most one per
+    # (sequence, KV head) unit
+    cfg = line["config"]
+    assert line["cpu_baseline"]["cores"] == min(len(os.sched_getaffinity(0)), cfg["B"] * cfg["H_kv"])
