@@ -69,7 +69,8 @@ cudaError_t kernel_setup(const void *fn, int threads, size_t smem, int *per_sm) 
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_mu);
   KernelEntry &k = entry(dev, fn);
-  if (smem > 48 * 1024 && k.smem_set < smem) {
+  // dynamic + static shared memory above 48 KB needs the opt-in: set it for any dynamic size
+  if (smem > 0 && k.smem_set < smem) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k.smem_set = smem;
