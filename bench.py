@@ -57,31 +57,15 @@ def peaks():
 # call, with a digest of the sources the kernels are built from: a digest that no longer matches
 # means the kernels changed since the capture, and the traffic is reported as null.
 TRAFFIC = {
-    # python bench.py --steps 5 --warmup 3 --no-cpu-baseline, then
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
-    #     -k regex:"page_s|decode_split" -s 4 -c 3 python bench.py --steps 5 --warmup 3 --no-cpu-baseline
-    ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel"):
-        {"bytes": 577_373_952 + 4_458_240, "digest": "6b457f0a50eb5b54"},
-    ("batched-ragged-b64-8k..64k-5pct", "page_select_kernel"):
-        {"bytes": 4_622_848 + 0, "digest": "9b065b1469e13666"},
-    ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 466_761_728 + 1_079_040, "digest": "17d6bc14093fb0fd"},
-    # python bench.py --workload 4 --steps 5 --warmup 3 --no-cpu-baseline, then
-    # ncu ... -k regex:"page_score" -s 2 -c 1 python bench.py --workload 4 --steps 5 --warmup 3 --no-cpu-baseline
-    ("long-1m-b1", "page_score_kernel"):
-        {"bytes": 268_734_720 + 3_986_432, "digest": "6b457f0a50eb5b54"},
-    # python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline, then
-    # ncu ... -k regex:"mla_" -s 0 -c 3 python bench.py --workload 5 --steps 5 --warmup 3 --no-cpu-baseline
-    ("mla-b16-128k-5pct", "mla_qsplit_kernel+mla_score_kernel"):
-        {"bytes": 2_363_648 + 0 + 80_295_680 + 34_560, "digest": "494eab7f3bf82b5b"},
-    ("mla-b16-128k-5pct", "mla_decode_kernel"):
-        {"bytes": 124_142_336 + 216_832, "digest": "494eab7f3bf82b5b"},
+    # filled in from one-pass captures of the current kernels (measurement)
 }
 KERNEL_SOURCES = {
-    "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
-    "page_select_kernel": ("select.cu", "psk_common.cuh", "psk_internal.h"),
+    "page_score_kernel": ("score_select.cu", "select_common.cuh", "psk_common.cuh", "psk_internal.h"),
+    "page_score_kernel+page_select_kernel": ("score_select.cu", "select.cu", "select_common.cuh", "psk_common.cuh",
+                                             "psk_internal.h"),
     "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),
-    "mla_qsplit_kernel+mla_score_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
+    "mla_qsplit_kernel+mla_score_kernel+page_select_kernel": ("mla.cu", "select.cu", "select_common.cuh",
+                                                              "psk_common.cuh", "psk_internal.h"),
     "mla_decode_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
 }
 
@@ -344,14 +328,9 @@ def run_psk(args):
         psk.page_score_select(L, q, cache.summaries, cache.block_table, cache.seq_lens, bud, w.b_max, cache.scale,
                               sel, ws)
 
-    # the same two stages as separate calls, so each kernel gets its own events in the eager loop
-    sel_prm = psk.select_params(budgets=bud)
-
-    def score_only():
-        psk.page_score(L, q, cache.summaries, cache.block_table, cache.seq_lens, sel_prm, w.b_max, cache.scale, ws)
-
-    def select_only():
-        psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
+    # kernels one score + select call launches: 1 when the selection runs in the score kernel's
+    # last CTA per (sequence, head group), 2 with a separate selection launch, 3 for the latent form
+    ss_launches = psk.score_select_launches(L, w.b_max)
 
     def decode(dst=None):  # dst: the output buffer (default: `out` in device memory)
         o = out if dst is None else dst
@@ -371,7 +350,7 @@ def run_psk(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    launches_per_step = 5 if w.latent else 4  # append, (q split,) score, select, decode
+    launches_per_step = 2 + ss_launches  # append, score (+ select, + q split), decode
     for _ in range(args.warmup):
         append(); score(); decode()
         append(); dense()
@@ -425,7 +404,7 @@ def run_psk(args):
 
     K = args.steps
     Kd = max(3, K // 4)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     evd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
     evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     evgd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
@@ -440,12 +419,10 @@ def run_psk(args):
         e[0].record(stream)
         append()
         e[1].record(stream)
-        score_only()
+        score()
         e[2].record(stream)
-        select_only()
-        e[3].record(stream)
         decode()
-        e[4].record(stream)
+        e[3].record(stream)
     marks[1].record(stream)
     for k in range(Kd):
         flush_l2()
@@ -486,9 +463,8 @@ def run_psk(args):
         else:
             graph_sparse_ms = graph_dense_ms = float("nan")
     t_app = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
-    t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
-    t_select = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
-    t_dec = statistics.mean(ev[k][3].elapsed_time(ev[k][4]) for k in range(K))
+    t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))  # score + select call
+    t_dec = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
     if dist is not None:
         sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = max_over_ranks(
             [sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], dev)
@@ -570,12 +546,15 @@ def run_psk(args):
     pk = peaks()
     peak_hbm = pk["hbm"]
     flops_decode = 2 * Hq * (D + w.D_v) * sel_tokens  # QK^T and P.V over the selected tokens
-    # the dominant kernel by time (score, select or decode), each timed by its own events
-    if t_score >= t_dec and t_score >= t_select:
-        dom = "mla_qsplit_kernel+mla_score_kernel" if w.latent else "page_score_kernel"
+    # the dominant call by time (score + select, or decode), each timed by its own events
+    if t_score >= t_dec:
+        dom = {1: "page_score_kernel", 2: "page_score_kernel+page_select_kernel",
+               3: "mla_qsplit_kernel+mla_score_kernel+page_select_kernel"}[ss_launches]
         roof = {"bound": "hbm", "kernel": dom, "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
                 "unit": "GB/s", "algorithmic_per_launch": score_bytes, "algorithmic_unit": "B",
                 "launch_us": t_score * 1e3}
+        if ss_launches == 1:
+            roof["note"] = "one launch: the page scores and, in each sequence's last CTA, the top-b selection"
     elif w.latent:
         # arithmetic intensity ~300 flop/B, above the measured ridge (~250-290): tensor-bound
         dom = "mla_decode_kernel"
@@ -635,8 +614,8 @@ def run_psk(args):
         "speedup_vs_dense": step_dense_ms / step_ms,
         "eager": {"us_per_step": sparse_ms * 1e3, "dense_us_per_step": dense_ms * 1e3,
                   "speedup_vs_dense": dense_ms / sparse_ms},
-        "kernels_us": {"append": t_app * 1e3, "score": t_score * 1e3, "select": t_select * 1e3,
-                       "score_select": (t_score + t_select) * 1e3, "sparse_decode": t_dec * 1e3},
+        "kernels_us": {"append": t_app * 1e3, "score_select": t_score * 1e3, "sparse_decode": t_dec * 1e3},
+        "score_select_launches": ss_launches,
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "timing": ("CUDA-graph replay" if e2e_ms != e2e_eager_ms else "eager launches")
                           + " of pinned-host H2D copies of q and the new K/V + the step, whose decode writes "

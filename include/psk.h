@@ -234,6 +234,13 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
                              int32_t *selected, float *scores_out, void *workspace,
                              size_t workspace_bytes, psk_stream_t stream);
 
+/* Kernel launches one psk_page_score_select_ex call makes for this layout, b_max and
+ * per_query_head (0 when the layout is invalid or unsupported): 1 when every unit fits one
+ * selection chunk (the score kernel's last CTA of each (sequence, head group) selects its
+ * units), 2 with a separate selection launch, 3 for the latent form (query split, score,
+ * selection). Useful for sizing CUDA graphs and counting launches. */
+int psk_score_select_launches(const psk_layout *layout, int32_t b_max, int32_t per_query_head);
+
 /* ---------------------------------------------------------------------------------------
  * The two stages of psk_page_score_select_ex as separate calls, for callers that run other
  * work between them or time them apart. psk_page_score writes one selection key per

@@ -26,6 +26,7 @@ EXPORTS = [
     "psk_sparse_paged_decode_ex", "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version", "psk_selftest_bounded_wait",
+    "psk_score_select_launches",
 ]
 
 
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
             "psk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "psk_version": (ctypes.c_int, []),
             "psk_selftest_bounded_wait": (ctypes.c_int, [P, Z, ctypes.c_uint32, P]),
+            "psk_score_select_launches": (ctypes.c_int, [LP, I, I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -158,6 +160,12 @@ def sparse_decode_workspace_size(layout: Layout, b_max: int) -> int:
 
 def dense_decode_workspace_size(layout: Layout) -> int:
     return int(lib().psk_dense_decode_workspace_size(ctypes.byref(layout.c())))
+
+
+def score_select_launches(layout: Layout, b_max: int, per_query_head: bool = False) -> int:
+    """Kernel launches of one page_score_select(_ex) call (1: selection fused into the score
+    kernel, 2: a separate selection launch, 3: latent form); 0 if unsupported."""
+    return int(lib().psk_score_select_launches(ctypes.byref(layout.c()), int(b_max), 1 if per_query_head else 0))
 
 
 def workspace_size(layout: Layout, b_max: int) -> int:

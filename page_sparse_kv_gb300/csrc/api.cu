@@ -91,6 +91,18 @@ size_t psk_score_select_workspace_size(const psk_layout *layout, int32_t b_max) 
   return bytes;
 }
 
+int psk_score_select_launches(const psk_layout *layout, int32_t b_max, int32_t per_query_head) {
+  if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
+  if (per_query_head != 0 && per_query_head != 1) return 0;
+  psk_layout U = *layout;
+  int kv_shift = 0;
+  if (per_query_head && !per_query_head_view(*layout, &U, &kv_shift)) return 0;
+  ScorePlan plan;
+  if (!plan_score(U, b_max, &plan, kv_shift)) return 0;
+  if (layout->latent) return 3;
+  return (plan.n_chunks_max == 1 && tuning().score_fused_select) ? 1 : 2;
+}
+
 static bool plan_any_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan) {
   return L.latent ? plan_mla_decode(L, entries, plan) : plan_decode(L, entries, dense, plan);
 }
@@ -264,6 +276,7 @@ static int score_select_common(const psk_layout *layout, const void *q, const vo
   a.budget_mode = sp.mode;
   a.budget_pages = sp.budget_pages;
   a.budget_frac = sp.budget_fraction;
+  a.fused_select = 0;  // chosen by the GQA launcher
   if (L.latent)
     return cuda_status(launch_mla_score_select(a, reinterpret_cast<uint16_t *>(ws + plan.off_qsplit),
                                                static_cast<cudaStream_t>(stream), stages));

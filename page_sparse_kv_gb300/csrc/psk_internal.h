@@ -57,6 +57,8 @@ struct ScoreArgs {
   int budget_mode;        // enum psk_budget_mode
   int budget_pages;       // PSK_BUDGET_PAGES
   double budget_frac;     // PSK_BUDGET_FRACTION
+  int fused_select;       // 1: the score kernel's last CTA of each (sequence, head group) selects
+                          // its units (one selection chunk per unit); no separate select launch
 };
 
 // Page p of a sequence of P pages is always kept: one of the first `sink` or the last `window`.

@@ -33,6 +33,7 @@
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
+#include "select_common.cuh"
 
 namespace psk {
 namespace {
@@ -224,30 +225,6 @@ __device__ int compact_taken(const uint32_t *keys, const int32_t *pages, int pag
   return (total & 0xFFFF) + (take_all ? 0 : min(total >> 16, need_eq));
 }
 
-// Row of a unit with count < P selected pages: the first S pages, the `wrote` winners (written
-// by the caller at sel_row + S, all inside [S, P - W)), the last W pages straight after them,
-// then -1 to b_max. count < P implies S + W < P, so the two always-kept runs do not overlap.
-// wrote < count - S - W happens only after a flagged bad block: the row is then shorter, and the
-// -1 padding still comes only at its end (the decode reads a row up to its first -1).
-__device__ void write_row_ends(int32_t *sel_row, int P, int wrote, int b_max, int S, int W) {
-  const int tid = threadIdx.x;
-  for (int x = tid; x < S; x += kSelThreads) sel_row[x] = x;
-  const int w0 = S + wrote;
-  for (int x = tid; x < W; x += kSelThreads) sel_row[w0 + x] = P - W + x;
-  for (int x = w0 + W + tid; x < b_max; x += kSelThreads) sel_row[x] = -1;
-}
-
-// Budget of a sequence of P pages (at least the always-kept count in the scalar modes);
-// budget_in: the sequence's entry of a.budgets in the per-sequence mode.
-__device__ int unit_budget(const ScoreArgs &a, int budget_in, int P, int n_forced) {
-  if (a.budget_mode == PSK_BUDGET_FRACTION) {
-    const int r = (int)ceil((double)P * a.budget_frac);  // IEEE double product, then the ceiling
-    return max(n_forced, min(P, max(1, r)));
-  }
-  if (a.budget_mode == PSK_BUDGET_PAGES) return max(n_forced, min(P, a.budget_pages));
-  return budget_in;
-}
-
 __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a) {
   pdl_wait();  // dependents are released when this grid completes
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -329,7 +306,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     if (!take_all) radix_select(keys, n, k_free, kmin, kmax, hist, sc, &thr, &need_eq);
     if (nch == 1) {
       wrote = compact_taken(keys, nullptr, p0, n, take_all, thr, need_eq, nullptr, sel_row + a.sink, sc);
-      write_row_ends(sel_row, P, wrote, a.b_max, a.sink, a.window);
+      write_row_ends(sel_row, P, wrote, a.b_max, a.sink, a.window, tid, kSelThreads);
       return;
     }
     const int slot = unit * a.n_chunks_max + c;
@@ -338,7 +315,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     if (tid == 0) a.cand_count[slot] = wrote;
   } else {
     if (nch == 1) {
-      write_row_ends(sel_row, P, 0, a.b_max, a.sink, a.window);
+      write_row_ends(sel_row, P, 0, a.b_max, a.sink, a.window, tid, kSelThreads);
       return;
     }
     if (tid == 0) a.cand_count[unit * a.n_chunks_max + c] = 0;
@@ -402,7 +379,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
     }
     wrote = compact_taken(mkey, mpage, 0, n_c, take_all, thr, need_eq, nullptr, sel_row + a.sink, sc);
   }
-  write_row_ends(sel_row, P, wrote, a.b_max, a.sink, a.window);
+  write_row_ends(sel_row, P, wrote, a.b_max, a.sink, a.window, tid, kSelThreads);
 }
 
 }  // namespace

@@ -171,3 +171,17 @@ def test_workspace_sizes_cover_every_form(lib):
     # the latent form has its own sizes and no per-query-head form
     M = psk.Layout(16, 128, 1, 576, 512, 64, 40000, 2048, latent=1)
     assert psk.score_select_workspace_size(M, 103) > 0 and psk.sparse_decode_workspace_size(M, 103) > 0
+
+
+def test_score_select_launch_count(lib):
+    """One launch when every unit fits one selection chunk (the selection runs in the score
+    kernel), two when the selection needs its own chunked launch, three for the latent form."""
+    import page_sparse_kv_gb300 as psk
+    batched = psk.Layout(64, 32, 8, 128, 128, 16, 150000, 4096)
+    assert psk.score_select_launches(batched, 205) == 1
+    assert psk.score_select_launches(batched, 205, per_query_head=True) == 1
+    long_ctx = psk.Layout(1, 32, 8, 128, 128, 16, 65536, 65536)
+    assert psk.score_select_launches(long_ctx, 128) == 2
+    latent = psk.Layout(16, 128, 1, 576, 512, 64, 40000, 2048, psk.PSK_BF16, 1)
+    assert psk.score_select_launches(latent, 103) == 3
+    assert psk.score_select_launches(psk.Layout(2, 32, 8, 96, 96, 16, 100, 50), 10) == 0
