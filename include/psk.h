@@ -242,6 +242,30 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
 int psk_score_select_launches(const psk_layout *layout, int32_t b_max, int32_t per_query_head);
 
 /* ---------------------------------------------------------------------------------------
+ * Stages 2 + 3 in the adaptive coverage mode (LOCKS PKG-INFO, "Configuration (LocksConfig)",
+ * `coverage`: adaptive per-head nucleus coverage over exact page masses, GQA only; AMASS PyPI
+ * page, "Key AmassConfig fields", the same option). Instead of a bound from the summaries,
+ * every page's exact softmax mass is computed from the keys themselves (a K-only pass over
+ * every page):
+ *   mass[i,g,p] = sum over tokens t of page p (t < seq_lens[i]) of softmax_t(scale * q[i,g] . k_t),
+ * the softmax over every token of sequence i in KV head h = g / G; the unit (i, h) takes
+ * mass[i,h,p] = max over the group's query heads. Selected: the always-kept pages
+ * [0, sink_pages) U [P_i - window_pages, P_i), then the other pages in order of mass (desc,
+ * ties to the lower page) until the selected mass reaches coverage times the unit's total mass
+ * (0 < coverage <= 1), at most b_max pages in all. Rows as psk_page_score_select:
+ * selected [batch, num_kv_heads, b_max] ascending, -1 padded. masses_out (optional, fp32
+ * [batch, num_kv_heads, max_pages]) receives mass[i,h,p] for p < P_i. Masses are fp32; their
+ * sums are taken in fixed point (units of 2^-40), so the selection does not depend on
+ * summation order. Reads k_cache (device memory) for every page, i.e. half the bytes of a
+ * dense decode. The workspace is the one psk_coverage_workspace_size reports.
+ * --------------------------------------------------------------------------------------- */
+int psk_page_select_coverage(const psk_layout *layout, const void *q, const void *k_cache,
+                             const int32_t *block_table, const int32_t *seq_lens, double coverage,
+                             int32_t sink_pages, int32_t window_pages, int32_t b_max, float scale,
+                             int32_t *selected, float *masses_out, void *workspace,
+                             size_t workspace_bytes, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * The two stages of psk_page_score_select_ex as separate calls, for callers that run other
  * work between them or time them apart. psk_page_score writes one selection key per
  * (unit, page) into the workspace (and scores_out when given); psk_page_select turns those
@@ -343,6 +367,7 @@ size_t psk_append_workspace_size(const psk_layout *layout);
 size_t psk_score_select_workspace_size(const psk_layout *layout, int32_t b_max);
 size_t psk_sparse_decode_workspace_size(const psk_layout *layout, int32_t b_max);
 size_t psk_dense_decode_workspace_size(const psk_layout *layout);
+size_t psk_coverage_workspace_size(const psk_layout *layout, int32_t b_max);
 
 /* Copy the sticky device status word of `workspace` to *flags (synchronises `stream`). */
 int psk_get_device_status(const void *workspace, uint32_t *flags, psk_stream_t stream);

@@ -31,6 +31,11 @@ online softmax or algebraic rewriting:
                          may come from a fraction of the pages or a fixed page count
                          (same table; the fraction rounds by the retained-count rule
                          of the vllm-rlt pull request #157 discussion).
+  S3 coverage mode    -- adaptive per-head nucleus coverage over exact page masses (LOCKS
+                         configuration table `coverage`; AMASS "Key AmassConfig fields"): the
+                         softmax mass of every page, max over the GQA group, and the fewest
+                         highest-mass pages that, with the always-kept ones, reach a fraction of
+                         the total mass.
   S4 attention        -- exact softmax attention over the selected pages' tokens
                          only (EntmaxKV introduction: "the attention is exact over
                          that selection"; LOCKS "How it works", Sparse decode), the
@@ -47,7 +52,12 @@ points the pages leave open:
   * ties in the page score (including -0.0 vs +0.0) go to the lower page index;
   * the scale 1/sqrt(D) is applied after the group max and is the same scale
     used for the attention logits;
-  * for a latent (MLA) cache the value is the first D_v dims of the latent key.
+  * for a latent (MLA) cache the value is the first D_v dims of the latent key;
+  * coverage: a page's mass is its exact softmax mass for a query head over every token of the
+    sequence; a KV head's page mass is the max over its group's query heads; the always-kept
+    pages are selected and their mass counts toward the target, which is the coverage fraction
+    of the unit's total page mass; the other pages join in (mass desc, index asc) order until
+    the target is reached, and the selection holds at most b_max pages.
 """
 from __future__ import annotations
 
@@ -252,6 +262,63 @@ def budget_for(P: int, *, fraction: float | None = None, pages: int | None = Non
             raise ValueError("pages >= 1")
         b = min(P, pages)
     return max(b, forced)
+
+
+# ----------------------------------------------------------------------------------
+# S3 budget mode: adaptive per-head coverage over exact page masses
+# ----------------------------------------------------------------------------------
+def page_masses(q: np.ndarray, keys: np.ndarray, seq_len: int, page_size: int, dtype: str, scale: float) -> np.ndarray:
+    """Exact softmax mass of every page for every query head (LOCKS PKG-INFO, "Configuration
+    (LocksConfig)", `coverage`: adaptive per-head nucleus coverage over exact page masses; AMASS
+    PyPI page, "Key AmassConfig fields", the same option). For query head g of KV head h:
+
+      mass[g, p] = sum over tokens t of page p (t < seq_len) of softmax_t(scale * q_g . k_{t,h}),
+
+    the softmax taken over every token of the sequence. q [H_q, D]; keys [T >= seq_len, H_kv, D]
+    stored. Returns float64 [H_q, P]; each row sums to 1."""
+    qv = to_f64(q, dtype)
+    H_q = qv.shape[0]
+    H_kv = keys.shape[1]
+    G = H_q // H_kv
+    P = -(-seq_len // page_size)
+    k = to_f64(keys[:seq_len], dtype)
+    out = np.empty((H_q, P))
+    for g in range(H_q):
+        logits = scale * (k[:, g // G, :] @ qv[g])
+        w = np.exp(logits - logits.max())
+        w /= w.sum()
+        for p in range(P):
+            out[g, p] = w[p * page_size:min((p + 1) * page_size, seq_len)].sum()
+    return out
+
+
+def group_masses(masses: np.ndarray, H_kv: int) -> np.ndarray:
+    """Page masses of each KV head: the max over the query heads of its GQA group (the group
+    combine `max` of the LOCKS configuration table). [H_q, P] -> [H_kv, P]."""
+    G = masses.shape[0] // H_kv
+    return np.stack([masses[h * G:(h + 1) * G].max(axis=0) for h in range(H_kv)])
+
+
+def select_coverage(mass: np.ndarray, coverage: float, b_max: int, sink_pages: int = 1,
+                    window_pages: int = 1) -> list[int]:
+    """Nucleus selection of one unit, ascending: the always-kept pages, then the other pages in
+    order of (mass desc, index asc), as few as make the selected mass reach coverage times the
+    unit's total mass (for a group of one query head the total is 1), and at most b_max pages in
+    all (the row's capacity). mass: [P] float64."""
+    P = len(mass)
+    forced = forced_pages(P, sink_pages, window_pages)
+    if b_max < len(forced):
+        raise ValueError("b_max must hold every always-kept page")
+    target = coverage * float(mass.sum())
+    have = float(mass[forced].sum()) if forced else 0.0
+    ranked = sorted((p for p in range(P) if p not in forced), key=lambda p: (-float(mass[p]), p))
+    chosen = []
+    for p in ranked:
+        if have >= target or len(forced) + len(chosen) >= b_max:
+            break
+        chosen.append(p)
+        have += float(mass[p])
+    return sorted(forced + chosen)
 
 
 # ----------------------------------------------------------------------------------

@@ -26,7 +26,7 @@ EXPORTS = [
     "psk_sparse_paged_decode_ex", "psk_dense_paged_decode", "psk_sparse_paged_decode_noalloc", "psk_append_workspace_size", "psk_score_select_workspace_size",
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version", "psk_selftest_bounded_wait",
-    "psk_score_select_launches",
+    "psk_score_select_launches", "psk_page_select_coverage", "psk_coverage_workspace_size",
 ]
 
 
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
             "psk_version": (ctypes.c_int, []),
             "psk_selftest_bounded_wait": (ctypes.c_int, [P, Z, ctypes.c_uint32, P]),
             "psk_score_select_launches": (ctypes.c_int, [LP, I, I]),
+            "psk_page_select_coverage": (ctypes.c_int, [LP, P, P, P, P, ctypes.c_double, I, I, I, F, P, P, P, Z, P]),
+            "psk_coverage_workspace_size": (Z, [LP, I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -168,19 +170,26 @@ def score_select_launches(layout: Layout, b_max: int, per_query_head: bool = Fal
     return int(lib().psk_score_select_launches(ctypes.byref(layout.c()), int(b_max), 1 if per_query_head else 0))
 
 
-def workspace_size(layout: Layout, b_max: int) -> int:
-    """Bytes of one workspace that serves every call of this layout and budget bound."""
+def coverage_workspace_size(layout: Layout, b_max: int) -> int:
+    return int(lib().psk_coverage_workspace_size(ctypes.byref(layout.c()), int(b_max)))
+
+
+def workspace_size(layout: Layout, b_max: int, coverage: bool = False) -> int:
+    """Bytes of one workspace that serves every call of this layout and budget bound (and the
+    coverage selection when ``coverage``)."""
     sizes = [append_workspace_size(layout), score_select_workspace_size(layout, b_max),
              sparse_decode_workspace_size(layout, b_max), dense_decode_workspace_size(layout)]
+    if coverage:
+        sizes.append(coverage_workspace_size(layout, b_max))
     if min(sizes) == 0:
         raise PskError("workspace_size", 2, "layout not supported")
     return max(sizes)
 
 
-def make_workspace(layout: Layout, b_max: int, device=None):
+def make_workspace(layout: Layout, b_max: int, device=None, coverage: bool = False):
     """A zero-filled workspace tensor (uint8) sized for every call of this layout."""
     import torch
-    return torch.zeros(workspace_size(layout, b_max), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(workspace_size(layout, b_max, coverage), dtype=torch.uint8, device=device or "cuda")
 
 
 # ------------------------------------------------------------------------------ calls
@@ -248,6 +257,18 @@ def page_score_select_ex(layout: Layout, q, summaries, block_table, seq_lens, b_
         ctypes.byref(layout.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens), ctypes.byref(prm),
         int(b_max), float(scale), _ptr(selected), _ptr(scores_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def page_select_coverage(layout: Layout, q, k_cache, block_table, seq_lens, coverage: float, b_max: int,
+                         scale: float, selected, workspace, sink_pages: int = 1, window_pages: int = 1,
+                         masses_out=None, stream=None):
+    """Adaptive per-head coverage: the always-kept pages plus the fewest highest-mass pages whose
+    exact softmax mass reaches ``coverage`` of the unit's total (see psk.h); rows into
+    ``selected`` [batch, num_kv_heads, b_max], masses into ``masses_out`` when given."""
+    _check("psk_page_select_coverage", lib().psk_page_select_coverage(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(seq_lens), float(coverage),
+        int(sink_pages), int(window_pages), int(b_max), float(scale), _ptr(selected), _ptr(masses_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def sparse_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max: int,

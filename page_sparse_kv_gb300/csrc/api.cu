@@ -277,6 +277,7 @@ static int score_select_common(const psk_layout *layout, const void *q, const vo
   a.budget_pages = sp.budget_pages;
   a.budget_frac = sp.budget_fraction;
   a.fused_select = 0;  // chosen by the GQA launcher
+  a.unit_budgets = nullptr;
   if (L.latent)
     return cuda_status(launch_mla_score_select(a, reinterpret_cast<uint16_t *>(ws + plan.off_qsplit),
                                                static_cast<cudaStream_t>(stream), stages));
@@ -302,6 +303,104 @@ int psk_page_select(const psk_layout *layout, const int32_t *seq_lens, const psk
                     int32_t b_max, int32_t *selected, void *workspace, size_t workspace_bytes, psk_stream_t stream) {
   return score_select_common(layout, nullptr, nullptr, nullptr, seq_lens, params, b_max, 0.f, selected, nullptr,
                              workspace, workspace_bytes, stream, kStageSelect);
+}
+
+// Workspace of the coverage selection: the score / select regions of the layout, then the
+// per-page (max, sum) pairs, the fixed-point masses and the per-unit budgets.
+struct CoveragePlan {
+  ScorePlan sel;
+  size_t off_pm, off_qmass, off_budgets, ws_bytes;
+};
+static bool plan_coverage(const psk_layout &L, int b_max, CoveragePlan *cp) {
+  if (L.latent) return false;
+  const int G = L.num_q_heads / L.num_kv_heads;
+  if (!coverage_supported(L.dtype, L.head_dim, G)) return false;
+  if (!plan_score(L, b_max, &cp->sel)) return false;
+  const size_t units = (size_t)L.batch * L.num_kv_heads;
+  size_t off = align_up(cp->sel.ws_bytes, 256);
+  cp->off_pm = off;
+  off = align_up(off + units * (size_t)L.max_pages * G * 2 * 4, 256);
+  cp->off_qmass = off;
+  off = align_up(off + units * (size_t)L.max_pages * 8, 256);
+  cp->off_budgets = off;
+  off = align_up(off + units * 4, 256);
+  cp->ws_bytes = off;
+  return true;
+}
+
+size_t psk_coverage_workspace_size(const psk_layout *layout, int32_t b_max) {
+  if (check_layout(layout) != PSK_OK || check_gqa_compute(layout) != PSK_OK || b_max < 1) return 0;
+  CoveragePlan cp;
+  return plan_coverage(*layout, b_max, &cp) ? cp.ws_bytes : 0;
+}
+
+int psk_page_select_coverage(const psk_layout *layout, const void *q, const void *k_cache, const int32_t *block_table,
+                             const int32_t *seq_lens, double coverage, int32_t sink_pages, int32_t window_pages,
+                             int32_t b_max, float scale, int32_t *selected, float *masses_out, void *workspace,
+                             size_t workspace_bytes, psk_stream_t stream) {
+  int rc = check_layout(layout);
+  if (rc != PSK_OK) return rc;
+  const psk_layout &L = *layout;
+  if (!q || !k_cache || !block_table || !seq_lens || !selected || b_max < 1) return PSK_ERR_INVALID_ARG;
+  if (!(coverage > 0.0 && coverage <= 1.0) || sink_pages < 0 || window_pages < 1) return PSK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache)) return PSK_ERR_INVALID_ARG;
+  rc = check_gqa_compute(layout);
+  if (rc != PSK_OK) return rc;
+  CoveragePlan cp;
+  if (!plan_coverage(L, b_max, &cp)) return PSK_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < cp.ws_bytes) return PSK_ERR_WORKSPACE;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  ScoreArgs a = {};
+  a.seq_lens = seq_lens;
+  a.selected = selected;
+  a.ws = workspace;
+  a.counters = reinterpret_cast<uint32_t *>(ws + cp.sel.off_counters);
+  a.keys = reinterpret_cast<uint32_t *>(ws + cp.sel.off_keys);
+  a.key_stride = (L.max_pages + 3) & ~3;
+  a.cand_key = reinterpret_cast<uint32_t *>(ws + cp.sel.off_key);
+  a.cand_page = reinterpret_cast<int32_t *>(ws + cp.sel.off_page);
+  a.cand_count = reinterpret_cast<int32_t *>(ws + cp.sel.off_count);
+  a.B = L.batch;
+  a.H_q = L.num_q_heads;
+  a.H_kv = L.num_kv_heads;
+  a.H_kv_cache = L.num_kv_heads;
+  a.D = L.head_dim;
+  a.ps = L.page_size;
+  a.nb = L.num_blocks;
+  a.max_pages = L.max_pages;
+  a.b_max = b_max;
+  a.chunk = cp.sel.chunk;
+  a.n_chunks_max = cp.sel.n_chunks_max;
+  a.k_cap = cp.sel.k_cap;
+  a.sink = sink_pages;
+  a.window = window_pages;
+  a.budget_mode = PSK_BUDGET_PER_SEQUENCE;
+  a.unit_budgets = reinterpret_cast<int32_t *>(ws + cp.off_budgets);
+  CoverageArgs c = {};
+  c.q = q;
+  c.k_cache = k_cache;
+  c.block_table = block_table;
+  c.seq_lens = seq_lens;
+  c.ws = workspace;
+  c.pm = reinterpret_cast<float *>(ws + cp.off_pm);
+  c.keys = a.keys;
+  c.qmass = reinterpret_cast<unsigned long long *>(ws + cp.off_qmass);
+  c.unit_budgets = reinterpret_cast<int32_t *>(ws + cp.off_budgets);
+  c.masses_out = masses_out;
+  c.B = L.batch;
+  c.H_q = L.num_q_heads;
+  c.H_kv = L.num_kv_heads;
+  c.D = L.head_dim;
+  c.ps = L.page_size;
+  c.nb = L.num_blocks;
+  c.max_pages = L.max_pages;
+  c.b_max = b_max;
+  c.key_stride = a.key_stride;
+  c.sink = sink_pages;
+  c.window = window_pages;
+  c.scale = scale;
+  c.coverage = coverage;
+  return cuda_status(launch_coverage_select(c, a, L.dtype, static_cast<cudaStream_t>(stream)));
 }
 
 static int decode_common(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,

@@ -64,7 +64,7 @@ struct Tuning {
   int decode_layout = 0;  // 0 default, 1 split, 2 flat
   int decode_split = -1;
   bool decode_no_taper = false;
-  bool score_fused_select = true;  // PSK_SCORE_FUSED_SELECT=0: select in its own launch
+  int score_fused_select = -1;  // PSK_SCORE_FUSED_SELECT: 1 fused, 0 separate, -1 default
 };
 const Tuning &tuning();
 

@@ -59,6 +59,7 @@ struct ScoreArgs {
   double budget_frac;     // PSK_BUDGET_FRACTION
   int fused_select;       // 1: the score kernel's last CTA of each (sequence, head group) selects
                           // its units (one selection chunk per unit); no separate select launch
+  const int32_t *unit_budgets;  // non-null: per-unit budgets (coverage mode) instead of budgets[i]
 };
 
 // Page p of a sequence of P pages is always kept: one of the first `sink` or the last `window`.
@@ -127,6 +128,25 @@ __host__ __device__ inline int split_off(int s, int sw, int taper) {
 }
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);
 bool decode_supported(int dtype, int D, int D_v, int G, int ps);
+
+// adaptive per-head coverage over exact page masses (coverage.cu)
+struct CoverageArgs {
+  const void *q;
+  const void *k_cache;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  void *ws;
+  float *pm;                   // [B * H_kv, max_pages, G, 2] per-page (max, sum of 2^(x - max)) per query head
+  uint32_t *keys;              // the selection keys (ScoreArgs::keys)
+  unsigned long long *qmass;   // [B * H_kv, max_pages] page masses in 2^-40 units
+  int32_t *unit_budgets;       // [B * H_kv] budget of each unit for the selection
+  float *masses_out;           // optional [B * H_kv, max_pages] page masses
+  int B, H_q, H_kv, D, ps, nb, max_pages, b_max, key_stride, sink, window;
+  float scale;
+  double coverage;
+};
+bool coverage_supported(int dtype, int D, int G);
+cudaError_t launch_coverage_select(const CoverageArgs &c, const ScoreArgs &sel, int dtype, cudaStream_t s);
 
 // latent (MLA) form on the tensor cores
 bool mla_supported(const psk_layout &L);

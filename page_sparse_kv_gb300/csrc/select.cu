@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) page_select_kernel(ScoreArgs a
   const int tid = threadIdx.x;
   const int seq_len = a.seq_lens[i];
   // the budget load is issued together with the length's (both are one L2 round trip)
-  const int budget_in = a.budget_mode == PSK_BUDGET_PER_SEQUENCE ? a.budgets[i] : 0;
+  const int budget_in =
+      a.budget_mode == PSK_BUDGET_PER_SEQUENCE ? (a.unit_budgets ? a.unit_budgets[unit] : a.budgets[i]) : 0;
   const int P = (seq_len + a.ps - 1) / a.ps;
   int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
 

@@ -14,6 +14,8 @@
 
 namespace psk {
 
+constexpr int kSelBatch = 8;  // four-key groups each lane loads at once in warp_select_unit's passes
+
 // Budget of a sequence of P pages (at least the always-kept count in the scalar modes);
 // budget_in: the sequence's entry of a.budgets in the per-sequence mode.
 __device__ __forceinline__ int unit_budget(const ScoreArgs &a, int budget_in, int P, int n_forced) {
@@ -55,7 +57,8 @@ __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
 // bit where the smallest and largest candidate keys differ; the digit whose bin crosses the
 // number of keys still needed is fixed, and the select stops once that bin holds exactly the keys
 // still needed. Then the winners ("key > T, plus the first need_eq keys equal to T") are written
-// in ascending page order.
+// in ascending page order. Every pass issues kSelBatch independent loads per lane before using
+// them, so a pass over P keys costs about P / (128 kSelBatch) L2 round trips.
 __device__ __forceinline__ void warp_select_unit(const ScoreArgs &a, int unit, int P, int budget_in, int *hist) {
   const int lane = threadIdx.x & 31;
   int32_t *sel_row = a.selected + (size_t)unit * a.b_max;
@@ -90,16 +93,21 @@ __device__ __forceinline__ void warp_select_unit(const ScoreArgs &a, int unit, i
   if (k_free > 0) {
     // count, min and max of the candidate keys
     uint32_t cnt = 0, lo = 0xFFFFFFFFu, hi = 0u;
-    for (int g = lane; g < n4; g += 32) {
-      const uint4 k = load4(g);
-      const uint32_t ks[4] = {k.x, k.y, k.z, k.w};
+    for (int g0 = lane; g0 < n4; g0 += 32 * kSelBatch) {
+      uint4 kb[kSelBatch];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (ks[j] != 0u) {
-          ++cnt;
-          lo = min(lo, ks[j]);
-          hi = max(hi, ks[j]);
-        }
+      for (int b = 0; b < kSelBatch; ++b) kb[b] = g0 + 32 * b < n4 ? load4(g0 + 32 * b) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int b = 0; b < kSelBatch; ++b) {
+        const uint32_t ks[4] = {kb[b].x, kb[b].y, kb[b].z, kb[b].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (ks[j] != 0u) {
+            ++cnt;
+            lo = min(lo, ks[j]);
+            hi = max(hi, ks[j]);
+          }
+      }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -121,12 +129,18 @@ __device__ __forceinline__ void warp_select_unit(const ScoreArgs &a, int unit, i
 #pragma unroll
         for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0;
         __syncwarp();
-        for (int g = lane; g < n4; g += 32) {
-          const uint4 k = load4(g);
-          const uint32_t ks[4] = {k.x, k.y, k.z, k.w};
+        for (int g0 = lane; g0 < n4; g0 += 32 * kSelBatch) {
+          uint4 kb[kSelBatch];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (ks[j] != 0u && (ks[j] & mask) == prefix) atomicAdd(&hist[(ks[j] >> shift) & 255u], 1);
+          for (int b = 0; b < kSelBatch; ++b)
+            kb[b] = g0 + 32 * b < n4 ? load4(g0 + 32 * b) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int b = 0; b < kSelBatch; ++b) {
+            const uint32_t ks[4] = {kb[b].x, kb[b].y, kb[b].z, kb[b].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (ks[j] != 0u && (ks[j] & mask) == prefix) atomicAdd(&hist[(ks[j] >> shift) & 255u], 1);
+          }
         }
         __syncwarp();
         // lane l owns the digits 255 - 8l .. 248 - 8l: descending digit order is lane order
@@ -175,9 +189,11 @@ __device__ __forceinline__ void warp_select_unit(const ScoreArgs &a, int unit, i
     // winners in ascending page order: lane l holds pages 4l .. 4l + 3 of each 128-page block
     int run_eq = 0;
     int32_t *dst = sel_row + a.sink;
+    uint4 next = lane < n4 ? load4(lane) : make_uint4(0u, 0u, 0u, 0u);
     for (int g0 = 0; g0 < n4; g0 += 32) {
       const int g = g0 + lane;
-      const uint4 k = g < n4 ? load4(g) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 k = next;  // this block's keys; the next block's load is in flight meanwhile
+      next = g + 32 < n4 ? load4(g + 32) : make_uint4(0u, 0u, 0u, 0u);
       const uint32_t ks[4] = {k.x, k.y, k.z, k.w};
       int eq = 0;
       if (!take_all) {

@@ -60,6 +60,42 @@ def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int, sink
     return (near and forced_ok), near, got, ref
 
 
+MASS_REL = 1e-5  # page masses (fp32 vs fp64), relative to the unit's largest mass; sums: to its total
+
+
+def compare_coverage(gpu_row: np.ndarray, mass: np.ndarray, coverage: float, b_max: int, sink_pages: int = 1,
+                     window_pages: int = 1):
+    """Adaptive coverage: gpu_row must be a valid nucleus under the oracle's fp64 masses [P], up
+    to fp32 rounding of the masses (MASS_REL): ascending, -1 padded, the always-kept pages
+    included, at most b_max pages; every other page chosen outweighs every page left out (up to
+    the tolerance); the coverage target is reached unless b_max or the pages run out; and dropping
+    the lightest chosen page would fall short of it. Returns (ok, same_as_oracle, gpu, oracle)."""
+    ref = O.select_coverage(mass, coverage, b_max, sink_pages, window_pages)
+    got = [int(x) for x in gpu_row if x >= 0]
+    pad_ok = all(x < 0 for x in gpu_row[len(got):])
+    P = len(mass)
+    if got == ref and pad_ok:
+        return True, True, got, ref
+    forced = O.forced_pages(P, sink_pages, window_pages)
+    if not pad_ok or got != sorted(set(got)) or not set(forced) <= set(got) or len(got) > b_max:
+        return False, False, got, ref
+    if any(p < 0 or p >= P for p in got):
+        return False, False, got, ref
+    tol = MASS_REL * float(mass.max())
+    tol_sum = MASS_REL * float(mass.sum())
+    chosen = [p for p in got if p not in forced]
+    left = [p for p in range(P) if p not in got]
+    if chosen and left and max(mass[left]) > min(mass[chosen]) + tol:
+        return False, False, got, ref
+    target = coverage * float(mass.sum())
+    have = float(mass[got].sum())
+    if have < target - tol_sum and len(got) < b_max and left:
+        return False, False, got, ref
+    if chosen and have - float(min(mass[chosen])) >= target + tol_sum:
+        return False, False, got, ref
+    return True, False, got, ref
+
+
 def score_tolerance(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarray, dtype: str, scale: float) -> np.ndarray:
     """Per (kv head, page) bound on fp32 accumulation error of the page score."""
     qv, lo, hi = O.to_f64(q, dtype), O.to_f64(kmin, dtype), O.to_f64(kmax, dtype)

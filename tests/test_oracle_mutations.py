@@ -14,7 +14,7 @@ import test_oracle_pins as PINS
 
 ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention",
                                              "forced_pages", "retained_count", "quest_scores_per_query_head",
-                                             "cutoff_score")}
+                                             "cutoff_score", "page_masses", "select_coverage")}
 
 
 @pytest.fixture
@@ -103,6 +103,32 @@ def _cutoff_one_too_far(scores, budget, sink_pages=1, window_pages=1):  # the k_
     return float(scores[ranked[min(k_free, len(ranked) - 1)]])
 
 
+def _masses_per_page_softmax(q, keys, seq_len, page_size, dtype, scale):  # normalised within each page
+    m = ORIG["page_masses"](q, keys, seq_len, page_size, dtype, scale)
+    P = m.shape[1]
+    out = np.empty_like(m)
+    qv, k = O.to_f64(q, dtype), O.to_f64(keys[:seq_len], dtype)
+    G = qv.shape[0] // keys.shape[1]
+    for g in range(qv.shape[0]):
+        for p in range(P):
+            lg = scale * (k[p * page_size:min((p + 1) * page_size, seq_len), g // G] @ qv[g])
+            out[g, p] = 1.0 if len(lg) else 0.0
+    return out
+
+
+def _coverage_ignores_forced_mass(mass, coverage, b_max, sink_pages=1, window_pages=1):  # forced mass not counted
+    P = len(mass)
+    forced = O.forced_pages(P, sink_pages, window_pages)
+    target, have = coverage * float(mass.sum()), 0.0
+    chosen = []
+    for p in sorted((p for p in range(P) if p not in forced), key=lambda p: (-float(mass[p]), p)):
+        if have >= target or len(forced) + len(chosen) >= b_max:
+            break
+        chosen.append(p)
+        have += float(mass[p])
+    return sorted(forced + chosen)
+
+
 # ---- each one is caught -------------------------------------------------------------------
 def test_dropped_kmin_term_is_caught(plant):
     plant("quest_scores", _quest_kmax_only)
@@ -167,3 +193,18 @@ def test_cutoff_one_place_too_far_is_caught(plant, golden_dir):
         ex = json.load(f)
     _fails(PINS.test_golden_cutoff_score, ex)
     _fails(PINS.test_cutoff_score_is_the_weakest_winner_by_enumeration, 8)
+
+
+def test_masses_normalised_per_page_are_caught(plant):
+    plant("page_masses", _masses_per_page_softmax)
+    _fails(PINS.test_page_masses_normalise_and_match_library_softmax, 0)
+
+
+def test_coverage_ignoring_forced_mass_is_caught(plant, golden_dir):
+    plant("select_coverage", _coverage_ignores_forced_mass)
+    import json
+    import os
+    with open(os.path.join(golden_dir, "coverage_example.json")) as f:
+        cov = json.load(f)
+    _fails(PINS.test_golden_page_masses_and_coverage, cov)
+    _fails(PINS.test_coverage_selection_brute_force, 7)

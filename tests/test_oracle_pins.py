@@ -535,3 +535,93 @@ def test_workload_chunked_draws_are_consistent():
     bt = w.block_table
     live = np.concatenate([bt[j, :w.pages(w.final_lens)[j]] for j in range(w.B)])
     assert len(set(live.tolist())) == len(live) and live.max() < w.num_blocks
+
+
+# ------------------------------------------------------------------ S3 coverage mode
+@pytest.fixture(scope="module")
+def cov(golden_dir):
+    with open(os.path.join(golden_dir, "coverage_example.json")) as f:
+        return json.load(f)
+
+
+def _cov_keys(cov):
+    return np.log(np.asarray(cov["key_weights"], dtype=np.float64)).astype(np.float32)[:, None, None]
+
+
+def test_golden_page_masses_and_coverage(cov):
+    keys = _cov_keys(cov)
+    q1 = _f32(cov["q_one_head"])
+    m = O.page_masses(q1, keys, cov["seq_len"], cov["page_size"], "f32", 1.0)
+    assert np.allclose(m[0], cov["masses_one_head"], rtol=0, atol=1e-6)
+    for c, sel in cov["selected_one_head"].items():
+        assert O.select_coverage(m[0], float(c), 4) == sel, c
+    assert O.select_coverage(m[0], 0.9, 3) == cov["selected_one_head_b_max_3_c_0.9"]
+    q2 = _f32(cov["q_two_heads"])
+    g = O.group_masses(O.page_masses(q2, keys, cov["seq_len"], cov["page_size"], "f32", 1.0), 1)
+    assert np.allclose(g[0], cov["group_masses_two_heads"], rtol=0, atol=1e-6)
+    for c, sel in cov["selected_two_heads"].items():
+        assert O.select_coverage(g[0], float(c), 4) == sel, c
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_page_masses_normalise_and_match_library_softmax(seed):
+    """Each query head's page masses sum to one and equal the page sums of torch's float64
+    softmax over the sequence's logits; one page holds all the mass; identical keys give masses
+    proportional to the pages' token counts."""
+    rng = np.random.default_rng(seed)
+    ps, n, H_kv, G, D = 16, 16 * 9 + 5, 2, 3, 32
+    keys = rng.standard_normal((n + 7, H_kv, D)).astype(np.float32)
+    q = rng.standard_normal((H_kv * G, D)).astype(np.float32)
+    scale = 1 / math.sqrt(D)
+    m = O.page_masses(q, keys, n, ps, "f32", scale)
+    assert np.allclose(m.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    for g in range(H_kv * G):
+        logits = torch.from_numpy(keys[:n, g // G].astype(np.float64)) @ torch.from_numpy(q[g].astype(np.float64))
+        w = torch.softmax(logits * scale, dim=0).numpy()
+        ref = np.array([w[p * ps:(p + 1) * ps].sum() for p in range(-(-n // ps))])
+        assert np.allclose(m[g], ref, rtol=1e-12, atol=1e-15)
+    one = O.page_masses(q, keys, 11, ps, "f32", scale)
+    assert one.shape == (H_kv * G, 1) and np.allclose(one, 1.0)
+    same = np.repeat(keys[:1], n, axis=0)
+    m2 = O.page_masses(q, same, n, ps, "f32", scale)
+    counts = np.array([min(ps, n - p * ps) for p in range(-(-n // ps))]) / n
+    assert np.allclose(m2, counts[None, :], rtol=1e-12)
+    gm = O.group_masses(m, H_kv)
+    for h in range(H_kv):
+        assert np.array_equal(gm[h], m[h * G:(h + 1) * G].max(axis=0))
+    assert np.array_equal(O.group_masses(m, H_kv * G), m)
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 7, 9])
+def test_coverage_selection_brute_force(P):
+    """Against subset enumeration: the selection holds the always-kept pages; it reaches the
+    target unless the b_max cap or the pages run out; no smaller set holding the always-kept
+    pages reaches the target; and its other pages beat every page left out under
+    (mass desc, index asc), ties included."""
+    rng = np.random.default_rng(50 + P)
+    for trial in range(12):
+        if trial % 3 == 2:
+            mass = rng.integers(0, 4, size=P).astype(np.float64)   # ties and zero masses
+        else:
+            mass = rng.dirichlet(np.ones(P))
+        for S, Wn in ((1, 1), (0, 1), (2, 1)):
+            forced = sorted(set(range(min(S, P))) | set(range(max(0, P - Wn), P)))
+            others = [p for p in range(P) if p not in forced]
+            for c in (0.05, 0.5, 0.9, 0.999, 1.0):
+                target = c * mass.sum()
+                for b_max in range(len(forced), P + 1):
+                    sel = O.select_coverage(mass, c, b_max, S, Wn)
+                    assert sel == sorted(set(sel)) and set(forced) <= set(sel) and len(sel) <= b_max
+                    got = mass[sel].sum()
+                    assert got >= target or len(sel) == b_max or len(sel) == P
+                    need = None
+                    for k in range(len(others) + 1):
+                        if any(mass[forced].sum() + mass[list(sub)].sum() >= target
+                               for sub in itertools.combinations(others, k)):
+                            need = k
+                            break
+                    if need is not None:
+                        assert len(sel) - len(forced) == min(need, b_max - len(forced))
+                    chosen = [p for p in sel if p not in forced]
+                    left = [p for p in others if p not in chosen]
+                    assert all((mass[x], -x) > (mass[y], -y) for x in chosen for y in left)
