@@ -60,12 +60,10 @@ TRAFFIC = {
     # filled in from one-pass captures of the current kernels (measurement)
 }
 KERNEL_SOURCES = {
-    "page_score_kernel": ("score_select.cu", "select_common.cuh", "psk_common.cuh", "psk_internal.h"),
-    "page_score_kernel+page_select_kernel": ("score_select.cu", "select.cu", "select_common.cuh", "psk_common.cuh",
-                                             "psk_internal.h"),
+    "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
+    "page_select_kernel": ("select.cu", "select_common.cuh", "psk_common.cuh", "psk_internal.h"),
     "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),
-    "mla_qsplit_kernel+mla_score_kernel+page_select_kernel": ("mla.cu", "select.cu", "select_common.cuh",
-                                                              "psk_common.cuh", "psk_internal.h"),
+    "mla_qsplit_kernel+mla_score_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
     "mla_decode_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
 }
 
@@ -328,9 +326,17 @@ def run_psk(args):
         psk.page_score_select(L, q, cache.summaries, cache.block_table, cache.seq_lens, bud, w.b_max, cache.scale,
                               sel, ws)
 
-    # kernels one score + select call launches: 1 when the selection runs in the score kernel's
-    # last CTA per (sequence, head group), 2 with a separate selection launch, 3 for the latent form
+    # kernels one score + select call launches: 2 (score, selection), 3 for the latent form
     ss_launches = psk.score_select_launches(L, w.b_max)
+
+    # the same two stages as separate calls, so each kernel gets its own events in the eager loop
+    sel_prm = psk.select_params(budgets=bud)
+
+    def score_only():
+        psk.page_score(L, q, cache.summaries, cache.block_table, cache.seq_lens, sel_prm, w.b_max, cache.scale, ws)
+
+    def select_only():
+        psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
 
     def decode(dst=None):  # dst: the output buffer (default: `out` in device memory)
         o = out if dst is None else dst
@@ -404,7 +410,7 @@ def run_psk(args):
 
     K = args.steps
     Kd = max(3, K // 4)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     evd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
     evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     evgd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kd)]
@@ -419,10 +425,12 @@ def run_psk(args):
         e[0].record(stream)
         append()
         e[1].record(stream)
-        score()
+        score_only()
         e[2].record(stream)
-        decode()
+        select_only()
         e[3].record(stream)
+        decode()
+        e[4].record(stream)
     marks[1].record(stream)
     for k in range(Kd):
         flush_l2()
@@ -463,8 +471,9 @@ def run_psk(args):
         else:
             graph_sparse_ms = graph_dense_ms = float("nan")
     t_app = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
-    t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))  # score + select call
-    t_dec = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
+    t_score = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    t_select = statistics.mean(ev[k][2].elapsed_time(ev[k][3]) for k in range(K))
+    t_dec = statistics.mean(ev[k][3].elapsed_time(ev[k][4]) for k in range(K))
     if dist is not None:
         sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms = max_over_ranks(
             [sparse_ms, dense_ms, graph_sparse_ms, graph_dense_ms], dev)
@@ -546,15 +555,12 @@ def run_psk(args):
     pk = peaks()
     peak_hbm = pk["hbm"]
     flops_decode = 2 * Hq * (D + w.D_v) * sel_tokens  # QK^T and P.V over the selected tokens
-    # the dominant call by time (score + select, or decode), each timed by its own events
-    if t_score >= t_dec:
-        dom = {1: "page_score_kernel", 2: "page_score_kernel+page_select_kernel",
-               3: "mla_qsplit_kernel+mla_score_kernel+page_select_kernel"}[ss_launches]
+    # the dominant kernel by time (score, select or decode), each timed by its own events
+    if t_score >= t_dec and t_score >= t_select:
+        dom = "mla_qsplit_kernel+mla_score_kernel" if w.latent else "page_score_kernel"
         roof = {"bound": "hbm", "kernel": dom, "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
                 "unit": "GB/s", "algorithmic_per_launch": score_bytes, "algorithmic_unit": "B",
                 "launch_us": t_score * 1e3}
-        if ss_launches == 1:
-            roof["note"] = "one launch: the page scores and, in each sequence's last CTA, the top-b selection"
     elif w.latent:
         # arithmetic intensity ~300 flop/B, above the measured ridge (~250-290): tensor-bound
         dom = "mla_decode_kernel"
@@ -614,7 +620,8 @@ def run_psk(args):
         "speedup_vs_dense": step_dense_ms / step_ms,
         "eager": {"us_per_step": sparse_ms * 1e3, "dense_us_per_step": dense_ms * 1e3,
                   "speedup_vs_dense": dense_ms / sparse_ms},
-        "kernels_us": {"append": t_app * 1e3, "score_select": t_score * 1e3, "sparse_decode": t_dec * 1e3},
+        "kernels_us": {"append": t_app * 1e3, "score": t_score * 1e3, "select": t_select * 1e3,
+                       "score_select": (t_score + t_select) * 1e3, "sparse_decode": t_dec * 1e3},
         "score_select_launches": ss_launches,
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "timing": ("CUDA-graph replay" if e2e_ms != e2e_eager_ms else "eager launches")

@@ -162,6 +162,22 @@ int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, con
                                 const int32_t *block_table, void *workspace, size_t workspace_bytes,
                                 psk_stream_t stream);
 
+/* The same with an optional second summary store (EntmaxKV README, introduction: pages are
+ * scored from per-page key statistics, "mean/std for Gaussian"; repository layout,
+ * gaussian/page_metadata.py, "Per-page k_mean / k_std refresh"):
+ *   stats  fp32 [num_blocks, num_kv_heads, 2, head_dim], device memory, indexed by physical
+ *          block: the elementwise mean of the page's valid keys at [...,0,:] and their population
+ *          standard deviation (divisor = the page's token count) at [...,1,:].
+ * Every page the call touches gets both recomputed in fp32 from all of its tokens below
+ * start_pos[i] + n_i (two passes over the page's rows in the cache), so they never drift from a
+ * rebuild. summaries or stats may be NULL (not both); psk_kv_append_and_summarize is this call
+ * with stats = NULL. */
+int psk_kv_append_and_summarize_ex(const psk_layout *layout, const void *k_new, const void *v_new,
+                                   const int32_t *start_pos, const int32_t *cu_new, int32_t total_new,
+                                   int32_t max_new, void *k_cache, void *v_cache, void *summaries,
+                                   float *stats, const int32_t *block_table, void *workspace,
+                                   size_t workspace_bytes, psk_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Stages 2 + 3: page scores and top-b selection.
  *
@@ -234,11 +250,30 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
                              int32_t *selected, float *scores_out, void *workspace,
                              size_t workspace_bytes, psk_stream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Stages 2 + 3 with the Gaussian page score instead of the bound (EntmaxKV README, "Two
+ * selection strategies", Gaussian-aware: each page's scores modelled as a Gaussian, pages kept
+ * whose estimated maximum is high). From the mean / std store of psk_kv_append_and_summarize_ex:
+ *   score[i,h,p] = scale * max_{g in group(h)} (q[i,g] . mean[p,h]
+ *                                                + z * sqrt(sum_d (q[i,g,d] * std[p,h,d])^2)),
+ * i.e. the page's logits modelled as a Gaussian with independent dimensions and its maximum
+ * estimated as mean + z standard deviations (z chosen by the caller, e.g. 1.5 to 2.5 for 16-
+ * token pages). The top-b pages are then selected exactly as psk_page_score_select_ex does
+ * (params: budget modes, sink / window pages; per_query_head must be 0). GQA only (head_dim 64
+ * or 128). The threshold solve of the entmax normaliser that the Gaussian selector uses is not
+ * part of this library: pages are ranked by the estimated maximum and the budget decides how
+ * many are kept. Same workspace as psk_page_score_select_ex.
+ * --------------------------------------------------------------------------------------- */
+int psk_page_score_select_gaussian(const psk_layout *layout, const void *q, const float *stats,
+                                   const int32_t *block_table, const int32_t *seq_lens,
+                                   const psk_select_params *params, int32_t b_max, float scale,
+                                   float z, int32_t *selected, float *scores_out, void *workspace,
+                                   size_t workspace_bytes, psk_stream_t stream);
+
 /* Kernel launches one psk_page_score_select_ex call makes for this layout, b_max and
- * per_query_head (0 when the layout is invalid or unsupported): 1 when every unit fits one
- * selection chunk (the score kernel's last CTA of each (sequence, head group) selects its
- * units), 2 with a separate selection launch, 3 for the latent form (query split, score,
- * selection). Useful for sizing CUDA graphs and counting launches. */
+ * per_query_head (0 when the layout is invalid or unsupported): 2 for GQA caches (score,
+ * selection), 3 for the latent form (query split, score, selection). Useful for sizing CUDA
+ * graphs and counting launches. */
 int psk_score_select_launches(const psk_layout *layout, int32_t b_max, int32_t per_query_head);
 
 /* ---------------------------------------------------------------------------------------

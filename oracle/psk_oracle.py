@@ -31,6 +31,9 @@ online softmax or algebraic rewriting:
                          may come from a fraction of the pages or a fixed page count
                          (same table; the fraction rounds by the retained-count rule
                          of the vllm-rlt pull request #157 discussion).
+  S2 Gaussian score   -- per-page key mean / std (EntmaxKV "mean/std for Gaussian") and the
+                         estimated page maximum q.mean + z * sqrt(sum (q std)^2), max over the
+                         group, times scale.
   S3 coverage mode    -- adaptive per-head nucleus coverage over exact page masses (LOCKS
                          configuration table `coverage`; AMASS "Key AmassConfig fields"): the
                          softmax mass of every page, max over the GQA group, and the fewest
@@ -53,6 +56,10 @@ points the pages leave open:
   * the scale 1/sqrt(D) is applied after the group max and is the same scale
     used for the attention logits;
   * for a latent (MLA) cache the value is the first D_v dims of the latent key;
+  * mean / std summaries: population standard deviation (divisor n) over the page's valid
+    tokens; the Gaussian score treats the key dimensions as independent and its estimated
+    maximum is mean + z * std with z chosen by the caller, ranked top-b like the bound (the
+    entmax threshold the EntmaxKV selector solves for is out of scope);
   * coverage: a page's mass is its exact softmax mass for a query head over every token of the
     sequence; a KV head's page mass is the max over its group's query heads; the always-kept
     pages are selected and their mass counts toward the target, which is the coverage fraction
@@ -143,6 +150,26 @@ def summary_after_append(kmin: np.ndarray, kmax: np.ndarray, k_new: np.ndarray, 
     return exact_to_storage(lo, dtype), exact_to_storage(hi, dtype)
 
 
+def page_mean_std(keys: np.ndarray, seq_len: int, page_size: int, dtype: str):
+    """Per-page, per-KV-head elementwise key mean and standard deviation (EntmaxKV README,
+    introduction: pages are scored from per-page key statistics, "mean/std for Gaussian";
+    repository layout, gaussian/page_metadata.py, "Per-page k_mean / k_std refresh"). The
+    standard deviation is the population one (divisor n, the page's valid token count); tokens
+    at or past seq_len are not part of any page. keys [T >= seq_len, H_kv, D] stored. Returns
+    float64 (mean, std), each [P, H_kv, D]."""
+    P = -(-seq_len // page_size)
+    vals = to_f64(keys[:seq_len], dtype)
+    H, D = vals.shape[1], vals.shape[2]
+    mean = np.empty((P, H, D))
+    std = np.empty((P, H, D))
+    for p in range(P):
+        page = vals[p * page_size:min((p + 1) * page_size, seq_len)]
+        n = page.shape[0]
+        mean[p] = page.sum(axis=0) / n
+        std[p] = np.sqrt(((page - mean[p]) ** 2).sum(axis=0) / n)
+    return mean, std
+
+
 # ----------------------------------------------------------------------------------
 # S2: page score
 # ----------------------------------------------------------------------------------
@@ -183,6 +210,33 @@ def quest_scores_per_query_head(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarra
     for g in range(H_q):
         h = g // G
         out[g] = np.maximum(qv[g] * lo[:, h, :], qv[g] * hi[:, h, :]).sum(axis=1) * scale
+    return out
+
+
+def gaussian_scores(q: np.ndarray, mean: np.ndarray, std: np.ndarray, dtype: str, scale: float, z: float) -> np.ndarray:
+    """Gaussian page score from the mean / std summaries (EntmaxKV README, "Two selection
+    strategies", Gaussian-aware: each page's scores modelled as a Gaussian, pages kept whose
+    estimated maximum is high). For query head g and page p the logits q_g . k_t of the page's
+    tokens are modelled as a Gaussian with mean q_g . mean_p and variance
+    sum_d q_gd^2 std_pd^2 (dimensions taken as independent); the page's estimated maximum is
+    mean + z * std. Combined over the GQA group by max and scaled like the bound:
+
+      score[h, p] = scale * max_{g in group(h)} (q_g . mean_p + z * sqrt(sum_d q_gd^2 std_pd^2)).
+
+    q [H_q, D] stored; mean, std [P, H_kv, D] float64. Returns float64 [H_kv, P]."""
+    qv = to_f64(q, dtype)
+    H_q = qv.shape[0]
+    P, H_kv, D = mean.shape
+    G = H_q // H_kv
+    out = np.empty((H_kv, P))
+    for h in range(H_kv):
+        per_head = np.empty((G, P))
+        for j in range(G):
+            g = h * G + j
+            mu = mean[:, h, :] @ qv[g]
+            sd = np.sqrt((std[:, h, :] ** 2) @ (qv[g] ** 2))
+            per_head[j] = mu + z * sd
+        out[h] = per_head.max(axis=0) * scale
     return out
 
 

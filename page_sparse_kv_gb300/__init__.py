@@ -27,6 +27,7 @@ EXPORTS = [
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version", "psk_selftest_bounded_wait",
     "psk_score_select_launches", "psk_page_select_coverage", "psk_coverage_workspace_size",
+    "psk_kv_append_and_summarize_ex", "psk_page_score_select_gaussian",
 ]
 
 
@@ -108,6 +109,9 @@ def lib() -> ctypes.CDLL:
             "psk_score_select_launches": (ctypes.c_int, [LP, I, I]),
             "psk_page_select_coverage": (ctypes.c_int, [LP, P, P, P, P, ctypes.c_double, I, I, I, F, P, P, P, Z, P]),
             "psk_coverage_workspace_size": (Z, [LP, I]),
+            "psk_kv_append_and_summarize_ex": (ctypes.c_int, [LP, P, P, P, P, I, I, P, P, P, P, P, P, Z, P]),
+            "psk_page_score_select_gaussian": (ctypes.c_int, [LP, P, P, P, P, ctypes.POINTER(PskSelectParams), I, F,
+                                                              F, P, P, P, Z, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -199,6 +203,30 @@ def kv_append_and_summarize(layout: Layout, k_new, v_new, start_pos, cu_new, max
     _check("psk_kv_append_and_summarize", lib().psk_kv_append_and_summarize(
         ctypes.byref(layout.c()), _ptr(k_new), _ptr(v_new), _ptr(start_pos), _ptr(cu_new), total_new,
         int(max_new), _ptr(k_cache), _ptr(v_cache), _ptr(summaries), _ptr(block_table), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kv_append_and_summarize_ex(layout: Layout, k_new, v_new, start_pos, cu_new, max_new: int, k_cache, v_cache,
+                               summaries, stats, block_table, workspace, stream=None):
+    """kv_append_and_summarize that also (or only) keeps the fp32 per-page key mean / std store
+    ``stats`` [num_blocks, num_kv_heads, 2, head_dim]; either store may be None, not both."""
+    total_new = int(k_new.shape[0]) if k_new is not None else 0
+    _check("psk_kv_append_and_summarize_ex", lib().psk_kv_append_and_summarize_ex(
+        ctypes.byref(layout.c()), _ptr(k_new), _ptr(v_new), _ptr(start_pos), _ptr(cu_new), total_new,
+        int(max_new), _ptr(k_cache), _ptr(v_cache), _ptr(summaries), _ptr(stats), _ptr(block_table),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def page_score_select_gaussian(layout: Layout, q, stats, block_table, seq_lens, b_max: int, scale: float, z: float,
+                               selected, workspace, *, budgets=None, budget_pages: int | None = None,
+                               budget_fraction: float | None = None, sink_pages: int = 1, window_pages: int = 1,
+                               scores_out=None, stream=None):
+    """Top-b pages by the Gaussian estimated maximum from the mean / std store (see psk.h)."""
+    prm = select_params(budgets=budgets, budget_pages=budget_pages, budget_fraction=budget_fraction,
+                        sink_pages=sink_pages, window_pages=window_pages)
+    _check("psk_page_score_select_gaussian", lib().psk_page_score_select_gaussian(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(stats), _ptr(block_table), _ptr(seq_lens), ctypes.byref(prm),
+        int(b_max), float(scale), float(z), _ptr(selected), _ptr(scores_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

@@ -99,8 +99,7 @@ int psk_score_select_launches(const psk_layout *layout, int32_t b_max, int32_t p
   if (per_query_head && !per_query_head_view(*layout, &U, &kv_shift)) return 0;
   ScorePlan plan;
   if (!plan_score(U, b_max, &plan, kv_shift)) return 0;
-  if (layout->latent) return 3;
-  return (plan.n_chunks_max == 1 && tuning().score_fused_select) ? 1 : 2;
+  return layout->latent ? 3 : 2;
 }
 
 static bool plan_any_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan) {
@@ -141,20 +140,21 @@ int psk_clear_device_status(void *workspace, psk_stream_t stream) {
   return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
 }
 
-int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, const void *v_new,
-                                const int32_t *start_pos, const int32_t *cu_new, int32_t total_new,
-                                int32_t max_new, void *k_cache, void *v_cache, void *summaries,
-                                const int32_t *block_table, void *workspace, size_t workspace_bytes,
-                                psk_stream_t stream) {
+int psk_kv_append_and_summarize_ex(const psk_layout *layout, const void *k_new, const void *v_new,
+                                   const int32_t *start_pos, const int32_t *cu_new, int32_t total_new,
+                                   int32_t max_new, void *k_cache, void *v_cache, void *summaries, float *stats,
+                                   const int32_t *block_table, void *workspace, size_t workspace_bytes,
+                                   psk_stream_t stream) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
   if (total_new < 0 || max_new < 0) return PSK_ERR_INVALID_ARG;
-  if (!start_pos || !cu_new || !k_cache || !summaries || !block_table) return PSK_ERR_INVALID_ARG;
+  if (!start_pos || !cu_new || !k_cache || !block_table || (!summaries && !stats)) return PSK_ERR_INVALID_ARG;
   if (L.latent ? (v_new != nullptr || v_cache != nullptr) : (!v_cache || (total_new > 0 && !v_new)))
     return PSK_ERR_INVALID_ARG;
   if (total_new > 0 && !k_new) return PSK_ERR_INVALID_ARG;
-  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(summaries))
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(summaries) || !aligned16(stats))
     return PSK_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < kWsHeader) return PSK_ERR_WORKSPACE;
   if (total_new == 0 || max_new == 0) return PSK_OK;
@@ -166,6 +166,7 @@ int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, con
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.summaries = summaries;
+  a.stats = stats;
   a.block_table = block_table;
   a.ws = workspace;
   a.B = L.batch;
@@ -176,6 +177,16 @@ int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, con
   a.nb = L.num_blocks;
   a.max_pages = L.max_pages;
   return cuda_status(launch_append(a, L.dtype, max_new, static_cast<cudaStream_t>(stream)));
+}
+
+int psk_kv_append_and_summarize(const psk_layout *layout, const void *k_new, const void *v_new,
+                                const int32_t *start_pos, const int32_t *cu_new, int32_t total_new,
+                                int32_t max_new, void *k_cache, void *v_cache, void *summaries,
+                                const int32_t *block_table, void *workspace, size_t workspace_bytes,
+                                psk_stream_t stream) {
+  if (!summaries) return PSK_ERR_INVALID_ARG;
+  return psk_kv_append_and_summarize_ex(layout, k_new, v_new, start_pos, cu_new, total_new, max_new, k_cache, v_cache,
+                                        summaries, nullptr, block_table, workspace, workspace_bytes, stream);
 }
 
 int psk_page_score_select(const psk_layout *layout, const void *q, const void *summaries,
@@ -208,7 +219,8 @@ static long long scalar_mode_budget(const psk_select_params &sp, long long P) {
 static int score_select_common(const psk_layout *layout, const void *q, const void *summaries,
                                const int32_t *block_table, const int32_t *seq_lens, const psk_select_params *params,
                                int32_t b_max, float scale, int32_t *selected, float *scores_out, void *workspace,
-                               size_t workspace_bytes, psk_stream_t stream, int stages) {
+                               size_t workspace_bytes, psk_stream_t stream, int stages, const float *gauss_stats = nullptr,
+                               float gauss_z = 0.f) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
@@ -232,6 +244,9 @@ static int score_select_common(const psk_layout *layout, const void *q, const vo
   if (do_score && (!aligned16(q) || !aligned16(summaries))) return PSK_ERR_INVALID_ARG;
   rc = check_gqa_compute(layout);
   if (rc != PSK_OK) return rc;
+  if (gauss_stats && (L.latent || sp.per_query_head ||
+                      !gauss_supported(L.dtype, L.head_dim, L.num_q_heads / L.num_kv_heads)))
+    return PSK_ERR_UNSUPPORTED;
   // the units' layout: the cache's own, or its per-query-head view
   psk_layout U = L;
   int kv_shift = 0;
@@ -276,8 +291,9 @@ static int score_select_common(const psk_layout *layout, const void *q, const vo
   a.budget_mode = sp.mode;
   a.budget_pages = sp.budget_pages;
   a.budget_frac = sp.budget_fraction;
-  a.fused_select = 0;  // chosen by the GQA launcher
   a.unit_budgets = nullptr;
+  if (gauss_stats)
+    return cuda_status(launch_gauss_score_select(a, gauss_stats, gauss_z, L.dtype, static_cast<cudaStream_t>(stream)));
   if (L.latent)
     return cuda_status(launch_mla_score_select(a, reinterpret_cast<uint16_t *>(ws + plan.off_qsplit),
                                                static_cast<cudaStream_t>(stream), stages));
@@ -290,6 +306,16 @@ int psk_page_score_select_ex(const psk_layout *layout, const void *q, const void
                              size_t workspace_bytes, psk_stream_t stream) {
   return score_select_common(layout, q, summaries, block_table, seq_lens, params, b_max, scale, selected, scores_out,
                              workspace, workspace_bytes, stream, kStageScore | kStageSelect);
+}
+
+int psk_page_score_select_gaussian(const psk_layout *layout, const void *q, const float *stats,
+                                   const int32_t *block_table, const int32_t *seq_lens,
+                                   const psk_select_params *params, int32_t b_max, float scale, float z,
+                                   int32_t *selected, float *scores_out, void *workspace, size_t workspace_bytes,
+                                   psk_stream_t stream) {
+  if (!stats || !(z == z)) return PSK_ERR_INVALID_ARG;
+  return score_select_common(layout, q, stats, block_table, seq_lens, params, b_max, scale, selected, scores_out,
+                             workspace, workspace_bytes, stream, kStageScore | kStageSelect, stats, z);
 }
 
 int psk_page_score(const psk_layout *layout, const void *q, const void *summaries, const int32_t *block_table,

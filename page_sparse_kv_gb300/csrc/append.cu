@@ -1,6 +1,8 @@
 // Stage 1: write appended tokens into the paged cache and refresh the per-page, per-KV-head
 // elementwise key min / max summaries (EntmaxKV README, kernels/page_metadata.py "per-page
-// k_min / k_max refresh"; the decode call appends k_new / v_new before scoring).
+// k_min / k_max refresh"; the decode call appends k_new / v_new before scoring) and, when asked,
+// the per-page key mean / std summaries (EntmaxKV README, introduction, "mean/std for
+// Gaussian"; gaussian/page_metadata.py "Per-page k_mean / k_std refresh").
 //
 // One CTA per (sequence, touched page). Each thread owns one 16-byte chunk of a token row
 // (H_kv * D elements) and walks the page's new tokens: it copies the chunk into the cache
@@ -48,6 +50,55 @@ template <typename T>
 __device__ __forceinline__ uint4 chunk_max(uint4 a, uint4 b) {
   return make_uint4(MinMax<T>::hi_word(a.x, b.x), MinMax<T>::hi_word(a.y, b.y), MinMax<T>::hi_word(a.z, b.z),
                     MinMax<T>::hi_word(a.w, b.w));
+}
+
+// Mean and population standard deviation of the page's valid tokens [0, n_valid) for the
+// elements of chunk c (one KV head's EPC consecutive dims), in fp32 by two passes over the
+// cache rows, written to stats. The rows this thread wrote in this launch are its own chunk's, so
+// program order makes them visible to it.
+template <typename T>
+__device__ __forceinline__ void refresh_page_stats(const AppendArgs &a, int blk, int n_valid, int c) {
+  constexpr int EPC = Elem<T>::kPerChunk;
+  const int cpr_k = a.D / EPC;
+  const int h = c / cpr_k;
+  const int e0 = (c - h * cpr_k) * EPC;
+  const size_t row_k = (size_t)a.H_kv * a.D;
+  const T *kc = reinterpret_cast<const T *>(a.k_cache) + (size_t)blk * a.ps * row_k + (size_t)c * EPC;
+  float sum[EPC];
+#pragma unroll
+  for (int e = 0; e < EPC; ++e) sum[e] = 0.f;
+  for (int r = 0; r < n_valid; ++r) {
+    float2 f[EPC / 2];
+    Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(kc + (size_t)r * row_k), f);
+#pragma unroll
+    for (int e = 0; e < EPC / 2; ++e) {
+      sum[2 * e] += f[e].x;
+      sum[2 * e + 1] += f[e].y;
+    }
+  }
+  const float inv_n = 1.f / (float)n_valid;
+  float mean[EPC], m2[EPC];
+#pragma unroll
+  for (int e = 0; e < EPC; ++e) {
+    mean[e] = sum[e] * inv_n;
+    m2[e] = 0.f;
+  }
+  for (int r = 0; r < n_valid; ++r) {
+    float2 f[EPC / 2];
+    Elem<T>::to_f2(*reinterpret_cast<const uint4 *>(kc + (size_t)r * row_k), f);
+#pragma unroll
+    for (int e = 0; e < EPC / 2; ++e) {
+      const float d0 = f[e].x - mean[2 * e], d1 = f[e].y - mean[2 * e + 1];
+      m2[2 * e] = fmaf(d0, d0, m2[2 * e]);
+      m2[2 * e + 1] = fmaf(d1, d1, m2[2 * e + 1]);
+    }
+  }
+  float *dst = a.stats + ((size_t)blk * a.H_kv + h) * 2 * a.D + e0;
+#pragma unroll
+  for (int e = 0; e < EPC; ++e) {
+    dst[e] = mean[e];
+    dst[a.D + e] = sqrtf(m2[e] * inv_n);
+  }
 }
 
 template <typename T>
@@ -101,9 +152,9 @@ __global__ void append_summarize_kernel(AppendArgs a) {
     if (c < nck) {
       const int h = c / cpr_k;
       const int e0 = (c - h * cpr_k) * EPC;
-      sum_lo = sm + ((size_t)blk * a.H_kv + h) * 2 * a.D + e0;
+      if (sm) sum_lo = sm + ((size_t)blk * a.H_kv + h) * 2 * a.D + e0;
       x = __ldg(reinterpret_cast<const uint4 *>(kn + (size_t)(c0 + t - s0) * row_k + (size_t)c * EPC));
-      if (!fresh) {
+      if (!fresh && sm) {
         olo = *reinterpret_cast<const uint4 *>(sum_lo);
         ohi = *reinterpret_cast<const uint4 *>(sum_lo + a.D);
       }
@@ -111,23 +162,26 @@ __global__ void append_summarize_kernel(AppendArgs a) {
     if (c < ncv) xv = __ldg(reinterpret_cast<const uint4 *>(vn + (size_t)(c0 + t - s0) * row_v + (size_t)c * EPC));
     if (c < nck) {
       *reinterpret_cast<uint4 *>(kc + ((size_t)blk * ps + (t - p * ps)) * row_k + (size_t)c * EPC) = x;
-      *reinterpret_cast<uint4 *>(sum_lo) = fresh ? x : chunk_min<T>(olo, x);
-      *reinterpret_cast<uint4 *>(sum_lo + a.D) = fresh ? x : chunk_max<T>(ohi, x);
+      if (sm) {
+        *reinterpret_cast<uint4 *>(sum_lo) = fresh ? x : chunk_min<T>(olo, x);
+        *reinterpret_cast<uint4 *>(sum_lo + a.D) = fresh ? x : chunk_max<T>(ohi, x);
+      }
     }
     if (c < ncv) *reinterpret_cast<uint4 *>(vc + ((size_t)blk * ps + (t - p * ps)) * row_v + (size_t)c * EPC) = xv;
+    if (a.stats && c < nck) refresh_page_stats<T>(a, blk, t_hi - p * ps, c);
     return;
   }
 
   for (int c = threadIdx.x; c < nck; c += blockDim.x) {
     const int h = c / cpr_k;
     const int e0 = (c - h * cpr_k) * EPC;
-    T *sum_lo = sm + ((size_t)blk * a.H_kv + h) * 2 * a.D + e0;
-    T *sum_hi = sum_lo + a.D;
+    T *sum_lo = sm ? sm + ((size_t)blk * a.H_kv + h) * 2 * a.D + e0 : nullptr;
+    T *sum_hi = sm ? sum_lo + a.D : nullptr;
     uint4 lo, hi;
     int t = t_lo;
     const uint4 first = *reinterpret_cast<const uint4 *>(kn + (size_t)(c0 + t - s0) * row_k + (size_t)c * EPC);
     *reinterpret_cast<uint4 *>(kc + ((size_t)blk * ps + (t - p * ps)) * row_k + (size_t)c * EPC) = first;
-    if (fresh) {
+    if (fresh || !sm) {
       lo = first;
       hi = first;
     } else {
@@ -140,8 +194,11 @@ __global__ void append_summarize_kernel(AppendArgs a) {
       lo = chunk_min<T>(lo, x);
       hi = chunk_max<T>(hi, x);
     }
-    *reinterpret_cast<uint4 *>(sum_lo) = lo;
-    *reinterpret_cast<uint4 *>(sum_hi) = hi;
+    if (sm) {
+      *reinterpret_cast<uint4 *>(sum_lo) = lo;
+      *reinterpret_cast<uint4 *>(sum_hi) = hi;
+    }
+    if (a.stats) refresh_page_stats<T>(a, blk, t_hi - p * ps, c);
   }
 
   for (int c = threadIdx.x; c < ncv; c += blockDim.x) {

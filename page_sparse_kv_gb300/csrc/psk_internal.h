@@ -16,7 +16,8 @@ struct AppendArgs {
   const int32_t *cu_new;
   void *k_cache;
   void *v_cache;
-  void *summaries;
+  void *summaries;    // k_min / k_max summaries (storage dtype), or NULL
+  float *stats;       // fp32 [num_blocks, H_kv, 2, D] key mean / std per page, or NULL
   const int32_t *block_table;
   void *ws;
   int B, H_kv, D, D_v, ps, nb, max_pages;
@@ -57,8 +58,6 @@ struct ScoreArgs {
   int budget_mode;        // enum psk_budget_mode
   int budget_pages;       // PSK_BUDGET_PAGES
   double budget_frac;     // PSK_BUDGET_FRACTION
-  int fused_select;       // 1: the score kernel's last CTA of each (sequence, head group) selects
-                          // its units (one selection chunk per unit); no separate select launch
   const int32_t *unit_budgets;  // non-null: per-unit budgets (coverage mode) instead of budgets[i]
 };
 
@@ -128,6 +127,10 @@ __host__ __device__ inline int split_off(int s, int sw, int taper) {
 }
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);
 bool decode_supported(int dtype, int D, int D_v, int G, int ps);
+
+// Gaussian page score from the mean / std summaries (gauss.cu): keys for the selection kernel
+cudaError_t launch_gauss_score_select(const ScoreArgs &a, const float *stats, float z, int dtype, cudaStream_t s);
+bool gauss_supported(int dtype, int D, int G);
 
 // adaptive per-head coverage over exact page masses (coverage.cu)
 struct CoverageArgs {

@@ -19,7 +19,6 @@
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
-#include "select_common.cuh"
 
 namespace psk {
 namespace {
@@ -131,14 +130,7 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   const int h0 = (x / a.B) * hpc;
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
-  if (seq_len < 1 || P > a.max_pages) {
-    // reported by the selection: here (fused) by the group's first body CTA, else the select kernel
-    if (a.fused_select && !in_tail && c == 0) {
-      if (tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
-      for (int x = tid; x < hpc * a.b_max; x += kThreads) a.selected[(size_t)(i * a.H_kv + h0) * a.b_max + x] = -1;
-    }
-    return;
-  }
+  if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
   const int body_end = P - min(P, a.tail_pages);
   const int p0 = in_tail ? body_end + c * a.tail_chunk : c * a.pchunk;
   const int p1 = in_tail ? min(P, p0 + a.tail_chunk) : min(body_end, p0 + a.pchunk);
@@ -299,26 +291,6 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
       produce(st + kStages, next_blk);
     }
   }
-  if (a.fused_select) {
-    // The CTAs of this (sequence, head group) that hold pages: ceil(body_end / pchunk) in the body
-    // region and ceil((P - body_end) / tail_chunk) in the tail region. The last of them to finish
-    // (atomic ticket, no waiting) selects the group's units, one warp per unit, from the keys every
-    // one of them wrote; its shared-memory ring is idle by now (every copy has landed).
-    __shared__ int last_flag;
-    const int n_ctas = (body_end + a.pchunk - 1) / a.pchunk + (P - body_end + a.tail_chunk - 1) / a.tail_chunk;
-    const int ticket = i * (a.H_kv / hpc) + h0 / hpc;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) last_flag = atomicAdd(&a.counters[ticket], 1u) == (unsigned)(n_ctas - 1);
-    __syncthreads();
-    if (last_flag) {
-      __threadfence();
-      if (tid == 0) a.counters[ticket] = 0u;
-      const int budget_in = a.budget_mode == PSK_BUDGET_PER_SEQUENCE ? a.budgets[i] : 0;
-      int *hist = reinterpret_cast<int *>(smem_raw) + warp * 256;
-      for (int u = warp; u < hpc; u += kWarps) warp_select_unit(a, i * a.H_kv + h0 + u, P, budget_in, hist);
-    }
-  }
   // released here rather than at the start: select CTAs made resident early would sit waiting
   // through this grid's drain
   pdl_trigger();
@@ -353,12 +325,10 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
     b.tail_chunks = (b.tail_pages + b.tail_chunk - 1) / b.tail_chunk;
     b.body_chunks = (a.max_pages + a.pchunk - 1) / a.pchunk;
   }
-  // one selection chunk per unit: the score kernel selects (fused); otherwise the select kernel
-  b.fused_select = (stages & kStageSelect) && a.n_chunks_max == 1 && tuning().score_fused_select ? 1 : 0;
   const long long n_ctas = (long long)(b.body_chunks + b.tail_chunks) * b.B * (b.H_kv / hpc);
   if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
   const cudaError_t e = launch_kernel(true, kfn, (unsigned)n_ctas, kThreads, k1_smem, s, b);
-  if (e != cudaSuccess || !(stages & kStageSelect) || b.fused_select) return e;
+  if (e != cudaSuccess || !(stages & kStageSelect)) return e;
   return launch_page_select(b, s);
 }
 

@@ -38,9 +38,10 @@ F32_ROW_REL = 1e-5
 
 
 def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int, sink_pages: int = 1,
-                      window_pages: int = 1):
-    """gpu_row: int32 [b_max] (ascending ids, -1 padded); scores: oracle fp64 [P].
-    Returns (ok, near_tie, gpu_ids, oracle_ids)."""
+                      window_pages: int = 1, near_rel: float = NEAR_TIE_REL):
+    """gpu_row: int32 [b_max] (ascending ids, -1 padded); scores: oracle fp64 [P]. near_rel: the
+    near-tie band relative to the cutoff score (1e-6 for the bound; wider for scores built from
+    fp32 statistics). Returns (ok, near_tie, gpu_ids, oracle_ids)."""
     ref = O.select_pages(scores, budget, sink_pages, window_pages)
     got = [int(x) for x in gpu_row if x >= 0]
     pad_ok = all(x < 0 for x in gpu_row[len(got):])
@@ -53,7 +54,7 @@ def compare_selection(gpu_row: np.ndarray, scores: np.ndarray, budget: int, sink
     diff = set(got) ^ set(ref)
     if cut is None:
         return False, False, got, ref
-    near = all(abs(scores[p] - cut) <= NEAR_TIE_REL * abs(cut) for p in diff)
+    near = all(abs(scores[p] - cut) <= near_rel * abs(cut) for p in diff)
     forced_ok = set(O.forced_pages(len(scores), sink_pages, window_pages)) <= set(got)
     if near and forced_ok:
         _log(True, diff, scores, cut)

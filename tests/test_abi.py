@@ -174,12 +174,11 @@ def test_workspace_sizes_cover_every_form(lib):
 
 
 def test_score_select_launch_count(lib):
-    """One launch when every unit fits one selection chunk (the selection runs in the score
-    kernel), two when the selection needs its own chunked launch, three for the latent form."""
+    """Two launches for GQA caches (score, selection), three for the latent form."""
     import page_sparse_kv_gb300 as psk
     batched = psk.Layout(64, 32, 8, 128, 128, 16, 150000, 4096)
-    assert psk.score_select_launches(batched, 205) == 1
-    assert psk.score_select_launches(batched, 205, per_query_head=True) == 1
+    assert psk.score_select_launches(batched, 205) == 2
+    assert psk.score_select_launches(batched, 205, per_query_head=True) == 2
     long_ctx = psk.Layout(1, 32, 8, 128, 128, 16, 65536, 65536)
     assert psk.score_select_launches(long_ctx, 128) == 2
     latent = psk.Layout(16, 128, 1, 576, 512, 64, 40000, 2048, psk.PSK_BF16, 1)

@@ -122,95 +122,3 @@ def test_radix_select_with_early_exit_is_the_top_k():
         for early in (False, True):
             T, need_eq = _radix_select(keys, k, early)
             assert sorted(_compact(keys, T, need_eq)) == sorted(ref)
-
-
-# ------------------------------------------------------------------ 3. one-warp selection of a unit
-def _warp_select(keys, P, k_free):
-    """Model of warp_select_unit's index logic (select_common.cuh), 32 lanes emulated: the keys
-    are read in four-key groups (group g -> lane g % 32), lane l owns the 8 digits
-    255 - 8l .. 248 - 8l of each pass's histogram, the crossing lane is found by a scan over the
-    lanes, and the winners are written by running prefix sums over 128-key blocks. Returns the
-    winners in the order they are written."""
-    n4 = (P + 3) // 4
-    grp = [[keys[4 * g + j] if 4 * g + j < P else 0 for j in range(4)] for g in range(n4)]
-    nz = [x for g in grp for x in g if x]
-    take_all = len(nz) <= k_free
-    T, need = 0, k_free
-    if not take_all:
-        lo, hi = min(nz), max(nz)
-        diff = lo ^ hi
-        top = diff.bit_length() - 1 if diff else 0
-        shift = top - 7 if top >= 7 else 0
-        prefix = 0 if shift + 8 >= 32 else (lo >> (shift + 8)) << (shift + 8)
-        mask = 0 if shift + 8 >= 32 else (0xFFFFFFFF << (shift + 8)) & 0xFFFFFFFF
-        while True:
-            hist = [0] * 256
-            for g in grp:
-                for x in g:
-                    if x and (x & mask) == prefix:
-                        hist[(x >> shift) & 255] += 1
-            c = [[hist[255 - 8 * lane - j] for j in range(8)] for lane in range(32)]
-            s = [sum(cl) for cl in c]
-            incl = [sum(s[:lane + 1]) for lane in range(32)]
-            excl = [incl[lane] - s[lane] for lane in range(32)]
-            hits = [lane for lane in range(32) if excl[lane] < need <= incl[lane]]
-            assert len(hits) == 1
-            src = hits[0]
-            run, d, above, in_bin = excl[src], 0, 0, 0
-            for j in range(8):
-                if in_bin == 0 and run + c[src][j] >= need and c[src][j] > 0:
-                    d, above, in_bin = 255 - src * 8 - j, run, c[src][j]
-                run += c[src][j]
-            need -= above
-            prefix |= d << shift
-            mask |= 255 << shift
-            if shift == 0:
-                break
-            if in_bin == need:
-                prefix = prefix - 1 if prefix else 0
-                need = 0
-                break
-            shift = shift - 8 if shift >= 8 else 0
-        T = prefix
-    out, run_eq = [], 0
-    for g0 in range(0, n4, 32):
-        lanes = [grp[g] if g < n4 else [0, 0, 0, 0] for g in range(g0, g0 + 32)]
-        eq = [0 if take_all else sum(1 for x in kl if x and x == T) for kl in lanes]
-        takes = []
-        for lane, kl in enumerate(lanes):
-            rank = run_eq + sum(eq[:lane])
-            t = []
-            for x in kl:
-                if take_all:
-                    t.append(x != 0)
-                else:
-                    tk = x > T
-                    if x and x == T:
-                        tk = rank < need
-                        rank += 1
-                    t.append(tk)
-            takes.append(t)
-        for lane in range(32):
-            for j in range(4):
-                if takes[lane][j]:
-                    out.append(4 * (g0 + lane) + j)
-        run_eq += sum(eq)
-    return out
-
-
-def test_one_warp_selection_is_the_top_k_in_page_order():
-    rng = random.Random(11)
-    for _ in range(1500):
-        P = rng.randint(1, 700)
-        kind = rng.random()
-        if kind < 0.3:
-            keys = [rng.randint(1, 2 ** 32 - 1) for _ in range(P)]
-        elif kind < 0.6:
-            keys = [rng.randint(1, 12) for _ in range(P)]          # heavy ties
-        else:
-            keys = [rng.choice([0, rng.randint(1 << 31, (1 << 31) + 500)]) for _ in range(P)]
-        keys += [rng.randint(0, 2 ** 32 - 1) for _ in range(3)]      # stale keys past P are ignored
-        nz = sum(1 for x in keys[:P] if x)
-        k_free = rng.randint(1, max(1, nz + 2))
-        ref = sorted(sorted((i for i in range(P) if keys[i]), key=lambda i: (-keys[i], i))[:k_free])
-        assert _warp_select(keys, P, k_free) == ref

@@ -14,7 +14,8 @@ import test_oracle_pins as PINS
 
 ORIG = {name: getattr(OP, name) for name in ("quest_scores", "select_pages", "page_summaries", "softmax_attention",
                                              "forced_pages", "retained_count", "quest_scores_per_query_head",
-                                             "cutoff_score", "page_masses", "select_coverage")}
+                                             "cutoff_score", "page_masses", "select_coverage", "page_mean_std",
+                                             "gaussian_scores")}
 
 
 @pytest.fixture
@@ -129,6 +130,18 @@ def _coverage_ignores_forced_mass(mass, coverage, b_max, sink_pages=1, window_pa
     return sorted(forced + chosen)
 
 
+def _std_sample_divisor(keys, seq_len, page_size, dtype):  # n - 1 instead of n
+    mean, std = ORIG["page_mean_std"](keys, seq_len, page_size, dtype)
+    P = mean.shape[0]
+    n = np.array([min(page_size, seq_len - p * page_size) for p in range(P)], dtype=np.float64)
+    fix = np.sqrt(n / np.maximum(n - 1, 1))[:, None, None]
+    return mean, std * fix
+
+
+def _gaussian_without_spread(q, mean, std, dtype, scale, z):  # the z * std term dropped
+    return ORIG["gaussian_scores"](q, mean, std, dtype, scale, 0.0)
+
+
 # ---- each one is caught -------------------------------------------------------------------
 def test_dropped_kmin_term_is_caught(plant):
     plant("quest_scores", _quest_kmax_only)
@@ -208,3 +221,18 @@ def test_coverage_ignoring_forced_mass_is_caught(plant, golden_dir):
         cov = json.load(f)
     _fails(PINS.test_golden_page_masses_and_coverage, cov)
     _fails(PINS.test_coverage_selection_brute_force, 7)
+
+
+def test_sample_std_divisor_is_caught(plant):
+    plant("page_mean_std", _std_sample_divisor)
+    _fails(PINS.test_mean_std_closed_forms_and_parallel_merge, "f32")
+
+
+def test_gaussian_spread_dropped_is_caught(plant, golden_dir):
+    plant("gaussian_scores", _gaussian_without_spread)
+    import json
+    import os
+    with open(os.path.join(golden_dir, "mean_std_example.json")) as f:
+        msx = json.load(f)
+    _fails(PINS.test_golden_mean_std_and_gaussian_score, msx)
+    _fails(PINS.test_gaussian_score_reductions, 0)

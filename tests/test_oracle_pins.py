@@ -625,3 +625,102 @@ def test_coverage_selection_brute_force(P):
                     chosen = [p for p in sel if p not in forced]
                     left = [p for p in others if p not in chosen]
                     assert all((mass[x], -x) > (mass[y], -y) for x in chosen for y in left)
+
+
+# ------------------------------------------------------------------ S1 / S2 mean-std summaries, Gaussian score
+@pytest.fixture(scope="module")
+def msx(golden_dir):
+    with open(os.path.join(golden_dir, "mean_std_example.json")) as f:
+        return json.load(f)
+
+
+def test_golden_mean_std_and_gaussian_score(msx):
+    keys = _f32(msx["keys"])[:, None, :]
+    mean, std = O.page_mean_std(keys, msx["seq_len"], msx["page_size"], "f32")
+    assert np.array_equal(mean[:, 0], np.asarray(msx["mean"], dtype=np.float64))
+    assert np.array_equal(std[:, 0], np.asarray(msx["std"], dtype=np.float64))
+    q = _f32(msx["q"])
+    per_head = O.gaussian_scores(q, np.repeat(mean, 2, axis=1), np.repeat(std, 2, axis=1), "f32", 1.0, msx["z"])
+    assert np.allclose(per_head, msx["score_per_query_head_unscaled"], rtol=0, atol=1e-12)
+    s = O.gaussian_scores(q, mean, std, "f32", 1.0 / math.sqrt(2.0), msx["z"])
+    assert np.allclose(s[0] * math.sqrt(2.0), msx["group_score_unscaled"], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_mean_std_closed_forms_and_parallel_merge(dtype):
+    """Two tokens: mean (a + b) / 2, std |a - b| / 2; a constant shift moves the mean and keeps
+    the std; a scale scales both; and the statistics of a page equal the merge of its two
+    halves' by the parallel-variance formula (n, mean, n * var) of Chan, Golub and LeVeque;
+    tokens past seq_len are ignored."""
+    rng = np.random.default_rng(3)
+    ps, n, H, D = 16, 16 * 4 + 6, 2, 8
+    keys = _rand_keys(rng, n + 10, H, D, dtype)
+    mean, std = O.page_mean_std(keys, n, ps, dtype)
+    v = O.to_f64(keys, dtype)
+    two = O.page_mean_std(keys[:2], 2, 2, dtype)
+    assert np.allclose(two[0][0], (v[0] + v[1]) / 2, rtol=0, atol=1e-15)
+    assert np.allclose(two[1][0], np.abs(v[0] - v[1]) / 2, rtol=1e-14, atol=1e-15)
+    # bf16-valued keys held as fp32: adding 0.5 or scaling by -4 is exact on them
+    f = O.to_f64(W.f32_to_bf16_bits(rng.standard_normal((n, H, D)).astype(np.float32)), "bf16").astype(np.float32)
+    m2, s2 = O.page_mean_std(f + np.float32(0.5), n, ps, "f32")
+    m1, s1 = O.page_mean_std(f, n, ps, "f32")
+    assert np.allclose(m2, m1 + 0.5, rtol=0, atol=1e-12) and np.allclose(s2, s1, rtol=1e-9, atol=1e-12)
+    m3, s3 = O.page_mean_std(f * np.float32(-4.0), n, ps, "f32")
+    assert np.allclose(m3, -4 * m1, rtol=1e-12, atol=1e-12) and np.allclose(s3, 4 * s1, rtol=1e-12, atol=1e-12)
+    for p in range(mean.shape[0]):
+        page = v[p * ps:min((p + 1) * ps, n)]
+        a, b = page[:len(page) // 2], page[len(page) // 2:]
+        if len(a) == 0:
+            continue
+        na, nb = len(a), len(b)
+        ma, mb = a.mean(axis=0), b.mean(axis=0)
+        Ma, Mb = ((a - ma) ** 2).sum(axis=0), ((b - mb) ** 2).sum(axis=0)
+        delta = mb - ma
+        M = Ma + Mb + delta ** 2 * na * nb / (na + nb)
+        assert np.allclose(mean[p], ma + delta * nb / (na + nb), rtol=1e-12, atol=1e-14)
+        assert np.allclose(std[p], np.sqrt(M / (na + nb)), rtol=1e-9, atol=1e-12)
+    junk = keys.copy()
+    junk[n:] = _rand_keys(rng, 10, H, D, dtype)
+    mj, sj = O.page_mean_std(junk, n, ps, dtype)
+    assert np.array_equal(mj, mean) and np.array_equal(sj, std)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_gaussian_score_reductions(seed):
+    """z = 0 gives scale times the page's average logit (brute force over its tokens); a page
+    whose keys vary in one dimension only has logit std |q_d| std_d exactly, so z = 1 gives the
+    mean plus the logits' own population std; single-token pages give the exact logit and the
+    selection equals the textbook top-k of the logits."""
+    rng = np.random.default_rng(seed)
+    ps, P, H_kv, G, D = 8, 12, 2, 2, 16
+    keys = rng.standard_normal((P * ps, H_kv, D)).astype(np.float32)
+    q = rng.standard_normal((H_kv * G, D)).astype(np.float32)
+    scale = 1 / math.sqrt(D)
+    mean, std = O.page_mean_std(keys, P * ps, ps, "f32")
+    s0 = O.gaussian_scores(q, mean, std, "f32", scale, 0.0)
+    for h in range(H_kv):
+        for p in range(P):
+            toks = keys[p * ps:(p + 1) * ps, h].astype(np.float64)
+            avg = max((toks @ q[g].astype(np.float64)).mean() for g in range(h * G, (h + 1) * G))
+            assert abs(s0[h, p] - scale * avg) <= 1e-12 * (1 + abs(avg))
+    one = np.repeat(keys[:1], P * ps, axis=0).copy()
+    one[:, :, 3] = rng.standard_normal((P * ps, H_kv)).astype(np.float32)
+    mean1, std1 = O.page_mean_std(one, P * ps, ps, "f32")
+    s1 = O.gaussian_scores(q, mean1, std1, "f32", 1.0, 1.0)
+    for h in range(H_kv):
+        for p in range(P):
+            toks = one[p * ps:(p + 1) * ps, h].astype(np.float64)
+            best = max((toks @ q[g].astype(np.float64)).mean() + (toks @ q[g].astype(np.float64)).std()
+                       for g in range(h * G, (h + 1) * G))
+            assert abs(s1[h, p] - best) <= 1e-9 * (1 + abs(best))
+    single = rng.standard_normal((P, 1, D)).astype(np.float32)
+    q1 = rng.standard_normal((1, D)).astype(np.float32)
+    m, sd = O.page_mean_std(single, P, 1, "f32")
+    assert np.all(sd == 0)
+    sc = O.gaussian_scores(q1, m, sd, "f32", 1.0, 3.0)[0]
+    logits = single[:, 0].astype(np.float64) @ q1[0].astype(np.float64)
+    assert np.allclose(sc, logits, rtol=1e-12, atol=1e-12)
+    b = 6
+    sel = O.select_pages(sc, b)
+    top = torch.topk(torch.from_numpy(logits[1:P - 1]), b - 2).indices.numpy() + 1
+    assert sel == sorted([0, P - 1] + [int(x) for x in top])
