@@ -313,8 +313,11 @@ def run_psk(args):
     ws = cache.ws
     setup_s = time.time() - t_setup
 
-    # --v-host: the value tier in pinned host memory, read (and appended to) over NVLink-C2C
+    # --v-host: the value tier in pinned host memory, read (and appended to) over NVLink-C2C;
+    # --v-hot F: plus a resident HBM hot buffer holding the fraction F of each row's selected pages
+    # (filled after the warm-up from that step's selection, which the timed steps repeat)
     v_store = cache.v_cache.cpu().pin_memory() if args.v_host else cache.v_cache
+    hot = None
     if args.v_host and (w.latent or w.dtype != "bf16" or D != 128):
         raise SystemExit("--v-host is built for GQA bf16 caches with head_dim 128")
 
@@ -340,7 +343,10 @@ def run_psk(args):
 
     def decode(dst=None):  # dst: the output buffer (default: `out` in device memory)
         o = out if dst is None else dst
-        if args.v_host:
+        if args.v_host and hot is not None:
+            psk.sparse_paged_decode_tiered(L, q, cache.k_cache, v_store, hot[0], hot[1], cache.block_table,
+                                           cache.seq_lens, sel, w.b_max, cache.scale, o, ws)
+        elif args.v_host:
             psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_store, cache.block_table, cache.seq_lens, sel, w.b_max,
                                        cache.scale, o, ws, v_host=True)
         else:
@@ -362,6 +368,24 @@ def run_psk(args):
         append(); dense()
     torch.cuda.synchronize()
     assert psk.get_device_status(ws) == 0, "device status set during warm-up"
+    hot_pages = 0
+    if args.v_host and args.v_hot > 0:
+        sel_np = sel.cpu().numpy()
+        ents = []
+        for i in range(B):
+            for h in range(Hkv):
+                row = [int(x) for x in sel_np[i, h] if x >= 0]
+                ents += [(i, h, p) for p in row[:int(round(len(row) * args.v_hot))]]
+        hot_pages = len(ents)
+        v_hot = torch.empty(max(1, hot_pages), w.page_size, D, dtype=cache.dtype, device=dev)
+        v_slot = torch.full((B, Hkv, w.max_pages), -1, dtype=torch.int32, device=dev)
+        if ents:
+            e_t = torch.tensor([(i, h, p, k) for k, (i, h, p) in enumerate(ents)], dtype=torch.int32, device=dev)
+            psk.value_tier_fill(L, v_store, cache.block_table, e_t, v_hot, v_slot, ws)
+        hot = (v_hot, v_slot)
+        append(); score(); decode()
+        torch.cuda.synchronize()
+        assert psk.get_device_status(ws) == 0, "device status set by the hot-buffer fill"
 
     # ---- the same steps captured once into CUDA graphs (replayed inside the timed window) ------
     # The one-token append touches only the tail page, whose summary the score call does not
@@ -610,7 +634,10 @@ def run_psk(args):
                              + "; CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}",
                    "v_cache": ("pinned host memory, read over NVLink-C2C (the selected pages' V bytes do not "
-                               "cross HBM; the dense step keeps V in HBM)") if args.v_host else "HBM"},
+                               "cross HBM; the dense step keeps V in HBM)"
+                               + (f"; HBM hot buffer of {hot_pages} (page, head) slots = {args.v_hot:.0%} of each "
+                                  "row's selected pages, filled from the warm-up selection the timed steps repeat"
+                                  if hot is not None else "")) if args.v_host else "HBM"},
         "roofline": roof,
         "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / (step_ms * 1e-3) / 1e9,
                      "frac_of_measured": step_bytes / (step_ms * 1e-3) / 1e9 / peak_hbm,
@@ -652,6 +679,8 @@ def main():
                     help="--impl reference: total seconds of timed oracle windows over warm-up + steps")
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--v-hot", type=float, default=0.0,
+                    help="with --v-host: fraction of each row's selected pages kept in an HBM hot buffer")
     ap.add_argument("--v-host", action="store_true",
                     help="keep the value cache in pinned host memory (the value tier; GQA bf16, head_dim 128)")
     args = ap.parse_args()

@@ -361,6 +361,43 @@ int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const vo
                                size_t workspace_bytes, psk_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * The value tier with a resident hot buffer (LOCKS PKG-INFO, "How it works", Optional DRAM tier
+ * (Stage B): V in a pinned host pool, the pages called each step resident; AMASS PyPI page: a
+ * pinned, device-mapped host pool with a bounded resident hot buffer plus staging).
+ *
+ *   v_hot   device bf16 [n_slots, page_size, v_head_dim]: slot s holds one KV head's V rows of
+ *           one page.
+ *   v_slot  device int32 [batch, num_kv_heads, max_pages]: the slot holding (sequence, KV head,
+ *           logical page), or -1. The caller owns the map and the replacement policy (for
+ *           example, keep the pages selected on the previous steps) and changes it only through
+ *           psk_value_tier_fill (or its own copies, in stream order with the decode).
+ *
+ * psk_sparse_paged_decode_tiered is psk_sparse_paged_decode_ex with PSK_DECODE_V_HOST, except
+ * that a selected page with a slot is read from v_hot (HBM) instead of over NVLink-C2C. The tail
+ * page P_i - 1 is always read from the host cache (it still takes appends); full pages never
+ * change, so their resident copies stay exact. A slot >= n_slots flags PSK_DEV_BAD_SELECTED and
+ * the page is read from the host. Results are bit-identical to the device-memory decode.
+ * PSK_BF16, GQA, head_dim 128.
+ *
+ * psk_value_tier_fill runs n_entries fill / evict steps, entries int32 [n_entries, 4] (device):
+ * (sequence, KV head, logical page, slot). slot >= 0 copies the page's page_size V rows of that
+ * head from the host cache into v_hot[slot] and sets v_slot for it; slot < 0 sets v_slot to -1.
+ * Entries must not name the same slot or the same (sequence, head, page) twice. Out-of-range
+ * entries flag PSK_DEV_BAD_SELECTED, bad block ids PSK_DEV_BAD_BLOCK, and are skipped. The
+ * workspace is only used for the status word.
+ * --------------------------------------------------------------------------------------- */
+int psk_sparse_paged_decode_tiered(const psk_layout *layout, const void *q, const void *k_cache,
+                                   const void *v_cache_host, const void *v_hot, int32_t n_slots,
+                                   const int32_t *v_slot, const int32_t *block_table,
+                                   const int32_t *seq_lens, const int32_t *selected, int32_t b_max,
+                                   float scale, void *out, void *workspace, size_t workspace_bytes,
+                                   psk_stream_t stream);
+int psk_value_tier_fill(const psk_layout *layout, const void *v_cache_host,
+                        const int32_t *block_table, const int32_t *entries, int32_t n_entries,
+                        void *v_hot, int32_t n_slots, int32_t *v_slot, void *workspace,
+                        size_t workspace_bytes, psk_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Stage 4 without a workspace (no counterpart in the pages: an addition for callers that
  * cannot allocate device memory). Some host programs own every byte of device memory
  * through their own allocator and pass a plugin only its inputs and outputs, or run a loop

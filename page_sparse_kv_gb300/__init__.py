@@ -27,7 +27,8 @@ EXPORTS = [
     "psk_sparse_decode_workspace_size", "psk_dense_decode_workspace_size", "psk_get_device_status",
     "psk_clear_device_status", "psk_status_string", "psk_version", "psk_selftest_bounded_wait",
     "psk_score_select_launches", "psk_page_select_coverage", "psk_coverage_workspace_size",
-    "psk_kv_append_and_summarize_ex", "psk_page_score_select_gaussian",
+    "psk_kv_append_and_summarize_ex", "psk_page_score_select_gaussian", "psk_sparse_paged_decode_tiered",
+    "psk_value_tier_fill",
 ]
 
 
@@ -110,6 +111,8 @@ def lib() -> ctypes.CDLL:
             "psk_page_select_coverage": (ctypes.c_int, [LP, P, P, P, P, ctypes.c_double, I, I, I, F, P, P, P, Z, P]),
             "psk_coverage_workspace_size": (Z, [LP, I]),
             "psk_kv_append_and_summarize_ex": (ctypes.c_int, [LP, P, P, P, P, I, I, P, P, P, P, P, P, Z, P]),
+            "psk_sparse_paged_decode_tiered": (ctypes.c_int, [LP, P, P, P, P, I, P, P, P, P, I, F, P, P, Z, P]),
+            "psk_value_tier_fill": (ctypes.c_int, [LP, P, P, P, I, P, I, P, P, Z, P]),
             "psk_page_score_select_gaussian": (ctypes.c_int, [LP, P, P, P, P, ctypes.POINTER(PskSelectParams), I, F,
                                                               F, P, P, P, Z, P]),
         }
@@ -317,6 +320,26 @@ def sparse_paged_decode_ex(layout: Layout, q, k_cache, v_cache, block_table, seq
         ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(selected), int(b_max), float(scale), flags, _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def sparse_paged_decode_tiered(layout: Layout, q, k_cache, v_cache_host, v_hot, v_slot, block_table, seq_lens,
+                               selected, b_max: int, scale: float, out, workspace, stream=None):
+    """Sparse decode with V in pinned host memory and the pages that have a slot in ``v_slot``
+    read from the resident HBM copies ``v_hot`` [n_slots, page_size, head_dim] (see psk.h)."""
+    _check("psk_sparse_paged_decode_tiered", lib().psk_sparse_paged_decode_tiered(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache_host), _ptr(v_hot), int(v_hot.shape[0]),
+        _ptr(v_slot), _ptr(block_table), _ptr(seq_lens), _ptr(selected), int(b_max), float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def value_tier_fill(layout: Layout, v_cache_host, block_table, entries, v_hot, v_slot, workspace, stream=None):
+    """Fill / evict hot-buffer slots: entries int32 [n, 4] of (sequence, KV head, page, slot), slot < 0
+    evicts (see psk.h)."""
+    n = 0 if entries is None else int(entries.shape[0])
+    _check("psk_value_tier_fill", lib().psk_value_tier_fill(
+        ctypes.byref(layout.c()), _ptr(v_cache_host), _ptr(block_table), _ptr(entries) if n else None, n,
+        _ptr(v_hot), int(v_hot.shape[0]), _ptr(v_slot), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def dense_paged_decode(layout: Layout, q, k_cache, v_cache, block_table, seq_lens, scale: float, out, workspace,

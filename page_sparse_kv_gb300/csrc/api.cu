@@ -432,7 +432,8 @@ int psk_page_select_coverage(const psk_layout *layout, const void *q, const void
 static int decode_common(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_table, const int32_t *seq_lens, const int32_t *selected,
                          int32_t b_max, float scale, void *out, void *workspace, size_t workspace_bytes,
-                         psk_stream_t stream, bool per_query_head = false, bool v_host = false) {
+                         psk_stream_t stream, bool per_query_head = false, bool v_host = false,
+                         const void *v_hot = nullptr, const int32_t *v_slot = nullptr, int32_t n_slots = 0) {
   int rc = check_layout(layout);
   if (rc != PSK_OK) return rc;
   const psk_layout &L = *layout;
@@ -469,6 +470,9 @@ static int decode_common(const psk_layout *layout, const void *q, const void *k_
   a.H_kv_cache = L.num_kv_heads;
   a.kv_shift = kv_shift;
   a.v_host = v_host ? 1 : 0;
+  a.v_hot = v_hot;
+  a.v_slot = v_slot;
+  a.n_slots = n_slots;
   a.D = L.head_dim;
   a.D_v = L.v_head_dim;
   a.ps = L.page_size;
@@ -503,6 +507,31 @@ int psk_sparse_paged_decode_ex(const psk_layout *layout, const void *q, const vo
   return decode_common(layout, q, k_cache, v_cache, block_table, seq_lens, selected, b_max, scale, out, workspace,
                        workspace_bytes, stream, (flags & PSK_DECODE_PER_QUERY_HEAD) != 0,
                        (flags & PSK_DECODE_V_HOST) != 0);
+}
+
+int psk_sparse_paged_decode_tiered(const psk_layout *layout, const void *q, const void *k_cache,
+                                   const void *v_cache_host, const void *v_hot, int32_t n_slots,
+                                   const int32_t *v_slot, const int32_t *block_table, const int32_t *seq_lens,
+                                   const int32_t *selected, int32_t b_max, float scale, void *out,
+                                   void *workspace, size_t workspace_bytes, psk_stream_t stream) {
+  if (!selected || b_max < 1 || !v_hot || !v_slot || n_slots < 1 || !aligned16(v_hot)) return PSK_ERR_INVALID_ARG;
+  return decode_common(layout, q, k_cache, v_cache_host, block_table, seq_lens, selected, b_max, scale, out, workspace,
+                       workspace_bytes, stream, false, true, v_hot, v_slot, n_slots);
+}
+
+int psk_value_tier_fill(const psk_layout *layout, const void *v_cache_host, const int32_t *block_table,
+                        const int32_t *entries, int32_t n_entries, void *v_hot, int32_t n_slots, int32_t *v_slot,
+                        void *workspace, size_t workspace_bytes, psk_stream_t stream) {
+  int rc = check_layout(layout);
+  if (rc != PSK_OK) return rc;
+  const psk_layout &L = *layout;
+  if (L.latent || L.dtype != PSK_BF16 || L.v_head_dim != 128) return PSK_ERR_UNSUPPORTED;
+  if (n_entries < 0 || n_slots < 1 || !v_cache_host || !block_table || !v_hot || !v_slot || (n_entries > 0 && !entries))
+    return PSK_ERR_INVALID_ARG;
+  if (!aligned16(v_cache_host) || !aligned16(v_hot)) return PSK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWsHeader) return PSK_ERR_WORKSPACE;
+  return cuda_status(launch_value_tier_fill(L, v_cache_host, block_table, entries, n_entries, v_hot, n_slots, v_slot,
+                                            workspace, static_cast<cudaStream_t>(stream)));
 }
 
 int psk_dense_paged_decode(const psk_layout *layout, const void *q, const void *k_cache, const void *v_cache,

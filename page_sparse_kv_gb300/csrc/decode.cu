@@ -40,6 +40,7 @@ constexpr int kFlatMaxCtas = 2048;   // grid of the flat layout, upper bound (si
 constexpr int kFlatMaxUnits = 4096;  // units the flat layout takes (its prefix sums live in shared memory)
 constexpr long long kFlatMinShare = 8;  // list entries per CTA of the flat layout, lower bound
 constexpr int kFastMerge = 8;          // partials a unit merge reads in one round trip
+constexpr int kHostPrefetch = 2;       // host value path: tiles of its own a warp prefetches ahead into L2
 
 template <typename T, int D, int G, int NW, int NST>
 struct DT {
@@ -58,7 +59,7 @@ struct DT {
                                  + STAGES                      // stages (reused by the merges)
                                  + (size_t)NW * 16 * G * 8     // (p, p) pairs
                                  + (size_t)NW * G * 2 * 4      // warp m, l
-                                 + (size_t)kSwMax * 2 * 4;     // entry table
+                                 + (size_t)kSwMax * 3 * 4;     // entry table
   static_assert(STAGES >= (size_t)NW * G * D * 4, "stage memory must hold the warps' O for the CTA merge");
   static_assert(NC % 8 == 0, "a row must be a multiple of 128 bytes");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
@@ -201,7 +202,7 @@ __device__ void merge_unit(const DecodeArgs &a, int unit, size_t it0, int n, flo
 // threads of the CTA take part; the caller synchronises.
 template <int NT>
 __device__ void load_entries(const DecodeArgs &a, int i, int unit, int P, int seq_len, int e0, int n, int *ent_blk,
-                             int *ent_valid) {
+                             int *ent_valid, int *ent_vslot = nullptr) {
   for (int x = threadIdx.x; x < n; x += NT) {
     int p = e0 + x, blk = -1;
     bool ok = true;
@@ -224,6 +225,19 @@ __device__ void load_entries(const DecodeArgs &a, int i, int unit, int P, int se
     }
     ent_blk[x] = blk;
     ent_valid[x] = ok ? min(a.ps, seq_len - p * a.ps) : 0;
+    if (ent_vslot) {
+      // a resident copy serves only full pages below the tail (the tail page still takes appends)
+      int slot = -1;
+      if (ok && a.v_slot && p < P - 1) {
+        const int hc = (unit % a.H_kv) >> a.kv_shift;
+        slot = a.v_slot[((size_t)i * a.H_kv_cache + hc) * a.max_pages + p];
+        if (slot >= a.n_slots) {
+          set_status(a.ws, PSK_DEV_BAD_SELECTED);
+          slot = -1;
+        }
+      }
+      ent_vslot[x] = slot;
+    }
   }
 }
 
@@ -261,7 +275,8 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
                                            float2 (&q2)[G][DT<T, D, G, NW, NST>::CPL * DT<T, D, G, NW, NST>::EPC / 2],
                                            const int *ent_blk, const int *ent_valid, int n_ent, unsigned char *stages,
                                            float2 *pp_all, uint64_t (*bars)[NST], int &cw, float (&m)[G], float (&l)[G],
-                                           float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2]) {
+                                           float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2],
+                                           const int *ent_vslot = nullptr) {
   using TR = DT<T, D, G, NW, NST>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tq = lane >> 3, dg = lane & 7;
@@ -307,14 +322,33 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
     issue(k + NST - 1);
     uint2 vh[kHostV ? 16 : 1];  // kHostV: this lane's V slice of the tile's rows
     if constexpr (kHostV) {
-      const int e = stp == 1 ? cur : cur / stp, sub = cur - e * stp;
-      const int nvh = min(16, ent_valid[e] - sub * 16);
-      const size_t row0 = (size_t)ent_blk[e] * a.ps + sub * 16;
-      const T *vb = reinterpret_cast<const T *>(a.v_cache) + (row0 * a.H_kv_cache + (h >> a.kv_shift)) * D +
-                    lane * TR::VPL;
+      // The tile's V rows: from the page's resident HBM slot when it has one, else from the host
+      // cache over NVLink-C2C. A later tile's host rows are first prefetched into L2 (one 128-byte
+      // line per lane, two lanes per row), so their C2C latency overlaps this tile.
+      auto vsrc = [&](int it, size_t *stride) -> const T * {
+        const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
+        const int slot = ent_vslot ? ent_vslot[e] : -1;
+        if (slot >= 0) {
+          *stride = D;
+          return reinterpret_cast<const T *>(a.v_hot) + ((size_t)slot * a.ps + sub * 16) * D;
+        }
+        *stride = (size_t)a.H_kv_cache * D;
+        return reinterpret_cast<const T *>(a.v_cache) +
+               (((size_t)ent_blk[e] * a.ps + sub * 16) * a.H_kv_cache + (h >> a.kv_shift)) * D;
+      };
+      const int pf = cur + kHostPrefetch * NW;
+      if (pf < ntiles && tile_rows(pf) > 0) {
+        size_t st;
+        const T *pb = vsrc(pf, &st);
+        if ((lane >> 1) < tile_rows(pf))
+          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pb + (size_t)(lane >> 1) * st + (lane & 1) * 64) : "memory");
+      }
+      const int nvh = tile_rows(cur);
+      size_t st;
+      const T *vb = vsrc(cur, &st) + lane * TR::VPL;
 #pragma unroll
       for (int tk = 0; tk < 16; ++tk)  // only rows below seq_len: the rest may hold anything
-        vh[tk] = tk < nvh ? *reinterpret_cast<const uint2 *>(vb + (size_t)tk * a.H_kv_cache * D) : make_uint2(0u, 0u);
+        vh[tk] = tk < nvh ? *reinterpret_cast<const uint2 *>(vb + (size_t)tk * st) : make_uint2(0u, 0u);
     }
     const int stage = (cw0 + k) % NST;
     mbar_wait(smem_u32(&bars[warp][stage]), ((cw0 + k) / NST) & 1, a.ws);
@@ -527,7 +561,7 @@ struct DecodeSmem {
   unsigned char *stages;
   float2 *pp_all;
   float *wML;
-  int *ent_blk, *ent_valid;
+  int *ent_blk, *ent_valid, *ent_vslot;
   int *extra;  // flat layout: the unit prefix sums
   __device__ explicit DecodeSmem(unsigned char *raw) {
     stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127));
@@ -535,7 +569,8 @@ struct DecodeSmem {
     wML = reinterpret_cast<float *>(pp_all + NW * 16 * G);
     ent_blk = reinterpret_cast<int *>(wML + NW * G * 2);
     ent_valid = ent_blk + kSwMax;
-    extra = ent_valid + kSwMax;
+    ent_vslot = ent_valid + kSwMax;
+    extra = ent_vslot + kSwMax;
   }
 };
 
@@ -576,7 +611,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
     for (int k = 0; k < NST; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
     fence_mbar_init();
   }
-  load_entries<NW * 32>(a, i, unit, P, seq_len, e0, n_ent, sm.ent_blk, sm.ent_valid);
+  load_entries<NW * 32>(a, i, unit, P, seq_len, e0, n_ent, sm.ent_blk, sm.ent_valid, kHostV ? sm.ent_vslot : nullptr);
   __syncthreads();
 
   // a unit whose whole list fits this split (sparse: no entry at index sw) needs no partials and
@@ -602,7 +637,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
     }
     int cw = 0;
     warp_tiles<T, D, G, NW, NST, kHostV>(a, &tmK, &tmV, h, i, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages,
-                                         sm.pp_all, bars, cw, m, l, O);
+                                         sm.pp_all, bars, cw, m, l, O, kHostV ? sm.ent_vslot : nullptr);
     __syncthreads();  // every warp is done with the stages; the merge below reuses them
     if (alone) {
       write_output<T, D, G, NW, NST>(a, unit, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
@@ -788,6 +823,39 @@ __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, cons
   }
 }
 
+// Value tier fill: entry x = (sequence, cache head, page, slot). slot >= 0 copies the page's
+// ps rows of that head from the host value cache (over NVLink-C2C) into hot-buffer slot `slot`
+// and records it in v_slot; slot < 0 clears the page's record (its V is read from the host
+// again). One CTA per entry, 16 bytes per thread and step.
+__global__ void value_tier_fill_kernel(const uint16_t *v_host, const int32_t *block_table, const int32_t *entries,
+                                       uint16_t *v_hot, int32_t *v_slot, void *ws, int H_kv, int D, int ps, int nb,
+                                       int max_pages, int B, int n_slots) {
+  pdl_begin();
+  const int32_t *ent = entries + (size_t)blockIdx.x * 4;
+  const int i = ent[0], h = ent[1], p = ent[2], slot = ent[3];
+  if (i < 0 || i >= B || h < 0 || h >= H_kv || p < 0 || p >= max_pages || slot >= n_slots) {
+    if (threadIdx.x == 0) set_status(ws, PSK_DEV_BAD_SELECTED);
+    return;
+  }
+  int32_t *rec = v_slot + ((size_t)i * H_kv + h) * max_pages + p;
+  if (slot < 0) {
+    if (threadIdx.x == 0) *rec = -1;
+    return;
+  }
+  const int blk = block_table[(size_t)i * max_pages + p];
+  if (blk < 0 || blk >= nb) {
+    if (threadIdx.x == 0) set_status(ws, PSK_DEV_BAD_BLOCK);
+    return;
+  }
+  const int cpr = D / 8;  // 16-byte chunks per row
+  for (int x = threadIdx.x; x < ps * cpr; x += blockDim.x) {
+    const int r = x / cpr, c = x - r * cpr;
+    const uint4 v = *reinterpret_cast<const uint4 *>(v_host + (((size_t)blk * ps + r) * H_kv + h) * D + c * 8);
+    *reinterpret_cast<uint4 *>(v_hot + ((size_t)slot * ps + r) * D + c * 8) = v;
+  }
+  if (threadIdx.x == 0) *rec = slot;
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   constexpr int NW = 4, NST = 2;
@@ -828,6 +896,15 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   return launch_kernel(!a.selected, kfn, ctas, NW * 32, smem, s, a, tmK, tmV);
 }
 }  // namespace
+
+cudaError_t launch_value_tier_fill(const psk_layout &L, const void *v_host, const int32_t *block_table,
+                                   const int32_t *entries, int n_entries, void *v_hot, int n_slots, int32_t *v_slot,
+                                   void *ws, cudaStream_t s) {
+  if (n_entries == 0) return cudaSuccess;
+  return launch_kernel(true, value_tier_fill_kernel, n_entries, 128, 0, s, reinterpret_cast<const uint16_t *>(v_host),
+                       block_table, entries, reinterpret_cast<uint16_t *>(v_hot), v_slot, ws, L.num_kv_heads,
+                       L.v_head_dim, L.page_size, L.num_blocks, L.max_pages, L.batch, n_slots);
+}
 
 bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan) {
   const long long units = (long long)L.batch * L.num_kv_heads;

@@ -93,6 +93,9 @@ extern "C" int psk_sparse_paged_decode_noalloc(const psk_layout *layout, const v
   a.H_kv_cache = L.num_kv_heads;
   a.kv_shift = 0;
   a.v_host = 0;
+  a.v_hot = nullptr;
+  a.v_slot = nullptr;
+  a.n_slots = 0;
   a.D = L.head_dim;
   a.D_v = L.v_head_dim;
   a.ps = L.page_size;

@@ -98,6 +98,9 @@ struct DecodeArgs {
   int H_kv_cache;      // KV heads of the cache (H_kv above counts the units' heads)
   int kv_shift;        // unit head h reads cache head h >> kv_shift
   int v_host;          // 1: v_cache is host memory read over NVLink-C2C (sparse split, bf16, D = 128)
+  const void *v_hot;   // v_host: resident HBM copies of full pages' V rows [n_slots, ps, D_v], or NULL
+  const int32_t *v_slot;  // v_host: slot of (sequence, cache head, logical page) [B, H_kv_cache, max_pages], -1 = host
+  int n_slots;
   int sw;              // list entries per item (split layout)
   int n_items_max;     // items per unit (split layout)
   int32_t *counts;     // [B * H_kv] list entries per unit (flat layout, sparse)
@@ -126,6 +129,11 @@ __host__ __device__ inline int split_off(int s, int sw, int taper) {
   return o;
 }
 cudaError_t launch_decode(const DecodeArgs &a, int dtype, cudaStream_t s);
+// Copies listed (sequence, cache head, page) V rows of a host value cache into hot-buffer slots
+// and records the slots (slot < 0: the entry is evicted); see psk_value_tier_fill.
+cudaError_t launch_value_tier_fill(const psk_layout &L, const void *v_host, const int32_t *block_table,
+                                   const int32_t *entries, int n_entries, void *v_hot, int n_slots, int32_t *v_slot,
+                                   void *ws, cudaStream_t s);
 bool decode_supported(int dtype, int D, int D_v, int G, int ps);
 
 // Gaussian page score from the mean / std summaries (gauss.cu): keys for the selection kernel

@@ -402,6 +402,80 @@ def test_value_tier_in_host_memory(ps):
         check_output(out_np[i], O.attend_pages(q_np[i], keys, vals, n, w.page_size, use, w.dtype, scale), w.dtype)
 
 
+def _hot_entries(sel_np, lens, ps, frac, first_slot=0):
+    """(sequence, KV head, page, slot) for the first `frac` of each row's selected pages (tail pages
+    included on purpose: the decode must read those from the host anyway)."""
+    ents = []
+    for i in range(sel_np.shape[0]):
+        for h in range(sel_np.shape[1]):
+            row = [int(x) for x in sel_np[i, h] if x >= 0]
+            for p in row[:max(1, int(len(row) * frac))] + [row[-1]]:
+                ents.append((i, h, p))
+    ents = sorted(set(ents))
+    return np.array([(i, h, p, first_slot + k) for k, (i, h, p) in enumerate(ents)], dtype=np.int32)
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+def test_value_tier_hot_buffer(ps):
+    """The value tier with a resident HBM hot buffer: pages with a slot are read from HBM, the rest
+    (and every tail page) from pinned host memory; the output equals the device-memory decode bit
+    for bit, after fills, after evictions, and with a tail page's resident copy overwritten with
+    NaN. A slot index past the buffer flags PSK_DEV_BAD_SELECTED and that page is read from host."""
+    w = _custom([ps * 75 + 5, ps * 19 + 9, ps * 40 + ps // 2 + 3, 17], [40, 9, 30, 2], ps=ps, H_q=32, H_kv=8)
+    cache = upload(w)
+    L = cache.layout
+    q = dev_queries(w)
+    v_host = cache.v_cache.cpu().pin_memory()
+    sel = cache.score_select(q, dev_budgets(w))
+    out_dev = cache.sparse_decode(q, sel)
+    torch.cuda.synchronize()
+    sel_np = sel.cpu().numpy()
+    lens = [int(x) for x in w.seq_lens]
+    ents = _hot_entries(sel_np, lens, ps, 0.6)
+    n_slots = len(ents) + 3
+    v_hot = torch.zeros(n_slots, ps, w.D, dtype=torch.bfloat16, device="cuda")
+    v_slot = torch.full((w.B, w.H_kv, w.max_pages), -1, dtype=torch.int32, device="cuda")
+    psk.value_tier_fill(L, v_host, cache.block_table, torch.from_numpy(ents).cuda(), v_hot, v_slot, cache.ws)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    vs = v_slot.cpu().numpy()
+    for i, h, p, slot in ents:
+        assert vs[i, h, p] == slot
+        blk = w.block_table[i, p]
+        assert torch.equal(v_hot[slot].cpu(), v_host[blk, :, h, :])
+    assert (vs >= 0).sum() == len(ents)
+
+    def tiered():
+        out = torch.full_like(out_dev, float("nan"))
+        psk.sparse_paged_decode_tiered(L, q, cache.k_cache, v_host, v_hot, v_slot, cache.block_table, cache.seq_lens,
+                                       sel, cache.b_max, cache.scale, out, cache.ws)
+        torch.cuda.synchronize()
+        return out
+
+    assert torch.equal(tiered(), out_dev)
+    # a tail page's resident copy is never used
+    Ps = [-(-n // ps) for n in lens]
+    tails = [(i, h, p, slot) for i, h, p, slot in ents if p == Ps[i] - 1]
+    assert tails
+    for _, _, _, slot in tails:
+        v_hot[slot].fill_(float("nan"))
+    assert torch.equal(tiered(), out_dev)
+    # evict half the entries, then run again
+    ev = ents[::2].copy()
+    ev[:, 3] = -1
+    psk.value_tier_fill(L, v_host, cache.block_table, torch.from_numpy(ev).cuda(), v_hot, v_slot, cache.ws)
+    torch.cuda.synchronize()
+    assert (v_slot.cpu().numpy() >= 0).sum() == len(ents) - len(ev)
+    assert torch.equal(tiered(), out_dev)
+    assert psk.get_device_status(cache.ws) == 0
+    # a slot past the buffer: flagged, and the page is read from the host
+    i, h, p, _ = ents[1]
+    v_slot[i, h, p] = n_slots + 4
+    assert torch.equal(tiered(), out_dev)
+    assert psk.get_device_status(cache.ws) == psk.DEV_BAD_SELECTED
+    psk.clear_device_status(cache.ws)
+
+
 def test_ties_resolve_to_lower_page():
     """Pages with identical keys (hence identical summaries and scores) tie; with the cutoff
     inside the tied group the lowest-indexed tied pages win."""
