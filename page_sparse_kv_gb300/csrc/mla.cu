@@ -291,6 +291,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   set_status(ws, PSK_DEV_TIMEOUT);
   return false;
 }
+// bulk copy (TMA engine) of `bytes` from this CTA's shared memory to the partner's, completing
+// `bytes` transactions on the partner's mbarrier; then wait until the source has been read
+__device__ __forceinline__ void bulk_s2peer(uint32_t peer_dst, uint32_t src, uint32_t bytes, uint32_t peer_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(peer_dst),
+               "r"(src), "r"(bytes), "r"(peer_bar)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
@@ -301,10 +310,14 @@ __device__ __forceinline__ void cluster_sync() {
 // the partial S over them, and the two partial S are exchanged through distributed shared memory
 // and added (in the same order on both sides, so both hold the same S, hence the same P, m and l).
 // Warps 0-3 own one query head per thread (the tensor-memory lanes); warp 4's lane 0 issues every
-// MMA, warp 5's lane 0 every TMA copy. Per 64-token tile t:
+// MMA, warp 5's lane 0 every TMA copy and its lane 1 the exchange: the softmax threads write their
+// partial S rows to xsend, and one bulk copy per tile moves them into the partner's xrecv,
+// completing on the partner's xfull (armed with the expected bytes by the partner's own exchange
+// thread). Per 64-token tile t:
 //   K(t)   : TMA of this CTA's blocks into stage t % 3                  (kfull; kempty after P.V(t))
 //   S(t)   = Q K(t)^T over those blocks (A = Q from tensor memory)      (sfull; sfree once read)
-//   x(t)   : partial S rows to the partner's exchange buffer t % 2      (xfull; xempty once read)
+//   x(t)   : partial S rows to the partner (xwritten -> bulk copy -> the partner's xfull; xsent
+//            once the copy has read xsend; xread -> the partner's xempty once the rows are read)
 //   P(t)   : softmax of S = mine + partner's, O rescaled when needed     (pready)
 //   O     += P(t) V(t)   (V = the CTA's four value blocks, MN-major)     (pvdone)
 // in the issue order S(t+1) (as soon as S(t) is in registers), then P.V(t).
@@ -315,9 +328,10 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
   unsigned char *base = align1024(dyn);
   unsigned char *sK = base;                     // kKStages stages of this CTA's blocks
   unsigned char *sP = sK + kKStages * kKStage;  // P
-  float *xbuf = reinterpret_cast<float *>(sP + kPBytes);  // 2 exchange buffers, written by the partner
-  __shared__ __align__(8) uint64_t kfull[kKStages], kempty[kKStages], sfull, sfree, pready, pvdone, drained, xfull[2],
-      xempty[2];
+  float *xsend = reinterpret_cast<float *>(sP + kPBytes);  // this CTA's partial S rows, sent to the partner
+  float *xrecv = xsend + kXBytes / 4;                      // the partner's partial S rows
+  __shared__ __align__(8) uint64_t kfull[kKStages], kempty[kKStages], sfull, sfree, pready, pvdone, drained, xfull,
+      xempty, xwritten, xsent, xread;
   __shared__ int abort_sh;  // set by the first wait that gives up: every later wait returns at once
   __shared__ uint32_t tslot;
   __shared__ int ent_blk[kMlaMaxSw], ent_valid[kMlaMaxSw];
@@ -377,10 +391,11 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
       mbar_init(smem_u32(&kfull[k]), 1);
       mbar_init(smem_u32(&kempty[k]), 1);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&xfull[k]), kHeads);   // the partner's 128 softmax threads
-      mbar_init(smem_u32(&xempty[k]), kHeads);
-    }
+    mbar_init(smem_u32(&xfull), 1);       // the exchange thread's arming + the partner's bytes
+    mbar_init(smem_u32(&xempty), 1);      // the partner's exchange thread: it has read what we sent
+    mbar_init(smem_u32(&xwritten), kHeads);
+    mbar_init(smem_u32(&xsent), 1);
+    mbar_init(smem_u32(&xread), kHeads);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -440,7 +455,26 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
     return false;
   };
 
-  if (warp == 5) {
+  if (warp == 5 && lane == 1 && n_tiles > 0) {
+    // ---------------- exchange thread: partial S rows to the partner, one bulk copy per tile ----
+    const uint32_t peer_xrecv = cluster_map(smem_u32(xrecv), peer);
+    const uint32_t peer_xfull = cluster_map(smem_u32(&xfull), peer);
+    const uint32_t peer_xempty = cluster_map(smem_u32(&xempty), peer);
+#pragma unroll 1
+    for (int t = 0; t < n_tiles; ++t) {
+      if (t >= 1) {
+        // our softmax threads have read the partner's rows of tile t-1: its next copy may land
+        if (!wait_ok(&xread, (t - 1) & 1)) break;
+        mbar_arrive_remote(peer_xempty);
+      }
+      mbar_arrive_expect_tx(smem_u32(&xfull), (uint32_t)kXBytes);  // receive tile t
+      if (!wait_ok(&xwritten, t & 1)) break;                         // our rows of tile t are in xsend
+      if (t >= 1 && !wait_cluster_ok(&xempty, (t - 1) & 1)) break;   // the partner read our tile t-1
+      bulk_s2peer(peer_xrecv, smem_u32(xsend), (uint32_t)kXBytes, peer_xfull);
+      mbar_arrive(smem_u32(&xsent));  // xsend may be rewritten
+    }
+    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");  // every copy to the partner has completed
+  } else if (warp == 5) {
     // ---------------- loading thread: TMA copies of this CTA's blocks ----------------
     if (lane == 0 && n_tiles > 0) {
       int issued = 0;
@@ -515,11 +549,6 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
     // ---------------- softmax warps: one query head per thread ----------------
     float m_run = -INFINITY, l_run = 0.f;
     const float qs = a.scale * kLog2e;
-    const uint32_t my_x0 = smem_u32(xbuf);
-    const uint32_t peer_x0 = cluster_map(my_x0, peer);
-    const uint32_t peer_xfull[2] = {cluster_map(smem_u32(&xfull[0]), peer), cluster_map(smem_u32(&xfull[1]), peer)};
-    const uint32_t peer_xempty[2] = {cluster_map(smem_u32(&xempty[0]), peer),
-                                     cluster_map(smem_u32(&xempty[1]), peer)};
 #pragma unroll 1
     for (int t = 0; t < n_tiles; ++t) {
       if (!__all_sync(0xffffffffu, wait_ok(&sfull, t & 1))) break;  // warp-uniform exit
@@ -536,20 +565,20 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sfree));  // the issuing thread may overwrite S now
-      // ---- exchange the partial S rows with the partner (16-byte chunks, swizzled by head) ----
-      const int b = t & 1;
-      if (t >= 2 && !__all_sync(0xffffffffu, wait_cluster_ok(&xempty[b], ((t >> 1) - 1) & 1))) break;
+      // ---- exchange the partial S rows with the partner (rows of 16-byte chunks, swizzled by head) ----
+      if (t >= 1 && !__all_sync(0xffffffffu, wait_ok(&xsent, (t - 1) & 1))) break;  // xsend is free again
       {
-        const uint32_t dst = peer_x0 + (uint32_t)(b * kXBytes + tid * kTile * 4);
+        float *dst = xsend + tid * kTile;
 #pragma unroll
         for (int c = 0; c < kTile / 4; ++c)
-          st_cluster_v4(dst + (uint32_t)(((c ^ (tid & 15)) * 16)),
-                        make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]));
-        mbar_arrive_remote(peer_xfull[b]);
+          *reinterpret_cast<float4 *>(dst + ((c ^ (tid & 15)) * 4)) =
+              make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+        fence_proxy_async_smem();  // the bulk copy reads these rows through the async proxy
+        mbar_arrive(smem_u32(&xwritten));
       }
-      if (!__all_sync(0xffffffffu, wait_cluster_ok(&xfull[b], (t >> 1) & 1))) break;
+      if (!__all_sync(0xffffffffu, wait_cluster_ok(&xfull, t & 1))) break;  // the partner's rows of tile t
       {
-        const float *src = xbuf + (size_t)b * (kXBytes / 4) + tid * kTile;
+        const float *src = xrecv + tid * kTile;
         // the rank-0 CTA adds (own + peer) and the rank-1 CTA (peer + own): the same two operands
         // in the same order, so both CTAs hold bit-identical S
 #pragma unroll
@@ -567,7 +596,7 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
             x[4 * c + 3] = y.w + x[4 * c + 3];
           }
         }
-        mbar_arrive_remote(peer_xempty[b]);  // this CTA has read the buffer the partner writes
+        mbar_arrive(smem_u32(&xread));  // the exchange thread tells the partner once all have read
       }
       float mt = -INFINITY;
 #pragma unroll
