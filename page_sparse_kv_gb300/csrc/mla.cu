@@ -248,7 +248,7 @@ constexpr int kKStages = 3;
 constexpr int kPBytes = kHeads * kTile * 2;  // 16384: P [128 x 64] bf16, 128-byte swizzle
 constexpr int kXBytes = kHeads * kTile * 4;  // 32768: one exchange buffer, fp32 partial S [128 x 64]
 constexpr int kDecSmem = 1024 + kKStages * kKStage + kPBytes + 2 * kXBytes;
-constexpr int kDecThreads = 192;             // 4 softmax warps (one thread per head), MMA warp, TMA warp
+constexpr int kDecThreads = 224;             // 4 softmax warps (one thread per head), MMA, TMA and exchange warps
 constexpr int kMlaMaxSw = 128;               // pages per split
 constexpr int kMlaMaxItems = 128;            // splits per (sequence, half); their merge weights fit the K stages
 static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKStage, "merge weights must fit the K stages");
@@ -310,7 +310,7 @@ __device__ __forceinline__ void cluster_sync() {
 // the partial S over them, and the two partial S are exchanged through distributed shared memory
 // and added (in the same order on both sides, so both hold the same S, hence the same P, m and l).
 // Warps 0-3 own one query head per thread (the tensor-memory lanes); warp 4's lane 0 issues every
-// MMA, warp 5's lane 0 every TMA copy and its lane 1 the exchange: the softmax threads write their
+// MMA, warp 5's lane 0 every TMA copy and warp 6's lane 0 the exchange: the softmax threads write their
 // partial S rows to xsend, and one bulk copy per tile moves them into the partner's xrecv,
 // completing on the partner's xfull (armed with the expected bytes by the partner's own exchange
 // thread). Per 64-token tile t:
@@ -455,8 +455,9 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
     return false;
   };
 
-  if (warp == 5 && lane == 1 && n_tiles > 0) {
+  if (warp == 6) {
     // ---------------- exchange thread: partial S rows to the partner, one bulk copy per tile ----
+    if (lane == 0 && n_tiles > 0) {
     const uint32_t peer_xrecv = cluster_map(smem_u32(xrecv), peer);
     const uint32_t peer_xfull = cluster_map(smem_u32(&xfull), peer);
     const uint32_t peer_xempty = cluster_map(smem_u32(&xempty), peer);
@@ -474,6 +475,7 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
       mbar_arrive(smem_u32(&xsent));  // xsend may be rewritten
     }
     asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");  // every copy to the partner has completed
+    }
   } else if (warp == 5) {
     // ---------------- loading thread: TMA copies of this CTA's blocks ----------------
     if (lane == 0 && n_tiles > 0) {
