@@ -35,6 +35,7 @@ namespace psk {
 namespace {
 
 constexpr int kD = 576, kDv = 512, kHeads = 128;
+constexpr int kKB = kD / 64;  // 64-element K blocks of a latent row
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------------------------
@@ -239,99 +240,45 @@ __global__ void __launch_bounds__(128) mla_score_kernel(ScoreArgs a, const uint1
 // ------------------------------------------------------------------------------------
 // decode
 // ------------------------------------------------------------------------------------
-constexpr int kHalf = 32;                   // tokens per TMA box (half a tile)
-constexpr int kTile = 64;                   // tokens per tile
-constexpr int kKBlock = kTile * 128;        // 8192: one 64-dim block of a tile, 128-byte swizzle
-constexpr int kOwnMax = 5;                  // 64-dim blocks a CTA of the pair holds: 5 (rank 0) or 4 (rank 1)
-constexpr int kKStage = kOwnMax * kKBlock;  // 40960: one stage of the ring (this CTA's blocks of one tile)
-constexpr int kKStages = 3;
-constexpr int kPBytes = kHeads * kTile * 2;  // 16384: P [128 x 64] bf16, 128-byte swizzle
-constexpr int kXBytes = kHeads * kTile * 4;  // 32768: one exchange buffer, fp32 partial S [128 x 64]
-constexpr int kDecSmem = 1024 + kKStages * kKStage + kPBytes + 2 * kXBytes;
-constexpr int kDecThreads = 224;             // 4 softmax warps (one thread per head), MMA, TMA and exchange warps
-constexpr int kMlaMaxSw = 128;               // pages per split
-constexpr int kMlaMaxItems = 128;            // splits per (sequence, half); their merge weights fit the K stages
-static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKStage, "merge weights must fit the K stages");
-// tensor-memory columns: O (128 x 256 fp32), S (128 x 64 fp32), Q of this CTA's blocks as bf16 pairs
+constexpr int kHalf = 32;                       // tokens per TMA box (half a tile)
+constexpr int kTile = 64;                       // tokens per tile
+constexpr int kQTmemKB = 6;                     // K blocks of Q held in tensor memory (dims 0..383)
+constexpr int kQSmemKB = kKB - kQTmemKB;        // K blocks of Q in shared memory (dims 384..575)
+constexpr int kQSBytes = kQSmemKB * kHeads * 128;  // 49152: 3 swizzled [128 x 64] blocks
+constexpr int kKBlock = kTile * 128;            // 8192: one 64-dim block of a tile, 128-byte swizzle
+constexpr int kKTile = kKB * kKBlock;           // 73728: a K tile (64 tokens x 576)
+constexpr int kKStages = 2;
+constexpr int kPBytes = kHeads * kTile * 2;     // 16384: P [128 x 64] bf16, 128-byte swizzle
+constexpr int kDecSmem = 1024 + kQSBytes + kKStages * kKTile + kPBytes;
+constexpr int kDecThreads = 192;                // 4 softmax warps (one thread per head), MMA warp, TMA warp
+constexpr int kMlaMaxSw = 128;                  // pages per split
+constexpr int kMlaMaxItems = 128;               // splits per (sequence, half); their merge weights fit the K stages
+static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKTile, "merge weights must fit the K stages");
+// tensor-memory columns: O (128 x 256 fp32), S (128 x 64 fp32), Q dims 0..383 as bf16 pairs
 constexpr uint32_t kOCol = 0, kSCol = 256, kQCol = 320;
-static_assert(kQCol + kOwnMax * 32 <= 512, "tensor-memory budget");
-constexpr float kRescaleSlack = 8.f;         // log2 headroom before O is rescaled
+static_assert(kQCol + kQTmemKB * 32 == 512, "tensor-memory budget");
+constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is rescaled
 
-// 64-dim block j of the blocks CTA `rank` of the pair holds: rank 0 the value blocks 0..3 and the
-// rope block 8, rank 1 the value blocks 4..7. The first four are the CTA's half of D_v.
-__device__ __forceinline__ int own_block(int rank, int j) { return rank == 0 ? (j < 4 ? j : 8) : 4 + j; }
-
-// ---- cluster (CTA pair) helpers ----------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_map(uint32_t local_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local_addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
-}
-// arrive on an mbarrier of the partner CTA, releasing this thread's prior writes at cluster scope
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote_bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait with cluster-scope acquire (for phases the partner CTA completes)
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, void *ws) {
-  for (uint32_t it = 0; it < kMbarSpinLimit; ++it)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-  set_status(ws, PSK_DEV_TIMEOUT);
-  return false;
-}
-// bulk copy (TMA engine) of `bytes` from this CTA's shared memory to the partner's, completing
-// `bytes` transactions on the partner's mbarrier; then wait until the source has been read
-__device__ __forceinline__ void bulk_s2peer(uint32_t peer_dst, uint32_t src, uint32_t bytes, uint32_t peer_bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(peer_dst),
-               "r"(src), "r"(bytes), "r"(peer_bar)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-// One CTA pair (a cluster of two) per (split, sequence); CTA `rank` of the pair owns half of D_v
-// and, for S = Q K^T, the 64-dim blocks own_block(rank, .): each CTA loads and multiplies only its
-// own blocks of every K tile (their first four blocks are its value half, read by P.V), computes
-// the partial S over them, and the two partial S are exchanged through distributed shared memory
-// and added (in the same order on both sides, so both hold the same S, hence the same P, m and l).
-// Warps 0-3 own one query head per thread (the tensor-memory lanes); warp 4's lane 0 issues every
-// MMA, warp 5's lane 0 every TMA copy and warp 6's lane 0 the exchange: the softmax threads write their
-// partial S rows to xsend, and one bulk copy per tile moves them into the partner's xrecv,
-// completing on the partner's xfull (armed with the expected bytes by the partner's own exchange
-// thread). Per 64-token tile t:
-//   K(t)   : TMA of this CTA's blocks into stage t % 3                  (kfull; kempty after P.V(t))
-//   S(t)   = Q K(t)^T over those blocks (A = Q from tensor memory)      (sfull; sfree once read)
-//   x(t)   : partial S rows to the partner (xwritten -> bulk copy -> the partner's xfull; xsent
-//            once the copy has read xsend; xread -> the partner's xempty once the rows are read)
-//   P(t)   : softmax of S = mine + partner's, O rescaled when needed     (pready)
-//   O     += P(t) V(t)   (V = the CTA's four value blocks, MN-major)     (pvdone)
-// in the issue order S(t+1) (as soon as S(t) is in registers), then P.V(t).
-__global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
-    mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK) {
+// One CTA per (split, half of D_v, sequence); warps 0-3 own one query head per thread (the
+// tensor-memory lanes), warp 4's lane 0 issues every TMA copy and every MMA. A tcgen05.mma
+// costs about the same to issue whatever its N up to 256, so S uses 64-token tiles (N = 64):
+//   K(t)  : TMA (two 32-row boxes per 64-dim block) into stage t % 2   (kfull; freed after P.V(t))
+//   S(t)  = Q K(t)^T (A = Q from tensor memory for dims 0..383, from shared memory for the rest)
+//   P(t)  : softmax warps read S(t), rescale O when needed, write P(t)   (pready)
+//   O    += P(t) V(t)   (V = the first 512 dims of K(t), MN-major)        (pvdone)
+// in the order P.V(t), S(t+1), then the copy of K(t+2) into the stage P.V(t) released.
+__global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
+                                                                   const __grid_constant__ CUtensorMap tmK) {
   pdl_wait();  // dependents are released when this grid completes
   extern __shared__ unsigned char dyn[];
   unsigned char *base = align1024(dyn);
-  unsigned char *sK = base;                     // kKStages stages of this CTA's blocks
-  unsigned char *sP = sK + kKStages * kKStage;  // P
-  float *xsend = reinterpret_cast<float *>(sP + kPBytes);  // this CTA's partial S rows, sent to the partner
-  float *xrecv = xsend + kXBytes / 4;                      // the partner's partial S rows
-  __shared__ __align__(8) uint64_t kfull[kKStages], kempty[kKStages], sfull, sfree, pready, pvdone, drained, xfull,
-      xempty, xwritten, xsent, xread;
+  unsigned char *sQ = base;                    // Q dims 384..575
+  unsigned char *sK = base + kQSBytes;         // kKStages K tiles
+  unsigned char *sP = sK + kKStages * kKTile;  // P
+  // K tile parts: A = the 64-dim blocks only S reads (free once S(t) is done), B = the four
+  // value blocks of this half of D_v (free once P.V(t) is done)
+  __shared__ __align__(8) uint64_t qbar, kfa[kKStages], kfb[kKStages], kea[kKStages], keb[kKStages], sfull, sfree,
+      pready, pvdone, drained;
   __shared__ int abort_sh;  // set by the first wait that gives up: every later wait returns at once
   __shared__ uint32_t tslot;
   __shared__ int ent_blk[kMlaMaxSw], ent_valid[kMlaMaxSw];
@@ -339,9 +286,7 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
   __shared__ int n_halves_sh;
   __shared__ int flag_last;
 
-  const int s = blockIdx.x, vh = blockIdx.y, i = blockIdx.z;  // vh: the CTA's rank in the pair
-  const uint32_t peer = (uint32_t)(vh ^ 1);
-  const int n_own = vh == 0 ? 5 : 4;
+  const int s = blockIdx.x, vh = blockIdx.y, i = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = i * 2 + vh;
   const size_t pbase = (size_t)unit * a.n_items_max + s;
@@ -382,20 +327,18 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
     ent_valid[x] = ok ? min(a.ps, seq_len - pg * a.ps) : 0;
   }
   if (tid == 0) {
+    mbar_init(smem_u32(&qbar), 1);
     mbar_init(smem_u32(&drained), 1);
     mbar_init(smem_u32(&sfull), 1);
     mbar_init(smem_u32(&sfree), 4);
     mbar_init(smem_u32(&pready), 4);
     mbar_init(smem_u32(&pvdone), 1);
     for (int k = 0; k < kKStages; ++k) {
-      mbar_init(smem_u32(&kfull[k]), 1);
-      mbar_init(smem_u32(&kempty[k]), 1);
+      mbar_init(smem_u32(&kfa[k]), 1);
+      mbar_init(smem_u32(&kfb[k]), 1);
+      mbar_init(smem_u32(&kea[k]), 1);
+      mbar_init(smem_u32(&keb[k]), 1);
     }
-    mbar_init(smem_u32(&xfull), 1);       // the exchange thread's arming + the partner's bytes
-    mbar_init(smem_u32(&xempty), 1);      // the partner's exchange thread: it has read what we sent
-    mbar_init(smem_u32(&xwritten), kHeads);
-    mbar_init(smem_u32(&xsent), 1);
-    mbar_init(smem_u32(&xread), kHeads);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -411,31 +354,28 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
   }
   const uint32_t tmem = tslot;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  if (warp < 4 && n_ent > 0) {  // Q of this CTA's blocks, head `tid`, into tensor memory (bf16 pairs)
+  if (warp < 4 && n_ent > 0) {  // Q dims 0..383 of head `tid` into tensor memory (bf16 pairs)
     const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) +
                                                         ((size_t)i * kHeads + tid) * kD);
 #pragma unroll 1
-    for (int j = 0; j < n_own; ++j) {
-      const int kb = own_block(vh, j);
+    for (int c = 0; c < kQTmemKB; ++c) {
       uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = __ldg(qrow + kb * 8 + c);
-        w[4 * c] = v.x;
-        w[4 * c + 1] = v.y;
-        w[4 * c + 2] = v.z;
-        w[4 * c + 3] = v.w;
+      for (int j = 0; j < 8; ++j) {
+        const uint4 v = __ldg(qrow + c * 8 + j);
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
       }
-      tmem_st32(tmem + lane_base + kQCol + j * 32, w);
+      tmem_st32(tmem + lane_base + kQCol + c * 32, w);
     }
   }
   tc_fence_before();
   __syncthreads();
-  // both CTAs' barriers are initialised before either touches the other's shared memory
-  cluster_sync();
   tc_fence_after();
   const int n_halves = n_halves_sh;
-  const int n_tiles = (n_halves + 1) / 2;  // the same in both CTAs of the pair (same split)
+  const int n_tiles = (n_halves + 1) / 2;
   // live rows of the two halves of tile t (0 for a missing second half)
   auto half_rows = [&](int hx) -> int {
     if (hx >= n_halves) return 0;
@@ -448,100 +388,109 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
     *reinterpret_cast<volatile int *>(&abort_sh) = 1;
     return false;
   };
-  auto wait_cluster_ok = [&](uint64_t *bar, uint32_t parity) -> bool {
-    if (*reinterpret_cast<volatile int *>(&abort_sh)) return false;
-    if (mbar_wait_cluster(smem_u32(bar), parity, a.ws)) return true;
-    *reinterpret_cast<volatile int *>(&abort_sh) = 1;
-    return false;
-  };
 
-  if (warp == 6) {
-    // ---------------- exchange thread: partial S rows to the partner, one bulk copy per tile ----
+  // the k-th 64-dim block S reads: part A (blocks outside this CTA's value half) first, then
+  // part B (the value blocks vh * 4 .. vh * 4 + 3)
+  auto s_block = [&](int k) -> int {
+    const int kb = k < kKB - 4 ? k : (k - (kKB - 4)) + vh * 4;  // k >= 5: part B
+    return k < kKB - 4 ? (kb < vh * 4 ? kb : kb + 4) : kb;
+  };
+  if (warp == 5) {
+    // ---------------- loading thread: TMA copies ----------------
     if (lane == 0 && n_tiles > 0) {
-    const uint32_t peer_xrecv = cluster_map(smem_u32(xrecv), peer);
-    const uint32_t peer_xfull = cluster_map(smem_u32(&xfull), peer);
-    const uint32_t peer_xempty = cluster_map(smem_u32(&xempty), peer);
-#pragma unroll 1
-    for (int t = 0; t < n_tiles; ++t) {
-      if (t >= 1) {
-        // our softmax threads have read the partner's rows of tile t-1: its next copy may land
-        if (!wait_ok(&xread, (t - 1) & 1)) break;
-        mbar_arrive_remote(peer_xempty);
-      }
-      mbar_arrive_expect_tx(smem_u32(&xfull), (uint32_t)kXBytes);  // receive tile t
-      if (!wait_ok(&xwritten, t & 1)) break;                         // our rows of tile t are in xsend
-      if (t >= 1 && !wait_cluster_ok(&xempty, (t - 1) & 1)) break;   // the partner read our tile t-1
-      bulk_s2peer(peer_xrecv, smem_u32(xsend), (uint32_t)kXBytes, peer_xfull);
-      mbar_arrive(smem_u32(&xsent));  // xsend may be rewritten
-    }
-    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");  // every copy to the partner has completed
-    }
-  } else if (warp == 5) {
-    // ---------------- loading thread: TMA copies of this CTA's blocks ----------------
-    if (lane == 0 && n_tiles > 0) {
-      int issued = 0;
-#pragma unroll 1
-      for (int t = 0; t < n_tiles; ++t) {
+      int na = 0, nb = 0;  // part A / part B copies issued
+      auto load_part = [&](int t, bool part_b) {
         const int st = t % kKStages;
-        if (t >= kKStages && !wait_ok(&kempty[st], ((t - kKStages) / kKStages) & 1)) break;  // P.V(t-3) done
         const int nh = (2 * t + 1 < n_halves) ? 2 : 1;
-        const uint32_t bar = smem_u32(&kfull[st]);
-        mbar_arrive_expect_tx(bar, (uint32_t)(nh * n_own * kHalf * 128));
-        const uint32_t dst = smem_u32(sK + st * kKStage);
+        const uint32_t bar = smem_u32(part_b ? &kfb[st] : &kfa[st]);
+        const int nblk = part_b ? 4 : kKB - 4;
+        mbar_arrive_expect_tx(bar, (uint32_t)(nh * nblk * kHalf * 128));
+        const uint32_t dst = smem_u32(sK + st * kKTile);
         for (int h2 = 0; h2 < nh; ++h2) {
           const int hx = 2 * t + h2;
           const int e = halves[hx] >> 1, hh = halves[hx] & 1;
           const int row0 = ent_blk[e] * a.ps + hh * kHalf;
 #pragma unroll 1
-          for (int j = 0; j < n_own; ++j)
-            tma_load_2d(dst + j * kKBlock + h2 * kHalf * 128, &tmK, own_block(vh, j) * 64, row0, bar);
+          for (int k = part_b ? kKB - 4 : 0; k < (part_b ? kKB : kKB - 4); ++k) {
+            const int kb = s_block(k);
+            tma_load_2d(dst + kb * kKBlock + h2 * kHalf * 128, &tmK, kb * 64, row0, bar);
+          }
         }
-        issued = t + 1;
+      };
+      mbar_arrive_expect_tx(smem_u32(&qbar), kQSBytes);
+#pragma unroll 1
+      for (int kb = 0; kb < kQSmemKB; ++kb)
+        tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, (kQTmemKB + kb) * 64, i * kHeads, smem_u32(&qbar));
+#pragma unroll 1
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % kKStages;
+        if (t >= kKStages && !wait_ok(&kea[st], ((t - kKStages) / kKStages) & 1)) break;  // S(t-2) done
+        load_part(t, false);
+        na = t + 1;
+        if (t >= kKStages && !wait_ok(&keb[st], ((t - kKStages) / kKStages) & 1)) break;  // P.V(t-2) done
+        load_part(t, true);
+        nb = t + 1;
       }
       // every copy in flight lands before shared memory is released (also after a wait gave up)
-      for (int t = max(0, issued - kKStages); t < issued; ++t)
-        mbar_wait(smem_u32(&kfull[t % kKStages]), (t / kKStages) & 1, a.ws);
+      for (int t = max(0, na - kKStages); t < na; ++t) mbar_wait(smem_u32(&kfa[t % kKStages]), (t / kKStages) & 1, a.ws);
+      for (int t = max(0, nb - kKStages); t < nb; ++t) mbar_wait(smem_u32(&kfb[t % kKStages]), (t / kKStages) & 1, a.ws);
+      mbar_wait(smem_u32(&qbar), 0, a.ws);
     }
   } else if (warp == 4) {
     // ---------------- issuing thread: MMAs ----------------
     if (lane == 0 && n_tiles > 0) {
+      bool ok = wait_ok(&qbar, 0);
       const uint32_t idesc_qk = umma_idesc(128, kTile, false);
       const uint32_t idesc_pv = umma_idesc(128, 256, true);
-      // Descriptors advance by (bytes >> 4): +32 bytes per 16-dim step of a block.
-      auto issue_s = [&](int u) -> bool {
+      // S(u) = Q K(u)^T in two parts: the blocks outside this CTA's value half (part A), then the
+      // value blocks (part B); P.V of the previous tile is issued between them so that the value
+      // blocks it frees can be refilled early. Descriptors advance by (bytes >> 4).
+      const uint32_t q0 = smem_u32(sQ);
+      auto issue_s_part = [&](int u, bool part_b) -> bool {
         const int st = u % kKStages;
-        if (!wait_ok(&kfull[st], (u / kKStages) & 1)) return false;
+        if (!wait_ok(part_b ? &kfb[st] : &kfa[st], (u / kKStages) & 1)) return false;
         tc_fence_after();
         const uint32_t d = tmem + kSCol;
-        const uint32_t k0 = smem_u32(sK + st * kKStage);
+        const uint32_t k0 = smem_u32(sK + st * kKTile);
 #pragma unroll 1
-        for (int j = 0; j < n_own; ++j) {
-          const uint64_t b0 = umma_desc(k0 + j * kKBlock, 16, 1024, 2);
-          const uint32_t a0 = tmem + kQCol + j * 32;
+        for (int k = part_b ? kKB - 4 : 0; k < (part_b ? kKB : kKB - 4); ++k) {
+          const int kb = s_block(k);
+          const uint64_t b0 = umma_desc(k0 + kb * kKBlock, 16, 1024, 2);
+          if (kb < kQTmemKB) {
+            const uint32_t a0 = tmem + kQCol + kb * 32;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) umma_bf16_ts(d, a0 + ks * 8, b0 + 2 * ks, idesc_qk, (j | ks) != 0);
+            for (int ks = 0; ks < 4; ++ks) umma_bf16_ts(d, a0 + ks * 8, b0 + 2 * ks, idesc_qk, (k | ks) != 0);
+          } else {
+            const uint64_t a0 = umma_desc(q0 + (kb - kQTmemKB) * kHeads * 128, 16, 1024, 2);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma_bf16(d, a0 + 2 * ks, b0 + 2 * ks, idesc_qk, (k | ks) != 0);
+          }
         }
-        umma_commit(smem_u32(&sfull));
+        umma_commit(smem_u32(part_b ? &sfull : &kea[st]));
         return true;
       };
       auto issue_pv = [&](int t) -> bool {
         if (!wait_ok(&pready, t & 1)) return false;  // P(t) written, O rescaled
         tc_fence_after();
         const uint64_t pa = umma_desc(smem_u32(sP), 16, 1024, 2);
-        const uint64_t vb = umma_desc(smem_u32(sK + (t % kKStages) * kKStage), kKBlock, 1024, 2);
+        const uint64_t vb = umma_desc(smem_u32(sK + (t % kKStages) * kKTile + vh * 4 * kKBlock), kKBlock, 1024, 2);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // P: +32 bytes per 16 tokens; V: +16 rows of 128 bytes
           umma_bf16(tmem + kOCol, pa + 2 * ks, vb + 128 * ks, idesc_pv, (t | ks) != 0);
         umma_commit(smem_u32(&pvdone));
-        umma_commit(smem_u32(&kempty[t % kKStages]));
+        umma_commit(smem_u32(&keb[t % kKStages]));
         return true;
       };
-      bool ok = issue_s(0);
+      ok = ok && issue_s_part(0, false) && issue_s_part(0, true);
 #pragma unroll 1
       for (int t = 0; ok && t < n_tiles; ++t) {
-        // S(t+1) as soon as the softmax warps hold S(t) in registers, then P.V(t)
-        if (t + 1 < n_tiles && (!wait_ok(&sfree, t & 1) || !issue_s(t + 1))) break;
-        if (!issue_pv(t)) break;
+        if (t + 1 < n_tiles) {
+          // S(t+1) part A as soon as the softmax warps hold S(t) in registers
+          if (!wait_ok(&sfree, t & 1) || !issue_s_part(t + 1, false)) break;
+          if (!issue_pv(t) || !issue_s_part(t + 1, true)) break;
+        } else if (!issue_pv(t)) {
+          break;
+        }
       }
       // every MMA issued completes before tensor memory and shared memory are released
       umma_commit(smem_u32(&drained));
@@ -557,56 +506,21 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
       tc_fence_after();
       const int nva = half_rows(2 * t), nvb = half_rows(2 * t + 1);
       float x[kTile];
+      float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t sv[32];
         tmem_ld32(tmem + lane_base + kSCol + c * 32, sv);
+        const int nv = c == 0 ? nva : nvb;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(sv[j]);
+        for (int j = 0; j < 32; ++j) {
+          x[c * 32 + j] = j < nv ? __uint_as_float(sv[j]) * qs : -INFINITY;
+          mt = fmaxf(mt, x[c * 32 + j]);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sfree));  // the issuing thread may overwrite S now
-      // ---- exchange the partial S rows with the partner (rows of 16-byte chunks, swizzled by head) ----
-      if (t >= 1 && !__all_sync(0xffffffffu, wait_ok(&xsent, (t - 1) & 1))) break;  // xsend is free again
-      {
-        float *dst = xsend + tid * kTile;
-#pragma unroll
-        for (int c = 0; c < kTile / 4; ++c)
-          *reinterpret_cast<float4 *>(dst + ((c ^ (tid & 15)) * 4)) =
-              make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-        fence_proxy_async_smem();  // the bulk copy reads these rows through the async proxy
-        mbar_arrive(smem_u32(&xwritten));
-      }
-      if (!__all_sync(0xffffffffu, wait_cluster_ok(&xfull, t & 1))) break;  // the partner's rows of tile t
-      {
-        const float *src = xrecv + tid * kTile;
-        // the rank-0 CTA adds (own + peer) and the rank-1 CTA (peer + own): the same two operands
-        // in the same order, so both CTAs hold bit-identical S
-#pragma unroll
-        for (int c = 0; c < kTile / 4; ++c) {
-          const float4 y = *reinterpret_cast<const float4 *>(src + ((c ^ (tid & 15)) * 4));
-          if (vh == 0) {
-            x[4 * c] += y.x;
-            x[4 * c + 1] += y.y;
-            x[4 * c + 2] += y.z;
-            x[4 * c + 3] += y.w;
-          } else {
-            x[4 * c] = y.x + x[4 * c];
-            x[4 * c + 1] = y.y + x[4 * c + 1];
-            x[4 * c + 2] = y.z + x[4 * c + 2];
-            x[4 * c + 3] = y.w + x[4 * c + 3];
-          }
-        }
-        mbar_arrive(smem_u32(&xread));  // the exchange thread tells the partner once all have read
-      }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        const int nv = j < kHalf ? nva : nvb;
-        x[j] = (j & (kHalf - 1)) < nv ? x[j] * qs : -INFINITY;
-        mt = fmaxf(mt, x[j]);
-      }
       // O holds P.V(t-1) and P is free once pvdone completes for t-1
       if (t > 0 && !__all_sync(0xffffffffu, wait_ok(&pvdone, (t - 1) & 1))) break;
       tc_fence_after();
@@ -648,7 +562,7 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
       // whatever the stage last received; their P is 0, but 0 * NaN is NaN, so the value rows
       // this CTA multiplies are zeroed (128 bytes per row and 64-dim block).
       if (nva < kHalf || nvb < kHalf) {
-        unsigned char *vblk = sK + (t % kKStages) * kKStage;
+        unsigned char *vblk = sK + (t % kKStages) * kKTile + vh * 4 * kKBlock;
         for (int x2 = tid; x2 < 4 * kTile * 8; x2 += kHeads) {
           const int kb = x2 / (kTile * 8), r = (x2 / 8) % kTile, c = x2 % 8;
           const bool live = r < kHalf ? r < nva : (r - kHalf) < nvb;
@@ -681,9 +595,6 @@ __global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(kDecThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // no remote store or arrive may target a CTA of the pair that has left: both pass this point
-  // only after every exchange of the launch
-  cluster_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
 
   // ---- the last CTA of (sequence, half) merges the splits ----------------------------------
@@ -793,10 +704,12 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
 }
 
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
-  CUtensorMap tmK;
-  if (!encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kHalf)) return cudaErrorInvalidValue;
-  dim3 grid(a.n_items_max, 2, a.B);  // the two CTAs of a (split, sequence) form one cluster
-  return launch_kernel(true, mla_decode_kernel, grid, kDecThreads, kDecSmem, s, a, tmK);
+  CUtensorMap tmQ, tmK;
+  if (!encode_matrix_map_sw128(&tmQ, a.q, kD, (long long)a.B * kHeads, 64, kHeads) ||
+      !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kHalf))
+    return cudaErrorInvalidValue;
+  dim3 grid(a.n_items_max, 2, a.B);
+  return launch_kernel(true, mla_decode_kernel, grid, kDecThreads, kDecSmem, s, a, tmQ, tmK);
 }
 
 }  // namespace psk
