@@ -57,7 +57,16 @@ def peaks():
 # call, with a digest of the sources the kernels are built from: a digest that no longer matches
 # means the kernels changed since the capture, and the traffic is reported as null.
 TRAFFIC = {
-    # filled in from one-pass captures of the current kernels (measurement)
+    # One-pass capture on the first 16 sequences (profiles/page_score_kernel_batched_ragged_b16.md):
+    #   python bench.py --batch 16 --steps 3 --warmup 3 --no-cpu-baseline, then
+    #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
+    #       -k regex:"page_score|page_select|decode_split" -s 0 -c 3 python bench.py --batch 16 --steps 3 ...
+    # 158,050,560 + 3,093,760 B for 38,540 pages; scaled by pages to the 140,808 of the full workload.
+    ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel"):
+        {"bytes": 588_795_911, "digest": "7990f3db0cb68871", "scaled_from": "first 16 sequences, by pages"},
+    # 129,216,768 + 801,024 B for 15,472 selected (page, head) pairs; 56,536 in the full workload
+    ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
+        {"bytes": 475_096_037, "digest": "38b706d4703ec790", "scaled_from": "first 16 sequences, by selected pages"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
@@ -80,8 +89,8 @@ def kernel_digest(call: str) -> str:
 def traffic_of(workload: str, call: str):
     rec = TRAFFIC.get((workload, call))
     if rec is None or rec["digest"] != kernel_digest(call):
-        return None
-    return rec["bytes"]
+        return None, None
+    return rec["bytes"], rec.get("scaled_from")
 
 
 def dist_env():
@@ -602,7 +611,9 @@ def run_psk(args):
         roof["note"] = "V of the selected pages crosses NVLink-C2C, not HBM; achieved counts K and V bytes"
 
     roof["peak_kind"] = pk["kind"] + (" sustained bf16" if roof["bound"] == "tensor" else " copy")
-    roof["traffic"] = traffic_of(w.name, dom)
+    roof["traffic"], scaled = traffic_of(w.name, dom)
+    if scaled:
+        roof["traffic_note"] = f"ncu dram read + write per launch, captured on the {scaled}"
     roof["traffic_digest"] = kernel_digest(dom)
 
     cpu = None
