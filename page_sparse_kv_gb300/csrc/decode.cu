@@ -880,22 +880,6 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   }
   if (!a.flat) {
     dim3 grid(a.B * a.H_kv, a.n_items_max);
-    if constexpr (sizeof(T) == 2 && D == 128 && G == 4) {
-      // tuning override: warps per CTA x ring stages per warp (same 64 KB of stages for 2 x 4)
-      switch (tuning().decode_shape) {
-        case 24:
-          return launch_kernel(true, decode_split_kernel<T, D, G, 2, 4, false>, grid, 2 * 32,
-                               DT<T, D, G, 2, 4>::SMEM, s, a, tmK, tmV);
-        case 43:
-          return launch_kernel(true, decode_split_kernel<T, D, G, 4, 3, false>, grid, 4 * 32,
-                               DT<T, D, G, 4, 3>::SMEM, s, a, tmK, tmV);
-        case 23:
-          return launch_kernel(true, decode_split_kernel<T, D, G, 2, 3, false>, grid, 2 * 32,
-                               DT<T, D, G, 2, 3>::SMEM, s, a, tmK, tmV);
-        default:
-          break;
-      }
-    }
     return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, false>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
   }
   const int U = a.B * a.H_kv;

@@ -64,7 +64,6 @@ struct Tuning {
   int decode_layout = 0;  // 0 default, 1 split, 2 flat
   int decode_split = -1;
   bool decode_no_taper = false;
-  int decode_shape = 0;  // PSK_DECODE_SHAPE: warps x stages of the split decode, e.g. 24 = 2 x 4 (bf16 D 128 G 4)
 };
 const Tuning &tuning();
 

@@ -115,7 +115,6 @@ const Tuning &tuning() {
     if (const char *v = std::getenv("PSK_DECODE_LAYOUT")) r.decode_layout = !std::strcmp(v, "split") ? 1 : (!std::strcmp(v, "flat") ? 2 : 0);
     if (const char *v = std::getenv("PSK_DECODE_SPLIT")) r.decode_split = std::atoi(v);
     r.decode_no_taper = std::getenv("PSK_DECODE_NO_TAPER") != nullptr;
-    if (const char *v = std::getenv("PSK_DECODE_SHAPE")) r.decode_shape = std::atoi(v);
     return r;
   }();
   return t;
