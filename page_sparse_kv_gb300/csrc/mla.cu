@@ -484,13 +484,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       ok = ok && issue_s_part(0, false) && issue_s_part(0, true);
 #pragma unroll 1
       for (int t = 0; ok && t < n_tiles; ++t) {
-        if (t + 1 < n_tiles) {
-          // S(t+1) part A as soon as the softmax warps hold S(t) in registers
-          if (!wait_ok(&sfree, t & 1) || !issue_s_part(t + 1, false)) break;
-          if (!issue_pv(t) || !issue_s_part(t + 1, true)) break;
-        } else if (!issue_pv(t)) {
+        // all of S(t+1) as soon as the softmax warps hold S(t) in registers, so the tensor pipe
+        // computes it while they turn S(t) into P(t); then P.V(t)
+        if (t + 1 < n_tiles &&
+            (!wait_ok(&sfree, t & 1) || !issue_s_part(t + 1, false) || !issue_s_part(t + 1, true)))
           break;
-        }
+        if (!issue_pv(t)) break;
       }
       // every MMA issued completes before tensor memory and shared memory are released
       umma_commit(smem_u32(&drained));
