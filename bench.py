@@ -611,7 +611,8 @@ def run_psk(args):
         roof["note"] = "V of the selected pages crosses NVLink-C2C, not HBM; achieved counts K and V bytes"
 
     roof["peak_kind"] = pk["kind"] + (" sustained bf16" if roof["bound"] == "tensor" else " copy")
-    roof["traffic"], scaled = traffic_of(w.name, dom)
+    # the captured traffic is of the HBM-resident decode: with V in host memory it does not apply
+    roof["traffic"], scaled = traffic_of(w.name, dom) if not (args.v_host and dom == "decode_split_kernel") else (None, None)
     if scaled:
         roof["traffic_note"] = f"ncu dram read + write per launch, captured on the {scaled}"
     roof["traffic_digest"] = kernel_digest(dom)
