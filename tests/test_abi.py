@@ -184,3 +184,72 @@ def test_score_select_launch_count(lib):
     latent = psk.Layout(16, 128, 1, 576, 512, 64, 40000, 2048, psk.PSK_BF16, 1)
     assert psk.score_select_launches(latent, 103) == 3
     assert psk.score_select_launches(psk.Layout(2, 32, 8, 96, 96, 16, 100, 50), 10) == 0
+
+
+def test_new_entry_points_reject_before_launch(lib):
+    """Coverage, mean/std append, Gaussian score and the value tier: host checks answer without a
+    GPU (every call here is refused before any launch)."""
+    import page_sparse_kv_gb300 as psk
+    P = ctypes.c_void_p
+    L = psk.Layout(2, 32, 8, 128, 128, 16, 100, 50).c()
+    latent = psk.Layout(2, 128, 1, 576, 512, 64, 100, 50, psk.PSK_BF16, 1).c()
+    f32 = psk.Layout(2, 4, 1, 64, 64, 16, 100, 50, psk.PSK_F32).c()
+    big = 1 << 30
+    # coverage: sizes, null pointers, coverage outside (0, 1], latent, small workspace
+    assert psk.coverage_workspace_size(psk.Layout(2, 32, 8, 128, 128, 16, 100, 50), 10) > \
+        psk.score_select_workspace_size(psk.Layout(2, 32, 8, 128, 128, 16, 100, 50), 10)
+    assert lib.psk_coverage_workspace_size(ctypes.byref(latent), 10) == 0
+    cov = lib.psk_page_select_coverage
+    assert cov(ctypes.byref(L), None, P(16), P(16), P(16), 0.9, 1, 1, 10, 1.0, P(16), None, P(16), big, None) == 1
+    assert cov(ctypes.byref(L), P(16), P(16), P(16), P(16), 0.0, 1, 1, 10, 1.0, P(16), None, P(16), big, None) == 1
+    assert cov(ctypes.byref(L), P(16), P(16), P(16), P(16), 1.5, 1, 1, 10, 1.0, P(16), None, P(16), big, None) == 1
+    assert cov(ctypes.byref(L), P(16), P(16), P(16), P(16), 0.9, 1, 0, 10, 1.0, P(16), None, P(16), big, None) == 1
+    assert cov(ctypes.byref(latent), P(16), P(16), P(16), P(16), 0.9, 1, 1, 10, 1.0, P(16), None, P(16), big,
+               None) == 2
+    assert cov(ctypes.byref(L), P(16), P(16), P(16), P(16), 0.9, 1, 1, 10, 1.0, P(16), None, P(16), 64, None) == 3
+    # append with the mean / std store: one store at least, 16-byte aligned
+    ap = lib.psk_kv_append_and_summarize_ex
+    assert ap(ctypes.byref(L), P(16), P(16), P(16), P(16), 1, 1, P(16), P(16), None, None, P(16), P(16), 256,
+              None) == 1
+    assert ap(ctypes.byref(L), P(16), P(16), P(16), P(16), 1, 1, P(16), P(16), None, P(20), P(16), P(16), 256,
+              None) == 1
+    assert ap(ctypes.byref(L), P(16), P(16), P(16), P(16), 0, 0, P(16), P(16), None, P(16), P(16), P(16), 256,
+              None) == 0  # nothing to append: OK before any launch
+    # Gaussian score: stats required; per-query-head rows and latent caches are not built
+    prm = psk.select_params(budgets=torch_free_budgets())
+    g = lib.psk_page_score_select_gaussian
+    assert g(ctypes.byref(L), P(16), None, P(16), P(16), ctypes.byref(prm), 10, 1.0, 1.5, P(16), None, P(16), big,
+             None) == 1
+    assert g(ctypes.byref(L), P(16), P(16), P(16), P(16), ctypes.byref(prm), 10, 1.0, float("nan"), P(16), None,
+             P(16), big, None) == 1
+    prm_q = psk.select_params(budgets=torch_free_budgets(), per_query_head=True)
+    assert g(ctypes.byref(L), P(16), P(16), P(16), P(16), ctypes.byref(prm_q), 10, 1.0, 1.5, P(16), None, P(16),
+             big, None) == 2
+    # value tier: hot buffer and slot map required; fill only for bf16 GQA with head_dim 128
+    t = lib.psk_sparse_paged_decode_tiered
+    assert t(ctypes.byref(L), P(16), P(16), P(16), P(16), 0, P(16), P(16), P(16), P(16), 10, 1.0, P(16), P(16), big,
+             None) == 1
+    assert t(ctypes.byref(L), P(16), P(16), P(16), P(16), 4, None, P(16), P(16), P(16), 10, 1.0, P(16), P(16), big,
+             None) == 1
+    fill = lib.psk_value_tier_fill
+    assert fill(ctypes.byref(latent), P(16), P(16), P(16), 1, P(16), 4, P(16), P(16), 256, None) == 2
+    assert fill(ctypes.byref(f32), P(16), P(16), P(16), 1, P(16), 4, P(16), P(16), 256, None) == 2
+    assert fill(ctypes.byref(L), P(16), P(16), None, 1, P(16), 4, P(16), P(16), 256, None) == 1
+    assert fill(ctypes.byref(L), P(16), P(16), P(16), -1, P(16), 4, P(16), P(16), 256, None) == 1
+    assert fill(ctypes.byref(L), P(16), P(16), P(16), 0, P(16), 4, P(16), P(16), 256, None) == 0  # nothing to do
+
+
+def torch_free_budgets():
+    """A stand-in for a device budget tensor: select_params only needs its pointer."""
+    class _T:
+        is_cuda = True
+
+        def is_pinned(self):
+            return False
+
+        def is_contiguous(self):
+            return True
+
+        def data_ptr(self):
+            return 16
+    return _T()
