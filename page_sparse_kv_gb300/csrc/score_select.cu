@@ -296,24 +296,233 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
   pdl_trigger();
 }
 
+// ------------------------------------------------------------------------------------
+// page scores on the tensor cores (bf16 caches, per-KV-head units)
+// ------------------------------------------------------------------------------------
+// A page's bound for query head g is one dot product of length 2D: its stored summary row
+// [kmin | kmax] against [min(q_g,0) | max(q_g,0)] (both halves exact in bf16). So a warp-level
+// mma.sync.m16n8k16 (bf16 in, fp32 accumulate) scores 16 (page, KV head) rows at once: rows 0-7
+// are 8 consecutive pages of head hA, rows 8-15 8 pages of head hB; columns 0-3 hold hA's query
+// heads, columns 4-7 hB's (columns past G are zero). Each row's score is the max over its own
+// head's columns; the cross terms are not used. The products are exact in fp32 and the sums are
+// fp32 (the tensor cores' order), so the result meets the same bound as the FMA kernel above, at
+// 2D / 16 MMAs per 16 rows instead of 2D * G / 16 FMAs per row on each lane.
+//
+// Staging is the same bulk-copy ring as page_score_kernel with two changes: stages hold a
+// multiple of 8 pages, and pages sit group_bytes + 16 bytes apart (group_bytes is a multiple of
+// 128), so the 8 rows of an ldmatrix (8 pages of one head, equal offsets inside their rows) fall
+// in 8 different bank groups. Four warps: warp w takes head pair w % n_pairs of the CTA's heads
+// (one pair per two heads; with one head, rows 8-15 take the next 8 pages of the same head).
+constexpr int kMmaThreads = 128;
+constexpr int kMmaWarps = kMmaThreads / 32;
+constexpr int kMmaStages = 2;
+constexpr int kMmaStageBytes = 32768 + 512;  // 8 pages x (4 KB + 16) at H = 8, D = 128; 32 x (1 KB + 16)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// c += A (16 x 16, row-major fragment) * B (16 x 8, column-major fragment), fp32 accumulate
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a) {
+  pdl_wait();
+  static_assert(G >= 1 && G <= 4, "four query heads per KV head at most");
+  constexpr int KS = 2 * D / 16;  // k-steps over a summary row [kmin | kmax]
+  constexpr int RB = 2 * D * 2;   // bytes of one (page, head) summary row
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kMmaStages];
+  __shared__ int okflag[kMmaStages][kMaxStagePages];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA (as page_score_kernel)
+  // work item (chunk, sequence, head group): the same order and regions as page_score_kernel
+  int x = blockIdx.x;
+  const int n_body = a.body_chunks * a.B * (a.H_kv / hpc);
+  const bool in_tail = x >= n_body;
+  if (in_tail) x -= n_body;
+  const int per_seq = in_tail ? a.tail_chunks : a.body_chunks;
+  const int c = x % per_seq;
+  x /= per_seq;
+  const int i = x % a.B;
+  const int h0 = (x / a.B) * hpc;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
+  const int body_end = P - min(P, a.tail_pages);
+  const int p0 = in_tail ? body_end + c * a.tail_chunk : c * a.pchunk;
+  const int p1 = in_tail ? min(P, p0 + a.tail_chunk) : min(body_end, p0 + a.pchunk);
+  if (p0 >= p1) return;
+  const int group_bytes = hpc * RB;
+  const int sp = a.stage_pages;  // a multiple of 8
+  const int n_stages = (p1 - p0 + sp - 1) / sp;
+  const bf16_t *sumbase = reinterpret_cast<const bf16_t *>(a.summaries);
+  const int32_t *bt = a.block_table + (size_t)i * a.max_pages;
+
+  if (tid == 0) {
+    for (int k = 0; k < kMmaStages; ++k) mbar_init(smem_u32(&bars[k]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto block_of = [&](int st) -> int {
+    const int p = p0 + st * sp + lane;
+    return (lane < sp && st < n_stages && p < p1) ? __ldg(bt + p) : -1;
+  };
+  const uint64_t stream_policy = l2_evict_first_policy();
+  auto produce = [&](int st, int blk) {
+    const int slot = st % kMmaStages;
+    const int p = p0 + st * sp + lane;
+    const bool in_chunk = lane < sp && p < p1;
+    const bool valid = blk >= 0 && blk < a.nb;
+    if (in_chunk && !valid) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+    const bool needed = a.scores_out != nullptr || !always_kept(p, P, a.sink, a.window);
+    const bool ok = in_chunk && valid && needed;
+    if (lane < sp) okflag[slot][lane] = ok;
+    const unsigned mask = __ballot_sync(0xffffffffu, ok);
+    const uint32_t bar = smem_u32(&bars[slot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(mask) * group_bytes);
+    __syncwarp();
+    if (ok)
+      bulk_g2s_stream(smem_u32(smem_raw + (size_t)slot * kMmaStageBytes + (size_t)lane * (group_bytes + 16)),
+                      sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar, stream_policy);
+  };
+
+  if (warp == 0)
+    for (int st = 0; st < kMmaStages && st < n_stages; ++st) produce(st, block_of(st));
+
+  // head pair of this warp (heads local to the CTA's group)
+  const int n_pairs = hpc >= 2 ? hpc / 2 : 1;
+  const int pair = warp % n_pairs, wsub = warp / n_pairs, wpp = kMmaWarps / n_pairs;
+  const int hlA = hpc >= 2 ? 2 * pair : 0, hlB = hpc >= 2 ? 2 * pair + 1 : 0;
+
+  // B fragments for all k-steps: lane holds column n = lane / 4 (head hA for n < 4, else hB;
+  // query head n % 4 of it) at k = 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) of each k-step, t = lane % 4.
+  // k-steps 0 .. D/16-1 meet kmin (min(q,0)), the rest kmax (max(q,0)).
+  uint32_t bq[KS][2];
+  {
+    const int n = lane >> 2, t = lane & 3;
+    const int g = n & 3;
+    const int hl = n < 4 ? hlA : hlB;
+    if (g < G) {
+      const uint32_t *qr = reinterpret_cast<const uint32_t *>(reinterpret_cast<const bf16_t *>(a.q) +
+                                                              ((size_t)i * a.H_q + (size_t)(h0 + hl) * G + g) * D);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t w = __ldg(qr + 8 * s + t + 4 * e);
+          const uint32_t m = ((w & 0x80008000u) >> 15) * 0xFFFFu;  // negative halves
+          bq[s][e] = w & m;               // min(q, 0)
+          bq[s + D / 16][e] = w & ~m;     // max(q, 0)
+        }
+      }
+    } else {
+#pragma unroll
+      for (int s = 0; s < KS; ++s) bq[s][0] = bq[s][1] = 0u;
+    }
+  }
+
+  // ldmatrix row of this lane: matrix mi = lane / 8 (rows 0-7 or 8-15, k 0-7 or 8-15 of the step)
+  const int mi = lane >> 3, rr = lane & 7;
+  const bool rowB = (mi & 1) != 0;
+  const uint32_t lane_off = (uint32_t)(rowB ? hlB : hlA) * RB + (uint32_t)(mi >> 1) * 16;
+  // epilogue position: rows r0 (item A) / r0 + 8 (item B), columns 2t, 2t + 1
+  const int r0 = lane >> 2, t = lane & 3;
+  const bool outB = t >= 2;
+  const int g0 = 2 * (t & 1);
+
+  for (int st = 0; st < n_stages; ++st) {
+    const int slot = st % kMmaStages;
+    const int next_blk = warp == 0 ? block_of(st + kMmaStages) : -1;
+    mbar_wait(smem_u32(&bars[slot]), (st / kMmaStages) & 1, a.ws);
+    const uint32_t stage_addr = smem_u32(smem_raw + (size_t)slot * kMmaStageBytes);
+    const int pb = p0 + st * sp;
+    const int np = min(sp, p1 - pb);
+    const int n_oct = (np + 7) >> 3;
+    const int n_items = hpc >= 2 ? n_oct : (n_oct + 1) >> 1;
+    for (int m = wsub; m < n_items; m += wpp) {  // warp-uniform bound
+      const int oA = hpc >= 2 ? m : 2 * m, oB = hpc >= 2 ? m : 2 * m + 1;
+      // rows past the stage's live pages read the last page of the stage (discarded below)
+      const int j = min(((rowB ? oB : oA) << 3) + rr, sp - 1);
+      const uint32_t addr = stage_addr + (uint32_t)j * (uint32_t)(group_bytes + 16) + lane_off;
+      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < KS; s += 2) {
+        uint32_t fa[4], fb[4];
+        ldsm_x4(addr + s * 32, fa);
+        ldsm_x4(addr + s * 32 + 32, fb);
+        mma_16816_bf16(acc0, fa, bq[s][0], bq[s][1]);
+        mma_16816_bf16(acc1, fb, bq[s + 1][0], bq[s + 1][1]);
+      }
+      const float x0 = outB ? acc0[2] + acc1[2] : acc0[0] + acc1[0];
+      const float x1 = outB ? acc0[3] + acc1[3] : acc0[1] + acc1[1];
+      float v = g0 < G ? x0 : -INFINITY;
+      if (g0 + 1 < G) v = fmaxf(v, x1);
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      const int jo = ((outB ? oB : oA) << 3) + r0;
+      if ((t & 1) == 0 && jo < np) {
+        const int p = pb + jo;
+        const int unit = i * a.H_kv + h0 + (outB ? hlB : hlA);
+        const float sc = v * a.scale;
+        const bool forced = always_kept(p, P, a.sink, a.window);
+        a.keys[(size_t)unit * a.key_stride + p] = (okflag[slot][jo] && !forced) ? score_key(sc) : 0u;
+        if (a.scores_out) a.scores_out[(size_t)unit * a.max_pages + p] = sc;
+      }
+    }
+    __syncthreads();  // every warp is done with this slot
+    if (warp == 0 && st + kMmaStages < n_stages) {
+      fence_proxy_async_smem();
+      produce(st + kMmaStages, next_blk);
+    }
+  }
+  pdl_trigger();
+}
+
+// The score kernel for these units: the tensor-core kernel for bf16 per-KV-head units (unless
+// PSK_SCORE_MMA=0), else the FMA kernel.
+enum class ScoreKernel { kFma, kFmaPerQueryHead, kMma };
+
+template <typename T, int D, int G>
+const void *score_kernel_fn(ScoreKernel k) {
+  if constexpr (sizeof(T) == 2 && G <= 4)
+    if (k == ScoreKernel::kMma) return reinterpret_cast<const void *>(page_score_mma_kernel<D, G>);
+  if (k == ScoreKernel::kFmaPerQueryHead) return reinterpret_cast<const void *>(page_score_kernel<T, D, G, true>);
+  return reinterpret_cast<const void *>(page_score_kernel<T, D, G, false>);
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   if (!(stages & kStageScore)) return launch_page_select(a, s, true);
+  if (G > 1 && a.kv_shift != 0) return cudaErrorInvalidValue;  // the per-query-head view has G = 1
   const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
-  const int k1_smem = kStages * kStageBytes;
-  auto kfn = page_score_kernel<T, D, G, false>;
-  if constexpr (G == 1) {
-    if (a.kv_shift != 0) kfn = page_score_kernel<T, D, G, true>;
-  } else {
-    if (a.kv_shift != 0) return cudaErrorInvalidValue;  // the per-query-head view has G = 1
+  ScoreArgs b = a;
+  ScoreKernel kind = a.kv_shift != 0 ? ScoreKernel::kFmaPerQueryHead : ScoreKernel::kFma;
+  int threads = kThreads;
+  int smem = kStages * kStageBytes;
+  if (sizeof(T) == 2 && G <= 4 && a.kv_shift == 0 && tuning().score_mma) {
+    kind = ScoreKernel::kMma;
+    threads = kMmaThreads;
+    smem = kMmaStages * kMmaStageBytes;
+    const int group_bytes = hpc * 2 * D * 2;  // <= 4 KB, so at least 8 pages per stage
+    b.stage_pages = std::min(kMaxStagePages, kMmaStageBytes / (group_bytes + 16)) / 8 * 8;
   }
   // Tail region: about kTailWaves waves of short CTAs over the sequences' last pages. A grid of
   // equal chunks ends with its last wave draining for one whole CTA lifetime at falling
   // occupancy; short CTAs last make that drain short.
-  ScoreArgs b = a;
   {
     int per_sm = 0;
-    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kfn), kThreads, k1_smem, &per_sm);
+    cudaError_t e = kernel_setup(score_kernel_fn<T, D, G>(kind), threads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     const Tuning &tu = tuning();
     b.tail_chunk = tu.score_tail_chunk > 0 ? tu.score_tail_chunk : kTailChunk;
@@ -327,7 +536,15 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   }
   const long long n_ctas = (long long)(b.body_chunks + b.tail_chunks) * b.B * (b.H_kv / hpc);
   if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
-  const cudaError_t e = launch_kernel(true, kfn, (unsigned)n_ctas, kThreads, k1_smem, s, b);
+  cudaError_t e = cudaErrorInvalidValue;
+  if (kind == ScoreKernel::kMma) {
+    if constexpr (sizeof(T) == 2 && G <= 4)
+      e = launch_kernel(true, page_score_mma_kernel<D, G>, (unsigned)n_ctas, threads, smem, s, b);
+  } else if (kind == ScoreKernel::kFmaPerQueryHead) {
+    if constexpr (G == 1) e = launch_kernel(true, page_score_kernel<T, D, G, true>, (unsigned)n_ctas, threads, smem, s, b);
+  } else {
+    e = launch_kernel(true, page_score_kernel<T, D, G, false>, (unsigned)n_ctas, threads, smem, s, b);
+  }
   if (e != cudaSuccess || !(stages & kStageSelect)) return e;
   return launch_page_select(b, s);
 }
