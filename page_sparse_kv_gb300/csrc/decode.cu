@@ -21,6 +21,14 @@
 // pairs. PV: the lane owns D/32 output dims of all G heads and accumulates with packed FMAs
 // from one conflict-free V row chunk per token.
 //
+// bf16 caches compute each tile on the tensor cores instead (warp_tiles over an MmaWarp state):
+// S = q K^T and O += P V as warp-level m16n8k16 MMAs (bf16 in, fp32 accumulate), with the query
+// heads as the M rows. The tiles then arrive as 128-byte TMA boxes stored with the 128-byte
+// swizzle, so ldmatrix reads K (as is) and V (transposed) without bank conflicts. P stays in
+// registers: its fp32 weights are split into a bf16 high part (rows 0..7 of the A fragment)
+// and the bf16 rounding of the remainder (rows 8..15, otherwise unused), so P V carries about
+// 16 bits of each weight, and the two halves of O are added at the end.
+//
 // The NW warp states are merged through shared memory into one partial per CTA (m, l and O
 // relative to m). Every CTA of a (sequence, KV head) then takes a ticket (CTAs without pages
 // write an empty partial first); the CTA holding the last ticket (no waiting) merges the
@@ -55,7 +63,7 @@ struct DT {
   static constexpr int NV = 4 * G;                 // partial logits per lane before reduce
   static constexpr int KEEP = NV >= 8 ? NV / 8 : 1;
   static constexpr size_t STAGES = (size_t)NW * NST * STAGE;
-  static constexpr size_t SMEM = 128                           // alignment slack
+  static constexpr size_t SMEM = 1024                          // alignment slack (swizzled TMA boxes)
                                  + STAGES                      // stages (reused by the merges)
                                  + (size_t)NW * 16 * G * 8     // (p, p) pairs
                                  + (size_t)NW * G * 2 * 4      // warp m, l
@@ -260,6 +268,47 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int i, int h, int dg
     }
 }
 
+// Value tier: this lane's 8-byte slice (dims lane * 4 ..) of the V rows of tile `it` of the
+// entry table, rows at or past the tile's live rows zero. A row comes from the page's resident
+// HBM slot when it has one, else from the host cache over NVLink-C2C. The host rows of tile
+// it + kHostPrefetch * nw are first prefetched into L2 (one 128-byte line per lane, two lanes
+// per row), so their C2C latency overlaps this tile. Built for bf16, D = 128.
+template <typename T, int D>
+__device__ __forceinline__ void host_v_rows(const DecodeArgs &a, int h, int it, int ntiles, int nw, int stp,
+                                            const int *ent_blk, const int *ent_valid, const int *ent_vslot,
+                                            uint2 (&vh)[16]) {
+  static_assert(D / 32 * sizeof(T) == 8, "8 bytes of V per lane and row");
+  const int lane = threadIdx.x & 31;
+  auto rows_of = [&](int x) -> int {
+    const int e = stp == 1 ? x : x / stp, sub = x - e * stp;
+    return min(16, ent_valid[e] - sub * 16);
+  };
+  auto vsrc = [&](int x, size_t *stride) -> const T * {
+    const int e = stp == 1 ? x : x / stp, sub = x - e * stp;
+    const int slot = ent_vslot ? ent_vslot[e] : -1;
+    if (slot >= 0) {
+      *stride = D;
+      return reinterpret_cast<const T *>(a.v_hot) + ((size_t)slot * a.ps + sub * 16) * D;
+    }
+    *stride = (size_t)a.H_kv_cache * D;
+    return reinterpret_cast<const T *>(a.v_cache) +
+           (((size_t)ent_blk[e] * a.ps + sub * 16) * a.H_kv_cache + (h >> a.kv_shift)) * D;
+  };
+  const int pf = it + kHostPrefetch * nw;
+  if (pf < ntiles && rows_of(pf) > 0) {
+    size_t st;
+    const T *pb = vsrc(pf, &st);
+    if ((lane >> 1) < rows_of(pf))
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pb + (size_t)(lane >> 1) * st + (lane & 1) * 64) : "memory");
+  }
+  const int nvh = rows_of(it);
+  size_t st;
+  const T *vb = vsrc(it, &st) + lane * (D / 32);
+#pragma unroll
+  for (int tk = 0; tk < 16; ++tk)  // only rows below seq_len: the rest may hold anything
+    vh[tk] = tk < nvh ? *reinterpret_cast<const uint2 *>(vb + (size_t)tk * st) : make_uint2(0u, 0u);
+}
+
 // Streams the 16-token tiles of the n_ent entries in the entry table through this warp's TMA
 // ring (warp w takes tiles w, w + NW, ...) and folds them into the warp's (m, l, O). cw is the
 // warp's running tile count: ring stage and mbarrier phase carry on across calls. q_seq >= 0:
@@ -321,35 +370,7 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
   for (int cur = warp; cur < ntiles; ++k, cur += NW) {
     issue(k + NST - 1);
     uint2 vh[kHostV ? 16 : 1];  // kHostV: this lane's V slice of the tile's rows
-    if constexpr (kHostV) {
-      // The tile's V rows: from the page's resident HBM slot when it has one, else from the host
-      // cache over NVLink-C2C. A later tile's host rows are first prefetched into L2 (one 128-byte
-      // line per lane, two lanes per row), so their C2C latency overlaps this tile.
-      auto vsrc = [&](int it, size_t *stride) -> const T * {
-        const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
-        const int slot = ent_vslot ? ent_vslot[e] : -1;
-        if (slot >= 0) {
-          *stride = D;
-          return reinterpret_cast<const T *>(a.v_hot) + ((size_t)slot * a.ps + sub * 16) * D;
-        }
-        *stride = (size_t)a.H_kv_cache * D;
-        return reinterpret_cast<const T *>(a.v_cache) +
-               (((size_t)ent_blk[e] * a.ps + sub * 16) * a.H_kv_cache + (h >> a.kv_shift)) * D;
-      };
-      const int pf = cur + kHostPrefetch * NW;
-      if (pf < ntiles && tile_rows(pf) > 0) {
-        size_t st;
-        const T *pb = vsrc(pf, &st);
-        if ((lane >> 1) < tile_rows(pf))
-          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pb + (size_t)(lane >> 1) * st + (lane & 1) * 64) : "memory");
-      }
-      const int nvh = tile_rows(cur);
-      size_t st;
-      const T *vb = vsrc(cur, &st) + lane * TR::VPL;
-#pragma unroll
-      for (int tk = 0; tk < 16; ++tk)  // only rows below seq_len: the rest may hold anything
-        vh[tk] = tk < nvh ? *reinterpret_cast<const uint2 *>(vb + (size_t)tk * st) : make_uint2(0u, 0u);
-    }
+    if constexpr (kHostV) host_v_rows<T, D>(a, h, cur, ntiles, NW, stp, ent_blk, ent_valid, ent_vslot, vh);
     const int stage = (cw0 + k) % NST;
     mbar_wait(smem_u32(&bars[warp][stage]), ((cw0 + k) / NST) & 1, a.ws);
     const int nv = tile_rows(cur);
@@ -472,56 +493,254 @@ __device__ __forceinline__ void warp_tiles(const DecodeArgs &a, const CUtensorMa
   cw = cw0 + k;
 }
 
-// Merges the NW warp states of the CTA into one partial (m, l and O relative to m) at `slot`.
-// wO aliases the stages: the caller has synchronised after the last tile.
-template <typename T, int D, int G, int NW, int NST>
-__device__ __forceinline__ void write_partial(const DecodeArgs &a, size_t slot, float (&m)[G], float (&l)[G],
-                                              float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2], float *wO, float *wML) {
-  using TR = DT<T, D, G, NW, NST>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// ---- tensor-core tiles (bf16) -------------------------------------------------------------------
+// Warp state of warp_tiles_mma. In the m16n8k16 fragments row g = lane / 4 is query head g
+// (rows G .. 7 are zero padding of q) and lane % 4 = t4 picks the columns 2 t4, 2 t4 + 1 of each
+// 8-column block. O rows g hold P_hi V and rows 8 + g hold P_lo V (see warp_tiles_mma).
+template <int D, int G>
+struct MmaWarp {
+  static_assert(G >= 1 && G <= 8, "query heads are the MMA rows 0..7");
+  static constexpr int KS = D / 16;  // k-steps of q K^T
+  static constexpr int NT = D / 8;   // 8-column blocks of O
+  uint32_t qa[KS][2];  // q as the A operand: a0 (columns 2 t4, + 1) and a2 (+ 8) of each k-step
+  float m, l;          // row g: running max of the log2-domain logits, this lane's share of the sum
+  float O[NT][4];      // O[n] = {row g: cols 8n + 2t4, +1; row 8 + g: the same cols}
+  __device__ __forceinline__ void reset() {
+    m = -INFINITY;
+    l = 0.f;
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float x = l[g];
+    for (int n = 0; n < NT; ++n) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
+  }
+  __device__ __forceinline__ void load_q(const DecodeArgs &a, int i, int h) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+    if (g < G) {
+      const uint32_t *qr = reinterpret_cast<const uint32_t *>(reinterpret_cast<const bf16_t *>(a.q) +
+                                                              ((size_t)i * a.H_q + (size_t)h * G + g) * D);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      for (int s = 0; s < KS; ++s) {
+        qa[s][0] = __ldg(qr + 8 * s + t4);
+        qa[s][1] = __ldg(qr + 8 * s + 4 + t4);
+      }
+    } else {
 #pragma unroll
-    for (int e = 0; e < TR::VPL / 2; ++e)
-      reinterpret_cast<float2 *>(wO + (warp * G + g) * D + lane * TR::VPL)[e] = O[g][e];
-    if (lane == 0) {
-      wML[(warp * G + g) * 2] = m[g];
-      wML[(warp * G + g) * 2 + 1] = x;
+      for (int s = 0; s < KS; ++s) qa[s][0] = qa[s][1] = 0u;
     }
   }
-  __syncthreads();
-  for (int idx = tid; idx < G * D; idx += NW * 32) {
-    const int g = idx / D, d = idx - g * D;
-    float M = -INFINITY;
+  // (m, l, O) of the warp into the CTA merge's shared arrays (see cta_partial).
+  __device__ __forceinline__ void stash(float *wO, float *wML) const {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
+    float lt = l + __shfl_xor_sync(0xffffffffu, l, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    if (g < G) {
+      float *o = wO + (size_t)(warp * G + g) * D + 2 * t4;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, wML[(w * G + g) * 2]);
-    float acc = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float sc = exp2f(wML[(w * G + g) * 2] - M);
-        acc = fmaf(sc, wO[(w * G + g) * D + d], acc);
-        L = fmaf(sc, wML[(w * G + g) * 2 + 1], L);
+      for (int n = 0; n < NT; ++n)
+        *reinterpret_cast<float2 *>(o + 8 * n) = make_float2(O[n][0] + O[n][2], O[n][1] + O[n][3]);
+      if (t4 == 0) {
+        wML[(warp * G + g) * 2] = m;
+        wML[(warp * G + g) * 2 + 1] = lt;
       }
     }
-    a.part_o[(slot * G + g) * D + d] = acc;
+  }
+};
+
+// warp_tiles on the tensor cores (bf16): the same tile walk and TMA ring, with each K and V tile
+// fetched as D / 64 boxes of 64 elements x 16 rows (128-byte swizzle: chunk c of row t at
+// ((c ^ (t % 8)) * 16) inside its 128-byte row). Per 16-token tile:
+//   S[g][t]  = sum_d q[g][d] K[t][d]: D/16 k-steps, each one ldmatrix (K rows as the column-major
+//              B operand of two 8-token blocks) and two MMAs;
+//   online softmax on the lane's four logits (tokens 2 t4, 2 t4 + 1, 8 + 2 t4, 9 + 2 t4), row max
+//              by two shuffles, rescale only when some row's max moved;
+//   P = exp2(x - m): A rows g = bf16(P), rows 8 + g = bf16(P - bf16(P)) (exact residual);
+//   O += P V:  D/16 transposed ldmatrix of V and D/8 MMAs.
+// V rows past the live tokens are zeroed first (P is 0 there, but 0 * NaN is NaN); K rows there
+// only reach their own logits, which are masked to -inf.
+// kHostV: V rows from the value tier (host_v_rows) into registers, then into the tile's V stage
+// in the same swizzled layout, so the arithmetic is the same as with V in HBM.
+template <int D, int G, int NW, int NST, bool kHostV = false>
+__device__ __forceinline__ void warp_tiles_mma(const DecodeArgs &a, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                               int h, int q_seq, MmaWarp<D, G> &w, const int *ent_blk,
+                                               const int *ent_valid, int n_ent, unsigned char *stages,
+                                               uint64_t (*bars)[NST], int &cw, const int *ent_vslot = nullptr) {
+  using TR = DT<bf16_t, D, G, NW, NST>;
+  static_assert(TR::ROW % 128 == 0 && TR::TILE % 1024 == 0, "rows of whole 128-byte boxes");
+  constexpr int NB = TR::ROW / 128;  // boxes per row
+  constexpr int BOX = 16 * 128;      // bytes of one box (16 rows)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int stp = a.ps / 16;  // tiles per page
+  const int ntiles = n_ent * stp;
+  unsigned char *my_stages = stages + (size_t)warp * NST * TR::STAGE;
+  const int cw0 = cw;
+  auto issue = [&](int k) {
+    const int it = warp + k * NW;
+    if (it >= ntiles) return;
+    if (lane == 0) {
+      const int stg = (cw0 + k) % NST;
+      const uint32_t bar = smem_u32(&bars[warp][stg]);
+      const int e = stp == 1 ? it : it / stp, sub = it - e * stp;
+      const int nv = min(16, ent_valid[e] - sub * 16);
+      if (nv > 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, (kHostV ? 1u : 2u) * TR::TILE);
+        const uint32_t sK = smem_u32(my_stages + (size_t)stg * TR::STAGE);
+        const int row = ent_blk[e] * a.ps + sub * 16;
+        const uint64_t pol = l2_evict_first_policy();  // K/V rows are read once per step
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {  // x = 64 b elements: 128-byte aligned
+          tma_load_3d_stream(sK + b * BOX, tmK, b * 64, h >> a.kv_shift, row, bar, pol);
+          if (!kHostV) tma_load_3d_stream(sK + TR::TILE + b * BOX, tmV, b * 64, h >> a.kv_shift, row, bar, pol);
+        }
+      } else {
+        mbar_arrive_expect_tx(bar, 0u);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int k = 0; k < NST - 1; ++k) issue(k);
+  if (q_seq >= 0) w.load_q(a, q_seq, h);
+  const float qs = a.scale * kLog2e;
+  const int t4 = lane & 3, r8 = lane & 7, mi = lane >> 3;
+  // ldmatrix row of this lane: K matrix mi = (token block mi / 2, chunk 2s + mi % 2); V matrix
+  // mi = (token block mi % 2, chunk 2n + mi / 2); the row is the token, so (row % 8) = r8
+  const uint32_t k_row = (uint32_t)(((mi >> 1) * 8 + r8) * 128);
+  const int k_ch = mi & 1;
+  const uint32_t v_row = (uint32_t)(((mi & 1) * 8 + r8) * 128);
+  const int v_ch = mi >> 1;
+  int k = 0;
+  for (int cur = warp; cur < ntiles; ++k, cur += NW) {
+    issue(k + NST - 1);
+    uint2 vh[kHostV ? 16 : 1];
+    if constexpr (kHostV) host_v_rows<bf16_t, D>(a, h, cur, ntiles, NW, stp, ent_blk, ent_valid, ent_vslot, vh);
+    const int stage = (cw0 + k) % NST;
+    mbar_wait(smem_u32(&bars[warp][stage]), ((cw0 + k) / NST) & 1, a.ws);
+    const int e = stp == 1 ? cur : cur / stp, sub = cur - e * stp;
+    const int nv = min(16, ent_valid[e] - sub * 16);
+    if (nv > 0) {
+      unsigned char *sV = my_stages + (size_t)stage * TR::STAGE + TR::TILE;
+      if constexpr (kHostV) {
+        // lane's 8 bytes of row t: chunk lane / 2 of the row, half lane % 2 (rows past nv are zero)
+        const int ch = lane >> 1;
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          *reinterpret_cast<uint2 *>(sV + (ch >> 3) * BOX + t * 128 + (((ch & 7) ^ (t & 7)) << 4) + (lane & 1) * 8) =
+              vh[t];
+      }
+      const uint32_t aK = smem_u32(my_stages + (size_t)stage * TR::STAGE), aV = smem_u32(sV);
+      // ---- S = q K^T ----
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < MmaWarp<D, G>::KS; ++s) {
+        const int ch = 2 * s + k_ch;
+        uint32_t kb[4];
+        ldsm_x4(aK + (ch >> 3) * BOX + k_row + (((ch & 7) ^ r8) << 4), kb);
+        const uint32_t qa4[4] = {w.qa[s][0], 0u, w.qa[s][1], 0u};
+        mma_16816_bf16(s0, qa4, kb[0], kb[1]);
+        mma_16816_bf16(s1, qa4, kb[2], kb[3]);
+      }
+      // ---- online softmax, row g ----
+      const int tb = 2 * t4;
+      float x[4] = {s0[0] * qs, s0[1] * qs, s1[0] * qs, s1[1] * qs};
+      if (tb >= nv) x[0] = -INFINITY;
+      if (tb + 1 >= nv) x[1] = -INFINITY;
+      if (tb + 8 >= nv) x[2] = -INFINITY;
+      if (tb + 9 >= nv) x[3] = -INFINITY;
+      float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float mnew = fmaxf(w.m, tmax);  // finite: token 0 of a tile is always live
+      if (__any_sync(0xffffffffu, mnew != w.m)) {
+        const float al = exp2f(w.m - mnew);  // 0 when m was -inf, 1 when it did not move
+        w.m = mnew;
+        w.l *= al;
+#pragma unroll
+        for (int n = 0; n < MmaWarp<D, G>::NT; ++n)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) w.O[n][j] *= al;
+      }
+      float p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p[j] = exp2f(x[j] - w.m);
+      w.l += (p[0] + p[1]) + (p[2] + p[3]);
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(p[0], p[1]);
+      pa[2] = pack_bf16x2(p[2], p[3]);
+      pa[1] = pack_bf16x2(p[0] - bf16_lo(pa[0]), p[1] - bf16_hi(pa[0]));
+      pa[3] = pack_bf16x2(p[2] - bf16_lo(pa[2]), p[3] - bf16_hi(pa[2]));
+      // ---- O += P V ----
+      if (!kHostV && nv < 16) {  // whole rows, so the swizzle does not matter
+        for (int z = lane; z < (16 - nv) * (D / 8); z += 32) {
+          const int t = nv + z / (D / 8), ch = z % (D / 8);
+          *reinterpret_cast<uint4 *>(sV + (ch >> 3) * BOX + t * 128 + (ch & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      __syncwarp();  // V rows written by the warp (zeros, or the value tier's rows) before ldmatrix
+#pragma unroll
+      for (int n2 = 0; n2 < D / 16; ++n2) {
+        const int ch = 2 * n2 + v_ch;
+        uint32_t vb[4];
+        ldsm_x4_trans(aV + (ch >> 3) * BOX + v_row + (((ch & 7) ^ r8) << 4), vb);
+        mma_16816_bf16(w.O[2 * n2], pa, vb[0], vb[1]);
+        mma_16816_bf16(w.O[2 * n2 + 1], pa, vb[2], vb[3]);
+      }
+    }
+    __syncwarp();
+  }
+  cw = cw0 + k;
+}
+
+// The CTA merge of its warps' states, stashed in shared memory by the warps (per warp w and head
+// g: O row wO[(w G + g) D ..] relative to m, and (m, l) at wML[(w G + g) 2]); the caller has
+// synchronised after the stash. cta_partial writes one partial (m, l and O relative to m) at
+// `slot`; cta_output writes the G output rows normalised by l (a unit one CTA covers entirely).
+template <int D, int G, int NW>
+__device__ __forceinline__ float cta_merge_elem(const float *wO, const float *wML, int g, int d, float *M_out,
+                                                float *L_out) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, wML[(w * G + g) * 2]);
+  float acc = 0.f, L = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float sc = exp2f(wML[(w * G + g) * 2] - M);
+      acc = fmaf(sc, wO[(w * G + g) * D + d], acc);
+      L = fmaf(sc, wML[(w * G + g) * 2 + 1], L);
+    }
+  }
+  *M_out = M;
+  *L_out = L;
+  return acc;
+}
+template <int D, int G, int NW>
+__device__ __forceinline__ void cta_partial(const DecodeArgs &a, size_t slot, const float *wO, const float *wML) {
+  for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M, L;
+    a.part_o[(slot * G + g) * D + d] = cta_merge_elem<D, G, NW>(wO, wML, g, d, &M, &L);
     if (d == 0) {
       a.part_ml[(slot * G + g) * 2] = M;
       a.part_ml[(slot * G + g) * 2 + 1] = L;
     }
   }
 }
+template <typename T, int D, int G, int NW>
+__device__ __forceinline__ void cta_output(const DecodeArgs &a, int unit, const float *wO, const float *wML) {
+  T *out = reinterpret_cast<T *>(a.out) + ((size_t)(unit / a.H_kv) * a.H_q + (size_t)(unit % a.H_kv) * G) * D;
+  for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M, L;
+    const float acc = cta_merge_elem<D, G, NW>(wO, wML, g, d, &M, &L);
+    Elem<T>::store(out + idx, L > 0.f ? acc / L : 0.f);
+  }
+}
 
-// The same merge of the warps written straight to the G output rows (normalised by l): for a
-// unit that one CTA covers entirely.
+// The FMA warp state (O over dims lane * VPL .., l a per-lane share) into the merge's arrays.
 template <typename T, int D, int G, int NW, int NST>
-__device__ __forceinline__ void write_output(const DecodeArgs &a, int unit, float (&m)[G], float (&l)[G],
-                                             float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2], float *wO, float *wML) {
+__device__ __forceinline__ void stash_fma(float (&m)[G], float (&l)[G], float2 (&O)[G][DT<T, D, G, NW, NST>::VPL / 2],
+                                          float *wO, float *wML) {
   using TR = DT<T, D, G, NW, NST>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float x = l[g];
@@ -534,24 +753,6 @@ __device__ __forceinline__ void write_output(const DecodeArgs &a, int unit, floa
       wML[(warp * G + g) * 2] = m[g];
       wML[(warp * G + g) * 2 + 1] = x;
     }
-  }
-  __syncthreads();
-  T *out = reinterpret_cast<T *>(a.out) + ((size_t)(unit / a.H_kv) * a.H_q + (size_t)(unit % a.H_kv) * G) * D;
-  for (int idx = tid; idx < G * D; idx += NW * 32) {
-    const int g = idx / D, d = idx - g * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, wML[(w * G + g) * 2]);
-    float acc = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float sc = exp2f(wML[(w * G + g) * 2] - M);
-        acc = fmaf(sc, wO[(w * G + g) * D + d], acc);
-        L = fmaf(sc, wML[(w * G + g) * 2 + 1], L);
-      }
-    }
-    Elem<T>::store(out + idx, L > 0.f ? acc / L : 0.f);
   }
 }
 
@@ -564,7 +765,7 @@ struct DecodeSmem {
   int *ent_blk, *ent_valid, *ent_vslot;
   int *extra;  // flat layout: the unit prefix sums
   __device__ explicit DecodeSmem(unsigned char *raw) {
-    stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127));
+    stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     pp_all = reinterpret_cast<float2 *>(stages + TR::STAGES);
     wML = reinterpret_cast<float *>(pp_all + NW * 16 * G);
     ent_blk = reinterpret_cast<int *>(wML + NW * G * 2);
@@ -575,9 +776,11 @@ struct DecodeSmem {
 };
 
 // ---- split layout: one CTA per (split of `sw` list entries, KV head, sequence) ----------------
-template <typename T, int D, int G, int NW, int NST, bool kHostV>
+// kMma: the tensor-core tiles (bf16, V in HBM; the tensor maps are the swizzled 128-byte boxes).
+template <typename T, int D, int G, int NW, int NST, bool kHostV, bool kMma = false>
 __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                                const __grid_constant__ CUtensorMap tmV) {
+  static_assert(!kMma || sizeof(T) == 2, "tensor-core tiles: bf16");
   pdl_wait();  // dependents are released when this grid completes
   using TR = DT<T, D, G, NW, NST>;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
@@ -625,25 +828,37 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(DecodeArgs a, con
   if (alone && s > 0) return;
 
   if (n_ent > 0) {
-    float2 q2[G][TR::CPL * TR::EPC / 2];  // loaded by warp_tiles, behind the first tile copies
-    float m[G], l[G];
-    float2 O[G][TR::VPL / 2];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
-#pragma unroll
-      for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = make_float2(0.f, 0.f);
-    }
+    float *wO = reinterpret_cast<float *>(sm.stages);  // the merge reuses the stages
     int cw = 0;
-    warp_tiles<T, D, G, NW, NST, kHostV>(a, &tmK, &tmV, h, i, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages,
-                                         sm.pp_all, bars, cw, m, l, O, kHostV ? sm.ent_vslot : nullptr);
-    __syncthreads();  // every warp is done with the stages; the merge below reuses them
+    if constexpr (kMma) {
+      MmaWarp<D, G> w;
+      w.reset();
+      warp_tiles_mma<D, G, NW, NST, kHostV>(a, &tmK, &tmV, h, i, w, sm.ent_blk, sm.ent_valid, n_ent, sm.stages, bars,
+                                            cw, kHostV ? sm.ent_vslot : nullptr);
+      __syncthreads();  // every warp is done with the stages
+      w.stash(wO, sm.wML);
+    } else {
+      float2 q2[G][TR::CPL * TR::EPC / 2];  // loaded by warp_tiles, behind the first tile copies
+      float m[G], l[G];
+      float2 O[G][TR::VPL / 2];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < TR::VPL / 2; ++e) O[g][e] = make_float2(0.f, 0.f);
+      }
+      warp_tiles<T, D, G, NW, NST, kHostV>(a, &tmK, &tmV, h, i, q2, sm.ent_blk, sm.ent_valid, n_ent, sm.stages,
+                                           sm.pp_all, bars, cw, m, l, O, kHostV ? sm.ent_vslot : nullptr);
+      __syncthreads();  // every warp is done with the stages
+      stash_fma<T, D, G, NW, NST>(m, l, O, wO, sm.wML);
+    }
+    __syncthreads();
     if (alone) {
-      write_output<T, D, G, NW, NST>(a, unit, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
+      cta_output<T, D, G, NW>(a, unit, wO, sm.wML);
       return;
     }
-    write_partial<T, D, G, NW, NST>(a, pbase, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
+    cta_partial<D, G, NW>(a, pbase, wO, sm.wML);
   } else if (alone) {  // nothing to read and nothing to merge: zero rows
     T *out = reinterpret_cast<T *>(a.out) + ((size_t)i * a.H_q + (size_t)h * G) * D;
     for (int idx = tid; idx < G * D; idx += NW * 32) Elem<T>::store(out + idx, 0.f);
@@ -696,9 +911,10 @@ __global__ void decode_counts_kernel(DecodeArgs a) {
 // slot c + u (unique: shares are ordered like the units), and the last CTA of a unit to finish
 // (ticket, no waiting) merges the unit's partials. Units without entries get zero rows from CTA
 // u % C. Balancing by entries removes the tail that budget-sized splits leave when budgets differ.
-template <typename T, int D, int G, int NW, int NST>
+template <typename T, int D, int G, int NW, int NST, bool kMma = false>
 __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                                                               const __grid_constant__ CUtensorMap tmV) {
+  static_assert(!kMma || sizeof(T) == 2, "tensor-core tiles: bf16");
   pdl_wait();  // dependents are released when this grid completes
   using TR = DT<T, D, G, NW, NST>;
   constexpr int NT = NW * 32;
@@ -787,27 +1003,45 @@ __global__ void __launch_bounds__(NW * 32) decode_flat_kernel(DecodeArgs a, cons
     const int i = u / a.H_kv, h = u % a.H_kv;
     const int seq_len = a.seq_lens[i];
     const int P = (seq_len + a.ps - 1) / a.ps;
-    float2 q2[G][TR::CPL * TR::EPC / 2];
-    load_q<T, D, G, NW, NST>(a, i, h, lane & 7, q2);
-    float m[G], l[G];
-    float2 O[G][TR::VPL / 2];
+    float *wO = reinterpret_cast<float *>(sm.stages);  // the merge reuses the stages
+    if constexpr (kMma) {
+      MmaWarp<D, G> w;
+      w.reset();
+      w.load_q(a, i, h);
+      for (long long x0 = e; x0 < seg_end; x0 += kSwMax) {
+        const int n = (int)min((long long)kSwMax, seg_end - x0);
+        __syncthreads();  // the previous entry table and stages are no longer in use
+        load_entries<NT>(a, i, u, P, seq_len, (int)(x0 - start[u]), n, sm.ent_blk, sm.ent_valid);
+        __syncthreads();
+        warp_tiles_mma<D, G, NW, NST>(a, &tmK, &tmV, h, -1, w, sm.ent_blk, sm.ent_valid, n, sm.stages, bars, cw);
+      }
+      __syncthreads();  // every warp is done with the stages
+      w.stash(wO, sm.wML);
+    } else {
+      float2 q2[G][TR::CPL * TR::EPC / 2];
+      load_q<T, D, G, NW, NST>(a, i, h, lane & 7, q2);
+      float m[G], l[G];
+      float2 O[G][TR::VPL / 2];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
+      for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
 #pragma unroll
-      for (int x = 0; x < TR::VPL / 2; ++x) O[g][x] = make_float2(0.f, 0.f);
+        for (int x = 0; x < TR::VPL / 2; ++x) O[g][x] = make_float2(0.f, 0.f);
+      }
+      for (long long x0 = e; x0 < seg_end; x0 += kSwMax) {
+        const int n = (int)min((long long)kSwMax, seg_end - x0);
+        __syncthreads();  // the previous entry table and stages are no longer in use
+        load_entries<NT>(a, i, u, P, seq_len, (int)(x0 - start[u]), n, sm.ent_blk, sm.ent_valid);
+        __syncthreads();
+        warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, -1, q2, sm.ent_blk, sm.ent_valid, n, sm.stages, sm.pp_all, bars,
+                                     cw, m, l, O);
+      }
+      __syncthreads();  // every warp is done with the stages
+      stash_fma<T, D, G, NW, NST>(m, l, O, wO, sm.wML);
     }
-    for (long long x0 = e; x0 < seg_end; x0 += kSwMax) {
-      const int n = (int)min((long long)kSwMax, seg_end - x0);
-      __syncthreads();  // the previous entry table and stages are no longer in use
-      load_entries<NT>(a, i, u, P, seq_len, (int)(x0 - start[u]), n, sm.ent_blk, sm.ent_valid);
-      __syncthreads();
-      warp_tiles<T, D, G, NW, NST>(a, &tmK, &tmV, h, -1, q2, sm.ent_blk, sm.ent_valid, n, sm.stages, sm.pp_all, bars, cw, m,
-                                   l, O);
-    }
-    __syncthreads();  // every warp is done with the stages; the merges below reuse them
-    write_partial<T, D, G, NW, NST>(a, (size_t)c + u, m, l, O, reinterpret_cast<float *>(sm.stages), sm.wML);
+    __syncthreads();
+    cta_partial<D, G, NW>(a, (size_t)c + u, wO, sm.wML);
     const int c_first = cta_of(start[u]), c_last = cta_of((long long)start[u + 1] - 1);
     const int nseg = c_last - c_first + 1;
     __threadfence();
@@ -862,17 +1096,23 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   using TR = DT<T, D, G, NW, NST>;
   static_assert(TR::STAGES >= (size_t)kMaxItems * G * 4, "stage memory must hold the merge weights");
   static_assert(TR::STAGES >= (size_t)kFlatMaxCtas * G * 4, "stage memory must hold the merge weights");
+  // bf16: the tensor-core tiles (unless PSK_DECODE_MMA=0)
+  constexpr bool kMmaOk = sizeof(T) == 2 && D % 64 == 0;
+  const bool mma = kMmaOk && tuning().decode_mma;
   CUtensorMap tmK, tmV;
   const long long rows = (long long)a.nb * a.ps;
   const int dt = sizeof(T) == 4 ? PSK_F32 : PSK_BF16;
   // host values: no tensor map over host memory (V is read with plain loads); tmV repeats tmK
-  if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv_cache, rows, 16) ||
-      !encode_cache_map(&tmV, a.v_host ? a.k_cache : a.v_cache, dt, D, a.H_kv_cache, rows, 16))
+  if (!encode_cache_map(&tmK, a.k_cache, dt, D, a.H_kv_cache, rows, 16, mma) ||
+      !encode_cache_map(&tmV, a.v_host ? a.k_cache : a.v_cache, dt, D, a.H_kv_cache, rows, 16, mma))
     return cudaErrorInvalidValue;
   if (a.v_host) {  // the value tier: sparse split layout only
     if constexpr (sizeof(T) == 2 && D == 128) {
       if (a.flat || !a.selected) return cudaErrorInvalidValue;
       dim3 grid(a.B * a.H_kv, a.n_items_max);
+      if (mma)
+        return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, true, true>, grid, NW * 32, TR::SMEM, s, a, tmK,
+                             tmV);
       return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, true>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
     } else {
       return cudaErrorInvalidValue;
@@ -880,6 +1120,10 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   }
   if (!a.flat) {
     dim3 grid(a.B * a.H_kv, a.n_items_max);
+    if constexpr (kMmaOk)
+      if (mma)
+        return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, false, true>, grid, NW * 32, TR::SMEM, s, a,
+                             tmK, tmV);
     return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, false>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
   }
   const int U = a.B * a.H_kv;
@@ -888,12 +1132,17 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     e = launch_kernel(true, decode_counts_kernel, (U + 7) / 8, 256, 0, s, a);
     if (e != cudaSuccess) return e;
   }
-  auto kfn = decode_flat_kernel<T, D, G, NW, NST>;
   const size_t smem = TR::SMEM + (size_t)(U + 1) * 4;
-  int per_sm = 0;
-  if ((e = kernel_setup(reinterpret_cast<const void *>(kfn), NW * 32, smem, &per_sm)) != cudaSuccess) return e;
-  const int ctas = std::max(1, std::min(kFlatMaxCtas, sm_count() * std::max(1, per_sm)));
-  return launch_kernel(!a.selected, kfn, ctas, NW * 32, smem, s, a, tmK, tmV);
+  auto flat_launch = [&](auto kfn) -> cudaError_t {
+    int per_sm = 0;
+    cudaError_t e2 = kernel_setup(reinterpret_cast<const void *>(kfn), NW * 32, smem, &per_sm);
+    if (e2 != cudaSuccess) return e2;
+    const int ctas = std::max(1, std::min(kFlatMaxCtas, sm_count() * std::max(1, per_sm)));
+    return launch_kernel(!a.selected, kfn, ctas, NW * 32, smem, s, a, tmK, tmV);
+  };
+  if constexpr (kMmaOk)
+    if (mma) return flat_launch(decode_flat_kernel<T, D, G, NW, NST, true>);
+  return flat_launch(decode_flat_kernel<T, D, G, NW, NST>);
 }
 }  // namespace
 

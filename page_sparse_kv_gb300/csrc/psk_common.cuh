@@ -57,12 +57,14 @@ void kernel_forget(const void *fn);
 
 // Tuning overrides from the environment, read once per process: PSK_SCORE_TAIL (pages),
 // PSK_SCORE_TAIL_CHUNK, PSK_SCORE_PCHUNK, PSK_SCORE_MMA (0: bf16 page scores on the FMA pipe
-// instead of the tensor cores), PSK_DECODE_LAYOUT ("split" / "flat"), PSK_DECODE_SPLIT (list
-// entries per CTA), PSK_DECODE_NO_TAPER. -1 / 0 = not set.
+// instead of the tensor cores), PSK_DECODE_MMA (0: bf16 decode tiles on the FMA pipe),
+// PSK_DECODE_LAYOUT ("split" / "flat"), PSK_DECODE_SPLIT (list entries per CTA),
+// PSK_DECODE_NO_TAPER. -1 / 0 = not set.
 struct Tuning {
   long long score_tail = -1;
   int score_tail_chunk = -1, score_pchunk = -1;
   bool score_mma = true;
+  bool decode_mma = true;
   int decode_layout = 0;  // 0 default, 1 split, 2 flat
   int decode_split = -1;
   bool decode_no_taper = false;
@@ -277,8 +279,10 @@ __device__ __forceinline__ void tma_load_3d_stream(uint32_t dst, const CUtensorM
 }
 
 // Host: encode a 3-D tiled tensor map over a paged cache [rows, H, D] (elements of `dtype`) with
-// a box of `box_rows` rows x 1 head x D elements. Returns false on failure.
-bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int D, int H, long long rows, int box_rows);
+// a box of `box_rows` rows x 1 head x D elements, or, with sw128, x 128 bytes of elements stored
+// with the 128-byte swizzle (a row then takes D * size / 128 boxes). Returns false on failure.
+bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int D, int H, long long rows, int box_rows,
+                      bool sw128 = false);
 // Host: 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {box_cols, box_rows}
 // box and the 128-byte swizzle (box_cols * 2 must be 128).
 bool encode_matrix_map_sw128(CUtensorMap *map, const void *base, long long cols, long long rows, int box_cols,
@@ -299,5 +303,38 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------------------------
+// warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) and its operand loads
+// ------------------------------------------------------------------------------------
+// Four 8x8 b16 matrices from shared memory: lanes 8j .. 8j + 7 give the 16-byte row addresses of
+// matrix j, which lands in r[j] (row lane / 4, elements 2 (lane % 4) and + 1).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// The same, transposed: r[j] holds rows 2 (lane % 4) and + 1 of column lane / 4 of matrix j.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// c += A (16 x 16, row-major fragment) * B (16 x 8, column-major fragment), fp32 accumulate.
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two fp32 values rounded to bf16 (nearest even) in one word: lo in bits 0..15, hi in 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 }  // namespace psk

@@ -113,6 +113,7 @@ const Tuning &tuning() {
       if (x >= 8 && x <= 4096) r.score_pchunk = x;
     }
     if (const char *v = std::getenv("PSK_SCORE_MMA")) r.score_mma = std::atoi(v) != 0;
+    if (const char *v = std::getenv("PSK_DECODE_MMA")) r.decode_mma = std::atoi(v) != 0;
     if (const char *v = std::getenv("PSK_DECODE_LAYOUT")) r.decode_layout = !std::strcmp(v, "split") ? 1 : (!std::strcmp(v, "flat") ? 2 : 0);
     if (const char *v = std::getenv("PSK_DECODE_SPLIT")) r.decode_split = std::atoi(v);
     r.decode_no_taper = std::getenv("PSK_DECODE_NO_TAPER") != nullptr;

@@ -318,21 +318,6 @@ constexpr int kMmaWarps = kMmaThreads / 32;
 constexpr int kMmaStages = 2;
 constexpr int kMmaStageBytes = 32768 + 512;  // 8 pages x (4 KB + 16) at H = 8, D = 128; 32 x (1 KB + 16)
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-// c += A (16 x 16, row-major fragment) * B (16 x 8, column-major fragment), fp32 accumulate
-__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 template <int D, int G>
 __global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a) {
   pdl_wait();
