@@ -57,19 +57,20 @@ def peaks():
 # call, with a digest of the sources the kernels are built from: a digest that no longer matches
 # means the kernels changed since the capture, and the traffic is reported as null.
 TRAFFIC = {
-    # One-pass capture on the first 16 sequences (profiles/page_score_kernel_batched_ragged_b16.md):
+    # One-pass capture on the first 16 sequences (profiles/page_score_mma_kernel_batched_ragged_b16.md):
     #   python bench.py --batch 16 --steps 3 --warmup 3 --no-cpu-baseline, then
     #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #       -k regex:"page_score|page_select|decode_split" -s 0 -c 3 python bench.py --batch 16 --steps 3 ...
-    # 158,050,560 + 3,093,760 B for 38,540 pages; scaled by pages to the 140,808 of the full workload.
-    ("batched-ragged-b64-8k..64k-5pct", "page_score_kernel"):
-        {"bytes": 588_795_911, "digest": "7990f3db0cb68871", "scaled_from": "first 16 sequences, by pages"},
-    # 129,216,768 + 801,024 B for 15,472 selected (page, head) pairs; 56,536 in the full workload
+    # 158,040,576 + 2,814,208 B for 38,540 pages; scaled by pages to the 140,808 of the full workload.
+    ("batched-ragged-b64-8k..64k-5pct", "page_score_mma_kernel"):
+        {"bytes": 587_691_759, "digest": "1ade29d774e61416", "scaled_from": "first 16 sequences, by pages"},
+    # 129,189,632 + 617,728 B for 15,472 selected (page, head) pairs; 56,536 in the full workload
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 475_096_037, "digest": "38b706d4703ec790", "scaled_from": "first 16 sequences, by selected pages"},
+        {"bytes": 474_327_100, "digest": "2bc4a559648e038a", "scaled_from": "first 16 sequences, by selected pages"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
+    "page_score_mma_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
     "page_select_kernel": ("select.cu", "select_common.cuh", "psk_common.cuh", "psk_internal.h"),
     "decode_split_kernel": ("decode.cu", "psk_common.cuh", "psk_internal.h"),
     "mla_qsplit_kernel+mla_score_kernel": ("mla.cu", "psk_common.cuh", "psk_internal.h"),
@@ -590,7 +591,9 @@ def run_psk(args):
     flops_decode = 2 * Hq * (D + w.D_v) * sel_tokens  # QK^T and P.V over the selected tokens
     # the dominant kernel by time (score, select or decode), each timed by its own events
     if t_score >= t_dec and t_score >= t_select:
-        dom = "mla_qsplit_kernel+mla_score_kernel" if w.latent else "page_score_kernel"
+        # bf16 GQA caches score on the tensor cores (page_score_mma_kernel), fp32 caches on the FMA pipe
+        dom = ("mla_qsplit_kernel+mla_score_kernel" if w.latent else
+               "page_score_mma_kernel" if w.dtype == "bf16" else "page_score_kernel")
         roof = {"bound": "hbm", "kernel": dom, "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
                 "unit": "GB/s", "algorithmic_per_launch": score_bytes, "algorithmic_unit": "B",
                 "launch_us": t_score * 1e3}
