@@ -753,6 +753,41 @@ def test_launch_modes_without_and_with_in_call_pdl(mode):
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
 
 
+_FMA_CHILD = r"""
+import sys
+sys.path.insert(0, sys.argv[1])
+import test_gpu_parity as T
+import workloads as W
+from workloads.device import upload
+cases = [W.reduced(3),
+         T._custom([16 * 45 + 8, 300, 17], [6, 4, 2], H_q=16, H_kv=8),           # G = 2
+         T._custom([16 * 50 + 3, 16 * 9], [7, 3], H_q=8, H_kv=8),                # G = 1
+         T._custom([16 * 61 + 2, 250], [8, 4], D=64, H_q=8, H_kv=4),             # D = 64
+         T._custom([16 * 70 + 3, 500], [9, 4], D=64, H_q=4, H_kv=1),             # one KV head
+         T._custom([64 * 9 + 1, 64 * 30], [4, 7], ps=64)]                        # four tiles per page
+for w in cases:
+    cache = upload(w)
+    seqs = list(range(w.B))
+    summ = T._check_cache_and_summaries(w, cache, seqs)
+    T._run_and_check(w, cache, seqs, summ, w.queries(), step_tag="fma " + w.name)
+print("ok")
+"""
+
+
+def test_fma_forms_of_the_bf16_score_and_decode():
+    """bf16 caches score and decode on the tensor cores by default; PSK_SCORE_MMA=0 and
+    PSK_DECODE_MMA=0 select the FMA forms of both, which must meet the same oracle checks
+    (scores within the fp32 bound, selected ids, sparse and dense outputs). The settings are read
+    once per process, so the FMA forms run in a child process."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PSK_SCORE_MMA="0", PSK_DECODE_MMA="0",
+               PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+    r = subprocess.run([sys.executable, "-c", _FMA_CHILD, root], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
 @pytest.mark.parametrize("latent", [False, True])
 def test_decode_writes_into_pinned_host_output(latent):
     """The decode's output buffer may be pinned host memory (written over NVLink-C2C by the
