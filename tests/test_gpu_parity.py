@@ -180,6 +180,8 @@ def _custom(seq_lens, budgets, ps=16, dtype="bf16", H_q=8, H_kv=2, D=128, n_hot=
     dict(seq_lens=[16 * 61 + 2, 250], budgets=[8, 4], D=64, H_q=8, H_kv=4),    # G = 2, D = 64
     dict(seq_lens=[16 * 20 + 9, 77], budgets=[6, 3], dtype="f32", D=64, H_q=2, H_kv=2),   # fp32, G = 1
     dict(seq_lens=[16 * 27 + 4, 40], budgets=[5, 3], dtype="f32", H_q=1, H_kv=1),        # fp32, D = 128, G = 1
+    dict(seq_lens=[16 * 40 + 7, 16 * 11], budgets=[6, 3], H_q=32, H_kv=16),    # two head groups, G = 2
+    dict(seq_lens=[16 * 33 + 9, 300], budgets=[5, 4], H_q=64, H_kv=16),        # two head groups, G = 4
 ])
 def test_edge_cases(case):
     w = _custom(**case)
