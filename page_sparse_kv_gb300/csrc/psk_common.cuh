@@ -56,13 +56,15 @@ cudaError_t kernel_setup(const void *fn, int threads, size_t smem, int *per_sm =
 void kernel_forget(const void *fn);
 
 // Tuning overrides from the environment, read once per process: PSK_SCORE_TAIL (pages),
-// PSK_SCORE_TAIL_CHUNK, PSK_SCORE_PCHUNK, PSK_SCORE_MMA (0: bf16 page scores on the FMA pipe
+// PSK_SCORE_TAIL_CHUNK, PSK_SCORE_PCHUNK, PSK_SELECT_CHUNK (pages per selection CTA: 1024, 2048,
+// 4096, 8192 or 16384; raised while the chunks' candidates exceed the merge), PSK_SCORE_MMA (0: bf16 page scores on the FMA pipe
 // instead of the tensor cores), PSK_DECODE_MMA (0: bf16 decode tiles on the FMA pipe),
 // PSK_DECODE_LAYOUT ("split" / "flat"), PSK_DECODE_SPLIT (list entries per CTA),
 // PSK_DECODE_NO_TAPER. -1 / 0 = not set.
 struct Tuning {
   long long score_tail = -1;
   int score_tail_chunk = -1, score_pchunk = -1;
+  int select_chunk = -1;
   bool score_mma = true;
   bool decode_mma = true;
   int decode_layout = 0;  // 0 default, 1 split, 2 flat

@@ -112,6 +112,10 @@ const Tuning &tuning() {
       const int x = std::atoi(v);
       if (x >= 8 && x <= 4096) r.score_pchunk = x;
     }
+    if (const char *v = std::getenv("PSK_SELECT_CHUNK")) {
+      const int x = std::atoi(v);
+      if (x >= 1024 && x <= 16384 && (x & (x - 1)) == 0) r.select_chunk = x;
+    }
     if (const char *v = std::getenv("PSK_SCORE_MMA")) r.score_mma = std::atoi(v) != 0;
     if (const char *v = std::getenv("PSK_DECODE_MMA")) r.decode_mma = std::atoi(v) != 0;
     if (const char *v = std::getenv("PSK_DECODE_LAYOUT")) r.decode_layout = !std::strcmp(v, "split") ? 1 : (!std::strcmp(v, "flat") ? 2 : 0);

@@ -541,6 +541,7 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
   if (L.num_kv_heads < kWarps && kWarps % L.num_kv_heads != 0) return false;
   const int kfree_max = std::max(1, b_max - 1);  // at least the tail page is always kept
   int chunk = 4096;
+  if (tuning().select_chunk > 0) chunk = tuning().select_chunk;  // tuning override: pages per selection CTA
   while (true) {
     const int nch = (L.max_pages + chunk - 1) / chunk;
     const int kcap = std::min(kfree_max, chunk);
