@@ -790,6 +790,37 @@ def test_fma_forms_of_the_bf16_score_and_decode():
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
 
 
+_CHUNK_CHILD = r"""
+import sys
+sys.path.insert(0, sys.argv[1])
+import test_gpu_parity as T
+import workloads as W
+from workloads.device import upload
+cases = [W.reduced(3), W.reduced(4),
+         T._custom([16 * 3000 + 5, 16 * 1100 + 9, 16 * 700], [90, 40, 700], H_q=8, H_kv=2),   # 3, 2, 1 chunks; b = P
+         T._custom([16 * 2100 + 3, 16 * 1025], [300, 2], D=64, H_q=4, H_kv=1)]                 # b = 2: no free slot
+for w in cases:
+    cache = upload(w)
+    seqs = list(range(w.B))
+    summ = T._check_cache_and_summaries(w, cache, seqs)
+    T._run_and_check(w, cache, seqs, summ, w.queries(), step_tag="chunk 1024 " + w.name)
+print("ok")
+"""
+
+
+def test_selection_in_small_chunks_with_merges():
+    """Units longer than one selection chunk select per chunk and merge the chunk winners in the
+    unit's last CTA. With PSK_SELECT_CHUNK=1024 (read once per process, so a child process) the
+    reduced workloads and a few edge cases (several chunks, b = P, no free slot) take that path
+    and must give the oracle's selection and outputs."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PSK_SELECT_CHUNK="1024", PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+    r = subprocess.run([sys.executable, "-c", _CHUNK_CHILD, root], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
 @pytest.mark.parametrize("latent", [False, True])
 def test_decode_writes_into_pinned_host_output(latent):
     """The decode's output buffer may be pinned host memory (written over NVLink-C2C by the
