@@ -627,6 +627,19 @@ def test_device_status_bounded_wait_times_out(limit):
     _run_and_check(w, cache, [0, 1], summ, w.queries(), step_tag="after a timed-out wait")
 
 
+def test_stream_argument_follows_torch_current_stream():
+    """The binding passes torch's current stream when no stream is given (through torch's raw
+    stream query): it must name the same cudaStream_t as torch.cuda.current_stream(), on the
+    default stream and inside a side-stream context."""
+    def raw(s):
+        return s.value or 0  # ctypes gives None for a null pointer
+    assert raw(psk._stream(None)) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert raw(psk._stream(None)) == side.cuda_stream != 0
+    assert raw(psk._stream(None)) == torch.cuda.current_stream().cuda_stream
+
+
 def test_host_argument_errors():
     w = _custom([64], [2], H_q=4, H_kv=1)
     cache = upload(w)
