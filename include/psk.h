@@ -122,8 +122,9 @@ enum psk_status {
  * Built shapes (anything else returns PSK_ERR_UNSUPPORTED and a workspace size of 0):
  *   GQA: v_head_dim = head_dim; page_size 16, 32, 48 or 64; num_kv_heads a divisor or a
  *        multiple of 8; PSK_BF16 with head_dim 64 or 128 and group size
- *        G = num_q_heads / num_kv_heads of 1, 2 or 4; PSK_F32 with head_dim 64 or 128 and G of
- *        1 or 4.
+ *        G = num_q_heads / num_kv_heads of 1, 2 or 4, and G = 8 at head_dim 128 (score, select
+ *        and decode; the coverage and Gaussian calls take G of 1, 2 or 4); PSK_F32 with head_dim
+ *        64 or 128 and G of 1 or 4.
  *   MLA: PSK_BF16, num_q_heads 128, head_dim 576, v_head_dim 512, page_size 32 or 64.
  */
 typedef struct psk_layout {

@@ -1090,6 +1090,7 @@ __global__ void value_tier_fill_kernel(const uint16_t *v_host, const int32_t *bl
   if (threadIdx.x == 0) *rec = slot;
 }
 
+// G = 8 is built on the tensor cores only (the FMA tiles' per-lane q would not fit).
 template <typename T, int D, int G>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   constexpr int NW = 4, NST = 2;
@@ -1098,7 +1099,9 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   static_assert(TR::STAGES >= (size_t)kFlatMaxCtas * G * 4, "stage memory must hold the merge weights");
   // bf16: the tensor-core tiles (unless PSK_DECODE_MMA=0)
   constexpr bool kMmaOk = sizeof(T) == 2 && D % 64 == 0;
-  const bool mma = kMmaOk && tuning().decode_mma;
+  constexpr bool kFmaOk = G <= 4;
+  const bool mma = kMmaOk && (tuning().decode_mma || !kFmaOk);
+  if (!mma && !kFmaOk) return cudaErrorInvalidValue;
   CUtensorMap tmK, tmV;
   const long long rows = (long long)a.nb * a.ps;
   const int dt = sizeof(T) == 4 ? PSK_F32 : PSK_BF16;
@@ -1110,13 +1113,19 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
     if constexpr (sizeof(T) == 2 && D == 128) {
       if (a.flat || !a.selected) return cudaErrorInvalidValue;
       dim3 grid(a.B * a.H_kv, a.n_items_max);
-      if (mma)
+      if (mma) {
+        // the same warp layout as the HBM decode below, so the two give identical bits
+        if ((long long)grid.x * grid.y < sm_count())
+          return launch_kernel(true, decode_split_kernel<T, D, G, 2 * NW, NST, true, true>, grid, 2 * NW * 32,
+                               DT<T, D, G, 2 * NW, NST>::SMEM, s, a, tmK, tmV);
         return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, true, true>, grid, NW * 32, TR::SMEM, s, a, tmK,
                              tmV);
-      return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, true>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
-    } else {
-      return cudaErrorInvalidValue;
+      }
+      if constexpr (kFmaOk)
+        return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, true>, grid, NW * 32, TR::SMEM, s, a, tmK,
+                             tmV);
     }
+    return cudaErrorInvalidValue;
   }
   if (!a.flat) {
     dim3 grid(a.B * a.H_kv, a.n_items_max);
@@ -1133,7 +1142,10 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
                              tmK, tmV);
       }
     }
-    return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, false>, grid, NW * 32, TR::SMEM, s, a, tmK, tmV);
+    if constexpr (kFmaOk)
+      return launch_kernel(true, decode_split_kernel<T, D, G, NW, NST, false>, grid, NW * 32, TR::SMEM, s, a, tmK,
+                           tmV);
+    return cudaErrorInvalidValue;
   }
   const int U = a.B * a.H_kv;
   cudaError_t e;
@@ -1151,7 +1163,8 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
   };
   if constexpr (kMmaOk)
     if (mma) return flat_launch(decode_flat_kernel<T, D, G, NW, NST, true>);
-  return flat_launch(decode_flat_kernel<T, D, G, NW, NST>);
+  if constexpr (kFmaOk) return flat_launch(decode_flat_kernel<T, D, G, NW, NST>);
+  return cudaErrorInvalidValue;
 }
 }  // namespace
 
@@ -1219,6 +1232,7 @@ bool plan_decode(const psk_layout &L, int entries, bool dense, DecodePlan *plan)
 
 #define PSK_DECODE_CASES(X)   \
   X(bf16_t, PSK_BF16, 128, 4) \
+  X(bf16_t, PSK_BF16, 128, 8) \
   X(bf16_t, PSK_BF16, 64, 4)  \
   X(float, PSK_F32, 64, 4)    \
   X(float, PSK_F32, 128, 4)   \

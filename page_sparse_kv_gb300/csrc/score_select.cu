@@ -308,20 +308,28 @@ __global__ void __launch_bounds__(kThreads, 4) page_score_kernel(ScoreArgs a) {
 // fp32 (the tensor cores' order), so the result meets the same bound as the FMA kernel above, at
 // 2D / 16 MMAs per 16 rows instead of 2D * G / 16 FMAs per row on each lane.
 //
+// With G = 8 a head's query heads fill all 8 columns: each MMA takes one KV head, rows 0-7 and
+// 8-15 its pages of two consecutive octets.
+//
 // Staging is the same bulk-copy ring as page_score_kernel with two changes: stages hold a
 // multiple of 8 pages, and pages sit group_bytes + 16 bytes apart (group_bytes is a multiple of
 // 128), so the 8 rows of an ldmatrix (8 pages of one head, equal offsets inside their rows) fall
-// in 8 different bank groups. Four warps: warp w takes head pair w % n_pairs of the CTA's heads
-// (one pair per two heads; with one head, rows 8-15 take the next 8 pages of the same head).
-constexpr int kMmaThreads = 128;
-constexpr int kMmaWarps = kMmaThreads / 32;
+// in 8 different bank groups. Warp w takes head pair w % n_pairs of the CTA's heads (one pair
+// per two heads, G <= 4: four warps; one head per "pair", G = 8: eight warps; with one head in
+// the CTA, or G = 8, rows 8-15 take the next 8 pages of the same head).
+template <int G>
+__host__ __device__ constexpr int mma_threads() {
+  return G > 4 ? 256 : 128;
+}
 constexpr int kMmaStages = 2;
 constexpr int kMmaStageBytes = 32768 + 512;  // 8 pages x (4 KB + 16) at H = 8, D = 128; 32 x (1 KB + 16)
 
 template <int D, int G>
-__global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreArgs a) {
   pdl_wait();
-  static_assert(G >= 1 && G <= 4, "four query heads per KV head at most");
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8, "1, 2, 4 or 8 query heads per KV head");
+  constexpr bool kWide = G > 4;                      // one KV head per MMA
+  constexpr int kMmaWarps = mma_threads<G>() / 32;
   constexpr int KS = 2 * D / 16;  // k-steps over a summary row [kmin | kmax]
   constexpr int RB = 2 * D * 2;   // bytes of one (page, head) summary row
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -386,19 +394,22 @@ __global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a
   if (warp == 0)
     for (int st = 0; st < kMmaStages && st < n_stages; ++st) produce(st, block_of(st));
 
-  // head pair of this warp (heads local to the CTA's group)
-  const int n_pairs = hpc >= 2 ? hpc / 2 : 1;
+  // head pair of this warp (heads local to the CTA's group); G = 8: one head
+  const int n_pairs = kWide ? hpc : (hpc >= 2 ? hpc / 2 : 1);
   const int pair = warp % n_pairs, wsub = warp / n_pairs, wpp = kMmaWarps / n_pairs;
-  const int hlA = hpc >= 2 ? 2 * pair : 0, hlB = hpc >= 2 ? 2 * pair + 1 : 0;
+  const int hlA = kWide ? pair : (hpc >= 2 ? 2 * pair : 0);
+  const int hlB = kWide ? pair : (hpc >= 2 ? 2 * pair + 1 : 0);
+  const bool octet_pairs = kWide || hpc == 1;  // rows 8-15: the next 8 pages of the same head
 
   // B fragments for all k-steps: lane holds column n = lane / 4 (head hA for n < 4, else hB;
-  // query head n % 4 of it) at k = 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) of each k-step, t = lane % 4.
-  // k-steps 0 .. D/16-1 meet kmin (min(q,0)), the rest kmax (max(q,0)).
+  // query head n % 4 of it; G = 8: query head n of the warp's head) at k = 2t, 2t+1 (b0) and
+  // 2t+8, 2t+9 (b1) of each k-step, t = lane % 4. k-steps 0 .. D/16-1 meet kmin (min(q,0)), the
+  // rest kmax (max(q,0)).
   uint32_t bq[KS][2];
   {
     const int n = lane >> 2, t = lane & 3;
-    const int g = n & 3;
-    const int hl = n < 4 ? hlA : hlB;
+    const int g = kWide ? n : (n & 3);
+    const int hl = (kWide || n < 4) ? hlA : hlB;
     if (g < G) {
       const uint32_t *qr = reinterpret_cast<const uint32_t *>(reinterpret_cast<const bf16_t *>(a.q) +
                                                               ((size_t)i * a.H_q + (size_t)(h0 + hl) * G + g) * D);
@@ -435,9 +446,9 @@ __global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a
     const int pb = p0 + st * sp;
     const int np = min(sp, p1 - pb);
     const int n_oct = (np + 7) >> 3;
-    const int n_items = hpc >= 2 ? n_oct : (n_oct + 1) >> 1;
+    const int n_items = octet_pairs ? (n_oct + 1) >> 1 : n_oct;
     for (int m = wsub; m < n_items; m += wpp) {  // warp-uniform bound
-      const int oA = hpc >= 2 ? m : 2 * m, oB = hpc >= 2 ? m : 2 * m + 1;
+      const int oA = octet_pairs ? 2 * m : m, oB = octet_pairs ? 2 * m + 1 : m;
       // rows past the stage's live pages read the last page of the stage (discarded below)
       const int j = min(((rowB ? oB : oA) << 3) + rr, sp - 1);
       const uint32_t addr = stage_addr + (uint32_t)j * (uint32_t)(group_bytes + 16) + lane_off;
@@ -450,19 +461,45 @@ __global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a
         mma_16816_bf16(acc0, fa, bq[s][0], bq[s][1]);
         mma_16816_bf16(acc1, fb, bq[s + 1][0], bq[s + 1][1]);
       }
-      const float x0 = outB ? acc0[2] + acc1[2] : acc0[0] + acc1[0];
-      const float x1 = outB ? acc0[3] + acc1[3] : acc0[1] + acc1[1];
-      float v = g0 < G ? x0 : -INFINITY;
-      if (g0 + 1 < G) v = fmaxf(v, x1);
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-      const int jo = ((outB ? oB : oA) << 3) + r0;
-      if ((t & 1) == 0 && jo < np) {
-        const int p = pb + jo;
-        const int unit = i * a.H_kv + h0 + (outB ? hlB : hlA);
-        const float sc = v * a.scale;
-        const bool forced = always_kept(p, P, a.sink, a.window);
-        a.keys[(size_t)unit * a.key_stride + p] = (okflag[slot][jo] && !forced) ? score_key(sc) : 0u;
-        if (a.scores_out) a.scores_out[(size_t)unit * a.max_pages + p] = sc;
+      if constexpr (kWide) {
+        // row r0 (octet oA) and row r0 + 8 (octet oB) of the warp's head, columns 2t, 2t + 1 of
+        // its 8 query heads: the max over the 8 columns takes two shuffles per row
+        float vA = fmaxf(acc0[0] + acc1[0], acc0[1] + acc1[1]);
+        float vB = fmaxf(acc0[2] + acc1[2], acc0[3] + acc1[3]);
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          vA = fmaxf(vA, __shfl_xor_sync(0xffffffffu, vA, o));
+          vB = fmaxf(vB, __shfl_xor_sync(0xffffffffu, vB, o));
+        }
+        if (t == 0) {
+          const int unit = i * a.H_kv + h0 + hlA;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int jo = ((r ? oB : oA) << 3) + r0;
+            if (jo < np) {
+              const int p = pb + jo;
+              const float sc = (r ? vB : vA) * a.scale;
+              const bool forced = always_kept(p, P, a.sink, a.window);
+              a.keys[(size_t)unit * a.key_stride + p] = (okflag[slot][jo] && !forced) ? score_key(sc) : 0u;
+              if (a.scores_out) a.scores_out[(size_t)unit * a.max_pages + p] = sc;
+            }
+          }
+        }
+      } else {
+        const float x0 = outB ? acc0[2] + acc1[2] : acc0[0] + acc1[0];
+        const float x1 = outB ? acc0[3] + acc1[3] : acc0[1] + acc1[1];
+        float v = g0 < G ? x0 : -INFINITY;
+        if (g0 + 1 < G) v = fmaxf(v, x1);
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+        const int jo = ((outB ? oB : oA) << 3) + r0;
+        if ((t & 1) == 0 && jo < np) {
+          const int p = pb + jo;
+          const int unit = i * a.H_kv + h0 + (outB ? hlB : hlA);
+          const float sc = v * a.scale;
+          const bool forced = always_kept(p, P, a.sink, a.window);
+          a.keys[(size_t)unit * a.key_stride + p] = (okflag[slot][jo] && !forced) ? score_key(sc) : 0u;
+          if (a.scores_out) a.scores_out[(size_t)unit * a.max_pages + p] = sc;
+        }
       }
     }
     __syncthreads();  // every warp is done with this slot
@@ -475,15 +512,18 @@ __global__ void __launch_bounds__(kMmaThreads) page_score_mma_kernel(ScoreArgs a
 }
 
 // The score kernel for these units: the tensor-core kernel for bf16 per-KV-head units (unless
-// PSK_SCORE_MMA=0), else the FMA kernel.
+// PSK_SCORE_MMA=0), else the FMA kernel. G = 8 is built on the tensor cores only.
 enum class ScoreKernel { kFma, kFmaPerQueryHead, kMma };
 
 template <typename T, int D, int G>
 const void *score_kernel_fn(ScoreKernel k) {
-  if constexpr (sizeof(T) == 2 && G <= 4)
+  if constexpr (sizeof(T) == 2)
     if (k == ScoreKernel::kMma) return reinterpret_cast<const void *>(page_score_mma_kernel<D, G>);
-  if (k == ScoreKernel::kFmaPerQueryHead) return reinterpret_cast<const void *>(page_score_kernel<T, D, G, true>);
-  return reinterpret_cast<const void *>(page_score_kernel<T, D, G, false>);
+  if constexpr (G <= 4) {
+    if (k == ScoreKernel::kFmaPerQueryHead) return reinterpret_cast<const void *>(page_score_kernel<T, D, G, true>);
+    return reinterpret_cast<const void *>(page_score_kernel<T, D, G, false>);
+  }
+  return nullptr;
 }
 
 template <typename T, int D, int G>
@@ -495,19 +535,21 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   ScoreKernel kind = a.kv_shift != 0 ? ScoreKernel::kFmaPerQueryHead : ScoreKernel::kFma;
   int threads = kThreads;
   int smem = kStages * kStageBytes;
-  if (sizeof(T) == 2 && G <= 4 && a.kv_shift == 0 && tuning().score_mma) {
+  if (sizeof(T) == 2 && a.kv_shift == 0 && (tuning().score_mma || G > 4)) {
     kind = ScoreKernel::kMma;
-    threads = kMmaThreads;
+    threads = mma_threads<G>();
     smem = kMmaStages * kMmaStageBytes;
     const int group_bytes = hpc * 2 * D * 2;  // <= 4 KB, so at least 8 pages per stage
     b.stage_pages = std::min(kMaxStagePages, kMmaStageBytes / (group_bytes + 16)) / 8 * 8;
   }
+  const void *fn = score_kernel_fn<T, D, G>(kind);
+  if (!fn) return cudaErrorInvalidValue;
   // Tail region: about kTailWaves waves of short CTAs over the sequences' last pages. A grid of
   // equal chunks ends with its last wave draining for one whole CTA lifetime at falling
   // occupancy; short CTAs last make that drain short.
   {
     int per_sm = 0;
-    cudaError_t e = kernel_setup(score_kernel_fn<T, D, G>(kind), threads, smem, &per_sm);
+    cudaError_t e = kernel_setup(fn, threads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     const Tuning &tu = tuning();
     b.tail_chunk = tu.score_tail_chunk > 0 ? tu.score_tail_chunk : kTailChunk;
@@ -523,12 +565,15 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   if (n_ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaErrorInvalidValue;
   if (kind == ScoreKernel::kMma) {
-    if constexpr (sizeof(T) == 2 && G <= 4)
+    if constexpr (sizeof(T) == 2)
       e = launch_kernel(true, page_score_mma_kernel<D, G>, (unsigned)n_ctas, threads, smem, s, b);
-  } else if (kind == ScoreKernel::kFmaPerQueryHead) {
-    if constexpr (G == 1) e = launch_kernel(true, page_score_kernel<T, D, G, true>, (unsigned)n_ctas, threads, smem, s, b);
-  } else {
-    e = launch_kernel(true, page_score_kernel<T, D, G, false>, (unsigned)n_ctas, threads, smem, s, b);
+  } else if constexpr (G <= 4) {
+    if (kind == ScoreKernel::kFmaPerQueryHead) {
+      if constexpr (G == 1)
+        e = launch_kernel(true, page_score_kernel<T, D, G, true>, (unsigned)n_ctas, threads, smem, s, b);
+    } else {
+      e = launch_kernel(true, page_score_kernel<T, D, G, false>, (unsigned)n_ctas, threads, smem, s, b);
+    }
   }
   if (e != cudaSuccess || !(stages & kStageSelect)) return e;
   return launch_page_select(b, s);
@@ -589,6 +634,7 @@ bool plan_score(const psk_layout &L, int b_max, ScorePlan *plan, int kv_shift) {
 
 #define PSK_SCORE_CASES(X)   \
   X(bf16_t, PSK_BF16, 128, 4) \
+  X(bf16_t, PSK_BF16, 128, 8) \
   X(bf16_t, PSK_BF16, 64, 4)  \
   X(float, PSK_F32, 64, 4)    \
   X(float, PSK_F32, 128, 4)   \

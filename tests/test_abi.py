@@ -52,6 +52,11 @@ def test_host_checks_reject_before_launch(lib):
     assert psk.score_select_workspace_size(psk.Layout(2, 32, 8, 96, 96, 16, 100, 50), 10) == 0
     assert psk.dense_decode_workspace_size(psk.Layout(2, 24, 8, 128, 128, 16, 100, 50)) == 0
     assert psk.dense_decode_workspace_size(psk.Layout(2, 32, 8, 128, 128, 8, 100, 50)) == 0
+    # G = 8 is built for bf16 at head_dim 128 only (tensor-core score and decode)
+    assert psk.score_select_workspace_size(psk.Layout(2, 64, 8, 128, 128, 16, 100, 50), 10) > 256
+    assert psk.sparse_decode_workspace_size(psk.Layout(2, 64, 8, 128, 128, 16, 100, 50), 10) > 256
+    assert psk.score_select_workspace_size(psk.Layout(2, 64, 8, 64, 64, 16, 100, 50), 10) == 0
+    assert psk.score_select_workspace_size(psk.Layout(2, 64, 8, 128, 128, 16, 100, 50, psk.PSK_F32), 10) == 0
     # invalid layouts
     assert psk.append_workspace_size(psk.Layout(0, 32, 8, 128, 128, 16, 100, 50)) == 0
     assert psk.append_workspace_size(psk.Layout(1, 30, 8, 128, 128, 16, 100, 50)) == 0

@@ -182,6 +182,10 @@ def _custom(seq_lens, budgets, ps=16, dtype="bf16", H_q=8, H_kv=2, D=128, n_hot=
     dict(seq_lens=[16 * 27 + 4, 40], budgets=[5, 3], dtype="f32", H_q=1, H_kv=1),        # fp32, D = 128, G = 1
     dict(seq_lens=[16 * 40 + 7, 16 * 11], budgets=[6, 3], H_q=32, H_kv=16),    # two head groups, G = 2
     dict(seq_lens=[16 * 33 + 9, 300], budgets=[5, 4], H_q=64, H_kv=16),        # two head groups, G = 4
+    dict(seq_lens=[16 * 47 + 3, 16 * 12, 90], budgets=[6, 4, 3], H_q=64, H_kv=8),   # G = 8
+    dict(seq_lens=[16 * 60 + 11, 250], budgets=[9, 4], H_q=32, H_kv=4),          # G = 8, 4 KV heads
+    dict(seq_lens=[16 * 41 + 1, 77], budgets=[7, 3], H_q=8, H_kv=1),             # G = 8, one KV head
+    dict(seq_lens=[64 * 13 + 5, 64 * 4], budgets=[5, 3], ps=64, H_q=64, H_kv=8), # G = 8, 64-token pages
 ])
 def test_edge_cases(case):
     w = _custom(**case)
@@ -625,6 +629,32 @@ def test_device_status_bounded_wait_times_out(limit):
     psk.clear_device_status(cache.ws)
     summ = _check_cache_and_summaries(w, cache, [0, 1])
     _run_and_check(w, cache, [0, 1], summ, w.queries(), step_tag="after a timed-out wait")
+
+
+def test_value_tier_in_host_memory_group_of_eight():
+    """The host-memory value tier with eight query heads per KV head (tensor-core tiles only):
+    the decode equals the device-memory decode bit for bit, and the oracle."""
+    w = _custom([16 * 75 + 5, 16 * 19 + 9, 17], [40, 9, 2], H_q=64, H_kv=8)
+    cache = upload(w)
+    L = cache.layout
+    q_np = w.queries()
+    q = to_torch(q_np, w.dtype).cuda()
+    v_host = cache.v_cache.cpu().pin_memory()
+    sel = cache.score_select(q, dev_budgets(w))
+    out_dev = cache.sparse_decode(q, sel)
+    out_host = torch.empty_like(out_dev)
+    psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_host, cache.block_table, cache.seq_lens, sel, cache.b_max,
+                               cache.scale, out_host, cache.ws, v_host=True)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    assert torch.equal(out_dev, out_host)
+    sel_np = sel.cpu().numpy()
+    out_np = from_torch(out_host.float(), "f32")
+    for i in range(w.B):
+        n = int(w.seq_lens[i])
+        use = [[int(x) for x in sel_np[i, h] if x >= 0] for h in range(w.H_kv)]
+        ref = O.attend_pages(q_np[i], w.keys(i), w.values(i), n, w.page_size, use, w.dtype, cache.scale)
+        check_output(out_np[i], ref, w.dtype)
 
 
 def test_stream_argument_follows_torch_current_stream():
