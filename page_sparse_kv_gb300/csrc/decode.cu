@@ -4,7 +4,8 @@
 // Sparse decode: a paged kernel that reads only the selected pages). The dense decode is the
 // same kernel with the implicit page list 0 .. P-1.
 //
-// Work: one CTA of NW warps per (split of `sw` list entries, KV head, sequence). The group's G
+// Work: one CTA of NW warps (4; 8 when the grid is smaller than one CTA per SM) per (split of
+// `sw` list entries, KV head, sequence). The group's G
 // query heads share every K/V element loaded, so each element is converted once and used G
 // times. A page is cut into 16-token tiles; warp w takes tiles w, w + NW, ... of the split and
 // keeps its own (m, l, O) state. Lane 0 of each warp stages the tiles into the warp's ring of
@@ -12,7 +13,8 @@
 // evict-first), completing on the stage's mbarrier, NST - 1 tiles in flight per warp. Rows past
 // seq_len may hold anything: their logits are masked to -inf and P.V stops at the last valid row.
 //
-// Per tile and warp: lane = (tq = lane / 8, dg = lane % 8). QK: the lane owns the 16-byte
+// FMA tiles (fp32 caches; bf16 when PSK_DECODE_MMA=0), per tile and warp: lane = (tq = lane / 8,
+// dg = lane % 8). QK: the lane owns the 16-byte
 // chunks dg, dg + 8, ... of each K row and the matching q slices (scaled by scale * log2(e) so
 // exp2 gives the softmax weights) and computes partial dot products for tokens tq, tq + 4,
 // tq + 8, tq + 12 and all G heads with packed fp32x2 FMAs; a transposing butterfly over the 8
@@ -21,9 +23,9 @@
 // pairs. PV: the lane owns D/32 output dims of all G heads and accumulates with packed FMAs
 // from one conflict-free V row chunk per token.
 //
-// bf16 caches compute each tile on the tensor cores instead (warp_tiles over an MmaWarp state):
-// S = q K^T and O += P V as warp-level m16n8k16 MMAs (bf16 in, fp32 accumulate), with the query
-// heads as the M rows. The tiles then arrive as 128-byte TMA boxes stored with the 128-byte
+// bf16 caches compute each tile on the tensor cores instead (warp_tiles_mma over an MmaWarp
+// state; the default, and the only form for G = 8): S = q K^T and O += P V as warp-level
+// m16n8k16 MMAs (bf16 in, fp32 accumulate), with the query heads as the M rows. The tiles then arrive as 128-byte TMA boxes stored with the 128-byte
 // swizzle, so ldmatrix reads K (as is) and V (transposed) without bank conflicts. P stays in
 // registers: its fp32 weights are split into a bf16 high part (rows 0..7 of the A fragment)
 // and the bf16 rounding of the remainder (rows 8..15, otherwise unused), so P V carries about

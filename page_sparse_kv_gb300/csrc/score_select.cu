@@ -2,18 +2,24 @@
 //
 // Score (EntmaxKV README, "Two selection strategies", Top-k; kernels/page_criticality.py):
 //   score[i,h,p] = scale * max_{g in group(h)} sum_d max(q_gd * kmin_pd, q_gd * kmax_pd)
-// The kernel evaluates each term as max(q,0) * kmax + min(q,0) * kmin, which equals
+// The kernels evaluate each term as max(q,0) * kmax + min(q,0) * kmin, which equals
 // max(q * kmin, q * kmax) exactly whenever kmin <= kmax (one of the two products is +-0),
-// so every kept product is the same fp32 product; accumulation is fp32 (bf16 caches: mixed
-// fma.f32.bf16 on the raw bf16 pairs; fp32 caches: packed fp32x2 FMAs).
+// so every kept product is the same fp32 product; accumulation is fp32.
 //
-// page_score_kernel streams the summaries: one CTA per (chunk of pages, sequence, group of up
-// to 8 KV heads); warp w scores KV head w % 8 of the group, so a page's summaries for all heads
-// (one 4 KB run at D = 128 bf16) are read together. A (page, head) summary row is read by
-// LPP = D * sizeof(T) / 16 lanes with one 16-byte load each. Partial sums are reduced across
-// the LPP lanes by a transposing butterfly (each step halves the values a lane carries), then
-// the group max is taken across the lanes that ended up holding different query heads. The
-// kernel writes one 32-bit order key per page to the workspace (0 = an always-kept page, or a
+// Two kernels stream the summaries, one CTA per (chunk of pages, sequence, group of up to 8 KV
+// heads), so a page's summaries for all the group's heads (one 4 KB run at D = 128 bf16) are
+// read together:
+// - page_score_mma_kernel (bf16 caches, per-KV-head units; the default): the sum over a
+//   summary row is one dot product of length 2D, taken on the tensor cores by warp-level
+//   mma.sync over 16 (page, head) rows at a time (see its section below).
+// - page_score_kernel (fp32 caches, the per-query-head view, and bf16 when PSK_SCORE_MMA=0):
+//   warp w scores KV head w % 8 of the group; a (page, head) summary row is read by
+//   LPP = D * sizeof(T) / 16 lanes with one 16-byte load each and summed with FMAs (bf16: mixed
+//   fma.f32.bf16 on the raw bf16 pairs; fp32: packed fp32x2 FMAs). Partial sums are reduced
+//   across the LPP lanes by a transposing butterfly (each step halves the values a lane
+//   carries), then the group max is taken across the lanes that ended up holding different
+//   query heads.
+// Both write one 32-bit order key per page to the workspace (0 = an always-kept page, or a
 // flagged bad block), which the selection kernel reads.
 #include <algorithm>
 
