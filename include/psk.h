@@ -42,7 +42,9 @@
  *     may also be host memory the GPU addresses directly (pinned, under unified addressing),
  *     e.g. an output written straight to the host. Index tensors are int32. q, k_new, v_new,
  *     caches, summaries and out share the storage type `layout->dtype` (PSK_BF16 or
- *     PSK_F32); arithmetic is fp32.
+ *     PSK_F32); arithmetic is fp32. With PSK_BF16 the page scores and q.k products run on the
+ *     tensor cores (bf16 x bf16 products are exact in fp32, sums are fp32), and the decode's
+ *     softmax weights enter P.V as the sum of two bf16 values (about 16 significant bits).
  *   - The caller owns every buffer. The library allocates nothing, frees nothing and
  *     keeps no state between calls apart from what it writes into the caller's buffers.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
