@@ -170,6 +170,7 @@ def _custom(seq_lens, budgets, ps=16, dtype="bf16", H_q=8, H_kv=2, D=128, n_hot=
     dict(seq_lens=[16 * 700 + 3, 5000], budgets=[700, 3]),             # many free slots, ragged tail
     dict(seq_lens=[64 * 9 + 1, 64 * 30], budgets=[4, 7], ps=64),       # page_size 64
     dict(seq_lens=[32 * 50 + 31, 32], budgets=[5, 3], ps=32),          # page_size 32
+    dict(seq_lens=[48 * 37 + 20, 48 * 3 + 1, 47], budgets=[6, 3, 2], ps=48),   # page_size 48: three tiles a page
     dict(seq_lens=[16 * 20 + 9, 77], budgets=[6, 3], dtype="f32", D=64, H_q=4, H_kv=1),
     dict(seq_lens=[16 * 30 + 2, 300], budgets=[5, 4], D=64),
     dict(seq_lens=[16 * 70 + 3, 500], budgets=[9, 4], D=64, H_q=4, H_kv=1),   # 256-byte page runs
@@ -362,7 +363,7 @@ def test_split_score_then_select_equals_combined(latent):
     assert torch.equal(torch.nan_to_num(sc1, nan=-1e30), torch.nan_to_num(sc2, nan=-1e30))
 
 
-@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("ps", [16, 48, 64])
 def test_value_tier_in_host_memory(ps):
     """V in pinned host memory, read over NVLink-C2C (PSK_DECODE_V_HOST): the decode equals the
     device-memory decode bit for bit and the oracle; a decode append writes the new token's value
