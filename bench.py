@@ -330,26 +330,79 @@ def run_psk(args):
     hot = None
     if args.v_host and (w.latent or w.dtype != "bf16" or D != 128):
         raise SystemExit("--v-host is built for GQA bf16 caches with head_dim 128")
+    selector = args.selector
+    if selector != "bound" and (w.latent or args.v_host):
+        raise SystemExit("--selector other than bound is built for GQA caches with V in HBM")
+    if selector == "per-query-head":  # one selected row per query head
+        sel = torch.empty(B, Hq, w.b_max, dtype=torch.int32, device=dev)
+    if selector == "coverage":  # the K-only mass pass needs the coverage workspace
+        ws = psk.make_workspace(L, w.b_max, dev, coverage=True)
+    stats = None
+    if selector == "gaussian":
+        # the fp32 key mean / std store, built (untimed) by re-appending every sequence's keys and
+        # values from the cache itself, a few sequences at a time
+        stats = torch.zeros(w.num_blocks, Hkv, 2, D, dtype=torch.float32, device=dev)
+        bt_dev = cache.block_table
+        for i0 in range(0, B, 4):
+            idx = list(range(i0, min(B, i0 + 4)))
+            ks, vs, cu_l = [], [], [0]
+            for i in idx:
+                n = int(lens[i])
+                P_i = (n + w.page_size - 1) // w.page_size
+                blocks = bt_dev[i, :P_i].long()
+                ks.append(cache.k_cache[blocks].reshape(-1, Hkv, D)[:n])
+                vs.append(cache.v_cache[blocks].reshape(-1, Hkv, w.D_v)[:n])
+                cu_l.append(cu_l[-1] + n)
+            cu_i = torch.tensor(cu_l, dtype=torch.int32, device=dev)
+            st_i = torch.zeros(len(idx), dtype=torch.int32, device=dev)
+            Li = psk.Layout(len(idx), Hq, Hkv, D, w.D_v, w.page_size, w.num_blocks, w.max_pages, L.dtype, L.latent)
+            psk.kv_append_and_summarize_ex(Li, torch.cat(ks), torch.cat(vs), st_i, cu_i, max(cu_l[j + 1] - cu_l[j]
+                                           for j in range(len(idx))), cache.k_cache, cache.v_cache, None, stats,
+                                           bt_dev[i0:i0 + len(idx)].contiguous(), ws)
+            del ks, vs
+        torch.cuda.synchronize()
 
     def append():
-        psk.kv_append_and_summarize(L, k_new, v_new, start, cu, 1, cache.k_cache, v_store, cache.summaries,
-                                    cache.block_table, ws)
+        if stats is not None:  # both stores kept in step
+            psk.kv_append_and_summarize_ex(L, k_new, v_new, start, cu, 1, cache.k_cache, v_store, cache.summaries,
+                                           stats, cache.block_table, ws)
+        else:
+            psk.kv_append_and_summarize(L, k_new, v_new, start, cu, 1, cache.k_cache, v_store, cache.summaries,
+                                        cache.block_table, ws)
 
     def score():
-        psk.page_score_select(L, q, cache.summaries, cache.block_table, cache.seq_lens, bud, w.b_max, cache.scale,
-                              sel, ws)
+        if selector == "per-query-head":
+            psk.page_score_select_ex(L, q, cache.summaries, cache.block_table, cache.seq_lens, w.b_max, cache.scale,
+                                     sel, ws, budgets=bud, per_query_head=True)
+        elif selector == "coverage":
+            psk.page_select_coverage(L, q, cache.k_cache, cache.block_table, cache.seq_lens, args.coverage, w.b_max,
+                                     cache.scale, sel, ws)
+        elif selector == "gaussian":
+            psk.page_score_select_gaussian(L, q, stats, cache.block_table, cache.seq_lens, w.b_max, cache.scale,
+                                           args.gauss_z, sel, ws, budgets=bud)
+        else:
+            psk.page_score_select(L, q, cache.summaries, cache.block_table, cache.seq_lens, bud, w.b_max,
+                                  cache.scale, sel, ws)
 
-    # kernels one score + select call launches: 2 (score, selection), 3 for the latent form
-    ss_launches = psk.score_select_launches(L, w.b_max)
+    # kernels one score + select call launches: 2 (score, selection), 3 for the latent form and
+    # for coverage (mass pass, keys and count, selection)
+    ss_launches = 3 if selector == "coverage" else psk.score_select_launches(L, w.b_max,
+                                                                             selector == "per-query-head")
 
     # the same two stages as separate calls, so each kernel gets its own events in the eager loop
-    sel_prm = psk.select_params(budgets=bud)
+    # (coverage and the Gaussian score are one call each: timed as the score, selection included)
+    sel_prm = psk.select_params(budgets=bud, per_query_head=selector == "per-query-head")
 
     def score_only():
-        psk.page_score(L, q, cache.summaries, cache.block_table, cache.seq_lens, sel_prm, w.b_max, cache.scale, ws)
+        if selector in ("coverage", "gaussian"):
+            score()
+        else:
+            psk.page_score(L, q, cache.summaries, cache.block_table, cache.seq_lens, sel_prm, w.b_max, cache.scale,
+                           ws)
 
     def select_only():
-        psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
+        if selector not in ("coverage", "gaussian"):
+            psk.page_select(L, cache.seq_lens, sel_prm, w.b_max, sel, ws)
 
     def decode(dst=None):  # dst: the output buffer (default: `out` in device memory)
         o = out if dst is None else dst
@@ -359,6 +412,9 @@ def run_psk(args):
         elif args.v_host:
             psk.sparse_paged_decode_ex(L, q, cache.k_cache, v_store, cache.block_table, cache.seq_lens, sel, w.b_max,
                                        cache.scale, o, ws, v_host=True)
+        elif selector == "per-query-head":
+            psk.sparse_paged_decode_ex(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
+                                       w.b_max, cache.scale, o, ws, per_query_head=True)
         else:
             psk.sparse_paged_decode(L, q, cache.k_cache, cache.v_cache, cache.block_table, cache.seq_lens, sel,
                                     w.b_max, cache.scale, o, ws)
@@ -403,13 +459,19 @@ def run_psk(args):
     # stream beside score + select, and the decode waits for both (page_sparse_kv_gb300.step,
     # the same step tests/test_gpu_step_graph.py checks against the oracle).
     from page_sparse_kv_gb300.step import DecodeStep, capture as graph_of
-    sparse_step = DecodeStep(append, score, decode)
+    # coverage reads every key row (the tail page's too) and the Gaussian score reads the tail
+    # page's statistics: there the append runs before the selection on the main stream
+    if selector in ("coverage", "gaussian"):
+        sparse_step = DecodeStep(lambda: None, lambda: (append(), score()), decode)
+    else:
+        sparse_step = DecodeStep(append, score, decode)
 
     def step_overlapped(pre_main=None, pre_side=None, post=None, dec_out=None):
         if dec_out is None:
             sparse_step.launch(pre_main, pre_side, post)
         else:
-            DecodeStep(append, score, lambda: decode(dec_out)).launch(pre_main, pre_side, post)
+            DecodeStep(sparse_step.append, sparse_step.score_select, lambda: decode(dec_out)).launch(
+                pre_main, pre_side, post)
 
     try:
         g_sparse = graph_of(step_overlapped)
@@ -543,7 +605,10 @@ def run_psk(args):
             k_new.copy_(kh, non_blocking=True)
             if vh is not None:
                 v_new.copy_(vh, non_blocking=True)
-        step_overlapped(pre_main=lambda: q.copy_(qh, non_blocking=True), pre_side=copy_kv, dec_out=oh)
+        if selector in ("coverage", "gaussian"):  # the append runs on the main stream: copy there
+            step_overlapped(pre_main=lambda: (q.copy_(qh, non_blocking=True), copy_kv()), dec_out=oh)
+        else:
+            step_overlapped(pre_main=lambda: q.copy_(qh, non_blocking=True), pre_side=copy_kv, dec_out=oh)
 
     e2e_ms = e2e_eager_ms
     if g_sparse is not None:  # the same step with its copies, replayed as one CUDA graph
@@ -577,11 +642,17 @@ def run_psk(args):
     kv_row = D if w.latent else D + w.D_v  # a latent row carries the value in its first D_v dims
     sel_np = sel.cpu().numpy()
     sel_tokens = 0
+    G_rows = sel_np.shape[1] // Hkv  # rows per cache head: 1, or G for per-query-head rows
     for i in range(B):
-        for h in range(Hkv):
-            pages = sel_np[i, h][sel_np[i, h] >= 0]
+        for h in range(Hkv):  # each (cache head, page) counted once, however many rows select it
+            rows = sel_np[i, h * G_rows:(h + 1) * G_rows]
+            pages = np.unique(rows[rows >= 0])
             sel_tokens += int(np.minimum(w.page_size, lens[i] - pages * w.page_size).sum())
     kv_bytes = sel_tokens * kv_row * es
+    if selector == "coverage":  # the exact page masses: every live key row once
+        summ_bytes = int(lens.sum()) * Hkv * D * es
+    elif selector == "gaussian":  # the fp32 mean / std rows of every live page
+        summ_bytes = int(P.sum()) * Hkv * 2 * D * 4
     score_bytes = summ_bytes + q_bytes
     decode_bytes = kv_bytes + q_bytes + out_bytes
     step_bytes = summ_bytes + kv_bytes + q_bytes + out_bytes
@@ -593,7 +664,9 @@ def run_psk(args):
     if t_score >= t_dec and t_score >= t_select:
         # bf16 GQA caches score on the tensor cores (page_score_mma_kernel), fp32 caches on the FMA pipe
         dom = ("mla_qsplit_kernel+mla_score_kernel" if w.latent else
-               "page_score_mma_kernel" if w.dtype == "bf16" else "page_score_kernel")
+               "page_mass_kernel+coverage_keys_kernel+page_select_kernel" if selector == "coverage" else
+               "gauss_score_kernel+page_select_kernel" if selector == "gaussian" else
+               "page_score_kernel" if selector == "per-query-head" or w.dtype != "bf16" else "page_score_mma_kernel")
         roof = {"bound": "hbm", "kernel": dom, "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
                 "unit": "GB/s", "algorithmic_per_launch": score_bytes, "algorithmic_unit": "B",
                 "launch_us": t_score * 1e3}
@@ -615,13 +688,15 @@ def run_psk(args):
 
     roof["peak_kind"] = pk["kind"] + (" sustained bf16" if roof["bound"] == "tensor" else " copy")
     # the captured traffic is of the HBM-resident decode: with V in host memory it does not apply
-    roof["traffic"], scaled = traffic_of(w.name, dom) if not (args.v_host and dom == "decode_split_kernel") else (None, None)
+    # the captured traffic is of the default selector's kernels
+    roof["traffic"], scaled = (traffic_of(w.name, dom) if not (args.v_host and dom == "decode_split_kernel")
+                               and selector == "bound" else (None, None))
     if scaled:
         roof["traffic_note"] = f"ncu dram read + write per launch, captured on the {scaled}"
-    roof["traffic_digest"] = kernel_digest(dom)
+    roof["traffic_digest"] = kernel_digest(dom) if dom in KERNEL_SOURCES else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and selector == "bound":
         secs, cores, nseq = oracle_parallel(args.workload, args.batch, 1, args.cpu_seconds)
         cpu = {"value": secs[0] * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"about {nseq} sequence-steps (in pages) of the {B}-sequence batch through the fp64 oracle's "
@@ -638,6 +713,8 @@ def run_psk(args):
         "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H_q": Hq, "H_kv": Hkv, "D": D, "page_size": w.page_size,
+                   "selector": (selector + (f", coverage {args.coverage} capped at b_max" if selector == "coverage"
+                                            else f", z = {args.gauss_z}" if selector == "gaussian" else "")),
                    "contexts": "U[8192, 65536] seeded" if args.workload == 3 else [int(x) for x in lens[:4]],
                    "budget_pages_total": int(w.budgets.sum()),
                    "l2": (f"flushed before every timed step (working set {ws_sparse / 2**20:.0f} MiB sparse, "
@@ -698,6 +775,12 @@ def main():
                     help="with --v-host: fraction of each row's selected pages kept in an HBM hot buffer")
     ap.add_argument("--v-host", action="store_true",
                     help="keep the value cache in pinned host memory (the value tier; GQA bf16, head_dim 128)")
+    ap.add_argument("--selector", default="bound", choices=["bound", "per-query-head", "coverage", "gaussian"],
+                    help="the step's page selector: the Quest bound per KV head (default), the bound per "
+                         "query head, adaptive coverage over exact page masses (--coverage, capped at the "
+                         "workload's b_max), or the Gaussian estimated maximum from mean/std summaries (--gauss-z)")
+    ap.add_argument("--coverage", type=float, default=0.95, help="--selector coverage: the mass fraction")
+    ap.add_argument("--gauss-z", type=float, default=1.0, help="--selector gaussian: z of mean + z * std")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
