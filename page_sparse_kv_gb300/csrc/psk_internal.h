@@ -59,6 +59,7 @@ struct ScoreArgs {
   int budget_pages;       // PSK_BUDGET_PAGES
   double budget_frac;     // PSK_BUDGET_FRACTION
   const int32_t *unit_budgets;  // non-null: per-unit budgets (coverage mode) instead of budgets[i]
+  int mma_hpc;            // unit heads per CTA of the tensor-core score kernel (set at launch)
 };
 
 // Page p of a sequence of P pages is always kept: one of the first `sink` or the last `window`.

@@ -330,10 +330,14 @@ __host__ __device__ constexpr int mma_threads() {
 constexpr int kMmaStages = 2;
 constexpr int kMmaStageBytes = 32768 + 512;  // 8 pages x (4 KB + 16) at H = 8, D = 128; 32 x (1 KB + 16)
 
-template <int D, int G>
+// kPerQueryHead: the units are the per-query-head view (one unit per query head, kv_shift =
+// log2 G); the same MMAs run over the cache heads, and each column (query head) is its own unit:
+// its score is written as its key, with no max over the group.
+template <int D, int G, bool kPerQueryHead = false>
 __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreArgs a) {
   pdl_wait();
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "1, 2, 4 or 8 query heads per KV head");
+  static_assert(!kPerQueryHead || G > 1, "the per-query-head view groups G > 1 query heads");
   constexpr bool kWide = G > 4;                      // one KV head per MMA
   constexpr int kMmaWarps = mma_threads<G>() / 32;
   constexpr int KS = 2 * D / 16;  // k-steps over a summary row [kmin | kmax]
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
   __shared__ int okflag[kMmaStages][kMaxStagePages];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // heads per CTA (as page_score_kernel)
+  const int hpc = a.mma_hpc;  // unit heads per CTA (chosen at launch)
   // work item (chunk, sequence, head group): the same order and regions as page_score_kernel
   int x = blockIdx.x;
   const int n_body = a.body_chunks * a.B * (a.H_kv / hpc);
@@ -354,6 +358,11 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
   x /= per_seq;
   const int i = x % a.B;
   const int h0 = (x / a.B) * hpc;
+  // cache heads of the CTA: per KV head, the unit heads themselves; per query head, the unit heads
+  // h0 .. h0 + hpc - 1 read cache heads h0 / G .. (h0 + hpc - 1) / G
+  const int hcc = kPerQueryHead ? hpc / G : hpc;
+  const int hc0 = kPerQueryHead ? h0 / G : h0;
+  const int H_cache = kPerQueryHead ? a.H_kv_cache : a.H_kv;
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
   if (seq_len < 1 || P > a.max_pages) return;  // reported by the select kernel
@@ -361,7 +370,7 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
   const int p0 = in_tail ? body_end + c * a.tail_chunk : c * a.pchunk;
   const int p1 = in_tail ? min(P, p0 + a.tail_chunk) : min(body_end, p0 + a.pchunk);
   if (p0 >= p1) return;
-  const int group_bytes = hpc * RB;
+  const int group_bytes = hcc * RB;
   const int sp = a.stage_pages;  // a multiple of 8
   const int n_stages = (p1 - p0 + sp - 1) / sp;
   const bf16_t *sumbase = reinterpret_cast<const bf16_t *>(a.summaries);
@@ -394,18 +403,18 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
     __syncwarp();
     if (ok)
       bulk_g2s_stream(smem_u32(smem_raw + (size_t)slot * kMmaStageBytes + (size_t)lane * (group_bytes + 16)),
-                      sumbase + ((size_t)blk * a.H_kv + h0) * 2 * D, group_bytes, bar, stream_policy);
+                      sumbase + ((size_t)blk * H_cache + hc0) * 2 * D, group_bytes, bar, stream_policy);
   };
 
   if (warp == 0)
     for (int st = 0; st < kMmaStages && st < n_stages; ++st) produce(st, block_of(st));
 
   // head pair of this warp (heads local to the CTA's group); G = 8: one head
-  const int n_pairs = kWide ? hpc : (hpc >= 2 ? hpc / 2 : 1);
+  const int n_pairs = kWide ? hcc : (hcc >= 2 ? hcc / 2 : 1);
   const int pair = warp % n_pairs, wsub = warp / n_pairs, wpp = kMmaWarps / n_pairs;
-  const int hlA = kWide ? pair : (hpc >= 2 ? 2 * pair : 0);
-  const int hlB = kWide ? pair : (hpc >= 2 ? 2 * pair + 1 : 0);
-  const bool octet_pairs = kWide || hpc == 1;  // rows 8-15: the next 8 pages of the same head
+  const int hlA = kWide ? pair : (hcc >= 2 ? 2 * pair : 0);
+  const int hlB = kWide ? pair : (hcc >= 2 ? 2 * pair + 1 : 0);
+  const bool octet_pairs = kWide || hcc == 1;  // rows 8-15: the next 8 pages of the same head
 
   // B fragments for all k-steps: lane holds column n = lane / 4 (head hA for n < 4, else hB;
   // query head n % 4 of it; G = 8: query head n of the warp's head) at k = 2t, 2t+1 (b0) and
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
     const int hl = (kWide || n < 4) ? hlA : hlB;
     if (g < G) {
       const uint32_t *qr = reinterpret_cast<const uint32_t *>(reinterpret_cast<const bf16_t *>(a.q) +
-                                                              ((size_t)i * a.H_q + (size_t)(h0 + hl) * G + g) * D);
+                                                              ((size_t)i * a.H_q + (size_t)(hc0 + hl) * G + g) * D);
 #pragma unroll
       for (int s = 0; s < D / 16; ++s) {
 #pragma unroll
@@ -467,7 +476,33 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
         mma_16816_bf16(acc0, fa, bq[s][0], bq[s][1]);
         mma_16816_bf16(acc1, fb, bq[s + 1][0], bq[s + 1][1]);
       }
-      if constexpr (kWide) {
+      if constexpr (kPerQueryHead) {
+        // every column is a unit. G <= 4: lane (r0, t) holds columns 2t, 2t + 1 of row r0 (head
+        // A) for t < 2, of row r0 + 8 (head B) for t >= 2. G = 8: columns 2t, 2t + 1 of rows r0
+        // and r0 + 8 (two octets of the same head).
+        auto put = [&](int oct, int hl, int g, float v) {
+          const int jo = (oct << 3) + r0;
+          if (g < G && jo < np) {
+            const int p = pb + jo;
+            const int unit = i * a.H_kv + (hc0 + hl) * G + g;
+            const float sc = v * a.scale;
+            const bool forced = always_kept(p, P, a.sink, a.window);
+            a.keys[(size_t)unit * a.key_stride + p] = (okflag[slot][jo] && !forced) ? score_key(sc) : 0u;
+            if (a.scores_out) a.scores_out[(size_t)unit * a.max_pages + p] = sc;
+          }
+        };
+        const float v0 = acc0[0] + acc1[0], v1 = acc0[1] + acc1[1];
+        const float v2 = acc0[2] + acc1[2], v3 = acc0[3] + acc1[3];
+        if constexpr (kWide) {
+          put(oA, hlA, 2 * t, v0);
+          put(oA, hlA, 2 * t + 1, v1);
+          put(oB, hlA, 2 * t, v2);
+          put(oB, hlA, 2 * t + 1, v3);
+        } else {
+          put(outB ? oB : oA, outB ? hlB : hlA, g0, outB ? v2 : v0);
+          put(outB ? oB : oA, outB ? hlB : hlA, g0 + 1, outB ? v3 : v1);
+        }
+      } else if constexpr (kWide) {
         // row r0 (octet oA) and row r0 + 8 (octet oB) of the warp's head, columns 2t, 2t + 1 of
         // its 8 query heads: the max over the 8 columns takes two shuffles per row
         float vA = fmaxf(acc0[0] + acc1[0], acc0[1] + acc1[1]);
@@ -478,7 +513,7 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
           vB = fmaxf(vB, __shfl_xor_sync(0xffffffffu, vB, o));
         }
         if (t == 0) {
-          const int unit = i * a.H_kv + h0 + hlA;
+          const int unit = i * a.H_kv + hc0 + hlA;
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int jo = ((r ? oB : oA) << 3) + r0;
@@ -500,7 +535,7 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
         const int jo = ((outB ? oB : oA) << 3) + r0;
         if ((t & 1) == 0 && jo < np) {
           const int p = pb + jo;
-          const int unit = i * a.H_kv + h0 + (outB ? hlB : hlA);
+          const int unit = i * a.H_kv + hc0 + (outB ? hlB : hlA);
           const float sc = v * a.scale;
           const bool forced = always_kept(p, P, a.sink, a.window);
           a.keys[(size_t)unit * a.key_stride + p] = (okflag[slot][jo] && !forced) ? score_key(sc) : 0u;
@@ -517,17 +552,32 @@ __global__ void __launch_bounds__(mma_threads<G>()) page_score_mma_kernel(ScoreA
   pdl_trigger();
 }
 
-// The score kernel for these units: the tensor-core kernel for bf16 per-KV-head units (unless
-// PSK_SCORE_MMA=0), else the FMA kernel. G = 8 is built on the tensor cores only.
-enum class ScoreKernel { kFma, kFmaPerQueryHead, kMma };
+// The score kernel for these units: the tensor-core kernel for bf16 caches (unless
+// PSK_SCORE_MMA=0), per KV head or per query head, else the FMA kernel. G = 8 is built on the
+// tensor cores only.
+enum class ScoreKernel { kFma, kFmaPerQueryHead, kMma, kMmaPerQueryHead };
+
+template <int D, int Gc>
+cudaError_t launch_mma_pqh(unsigned n_ctas, int smem, cudaStream_t s, const ScoreArgs &b) {
+  return launch_kernel(true, page_score_mma_kernel<D, Gc, true>, n_ctas, mma_threads<Gc>(), smem, s, b);
+}
 
 template <typename T, int D, int G>
-const void *score_kernel_fn(ScoreKernel k) {
-  if constexpr (sizeof(T) == 2)
+const void *score_kernel_fn(ScoreKernel k, int kv_shift) {
+  if constexpr (sizeof(T) == 2) {
     if (k == ScoreKernel::kMma) return reinterpret_cast<const void *>(page_score_mma_kernel<D, G>);
+    if constexpr (G == 1) {
+      if (k == ScoreKernel::kMmaPerQueryHead) {
+        if (kv_shift == 1) return reinterpret_cast<const void *>(page_score_mma_kernel<D, 2, true>);
+        if (kv_shift == 2) return reinterpret_cast<const void *>(page_score_mma_kernel<D, 4, true>);
+        if (kv_shift == 3) return reinterpret_cast<const void *>(page_score_mma_kernel<D, 8, true>);
+        return nullptr;
+      }
+    }
+  }
   if constexpr (G <= 4) {
     if (k == ScoreKernel::kFmaPerQueryHead) return reinterpret_cast<const void *>(page_score_kernel<T, D, G, true>);
-    return reinterpret_cast<const void *>(page_score_kernel<T, D, G, false>);
+    if (k == ScoreKernel::kFma) return reinterpret_cast<const void *>(page_score_kernel<T, D, G, false>);
   }
   return nullptr;
 }
@@ -536,19 +586,24 @@ template <typename T, int D, int G>
 cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   if (!(stages & kStageScore)) return launch_page_select(a, s, true);
   if (G > 1 && a.kv_shift != 0) return cudaErrorInvalidValue;  // the per-query-head view has G = 1
-  const int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;
+  int hpc = a.H_kv < kWarps ? a.H_kv : kWarps;  // unit heads per CTA
   ScoreArgs b = a;
   ScoreKernel kind = a.kv_shift != 0 ? ScoreKernel::kFmaPerQueryHead : ScoreKernel::kFma;
   int threads = kThreads;
   int smem = kStages * kStageBytes;
-  if (sizeof(T) == 2 && a.kv_shift == 0 && (tuning().score_mma || G > 4)) {
-    kind = ScoreKernel::kMma;
-    threads = mma_threads<G>();
+  if (sizeof(T) == 2 && a.kv_shift <= 3 && (tuning().score_mma || G > 4)) {
+    kind = a.kv_shift != 0 ? ScoreKernel::kMmaPerQueryHead : ScoreKernel::kMma;
+    threads = a.kv_shift == 3 || G > 4 ? 256 : 128;  // mma_threads of the cache group size
     smem = kMmaStages * kMmaStageBytes;
-    const int group_bytes = hpc * 2 * D * 2;  // <= 4 KB, so at least 8 pages per stage
+    if (a.kv_shift != 0) {  // per query head: 8 cache heads' query heads when they divide the units
+      const int wide = std::min(a.H_kv, kWarps << a.kv_shift);
+      if (a.H_kv % wide == 0) hpc = wide;
+    }
+    b.mma_hpc = hpc;
+    const int group_bytes = (hpc >> a.kv_shift) * 2 * D * 2;  // <= 4 KB, so at least 8 pages per stage
     b.stage_pages = std::min(kMaxStagePages, kMmaStageBytes / (group_bytes + 16)) / 8 * 8;
   }
-  const void *fn = score_kernel_fn<T, D, G>(kind);
+  const void *fn = score_kernel_fn<T, D, G>(kind, a.kv_shift);
   if (!fn) return cudaErrorInvalidValue;
   // Tail region: about kTailWaves waves of short CTAs over the sequences' last pages. A grid of
   // equal chunks ends with its last wave draining for one whole CTA lifetime at falling
@@ -573,6 +628,12 @@ cudaError_t launch_t(const ScoreArgs &a, cudaStream_t s, int stages) {
   if (kind == ScoreKernel::kMma) {
     if constexpr (sizeof(T) == 2)
       e = launch_kernel(true, page_score_mma_kernel<D, G>, (unsigned)n_ctas, threads, smem, s, b);
+  } else if (kind == ScoreKernel::kMmaPerQueryHead) {
+    if constexpr (sizeof(T) == 2 && G == 1) {
+      if (a.kv_shift == 1) e = launch_mma_pqh<D, 2>((unsigned)n_ctas, smem, s, b);
+      if (a.kv_shift == 2) e = launch_mma_pqh<D, 4>((unsigned)n_ctas, smem, s, b);
+      if (a.kv_shift == 3) e = launch_mma_pqh<D, 8>((unsigned)n_ctas, smem, s, b);
+    }
   } else if constexpr (G <= 4) {
     if (kind == ScoreKernel::kFmaPerQueryHead) {
       if constexpr (G == 1)

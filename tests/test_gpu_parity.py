@@ -299,6 +299,8 @@ def _run_select_params(w, cache, S, W, mode, value, step_tag, per_query_head=Fal
     dict(S=0, W=1, mode="pages", value=16, budgets=[2] * 5, dtype="f32", D=64, H_q=4, H_kv=1),
     dict(S=2, W=2, mode="fraction", value=0.05, budgets=[2] * 5, H_q=16, H_kv=8),
     dict(S=1, W=3, mode="pages", value=9, budgets=[2] * 5, D=64, H_q=32, H_kv=8),
+    dict(S=1, W=1, mode="per_seq", value=None, budgets=[30, 9, 7, 3, 5], H_q=64, H_kv=8),   # G = 8
+    dict(S=0, W=1, mode="pages", value=12, budgets=[2] * 5, H_q=8, H_kv=1),                # G = 8, one KV head
 ])
 def test_per_query_head_selection(case):
     """Pages ranked and kept per query head (the EntmaxKV top-k form; S = 0 with W = 1 is its
@@ -816,6 +818,9 @@ for w in cases:
     seqs = list(range(w.B))
     summ = T._check_cache_and_summaries(w, cache, seqs)
     T._run_and_check(w, cache, seqs, summ, w.queries(), step_tag="fma " + w.name)
+for extra in (dict(), dict(H_q=16, H_kv=8)):  # per-query-head rows, G = 4 and 2
+    w = T._custom([16 * 300 + 5, 16 * 77, 16 * 40 + 9, 33, 16 * 12], [40, 20, 12, 3, 12], **extra)
+    T._run_select_params(w, upload(w), 1, 1, "per_seq", None, "fma per q head", per_query_head=True)
 print("ok")
 """
 
