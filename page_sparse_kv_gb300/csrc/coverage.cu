@@ -10,7 +10,9 @@
 //
 //   page_mass_kernel      a K-only pass over every page: per (unit, page, query head) the max
 //                         m and the sum s = sum_t 2^(x_t - m) of the page's logits x_t =
-//                         scale * log2(e) * q . k_t (fp32).
+//                         scale * log2(e) * q . k_t (fp32). bf16 caches take
+//                         page_mass_mma_kernel instead: the same sums with q . k on the tensor
+//                         cores, K staged by TMA (unless PSK_DECODE_MMA=0).
 //   coverage_keys_kernel  one CTA per unit: the group's normalisers M_g = max_p m, Z_g =
 //                         sum_p s 2^(m - M_g); each page's mass max_g s 2^(m - M_g) / Z_g;
 //                         the selection key of that mass (0 for an always-kept page); and the
@@ -33,6 +35,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMassThreads = 128;  // four warps, one page at a time each
 constexpr int kMassPages = 32;     // pages per CTA of the mass pass
 constexpr int kCovThreads = 256;
+constexpr int kCovHist = 8;        // histogram copies of the nucleus search
 constexpr double kMassQuant = 1099511627776.0;  // 2^40: fixed-point unit of a page mass
 
 // ---- K-only pass ----------------------------------------------------------------------------
@@ -134,6 +137,143 @@ __global__ void __launch_bounds__(kMassThreads) page_mass_kernel(CoverageArgs a)
   }
 }
 
+// ---- K-only pass on the tensor cores (bf16) -------------------------------------------------
+// Grid (page chunk, unit), four warps; warp w takes pages w, w + 4, ... of the chunk. Each page's
+// 16-token K tiles stream through the warp's two-stage TMA ring as 128-byte boxes stored with
+// the 128-byte swizzle (the decode's tile layout), and S = q K^T is D/16 k-steps of one
+// ldmatrix and two mma.sync m16n8k16 with the G query heads as the M rows. Lane (g = lane / 4,
+// t4 = lane % 4) holds the logits of tokens 2 t4, 2 t4 + 1, 8 + 2 t4, 9 + 2 t4 for head g; the
+// page's (m, s) per head is an online max / sum over its tiles, reduced over the row's 4 lanes
+// when the page ends. Rows past seq_len may hold anything: their logits are set to -inf.
+constexpr int kMassMmaWarps = 4;
+constexpr int kMassStages = 2;
+
+template <int D>
+constexpr size_t mass_mma_smem() {
+  return 1024 + (size_t)kMassMmaWarps * kMassStages * 16 * D * 2;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMassMmaWarps * 32) page_mass_mma_kernel(CoverageArgs a,
+                                                                           const __grid_constant__ CUtensorMap tmK) {
+  pdl_begin();
+  static_assert(G >= 1 && G <= 8, "query heads are the MMA rows 0..7");
+  constexpr int KS = D / 16;          // k-steps of q K^T
+  constexpr int TILE = 16 * D * 2;    // one K tile: 16 rows
+  constexpr int BOX = 16 * 128;       // one 128-byte box of 16 rows
+  constexpr int NB = D * 2 / 128;     // boxes per row
+  extern __shared__ unsigned char mass_dyn[];
+  unsigned char *base =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(mass_dyn) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bars[kMassMmaWarps][kMassStages];
+  const int unit = blockIdx.y;
+  const int i = unit / a.H_kv, h = unit - i * a.H_kv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seq_len = a.seq_lens[i];
+  const int P = (seq_len + a.ps - 1) / a.ps;
+  if (seq_len < 1 || P > a.max_pages) return;  // reported by coverage_keys_kernel
+  const int pc0 = blockIdx.x * kMassPages, pc1 = min(P, pc0 + kMassPages);
+  if (pc0 >= pc1) return;
+  const int stp = a.ps / 16;  // tiles per page
+  const int n_pages = pc1 - pc0 > warp ? (pc1 - pc0 - warp + kMassMmaWarps - 1) / kMassMmaWarps : 0;
+  const int ntiles = n_pages * stp;
+  unsigned char *my = base + (size_t)warp * kMassStages * TILE;
+  if (lane == 0) {
+    for (int k = 0; k < kMassStages; ++k) mbar_init(smem_u32(&bars[warp][k]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // tile k of this warp: page pc0 + warp + (k / stp) * 4, 16-row slice k % stp
+  auto tile_page = [&](int k) { return pc0 + warp + (k / stp) * kMassMmaWarps; };
+  auto tile_rows = [&](int k) {
+    const int p = tile_page(k), sub = k % stp;
+    return min(16, seq_len - p * a.ps - sub * 16);
+  };
+  auto tile_blk = [&](int k) { return a.block_table[(size_t)i * a.max_pages + tile_page(k)]; };
+  auto issue = [&](int k) {
+    if (k >= ntiles || lane != 0) return;
+    const int stg = k % kMassStages;
+    const uint32_t bar = smem_u32(&bars[warp][stg]);
+    const int blk = tile_blk(k), nv = tile_rows(k);
+    if (nv > 0 && blk >= 0 && blk < a.nb) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, TILE);
+      const uint32_t dst = smem_u32(my + (size_t)stg * TILE);
+      const int row = blk * a.ps + (k % stp) * 16;
+      const uint64_t pol = l2_evict_first_policy();  // read once
+#pragma unroll
+      for (int b = 0; b < NB; ++b) tma_load_3d_stream(dst + b * BOX, &tmK, b * 64, h, row, bar, pol);
+    } else {
+      mbar_arrive_expect_tx(bar, 0u);
+    }
+  };
+  for (int k = 0; k < kMassStages - 1; ++k) issue(k);
+
+  const int g = lane >> 2, t4 = lane & 3, r8 = lane & 7, mi = lane >> 3;
+  uint32_t qa[KS][2];  // q as the A operand (rows 0..G-1; rows 8..15 zero)
+  if (g < G) {
+    const uint32_t *qr = reinterpret_cast<const uint32_t *>(reinterpret_cast<const bf16_t *>(a.q) +
+                                                            ((size_t)i * a.H_q + (size_t)h * G + g) * D);
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      qa[s][0] = __ldg(qr + 8 * s + t4);
+      qa[s][1] = __ldg(qr + 8 * s + 4 + t4);
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < KS; ++s) qa[s][0] = qa[s][1] = 0u;
+  }
+  const float qs = a.scale * kLog2e;
+  const int k_tok = (mi >> 1) * 8 + r8, k_ch = mi & 1;
+  float m_run = -INFINITY, s_run = 0.f;  // row g's running (max, this lane's share of the sum)
+  for (int k = 0; k < ntiles; ++k) {
+    issue(k + kMassStages - 1);
+    const int stg = k % kMassStages;
+    mbar_wait(smem_u32(&bars[warp][stg]), (k / kMassStages) & 1, a.ws);
+    const int blk = tile_blk(k), nv = tile_rows(k);
+    const bool ok = blk >= 0 && blk < a.nb;
+    if (!ok && lane == 0 && k % stp == 0) set_status(a.ws, PSK_DEV_BAD_BLOCK);
+    if (ok && nv > 0) {
+      const uint32_t aK = smem_u32(my + (size_t)stg * TILE);
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        const int ch = 2 * s + k_ch;
+        uint32_t kb[4];
+        ldsm_x4(aK + (ch >> 3) * BOX + k_tok * 128 + (((ch & 7) ^ r8) << 4), kb);
+        const uint32_t qa4[4] = {qa[s][0], 0u, qa[s][1], 0u};
+        mma_16816_bf16(s0, qa4, kb[0], kb[1]);
+        mma_16816_bf16(s1, qa4, kb[2], kb[3]);
+      }
+      const int tb = 2 * t4;
+      float x[4] = {s0[0] * qs, s0[1] * qs, s1[0] * qs, s1[1] * qs};
+      if (tb >= nv) x[0] = -INFINITY;
+      if (tb + 1 >= nv) x[1] = -INFINITY;
+      if (tb + 8 >= nv) x[2] = -INFINITY;
+      if (tb + 9 >= nv) x[3] = -INFINITY;
+      float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float mnew = fmaxf(m_run, tmax);  // finite: token 0 of a tile is live
+      s_run = s_run * exp2f(m_run - mnew) + ((exp2f(x[0] - mnew) + exp2f(x[1] - mnew)) +
+                                             (exp2f(x[2] - mnew) + exp2f(x[3] - mnew)));
+      m_run = mnew;
+    }
+    __syncwarp();  // the stage is read before its next copy
+    if (k % stp == stp - 1) {  // the page's last tile: its (m, s) per query head
+      float s_tot = s_run + __shfl_xor_sync(0xffffffffu, s_run, 1);
+      s_tot += __shfl_xor_sync(0xffffffffu, s_tot, 2);
+      if (t4 == 0 && g < G) {
+        float *dst = a.pm + (((size_t)unit * a.max_pages + tile_page(k)) * G + g) * 2;
+        dst[0] = m_run;
+        dst[1] = s_tot;
+      }
+      m_run = -INFINITY;
+      s_run = 0.f;
+    }
+  }
+}
+
 // ---- per-unit normalisation, keys and nucleus size -----------------------------------------
 __device__ __forceinline__ float block_max(float v, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -177,8 +317,10 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
   pdl_wait();  // dependents are released when this grid completes
   __shared__ float redf[kCovThreads / 32];
   __shared__ unsigned long long redu[kCovThreads / 32];
-  __shared__ unsigned long long hmass[256];
-  __shared__ int hcount[256];
+  __shared__ unsigned long long hmass[kCovHist][256];  // warp w counts into copy w % kCovHist
+  __shared__ int hcount[kCovHist][256];
+  __shared__ unsigned long long scan_m[kCovThreads / 32];
+  __shared__ int scan_n[kCovThreads / 32];
   __shared__ int pick[3];
   __shared__ unsigned long long pick_mass[2];
   const int unit = blockIdx.x;
@@ -213,6 +355,7 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
   unsigned long long *qrow = a.qmass + (size_t)unit * a.max_pages;
   unsigned long long forced_q = 0, total_q = 0;
   int n_cand = 0;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;  // of the candidates' keys
   for (int p = tid; p < P; p += kCovThreads) {
     float mass = 0.f;
     bool read = false;  // false only for a page whose block id was out of range (flagged)
@@ -227,54 +370,110 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
     const unsigned long long qm = (unsigned long long)((double)mass * kMassQuant + 0.5);
     if (a.masses_out) a.masses_out[(size_t)unit * a.max_pages + p] = mass;
     const bool forced = always_kept(p, P, a.sink, a.window);
-    krow[p] = (forced || !read) ? 0u : score_key(mass);
+    const uint32_t key = (forced || !read) ? 0u : score_key(mass);
+    krow[p] = key;
     qrow[p] = qm;
     total_q += qm;
     if (forced) forced_q += qm;
     else if (read) ++n_cand;
+    if (key != 0u) {
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
   }
   total_q = block_sum_u64(total_q, redu);
   forced_q = block_sum_u64(forced_q, redu);
   n_cand = (int)block_sum_u64((unsigned long long)n_cand, redu);
+  {  // the candidates' smallest and largest key over the block
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) {  // the scan arrays are not in use yet (redu may still be read)
+      scan_n[warp] = (int)kmin;
+      scan_m[warp] = kmax;
+    }
+    __syncthreads();
+    kmin = 0xFFFFFFFFu;
+    kmax = 0u;
+#pragma unroll
+    for (int w = 0; w < kCovThreads / 32; ++w) {
+      kmin = min(kmin, (uint32_t)scan_n[w]);
+      kmax = max(kmax, (uint32_t)scan_m[w]);
+    }
+  }
   __syncthreads();  // keys and masses of the row are written (each thread reads back any of them)
   const unsigned long long target = (unsigned long long)ceil((double)total_q * a.coverage);
   int k = 0;
   if (forced_q < target && n_cand > 0) {
+    // MSB-first radix over the candidates' keys, starting at the highest bit where their
+    // smallest and largest key differ (as the selection kernel does): per 8-bit digit a count
+    // and a fixed-point mass histogram (kCovHist copies against atomic contention), then the
+    // first digit, in descending order, whose running mass reaches what is still needed
     unsigned long long need = target - forced_q;  // mass still to cover
     int taken = 0;                                // keys above the running prefix
-    uint32_t prefix = 0u, mask = 0u;
+    const uint32_t diff = kmin ^ kmax;
+    const int top = diff ? 31 - __clz(diff) : 0;
+    int shift = top >= 7 ? top - 7 : 0;
+    uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
+    uint32_t mask = shift + 8 >= 32 ? 0u : (0xFFFFFFFFu << (shift + 8));
+    const int lane = tid & 31, warp = tid >> 5;
     bool all = false;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int x = tid; x < 256; x += kCovThreads) {
-        hmass[x] = 0ull;
-        hcount[x] = 0;
+#pragma unroll 1
+    for (;;) {
+      for (int x = tid; x < kCovHist * 256; x += kCovThreads) {
+        (&hmass[0][0])[x] = 0ull;
+        (&hcount[0][0])[x] = 0;
       }
+      if (tid == 0) pick[0] = -1;
       __syncthreads();
       for (int p = tid; p < P; p += kCovThreads) {
         const uint32_t key = krow[p];
         if (key != 0u && (key & mask) == prefix) {
-          atomicAdd(&hmass[(key >> shift) & 255u], qrow[p]);
-          atomicAdd(&hcount[(key >> shift) & 255u], 1);
+          const uint32_t bin = (key >> shift) & 255u;
+          atomicAdd(&hmass[warp % kCovHist][bin], qrow[p]);
+          atomicAdd(&hcount[warp % kCovHist][bin], 1);
         }
       }
       __syncthreads();
-      if (tid == 0) {
-        // descending digits: the first whose running mass reaches what is still needed
-        unsigned long long run = 0;
-        int cnt = 0, d = -1;
-        for (int b = 255; b >= 0; --b) {
-          if (run + hmass[b] >= need && hcount[b] > 0) {
-            d = b;
-            break;
-          }
-          run += hmass[b];
-          cnt += hcount[b];
+      // thread t owns digit 255 - t: descending digit order is thread order
+      const int bin = 255 - tid;
+      unsigned long long m = 0;
+      int n = 0;
+#pragma unroll
+      for (int c = 0; c < kCovHist; ++c) {
+        m += hmass[c][bin];
+        n += hcount[c][bin];
+      }
+      unsigned long long incl_m = m;
+      int incl_n = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long ym = __shfl_up_sync(0xffffffffu, incl_m, o);
+        const int yn = __shfl_up_sync(0xffffffffu, incl_n, o);
+        if (lane >= o) {
+          incl_m += ym;
+          incl_n += yn;
         }
-        pick[0] = d;
-        pick[1] = cnt;
-        pick[2] = d >= 0 ? hcount[d] : 0;
-        pick_mass[0] = run;
-        pick_mass[1] = d >= 0 ? hmass[d] : 0ull;
+      }
+      if (lane == 31) {
+        scan_m[warp] = incl_m;
+        scan_n[warp] = incl_n;
+      }
+      __syncthreads();
+      for (int w = 0; w < warp; ++w) {
+        incl_m += scan_m[w];
+        incl_n += scan_n[w];
+      }
+      const unsigned long long excl_m = incl_m - m;
+      if (excl_m < need && incl_m >= need && n > 0) {  // exactly one digit qualifies, or none
+        pick[0] = bin;
+        pick[1] = incl_n - n;  // keys above this digit
+        pick[2] = n;
+        pick_mass[0] = excl_m;
+        pick_mass[1] = m;
       }
       __syncthreads();
       const int d = pick[0];
@@ -286,13 +485,16 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
       taken += pick[1];
       prefix |= (uint32_t)d << shift;
       mask |= 255u << shift;
-      if (shift == 0) {
-        // every key equal to prefix has the same mass: how many of them make up `need`
+      if (shift == 0 || pick[2] == 1) {
+        // every key equal to prefix has the same mass (a single key: it alone): how many of
+        // them make up `need`
         const unsigned long long each = pick_mass[1] / (unsigned long long)pick[2];
         const unsigned long long n_eq = each > 0 ? (need + each - 1) / each : (unsigned long long)pick[2];
         taken += (int)min((unsigned long long)pick[2], max(1ull, n_eq));
+        break;
       }
-      __syncthreads();  // pick is rewritten by the next pass
+      shift = shift >= 8 ? shift - 8 : 0;  // an overlap with bits already fixed is harmless
+      __syncthreads();                     // pick is rewritten by the next pass
     }
     k = all ? n_cand : taken;
   }
@@ -305,7 +507,18 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
 template <typename T, int D, int G>
 cudaError_t launch_t(const CoverageArgs &c, const ScoreArgs &sel, cudaStream_t s) {
   dim3 g1((c.max_pages + kMassPages - 1) / kMassPages, c.B * c.H_kv);
-  cudaError_t e = launch_kernel(true, page_mass_kernel<T, D, G>, g1, kMassThreads, 0, s, c);
+  cudaError_t e = cudaErrorInvalidValue;
+  bool done = false;
+  if constexpr (sizeof(T) == 2) {
+    if (tuning().decode_mma) {  // the tensor-core tiles of the decode, K only
+      CUtensorMap tmK;
+      if (!encode_cache_map(&tmK, c.k_cache, PSK_BF16, D, c.H_kv, (long long)c.nb * c.ps, 16, true))
+        return cudaErrorInvalidValue;
+      e = launch_kernel(true, page_mass_mma_kernel<D, G>, g1, kMassMmaWarps * 32, mass_mma_smem<D>(), s, c, tmK);
+      done = true;
+    }
+  }
+  if (!done) e = launch_kernel(true, page_mass_kernel<T, D, G>, g1, kMassThreads, 0, s, c);
   if (e != cudaSuccess) return e;
   e = launch_kernel(false, coverage_keys_kernel<G>, c.B * c.H_kv, kCovThreads, 0, s, c);
   if (e != cudaSuccess) return e;
