@@ -275,30 +275,6 @@ __global__ void __launch_bounds__(kMassMmaWarps * 32) page_mass_mma_kernel(Cover
 }
 
 // ---- per-unit normalisation, keys and nucleus size -----------------------------------------
-__device__ __forceinline__ float block_max(float v, float *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < kCovThreads / 32; ++w) r = fmaxf(r, red[w]);
-  return r;
-}
-__device__ __forceinline__ float block_sum(float v, float *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = 0.f;
-#pragma unroll
-  for (int w = 0; w < kCovThreads / 32; ++w) r += red[w];
-  return r;
-}
 __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -315,7 +291,6 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 template <int G>
 __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs a) {
   pdl_wait();  // dependents are released when this grid completes
-  __shared__ float redf[kCovThreads / 32];
   __shared__ unsigned long long redu[kCovThreads / 32];
   __shared__ unsigned long long hmass[kCovHist][256];  // warp w counts into copy w % kCovHist
   __shared__ int hcount[kCovHist][256];
@@ -335,20 +310,52 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
     }
     return;
   }
-  const float *pm = a.pm + (size_t)unit * a.max_pages * G * 2;
+  const float2 *pm2 = reinterpret_cast<const float2 *>(a.pm) + (size_t)unit * a.max_pages * G;
+  // the group's normalisers in one pass: per head an online (max, sum) over the pages' pairs,
+  // combined over the block
+  __shared__ float2 redp[kCovThreads / 32][G];
   float M[G], Zinv[G];
+  {
+    float mr[G], zr[G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float mx = -INFINITY;
-    for (int p = tid; p < P; p += kCovThreads) mx = fmaxf(mx, pm[(p * G + g) * 2]);
-    M[g] = block_max(mx, redf);
-    float z = 0.f;
-    for (int p = tid; p < P; p += kCovThreads) {
-      const float m = pm[(p * G + g) * 2];
-      if (m != -INFINITY) z += pm[(p * G + g) * 2 + 1] * exp2f(m - M[g]);
+    for (int g = 0; g < G; ++g) {
+      mr[g] = -INFINITY;
+      zr[g] = 0.f;
     }
-    const float Z = block_sum(z, redf);
-    Zinv[g] = Z > 0.f ? 1.f / Z : 0.f;
+    auto fold = [](float &m, float &z, float mo, float zo) {  // (m, z) += (mo, zo), both relative to their max
+      const float mn = fmaxf(m, mo);
+      if (mn == -INFINITY) return;
+      z = (m == -INFINITY ? 0.f : z * exp2f(m - mn)) + (mo == -INFINITY ? 0.f : zo * exp2f(mo - mn));
+      m = mn;
+    };
+#pragma unroll 4
+    for (int p = tid; p < P; p += kCovThreads)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float2 ms = pm2[(size_t)p * G + g];
+        fold(mr[g], zr[g], ms.x, ms.y);
+      }
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float mo = __shfl_xor_sync(0xffffffffu, mr[g], o);
+        const float zo = __shfl_xor_sync(0xffffffffu, zr[g], o);
+        fold(mr[g], zr[g], mo, zo);
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int g = 0; g < G; ++g) redp[warp][g] = make_float2(mr[g], zr[g]);
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float m = -INFINITY, z = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCovThreads / 32; ++w) fold(m, z, redp[w][g].x, redp[w][g].y);
+      M[g] = m;
+      Zinv[g] = z > 0.f ? 1.f / z : 0.f;
+    }
   }
   // page masses, keys, fixed-point masses
   uint32_t *krow = a.keys + (size_t)unit * a.key_stride;
@@ -356,15 +363,16 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
   unsigned long long forced_q = 0, total_q = 0;
   int n_cand = 0;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;  // of the candidates' keys
+#pragma unroll 4
   for (int p = tid; p < P; p += kCovThreads) {
     float mass = 0.f;
     bool read = false;  // false only for a page whose block id was out of range (flagged)
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float m = pm[(p * G + g) * 2];
-      if (m != -INFINITY) {
+      const float2 ms = pm2[(size_t)p * G + g];
+      if (ms.x != -INFINITY) {
         read = true;
-        mass = fmaxf(mass, pm[(p * G + g) * 2 + 1] * exp2f(m - M[g]) * Zinv[g]);
+        mass = fmaxf(mass, ms.y * exp2f(ms.x - M[g]) * Zinv[g]);
       }
     }
     const unsigned long long qm = (unsigned long long)((double)mass * kMassQuant + 0.5);
@@ -429,6 +437,7 @@ __global__ void __launch_bounds__(kCovThreads) coverage_keys_kernel(CoverageArgs
       }
       if (tid == 0) pick[0] = -1;
       __syncthreads();
+#pragma unroll 4
       for (int p = tid; p < P; p += kCovThreads) {
         const uint32_t key = krow[p];
         if (key != 0u && (key & mask) == prefix) {
