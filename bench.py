@@ -61,12 +61,12 @@ TRAFFIC = {
     #   python bench.py --batch 16 --steps 3 --warmup 3 --no-cpu-baseline, then
     #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
     #       -k regex:"page_score|page_select|decode_split" -s 0 -c 3 python bench.py --batch 16 --steps 3 ...
-    # 158,039,808 + 2,776,576 B for 38,540 pages; scaled by pages to the 140,808 of the full workload.
+    # 158,038,272 + 2,779,904 B for 38,540 pages; scaled by pages to the 140,808 of the full workload.
     ("batched-ragged-b64-8k..64k-5pct", "page_score_mma_kernel"):
-        {"bytes": 587_551_463, "digest": "dcbe0b5bf41ef10e", "scaled_from": "first 16 sequences, by pages"},
-    # 129,192,960 + 646,656 B for 15,472 selected (page, head) pairs; 56,536 in the full workload
+        {"bytes": 587_558_011, "digest": "fee1dcb211b0b4f0", "scaled_from": "first 16 sequences, by pages"},
+    # 129,191,168 + 603,648 B for 15,472 selected (page, head) pairs; 56,536 in the full workload
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 474_444_967, "digest": "dbf85d294768238c", "scaled_from": "first 16 sequences, by selected pages"},
+        {"bytes": 474_281_264, "digest": "e68f0527ebf4aaff", "scaled_from": "first 16 sequences, by selected pages"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),
