@@ -108,6 +108,41 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
   return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
+// thread-block cluster: this CTA's rank and the cluster's size (1 and 1 without a cluster launch),
+// a shared-memory address of the same variable in CTA `rank`, loads through it, and the
+// cluster-wide barrier (every thread of every CTA of the cluster, warp-converged)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 
 // ------------------------------------------------------------------------------------
 // score
@@ -258,6 +293,9 @@ static_assert(kMlaMaxItems * kHeads * 4 <= kKStages * kKTile, "merge weights mus
 constexpr uint32_t kOCol = 0, kSCol = 256, kQCol = 320;
 static_assert(kQCol + kQTmemKB * 32 == 512, "tensor-memory budget");
 constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is rescaled
+constexpr int kMlaClusterMax = 8;               // splits per (sequence, half) merged inside one cluster
+constexpr int kORow = 256 + 4;                  // floats per parked O row (+4: conflict-free float4 reads)
+static_assert(kHeads * kORow * 4 + kHeads * 8 <= kKStages * kKTile, "parked O rows and (m, l) must fit the K stages");
 
 // One CTA per (split, half of D_v, sequence); warps 0-3 own one query head per thread (the
 // tensor-memory lanes), warp 4's lane 0 issues every TMA copy and every MMA. A tcgen05.mma
@@ -293,6 +331,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
   const int e0 = s * a.sw;
+  // Q dims 0..383 of head `tid` go to tensor memory after the allocation below; the first half
+  // of its loads is issued now, so that it overlaps the list-entry loads (warps 0-3)
+  constexpr int kQHalfLd = kQTmemKB * 4;  // 16-byte loads in half of those dims
+  const uint4 *qrow =
+      reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) + ((size_t)i * kHeads + (tid & 127)) * kD);
+  uint4 qv[kQHalfLd];
+  if (warp < 4) {
+#pragma unroll
+    for (int j = 0; j < kQHalfLd; ++j) qv[j] = __ldg(qrow + j);
+  }
 
   int n_ent = 0;
   if (seq_len < 1 || P > a.max_pages) {
@@ -355,21 +403,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   const uint32_t tmem = tslot;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   if (warp < 4 && n_ent > 0) {  // Q dims 0..383 of head `tid` into tensor memory (bf16 pairs)
-    const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) +
-                                                        ((size_t)i * kHeads + tid) * kD);
-#pragma unroll 1
-    for (int c = 0; c < kQTmemKB; ++c) {
-      uint32_t w[32];
+    auto store_half = [&](int c0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 v = __ldg(qrow + c * 8 + j);
-        w[4 * j] = v.x;
-        w[4 * j + 1] = v.y;
-        w[4 * j + 2] = v.z;
-        w[4 * j + 3] = v.w;
+      for (int c = 0; c < kQTmemKB / 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          w[4 * j] = qv[c * 8 + j].x;
+          w[4 * j + 1] = qv[c * 8 + j].y;
+          w[4 * j + 2] = qv[c * 8 + j].z;
+          w[4 * j + 3] = qv[c * 8 + j].w;
+        }
+        tmem_st32(tmem + lane_base + kQCol + (c0 + c) * 32, w);
       }
-      tmem_st32(tmem + lane_base + kQCol + c * 32, w);
-    }
+    };
+    store_half(0);
+#pragma unroll
+    for (int j = 0; j < kQHalfLd; ++j) qv[j] = __ldg(qrow + kQHalfLd + j);
+    store_half(kQTmemKB / 2);
   }
   tc_fence_before();
   __syncthreads();
@@ -395,6 +446,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
     const int kb = k < kKB - 4 ? k : (k - (kKB - 4)) + vh * 4;  // k >= 5: part B
     return k < kKB - 4 ? (kb < vh * 4 ? kb : kb + 4) : kb;
   };
+  float m_fin = -INFINITY, l_fin = 0.f;  // softmax warps: this head's (m, l) after the last tile
   if (warp == 5) {
     // ---------------- loading thread: TMA copies ----------------
     if (lane == 0 && n_tiles > 0) {
@@ -574,29 +626,123 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       if (lane == 0) mbar_arrive(smem_u32(&pready));
     }
     __all_sync(0xffffffffu, wait_ok(&pvdone, (n_tiles - 1) & 1));
+    m_fin = m_run;
+    l_fin = l_run;
+  }
+
+  // ---- the splits of a (sequence, half) merge ------------------------------------------------
+  // Launched as one cluster per (sequence, half) (at most kMlaClusterMax splits), each CTA parks
+  // its unnormalised O rows and (m, l) in its own shared memory (the K stages are free now) and
+  // merges one slice of the value dims over distributed shared memory. Otherwise the partials
+  // go to the workspace and the last CTA to finish merges them.
+  const uint32_t n_clu = cluster_size();
+  const bool clustered = n_clu == (uint32_t)a.n_items_max;
+  float *sO = reinterpret_cast<float *>(sK);                     // [128][kORow]
+  float2 *sML = reinterpret_cast<float2 *>(sK + kHeads * kORow * 4);  // [128]
+  __syncthreads();  // the loading and issuing threads' last waits are over: no copy or MMA in flight
+  if (warp < 4) {
     tc_fence_after();
-    // partial O row (unnormalised) and (m, l) of head `tid`
-    float *po = a.part_o + (pbase * kHeads + tid) * 256;
+    if (clustered) {
+      if (n_tiles > 0) {
+        float *orow = sO + tid * kORow;
 #pragma unroll 1
-    for (int c0 = 0; c0 < 256; c0 += 32) {
-      uint32_t ov[32];
-      tmem_ld32(tmem + lane_base + kOCol + c0, ov);
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kOCol + c0, ov);
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4 *>(po + c0 + j) = make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
-                                                               __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(orow + c0 + j) = make_float4(
+                __uint_as_float(ov[j]), __uint_as_float(ov[j + 1]), __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+        }
+      }
+      sML[tid] = make_float2(m_fin, l_fin);
+    } else {
+      if (n_tiles > 0) {  // partial O row (unnormalised) of head `tid`
+        float *po = a.part_o + (pbase * kHeads + tid) * 256;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kOCol + c0, ov);
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(po + c0 + j) = make_float4(
+                __uint_as_float(ov[j]), __uint_as_float(ov[j + 1]), __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+        }
+      }
+      a.part_ml[(pbase * kHeads + tid) * 2] = m_fin;
+      a.part_ml[(pbase * kHeads + tid) * 2 + 1] = l_fin;
     }
-    a.part_ml[(pbase * kHeads + tid) * 2] = m_run;
-    a.part_ml[(pbase * kHeads + tid) * 2 + 1] = l_run;
-  } else {
-    a.part_ml[(pbase * kHeads + tid) * 2] = -INFINITY;
-    a.part_ml[(pbase * kHeads + tid) * 2 + 1] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
 
-  // ---- the last CTA of (sequence, half) merges the splits ----------------------------------
+  if (clustered) {
+    cluster_sync_all();  // every CTA of the cluster has parked its rows
+    if (tid < kHeads) {
+      const int n = (int)n_clu;
+      const int r = (int)cluster_rank();
+      const int span = ((256 + n - 1) / n + 3) & ~3;  // value dims this CTA writes (a multiple of 4)
+      const int d0 = min(256, r * span), d1 = min(256, d0 + span);
+      float mk[kMlaClusterMax], lk[kMlaClusterMax], wk[kMlaClusterMax];
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kMlaClusterMax; ++k) {
+        mk[k] = -INFINITY;
+        lk[k] = 0.f;
+        if (k < n) {
+          const float2 ml = ld_dsmem_f2(dsmem_addr(smem_u32(&sML[tid]), (uint32_t)k));
+          mk[k] = ml.x;
+          lk[k] = ml.y;
+          M = fmaxf(M, ml.x);
+        }
+      }
+      float L = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMlaClusterMax; ++k) {
+        const float w = mk[k] == -INFINITY ? 0.f : exp2f(mk[k] - M);
+        if (w > 0.f) L = fmaf(w, lk[k], L);
+        wk[k] = w;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      uint16_t *out = reinterpret_cast<uint16_t *>(a.out) + ((size_t)i * kHeads + tid) * kDv + vh * 256;
+      const uint32_t orow = smem_u32(sO + tid * kORow);
+#pragma unroll 1
+      for (int d = d0; d < d1; d += 16) {
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMlaClusterMax; ++k) {
+          if (wk[k] == 0.f) continue;  // also every k >= n
+          const uint32_t src = dsmem_addr(orow + d * 4, (uint32_t)k);
+          float4 o[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            o[q4] = d + 4 * q4 < d1 ? ld_dsmem_f4(src + q4 * 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            acc[4 * q4] = fmaf(wk[k], o[q4].x, acc[4 * q4]);
+            acc[4 * q4 + 1] = fmaf(wk[k], o[q4].y, acc[4 * q4 + 1]);
+            acc[4 * q4 + 2] = fmaf(wk[k], o[q4].z, acc[4 * q4 + 2]);
+            acc[4 * q4 + 3] = fmaf(wk[k], o[q4].w, acc[4 * q4 + 3]);
+          }
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          if (d + 4 * q4 < d1) {
+            uint2 w;
+            w.x = (uint32_t)f32_to_bf16_bits(acc[4 * q4] * inv) | ((uint32_t)f32_to_bf16_bits(acc[4 * q4 + 1] * inv) << 16);
+            w.y = (uint32_t)f32_to_bf16_bits(acc[4 * q4 + 2] * inv) | ((uint32_t)f32_to_bf16_bits(acc[4 * q4 + 3] * inv) << 16);
+            *reinterpret_cast<uint2 *>(out + d + 4 * q4) = w;
+          }
+        }
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+    return;
+  }
+
   __threadfence();
   __syncthreads();
   if (tid == 0) flag_last = atomicAdd(a.tickets + unit, 1u) == (unsigned)(a.n_items_max - 1);
@@ -617,22 +763,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   uint16_t *out = reinterpret_cast<uint16_t *>(a.out) + ((size_t)i * kHeads + tid) * kDv + vh * 256;
+  // four splits' 32-dim slices in flight at once (a walk over the splits one at a time waited a
+  // full L2 round trip per slice)
 #pragma unroll 1
   for (int c = 0; c < 8; ++c) {
     float acc[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-    for (int k = 0; k < a.n_items_max; ++k) {
-      const float w = wsm[k * kHeads + tid];
-      if (w == 0.f) continue;
-      const float *pk = a.part_o + ((it0 + k) * kHeads + tid) * 256 + c * 32;
+#pragma unroll 1
+    for (int k0 = 0; k0 < a.n_items_max; k0 += 4) {
+      float4 o[4][8];
+      float w4[4];
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 o = __ldcg(reinterpret_cast<const float4 *>(pk + j));
-        acc[j] = fmaf(w, o.x, acc[j]);
-        acc[j + 1] = fmaf(w, o.y, acc[j + 1]);
-        acc[j + 2] = fmaf(w, o.z, acc[j + 2]);
-        acc[j + 3] = fmaf(w, o.w, acc[j + 3]);
+      for (int kk = 0; kk < 4; ++kk) {
+        const int k = k0 + kk;
+        w4[kk] = k < a.n_items_max ? wsm[k * kHeads + tid] : 0.f;
+        const float4 *pk = reinterpret_cast<const float4 *>(a.part_o + ((it0 + k) * kHeads + tid) * 256 + c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[kk][j] = w4[kk] != 0.f ? __ldcg(pk + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        if (w4[kk] == 0.f) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc[4 * j] = fmaf(w4[kk], o[kk][j].x, acc[4 * j]);
+          acc[4 * j + 1] = fmaf(w4[kk], o[kk][j].y, acc[4 * j + 1]);
+          acc[4 * j + 2] = fmaf(w4[kk], o[kk][j].z, acc[4 * j + 2]);
+          acc[4 * j + 3] = fmaf(w4[kk], o[kk][j].w, acc[4 * j + 3]);
+        }
       }
     }
 #pragma unroll
@@ -673,7 +832,10 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   const long long units = (long long)L.batch * 2;
   const long long sms = sm_count();
   // One CTA per SM (shared memory). Pick the split width that minimises
-  //   waves * (pages per split + ~2 pages of fixed per-CTA cost) + ~0.5 page per split merged.
+  //   waves * (pages per split + ~2 pages of fixed per-CTA cost) + the merge,
+  // where a merge inside one cluster (at most kMlaClusterMax splits) costs about a page and the
+  // workspace merge about a page per split (measured on the latent workload: 4 splits merged by
+  // the last CTA took 52 us before its loads were batched, about 20 pages).
   int sw = std::max(1, std::min(entries, kMlaMaxSw));
   double best = 1e300;
   for (int items = 1; items <= std::min(std::max(entries, 1), kMlaMaxItems); ++items) {
@@ -681,7 +843,7 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
     if (w > kMlaMaxSw) continue;
     const int n = (std::max(entries, 1) + w - 1) / w;
     const long long waves = (units * n + sms - 1) / sms;
-    const double cost = (double)waves * (w + 2.0) + 0.5 * n;
+    const double cost = (double)waves * (w + 2.0) + (n <= kMlaClusterMax ? 1.0 : 1.0 * n);
     if (cost < best - 1e-9) {
       best = cost;
       sw = w;
@@ -708,6 +870,28 @@ cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
       !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kHalf))
     return cudaErrorInvalidValue;
   dim3 grid(a.n_items_max, 2, a.B);
+  if (a.n_items_max > 1 && a.n_items_max <= kMlaClusterMax) {
+    // the splits of each (sequence, half) as one cluster: they merge in distributed shared memory
+    const void *fn = reinterpret_cast<const void *>(mla_decode_kernel);
+    cudaError_t e = kernel_setup(fn, kDecThreads, kDecSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = kDecSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.n_items_max;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled(true) ? 2 : 1;
+    if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, a, tmQ, tmK) == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();  // clusters of this size cannot be placed: the workspace merge below
+  }
   return launch_kernel(true, mla_decode_kernel, grid, kDecThreads, kDecSmem, s, a, tmQ, tmK);
 }
 
