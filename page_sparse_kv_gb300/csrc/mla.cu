@@ -295,7 +295,8 @@ static_assert(kQCol + kQTmemKB * 32 == 512, "tensor-memory budget");
 constexpr float kRescaleSlack = 8.f;            // log2 headroom before O is rescaled
 constexpr int kMlaClusterMax = 8;               // splits per (sequence, half) merged inside one cluster
 constexpr int kORow = 256 + 4;                  // floats per parked O row (+4: conflict-free float4 reads)
-static_assert(kHeads * kORow * 4 + kHeads * 8 <= kKStages * kKTile, "parked O rows and (m, l) must fit the K stages");
+static_assert(kHeads * kORow * 4 + kHeads * 8 + (kMlaClusterMax + 1) * kHeads * 4 <= kKStages * kKTile,
+              "parked O rows, (m, l) and the merge weights must fit the K stages");
 
 // One CTA per (split, half of D_v, sequence); warps 0-3 own one query head per thread (the
 // tensor-memory lanes), warp 4's lane 0 issues every TMA copy and every MMA. A tcgen05.mma
@@ -331,48 +332,59 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   const int seq_len = a.seq_lens[i];
   const int P = (seq_len + a.ps - 1) / a.ps;
   const int e0 = s * a.sw;
-  // Q dims 0..383 of head `tid` go to tensor memory after the allocation below; the first half
-  // of its loads is issued now, so that it overlaps the list-entry loads (warps 0-3)
-  constexpr int kQHalfLd = kQTmemKB * 4;  // 16-byte loads in half of those dims
+  // the list loads do not depend on the length, so they go out with it (one list entry per
+  // thread: sw <= kMlaMaxSw <= kDecThreads)
+  const int32_t *row = a.selected ? a.selected + (size_t)i * a.b_max : nullptr;
+  int first = -1, pg_x = e0 + tid, prev_x = -1;
+  if (row && e0 < a.b_max) {
+    first = row[e0];
+    if (tid < a.sw && e0 + tid < a.b_max) {
+      pg_x = row[e0 + tid];
+      prev_x = e0 + tid > 0 ? row[e0 + tid - 1] : -1;
+    }
+  }
+  // Q dims 0..383 of head `tid` go to tensor memory after the allocation below; its loads are
+  // issued right behind the list loads above (volatile with a memory clobber, so neither moves),
+  // and land while the block-table loads below and the set-up run (warps 0-3)
+  constexpr int kQLd = kQTmemKB * 8;  // 16-byte loads in those dims
   const uint4 *qrow =
       reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) + ((size_t)i * kHeads + (tid & 127)) * kD);
-  uint4 qv[kQHalfLd];
+  uint4 qv[kQLd];
   if (warp < 4) {
 #pragma unroll
-    for (int j = 0; j < kQHalfLd; ++j) qv[j] = __ldg(qrow + j);
+    for (int j = 0; j < kQLd; ++j)
+      asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                   : "=r"(qv[j].x), "=r"(qv[j].y), "=r"(qv[j].z), "=r"(qv[j].w)
+                   : "l"(qrow + j)
+                   : "memory");
   }
-
   int n_ent = 0;
   if (seq_len < 1 || P > a.max_pages) {
     if (s == 0 && vh == 0 && tid == 0) set_status(a.ws, PSK_DEV_BAD_SEQLEN);
-  } else if (a.selected) {
-    const int32_t *row = a.selected + (size_t)i * a.b_max;
-    if (e0 < a.b_max && row[e0] >= 0) n_ent = min(a.sw, a.b_max - e0);
+  } else if (row) {
+    if (e0 < a.b_max && first >= 0) n_ent = min(a.sw, a.b_max - e0);
   } else if (e0 < P) {
     n_ent = min(a.sw, P - e0);
   }
-  for (int x = tid; x < n_ent; x += kDecThreads) {
-    int pg = e0 + x, blk = -1;
+  if (tid < n_ent) {
+    int blk = -1;
     bool ok = true;
-    if (a.selected) {
-      const int32_t *row = a.selected + (size_t)i * a.b_max;
-      pg = row[e0 + x];
-      const int prev = (e0 + x > 0) ? row[e0 + x - 1] : -1;
-      if (pg >= 0 && (pg >= P || pg <= prev || (e0 + x > 0 && prev < 0))) {
+    if (row) {
+      if (pg_x >= 0 && (pg_x >= P || pg_x <= prev_x || (e0 + tid > 0 && prev_x < 0))) {
         if (vh == 0) set_status(a.ws, PSK_DEV_BAD_SELECTED);
         ok = false;
       }
-      if (pg < 0) ok = false;
+      if (pg_x < 0) ok = false;
     }
     if (ok) {
-      blk = a.block_table[(size_t)i * a.max_pages + pg];
+      blk = a.block_table[(size_t)i * a.max_pages + pg_x];
       if (blk < 0 || blk >= a.nb) {
         if (vh == 0) set_status(a.ws, PSK_DEV_BAD_BLOCK);
         ok = false;
       }
     }
-    ent_blk[x] = blk;
-    ent_valid[x] = ok ? min(a.ps, seq_len - pg * a.ps) : 0;
+    ent_blk[tid] = blk;
+    ent_valid[tid] = ok ? min(a.ps, seq_len - pg_x * a.ps) : 0;
   }
   if (tid == 0) {
     mbar_init(smem_u32(&qbar), 1);
@@ -394,33 +406,85 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) {
-    int n = 0;
-    for (int e = 0; e < n_ent; ++e)
-      for (int hh = 0; hh * kHalf < ent_valid[e]; ++hh) halves[n++] = (short)(e * 2 + hh);
-    n_halves_sh = n;
-  }
   const uint32_t tmem = tslot;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  if (warp < 4 && n_ent > 0) {  // Q dims 0..383 of head `tid` into tensor memory (bf16 pairs)
-    auto store_half = [&](int c0) {
-#pragma unroll
-      for (int c = 0; c < kQTmemKB / 2; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          w[4 * j] = qv[c * 8 + j].x;
-          w[4 * j + 1] = qv[c * 8 + j].y;
-          w[4 * j + 2] = qv[c * 8 + j].z;
-          w[4 * j + 3] = qv[c * 8 + j].w;
-        }
-        tmem_st32(tmem + lane_base + kQCol + (c0 + c) * 32, w);
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) -> bool {
+    if (*reinterpret_cast<volatile int *>(&abort_sh)) return false;
+    if (mbar_wait(smem_u32(bar), parity, a.ws)) return true;
+    *reinterpret_cast<volatile int *>(&abort_sh) = 1;
+    return false;
+  };
+  // the k-th 64-dim block S reads: part A (blocks outside this CTA's value half) first, then
+  // part B (the value blocks vh * 4 .. vh * 4 + 3)
+  auto s_block = [&](int k) -> int {
+    const int kb = k < kKB - 4 ? k : (k - (kKB - 4)) + vh * 4;  // k >= 5: part B
+    return k < kKB - 4 ? (kb < vh * 4 ? kb : kb + 4) : kb;
+  };
+  // Loading warp, before the others finish setting up: the (entry, 32-token half) pairs with at
+  // least one live row in list order (a warp scan of each entry's 0-2 halves), then the copies
+  // that wait for nothing (Q dims 384..575 and the first kKStages K tiles).
+  int n_halves_l = 0, na = 0, nb = 0;  // loading warp: halves; part A / part B copies issued
+  auto load_part = [&](int t, bool part_b) {
+    const int st = t % kKStages;
+    const int nh = (2 * t + 1 < n_halves_l) ? 2 : 1;
+    const uint32_t bar = smem_u32(part_b ? &kfb[st] : &kfa[st]);
+    const int nblk = part_b ? 4 : kKB - 4;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nh * nblk * kHalf * 128));
+    const uint32_t dst = smem_u32(sK + st * kKTile);
+    for (int h2 = 0; h2 < nh; ++h2) {
+      const int hx = 2 * t + h2;
+      const int e = halves[hx] >> 1, hh = halves[hx] & 1;
+      const int row0 = ent_blk[e] * a.ps + hh * kHalf;
+#pragma unroll 1
+      for (int k = part_b ? kKB - 4 : 0; k < (part_b ? kKB : kKB - 4); ++k) {
+        const int kb = s_block(k);
+        tma_load_2d(dst + kb * kKBlock + h2 * kHalf * 128, &tmK, kb * 64, row0, bar);
       }
-    };
-    store_half(0);
+    }
+  };
+  if (warp == 5) {
+    for (int eb = 0; eb < n_ent; eb += 32) {
+      const int e = eb + lane;
+      const int c = e < n_ent ? (ent_valid[e] + kHalf - 1) / kHalf : 0;  // halves with live rows
+      int incl = c;
 #pragma unroll
-    for (int j = 0; j < kQHalfLd; ++j) qv[j] = __ldg(qrow + kQHalfLd + j);
-    store_half(kQTmemKB / 2);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      for (int hh = 0; hh < c; ++hh) halves[n_halves_l + incl - c + hh] = (short)(e * 2 + hh);
+      n_halves_l += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      n_halves_sh = n_halves_l;
+      if (n_halves_l > 0) {
+        mbar_arrive_expect_tx(smem_u32(&qbar), kQSBytes);
+#pragma unroll 1
+        for (int kb = 0; kb < kQSmemKB; ++kb)
+          tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, (kQTmemKB + kb) * 64, i * kHeads, smem_u32(&qbar));
+        const int t0 = min((n_halves_l + 1) / 2, kKStages);
+        for (int t = 0; t < t0; ++t) {
+          load_part(t, false);
+          load_part(t, true);
+        }
+        na = nb = t0;
+      }
+    }
+  }
+  if (warp < 4 && n_ent > 0) {  // Q dims 0..383 of head `tid` into tensor memory (bf16 pairs)
+#pragma unroll
+    for (int c = 0; c < kQTmemKB; ++c) {
+      uint32_t w[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        w[4 * j] = qv[c * 8 + j].x;
+        w[4 * j + 1] = qv[c * 8 + j].y;
+        w[4 * j + 2] = qv[c * 8 + j].z;
+        w[4 * j + 3] = qv[c * 8 + j].w;
+      }
+      tmem_st32(tmem + lane_base + kQCol + c * 32, w);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -433,48 +497,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
     const int e = halves[hx] >> 1, hh = halves[hx] & 1;
     return min(kHalf, ent_valid[e] - hh * kHalf);
   };
-  auto wait_ok = [&](uint64_t *bar, uint32_t parity) -> bool {
-    if (*reinterpret_cast<volatile int *>(&abort_sh)) return false;
-    if (mbar_wait(smem_u32(bar), parity, a.ws)) return true;
-    *reinterpret_cast<volatile int *>(&abort_sh) = 1;
-    return false;
-  };
-
-  // the k-th 64-dim block S reads: part A (blocks outside this CTA's value half) first, then
-  // part B (the value blocks vh * 4 .. vh * 4 + 3)
-  auto s_block = [&](int k) -> int {
-    const int kb = k < kKB - 4 ? k : (k - (kKB - 4)) + vh * 4;  // k >= 5: part B
-    return k < kKB - 4 ? (kb < vh * 4 ? kb : kb + 4) : kb;
-  };
   float m_fin = -INFINITY, l_fin = 0.f;  // softmax warps: this head's (m, l) after the last tile
   if (warp == 5) {
     // ---------------- loading thread: TMA copies ----------------
-    if (lane == 0 && n_tiles > 0) {
-      int na = 0, nb = 0;  // part A / part B copies issued
-      auto load_part = [&](int t, bool part_b) {
-        const int st = t % kKStages;
-        const int nh = (2 * t + 1 < n_halves) ? 2 : 1;
-        const uint32_t bar = smem_u32(part_b ? &kfb[st] : &kfa[st]);
-        const int nblk = part_b ? 4 : kKB - 4;
-        mbar_arrive_expect_tx(bar, (uint32_t)(nh * nblk * kHalf * 128));
-        const uint32_t dst = smem_u32(sK + st * kKTile);
-        for (int h2 = 0; h2 < nh; ++h2) {
-          const int hx = 2 * t + h2;
-          const int e = halves[hx] >> 1, hh = halves[hx] & 1;
-          const int row0 = ent_blk[e] * a.ps + hh * kHalf;
+    if (lane == 0 && n_tiles > 0) {  // tiles 0 .. kKStages - 1 went out before the set-up barrier
 #pragma unroll 1
-          for (int k = part_b ? kKB - 4 : 0; k < (part_b ? kKB : kKB - 4); ++k) {
-            const int kb = s_block(k);
-            tma_load_2d(dst + kb * kKBlock + h2 * kHalf * 128, &tmK, kb * 64, row0, bar);
-          }
-        }
-      };
-      mbar_arrive_expect_tx(smem_u32(&qbar), kQSBytes);
-#pragma unroll 1
-      for (int kb = 0; kb < kQSmemKB; ++kb)
-        tma_load_2d(smem_u32(sQ + kb * kHeads * 128), &tmQ, (kQTmemKB + kb) * 64, i * kHeads, smem_u32(&qbar));
-#pragma unroll 1
-      for (int t = 0; t < n_tiles; ++t) {
+      for (int t = na; t < n_tiles; ++t) {
         const int st = t % kKStages;
         if (t >= kKStages && !wait_ok(&kea[st], ((t - kKStages) / kKStages) & 1)) break;  // S(t-2) done
         load_part(t, false);
@@ -679,62 +707,69 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
 
   if (clustered) {
     cluster_sync_all();  // every CTA of the cluster has parked its rows
-    if (tid < kHeads) {
-      const int n = (int)n_clu;
-      const int r = (int)cluster_rank();
-      const int span = ((256 + n - 1) / n + 3) & ~3;  // value dims this CTA writes (a multiple of 4)
-      const int d0 = min(256, r * span), d1 = min(256, d0 + span);
-      float mk[kMlaClusterMax], lk[kMlaClusterMax], wk[kMlaClusterMax];
-      float M = -INFINITY;
+    const int n = (int)n_clu;
+    const int r = (int)cluster_rank();
+    const int span = ((256 + n - 1) / n + 3) & ~3;  // value dims this CTA writes (a multiple of 4)
+    const int d0 = min(256, r * span), d1 = min(256, d0 + span);
+    float *wts = reinterpret_cast<float *>(sK + kHeads * kORow * 4 + kHeads * 8);  // [kMlaClusterMax + 1][128]
+    if (tid < kHeads) {  // the merge weights of head `tid` (and 1 / L in the last row)
+      float mk[kMlaClusterMax], lk[kMlaClusterMax];
 #pragma unroll
       for (int k = 0; k < kMlaClusterMax; ++k) {
-        mk[k] = -INFINITY;
-        lk[k] = 0.f;
-        if (k < n) {
-          const float2 ml = ld_dsmem_f2(dsmem_addr(smem_u32(&sML[tid]), (uint32_t)k));
-          mk[k] = ml.x;
-          lk[k] = ml.y;
-          M = fmaxf(M, ml.x);
-        }
+        const float2 ml = k < n ? ld_dsmem_f2(dsmem_addr(smem_u32(&sML[tid]), (uint32_t)k)) : make_float2(-INFINITY, 0.f);
+        mk[k] = ml.x;
+        lk[k] = ml.y;
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kMlaClusterMax; ++k) M = fmaxf(M, mk[k]);
       float L = 0.f;
 #pragma unroll
       for (int k = 0; k < kMlaClusterMax; ++k) {
-        const float w = mk[k] == -INFINITY ? 0.f : exp2f(mk[k] - M);
+        const float w = mk[k] == -INFINITY ? 0.f : exp2f(mk[k] - M);  // 0 for every k >= n
         if (w > 0.f) L = fmaf(w, lk[k], L);
-        wk[k] = w;
+        wts[k * kHeads + tid] = w;
       }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint16_t *out = reinterpret_cast<uint16_t *>(a.out) + ((size_t)i * kHeads + tid) * kDv + vh * 256;
-      const uint32_t orow = smem_u32(sO + tid * kORow);
+      wts[kMlaClusterMax * kHeads + tid] = L > 0.f ? 1.f / L : 0.f;
+    }
+    __syncthreads();
+    if (warp < 4) {
+      // each half-warp takes one head row and 16 consecutive float4 of it, so a warp's remote
+      // loads are two contiguous 256-byte runs; four head pairs per step keep 4n loads in flight
+      const int hl = lane >> 4, l16 = lane & 15;
+      uint16_t *out_i = reinterpret_cast<uint16_t *>(a.out) + (size_t)i * kHeads * kDv + vh * 256;
 #pragma unroll 1
-      for (int d = d0; d < d1; d += 16) {
-        float acc[16];
+      for (int pb = warp; pb < kHeads / 2; pb += 16) {
+#pragma unroll 1
+        for (int d = d0 + l16 * 4; d < d1; d += 64) {
+          float4 o[4][kMlaClusterMax];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+          for (int u = 0; u < 4; ++u) {
+            const int h = 2 * (pb + 4 * u) + hl;
+            const uint32_t src = smem_u32(sO + h * kORow + d);
 #pragma unroll
-        for (int k = 0; k < kMlaClusterMax; ++k) {
-          if (wk[k] == 0.f) continue;  // also every k >= n
-          const uint32_t src = dsmem_addr(orow + d * 4, (uint32_t)k);
-          float4 o[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            o[q4] = d + 4 * q4 < d1 ? ld_dsmem_f4(src + q4 * 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            acc[4 * q4] = fmaf(wk[k], o[q4].x, acc[4 * q4]);
-            acc[4 * q4 + 1] = fmaf(wk[k], o[q4].y, acc[4 * q4 + 1]);
-            acc[4 * q4 + 2] = fmaf(wk[k], o[q4].z, acc[4 * q4 + 2]);
-            acc[4 * q4 + 3] = fmaf(wk[k], o[q4].w, acc[4 * q4 + 3]);
+            for (int k = 0; k < kMlaClusterMax; ++k)
+              o[u][k] = wts[k * kHeads + h] != 0.f ? ld_dsmem_f4(dsmem_addr(src, (uint32_t)k))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-        }
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          if (d + 4 * q4 < d1) {
-            uint2 w;
-            w.x = (uint32_t)f32_to_bf16_bits(acc[4 * q4] * inv) | ((uint32_t)f32_to_bf16_bits(acc[4 * q4 + 1] * inv) << 16);
-            w.y = (uint32_t)f32_to_bf16_bits(acc[4 * q4 + 2] * inv) | ((uint32_t)f32_to_bf16_bits(acc[4 * q4 + 3] * inv) << 16);
-            *reinterpret_cast<uint2 *>(out + d + 4 * q4) = w;
+          for (int u = 0; u < 4; ++u) {
+            const int h = 2 * (pb + 4 * u) + hl;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kMlaClusterMax; ++k) {
+              const float w = wts[k * kHeads + h];
+              if (w == 0.f) continue;
+              acc.x = fmaf(w, o[u][k].x, acc.x);
+              acc.y = fmaf(w, o[u][k].y, acc.y);
+              acc.z = fmaf(w, o[u][k].z, acc.z);
+              acc.w = fmaf(w, o[u][k].w, acc.w);
+            }
+            const float inv = wts[kMlaClusterMax * kHeads + h];
+            uint2 wv;
+            wv.x = (uint32_t)f32_to_bf16_bits(acc.x * inv) | ((uint32_t)f32_to_bf16_bits(acc.y * inv) << 16);
+            wv.y = (uint32_t)f32_to_bf16_bits(acc.z * inv) | ((uint32_t)f32_to_bf16_bits(acc.w * inv) << 16);
+            *reinterpret_cast<uint2 *>(out_i + (size_t)h * kDv + d) = wv;
           }
         }
       }
