@@ -64,9 +64,10 @@ TRAFFIC = {
     # 158,038,272 + 2,779,904 B for 38,540 pages; scaled by pages to the 140,808 of the full workload.
     ("batched-ragged-b64-8k..64k-5pct", "page_score_mma_kernel"):
         {"bytes": 587_558_011, "digest": "fee1dcb211b0b4f0", "scaled_from": "first 16 sequences, by pages"},
-    # 129,191,168 + 603,648 B for 15,472 selected (page, head) pairs; 56,536 in the full workload
+    # 129,188,864 + 2,953,728 B for 15,472 selected (page, head) pairs (ncu -k regex:decode_split
+    # -s 0 -c 1, the same command otherwise); 56,536 in the full workload
     ("batched-ragged-b64-8k..64k-5pct", "decode_split_kernel"):
-        {"bytes": 474_281_264, "digest": "e68f0527ebf4aaff", "scaled_from": "first 16 sequences, by selected pages"},
+        {"bytes": 482_860_237, "digest": "b3d841046fbd5db0", "scaled_from": "first 16 sequences, by selected pages"},
 }
 KERNEL_SOURCES = {
     "page_score_kernel": ("score_select.cu", "psk_common.cuh", "psk_internal.h"),

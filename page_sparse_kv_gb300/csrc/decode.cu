@@ -49,7 +49,7 @@ constexpr int kMaxItems = 256; // splits per (sequence, KV head), upper bound (b
 constexpr int kFlatMaxCtas = 2048;   // grid of the flat layout, upper bound (sizes the partials)
 constexpr int kFlatMaxUnits = 4096;  // units the flat layout takes (its prefix sums live in shared memory)
 constexpr long long kFlatMinShare = 8;  // list entries per CTA of the flat layout, lower bound
-constexpr int kFastMerge = 8;          // partials a unit merge reads in one round trip
+constexpr int kFastMerge = 16;         // partials a unit merge reads in one round trip
 constexpr int kHostPrefetch = 2;       // host value path: tiles of its own a warp prefetches ahead into L2
 
 template <typename T, int D, int G, int NW, int NST>
