@@ -126,6 +126,7 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+// (a shared::cta address is also the shared::cluster address of this CTA's own shared memory)
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
@@ -706,7 +707,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
   if (warp == 0) tmem_dealloc(tmem, 512);
 
   if (clustered) {
-    cluster_sync_all();  // every CTA of the cluster has parked its rows
+    // one split per (sequence, half): a CTA barrier and this CTA's own addresses (no cluster launch)
+    const bool multi = n_clu > 1;
+    if (multi) cluster_sync_all();  // every CTA of the cluster has parked its rows
+    else __syncthreads();
     const int n = (int)n_clu;
     const int r = (int)cluster_rank();
     const int span = ((256 + n - 1) / n + 3) & ~3;  // value dims this CTA writes (a multiple of 4)
@@ -716,7 +720,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       float mk[kMlaClusterMax], lk[kMlaClusterMax];
 #pragma unroll
       for (int k = 0; k < kMlaClusterMax; ++k) {
-        const float2 ml = k < n ? ld_dsmem_f2(dsmem_addr(smem_u32(&sML[tid]), (uint32_t)k)) : make_float2(-INFINITY, 0.f);
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (k < n) ml = ld_dsmem_f2(multi ? dsmem_addr(smem_u32(&sML[tid]), (uint32_t)k) : smem_u32(&sML[tid]));
         mk[k] = ml.x;
         lk[k] = ml.y;
       }
@@ -749,7 +754,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
             const uint32_t src = smem_u32(sO + h * kORow + d);
 #pragma unroll
             for (int k = 0; k < kMlaClusterMax; ++k)
-              o[u][k] = wts[k * kHeads + h] != 0.f ? ld_dsmem_f4(dsmem_addr(src, (uint32_t)k))
+              o[u][k] = wts[k * kHeads + h] != 0.f ? ld_dsmem_f4(multi ? dsmem_addr(src, (uint32_t)k) : src)
                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
         }
       }
     }
-    cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+    if (multi) cluster_sync_all();  // no CTA leaves while another still reads its shared memory
     return;
   }
 

@@ -221,6 +221,20 @@ def test_mla_edge_cases(case):
     _run_and_check(w, cache, seqs, summ, w.queries(), step_tag="mla " + str(case))
 
 
+@pytest.mark.parametrize("B, budget", [(80, 3), (2, 3), (2, 7)])
+def test_mla_split_counts(B, budget):
+    """The latent decode's merge with one split per (sequence, half) (80 sequences: 160 units, more
+    than the SMs, so each unit gets one split and merges on its own) and with clusters of 3 and 7
+    splits (value-dim slices of 88 and 40 dims, the last one shorter)."""
+    rng = np.random.default_rng(B * 10 + budget)
+    lens = [int(x) for x in rng.integers(64 * 2, 64 * 9, size=B)]
+    w = _custom_mla(lens, [budget] * B, seed=B + budget)
+    cache = upload(w)
+    seqs = list(range(B)) if B <= 4 else [0, 1, B // 2, B - 1]
+    summ = _check_cache_and_summaries(w, cache, seqs)
+    _run_and_check(w, cache, seqs, summ, w.queries(), step_tag=f"mla splits B={B} b={budget}")
+
+
 @pytest.mark.parametrize("ps", [32, 64])
 def test_mla_nan_junk_past_seq_len_is_never_read(ps):
     """The latent decode multiplies whole 32-row boxes: the rows past seq_len must not reach O."""
