@@ -25,7 +25,10 @@
 // (N = 256 value dims, V read MN-major straight out of the K tile) accumulates in tensor
 // memory. Six warps: four softmax warps (one thread per head), one warp whose lane 0 issues the
 // MMAs (S of the next tile ahead of P.V of this one) and one whose lane 0 issues the TMA copies.
-// Splits are merged by log-sum-exp by the last CTA of each (sequence, half).
+// Splits are merged by log-sum-exp: with at most 8 splits per (sequence, half) they run as one
+// thread-block cluster, park their O rows and (m, l) in shared memory and each merge a slice of
+// the value dims over distributed shared memory; with more, the last CTA of each (sequence,
+// half) merges them from the workspace.
 #include <algorithm>
 
 #include "psk_common.cuh"
