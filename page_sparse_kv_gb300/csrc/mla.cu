@@ -30,6 +30,7 @@
 // the value dims over distributed shared memory; with more, the last CTA of each (sequence,
 // half) merges them from the workspace.
 #include <algorithm>
+#include <cstdlib>
 
 #include "psk_common.cuh"
 #include "psk_internal.h"
@@ -907,13 +908,23 @@ bool plan_mla_decode(const psk_layout &L, int entries, DecodePlan *plan) {
   return plan->n_items_max <= kMlaMaxItems;
 }
 
+// PSK_MLA_CLUSTER=0: the latent decode without clusters (its splits then merge in the workspace,
+// with the same arithmetic in the same order); read once per process
+bool mla_cluster_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("PSK_MLA_CLUSTER");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
   CUtensorMap tmQ, tmK;
   if (!encode_matrix_map_sw128(&tmQ, a.q, kD, (long long)a.B * kHeads, 64, kHeads) ||
       !encode_matrix_map_sw128(&tmK, a.k_cache, kD, (long long)a.nb * a.ps, 64, kHalf))
     return cudaErrorInvalidValue;
   dim3 grid(a.n_items_max, 2, a.B);
-  if (a.n_items_max > 1 && a.n_items_max <= kMlaClusterMax) {
+  if (a.n_items_max > 1 && a.n_items_max <= kMlaClusterMax && mla_cluster_enabled()) {
     // the splits of each (sequence, half) as one cluster: they merge in distributed shared memory
     const void *fn = reinterpret_cast<const void *>(mla_decode_kernel);
     cudaError_t e = kernel_setup(fn, kDecThreads, kDecSmem);

@@ -815,6 +815,57 @@ def test_launch_modes_without_and_with_in_call_pdl(mode):
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
 
 
+_MLA_MERGE_CHILD = r"""
+import sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import page_sparse_kv_gb300 as psk
+import workloads as W
+from workloads.device import budgets as dev_budgets, from_torch, to_torch, upload
+for tag, w in (("reduced", W.reduced(5)),
+               ("b3", W.Workload("custom-mla", 21, "bf16", B=2, H_q=128, H_kv=1, D=576, D_v=512, page_size=64,
+                                 seq_lens=[64 * 6 + 17, 64 * 5], budgets=[3, 3], n_hot=2, hot_rule="random",
+                                 latent=True, pool_slack=3))):
+    cache = upload(w)
+    q = to_torch(w.queries(), w.dtype).cuda()
+    sel = cache.score_select(q, dev_budgets(w))
+    out = cache.sparse_decode(q, sel)
+    dense = cache.dense_decode(q)
+    torch.cuda.synchronize()
+    assert psk.get_device_status(cache.ws) == 0
+    np.save(sys.argv[2] + "." + tag + ".out.npy", from_torch(out, w.dtype).view(np.uint16))
+    np.save(sys.argv[2] + "." + tag + ".dense.npy", from_torch(dense, w.dtype).view(np.uint16))
+    np.save(sys.argv[2] + "." + tag + ".sel.npy", sel.cpu().numpy())
+print("ok")
+"""
+
+
+def test_latent_cluster_merge_equals_workspace_merge(tmp_path):
+    """The latent decode merges up to 8 splits per (sequence, half) inside a thread-block cluster
+    and more in the workspace, with the same arithmetic in the same order: with clusters switched
+    off (PSK_MLA_CLUSTER=0, read once per process, so each form runs in a child process) the
+    sparse and dense outputs must be bit-identical (clusters of 8 and of 3 splits here)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = {}
+    for flag in (None, "0"):
+        env = dict(os.environ, PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+        env.pop("PSK_MLA_CLUSTER", None)
+        if flag is not None:
+            env["PSK_MLA_CLUSTER"] = flag
+        tag = str(tmp_path / f"clu{flag}")
+        r = subprocess.run([sys.executable, "-c", _MLA_MERGE_CHILD, root, tag], env=env, capture_output=True,
+                           text=True, timeout=900)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+        res[flag] = tag
+    for w in ("reduced", "b3"):
+        for part in ("sel", "out", "dense"):
+            a = np.load(res[None] + f".{w}.{part}.npy")
+            b = np.load(res["0"] + f".{w}.{part}.npy")
+            assert np.array_equal(a, b), f"{w} {part}: cluster and workspace merges differ"
+
+
 _FMA_CHILD = r"""
 import sys
 sys.path.insert(0, sys.argv[1])
