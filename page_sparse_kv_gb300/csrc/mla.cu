@@ -98,6 +98,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
+// 32 columns of this warp's 32 lanes; tmem_st32 waits for the store, tmem_st32_async does not
+// (tmem_wait_st then waits for every store this thread issued)
+__device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%"
+      "21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%"
@@ -348,9 +361,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       prev_x = e0 + tid > 0 ? row[e0 + tid - 1] : -1;
     }
   }
+  // the block id of this thread's entry, requested as soon as its page id is known (in bounds of
+  // the block table whatever the length; used only if the entry turns out valid), ahead of the
+  // query loads below so that it does not queue behind them
+  int blk_x = -1;
+  if (tid < a.sw && pg_x >= 0 && pg_x < a.max_pages) blk_x = a.block_table[(size_t)i * a.max_pages + pg_x];
   // Q dims 0..383 of head `tid` go to tensor memory after the allocation below; its loads are
-  // issued right behind the list loads above (volatile with a memory clobber, so neither moves),
-  // and land while the block-table loads below and the set-up run (warps 0-3)
+  // issued right behind the list and block-table loads above (volatile with a memory clobber, so
+  // nothing moves across them), and land while the set-up runs (warps 0-3)
   constexpr int kQLd = kQTmemKB * 8;  // 16-byte loads in those dims
   const uint4 *qrow =
       reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) + ((size_t)i * kHeads + (tid & 127)) * kD);
@@ -382,7 +400,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
       if (pg_x < 0) ok = false;
     }
     if (ok) {
-      blk = a.block_table[(size_t)i * a.max_pages + pg_x];
+      blk = blk_x;
       if (blk < 0 || blk >= a.nb) {
         if (vh == 0) set_status(a.ws, PSK_DEV_BAD_BLOCK);
         ok = false;
@@ -488,8 +506,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) mla_decode_kernel(DecodeArgs a
         w[4 * j + 2] = qv[c * 8 + j].z;
         w[4 * j + 3] = qv[c * 8 + j].w;
       }
-      tmem_st32(tmem + lane_base + kQCol + c * 32, w);
+      tmem_st32_async(tmem + lane_base + kQCol + c * 32, w);  // the six stores in flight together
     }
+    tmem_wait_st();
   }
   tc_fence_before();
   __syncthreads();
