@@ -10,6 +10,12 @@
    smallest and largest nonzero keys differ, stopping early when the chosen bin holds exactly the
    keys still needed, then the "key > T, plus the first need_eq keys equal to T" compaction. The
    chosen set must equal the top k by (key desc, index asc), ties included.
+3. The latent decode's split plan and its cluster merge: the planner's split width (waves of one
+   CTA per SM against the merge's cost) must cover every list entry once with at most 128 splits;
+   with at most 8 splits per (sequence, half) the merge runs in a cluster, where rank r writes the
+   value dims [r·span, (r+1)·span) of every head through four warps that take head pairs
+   warp + 4u + 16j and, per half-warp, 4-dim pieces 64 apart. Every (head, value dim) of the half
+   must be written exactly once, and no remote rank at or past the cluster size is addressed.
 """
 import random
 
@@ -122,3 +128,77 @@ def test_radix_select_with_early_exit_is_the_top_k():
         for early in (False, True):
             T, need_eq = _radix_select(keys, k, early)
             assert sorted(_compact(keys, T, need_eq)) == sorted(ref)
+
+
+# ------------------------------------------------------------------ 3. latent split plan and merge
+_MLA_MAX_SW, _MLA_MAX_ITEMS, _MLA_CLUSTER_MAX = 128, 128, 8
+
+
+def _mla_plan(units, entries, sms=152):
+    """Split width and count the way the latent decode's planner picks them."""
+    e = max(entries, 1)
+    sw, best = max(1, min(entries, _MLA_MAX_SW)), 1e300
+    for items in range(1, min(e, _MLA_MAX_ITEMS) + 1):
+        w = -(-e // items)
+        if w > _MLA_MAX_SW:
+            continue
+        n = -(-e // w)
+        waves = -(-(units * n) // sms)
+        cost = waves * (w + 2.0) + (1.0 if n <= _MLA_CLUSTER_MAX else 1.0 * n)
+        if cost < best - 1e-9:
+            best, sw = cost, w
+    return sw, -(-entries // sw)
+
+
+def _cluster_merge_writes(n, rank, m_of_rank):
+    """(head, dim) pairs CTA `rank` of an n-CTA cluster writes, and the ranks whose rows it reads:
+    rank k's row is read only where its merge weight is nonzero, and the weight of every k at or
+    past the cluster size, or of a split with no tiles (m = -inf), is 0."""
+    span = (-(-256 // n) + 3) & ~3
+    d0 = min(256, rank * span)
+    d1 = min(256, d0 + span)
+    mk = [m_of_rank[k] if k < n else float("-inf") for k in range(_MLA_CLUSTER_MAX)]
+    weight_nonzero = [m != float("-inf") for m in mk]
+    writes, ranks = [], set()
+    for warp in range(4):
+        for lane in range(32):
+            hl, l16 = lane >> 4, lane & 15
+            for pb in range(warp, 64, 16):
+                d = d0 + l16 * 4
+                while d < d1:
+                    for u in range(4):
+                        h = 2 * (pb + 4 * u) + hl
+                        ranks.update(k for k in range(_MLA_CLUSTER_MAX) if weight_nonzero[k])
+                        writes.extend((h, d + j) for j in range(4) if d + j < d1)
+                    d += 64
+    return writes, ranks
+
+
+def test_latent_split_plan_covers_every_entry():
+    rng = random.Random(7)
+    cases = [(32, 103), (2, 103), (8, 103), (160, 3), (4, 3), (4, 7), (6, 16), (32, 2048), (2, 1)]
+    cases += [(rng.randint(1, 400), rng.randint(1, 4096)) for _ in range(300)]
+    for units, entries in cases:
+        sw, n = _mla_plan(units, entries)
+        assert 1 <= sw <= _MLA_MAX_SW and n <= _MLA_MAX_ITEMS
+        covered = [e for s in range(n) for e in range(s * sw, min(entries, (s + 1) * sw))]
+        assert covered == list(range(entries))
+    assert _mla_plan(32, 103) == (26, 4)       # the latent workload: clusters of 4 splits
+    assert _mla_plan(160, 3)[1] == 1            # more units than SMs: one split each
+    assert _mla_plan(4, 3)[1] == 3 and _mla_plan(4, 7)[1] == 7
+
+
+def test_cluster_merge_writes_every_value_dim_once():
+    rng = random.Random(3)
+    for n in range(1, _MLA_CLUSTER_MAX + 1):
+        # some splits of a short list have no tiles (m = -inf); at least one has
+        m = [rng.choice([float("-inf"), rng.uniform(-4.0, 4.0)]) for _ in range(n)]
+        m[rng.randrange(n)] = 0.5
+        seen = {}
+        for r in range(n):
+            writes, ranks = _cluster_merge_writes(n, r, m)
+            assert ranks == {k for k in range(n) if m[k] != float("-inf")} and ranks <= set(range(n))
+            for key in writes:
+                assert key not in seen, (n, r, key)
+                seen[key] = r
+        assert set(seen) == {(h, d) for h in range(128) for d in range(256)}, n
