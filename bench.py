@@ -688,6 +688,18 @@ def run_psk(args):
         roof["note"] = "V of the selected pages crosses NVLink-C2C, not HBM; achieved counts K and V bytes"
 
     roof["peak_kind"] = pk["kind"] + (" sustained bf16" if roof["bound"] == "tensor" else " copy")
+    # the two stages that move the step's bytes, each against its own roofline (`roofline` above is
+    # the longer of them); the selection moves no HBM bytes to speak of
+    kroof = {"score": {"bound": "hbm", "achieved": score_bytes / (t_score * 1e-3) / 1e9, "peak": peak_hbm,
+                       "unit": "GB/s", "launch_us": t_score * 1e3}}
+    if w.latent:
+        kroof["decode"] = {"bound": "tensor", "achieved": flops_decode / (t_dec * 1e-3) / 1e12,
+                           "peak": pk["bf16_sustained"], "unit": "TFLOP/s", "launch_us": t_dec * 1e3}
+    else:
+        kroof["decode"] = {"bound": "hbm", "achieved": decode_bytes / (t_dec * 1e-3) / 1e9, "peak": peak_hbm,
+                           "unit": "GB/s", "launch_us": t_dec * 1e3}
+    for kr in kroof.values():
+        kr["frac"] = kr["achieved"] / kr["peak"]
     # the captured traffic is of the HBM-resident decode: with V in host memory it does not apply
     # the captured traffic is of the default selector's kernels
     roof["traffic"], scaled = (traffic_of(w.name, dom) if not (args.v_host and dom == "decode_split_kernel")
@@ -732,6 +744,7 @@ def run_psk(args):
                                   "row's selected pages, filled from the warm-up selection the timed steps repeat"
                                   if hot is not None else "")) if args.v_host else "HBM"},
         "roofline": roof,
+        "kernels_roofline": kroof,
         "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / (step_ms * 1e-3) / 1e9,
                      "frac_of_measured": step_bytes / (step_ms * 1e-3) / 1e9 / peak_hbm,
                      "frac_of_8TBs": step_bytes / (step_ms * 1e-3) / 1e9 / 8000.0},
